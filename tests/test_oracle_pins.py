@@ -1,0 +1,258 @@
+"""Pins of the CPU oracle to what the pages and the mathematics fix.
+
+None of these compare the oracle with itself: each check uses a worked value
+printed on a page, a library routine (numpy transpose / flip), a brute-force
+enumeration, or a second independent restatement (the C loop against the
+Python one).  A dropped term, a wrong bit order, a transposed operand or a
+gather written for a scatter fails at least one of them.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import reference as ref
+from bmmc_index_transforms_gb300 import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def _rows_for(kind, n):
+    if kind == "bitrev":
+        return ref.bitrev_rows(n)
+    if kind == "identity":
+        return ref.identity_rows(n)
+    if kind == "swap4x4":
+        # [x0,x1,x2,x3] -> [x2,x3,x0,x1]: output bit i is input bit (i+2) mod 4
+        return [1 << 2, 1 << 3, 1 << 0, 1 << 1]
+    if kind.startswith("rot"):
+        return ref.rotate_rows(n, int(kind[3:]))
+    raise ValueError(kind)
+
+
+def test_worked_examples_python_and_c(golden):
+    rows = golden("worked_examples.txt")
+    assert len(rows) >= 9
+    for name, n, kind, c, x, y in rows:
+        n, c, x, y = int(n), int(c), int(x), int(y)
+        A = _rows_for(kind, n)
+        assert ref.bmmc_index(n, A, c, x) == y, name
+        assert oracle.index(n, A, c, x) == y, name
+        assert int(ref.bmmc_index_array(n, A, c, np.array([x], dtype=np.uint64))[0]) == y, name
+
+
+def test_bitrev15_appendix_bit_map(golden):
+    """Every single-bit index lands where the appendix's naive kernel puts it,
+    and every index agrees with reversing its 15-digit binary string."""
+    n = 15
+    A = ref.bitrev_rows(n)
+    for ib, ob in golden("bitrev15_appendix_bits.txt"):
+        assert ref.bmmc_index(n, A, 0, 1 << int(ib)) == 1 << int(ob)
+    xs = np.arange(1 << n, dtype=np.uint64)
+    ys = ref.bmmc_index_array(n, A, 0, xs)
+    want = np.array([int(format(int(x), "015b")[::-1], 2) for x in range(1 << n)], dtype=np.uint64)
+    assert np.array_equal(ys, want)
+
+
+@pytest.mark.parametrize("r,s", [(3, 5), (5, 3), (4, 4), (1, 6), (6, 0)])
+def test_transpose_matches_numpy(r, s):
+    """Row-major R x C transpose as a BMMC (output bit i = input bit (i+s) mod n)
+    equals numpy's transpose, the two-loop check and the C two-loop check."""
+    n = r + s
+    arr = np.arange(1 << n, dtype=np.uint32)
+    want = arr.reshape(1 << r, 1 << s).T.copy().ravel()
+    got = ref.bmmc_permute(n, ref.rotate_rows(n, s), 0, arr)
+    assert np.array_equal(got, want)
+    assert np.array_equal(ref.transpose2d(r, s, arr), want)
+    assert np.array_equal(oracle.transpose2d(r, s, arr), want)
+    small = ref.bmmc_permute_small(n, ref.rotate_rows(n, s), 0, list(arr)) if n <= 10 else None
+    if small is not None:
+        assert np.array_equal(np.array(small, dtype=np.uint32), want)
+
+
+def test_transpose_4096_full_c_oracle():
+    n = 24
+    arr = synth.fill_float_index(24)
+    want = arr.reshape(4096, 4096).T.copy().ravel()
+    got = oracle.scatter(n, ref.rotate_rows(n, 12), 0, arr, threads=oracle.host_threads())
+    assert got.tobytes() == want.tobytes()
+
+
+def test_identity_is_copy_and_complement_is_flip():
+    n = 10
+    arr = np.arange(1 << n, dtype=np.uint32) * 7 + 3
+    assert np.array_equal(ref.bmmc_permute(n, ref.identity_rows(n), 0, arr), arr)
+    assert np.array_equal(ref.bmmc_permute(n, ref.identity_rows(n), (1 << n) - 1, arr), np.flip(arr))
+    # reversed rows (Futhark "reversed_rows"): c covers only the column bits
+    rows, cols = 4, 6
+    m = arr.reshape(1 << rows, 1 << cols)
+    got = ref.bmmc_permute(n, ref.identity_rows(n), (1 << cols) - 1, arr)
+    assert np.array_equal(got, np.flip(m, axis=1).ravel())
+    got_c = oracle.scatter(n, ref.identity_rows(n), (1 << cols) - 1, arr)
+    assert np.array_equal(got_c, np.flip(m, axis=1).ravel())
+
+
+def test_axes_permute_matches_numpy_transpose():
+    """BPC of a row-major power-of-two array under permute(axes) equals numpy's
+    transpose(...).copy(); shape scaled down from [32,64,64,64,32]."""
+    shape_log2 = (1, 2, 2, 3, 2)
+    axes = synth.FIVE_D_AXES
+    n = sum(shape_log2)
+    arr = np.arange(1 << n, dtype=np.uint32)
+    want = arr.reshape([1 << b for b in shape_log2]).transpose(axes).copy().ravel()
+    perm = ref.axes_permute_bits(shape_log2, axes)
+    assert sorted(perm) == list(range(n))
+    assert np.array_equal(ref.bpc_permute(n, perm, 0, arr), want)
+    A = [1 << p for p in perm]
+    assert np.array_equal(ref.bmmc_permute(n, A, 0, arr), want)
+    assert np.array_equal(oracle.scatter(n, A, 0, arr), want)
+
+
+def test_five_d_bit_map_full_shape():
+    """The full [32,64,64,64,32] permutation (4,2,0,3,1): output bits 0..27 come
+    from input bits [17..22, 5..10, 23..27, 11..16, 0..4]."""
+    perm = ref.axes_permute_bits((5, 6, 6, 6, 5), (4, 2, 0, 3, 1))
+    want = list(range(17, 23)) + list(range(5, 11)) + list(range(23, 28)) + list(range(11, 17)) + list(range(0, 5))
+    assert perm == want
+
+
+def _all_matrices(n):
+    """Every n x n bit matrix as an array [2**(n*n), n] of row masks."""
+    codes = np.arange(1 << (n * n), dtype=np.uint64)
+    return np.stack([(codes >> np.uint64(n * i)) & np.uint64((1 << n) - 1) for i in range(n)], axis=1)
+
+
+def _index_maps(n, mats):
+    xs = np.arange(1 << n, dtype=np.uint64)
+    ys = np.zeros((mats.shape[0], 1 << n), dtype=np.uint64)
+    for i in range(n):
+        ys |= (np.bitwise_count(mats[:, i:i + 1] & xs[None, :]).astype(np.uint64) & np.uint64(1)) << np.uint64(i)
+    return ys
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_brute_force_bijection_iff_full_rank(n):
+    """Over every n x n bit matrix: the index map is a permutation exactly when
+    the oracle's rank is n, and the count is |GL(n,2)| = prod (2^n - 2^i)."""
+    mats = _all_matrices(n)
+    maps = _index_maps(n, mats)
+    bij = np.array([len(np.unique(m)) == (1 << n) for m in maps])
+    ranks = np.array([ref.f2_rank(n, [int(v) for v in row]) for row in mats])
+    assert np.array_equal(bij, ranks == n)
+    glcount = math.prod((1 << n) - (1 << i) for i in range(n))
+    assert int(bij.sum()) == glcount
+    # every (A, c) pair with A invertible permutes the index fill: a few c per A
+    inv_idx = np.nonzero(bij)[0]
+    for k in inv_idx[:: max(1, len(inv_idx) // 200)]:
+        A = [int(v) for v in mats[k]]
+        for c in range(1 << n):
+            out = ref.bmmc_permute(n, A, c, np.arange(1 << n))
+            assert sorted(out.tolist()) == list(range(1 << n))
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_inverse_against_brute_force(n):
+    """f2_inverse's index map equals the inverse permutation of A's index map
+    (found by argsort), for every invertible A; singular A give None."""
+    mats = _all_matrices(n)
+    maps = _index_maps(n, mats)
+    for k in range(mats.shape[0]):
+        A = [int(v) for v in mats[k]]
+        inv = ref.f2_inverse(n, A)
+        if len(np.unique(maps[k])) != (1 << n):
+            assert inv is None
+            continue
+        want = np.argsort(maps[k])  # want[y] = x with A x = y
+        got = [ref.bmmc_index(n, inv, 0, y) for y in range(1 << n)]
+        assert got == want.tolist()
+
+
+def _random_invertible(seed, n):
+    rows, c, _ = synth.draw_bmmc(seed, n, lambda r: ref.f2_rank(n, r) == n)
+    return rows, c
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_composition_law(seed):
+    """Permuting by (A1, c1) then (A2, c2) equals permuting once by
+    (A2 A1, A2 c1 + c2), checked element by element on the index fill."""
+    n = 9
+    A1, c1 = _random_invertible(seed, n)
+    A2, c2 = _random_invertible(seed + 100, n)
+    arr = np.arange(1 << n, dtype=np.uint32)
+    two = ref.bmmc_permute(n, A2, c2, ref.bmmc_permute(n, A1, c1, arr))
+    A3, c3 = ref.compose(n, (A2, c2), (A1, c1))
+    assert np.array_equal(ref.bmmc_permute(n, A3, c3, arr), two)
+    # the product is not commutative in general: the wrong order must differ
+    A4, c4 = ref.compose(n, (A1, c1), (A2, c2))
+    assert not np.array_equal(ref.bmmc_permute(n, A4, c4, arr), two)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_inverse_undoes_and_scatter_is_gather_by_inverse(seed):
+    n = 11
+    A, c = _random_invertible(seed, n)
+    inv = ref.f2_inverse(n, A)
+    arr = np.arange(1 << n, dtype=np.uint32)
+    fwd = ref.bmmc_permute(n, A, c, arr)
+    # P_(A^-1, A^-1 c) undoes P_(A, c)
+    back = ref.bmmc_permute(n, inv, ref.f2_matvec(n, inv, c), fwd)
+    assert np.array_equal(back, arr)
+    # scatter by A equals gather by A^-1: out[y] = in[A^-1 (y + c)]
+    ys = np.arange(1 << n, dtype=np.uint64)
+    src = ref.bmmc_index_array(n, inv, 0, ys ^ np.uint64(c))
+    assert np.array_equal(fwd, arr[src.astype(np.int64)])
+    # and equals the pure-Python loop
+    assert ref.bmmc_permute_small(n, A, c, arr.tolist()) == fwd.tolist()
+
+
+@pytest.mark.parametrize("elem", [4, 8, 16])
+@pytest.mark.parametrize("n", [1, 5, 13])
+def test_c_oracle_equals_python_oracle(n, elem):
+    A, c = _random_invertible(n * 31 + elem, n)
+    arr = synth.fill_int(n, elem)
+    want = ref.bmmc_permute(n, A, c, arr)
+    got = oracle.scatter(n, A, c, arr)
+    assert got.tobytes() == want.tobytes()
+    got_t = oracle.scatter(n, A, c, arr, threads=3)
+    assert got_t.tobytes() == want.tobytes()
+    inv = ref.f2_inverse(n, A)
+    bad, first = oracle.check_index_fill(n, inv, c, got, elem)
+    assert bad == 0 and first is None
+
+
+def test_check_index_fill_catches_a_planted_swap():
+    n, elem = 12, 4
+    A, c = _random_invertible(7, n)
+    out = oracle.scatter(n, A, c, synth.fill_int(n, elem))
+    out[[5, 9]] = out[[9, 5]]
+    bad, first = oracle.check_index_fill(n, ref.f2_inverse(n, A), c, out, elem)
+    assert bad == 2 and first == 5
+
+
+def test_r2_tiled_predicate():
+    # every bit permutation is tiled (the paper: tiled BMMCs include all BPCs)
+    for n, t in [(15, 5), (28, 6), (10, 3)]:
+        assert ref.r2_tiled(n, ref.bitrev_rows(n), t)
+        assert ref.r2_tiled(n, ref.rotate_rows(n, n // 2), t)
+    # hand-built counterexample: A^-1 e_0 = 0b110 needs 2 high coordinate bits
+    inv = [0b100, 0b011, 0b001]
+    A = ref.f2_inverse(3, inv)
+    assert not ref.r2_tiled(3, A, 1)
+    assert ref.r2_tiled(3, A, 2)
+
+
+def test_generator_is_splitmix64_and_deterministic():
+    # published splitmix64 first outputs for seed 0 (Vigna's reference code)
+    g = synth.SplitMix64(0)
+    assert g.next() == 0xE220A8397B1DCDAF
+    assert g.next() == 0x6E789E6AA1B965F4
+    r1 = synth.draw_bmmc(0, 16, lambda r: ref.f2_rank(16, r) == 16)
+    r2 = synth.draw_bmmc(0, 16, lambda r: ref.f2_rank(16, r) == 16)
+    assert r1 == r2
+    rows, c, tries = synth.draw_bmmc(3, 28, lambda r: ref.f2_rank(28, r) == 28, low_to_high=10)
+    for i in range(10):
+        assert rows[i] & 0x3FF == 0
