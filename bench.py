@@ -1,0 +1,518 @@
+"""Benchmark: effective GB/s of random BMMC permutations at n = 28, int32.
+
+Workload (one step): the 1 GiB array in[i] = i (2^28 int32) permuted by the
+32 random invertible BMMCs of seeds 0..31 (splitmix64 rejection sampling,
+c drawn after acceptance), one single-pass launch each, inputs resident in
+HBM.  Effective bandwidth = (read + write bytes) / time = 2 * 2^28 * 4 bytes
+per permutation ("A kernel that is correct", "One number").  The array is
+8x the L2, so no L2 flush is needed between launches.
+
+Also reported: the copy kernel on the same bytes (the practical ceiling),
+the worst-case matrix (low 10 bits mapped entirely to high bits), the other
+benchmark configurations, the end-to-end figure through the host-buffer C
+entry point, the roofline of the dominant kernel, SM clocks sampled during
+the timed region, and the CPU oracle on a bounded sample (the baseline).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (under torchrun) every rank runs the same workload on its own GPU
+(replicas: the permutation needs no exchange at one array per GPU) and the
+time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective GB/s (read+write) for random BMMC at n=28 int32; % of copy & HBM peak"
+UNIT = "GB/s"
+N_BITS = 28
+ELEM = 4
+SEEDS = 32
+WORST_LOW = 10
+HBM_NOMINAL_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["bmmc_index_transforms_gb300/csrc/kernels.cu",
+                  "bmmc_index_transforms_gb300/csrc/kernel_params.h",
+                  "bmmc_index_transforms_gb300/csrc/planner.cpp"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "bmmc_tiled_kernel_n28_int32_random.md")
+
+
+def workload_name() -> str:
+    return (f"random invertible BMMC n={N_BITS} int32 (in[i]=i, 1 GiB), seeds 0..{SEEDS - 1}, "
+            "one single-pass permutation per seed")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """Bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (null otherwise)."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: power above the midpoint of idle and peak draw
+        thr = (min(power) + max(power)) / 2 if power else 0
+        loaded = [s for s, p in zip(sm, power) if p >= thr] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def gpu_id_for_smi(torch, dev_index: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_gbs(sample_log2: int, seed: int, threads: int, x_offset: int = 0):
+    """Time the CPU oracle (as it stands) scattering a contiguous sample of
+    2^sample_log2 source indices of the n = 28 workload for one seed."""
+    import numpy as np
+
+    import oracle
+    from oracle import reference as ref
+    from bmmc_index_transforms_gb300 import synth
+
+    rows, c, _ = synth.draw_bmmc(seed, N_BITS, lambda r: ref.f2_rank(N_BITS, r) == N_BITS)
+    global _ORACLE_BUFS
+    try:
+        inp, out = _ORACLE_BUFS
+    except NameError:
+        inp = np.arange(1 << N_BITS, dtype=np.uint32)
+        out = np.empty_like(inp)
+        _ORACLE_BUFS = (inp, out)
+    lo = x_offset % (1 << N_BITS)
+    hi = min(1 << N_BITS, lo + (1 << sample_log2))
+    t0 = time.perf_counter()
+    oracle.scatter(N_BITS, rows, c, inp, out, threads=threads, x_range=(lo, hi))
+    dt = time.perf_counter() - t0
+    return 2.0 * (hi - lo) * ELEM / dt / 1e9, dt, hi - lo
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    threads = oracle.host_threads()
+    total = args.warmup + args.steps
+    sample_log2 = 23 if total <= 60 else 22 if total <= 200 else 20
+    vals = []
+    t_all = 0.0
+    for s in range(total):
+        gbs, dt, cnt = oracle_sample_gbs(sample_log2, s % SEEDS, threads, x_offset=s << sample_log2)
+        if s >= args.warmup:
+            vals.append((cnt, dt))
+            t_all += dt
+    moved = sum(2.0 * cnt * ELEM for cnt, _ in vals)
+    value = moved / t_all / 1e9
+    sample = (f"per step 2^{sample_log2} consecutive source indices of one seed's n=28 int32 "
+              f"permutation (seed = step mod 32), plain C oracle loop split over {threads} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_all / max(1, args.steps) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic", "config": {"workload": workload_name(), "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def median(xs):
+    return statistics.median(xs) if xs else float("nan")
+
+
+def time_launches(torch, fn, reps: int, warm: int = 2):
+    """Median / min / mean milliseconds of fn() with CUDA events on the
+    current stream."""
+    for _ in range(warm):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return median(ms), min(ms), sum(ms) / len(ms)
+
+
+def run_ours(args):
+    import torch
+
+    import bmmc_index_transforms_gb300 as bm
+    from bmmc_index_transforms_gb300 import _build, synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        _build.build()
+    if dist:
+        dist.barrier()
+    _build.build()  # no-op when fresh
+
+    N = 1 << N_BITS
+    nbytes = N * ELEM
+    alg_bytes = 2.0 * nbytes  # one read + one write of the array per permutation
+
+    def planner_accepts(rows):
+        try:
+            h = bm.bmmc_plan(N_BITS, rows, 0, ELEM)
+        except bm.BmmcError as e:
+            if e.status == 2:
+                return False
+            raise
+        bm.bmmc_plan_destroy(h)
+        return True
+
+    plans, mats = [], []
+    for s in range(SEEDS):
+        rows, c, _ = synth.draw_bmmc(s, N_BITS, planner_accepts)
+        plans.append(bm.Plan(rows, c, ELEM))
+        mats.append((rows, c))
+    wrows, wc, _ = synth.draw_bmmc(0, N_BITS, planner_accepts, low_to_high=WORST_LOW)
+    worst = bm.Plan(wrows, wc, ELEM)
+
+    d_in = torch.arange(N, dtype=torch.int32, device=dev)
+    d_out = torch.empty_like(d_in)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(record=None):
+        for k, p in enumerate(plans):
+            if record is not None:
+                record[k][0].record(stream)
+            p.permute(d_in, d_out, stream)
+            if record is not None:
+                record[k][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    per_launch = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                   for _ in plans] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(per_launch[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    launches = args.steps * len(plans)
+    value = world * launches * alg_bytes / (elapsed_ms / 1e3) / 1e9
+    launch_ms = [[a.elapsed_time(b) for a, b in per_launch[k]] for k in range(args.steps)]
+    all_launch_ms = [x for row in launch_ms for x in row]
+    mean_launch_ms = sum(all_launch_ms) / len(all_launch_ms)
+    per_seed_gbs = [alg_bytes / (median([launch_ms[k][s] for k in range(args.steps)]) / 1e3) / 1e9
+                    for s in range(len(plans))]
+
+    # --- extras (outside the timed region) ---
+    copy_med, copy_min, _ = time_launches(torch, lambda: bm.bmmc_copy(d_in, d_out, nbytes, stream), 30)
+    copy_gbs = alg_bytes / (copy_med / 1e3) / 1e9
+    torch_copy_med, _, _ = time_launches(torch, lambda: d_out.copy_(d_in), 20)
+    torch_copy_gbs = alg_bytes / (torch_copy_med / 1e3) / 1e9
+    w_med, w_min, w_mean = time_launches(torch, lambda: worst.permute(d_in, d_out, stream), 30)
+    worst_gbs = alg_bytes / (w_med / 1e3) / 1e9
+    configs = other_configs(torch, bm, synth, dev, stream) if not args.quick else {}
+    e2e = end_to_end(torch, bm, plans, dev, stream, nbytes, alg_bytes)
+
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": committed_traffic(),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "kernel": "bmmc_tiled_kernel<4,256,4>",
+                "algorithmic_bytes_per_launch": int(alg_bytes)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+
+        threads = oracle.host_threads()
+        gbs, dt, cnt = oracle_sample_gbs(24, 0, threads)
+        # scale the sample so that it holds roughly 10-30 s of CPU work
+        target_cpu_s = 15.0
+        log2 = 24
+        while dt * threads < target_cpu_s / 2 and log2 < 27:
+            log2 += 1
+            gbs, dt, cnt = oracle_sample_gbs(log2, 0, threads)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"2^{log2} consecutive source indices of the seed-0 n=28 int32 permutation "
+                         f"({dt:.2f} s wall on {threads} host threads; plain C oracle loop)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic",
+            "config": {"workload": workload_name(), "n": N_BITS, "elem_bytes": ELEM,
+                       "matrices_per_step": len(plans), "mode": "single pass",
+                       "l2": "inputs larger than L2 (1 GiB array, 126 MB L2): no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_copy": round(value / world / copy_gbs, 4),
+            "pct_of_hbm_8tbs": round(value / world / HBM_NOMINAL_GBS, 4),
+            "copy_kernel_gbs": round(copy_gbs, 1),
+            "torch_copy_gbs": round(torch_copy_gbs, 1),
+            "per_seed_median_gbs": {"mean": round(sum(per_seed_gbs) / len(per_seed_gbs), 1),
+                                    "min": round(min(per_seed_gbs), 1),
+                                    "max": round(max(per_seed_gbs), 1)},
+            "worst_case_gbs": round(worst_gbs, 1),
+            "configs": configs,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    for p in plans:
+        p.close()
+    worst.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def other_configs(torch, bm, synth, dev, stream):
+    """Effective GB/s of the other benchmark configurations (median of 30)."""
+    from bmmc_index_transforms_gb300.maps import axes_rows, bitrev_rows, rotate_rows
+
+    out = {}
+
+    def gbs(n, elem, fn):
+        med, mn, mean = time_launches(torch, fn, 30)
+        b = 2.0 * (1 << n) * elem
+        return {"median_gbs": round(b / (med / 1e3) / 1e9, 1), "min_ms": round(mn, 4),
+                "median_ms": round(med, 4)}
+
+    def accept(n):
+        def f(rows):
+            try:
+                bm.bmmc_plan_destroy(bm.bmmc_plan(n, rows, 0, 4))
+                return True
+            except bm.BmmcError:
+                return False
+        return f
+
+    # C1: n=16 random int32, seed 0 (launch-bound)
+    rows, c, _ = synth.draw_bmmc(0, 16, accept(16))
+    a = torch.arange(1 << 16, dtype=torch.int32, device=dev)
+    b = torch.empty_like(a)
+    with bm.Plan(rows, c, 4) as p:
+        out["n16_random_int32"] = gbs(16, 4, lambda: p.permute(a, b, stream))
+    # C2: 4096^2 fp32 transpose (n=24, 128 MiB: near L2 size, no flush)
+    a = torch.arange(1 << 24, dtype=torch.float32, device=dev)
+    b = torch.empty_like(a)
+    with bm.Plan(rotate_rows(24, 12), 0, 4) as p:
+        out["transpose_4096_fp32"] = gbs(24, 4, lambda: p.permute(a, b, stream))
+    del a, b
+    # C3: bit reversal n=28 int32 / int64
+    a = torch.arange(1 << 28, dtype=torch.int64, device=dev)
+    b = torch.empty_like(a)
+    with bm.Plan(bitrev_rows(28), 0, 8) as p:
+        out["bitrev_n28_int64"] = gbs(28, 8, lambda: p.permute(a, b, stream))
+    a32 = a[: 1 << 27].view(torch.int32)
+    b32 = b[: 1 << 27].view(torch.int32)
+    with bm.Plan(bitrev_rows(28), 0, 4) as p:
+        out["bitrev_n28_int32"] = gbs(28, 4, lambda: p.permute(a32, b32, stream))
+    # C5: 5-D [32,64,64,64,32] fp32 perm (4,2,0,3,1), and the float4 view
+    with bm.Plan(axes_rows((5, 6, 6, 6, 5), synth.FIVE_D_AXES), 0, 4) as p:
+        out["dims5_fp32"] = gbs(28, 4, lambda: p.permute(a32, b32, stream))
+    with bm.Plan(axes_rows((5, 6, 6, 6, 3), synth.FIVE_D_AXES), 0, 16) as p:
+        out["dims5_float4"] = gbs(26, 16, lambda: p.permute(a32, b32, stream))
+    # two-factor mode on seed 0 (the paper's two-kernel scheme), same bytes
+    rows, c, _ = synth.draw_bmmc(0, 28, accept(28))
+    scratch = torch.empty(1 << 28, dtype=torch.int32, device=dev)
+    with bm.Plan(rows, c, 4, mode=1) as p:
+        out["random_n28_int32_two_factor"] = gbs(28, 4, lambda: p.permute_scratch(a32, b32, scratch, stream))
+    del a, b, scratch
+    torch.cuda.empty_cache()
+    return out
+
+
+def end_to_end(torch, bm, plans, dev, stream, nbytes, alg_bytes, steps: int = 4):
+    """Same metric through bmmc_permute_host: pinned host input copied in,
+    permuted, copied back, every step (one seed per step)."""
+    h_in = torch.arange(nbytes // ELEM, dtype=torch.int32).pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    d_in = torch.empty(nbytes // ELEM, dtype=torch.int32, device=dev)
+    d_out = torch.empty_like(d_in)
+    plans[0].permute_host(h_in, h_out, d_in, d_out, stream)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(steps):
+        plans[k % len(plans)].permute_host(h_in, h_out, d_in, d_out, stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    del h_in, h_out, d_in, d_out
+    return {"value": round(alg_bytes / (ms / 1e3) / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "ms_per_step": round(ms, 3),
+            "path": "bmmc_permute_host (pinned host -> device, permute, device -> pinned host)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=150)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="skip the other configurations")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

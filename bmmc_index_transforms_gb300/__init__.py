@@ -1,1 +1,237 @@
-"""BMMC index permutations on GB300 (placeholder; binding added with the library)."""
+"""BMMC index permutations on GB300: a thin Python binding of libbmmc_gb300.
+
+The functions below carry the names of the C entry points in
+``include/bmmc.h`` and only marshal arguments: tensors become device
+pointers, streams become ``cudaStream_t`` handles, and every byte is moved
+by the library's CUDA kernels.  PyTorch is used for device memory and
+streams only.  If the shared library is missing, every call raises; there is
+no fallback.
+
+Permuting by (A, c) is the scatter ``out[A.x ^ c] = in[x]`` over the
+2**n elements of ``in`` ("Efficient GPU Implementation of Affine Index
+Permutations on Arrays", §1); ``A_rows[i]`` bit j is A[i][j].
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+from . import _capi
+from ._capi import PlanInfo, PlanOpts
+
+__all__ = [
+    "BmmcError", "Plan", "bmmc_plan", "bmmc_plan_ex", "bmmc_plan_destroy", "bmmc_plan_info",
+    "bmmc_plan_factor", "bmmc_plan_tile", "bmmc_permute", "bmmc_permute_scratch",
+    "bmmc_permute_host", "transpose2d", "bpc_permute", "bmmc_dims_permute",
+    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_status_string", "bmmc_version", "library_path",
+]
+
+CLASS_NAMES = {0: "identity", 1: "complement", 2: "bp", 3: "bpc", 4: "bmmc"}
+KERNEL_NAMES = {0: "tiled", 1: "copy", 2: "per-element"}
+
+
+class BmmcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bmmc_status_string(status)} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != _capi.OK:
+        raise BmmcError(status, where)
+
+
+def _ptr(x) -> int | None:
+    """Device or host address of a tensor / numpy array / raw int."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(stream, *tensors) -> int | None:
+    if stream is None:
+        for t in tensors:
+            if getattr(t, "is_cuda", False):
+                import torch
+
+                return int(torch.cuda.current_stream(t.device).cuda_stream)
+        return None
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _rows(n: int, A_rows: Sequence[int]):
+    if len(A_rows) != n:
+        raise ValueError(f"A_rows must have n = {n} rows, got {len(A_rows)}")
+    return (ctypes.c_uint64 * max(1, n))(*[int(r) for r in A_rows])
+
+
+def bmmc_status_string(status: int) -> str:
+    return _capi.lib().bmmc_status_string(int(status)).decode()
+
+
+def bmmc_version() -> int:
+    return _capi.lib().bmmc_version()
+
+
+def library_path() -> str:
+    return _capi.library_path()
+
+
+# --------------------------------------------------------------------------
+# Plans
+# --------------------------------------------------------------------------
+
+def bmmc_plan_ex(n: int, A_rows: Sequence[int], c: int, elem_size: int, mode: int = 0,
+                 t_in: int = 0, t_out: int = 0, tile_bits: int = 0,
+                 alloc_scratch: bool = False) -> int:
+    """Returns an opaque plan handle (int); free it with bmmc_plan_destroy."""
+    h = ctypes.c_void_p()
+    opts = PlanOpts(mode, t_in, t_out, tile_bits, int(bool(alloc_scratch)))
+    _check(_capi.lib().bmmc_plan_ex(ctypes.byref(h), n, _rows(n, A_rows), int(c), elem_size,
+                                    ctypes.byref(opts)), "bmmc_plan_ex")
+    return int(h.value)
+
+
+def bmmc_plan(n: int, A_rows: Sequence[int], c: int, elem_size: int) -> int:
+    h = ctypes.c_void_p()
+    _check(_capi.lib().bmmc_plan(ctypes.byref(h), n, _rows(n, A_rows), int(c), elem_size), "bmmc_plan")
+    return int(h.value)
+
+
+def bmmc_plan_destroy(plan: int) -> None:
+    _check(_capi.lib().bmmc_plan_destroy(plan), "bmmc_plan_destroy")
+
+
+def bmmc_plan_info(plan: int) -> dict:
+    info = PlanInfo()
+    _check(_capi.lib().bmmc_plan_info(plan, ctypes.byref(info)), "bmmc_plan_info")
+    d = {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+    d["class_name"] = CLASS_NAMES.get(d["cls"], "?")
+    d["kernel_name"] = KERNEL_NAMES.get(d["kernel"], "?")
+    return d
+
+
+def bmmc_plan_factor(plan: int, which: int) -> list[int]:
+    n = bmmc_plan_info(plan)["n"]
+    out = (ctypes.c_uint64 * 64)()
+    _check(_capi.lib().bmmc_plan_factor(plan, which, out), "bmmc_plan_factor")
+    return [int(out[i]) for i in range(n)]
+
+
+def bmmc_plan_tile(plan: int) -> tuple[list[int], list[int]]:
+    info = bmmc_plan_info(plan)
+    basis = (ctypes.c_uint64 * 64)()
+    bits = (ctypes.c_int * 64)()
+    _check(_capi.lib().bmmc_plan_tile(plan, basis, bits), "bmmc_plan_tile")
+    D = info["tile_bits"]
+    return [int(basis[i]) for i in range(D)], [int(bits[i]) for i in range(info["n"] - D)]
+
+
+# --------------------------------------------------------------------------
+# Permutes (device pointers; torch tensors accepted)
+# --------------------------------------------------------------------------
+
+def bmmc_permute(plan: int, inp, out, stream=None) -> None:
+    _check(_capi.lib().bmmc_permute(plan, _ptr(inp), _ptr(out), _stream(stream, inp, out)),
+           "bmmc_permute")
+
+
+def bmmc_permute_scratch(plan: int, inp, out, scratch, stream=None) -> None:
+    _check(_capi.lib().bmmc_permute_scratch(plan, _ptr(inp), _ptr(out), _ptr(scratch),
+                                            _stream(stream, inp, out)), "bmmc_permute_scratch")
+
+
+def bmmc_permute_host(plan: int, h_in, h_out, d_in, d_out, stream=None) -> None:
+    _check(_capi.lib().bmmc_permute_host(plan, _ptr(h_in), _ptr(h_out), _ptr(d_in), _ptr(d_out),
+                                         _stream(stream, d_in, d_out)), "bmmc_permute_host")
+
+
+def transpose2d(rows_log2: int, cols_log2: int, elem_size: int, inp, out, stream=None) -> None:
+    _check(_capi.lib().transpose2d(rows_log2, cols_log2, elem_size, _ptr(inp), _ptr(out),
+                                   _stream(stream, inp, out)), "transpose2d")
+
+
+def bpc_permute(n: int, perm: Sequence[int], c: int, elem_size: int, inp, out, stream=None) -> None:
+    p = (ctypes.c_int * max(1, n))(*perm)
+    _check(_capi.lib().bpc_permute(n, p, int(c), elem_size, _ptr(inp), _ptr(out),
+                                   _stream(stream, inp, out)), "bpc_permute")
+
+
+def bmmc_dims_permute(dims_log2: Sequence[int], axes: Sequence[int], elem_size: int, inp, out,
+                      stream=None) -> None:
+    d = len(dims_log2)
+    dl = (ctypes.c_int * d)(*dims_log2)
+    ax = (ctypes.c_int * d)(*axes)
+    _check(_capi.lib().bmmc_dims_permute(d, dl, ax, elem_size, _ptr(inp), _ptr(out),
+                                         _stream(stream, inp, out)), "bmmc_dims_permute")
+
+
+def bmmc_dims_permute_bits(dims_log2: Sequence[int], axes: Sequence[int]) -> list[int]:
+    d = len(dims_log2)
+    dl = (ctypes.c_int * d)(*dims_log2)
+    ax = (ctypes.c_int * d)(*axes)
+    out = (ctypes.c_int * 64)()
+    _check(_capi.lib().bmmc_dims_permute_bits(d, dl, ax, out), "bmmc_dims_permute_bits")
+    return [int(out[i]) for i in range(sum(dims_log2))]
+
+
+def bmmc_copy(inp, out, nbytes: int | None = None, stream=None) -> None:
+    if nbytes is None:
+        nbytes = inp.numel() * inp.element_size()
+    _check(_capi.lib().bmmc_copy(_ptr(inp), _ptr(out), nbytes, _stream(stream, inp, out)), "bmmc_copy")
+
+
+class Plan:
+    """Owning wrapper of a plan handle."""
+
+    def __init__(self, A_rows: Sequence[int], c: int = 0, elem_size: int = 4, *, mode: int = 0,
+                 t_in: int = 0, t_out: int = 0, tile_bits: int = 0, alloc_scratch: bool = False):
+        self.n = len(A_rows)
+        self.handle = bmmc_plan_ex(self.n, A_rows, c, elem_size, mode, t_in, t_out, tile_bits,
+                                   alloc_scratch)
+        self.elem_size = elem_size
+
+    @property
+    def info(self) -> dict:
+        return bmmc_plan_info(self.handle)
+
+    def factor(self, which: int) -> list[int]:
+        return bmmc_plan_factor(self.handle, which)
+
+    def tile(self):
+        return bmmc_plan_tile(self.handle)
+
+    def permute(self, inp, out, stream=None) -> None:
+        bmmc_permute(self.handle, inp, out, stream)
+
+    def permute_scratch(self, inp, out, scratch, stream=None) -> None:
+        bmmc_permute_scratch(self.handle, inp, out, scratch, stream)
+
+    def permute_host(self, h_in, h_out, d_in, d_out, stream=None) -> None:
+        bmmc_permute_host(self.handle, h_in, h_out, d_in, d_out, stream)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bmmc_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

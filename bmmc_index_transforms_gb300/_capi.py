@@ -1,0 +1,96 @@
+"""ctypes declarations of the C ABI in include/bmmc.h.
+
+Loading fails loudly when the shared library has not been built: there is no
+fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+u64 = ctypes.c_uint64
+u64p = ctypes.POINTER(ctypes.c_uint64)
+intp = ctypes.POINTER(ctypes.c_int)
+vp = ctypes.c_void_p
+
+# Status codes (bmmc_status)
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_SINGULAR = 2
+ERR_UNSUPPORTED_ELEM = 3
+ERR_MISALIGNED = 4
+ERR_ALIAS = 5
+ERR_CUDA = 6
+ERR_TIMEOUT = 7
+ERR_NO_SCRATCH = 8
+ERR_INTERNAL = 9
+
+MODE_SINGLE_PASS = 0
+MODE_TWO_FACTOR = 1
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("t_in", ctypes.c_int), ("t_out", ctypes.c_int),
+                ("tile_bits", ctypes.c_int), ("alloc_scratch", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("elem_size", ctypes.c_int), ("cls", ctypes.c_int),
+                ("mode", ctypes.c_int), ("t_in", ctypes.c_int), ("t_out", ctypes.c_int),
+                ("tile_bits", ctypes.c_int), ("n_over", ctypes.c_int),
+                ("r2_factors", ctypes.c_int), ("kernel", ctypes.c_int), ("threads", ctypes.c_int),
+                ("chunks_per_thread", ctypes.c_int), ("tiles", ctypes.c_uint64),
+                ("smem_bytes", ctypes.c_int), ("bank_conflicts", ctypes.c_int),
+                ("c", ctypes.c_uint64)]
+
+
+# name -> (restype, argtypes); every function declared in include/bmmc.h
+SIGNATURES = {
+    "bmmc_plan": (ctypes.c_int, [ctypes.POINTER(vp), ctypes.c_int, u64p, u64, ctypes.c_size_t]),
+    "bmmc_plan_ex": (ctypes.c_int, [ctypes.POINTER(vp), ctypes.c_int, u64p, u64, ctypes.c_size_t,
+                                    ctypes.POINTER(PlanOpts)]),
+    "bmmc_plan_destroy": (ctypes.c_int, [vp]),
+    "bmmc_plan_info": (ctypes.c_int, [vp, ctypes.POINTER(PlanInfo)]),
+    "bmmc_plan_factor": (ctypes.c_int, [vp, ctypes.c_int, u64p]),
+    "bmmc_plan_tile": (ctypes.c_int, [vp, u64p, intp]),
+    "bmmc_permute": (ctypes.c_int, [vp, vp, vp, vp]),
+    "bmmc_permute_scratch": (ctypes.c_int, [vp, vp, vp, vp, vp]),
+    "bmmc_permute_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
+    "transpose2d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_size_t, vp, vp, vp]),
+    "bpc_permute": (ctypes.c_int, [ctypes.c_int, intp, u64, ctypes.c_size_t, vp, vp, vp]),
+    "bmmc_dims_permute": (ctypes.c_int, [ctypes.c_int, intp, intp, ctypes.c_size_t, vp, vp, vp]),
+    "bmmc_dims_permute_bits": (ctypes.c_int, [ctypes.c_int, intp, intp, intp]),
+    "bmmc_copy": (ctypes.c_int, [vp, vp, ctypes.c_size_t, vp]),
+    "bmmc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "bmmc_version": (ctypes.c_int, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library; raises if it was never built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libbmmc_gb300.so is not built ({path}); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib

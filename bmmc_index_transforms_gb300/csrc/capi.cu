@@ -1,0 +1,344 @@
+// C ABI of the BMMC permutation library (declared in include/bmmc.h).
+// Argument checking, plan ownership and dispatch to the launchers; every
+// byte of array data is moved by the kernels in kernels.cu.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+
+#include "../../include/bmmc.h"
+#include "f2.hpp"
+#include "launch.hpp"
+#include "planner.hpp"
+
+using namespace bmmc;
+
+namespace {
+
+bool valid_elem(size_t e) { return e == 4 || e == 8 || e == 16; }
+
+bmmc_status check_matrix(int n, const uint64_t* rows, uint64_t c) {
+    if (!rows || n < 1 || n > kMaxN) return BMMC_ERR_INVALID_ARG;
+    const uint64_t hi = ~lowmask(n);
+    for (int i = 0; i < n; ++i)
+        if (rows[i] & hi) return BMMC_ERR_INVALID_ARG;
+    if (c & hi) return BMMC_ERR_INVALID_ARG;
+    return BMMC_OK;
+}
+
+bool overlaps(const void* a, const void* b, size_t bytes) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bytes && y < x + bytes;
+}
+
+// Device pointers must be reachable by the GPU: device, managed or pinned
+// memory, or any host memory on a device that can access pageable memory.
+bmmc_status check_reachable(const void* p) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return BMMC_ERR_CUDA;
+    }
+    if (attr.type != cudaMemoryTypeUnregistered) return BMMC_OK;
+    static std::mutex mu;
+    static std::map<int, int> pageable;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BMMC_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = pageable.find(dev);
+    if (it == pageable.end()) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) return BMMC_ERR_CUDA;
+        it = pageable.emplace(dev, v).first;
+    }
+    return it->second ? BMMC_OK : BMMC_ERR_INVALID_ARG;
+}
+
+bmmc_status check_buffers(const void* in, const void* out, size_t bytes) {
+    if (!in || !out) return BMMC_ERR_INVALID_ARG;
+    if (((uintptr_t)in | (uintptr_t)out) & 15u) return BMMC_ERR_MISALIGNED;
+    if (overlaps(in, out, bytes)) return BMMC_ERR_ALIAS;
+    bmmc_status s = check_reachable(in);
+    if (s != BMMC_OK) return s;
+    return check_reachable(out);
+}
+
+bmmc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BMMC_OK : BMMC_ERR_CUDA; }
+
+bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows, uint64_t c, size_t elem,
+                       const bmmc_plan_opts* opts) {
+    p->n = n;
+    p->elem = (int)elem;
+    p->c = c;
+    for (int i = 0; i < n; ++i) p->rows[i] = rows[i];
+    if (!inverse_rows(n, rows, p->inv)) return BMMC_ERR_SINGULAR;
+    p->cls = classify(n, rows, c);
+    PlanRequest req;
+    if (opts) {
+        if (opts->t_in < 0 || opts->t_in > 16 || opts->t_out < 0 || opts->t_out > 16 ||
+            opts->tile_bits < 0 || opts->tile_bits > kMaxTileBits)
+            return BMMC_ERR_INVALID_ARG;
+        if (opts->mode != BMMC_MODE_SINGLE_PASS && opts->mode != BMMC_MODE_TWO_FACTOR)
+            return BMMC_ERR_INVALID_ARG;
+        req.t_in = opts->t_in;
+        req.t_out = opts->t_out;
+        req.tile_bits = opts->tile_bits;
+        p->mode = opts->mode;
+    }
+    bmmc_status s = plan_pass(n, p->rows, p->inv, c, (int)elem, req, &p->main);
+    if (s != BMMC_OK) return s;
+    // Two-factor contract at t = the output run length (or the default).
+    int t = p->main.kernel == KERNEL_TILED ? p->main.t_out : default_run_bits((int)elem);
+    if (t > n) t = n;
+    p->r2_factors = r2_factorize(n, p->rows, p->inv, t, p->T1, p->T2);
+    if (p->mode == BMMC_MODE_TWO_FACTOR) {
+        uint64_t inv1[64], inv2[64];
+        if (!inverse_rows(n, p->T1, inv1) || !inverse_rows(n, p->T2, inv2)) return BMMC_ERR_INTERNAL;
+        PlanRequest r2 = req;
+        r2.t_in = r2.t_out = t;
+        if ((s = plan_pass(n, p->T2, inv2, 0, (int)elem, r2, &p->first_pass)) != BMMC_OK) return s;
+        if ((s = plan_pass(n, p->T1, inv1, c, (int)elem, r2, &p->second_pass)) != BMMC_OK) return s;
+        if (opts && opts->alloc_scratch) {
+            const size_t bytes = ((size_t)1 << n) * elem;
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return BMMC_ERR_CUDA; }
+            if (cudaMalloc(&p->scratch, bytes) != cudaSuccess) {
+                cudaGetLastError();
+                p->scratch = nullptr;
+                return BMMC_ERR_CUDA;
+            }
+            p->scratch_bytes = bytes;
+            p->scratch_device = dev;
+        }
+    }
+    return BMMC_OK;
+}
+
+bmmc_status run_plan(const bmmc_plan_s* p, const void* in, void* out, void* scratch, void* stream) {
+    const size_t bytes = ((size_t)1 << p->n) * p->elem;
+    bmmc_status s = check_buffers(in, out, bytes);
+    if (s != BMMC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (p->mode == BMMC_MODE_SINGLE_PASS) return from_cuda(launch_pass(p->main, in, out, st));
+    if (!scratch) return BMMC_ERR_NO_SCRATCH;
+    if ((uintptr_t)scratch & 15u) return BMMC_ERR_MISALIGNED;
+    if (overlaps(scratch, in, bytes) || overlaps(scratch, out, bytes)) return BMMC_ERR_ALIAS;
+    if ((s = check_reachable(scratch)) != BMMC_OK) return s;
+    cudaError_t e = launch_pass(p->first_pass, in, scratch, st);
+    if (e != cudaSuccess) return BMMC_ERR_CUDA;
+    return from_cuda(launch_pass(p->second_pass, scratch, out, st));
+}
+
+// Plan on the stack, run once (convenience entry points).
+bmmc_status permute_once(int n, const uint64_t* rows, uint64_t c, size_t elem, const void* in,
+                         void* out, void* stream) {
+    if (!valid_elem(elem)) return BMMC_ERR_UNSUPPORTED_ELEM;
+    bmmc_status s = check_matrix(n, rows, c);
+    if (s != BMMC_OK) return s;
+    bmmc_plan_s* p = new (std::nothrow) bmmc_plan_s();
+    if (!p) return BMMC_ERR_INTERNAL;
+    s = build_plan(p, n, rows, c, elem, nullptr);
+    if (s == BMMC_OK) s = run_plan(p, in, out, nullptr, stream);
+    delete p;
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+bmmc_status bmmc_plan_ex(bmmc_plan_t* plan, int n, const uint64_t* A_rows, uint64_t c,
+                         size_t elem_size, const bmmc_plan_opts* opts) {
+    if (!plan) return BMMC_ERR_INVALID_ARG;
+    *plan = nullptr;
+    bmmc_status s = check_matrix(n, A_rows, c);
+    if (s != BMMC_OK) return s;
+    if (!valid_elem(elem_size)) return BMMC_ERR_UNSUPPORTED_ELEM;
+    bmmc_plan_s* p = new (std::nothrow) bmmc_plan_s();
+    if (!p) return BMMC_ERR_INTERNAL;
+    s = build_plan(p, n, A_rows, c, elem_size, opts);
+    if (s != BMMC_OK) {
+        bmmc_plan_destroy(p);
+        return s;
+    }
+    *plan = p;
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_plan(bmmc_plan_t* plan, int n, const uint64_t* A_rows, uint64_t c, size_t elem_size) {
+    return bmmc_plan_ex(plan, n, A_rows, c, elem_size, nullptr);
+}
+
+bmmc_status bmmc_plan_destroy(bmmc_plan_t plan) {
+    if (!plan) return BMMC_OK;
+    bmmc_status s = BMMC_OK;
+    if (plan->scratch) {
+        int cur = 0;
+        if (cudaGetDevice(&cur) == cudaSuccess && cur != plan->scratch_device) cudaSetDevice(plan->scratch_device);
+        if (cudaFree(plan->scratch) != cudaSuccess) s = BMMC_ERR_CUDA;
+        if (cur != plan->scratch_device) cudaSetDevice(cur);
+        cudaGetLastError();
+    }
+    delete plan;
+    return s;
+}
+
+bmmc_status bmmc_plan_info(bmmc_plan_t plan, bmmc_plan_info_t* info) {
+    if (!plan || !info) return BMMC_ERR_INVALID_ARG;
+    std::memset(info, 0, sizeof *info);
+    const PassPlan& m = plan->main;
+    info->n = plan->n;
+    info->elem_size = plan->elem;
+    info->cls = plan->cls;
+    info->mode = plan->mode;
+    info->t_in = m.t_in;
+    info->t_out = m.t_out;
+    info->tile_bits = m.tile_bits;
+    info->n_over = m.n_over;
+    info->r2_factors = plan->r2_factors;
+    info->kernel = m.kernel;
+    info->threads = m.threads;
+    info->chunks_per_thread = m.qpt;
+    info->tiles = m.tiles;
+    info->smem_bytes = m.smem_bytes;
+    info->bank_conflicts = m.bank_conflicts;
+    if (plan->mode == BMMC_MODE_TWO_FACTOR)
+        info->bank_conflicts += plan->first_pass.bank_conflicts + plan->second_pass.bank_conflicts;
+    info->c = plan->c;
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_plan_factor(bmmc_plan_t plan, int which, uint64_t* rows_out) {
+    if (!plan || !rows_out || (which != 1 && which != 2)) return BMMC_ERR_INVALID_ARG;
+    const uint64_t* src = which == 1 ? plan->T1 : plan->T2;
+    for (int i = 0; i < plan->n; ++i) rows_out[i] = src[i];
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_plan_tile(bmmc_plan_t plan, uint64_t* tile_basis, int* block_bits) {
+    if (!plan) return BMMC_ERR_INVALID_ARG;
+    const PassPlan& m = plan->main;
+    if (m.kernel != KERNEL_TILED) return BMMC_ERR_INVALID_ARG;
+    if (tile_basis)
+        for (size_t i = 0; i < m.tile_basis.size(); ++i) tile_basis[i] = m.tile_basis[i];
+    if (block_bits)
+        for (size_t i = 0; i < m.block_bits.size(); ++i) block_bits[i] = m.block_bits[i];
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_permute(bmmc_plan_t plan, const void* in, void* out, void* stream) {
+    if (!plan) return BMMC_ERR_INVALID_ARG;
+    return run_plan(plan, in, out, plan->scratch, stream);
+}
+
+bmmc_status bmmc_permute_scratch(bmmc_plan_t plan, const void* in, void* out, void* scratch,
+                                 void* stream) {
+    if (!plan) return BMMC_ERR_INVALID_ARG;
+    return run_plan(plan, in, out, plan->mode == BMMC_MODE_TWO_FACTOR ? scratch : nullptr, stream);
+}
+
+bmmc_status bmmc_permute_host(bmmc_plan_t plan, const void* h_in, void* h_out, void* d_in, void* d_out,
+                              void* stream) {
+    if (!plan || !h_in || !h_out) return BMMC_ERR_INVALID_ARG;
+    const size_t bytes = ((size_t)1 << plan->n) * plan->elem;
+    bmmc_status s = check_buffers(d_in, d_out, bytes);
+    if (s != BMMC_OK) return s;
+    if (plan->mode == BMMC_MODE_TWO_FACTOR && !plan->scratch) return BMMC_ERR_NO_SCRATCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(d_in, h_in, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return BMMC_ERR_CUDA;
+    }
+    if ((s = run_plan(plan, d_in, d_out, plan->scratch, stream)) != BMMC_OK) return s;
+    if (cudaMemcpyAsync(h_out, d_out, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+        cudaGetLastError();
+        return BMMC_ERR_CUDA;
+    }
+    return BMMC_OK;
+}
+
+bmmc_status transpose2d(int rows_log2, int cols_log2, size_t elem_size, const void* in, void* out,
+                        void* stream) {
+    if (rows_log2 < 0 || cols_log2 < 0) return BMMC_ERR_INVALID_ARG;
+    const int n = rows_log2 + cols_log2;
+    if (n < 1 || n > kMaxN) return BMMC_ERR_INVALID_ARG;
+    uint64_t rows[64];
+    for (int i = 0; i < n; ++i) rows[i] = 1ull << ((i + cols_log2) % n);
+    return permute_once(n, rows, 0, elem_size, in, out, stream);
+}
+
+bmmc_status bpc_permute(int n, const int* perm, uint64_t c, size_t elem_size, const void* in, void* out,
+                        void* stream) {
+    if (!perm || n < 1 || n > kMaxN) return BMMC_ERR_INVALID_ARG;
+    uint64_t seen = 0, rows[64];
+    for (int i = 0; i < n; ++i) {
+        if (perm[i] < 0 || perm[i] >= n || ((seen >> perm[i]) & 1ull)) return BMMC_ERR_INVALID_ARG;
+        seen |= 1ull << perm[i];
+        rows[i] = 1ull << perm[i];
+    }
+    return permute_once(n, rows, c, elem_size, in, out, stream);
+}
+
+bmmc_status bmmc_dims_permute_bits(int ndims, const int* dims_log2, const int* axes, int* perm_out) {
+    if (!dims_log2 || !axes || !perm_out || ndims < 1 || ndims > kMaxN) return BMMC_ERR_INVALID_ARG;
+    int n = 0;
+    uint64_t seen = 0;
+    for (int k = 0; k < ndims; ++k) {
+        if (dims_log2[k] < 0 || dims_log2[k] > kMaxN) return BMMC_ERR_INVALID_ARG;
+        n += dims_log2[k];
+        if (axes[k] < 0 || axes[k] >= ndims || ((seen >> axes[k]) & 1ull)) return BMMC_ERR_INVALID_ARG;
+        seen |= 1ull << axes[k];
+    }
+    if (n < 1 || n > kMaxN) return BMMC_ERR_INVALID_ARG;
+    // Row-major: the last dimension owns the lowest bits.
+    int in_off[64];
+    int acc = 0;
+    for (int k = ndims - 1; k >= 0; --k) { in_off[k] = acc; acc += dims_log2[k]; }
+    int o = 0;
+    for (int k = ndims - 1; k >= 0; --k) {
+        const int src = axes[k];
+        for (int j = 0; j < dims_log2[src]; ++j) perm_out[o++] = in_off[src] + j;
+    }
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_dims_permute(int ndims, const int* dims_log2, const int* axes, size_t elem_size,
+                              const void* in, void* out, void* stream) {
+    int perm[64];
+    bmmc_status s = bmmc_dims_permute_bits(ndims, dims_log2, axes, perm);
+    if (s != BMMC_OK) return s;
+    int n = 0;
+    for (int k = 0; k < ndims; ++k) n += dims_log2[k];
+    return bpc_permute(n, perm, 0, elem_size, in, out, stream);
+}
+
+bmmc_status bmmc_copy(const void* in, void* out, size_t bytes, void* stream) {
+    if (bytes == 0) return BMMC_OK;
+    bmmc_status s = check_buffers(in, out, bytes);
+    if (s != BMMC_OK) return s;
+    return from_cuda(launch_copy(in, out, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+const char* bmmc_status_string(bmmc_status status) {
+    switch (status) {
+        case BMMC_OK: return "ok";
+        case BMMC_ERR_INVALID_ARG: return "invalid argument";
+        case BMMC_ERR_SINGULAR: return "matrix is singular over F2 (not a permutation)";
+        case BMMC_ERR_UNSUPPORTED_ELEM: return "element size must be 4, 8 or 16 bytes";
+        case BMMC_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case BMMC_ERR_ALIAS: return "buffers overlap";
+        case BMMC_ERR_CUDA: return "CUDA error";
+        case BMMC_ERR_TIMEOUT: return "bounded device wait timed out";
+        case BMMC_ERR_NO_SCRATCH: return "two-factor plan needs scratch memory";
+        case BMMC_ERR_INTERNAL: return "internal planner error";
+    }
+    return "unknown status";
+}
+
+int bmmc_version(void) { return 100; }
+
+}  // extern "C"

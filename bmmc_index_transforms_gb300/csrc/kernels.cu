@@ -1,0 +1,360 @@
+// Device kernels for BMMC permutations on GB300 (sm_103a) and their
+// launchers.
+//
+// bmmc_tiled_kernel is the single pass (any invertible A): each block walks
+// tiles b = blockIdx.x, blockIdx.x + gridDim.x, ... .  For one tile it
+//   1. loads the tile's input runs with 16-byte vector loads (every warp
+//      reads whole aligned runs, so every 32-byte sector fetched is used),
+//   2. scatters the elements into shared memory through the planner's XOR
+//      layout (conflict-free),
+//   3. after a barrier, already issues the loads of its next tile, and
+//   4. gathers each output vector from shared memory and writes it with one
+//      16-byte store, whole aligned output runs per warp.
+// The per-tile origins are linear in the tile index b; each lane of a warp
+// holds one column of that linear map and a warp-wide XOR reduction
+// evaluates it, so a tile costs a handful of instructions of index math
+// ("Efficient GPU Implementation of Affine Index Permutations on Arrays",
+// §6: the per-thread binary matrix-vector product must stay a few percent).
+// There are no spin waits: the only synchronisation is __syncthreads.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "kernel_params.h"
+#include "launch.hpp"
+
+namespace bmmc {
+
+template <int ELEM> struct ElemType;
+template <> struct ElemType<4> { using T = uint32_t; };
+template <> struct ElemType<8> { using T = uint2; };
+template <> struct ElemType<16> { using T = uint4; };
+
+// Streaming 16-byte load: read-only path, no L1 allocation (each byte is
+// read once).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// Streaming 16-byte store (evict-first: nothing rereads the output).
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t warp_xor64(uint64_t v) {
+    const uint32_t lo = __reduce_xor_sync(0xffffffffu, (uint32_t)v);
+    const uint32_t hi = __reduce_xor_sync(0xffffffffu, (uint32_t)(v >> 32));
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// Blocks per SM the register budget is sized for: enough 16-byte loads in
+// flight per SM to cover HBM latency, without spilling.
+template <int NT, int QPT>
+struct TiledMinBlocks {
+    static constexpr int value = NT < 256 ? 1 : QPT <= 1 ? 8 : 1;
+};
+
+template <int ELEM, int NT, int QPT>
+__global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT>::value))
+    bmmc_tiled_kernel(const __grid_constant__ TiledParams p, const uint4* __restrict__ in,
+                      uint4* __restrict__ out) {
+    using T = typename ElemType<ELEM>::T;
+    constexpr int VEC = 16 / ELEM;
+    constexpr int VB = VEC == 4 ? 2 : VEC == 2 ? 1 : 0;
+    constexpr int EB = ELEM == 4 ? 2 : ELEM == 8 ? 3 : 4;
+    extern __shared__ uint4 smem_raw[];
+    unsigned char* tile = reinterpret_cast<unsigned char*>(smem_raw);
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
+    unsigned char* dst = reinterpret_cast<unsigned char*>(out);
+
+    const uint32_t tid = threadIdx.x;
+    const uint32_t lane = tid & 31u;
+    const int D = p.tile_bits;
+
+    // Linear parts owned by this thread (the bits of its chunk index that come
+    // from threadIdx), all as byte offsets; the iteration and element bits
+    // come from the uniform tables.
+    const uint32_t tau0 = tid << VB;
+    uint64_t in_t = 0, out_t = 0;
+    uint32_t ph_t = 0, ga_t = 0;
+#pragma unroll 1
+    for (int i = VB; i < D; ++i) {
+        if ((tau0 >> i) & 1u) {
+            in_t ^= p.tau_in[i];
+            out_t ^= p.om_out[i];
+            ph_t ^= p.phi[i];
+            ga_t ^= p.gam[i];
+        }
+    }
+    in_t <<= EB;
+    out_t <<= EB;
+    ph_t <<= EB;
+    ga_t <<= EB;
+    uint64_t my_cin = 0, my_cout = 0;
+    if ((int)lane < p.n_block_bits) {
+        my_cin = p.col_in[lane] << EB;
+        my_cout = p.col_out[lane];
+    }
+    uint32_t my_gl = 0;
+    if ((int)lane < p.t_out) my_gl = p.gam[lane] << EB;
+    const uint64_t lowm = (1ull << p.t_out) - 1ull;
+
+    bool act[QPT];
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) act[i] = tid + (uint32_t)i * NT < p.chunks;
+
+    // Byte origins of tile b: input origin ib, output run origin ob, and the
+    // shared-memory offset g that realigns output run positions with the tile.
+    auto tile_bases = [&](uint64_t b, uint64_t& ib, uint64_t& ob, uint32_t& g) {
+        const bool bit = (b >> lane) & 1ull;
+        ib = warp_xor64(bit ? my_cin : 0ull);
+        const uint64_t raw = warp_xor64(bit ? my_cout : 0ull) ^ p.c;
+        ob = (raw & ~lowm) << EB;
+        const uint32_t delta = (uint32_t)(raw & lowm);
+        g = __reduce_xor_sync(0xffffffffu, ((delta >> lane) & 1u) ? my_gl : 0u);
+    };
+    // The thread's own offsets are passed through an empty asm each tile so
+    // the compiler recomputes the per-chunk addresses (one XOR each) instead of
+    // holding dozens of loop-invariant addresses in registers.
+    auto load_tile = [&](uint64_t ib, uint4 (&r)[QPT]) {
+        uint64_t it = in_t ^ ib;
+        asm volatile("" : "+l"(it));
+#pragma unroll
+        for (int i = 0; i < QPT; ++i)
+            if (act[i]) r[i] = ld_stream(reinterpret_cast<const uint4*>(src + (it ^ p.it_in[i])));
+    };
+
+    const uint64_t nt = p.n_tiles;
+    uint64_t b = blockIdx.x;
+    uint4 r[QPT];
+    uint64_t ib = 0, ob = 0;
+    uint32_t g = 0;
+    if (b < nt) {
+        tile_bases(b, ib, ob, g);
+        load_tile(ib, r);
+    }
+    for (; b < nt; b += gridDim.x) {
+        uint32_t ph = ph_t;
+        asm volatile("" : "+r"(ph));
+#pragma unroll
+        for (int i = 0; i < QPT; ++i) {
+            if (!act[i]) continue;
+            T e[VEC];
+            memcpy(e, &r[i], 16);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) *reinterpret_cast<T*>(tile + (ph ^ p.st_slot[i * VEC + j])) = e[j];
+        }
+        __syncthreads();
+        const uint64_t cur_ob = ob;
+        const uint32_t ga = ga_t ^ g;
+        const uint64_t nb = b + gridDim.x;
+        if (nb < nt) {
+            tile_bases(nb, ib, ob, g);
+            load_tile(ib, r);
+        }
+        uint64_t ot = out_t ^ cur_ob;
+        asm volatile("" : "+l"(ot));
+#pragma unroll
+        for (int i = 0; i < QPT; ++i) {
+            if (!act[i]) continue;
+            T e[VEC];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) e[j] = *reinterpret_cast<const T*>(tile + (ga ^ p.ld_slot[i * VEC + j]));
+            uint4 v;
+            memcpy(&v, e, 16);
+            st_stream(reinterpret_cast<uint4*>(dst + (ot ^ p.it_out[i])), v);
+        }
+        __syncthreads();
+    }
+}
+
+// Per-element kernel for arrays too small for one 16-byte vector per run.
+template <int ELEM>
+__global__ void __launch_bounds__(32)
+    bmmc_naive_kernel(const __grid_constant__ NaiveParams p, const void* __restrict__ in_,
+                      void* __restrict__ out_) {
+    using T = typename ElemType<ELEM>::T;
+    const T* in = static_cast<const T*>(in_);
+    T* out = static_cast<T*>(out_);
+    for (uint64_t x = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; x < p.count;
+         x += (uint64_t)gridDim.x * blockDim.x) {
+        uint64_t y = 0;
+        for (int i = 0; i < p.n; ++i) y |= (uint64_t)(__popcll(p.rows[i] & x) & 1) << i;
+        out[y ^ p.c] = in[x];
+    }
+}
+
+// Plain copy: U independent 16-byte vectors in flight per thread.
+template <int U>
+__global__ void __launch_bounds__(256)
+    bmmc_copy_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, uint64_t nvec) {
+    const uint64_t stride = (uint64_t)gridDim.x * 256u * U;
+    for (uint64_t base = (uint64_t)blockIdx.x * 256u * U + threadIdx.x; base < nvec; base += stride) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + (uint64_t)u * 256u < nvec) v[u] = ld_stream(in + base + (uint64_t)u * 256u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + (uint64_t)u * 256u < nvec) st_stream(out + base + (uint64_t)u * 256u, v[u]);
+    }
+}
+
+__global__ void bmmc_copy_tail_kernel(const unsigned char* __restrict__ in,
+                                      unsigned char* __restrict__ out, uint64_t bytes) {
+    for (uint64_t i = threadIdx.x; i < bytes; i += blockDim.x) out[i] = in[i];
+}
+
+// ---------------------------------------------------------------------------
+// Launch helpers
+// ---------------------------------------------------------------------------
+
+using TiledFn = void (*)(const TiledParams, const uint4*, uint4*);
+
+template <int ELEM>
+static TiledFn pick_tiled(int nt, int qpt) {
+    if (nt == 32) return bmmc_tiled_kernel<ELEM, 32, 1>;
+    if (nt == 64) return bmmc_tiled_kernel<ELEM, 64, 1>;
+    if (nt == 128) return bmmc_tiled_kernel<ELEM, 128, 1>;
+    if (nt == 256) {
+        switch (qpt) {
+            case 1: return bmmc_tiled_kernel<ELEM, 256, 1>;
+            case 2: return bmmc_tiled_kernel<ELEM, 256, 2>;
+            case 4: return bmmc_tiled_kernel<ELEM, 256, 4>;
+            case 8: return bmmc_tiled_kernel<ELEM, 256, 8>;
+            case 16: return bmmc_tiled_kernel<ELEM, 256, 16>;
+        }
+    }
+    return nullptr;
+}
+
+static TiledFn tiled_fn(int elem, int nt, int qpt) {
+    switch (elem) {
+        case 4: return pick_tiled<4>(nt, qpt);
+        case 8: return pick_tiled<8>(nt, qpt);
+        case 16: return pick_tiled<16>(nt, qpt);
+    }
+    return nullptr;
+}
+
+namespace {
+struct DeviceCache {
+    std::mutex mu;
+    std::map<int, int> sms;                                  // device -> SM count
+    std::map<std::tuple<int, const void*, int>, int> occ;    // (device, fn, smem) -> blocks/SM
+};
+DeviceCache& cache() {
+    static DeviceCache c;
+    return c;
+}
+}  // namespace
+
+static cudaError_t sm_count(int dev, int* out) {
+    auto& c = cache();
+    std::lock_guard<std::mutex> lk(c.mu);
+    auto it = c.sms.find(dev);
+    if (it != c.sms.end()) { *out = it->second; return cudaSuccess; }
+    int v = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    c.sms[dev] = v;
+    *out = v;
+    return cudaSuccess;
+}
+
+static cudaError_t blocks_per_sm(int dev, const void* fn, int threads, int smem, int* out) {
+    auto& c = cache();
+    std::lock_guard<std::mutex> lk(c.mu);
+    auto key = std::make_tuple(dev, fn, smem);
+    auto it = c.occ.find(key);
+    if (it != c.occ.end()) { *out = it->second; return cudaSuccess; }
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    int v = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (v < 1) return cudaErrorInvalidConfiguration;
+    c.occ[key] = v;
+    *out = v;
+    return cudaSuccess;
+}
+
+cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStream_t stream,
+                         int grid_override) {
+    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per = 0;
+    if ((e = sm_count(dev, &sms)) != cudaSuccess) return e;
+    if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
+    uint64_t grid = (uint64_t)sms * (uint64_t)per;
+    if (grid_override > 0) grid = (uint64_t)grid_override;
+    if (grid > P.tiles) grid = P.tiles;
+    fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(P.tp, static_cast<const uint4*>(in),
+                                                             static_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_naive(const PassPlan& P, const void* in, void* out, cudaStream_t stream) {
+    const unsigned blocks = (unsigned)((P.np.count + 31) / 32);
+    switch (P.elem) {
+        case 4: bmmc_naive_kernel<4><<<blocks, 32, 0, stream>>>(P.np, in, out); break;
+        case 8: bmmc_naive_kernel<8><<<blocks, 32, 0, stream>>>(P.np, in, out); break;
+        case 16: bmmc_naive_kernel<16><<<blocks, 32, 0, stream>>>(P.np, in, out); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t stream) {
+    constexpr int U = 4;
+    const uint64_t nvec = bytes / 16;
+    if (nvec) {
+        auto fn = bmmc_copy_kernel<U>;
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        int sms = 0, per = 0;
+        if ((e = sm_count(dev, &sms)) != cudaSuccess) return e;
+        if ((e = blocks_per_sm(dev, (const void*)fn, 256, 0, &per)) != cudaSuccess) return e;
+        uint64_t need = (nvec + 256u * U - 1) / (256u * U);
+        uint64_t grid = (uint64_t)sms * per;
+        if (grid > need) grid = need;
+        fn<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out),
+                                                nvec);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const uint64_t tail = bytes - nvec * 16;
+    if (tail) {
+        bmmc_copy_tail_kernel<<<1, 32, 0, stream>>>(static_cast<const unsigned char*>(in) + nvec * 16,
+                                                    static_cast<unsigned char*>(out) + nvec * 16, tail);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_pass(const PassPlan& P, const void* in, void* out, cudaStream_t stream) {
+    switch (P.kernel) {
+        case KERNEL_COPY: return launch_copy(in, out, ((size_t)1 << P.n) * P.elem, stream);
+        case KERNEL_NAIVE: return launch_naive(P, in, out, stream);
+        case KERNEL_TILED: return launch_tiled(P, in, out, stream, 0);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace bmmc

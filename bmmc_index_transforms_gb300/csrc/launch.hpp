@@ -1,0 +1,22 @@
+// Launchers of the device kernels (defined in kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+
+#include "planner.hpp"
+
+namespace bmmc {
+
+// One pass of a plan on `stream` (copy, per-element or tiled kernel).
+cudaError_t launch_pass(const PassPlan& P, const void* in, void* out, cudaStream_t stream);
+
+// The tiled kernel with an explicit grid (0 = one resident wave).
+cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStream_t stream,
+                         int grid_override);
+
+// Plain copy of `bytes` bytes.
+cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t stream);
+
+}  // namespace bmmc

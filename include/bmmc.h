@@ -1,0 +1,208 @@
+/*
+ * bmmc.h - permuting arrays of 2^n elements by BMMC index maps on GB300.
+ *
+ * A BMMC (bit-matrix-multiply-and-complement) map sends index x, viewed as a
+ * bit vector in F2^n with bit i worth 2^i, to y = A.x XOR c, where A is an
+ * invertible n x n bit matrix and c an n-bit vector.  Each bit of y is the
+ * parity of the AND of one row of A with x, XOR one bit of c.  Transposes of
+ * power-of-two matrices, bit reversal and array reversal are special cases.
+ * Definition, examples and the BP / BPC / BMMC classes: "Efficient GPU
+ * Implementation of Affine Index Permutations on Arrays" (FHPNC '23), §1.
+ *
+ * Permuting an array is the scatter   out[A.x XOR c] = in[x]   for every x in
+ * [0, 2^n), each element an opaque block of elem_size bytes (4, 8 or 16):
+ * the convention of that paper's appendix kernels.  The library is
+ * out-of-place; in and out must not overlap.
+ *
+ * Conventions shared by every entry point:
+ *   - A_rows[i] holds row i of A: bit j of A_rows[i] is A[i][j], so output
+ *     bit i is parity(A_rows[i] & x) XOR bit i of c.  Bits at or above n in
+ *     A_rows[i] or in c are rejected (BMMC_ERR_INVALID_ARG).
+ *   - Device pointers are caller-owned device (or managed) memory of exactly
+ *     2^n * elem_size bytes, 16-byte aligned (BMMC_ERR_MISALIGNED otherwise).
+ *     The library never allocates on a permute call, except as stated for the
+ *     two-factor mode below.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return without synchronising; launch
+ *     failures are reported as BMMC_ERR_CUDA.  A failed call enqueues nothing
+ *     and writes nothing to `out`.
+ *   - There is no CPU fallback: without a usable CUDA device the permute
+ *     calls return BMMC_ERR_CUDA.  The planning calls are host-only and need
+ *     no device.
+ *   - 1 <= n <= 40.
+ */
+#ifndef BMMC_GB300_H
+#define BMMC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BMMC_OK = 0,
+    BMMC_ERR_INVALID_ARG = 1,     /* n out of range, stray bits, null pointer, bad option */
+    BMMC_ERR_SINGULAR = 2,        /* A is not invertible over F2: the map is no permutation */
+    BMMC_ERR_UNSUPPORTED_ELEM = 3,/* elem_size not in {4, 8, 16} */
+    BMMC_ERR_MISALIGNED = 4,      /* a device pointer is not 16-byte aligned */
+    BMMC_ERR_ALIAS = 5,           /* in and out (or scratch) overlap */
+    BMMC_ERR_CUDA = 6,            /* a CUDA runtime call or a launch failed */
+    BMMC_ERR_TIMEOUT = 7,         /* a bounded device-side wait gave up */
+    BMMC_ERR_NO_SCRATCH = 8,      /* two-factor plan run without scratch memory */
+    BMMC_ERR_INTERNAL = 9         /* a planner self-check failed (a bug; please report) */
+} bmmc_status;
+
+/* Class of (A, c), from the paper's §1 hierarchy. */
+typedef enum {
+    BMMC_CLASS_IDENTITY = 0,      /* A = I, c = 0: a copy */
+    BMMC_CLASS_COMPLEMENT = 1,    /* A = I, c != 0: e.g. array reversal */
+    BMMC_CLASS_BP = 2,            /* A a permutation matrix, c = 0 (transpose, bit reversal) */
+    BMMC_CLASS_BPC = 3,           /* A a permutation matrix, c != 0 */
+    BMMC_CLASS_BMMC = 4           /* any other invertible A */
+} bmmc_class;
+
+/* Execution mode.
+ * SINGLE_PASS: one tiled kernel for any invertible A.  The tile is the
+ *   subspace spanned by the low t_in input bits and A^-1 of the low t_out
+ *   output bits (enlarged to 2^tile_bits elements), so every tile is read as
+ *   aligned runs of 2^t_in elements and written as aligned runs of 2^t_out.
+ * TWO_FACTOR: A = T1.T2 with T1 and T2 each tiled in the paper's narrower
+ *   sense (§5: any BMMC is a product of at most two tiled BMMCs); T2 is
+ *   applied into a scratch buffer, then T1 (with c) into out.  Twice the
+ *   memory traffic; kept for the paper's two-kernel comparison. */
+typedef enum {
+    BMMC_MODE_SINGLE_PASS = 0,
+    BMMC_MODE_TWO_FACTOR = 1
+} bmmc_mode;
+
+typedef struct {
+    int mode;            /* bmmc_mode */
+    int t_in;            /* log2 elements per contiguous input run; 0 = default (256 B runs) */
+    int t_out;           /* log2 elements per contiguous output run; 0 = default */
+    int tile_bits;       /* log2 elements per tile; 0 = default */
+    int alloc_scratch;   /* TWO_FACTOR only: 1 = the plan owns a device scratch buffer
+                            of 2^n * elem_size bytes, allocated by bmmc_plan_ex on the
+                            current device and freed by bmmc_plan_destroy */
+} bmmc_plan_opts;
+
+typedef struct bmmc_plan_s *bmmc_plan_t;
+
+typedef struct {
+    int n;
+    int elem_size;
+    int cls;             /* bmmc_class */
+    int mode;            /* bmmc_mode */
+    int t_in, t_out;     /* run lengths actually used (log2 elements) */
+    int tile_bits;       /* log2 elements per tile actually used */
+    int n_over;          /* dim(L_in intersect A^-1 L_out): low input bits that also feed
+                            low output bits (paper §6 discussion of n_over) */
+    int r2_factors;      /* 1 if A is tiled in the narrow sense at t = t_out, else 2 */
+    int kernel;          /* 0 = tiled kernel, 1 = copy kernel, 2 = per-element kernel */
+    int threads;         /* threads per block of the tiled kernel */
+    int chunks_per_thread;
+    uint64_t tiles;      /* number of tiles (units of work) of the tiled kernel */
+    int smem_bytes;      /* shared memory per block */
+    int bank_conflicts;  /* extra shared-memory wavefronts per tile found by the planner's
+                            self-check of its layout (0 = conflict-free on both phases) */
+    uint64_t c;
+} bmmc_plan_info_t;
+
+/* Build a plan for (A, c) with default options.  Host only; no device work.
+ * On success *plan receives a new plan owned by the caller (free it with
+ * bmmc_plan_destroy); on failure *plan is set to NULL.
+ * Errors: INVALID_ARG (plan or A_rows NULL, n outside [1, 40], bits >= n),
+ * UNSUPPORTED_ELEM, SINGULAR, INTERNAL. */
+bmmc_status bmmc_plan(bmmc_plan_t *plan, int n, const uint64_t *A_rows, uint64_t c,
+                      size_t elem_size);
+
+/* bmmc_plan with options (opts may be NULL for defaults).  With
+ * mode = TWO_FACTOR and alloc_scratch = 1 this call allocates device memory
+ * (BMMC_ERR_CUDA when that fails). */
+bmmc_status bmmc_plan_ex(bmmc_plan_t *plan, int n, const uint64_t *A_rows, uint64_t c,
+                         size_t elem_size, const bmmc_plan_opts *opts);
+
+/* Free a plan (NULL is accepted).  A plan must not be destroyed while work
+ * using its scratch buffer is still running on a stream. */
+bmmc_status bmmc_plan_destroy(bmmc_plan_t plan);
+
+/* Describe a plan.  Errors: INVALID_ARG for NULL arguments. */
+bmmc_status bmmc_plan_info(bmmc_plan_t plan, bmmc_plan_info_t *info);
+
+/* The paper's §5 contract: A = T1.T2 with both factors tiled in the narrow
+ * sense.  which = 1 writes T1's n rows, which = 2 writes T2's (T2 is the
+ * identity and T1 = A when A is already tiled).  Host only. */
+bmmc_status bmmc_plan_factor(bmmc_plan_t plan, int which, uint64_t *rows_out);
+
+/* Input tile of the single-pass plan, for inspection: tile_basis receives
+ * tile_bits vectors in F2^n (the low t_in unit vectors first, then the
+ * extra row vectors), block_bits receives the n - tile_bits input bit
+ * positions that select the tile.  Either pointer may be NULL. */
+bmmc_status bmmc_plan_tile(bmmc_plan_t plan, uint64_t *tile_basis, int *block_bits);
+
+/* Permute: out[A.x XOR c] = in[x].  in, out: device pointers of
+ * 2^n * elem_size bytes each, 16-byte aligned, not overlapping.
+ * A TWO_FACTOR plan needs its own scratch (alloc_scratch) or
+ * bmmc_permute_scratch; otherwise NO_SCRATCH. */
+bmmc_status bmmc_permute(bmmc_plan_t plan, const void *in, void *out, void *stream);
+
+/* Permute with caller-supplied scratch (2^n * elem_size bytes, 16-byte
+ * aligned, overlapping neither in nor out).  Single-pass plans ignore it. */
+bmmc_status bmmc_permute_scratch(bmmc_plan_t plan, const void *in, void *out, void *scratch,
+                                 void *stream);
+
+/* End-to-end permute of HOST arrays through caller-owned device staging
+ * buffers: enqueues on `stream`, in order, a copy of h_in to d_in, the
+ * permutation d_in -> d_out, and a copy of d_out to h_out (one
+ * cudaMemcpyAsync per direction; with pinned host memory the call returns
+ * before the copies finish, so synchronise the stream before reading h_out).
+ * h_in, h_out: 2^n * elem_size bytes of host memory; d_in, d_out: device
+ * buffers of the same size, 16-byte aligned, not overlapping.  Single-pass
+ * plans, or two-factor plans that own their scratch. */
+bmmc_status bmmc_permute_host(bmmc_plan_t plan, const void *h_in, void *h_out, void *d_in,
+                              void *d_out, void *stream);
+
+/* Row-major R x C matrix (R = 2^rows_log2, C = 2^cols_log2) to its C x R
+ * transpose: the element at in[y*C + x] goes to out[x*R + y] ("A kernel that
+ * is correct", Kernels from zero ep. 1).  As a BMMC: output bit i is input
+ * bit (i + cols_log2) mod n, n = rows_log2 + cols_log2, c = 0. */
+bmmc_status transpose2d(int rows_log2, int cols_log2, size_t elem_size, const void *in,
+                        void *out, void *stream);
+
+/* Bit-permute-complement: output bit i is input bit perm[i] XOR bit i of c
+ * (paper §1, BPC).  perm must be a permutation of 0..n-1. */
+bmmc_status bpc_permute(int n, const int *perm, uint64_t c, size_t elem_size, const void *in,
+                        void *out, void *stream);
+
+/* Dimension permutation of a row-major array whose ndims dimensions are all
+ * powers of two (sizes 2^dims_log2[k]): out = in.permute(axes) made
+ * contiguous, i.e. output dimension k is input dimension axes[k].  This is
+ * the power-of-two case of the LMAD permuted copies of "Speeding up GPU
+ * copies by permuting iteration spaces" (Futhark blog), run as one BPC.
+ * 1 <= ndims <= 40, sum of dims_log2 in [1, 40]. */
+bmmc_status bmmc_dims_permute(int ndims, const int *dims_log2, const int *axes,
+                              size_t elem_size, const void *in, void *out, void *stream);
+
+/* The bit permutation bmmc_dims_permute uses: perm_out[i] (n entries, n the
+ * sum of dims_log2) is the input bit that output bit i is taken from.  Host
+ * only. */
+bmmc_status bmmc_dims_permute_bits(int ndims, const int *dims_log2, const int *axes,
+                                   int *perm_out);
+
+/* Plain copy of `bytes` bytes (16-byte vectors, any tail byte-wise): the
+ * practical ceiling a permutation is measured against ("A kernel that is
+ * correct", "The ceiling: a copy").  Pointers 16-byte aligned. */
+bmmc_status bmmc_copy(const void *in, void *out, size_t bytes, void *stream);
+
+/* Static string for a status code (never NULL). */
+const char *bmmc_status_string(bmmc_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int bmmc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BMMC_GB300_H */

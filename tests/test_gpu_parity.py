@@ -1,0 +1,343 @@
+"""GPU parity: the CUDA path against the CPU oracle, bit for bit.
+
+Every expected value is computed by ``oracle/`` from the same seeded
+inputs.  The tolerance is zero (byte equality): a permutation moves bytes and
+never rounds.  Inputs are filled with each element's own index, so a
+misplaced element can never pass for the right one ("A kernel that is
+correct", "The check").
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import reference as ref
+from bmmc_index_transforms_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+HOST_THREADS = max(1, min(32, oracle.host_threads()))
+
+
+@pytest.fixture(scope="module")
+def bm():
+    from bmmc_index_transforms_gb300 import _build
+
+    _build.build()
+    import bmmc_index_transforms_gb300 as m
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def _dev(a: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)).cuda()
+
+
+def _host(t, like: np.ndarray):
+    return t.cpu().numpy().view(like.dtype).reshape(like.shape)
+
+
+def _random(seed, n, low_to_high=0):
+    rows, c, _ = synth.draw_bmmc(seed, n, lambda r: ref.f2_rank(n, r) == n, low_to_high=low_to_high)
+    return rows, c
+
+
+def _run(bm, rows, c, arr, **opts):
+    n = len(rows)
+    elem = arr.nbytes >> n
+    d_in = _dev(arr)
+    d_out = torch.zeros_like(d_in)
+    with bm.Plan(rows, c, elem, **opts) as p:
+        info = p.info
+        if info["mode"] == 1 and not opts.get("alloc_scratch"):
+            scratch = torch.empty_like(d_in)
+            p.permute_scratch(d_in, d_out, scratch)
+        else:
+            p.permute(d_in, d_out)
+    torch.cuda.synchronize()
+    return _host(d_out, arr), info
+
+
+# ---------------------------------------------------------------------------
+# Exhaustive tiny sizes and seeded moderate sizes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("elem", [4, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_every_bmmc_of_tiny_size(bm, n, elem):
+    arr = synth.fill_int(n, elem)
+    cases = 0
+    for A in itertools.product(range(1 << n), repeat=n):
+        A = list(A)
+        if ref.f2_rank(n, A) != n:
+            continue
+        for c in range(1 << n):
+            got, _ = _run(bm, A, c, arr)
+            assert got.tobytes() == ref.bmmc_permute(n, A, c, arr).tobytes(), (A, c)
+            cases += 1
+    assert cases == (1 << n) * {1: 1, 2: 6, 3: 168}[n]
+
+
+@pytest.mark.parametrize("elem", [4, 8, 16])
+@pytest.mark.parametrize("n", [4, 5, 7, 9, 11, 12, 13, 14, 15, 17, 19, 21])
+def test_random_bmmc_moderate_sizes(bm, n, elem):
+    for seed in range(3):
+        rows, c = _random(1000 * n + seed, n)
+        arr = synth.fill_int(n, elem)
+        got, info = _run(bm, rows, c, arr)
+        want = oracle.scatter(n, rows, c, arr)
+        assert got.tobytes() == want.tobytes(), (n, elem, seed, info)
+
+
+@pytest.mark.parametrize("elem", [4, 8, 16])
+@pytest.mark.parametrize("t_in,t_out,tile_bits", [(3, 3, 0), (4, 6, 0), (6, 4, 11), (5, 5, 12), (7, 6, 13),
+                                                  (2, 2, 5), (6, 6, 14)])
+def test_tile_shapes(bm, elem, t_in, t_out, tile_bits):
+    """Asymmetric runs, enlarged tiles and tiny tiles (fewer chunks than
+    threads) all give the oracle's bytes."""
+    vb = {4: 2, 8: 1, 16: 0}[elem]
+    if t_in < vb or t_out < vb or (tile_bits and (1 << tile_bits) * elem > 200 * 1024):
+        pytest.skip("shape not valid for this element size")
+    for n, seed in [(16, 1), (18, 2), (13, 3)]:
+        rows, c = _random(seed * 97 + elem, n)
+        arr = synth.fill_int(n, elem)
+        got, info = _run(bm, rows, c, arr, t_in=t_in, t_out=t_out, tile_bits=tile_bits)
+        assert info["bank_conflicts"] == 0
+        assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), info
+
+
+def test_structured_maps_moderate(bm):
+    n = 18
+    for rows in (ref.bitrev_rows(n), ref.rotate_rows(n, 7), ref.identity_rows(n)):
+        for c in (0, 1, (1 << n) - 1, 0x2A5F3):
+            for elem in (4, 8, 16):
+                arr = synth.fill_int(n, elem)
+                got, _ = _run(bm, rows, c, arr)
+                assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
+
+
+def test_two_factor_mode_matches_oracle(bm):
+    for n, elem, seed in [(12, 4, 0), (16, 8, 1), (20, 4, 2), (20, 16, 3), (22, 4, 4)]:
+        rows, c = _random(seed, n, low_to_high=min(10, n // 2))
+        arr = synth.fill_int(n, elem)
+        got, info = _run(bm, rows, c, arr, mode=1)
+        assert info["mode"] == 1
+        assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
+        got2, _ = _run(bm, rows, c, arr, mode=1, alloc_scratch=True)
+        assert got2.tobytes() == got.tobytes()
+
+
+# ---------------------------------------------------------------------------
+# The benchmark configurations
+# ---------------------------------------------------------------------------
+
+def test_config_random_n16_seed0(bm):
+    n = synth.SMALL_N
+    rows, c = _random(0, n)
+    arr = synth.fill_int(n, 4)
+    got, _ = _run(bm, rows, c, arr)
+    assert got.tobytes() == ref.bmmc_permute(n, rows, c, arr).tobytes()
+
+
+def test_config_transpose_4096(bm):
+    s = synth.TRANSPOSE_SIDE_LOG2
+    arr = synth.fill_float_index(2 * s)
+    want = oracle.transpose2d(s, s, arr)
+    got, info = _run(bm, ref.rotate_rows(2 * s, s), 0, arr)
+    assert got.tobytes() == want.tobytes()
+    assert info["class_name"] == "bp"
+    d_in, d_out = _dev(arr), torch.zeros(arr.nbytes, dtype=torch.uint8, device="cuda")
+    bm.transpose2d(s, s, 4, d_in, d_out)
+    torch.cuda.synchronize()
+    assert _host(d_out, arr).tobytes() == want.tobytes()
+    # non-square transposes through the convenience call
+    for r, cl, elem in [(10, 13, 4), (13, 10, 8), (7, 11, 16)]:
+        a = synth.fill_int(r + cl, elem)
+        d_in, d_out = _dev(a), torch.zeros(a.nbytes, dtype=torch.uint8, device="cuda")
+        bm.transpose2d(r, cl, elem, d_in, d_out)
+        torch.cuda.synchronize()
+        assert _host(d_out, a).tobytes() == oracle.transpose2d(r, cl, a).tobytes()
+
+
+def _full_check(bm, rows, c, elem, sampled_only=False):
+    """Run at n = 28 on the index fill and check every output (or a sample)
+    against the oracle's gather form out[y] == A^-1 (y ^ c)."""
+    n = len(rows)
+    N = 1 << n
+    if elem == 4:
+        d_in = torch.arange(N, dtype=torch.int64, device="cuda").to(torch.int32)
+    elif elem == 8:
+        d_in = torch.arange(N, dtype=torch.int64, device="cuda")
+    else:
+        d_in = torch.zeros((N, 2), dtype=torch.int64, device="cuda")
+        d_in[:, 0] = torch.arange(N, dtype=torch.int64, device="cuda")
+    d_out = torch.empty_like(d_in)
+    with bm.Plan(rows, c, elem) as p:
+        p.permute(d_in, d_out)
+        info = p.info
+    torch.cuda.synchronize()
+    inv = ref.f2_inverse(n, rows)
+    # sampled, one by one through the oracle
+    xs = synth.sample_indices(n * 7 + c % 1000, n, 4096)
+    ys = np.array([oracle.index(n, rows, c, int(x)) for x in xs], dtype=np.int64)
+    got = d_out.view(torch.int64 if elem == 8 else torch.int32).reshape(N, -1)[torch.from_numpy(ys).cuda()]
+    got = got.cpu().numpy()
+    if elem == 16:
+        assert np.array_equal(got.view(np.int64)[:, 0], xs.astype(np.int64))
+        assert np.all(got.view(np.int64)[:, 1] == 0)
+    else:
+        assert np.array_equal(got[:, 0].astype(np.int64), xs.astype(np.int64))
+    if not sampled_only:
+        host = d_out.cpu().numpy()
+        bad, first = oracle.check_index_fill(n, inv, c, host, elem, threads=HOST_THREADS)
+        assert bad == 0, f"{bad} mismatches, first at y={first}"
+    del d_in, d_out
+    torch.cuda.empty_cache()
+    return info
+
+
+def test_config_bitrev_n28_int32(bm):
+    _full_check(bm, ref.bitrev_rows(28), 0, 4)
+
+
+def test_config_bitrev_n28_int64(bm):
+    _full_check(bm, ref.bitrev_rows(28), 0, 8)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_config_random_n28_full(bm, seed):
+    rows, c = _random(seed, 28)
+    info = _full_check(bm, rows, c, 4)
+    assert info["bank_conflicts"] == 0
+
+
+def test_config_random_n28_all_seeds_sampled(bm):
+    for seed in range(32):
+        rows, c = _random(seed, 28)
+        _full_check(bm, rows, c, 4, sampled_only=True)
+    rows, c = _random(0, 28, low_to_high=synth.WORST_LOW_BITS)
+    info = _full_check(bm, rows, c, 4)
+    assert info["r2_factors"] == 2
+
+
+def test_config_five_d_permute(bm):
+    """[32,64,64,64,32] fp32 permuted (4,2,0,3,1): the integer-bit fill checks
+    every element, the (float)(i mod 2^24) fill is compared on a sample, and
+    the float4 view [32,64,64,64,8] likewise."""
+    shape_log2 = (5, 6, 6, 6, 5)
+    axes = synth.FIVE_D_AXES
+    perm = ref.axes_permute_bits(shape_log2, axes)
+    rows = [1 << p for p in perm]
+    n = 28
+    N = 1 << n
+    d_in = torch.arange(N, dtype=torch.int64, device="cuda").to(torch.int32)
+    d_out = torch.empty_like(d_in)
+    bm.bmmc_dims_permute(shape_log2, axes, 4, d_in, d_out)
+    torch.cuda.synchronize()
+    bad, first = oracle.check_index_fill(n, ref.f2_inverse(n, rows), 0, d_out.cpu().numpy(), 4,
+                                         threads=HOST_THREADS)
+    assert bad == 0, first
+    # float fill, sampled against numpy's transpose of the same shape (library routine)
+    f = (torch.arange(N, dtype=torch.int64, device="cuda") % (1 << 24)).to(torch.float32)
+    fo = torch.empty_like(f)
+    bm.bmmc_dims_permute(shape_log2, axes, 4, f, fo)
+    xs = synth.sample_indices(5, n, 4096).astype(np.int64)
+    ys = np.array([ref.bpc_index(n, perm, 0, int(x)) for x in xs], dtype=np.int64)
+    assert np.array_equal(fo[torch.from_numpy(ys).cuda()].cpu().numpy(),
+                          (xs % (1 << 24)).astype(np.float32))
+    del d_in, d_out, f, fo
+    # float4 view: 2^26 elements of 16 bytes
+    shape4 = (5, 6, 6, 6, 3)
+    perm4 = ref.axes_permute_bits(shape4, axes)
+    rows4 = [1 << p for p in perm4]
+    info = _full_check(bm, rows4, 0, 16)
+    assert info["bank_conflicts"] == 0
+
+
+# ---------------------------------------------------------------------------
+# Convenience entry points, copy, end-to-end, edge cases
+# ---------------------------------------------------------------------------
+
+def test_bpc_permute_and_dims_permute(bm):
+    n = 20
+    perm = [(5 * i + 3) % n for i in range(n)]
+    for c in (0, 0xABCDE & ((1 << n) - 1)):
+        for elem in (4, 8, 16):
+            arr = synth.fill_int(n, elem)
+            d_in, d_out = _dev(arr), torch.zeros(arr.nbytes, dtype=torch.uint8, device="cuda")
+            bm.bpc_permute(n, perm, c, elem, d_in, d_out)
+            torch.cuda.synchronize()
+            assert _host(d_out, arr).tobytes() == ref.bpc_permute(n, perm, c, arr).tobytes()
+    shape, axes = (3, 4, 2, 5), (2, 0, 3, 1)
+    arr = np.arange(1 << 14, dtype=np.uint32)
+    d_in, d_out = _dev(arr), torch.zeros(arr.nbytes, dtype=torch.uint8, device="cuda")
+    bm.bmmc_dims_permute(shape, axes, 4, d_in, d_out)
+    torch.cuda.synchronize()
+    want = arr.reshape([1 << s for s in shape]).transpose(axes).copy().ravel()
+    assert np.array_equal(_host(d_out, arr), want)
+
+
+@pytest.mark.parametrize("nbytes", [16, 48, 4096, 4096 + 7, (1 << 20) + 3, 123456789])
+def test_copy_kernel(bm, nbytes):
+    a = (np.arange(nbytes, dtype=np.uint64) * 2654435761 % 251).astype(np.uint8)
+    d_in = torch.from_numpy(a).cuda()
+    d_out = torch.zeros_like(d_in)
+    bm.bmmc_copy(d_in, d_out, nbytes)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_out.cpu().numpy(), a)
+
+
+def test_end_to_end_host_buffers(bm):
+    n, elem = 22, 4
+    rows, c = _random(5, n)
+    arr = synth.fill_int(n, elem)
+    h_in = torch.from_numpy(arr.view(np.uint8).copy()).pin_memory()
+    h_out = torch.zeros_like(h_in).pin_memory()
+    d_in = torch.empty(arr.nbytes, dtype=torch.uint8, device="cuda")
+    d_out = torch.empty_like(d_in)
+    with bm.Plan(rows, c, elem) as p:
+        p.permute_host(h_in, h_out, d_in, d_out)
+        torch.cuda.current_stream().synchronize()
+    assert h_out.numpy().view(np.uint32).tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
+
+
+def test_streams_and_repeat_calls(bm):
+    """Two plans on two streams, each launched twice: same bytes as the oracle."""
+    n, elem = 20, 8
+    outs = []
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    arr = synth.fill_int(n, elem)
+    d_in = _dev(arr)
+    plans = [bm.Plan(*_random(s, n), elem) for s in (8, 9)]
+    for p, s in zip(plans, (s1, s2)):
+        o = torch.zeros_like(d_in)
+        with torch.cuda.stream(s):
+            p.permute(d_in, o)
+            p.permute(d_in, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for p, o, seed in zip(plans, outs, (8, 9)):
+        rows, c = _random(seed, n)
+        assert _host(o, arr).tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
+        p.close()
+
+
+def test_device_pointer_errors(bm):
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    h = bm.Plan(ref.bitrev_rows(12), 0, 4)
+    with pytest.raises(bm.BmmcError) as e:
+        h.permute(d.data_ptr() + 4, d.data_ptr() + 32768)
+    assert e.value.status == 4
+    with pytest.raises(bm.BmmcError) as e:
+        h.permute(d.data_ptr(), d.data_ptr() + 8192)
+    assert e.value.status == 5
+    h2 = bm.Plan(_random(1, 12)[0], 0, 4, mode=1)
+    with pytest.raises(bm.BmmcError) as e:
+        h2.permute(d.data_ptr(), d.data_ptr() + 32768)
+    assert e.value.status == 8
+    h.close()
+    h2.close()
