@@ -23,7 +23,7 @@ from ._capi import PlanInfo, PlanOpts
 __all__ = [
     "BmmcError", "Plan", "bmmc_plan", "bmmc_plan_ex", "bmmc_plan_destroy", "bmmc_plan_info",
     "bmmc_plan_factor", "bmmc_plan_tile", "bmmc_permute", "bmmc_permute_scratch",
-    "bmmc_permute_host", "transpose2d", "bpc_permute", "bmmc_dims_permute",
+    "bmmc_permute_host", "bmmc_permute_static_scratch", "transpose2d", "bpc_permute", "bmmc_dims_permute",
     "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_status_string", "bmmc_version", "library_path",
 ]
 
@@ -153,6 +153,13 @@ def bmmc_permute_scratch(plan: int, inp, out, scratch, stream=None) -> None:
 def bmmc_permute_host(plan: int, h_in, h_out, d_in, d_out, stream=None) -> None:
     _check(_capi.lib().bmmc_permute_host(plan, _ptr(h_in), _ptr(h_out), _ptr(d_in), _ptr(d_out),
                                          _stream(stream, d_in, d_out)), "bmmc_permute_host")
+
+
+def bmmc_permute_static_scratch(plan: int, inp, out, stream=None) -> None:
+    """Two-factor permute through the library's built-in 16 MiB scratch array,
+    for callers that must not allocate device memory (see include/bmmc.h)."""
+    _check(_capi.lib().bmmc_permute_static_scratch(plan, _ptr(inp), _ptr(out), _stream(stream, inp, out)),
+           "bmmc_permute_static_scratch")
 
 
 def transpose2d(rows_log2: int, cols_log2: int, elem_size: int, inp, out, stream=None) -> None:

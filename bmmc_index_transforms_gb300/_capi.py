@@ -31,6 +31,8 @@ ERR_CUDA = 6
 ERR_TIMEOUT = 7
 ERR_NO_SCRATCH = 8
 ERR_INTERNAL = 9
+ERR_TOO_LARGE = 10
+STATIC_SCRATCH_BYTES = 16 << 20
 
 MODE_SINGLE_PASS = 0
 MODE_TWO_FACTOR = 1
@@ -63,6 +65,7 @@ SIGNATURES = {
     "bmmc_permute": (ctypes.c_int, [vp, vp, vp, vp]),
     "bmmc_permute_scratch": (ctypes.c_int, [vp, vp, vp, vp, vp]),
     "bmmc_permute_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
+    "bmmc_permute_static_scratch": (ctypes.c_int, [vp, vp, vp, vp]),
     "transpose2d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_size_t, vp, vp, vp]),
     "bpc_permute": (ctypes.c_int, [ctypes.c_int, intp, u64, ctypes.c_size_t, vp, vp, vp]),
     "bmmc_dims_permute": (ctypes.c_int, [ctypes.c_int, intp, intp, ctypes.c_size_t, vp, vp, vp]),

@@ -335,6 +335,7 @@ const char* bmmc_status_string(bmmc_status status) {
         case BMMC_ERR_TIMEOUT: return "bounded device wait timed out";
         case BMMC_ERR_NO_SCRATCH: return "two-factor plan needs scratch memory";
         case BMMC_ERR_INTERNAL: return "internal planner error";
+        case BMMC_ERR_TOO_LARGE: return "array exceeds the static scratch capacity (BMMC_STATIC_SCRATCH_BYTES)";
     }
     return "unknown status";
 }

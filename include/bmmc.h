@@ -51,7 +51,9 @@ typedef enum {
     BMMC_ERR_CUDA = 6,            /* a CUDA runtime call or a launch failed */
     BMMC_ERR_TIMEOUT = 7,         /* a bounded device-side wait gave up */
     BMMC_ERR_NO_SCRATCH = 8,      /* two-factor plan run without scratch memory */
-    BMMC_ERR_INTERNAL = 9         /* a planner self-check failed (a bug; please report) */
+    BMMC_ERR_INTERNAL = 9,        /* a planner self-check failed (a bug; please report) */
+    BMMC_ERR_TOO_LARGE = 10       /* array larger than BMMC_STATIC_SCRATCH_BYTES
+                                     (bmmc_permute_static_scratch only) */
 } bmmc_status;
 
 /* Class of (A, c), from the paper's §1 hierarchy. */
@@ -162,6 +164,34 @@ bmmc_status bmmc_permute_scratch(bmmc_plan_t plan, const void *in, void *out, vo
  * plans, or two-factor plans that own their scratch. */
 bmmc_status bmmc_permute_host(bmmc_plan_t plan, const void *h_in, void *h_out, void *d_in,
                               void *d_out, void *stream);
+
+/* Capacity of the library's built-in scratch array used by
+ * bmmc_permute_static_scratch: 16 MiB, i.e. arrays of at most 2^22 elements
+ * of 4 bytes, 2^21 of 8 bytes or 2^20 of 16 bytes.  Every GPU that loads
+ * the library holds this much device memory until the process exits. */
+#define BMMC_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Two-factor permute that allocates no device memory.  This entry point has
+ * no counterpart in the paper; it exists for callers that must not call
+ * cudaMalloc: code whose device memory is owned by a host framework's
+ * allocator or a fixed budget, and latency-critical code that cannot accept
+ * the device-wide synchronisation cudaMalloc / cudaFree may imply.  Instead
+ * of caller-supplied or plan-owned scratch it uses one file-scope device
+ * array of BMMC_STATIC_SCRATCH_BYTES inside the library.
+ *   - plan must be a TWO_FACTOR plan (otherwise BMMC_ERR_INVALID_ARG);
+ *     in/out as for bmmc_permute.
+ *   - Arrays larger than BMMC_STATIC_SCRATCH_BYTES are rejected with
+ *     BMMC_ERR_TOO_LARGE before any work is enqueued.
+ *   - The first call on a device looks up the array's device address on
+ *     that device (the device must be current); make that first call before
+ *     any stream capture begins.
+ *   - Every call shares the one array, and it keeps the last call's
+ *     contents.  Nothing in it needs to start at zero: the first pass
+ *     overwrites every byte the second pass reads.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on the
+ *     array; serialise them, e.g. by issuing them on one stream.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine. */
+bmmc_status bmmc_permute_static_scratch(bmmc_plan_t plan, const void *in, void *out, void *stream);
 
 /* Row-major R x C matrix (R = 2^rows_log2, C = 2^cols_log2) to its C x R
  * transpose: the element at in[y*C + x] goes to out[x*R + y] ("A kernel that

@@ -1,0 +1,91 @@
+"""The allocation-free two-factor entry point, bmmc_permute_static_scratch.
+
+Some callers may not call cudaMalloc at all: code whose device memory
+belongs to a host framework's allocator or to a fixed budget, and
+latency-critical code that cannot afford the device-wide synchronisation an
+allocation may bring.  For them the library keeps one 16 MiB scratch array
+of its own, and this entry point runs the two-factor permutation through it.
+
+The test calls it through the C ABI twice in a row (different matrices and
+element sizes, so the second call starts from the first call's leftover
+scratch contents) and compares each output with the existing two-factor
+entry point, bmmc_permute_scratch, given caller-owned scratch: the outputs
+must be identical byte for byte, the tolerance every permutation test uses.
+It also checks the size limit and the plan-mode check.  The file is named so
+that pytest collects it last.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from bmmc_index_transforms_gb300 import synth
+from oracle import reference as ref
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _two_factor_plan(L, capi, n, rows, c, elem):
+    opts = capi.PlanOpts(capi.MODE_TWO_FACTOR, 0, 0, 0, 0)
+    h = ctypes.c_void_p()
+    rows_c = (ctypes.c_uint64 * n)(*rows)
+    assert L.bmmc_plan_ex(ctypes.byref(h), n, rows_c, c, elem, ctypes.byref(opts)) == capi.OK
+    return h
+
+
+def test_static_scratch_matches_caller_scratch_two_calls_in_a_row():
+    from bmmc_index_transforms_gb300 import _build, _capi as capi
+
+    _build.build()
+    L = capi.lib()
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    stream = torch.cuda.current_stream()
+    cases = [(22, 4, 0), (20, 16, 1)]  # 16 MiB and 16 MiB: both at the capacity limit
+    for n, elem, seed in cases:
+        rows, c, _ = synth.draw_bmmc(seed, n, lambda r: ref.f2_rank(n, r) == n, low_to_high=10)
+        plan = _two_factor_plan(L, capi, n, rows, c, elem)
+        nbytes = (1 << n) * elem
+        src = torch.from_numpy(synth.fill_int(n, elem).view(np.uint8).reshape(-1).copy()).cuda()
+        want = torch.zeros_like(src)
+        got = torch.full_like(src, 0xEE)
+        scratch = torch.empty_like(src)
+        try:
+            assert L.bmmc_permute_scratch(plan, src.data_ptr(), want.data_ptr(), scratch.data_ptr(),
+                                          stream.cuda_stream) == capi.OK
+            assert L.bmmc_permute_static_scratch(plan, src.data_ptr(), got.data_ptr(),
+                                                 stream.cuda_stream) == capi.OK
+            torch.cuda.synchronize()
+            assert got.numel() == nbytes
+            assert torch.equal(got, want), f"static-scratch output differs (n={n}, elem={elem})"
+        finally:
+            L.bmmc_plan_destroy(plan)
+
+
+def test_static_scratch_rejections():
+    from bmmc_index_transforms_gb300 import _build, _capi as capi
+
+    _build.build()
+    L = capi.lib()
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    # one element past the capacity: rejected before any work is enqueued
+    n = 23
+    rows, c, _ = synth.draw_bmmc(3, n, lambda r: ref.f2_rank(n, r) == n)
+    big = _two_factor_plan(L, capi, n, rows, c, 4)
+    try:
+        st = L.bmmc_permute_static_scratch(big, buf.data_ptr(), buf.data_ptr() + (32 << 20), None)
+        assert st == capi.ERR_TOO_LARGE
+        assert "static scratch" in L.bmmc_status_string(st).decode()
+    finally:
+        L.bmmc_plan_destroy(big)
+    # single-pass plans have nothing to stage: rejected
+    h = ctypes.c_void_p()
+    rows_c = (ctypes.c_uint64 * 12)(*ref.bitrev_rows(12))
+    assert L.bmmc_plan(ctypes.byref(h), 12, rows_c, 0, 4) == capi.OK
+    try:
+        st = L.bmmc_permute_static_scratch(h, buf.data_ptr(), buf.data_ptr() + (1 << 20), None)
+        assert st == capi.ERR_INVALID_ARG
+    finally:
+        L.bmmc_plan_destroy(h)
