@@ -364,7 +364,8 @@ def run_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": committed_traffic(),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "kernel": "bmmc_tiled_kernel<4,256,4>",
+                "kernel": "bmmc_tiled_kernel<elem=4, threads=%d, chunks_per_thread=%d>" % (
+                    plans[0].info["threads"], plans[0].info["chunks_per_thread"]),
                 "algorithmic_bytes_per_launch": int(alg_bytes)}
 
     cpu = None
@@ -374,7 +375,7 @@ def run_ours(args):
         threads = oracle.host_threads()
         gbs, dt, cnt = oracle_sample_gbs(24, 0, threads)
         # scale the sample so that it holds roughly 10-30 s of CPU work
-        target_cpu_s = 15.0
+        target_cpu_s = 20.0
         log2 = 24
         while dt * threads < target_cpu_s / 2 and log2 < 27:
             log2 += 1

@@ -1,13 +1,16 @@
 // Device kernels for BMMC permutations on GB300 (sm_103a) and their
 // launchers.
 //
-// bmmc_tiled_kernel is the single pass (any invertible A): each block walks
-// tiles b = blockIdx.x, blockIdx.x + gridDim.x, ... .  For one tile it
+// bmmc_tiled_kernel is the single pass (any invertible A).  Block k walks
+// tiles b = k, k + gridDim.x, ...; the default grid is 64 blocks per SM, so
+// with 32 KiB tiles most blocks handle one or two tiles (a flat, heavily
+// oversubscribed grid measured faster on GB300 than one resident wave).  For
+// one tile a block
 //   1. loads the tile's input runs with 16-byte vector loads (every warp
 //      reads whole aligned runs, so every 32-byte sector fetched is used),
 //   2. scatters the elements into shared memory through the planner's XOR
 //      layout (conflict-free),
-//   3. after a barrier, already issues the loads of its next tile, and
+//   3. after a barrier, already issues the loads of its next tile, if any,
 //   4. gathers each output vector from shared memory and writes it with one
 //      16-byte store, whole aligned output runs per warp.
 // The per-tile origins are linear in the tile index b; each lane of a warp
@@ -57,15 +60,36 @@ __device__ __forceinline__ uint64_t warp_xor64(uint64_t v) {
     return ((uint64_t)hi << 32) | lo;
 }
 
+template <typename OFF>
+__device__ __forceinline__ OFF warp_xor(OFF v);
+template <>
+__device__ __forceinline__ uint32_t warp_xor<uint32_t>(uint32_t v) {
+    return __reduce_xor_sync(0xffffffffu, v);
+}
+template <>
+__device__ __forceinline__ uint64_t warp_xor<uint64_t>(uint64_t v) {
+    return warp_xor64(v);
+}
+
+// An empty asm that makes the compiler treat v as unknown from here on, so
+// values derived from it are recomputed where they are used instead of being
+// hoisted out of the tile loop into registers.
+__device__ __forceinline__ void opaque(uint32_t& v) { asm volatile("" : "+r"(v)); }
+__device__ __forceinline__ void opaque(uint64_t& v) { asm volatile("" : "+l"(v)); }
+
 // Blocks per SM the register budget is sized for: enough 16-byte loads in
 // flight per SM to cover HBM latency, without spilling.
-template <int NT, int QPT>
+template <int NT, int QPT, bool WIDE>
 struct TiledMinBlocks {
-    static constexpr int value = NT < 256 ? 1 : QPT <= 1 ? 8 : 1;
+    static constexpr int value = NT < 256 ? 1
+                                 : WIDE ? (QPT <= 2 ? 6 : QPT == 4 ? 5 : QPT == 8 ? 3 : 2)
+                                        : (QPT <= 2 ? 8 : QPT == 4 ? 6 : QPT == 8 ? 4 : 2);
 };
 
-template <int ELEM, int NT, int QPT>
-__global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT>::value))
+// OFF is the type of byte offsets into the arrays: 32-bit when the array
+// is smaller than 4 GiB (fewer registers, one XOR per address), else 64-bit.
+template <int ELEM, int NT, int QPT, typename OFF>
+__global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)>::value))
     bmmc_tiled_kernel(const __grid_constant__ TiledParams p, const uint4* __restrict__ in,
                       uint4* __restrict__ out) {
     using T = typename ElemType<ELEM>::T;
@@ -85,13 +109,13 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT>::value))
     // from threadIdx), all as byte offsets; the iteration and element bits
     // come from the uniform tables.
     const uint32_t tau0 = tid << VB;
-    uint64_t in_t = 0, out_t = 0;
+    OFF in_t = 0, out_t = 0;
     uint32_t ph_t = 0, ga_t = 0;
 #pragma unroll 1
     for (int i = VB; i < D; ++i) {
         if ((tau0 >> i) & 1u) {
-            in_t ^= p.tau_in[i];
-            out_t ^= p.om_out[i];
+            in_t ^= (OFF)p.tau_in[i];
+            out_t ^= (OFF)p.om_out[i];
             ph_t ^= p.phi[i];
             ga_t ^= p.gam[i];
         }
@@ -100,9 +124,10 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT>::value))
     out_t <<= EB;
     ph_t <<= EB;
     ga_t <<= EB;
-    uint64_t my_cin = 0, my_cout = 0;
+    OFF my_cin = 0;
+    uint64_t my_cout = 0;
     if ((int)lane < p.n_block_bits) {
-        my_cin = p.col_in[lane] << EB;
+        my_cin = (OFF)(p.col_in[lane] << EB);
         my_cout = p.col_out[lane];
     }
     uint32_t my_gl = 0;
@@ -115,29 +140,29 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT>::value))
 
     // Byte origins of tile b: input origin ib, output run origin ob, and the
     // shared-memory offset g that realigns output run positions with the tile.
-    auto tile_bases = [&](uint64_t b, uint64_t& ib, uint64_t& ob, uint32_t& g) {
+    auto tile_bases = [&](uint64_t b, OFF& ib, OFF& ob, uint32_t& g) {
         const bool bit = (b >> lane) & 1ull;
-        ib = warp_xor64(bit ? my_cin : 0ull);
+        ib = warp_xor<OFF>(bit ? my_cin : (OFF)0);
         const uint64_t raw = warp_xor64(bit ? my_cout : 0ull) ^ p.c;
-        ob = (raw & ~lowm) << EB;
+        ob = (OFF)((raw & ~lowm) << EB);
         const uint32_t delta = (uint32_t)(raw & lowm);
         g = __reduce_xor_sync(0xffffffffu, ((delta >> lane) & 1u) ? my_gl : 0u);
     };
     // The thread's own offsets are passed through an empty asm each tile so
     // the compiler recomputes the per-chunk addresses (one XOR each) instead of
     // holding dozens of loop-invariant addresses in registers.
-    auto load_tile = [&](uint64_t ib, uint4 (&r)[QPT]) {
-        uint64_t it = in_t ^ ib;
-        asm volatile("" : "+l"(it));
+    auto load_tile = [&](OFF ib, uint4 (&r)[QPT]) {
+        OFF it = in_t ^ ib;
+        opaque(it);
 #pragma unroll
         for (int i = 0; i < QPT; ++i)
-            if (act[i]) r[i] = ld_stream(reinterpret_cast<const uint4*>(src + (it ^ p.it_in[i])));
+            if (act[i]) r[i] = ld_stream(reinterpret_cast<const uint4*>(src + (it ^ (OFF)p.it_in[i])));
     };
 
     const uint64_t nt = p.n_tiles;
     uint64_t b = blockIdx.x;
     uint4 r[QPT];
-    uint64_t ib = 0, ob = 0;
+    OFF ib = 0, ob = 0;
     uint32_t g = 0;
     if (b < nt) {
         tile_bases(b, ib, ob, g);
@@ -151,28 +176,32 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT>::value))
             if (!act[i]) continue;
             T e[VEC];
             memcpy(e, &r[i], 16);
+            uint32_t pi = ph;
+            opaque(pi);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) *reinterpret_cast<T*>(tile + (ph ^ p.st_slot[i * VEC + j])) = e[j];
+            for (int j = 0; j < VEC; ++j) *reinterpret_cast<T*>(tile + (pi ^ p.st_slot[i * VEC + j])) = e[j];
         }
         __syncthreads();
-        const uint64_t cur_ob = ob;
+        const OFF cur_ob = ob;
         const uint32_t ga = ga_t ^ g;
         const uint64_t nb = b + gridDim.x;
         if (nb < nt) {
             tile_bases(nb, ib, ob, g);
             load_tile(ib, r);
         }
-        uint64_t ot = out_t ^ cur_ob;
-        asm volatile("" : "+l"(ot));
+        OFF ot = out_t ^ cur_ob;
+        opaque(ot);
 #pragma unroll
         for (int i = 0; i < QPT; ++i) {
             if (!act[i]) continue;
             T e[VEC];
+            uint32_t gi = ga;
+            opaque(gi);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) e[j] = *reinterpret_cast<const T*>(tile + (ga ^ p.ld_slot[i * VEC + j]));
+            for (int j = 0; j < VEC; ++j) e[j] = *reinterpret_cast<const T*>(tile + (gi ^ p.ld_slot[i * VEC + j]));
             uint4 v;
             memcpy(&v, e, 16);
-            st_stream(reinterpret_cast<uint4*>(dst + (ot ^ p.it_out[i])), v);
+            st_stream(reinterpret_cast<uint4*>(dst + (ot ^ (OFF)p.it_out[i])), v);
         }
         __syncthreads();
     }
@@ -194,20 +223,21 @@ __global__ void __launch_bounds__(32)
     }
 }
 
-// Plain copy: U independent 16-byte vectors in flight per thread.
+// Plain copy: each block moves 256 * U 16-byte vectors once and exits.  A
+// flat grid of short blocks (rather than one resident wave striding over the
+// array) measured fastest on GB300: block scheduling keeps every SM's memory
+// pipeline full to the end without synchronised strides.
 template <int U>
 __global__ void __launch_bounds__(256)
     bmmc_copy_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, uint64_t nvec) {
-    const uint64_t stride = (uint64_t)gridDim.x * 256u * U;
-    for (uint64_t base = (uint64_t)blockIdx.x * 256u * U + threadIdx.x; base < nvec; base += stride) {
-        uint4 v[U];
+    const uint64_t base = (uint64_t)blockIdx.x * 256u * U + threadIdx.x;
+    uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (base + (uint64_t)u * 256u < nvec) v[u] = ld_stream(in + base + (uint64_t)u * 256u);
+    for (int u = 0; u < U; ++u)
+        if (base + (uint64_t)u * 256u < nvec) v[u] = ld_stream(in + base + (uint64_t)u * 256u);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (base + (uint64_t)u * 256u < nvec) st_stream(out + base + (uint64_t)u * 256u, v[u]);
-    }
+    for (int u = 0; u < U; ++u)
+        if (base + (uint64_t)u * 256u < nvec) st_stream(out + base + (uint64_t)u * 256u, v[u]);
 }
 
 __global__ void bmmc_copy_tail_kernel(const unsigned char* __restrict__ in,
@@ -221,28 +251,28 @@ __global__ void bmmc_copy_tail_kernel(const unsigned char* __restrict__ in,
 
 using TiledFn = void (*)(const TiledParams, const uint4*, uint4*);
 
-template <int ELEM>
+template <int ELEM, typename OFF>
 static TiledFn pick_tiled(int nt, int qpt) {
-    if (nt == 32) return bmmc_tiled_kernel<ELEM, 32, 1>;
-    if (nt == 64) return bmmc_tiled_kernel<ELEM, 64, 1>;
-    if (nt == 128) return bmmc_tiled_kernel<ELEM, 128, 1>;
+    if (nt == 32) return bmmc_tiled_kernel<ELEM, 32, 1, OFF>;
+    if (nt == 64) return bmmc_tiled_kernel<ELEM, 64, 1, OFF>;
+    if (nt == 128) return bmmc_tiled_kernel<ELEM, 128, 1, OFF>;
     if (nt == 256) {
         switch (qpt) {
-            case 1: return bmmc_tiled_kernel<ELEM, 256, 1>;
-            case 2: return bmmc_tiled_kernel<ELEM, 256, 2>;
-            case 4: return bmmc_tiled_kernel<ELEM, 256, 4>;
-            case 8: return bmmc_tiled_kernel<ELEM, 256, 8>;
-            case 16: return bmmc_tiled_kernel<ELEM, 256, 16>;
+            case 1: return bmmc_tiled_kernel<ELEM, 256, 1, OFF>;
+            case 2: return bmmc_tiled_kernel<ELEM, 256, 2, OFF>;
+            case 4: return bmmc_tiled_kernel<ELEM, 256, 4, OFF>;
+            case 8: return bmmc_tiled_kernel<ELEM, 256, 8, OFF>;
+            case 16: return bmmc_tiled_kernel<ELEM, 256, 16, OFF>;
         }
     }
     return nullptr;
 }
 
-static TiledFn tiled_fn(int elem, int nt, int qpt) {
+static TiledFn tiled_fn(int elem, int nt, int qpt, bool wide) {
     switch (elem) {
-        case 4: return pick_tiled<4>(nt, qpt);
-        case 8: return pick_tiled<8>(nt, qpt);
-        case 16: return pick_tiled<16>(nt, qpt);
+        case 4: return wide ? pick_tiled<4, uint64_t>(nt, qpt) : pick_tiled<4, uint32_t>(nt, qpt);
+        case 8: return wide ? pick_tiled<8, uint64_t>(nt, qpt) : pick_tiled<8, uint32_t>(nt, qpt);
+        case 16: return wide ? pick_tiled<16, uint64_t>(nt, qpt) : pick_tiled<16, uint32_t>(nt, qpt);
     }
     return nullptr;
 }
@@ -294,7 +324,8 @@ static cudaError_t blocks_per_sm(int dev, const void* fn, int threads, int smem,
 
 cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStream_t stream,
                          int grid_override) {
-    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt);
+    const bool wide = ((uint64_t)P.elem << P.n) > 0xFFFFFFFFull;
+    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide);
     if (!fn) return cudaErrorInvalidConfiguration;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -302,7 +333,11 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
     int sms = 0, per = 0;
     if ((e = sm_count(dev, &sms)) != cudaSuccess) return e;
     if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
-    uint64_t grid = (uint64_t)sms * (uint64_t)per;
+    // Default grid: 64 blocks per SM (several times the resident limit), each
+    // block walking tiles blockIdx.x, blockIdx.x + grid, ...; oversubscribing
+    // the SMs measured faster than one resident wave on GB300.
+    (void)per;
+    uint64_t grid = (uint64_t)sms * 64u;
     if (grid_override > 0) grid = (uint64_t)grid_override;
     if (grid > P.tiles) grid = P.tiles;
     fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(P.tp, static_cast<const uint4*>(in),
@@ -322,22 +357,15 @@ cudaError_t launch_naive(const PassPlan& P, const void* in, void* out, cudaStrea
 }
 
 cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t stream) {
-    constexpr int U = 4;
+    constexpr int U = 2;
     const uint64_t nvec = bytes / 16;
     if (nvec) {
-        auto fn = bmmc_copy_kernel<U>;
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+        const uint64_t grid = (nvec + 256u * U - 1) / (256u * U);
+        if (grid > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+        bmmc_copy_kernel<U><<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint4*>(in),
+                                                                static_cast<uint4*>(out), nvec);
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        int sms = 0, per = 0;
-        if ((e = sm_count(dev, &sms)) != cudaSuccess) return e;
-        if ((e = blocks_per_sm(dev, (const void*)fn, 256, 0, &per)) != cudaSuccess) return e;
-        uint64_t need = (nvec + 256u * U - 1) / (256u * U);
-        uint64_t grid = (uint64_t)sms * per;
-        if (grid > need) grid = need;
-        fn<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out),
-                                                nvec);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const uint64_t tail = bytes - nvec * 16;
     if (tail) {
@@ -352,7 +380,7 @@ cudaError_t launch_pass(const PassPlan& P, const void* in, void* out, cudaStream
     switch (P.kernel) {
         case KERNEL_COPY: return launch_copy(in, out, ((size_t)1 << P.n) * P.elem, stream);
         case KERNEL_NAIVE: return launch_naive(P, in, out, stream);
-        case KERNEL_TILED: return launch_tiled(P, in, out, stream, 0);
+        case KERNEL_TILED: return launch_tiled(P, in, out, stream, P.grid_blocks);
     }
     return cudaErrorInvalidValue;
 }

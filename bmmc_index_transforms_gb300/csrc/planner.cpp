@@ -45,7 +45,7 @@ static int ilog2(int x) {
 }
 
 int default_run_bits(int elem) { return ilog2(256 / elem); }      // 256-byte runs
-int default_tile_bits(int elem) { return std::max(2 * default_run_bits(elem), ilog2(16384 / elem)); }
+int default_tile_bits(int elem) { return std::max(2 * default_run_bits(elem), ilog2(32768 / elem)); }  // 32 KiB tiles
 
 int classify(int n, const uint64_t* rows, uint64_t c) {
     bool ident = true, perm = true;
@@ -320,6 +320,7 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     }
 
     P.kernel = KERNEL_TILED;
+    P.grid_blocks = req.grid_blocks;
     P.threads = NT;
     P.qpt = qpt;
     P.smem_bytes = (int)((1ull << D) * elem);

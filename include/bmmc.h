@@ -87,6 +87,9 @@ typedef struct {
     int alloc_scratch;   /* TWO_FACTOR only: 1 = the plan owns a device scratch buffer
                             of 2^n * elem_size bytes, allocated by bmmc_plan_ex on the
                             current device and freed by bmmc_plan_destroy */
+    int grid_blocks;     /* blocks launched by the tiled kernel; each walks tiles
+                            blockIdx.x, blockIdx.x + grid, ...; 0 = default, capped at
+                            the number of tiles */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;

@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _two_factor_plan(L, capi, n, rows, c, elem):
-    opts = capi.PlanOpts(capi.MODE_TWO_FACTOR, 0, 0, 0, 0)
+    opts = capi.PlanOpts(capi.MODE_TWO_FACTOR, 0, 0, 0, 0, 0)
     h = ctypes.c_void_p()
     rows_c = (ctypes.c_uint64 * n)(*rows)
     assert L.bmmc_plan_ex(ctypes.byref(h), n, rows_c, c, elem, ctypes.byref(opts)) == capi.OK
