@@ -51,7 +51,7 @@ class PlanInfo(ctypes.Structure):
                 ("r2_factors", ctypes.c_int), ("kernel", ctypes.c_int), ("threads", ctypes.c_int),
                 ("chunks_per_thread", ctypes.c_int), ("tiles", ctypes.c_uint64),
                 ("smem_bytes", ctypes.c_int), ("bank_conflicts", ctypes.c_int),
-                ("c", ctypes.c_uint64)]
+                ("c", ctypes.c_uint64), ("vector_stores", ctypes.c_int)]
 
 
 # name -> (restype, argtypes); every function declared in include/bmmc.h

@@ -210,6 +210,7 @@ bmmc_status bmmc_plan_info(bmmc_plan_t plan, bmmc_plan_info_t* info) {
     if (plan->mode == BMMC_MODE_TWO_FACTOR)
         info->bank_conflicts += plan->first_pass.bank_conflicts + plan->second_pass.bank_conflicts;
     info->c = plan->c;
+    info->vector_stores = m.vector_scatter ? 1 : 0;
     return BMMC_OK;
 }
 

@@ -9,6 +9,7 @@ namespace bmmc {
 constexpr int kMaxN = 40;       // largest supported n (array of 2^n elements)
 constexpr int kMaxTileBits = 15;  // largest tile: 2^15 elements
 constexpr int kMaxQpt = 16;     // 16-byte chunks per thread per tile
+constexpr int kMaxThreadBits = 8; // up to 256 threads per block
 constexpr int kMaxBlockBits = 32; // tile-index bits, one per lane of a warp
 
 // Tiled single-pass kernel.  Notation (all vectors are element indices seen
@@ -24,14 +25,19 @@ struct TiledParams {
     uint64_t n_tiles;           // 2^(n - tile_bits)
     uint64_t col_in[kMaxBlockBits];   // e_{C_i}: input origin of block bit i
     uint64_t col_out[kMaxBlockBits];  // A e_{C_i}: output origin of block bit i
-    uint64_t tau_in[kMaxTileBits];    // input element offset of tile-coordinate bit i
-    uint64_t om_out[kMaxTileBits];    // output element offset of output-coordinate bit i
-    uint32_t phi[kMaxTileBits];       // shared-memory slot of tile-coordinate bit i
-    uint32_t gam[kMaxTileBits];       // shared-memory slot read for output-coordinate bit i
+    // Per thread-index bit k (threadIdx.x bit k), the byte offsets that bit
+    // contributes: to the input chunk, to the shared-memory slot it stores,
+    // to the output chunk, and to the shared-memory slot gathered for it.
+    uint64_t tid_in[8];
+    uint64_t tid_out[8];
+    uint32_t tid_phi[8];
+    uint32_t tid_gam[8];
+    uint32_t gam[kMaxTileBits];       // shared-memory slot (elements) gathered for output-run bit j
     uint64_t it_in[kMaxQpt];          // input BYTE offset of the i-th chunk of a thread
     uint64_t it_out[kMaxQpt];         // output BYTE offset of the i-th chunk
     uint32_t st_slot[kMaxQpt * 4];    // shared-memory BYTE offset of element j of input chunk i
-                                      //   (index i * VEC + j), before the thread's own part
+                                      //   (index i * VEC + j), before the thread's own part;
+                                      //   with vector stores only j = 0 (the chunk base) is used
     uint32_t ld_slot[kMaxQpt * 4];    // shared-memory BYTE offset of element j of output chunk i
     uint32_t chunks;                  // 16-byte chunks per tile
     int32_t tile_bits;                // D: log2 elements per tile

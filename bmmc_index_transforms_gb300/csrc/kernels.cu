@@ -2,10 +2,9 @@
 // launchers.
 //
 // bmmc_tiled_kernel is the single pass (any invertible A).  Block k walks
-// tiles b = k, k + gridDim.x, ...; the default grid is 64 blocks per SM, so
-// with 32 KiB tiles most blocks handle one or two tiles (a flat, heavily
-// oversubscribed grid measured faster on GB300 than one resident wave).  For
-// one tile a block
+// tiles b = k, k + gridDim.x, ...; by default the 32 KiB tiles get one block
+// each (a flat grid of short blocks measured faster on GB300 than one
+// resident wave of persistent blocks).  For one tile a block
 //   1. loads the tile's input runs with 16-byte vector loads (every warp
 //      reads whole aligned runs, so every 32-byte sector fetched is used),
 //   2. scatters the elements into shared memory through the planner's XOR
@@ -88,13 +87,14 @@ struct TiledMinBlocks {
 
 // OFF is the type of byte offsets into the arrays: 32-bit when the array
 // is smaller than 4 GiB (fewer registers, one XOR per address), else 64-bit.
-template <int ELEM, int NT, int QPT, typename OFF>
+// VS: the planner's layout keeps each input vector whole in shared memory,
+// so it is stored with one 16-byte store instead of one store per element.
+template <int ELEM, int NT, int QPT, typename OFF, bool VS>
 __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)>::value))
     bmmc_tiled_kernel(const __grid_constant__ TiledParams p, const uint4* __restrict__ in,
                       uint4* __restrict__ out) {
     using T = typename ElemType<ELEM>::T;
     constexpr int VEC = 16 / ELEM;
-    constexpr int VB = VEC == 4 ? 2 : VEC == 2 ? 1 : 0;
     constexpr int EB = ELEM == 4 ? 2 : ELEM == 8 ? 3 : 4;
     extern __shared__ uint4 smem_raw[];
     unsigned char* tile = reinterpret_cast<unsigned char*>(smem_raw);
@@ -103,27 +103,21 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
 
     const uint32_t tid = threadIdx.x;
     const uint32_t lane = tid & 31u;
-    const int D = p.tile_bits;
 
-    // Linear parts owned by this thread (the bits of its chunk index that come
-    // from threadIdx), all as byte offsets; the iteration and element bits
-    // come from the uniform tables.
-    const uint32_t tau0 = tid << VB;
+    // Offsets owned by this thread (the bits of its chunk index that come
+    // from threadIdx.x), all in bytes; the iteration and element bits come
+    // from the uniform tables.
     OFF in_t = 0, out_t = 0;
     uint32_t ph_t = 0, ga_t = 0;
-#pragma unroll 1
-    for (int i = VB; i < D; ++i) {
-        if ((tau0 >> i) & 1u) {
-            in_t ^= (OFF)p.tau_in[i];
-            out_t ^= (OFF)p.om_out[i];
-            ph_t ^= p.phi[i];
-            ga_t ^= p.gam[i];
+#pragma unroll
+    for (int k = 0; k < kMaxThreadBits; ++k) {
+        if ((1 << k) < NT && ((tid >> k) & 1u)) {
+            in_t ^= (OFF)p.tid_in[k];
+            out_t ^= (OFF)p.tid_out[k];
+            ph_t ^= p.tid_phi[k];
+            ga_t ^= p.tid_gam[k];
         }
     }
-    in_t <<= EB;
-    out_t <<= EB;
-    ph_t <<= EB;
-    ga_t <<= EB;
     OFF my_cin = 0;
     uint64_t my_cout = 0;
     if ((int)lane < p.n_block_bits) {
@@ -174,12 +168,16 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
 #pragma unroll
         for (int i = 0; i < QPT; ++i) {
             if (!act[i]) continue;
-            T e[VEC];
-            memcpy(e, &r[i], 16);
             uint32_t pi = ph;
             opaque(pi);
+            if (VS) {
+                *reinterpret_cast<uint4*>(tile + (pi ^ p.st_slot[i * VEC])) = r[i];
+            } else {
+                T e[VEC];
+                memcpy(e, &r[i], 16);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) *reinterpret_cast<T*>(tile + (pi ^ p.st_slot[i * VEC + j])) = e[j];
+                for (int j = 0; j < VEC; ++j) *reinterpret_cast<T*>(tile + (pi ^ p.st_slot[i * VEC + j])) = e[j];
+            }
         }
         __syncthreads();
         const OFF cur_ob = ob;
@@ -251,28 +249,34 @@ __global__ void bmmc_copy_tail_kernel(const unsigned char* __restrict__ in,
 
 using TiledFn = void (*)(const TiledParams, const uint4*, uint4*);
 
-template <int ELEM, typename OFF>
+template <int ELEM, typename OFF, bool VS>
 static TiledFn pick_tiled(int nt, int qpt) {
-    if (nt == 32) return bmmc_tiled_kernel<ELEM, 32, 1, OFF>;
-    if (nt == 64) return bmmc_tiled_kernel<ELEM, 64, 1, OFF>;
-    if (nt == 128) return bmmc_tiled_kernel<ELEM, 128, 1, OFF>;
+    if (nt == 32) return bmmc_tiled_kernel<ELEM, 32, 1, OFF, VS>;
+    if (nt == 64) return bmmc_tiled_kernel<ELEM, 64, 1, OFF, VS>;
+    if (nt == 128) return bmmc_tiled_kernel<ELEM, 128, 1, OFF, VS>;
     if (nt == 256) {
         switch (qpt) {
-            case 1: return bmmc_tiled_kernel<ELEM, 256, 1, OFF>;
-            case 2: return bmmc_tiled_kernel<ELEM, 256, 2, OFF>;
-            case 4: return bmmc_tiled_kernel<ELEM, 256, 4, OFF>;
-            case 8: return bmmc_tiled_kernel<ELEM, 256, 8, OFF>;
-            case 16: return bmmc_tiled_kernel<ELEM, 256, 16, OFF>;
+            case 1: return bmmc_tiled_kernel<ELEM, 256, 1, OFF, VS>;
+            case 2: return bmmc_tiled_kernel<ELEM, 256, 2, OFF, VS>;
+            case 4: return bmmc_tiled_kernel<ELEM, 256, 4, OFF, VS>;
+            case 8: return bmmc_tiled_kernel<ELEM, 256, 8, OFF, VS>;
+            case 16: return bmmc_tiled_kernel<ELEM, 256, 16, OFF, VS>;
         }
     }
     return nullptr;
 }
 
-static TiledFn tiled_fn(int elem, int nt, int qpt, bool wide) {
+template <int ELEM, bool VS>
+static TiledFn pick_width(int nt, int qpt, bool wide) {
+    return wide ? pick_tiled<ELEM, uint64_t, VS>(nt, qpt) : pick_tiled<ELEM, uint32_t, VS>(nt, qpt);
+}
+
+// 16-byte elements are always stored whole (one element per vector).
+static TiledFn tiled_fn(int elem, int nt, int qpt, bool wide, bool vs) {
     switch (elem) {
-        case 4: return wide ? pick_tiled<4, uint64_t>(nt, qpt) : pick_tiled<4, uint32_t>(nt, qpt);
-        case 8: return wide ? pick_tiled<8, uint64_t>(nt, qpt) : pick_tiled<8, uint32_t>(nt, qpt);
-        case 16: return wide ? pick_tiled<16, uint64_t>(nt, qpt) : pick_tiled<16, uint32_t>(nt, qpt);
+        case 4: return vs ? pick_width<4, true>(nt, qpt, wide) : pick_width<4, false>(nt, qpt, wide);
+        case 8: return vs ? pick_width<8, true>(nt, qpt, wide) : pick_width<8, false>(nt, qpt, wide);
+        case 16: return pick_width<16, true>(nt, qpt, wide);
     }
     return nullptr;
 }
@@ -325,7 +329,7 @@ static cudaError_t blocks_per_sm(int dev, const void* fn, int threads, int smem,
 cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStream_t stream,
                          int grid_override) {
     const bool wide = ((uint64_t)P.elem << P.n) > 0xFFFFFFFFull;
-    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide);
+    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide, P.vector_scatter);
     if (!fn) return cudaErrorInvalidConfiguration;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -333,11 +337,13 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
     int sms = 0, per = 0;
     if ((e = sm_count(dev, &sms)) != cudaSuccess) return e;
     if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
-    // Default grid: 64 blocks per SM (several times the resident limit), each
-    // block walking tiles blockIdx.x, blockIdx.x + grid, ...; oversubscribing
-    // the SMs measured faster than one resident wave on GB300.
+    // Default grid: one block per tile for tiles of 8 chunks per thread or
+    // more, else 64 blocks per SM, each block walking tiles blockIdx.x,
+    // blockIdx.x + grid, ...; on GB300 these flat, oversubscribed grids
+    // measured faster than one resident wave of persistent blocks.
     (void)per;
-    uint64_t grid = (uint64_t)sms * 64u;
+    uint64_t grid = P.qpt >= 8 ? P.tiles : (uint64_t)sms * 64u;
+    if (grid > 0x7FFFFFFFull) grid = 0x7FFFFFFFull;
     if (grid_override > 0) grid = (uint64_t)grid_override;
     if (grid > P.tiles) grid = P.tiles;
     fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(P.tp, static_cast<const uint4*>(in),

@@ -144,6 +144,113 @@ static int count_conflicts(const std::vector<uint32_t>& slots, int elem) {
     return extra;
 }
 
+// A shared-memory layout candidate: the slot image of every tile-coordinate
+// bit, the output bit assigned to every bit of a thread's linear chunk index
+// (lanes first), and whether input vectors are stored whole.
+struct LayoutChoice {
+    bool vector_scatter = false;
+    std::vector<int> opos;
+    std::vector<uint64_t> phiu;
+    int conflicts = -1;
+    bool valid() const { return conflicts >= 0; }
+};
+
+// Vector layout slot map: the vb element bits stay in place and the chunk
+// bits go through psi, a bijection chosen so that (a) the 8 lanes of a
+// 16-byte store wavefront (chunk bits 0..2) land in distinct bank groups and
+// (b) the bw gather lanes (output bits opos[0..bw-1]) reach bw independent
+// bank bits: their sources must span the vb element bits (checked here), and
+// psi must be injective on the chunk parts of the lane combinations whose
+// element bits cancel (a common complement again).
+static bool vector_layout(int D, int vb, int bw, const std::vector<uint64_t>& lam,
+                          const std::vector<int>& opos, std::vector<uint64_t>* phiu) {
+    const uint64_t lo_mask = (1ull << vb) - 1;
+    std::vector<uint64_t> V;
+    for (int k = 0; k < bw; ++k) V.push_back(lam[opos[k]]);
+    // Split V into vectors with independent element parts and the rest
+    // reduced to zero element part.
+    std::vector<uint64_t> piv, zero;
+    for (uint64_t v : V) {
+        uint64_t x = v;
+        for (uint64_t p : piv)
+            if ((x & lo_mask) >> highbit(p & lo_mask) & 1ull) x ^= p;
+        if (x & lo_mask) {
+            for (uint64_t& p : piv)
+                if ((p & lo_mask) >> highbit(x & lo_mask) & 1ull) p ^= x;
+            piv.push_back(x);
+        } else {
+            zero.push_back(x >> vb);
+        }
+    }
+    if ((int)piv.size() != vb) return false;  // sources do not cover the element bits
+    const int cdim = D - vb;
+    std::vector<uint64_t> U = {1, 2, 4};
+    if ((int)zero.size() != 3 || cdim < 3) return false;
+    std::vector<uint64_t> K;
+    if (!common_complement(cdim, U, zero, &K)) return false;
+    std::vector<uint64_t> Bc(U);
+    Bc.insert(Bc.end(), K.begin(), K.end());
+    phiu->assign(D, 0);
+    for (int i = 0; i < vb; ++i) (*phiu)[i] = 1ull << i;
+    for (int i = vb; i < D; ++i) {
+        uint64_t a;
+        if (!coords_in(Bc.data(), cdim, 1ull << (i - vb), &a)) return false;
+        (*phiu)[i] = a << vb;
+    }
+    return true;
+}
+
+// Extra shared-memory wavefronts of one tile for a layout, simulating every
+// store and gather instruction of every warp: 16-byte accesses go 8 lanes
+// per wavefront (bank group = slot / (16 / elem) mod 8), elem-byte accesses
+// 128 / elem lanes per wavefront (bank = slot mod 128 / elem).
+static int simulate(int elem, int vb, int NT, int qpt, uint32_t chunks, const std::vector<uint64_t>& lam,
+                    const LayoutChoice& ch) {
+    const int vec = 1 << vb;
+    auto lin = [](const std::vector<uint64_t>& img, uint64_t v) {
+        uint64_t o = 0;
+        for (int i = 0; v; ++i, v >>= 1)
+            if (v & 1ull) o ^= img[i];
+        return o;
+    };
+    std::vector<uint64_t> gamu(lam.size());
+    for (size_t i = 0; i < lam.size(); ++i) gamu[i] = lin(ch.phiu, lam[i]);
+    auto omega_of = [&](uint64_t q) {
+        uint64_t o = 0;
+        for (int k = 0; q; ++k, q >>= 1)
+            if (q & 1ull) o |= 1ull << ch.opos[k];
+        return o;
+    };
+    // Every warp and every chunk iteration sees the warp-0, iteration-0
+    // pattern XORed with one constant (the maps are linear and the lane bits
+    // are disjoint from the others), which permutes banks without changing
+    // how many lanes share one; so one instruction of each kind is simulated
+    // and scaled.
+    std::vector<uint64_t> qs;
+    for (int lane = 0; lane < 32; ++lane)
+        if ((uint64_t)lane < chunks) qs.push_back((uint64_t)lane);
+    int extra = 0;
+    if (ch.vector_scatter) {
+        std::vector<uint32_t> sl;
+        for (uint64_t q : qs) sl.push_back((uint32_t)(lin(ch.phiu, q << vb) >> vb));
+        extra += count_conflicts(sl, 16);
+    } else {
+        for (int j = 0; j < vec; ++j) {
+            std::vector<uint32_t> sl;
+            for (uint64_t q : qs) sl.push_back((uint32_t)lin(ch.phiu, (q << vb) | (uint64_t)j));
+            extra += count_conflicts(sl, elem);
+        }
+    }
+    for (int j = 0; j < vec; ++j) {
+        std::vector<uint32_t> sl;
+        for (uint64_t q : qs) sl.push_back((uint32_t)lin(gamu, omega_of(q) ^ (uint64_t)j));
+        extra += count_conflicts(sl, elem);
+    }
+    const int instances = (int)std::min<uint64_t>((uint64_t)(NT / 32) * qpt, (chunks + 31) / 32);
+    extra *= instances;
+    return extra;
+}
+
 bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t c, int elem,
                       const PlanRequest& req, PassPlan* out) {
     PassPlan P;
@@ -216,18 +323,94 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
         lam[j] = a;
     }
 
-    // Lane subspaces of one wavefront: tau / om bits vb .. vb+m-1.
-    const int m = std::min(bw, D - vb);
-    std::vector<uint64_t> Rl, Wl;
-    for (int i = 0; i < m; ++i) {
-        Rl.push_back(1ull << (vb + i));
-        Wl.push_back(lam[vb + i]);
+    // Thread shape: 256 threads unless the tile has fewer 16-byte chunks.
+    const uint32_t chunks = (uint32_t)((1ull << D) / vec);
+    int NT = 256;
+    while (NT > 32 && (uint32_t)NT > chunks) NT >>= 1;
+    const int qpt = (int)std::max<uint32_t>(1, chunks / NT);
+    if (qpt > kMaxQpt) return BMMC_ERR_INVALID_ARG;
+    const int tbits = ilog2(NT);      // thread-index bits
+    const int cb = D - vb;            // chunk-index bits
+    const int eb = ilog2(elem);       // byte shift of one element
+
+    LayoutChoice best;
+    // Vector layout: each input vector stays whole in shared memory (one
+    // 16-byte store); the gather lanes are chosen among the output bits so
+    // that their sources cover every bank.
+    if (elem < 16 && cb >= bw) {
+        const int extra = bw - 3;  // gather lane bits beyond the three that keep 128-byte store segments
+        std::vector<int> cand;
+        for (int w = vb + 3; w < D; ++w) cand.push_back(w);
+        std::vector<int> pick(extra);
+        bool found = false;
+        // enumerate subsets of size `extra` of cand (extra <= 2)
+        auto try_set = [&](const std::vector<int>& S) {
+            std::vector<int> opos = {vb, vb + 1, vb + 2};
+            for (int w : S) opos.push_back(w);
+            for (int w = vb; w < D; ++w)
+                if (std::find(opos.begin(), opos.end(), w) == opos.end()) opos.push_back(w);
+            std::vector<uint64_t> phiu;
+            if (!vector_layout(D, vb, bw, lam, opos, &phiu)) return false;
+            LayoutChoice ch;
+            ch.vector_scatter = true;
+            ch.opos = opos;
+            ch.phiu = phiu;
+            ch.conflicts = simulate(elem, vb, NT, qpt, chunks, lam, ch);
+            if (ch.conflicts == 0) {
+                best = ch;
+                return true;
+            }
+            return false;
+        };
+        if (extra == 1) {
+            for (size_t a = 0; a < cand.size() && !found; ++a) found = try_set({cand[a]});
+        } else if (extra == 2) {
+            for (size_t a = 0; a < cand.size() && !found; ++a)
+                for (size_t b2 = a + 1; b2 < cand.size() && !found; ++b2) found = try_set({cand[a], cand[b2]});
+        }
     }
-    std::vector<uint64_t> K;
-    if (!common_complement(D, Rl, Wl, &K)) return BMMC_ERR_INTERNAL;
-    std::vector<uint64_t> B(Rl);
-    B.insert(B.end(), K.begin(), K.end());
-    auto phi = [&](uint64_t tau, uint64_t* slot) { return coords_in(B.data(), D, tau, slot); };
+    if (!best.valid()) {
+        // Scalar layout: per-element stores through a slot map that is
+        // conflict-free on both phases for the natural lane order.
+        std::vector<int> opos;
+        for (int w = vb; w < D; ++w) opos.push_back(w);
+        const int m = std::min(bw, D - vb);
+        std::vector<uint64_t> Rl, Wl;
+        for (int i = 0; i < m; ++i) {
+            Rl.push_back(1ull << (vb + i));
+            Wl.push_back(lam[vb + i]);
+        }
+        std::vector<uint64_t> K;
+        if (!common_complement(D, Rl, Wl, &K)) return BMMC_ERR_INTERNAL;
+        std::vector<uint64_t> B(Rl);
+        B.insert(B.end(), K.begin(), K.end());
+        LayoutChoice ch;
+        ch.vector_scatter = elem == 16;
+        ch.opos = opos;
+        ch.phiu.resize(D);
+        for (int i = 0; i < D; ++i)
+            if (!coords_in(B.data(), D, 1ull << i, &ch.phiu[i])) return BMMC_ERR_INTERNAL;
+        ch.conflicts = simulate(elem, vb, NT, qpt, chunks, lam, ch);
+        best = ch;
+    }
+
+    // Linear maps of the chosen layout.
+    auto lin = [&](const std::vector<uint64_t>& img, uint64_t v) {
+        uint64_t o = 0;
+        for (int i = 0; v; ++i, v >>= 1)
+            if (v & 1ull) o ^= img[i];
+        return o;
+    };
+    std::vector<uint64_t> tau_in(tb), om_out(D), gamu(D);
+    for (int i = 0; i < D; ++i) om_out[i] = i < t_out ? (1ull << i) : Ws[i - t_out];
+    for (int i = 0; i < D; ++i) gamu[i] = lin(best.phiu, lam[i]);
+    // output coordinate of linear chunk index q: chunk bit k -> omega bit opos[k]
+    auto omega_of = [&](uint64_t q) {
+        uint64_t o = 0;
+        for (int k = 0; q; ++k, q >>= 1)
+            if (q & 1ull) o |= 1ull << best.opos[k];
+        return o;
+    };
 
     TiledParams& tp = P.tp;
     std::memset(&tp, 0, sizeof tp);
@@ -236,98 +419,48 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     tp.n_block_bits = n - D;
     tp.t_out = t_out;
     tp.n_tiles = 1ull << (n - D);
+    tp.chunks = chunks;
     for (size_t i = 0; i < C.size(); ++i) {
         tp.col_in[i] = 1ull << C[i];
         tp.col_out[i] = matvec_rows(n, rows, 1ull << C[i]);
     }
-    std::vector<uint32_t> phi_bit(D), gam_bit(D);
-    for (int i = 0; i < D; ++i) {
-        tp.tau_in[i] = tb[i];
-        tp.om_out[i] = i < t_out ? (1ull << i) : Ws[i - t_out];
-        uint64_t s;
-        if (!phi(1ull << i, &s)) return BMMC_ERR_INTERNAL;
-        phi_bit[i] = (uint32_t)s;
-        if (!phi(lam[i], &s)) return BMMC_ERR_INTERNAL;
-        gam_bit[i] = (uint32_t)s;
-        tp.phi[i] = phi_bit[i];
-        tp.gam[i] = gam_bit[i];
+    for (int j = 0; j < D; ++j) tp.gam[j] = (uint32_t)gamu[j];
+    for (int k = 0; k < tbits && k < cb; ++k) {
+        const uint64_t tin = 1ull << (vb + k);
+        const uint64_t tout = omega_of(1ull << k);
+        tp.tid_in[k] = lin(tau_in, tin) << eb;
+        tp.tid_phi[k] = (uint32_t)(lin(best.phiu, tin) << eb);
+        tp.tid_out[k] = lin(om_out, tout) << eb;
+        tp.tid_gam[k] = (uint32_t)(lin(gamu, tout) << eb);
     }
-    auto lin_in = [&](uint64_t tau) {
-        uint64_t o = 0;
-        for (int i = 0; i < D; ++i)
-            if ((tau >> i) & 1ull) o ^= tp.tau_in[i];
-        return o;
-    };
-    auto lin_out = [&](uint64_t om) {
-        uint64_t o = 0;
-        for (int i = 0; i < D; ++i)
-            if ((om >> i) & 1ull) o ^= tp.om_out[i];
-        return o;
-    };
-    auto lin_phi = [&](uint64_t tau) {
-        uint32_t o = 0;
-        for (int i = 0; i < D; ++i)
-            if ((tau >> i) & 1ull) o ^= phi_bit[i];
-        return o;
-    };
-    auto lin_gam = [&](uint64_t om) {
-        uint32_t o = 0;
-        for (int i = 0; i < D; ++i)
-            if ((om >> i) & 1ull) o ^= gam_bit[i];
-        return o;
-    };
-
-    // Thread shape: 256 threads unless the tile has fewer 16-byte chunks.
-    const uint32_t chunks = (uint32_t)((1ull << D) / vec);
-    int NT = 256;
-    while (NT > 32 && (uint32_t)NT > chunks) NT >>= 1;
-    int qpt = (int)std::max<uint32_t>(1, chunks / NT);
-    if (qpt > kMaxQpt) return BMMC_ERR_INVALID_ARG;
-    tp.chunks = chunks;
-    const int eb = ilog2(elem);  // byte shift of one element
     for (int i = 0; i < qpt; ++i) {
-        uint64_t it = (uint64_t)i * NT << vb;
-        tp.it_in[i] = lin_in(it) << eb;
-        tp.it_out[i] = lin_out(it) << eb;
+        const uint64_t q = (uint64_t)i * NT;
+        const uint64_t it_t = q << vb;
+        const uint64_t it_o = omega_of(q);
+        tp.it_in[i] = lin(tau_in, it_t) << eb;
+        tp.it_out[i] = lin(om_out, it_o) << eb;
         for (int j = 0; j < vec; ++j) {
-            tp.st_slot[i * vec + j] = lin_phi(it | (uint64_t)j) << eb;
-            tp.ld_slot[i * vec + j] = lin_gam(it | (uint64_t)j) << eb;
+            tp.st_slot[i * vec + j] = (uint32_t)(lin(best.phiu, it_t | (uint64_t)j) << eb);
+            tp.ld_slot[i * vec + j] = (uint32_t)(lin(gamu, it_o | (uint64_t)j) << eb);
         }
     }
 
-    // Self-check: slots are a bijection and both phases are conflict-free.
-    {
-        std::vector<uint8_t> seen((size_t)1 << D, 0);
-        for (uint64_t tau = 0; tau < (1ull << D); ++tau) {
-            uint32_t s = lin_phi(tau);
-            if (s >= (1u << D) || seen[s]) return BMMC_ERR_INTERNAL;
-            seen[s] = 1;
-        }
-        int conflicts = 0;
-        for (int warp = 0; warp < NT / 32; ++warp)
-            for (int i = 0; i < qpt; ++i)
-                for (int j = 0; j < vec; ++j) {
-                    std::vector<uint32_t> rs, ws;
-                    for (int lane = 0; lane < 32; ++lane) {
-                        uint64_t q = (uint64_t)(warp * 32 + lane) + (uint64_t)i * NT;
-                        if (q >= chunks) continue;
-                        rs.push_back(lin_phi((q << vb) | (uint64_t)j));
-                        ws.push_back(lin_gam((q << vb) | (uint64_t)j));
-                    }
-                    conflicts += count_conflicts(rs, elem) + count_conflicts(ws, elem);
-                }
-        P.bank_conflicts = conflicts;
-    }
+    // Self-check: the slot map is a bijection (its images form a basis).
+    if (rank_of(best.phiu.data(), D) != D) return BMMC_ERR_INTERNAL;
+    for (uint64_t v : best.phiu)
+        if (v >> D) return BMMC_ERR_INTERNAL;
 
     P.kernel = KERNEL_TILED;
     P.grid_blocks = req.grid_blocks;
     P.threads = NT;
     P.qpt = qpt;
+    P.vector_scatter = best.vector_scatter;
     P.smem_bytes = (int)((1ull << D) * elem);
     P.t_in = t_in;
     P.t_out = t_out;
     P.tile_bits = D;
     P.n_over = n_over;
+    P.bank_conflicts = best.conflicts;
     P.tiles = tp.n_tiles;
     P.tile_basis = tb;
     P.block_bits = C;

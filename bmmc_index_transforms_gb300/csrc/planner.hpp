@@ -21,6 +21,7 @@ struct PassPlan {
     int n = 0;
     int threads = 256;
     int qpt = 1;             // 16-byte chunks per thread per tile
+    bool vector_scatter = false;  // input vectors stored whole (one 16-byte store each)
     int grid_blocks = 0;     // requested grid (0 = default)
     int smem_bytes = 0;
     int t_in = 0, t_out = 0, tile_bits = 0, n_over = 0;

@@ -112,6 +112,8 @@ typedef struct {
     int bank_conflicts;  /* extra shared-memory wavefronts per tile found by the planner's
                             self-check of its layout (0 = conflict-free on both phases) */
     uint64_t c;
+    int vector_stores;   /* 1 = input vectors are stored whole in shared memory (one
+                            16-byte store each), 0 = one store per element */
 } bmmc_plan_info_t;
 
 /* Build a plan for (A, c) with default options.  Host only; no device work.

@@ -215,6 +215,20 @@ def test_bank_conflict_free_on_structured_maps(elem):
                 assert p.info["bank_conflicts"] == 0
 
 
+@pytest.mark.parametrize("elem", [4, 8, 16])
+def test_vector_layout_chosen_and_conflict_free(elem):
+    """On the benchmark maps the planner keeps input vectors whole (one
+    16-byte shared store each) with a conflict-free gather."""
+    cases = [_random(0, 28)[0], ref.bitrev_rows(28), ref.rotate_rows(24, 12),
+             [1 << p for p in ref.axes_permute_bits((5, 6, 6, 6, 5), (4, 2, 0, 3, 1))],
+             _random(0, 28, low_to_high=10)[0]]
+    for rows in cases:
+        with bm.Plan(rows, 0, elem) as p:
+            info = p.info
+            assert info["vector_stores"] == 1, info
+            assert info["bank_conflicts"] == 0
+
+
 def test_classes():
     with bm.Plan(ref.identity_rows(8), 0, 4) as p:
         assert p.info["class_name"] == "identity" and p.info["kernel_name"] == "copy"
