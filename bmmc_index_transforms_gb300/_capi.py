@@ -41,7 +41,7 @@ MODE_TWO_FACTOR = 1
 class PlanOpts(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("t_in", ctypes.c_int), ("t_out", ctypes.c_int),
                 ("tile_bits", ctypes.c_int), ("alloc_scratch", ctypes.c_int),
-                ("grid_blocks", ctypes.c_int)]
+                ("grid_blocks", ctypes.c_int), ("load_mode", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

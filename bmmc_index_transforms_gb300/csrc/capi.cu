@@ -80,7 +80,8 @@ bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows, uint64_t c, 
     PlanRequest req;
     if (opts) {
         if (opts->t_in < 0 || opts->t_in > 16 || opts->t_out < 0 || opts->t_out > 16 ||
-            opts->tile_bits < 0 || opts->tile_bits > kMaxTileBits || opts->grid_blocks < 0)
+            opts->tile_bits < 0 || opts->tile_bits > kMaxTileBits || opts->grid_blocks < 0 ||
+            opts->load_mode < 0 || opts->load_mode > 2)
             return BMMC_ERR_INVALID_ARG;
         if (opts->mode != BMMC_MODE_SINGLE_PASS && opts->mode != BMMC_MODE_TWO_FACTOR)
             return BMMC_ERR_INVALID_ARG;
@@ -88,6 +89,7 @@ bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows, uint64_t c, 
         req.t_out = opts->t_out;
         req.tile_bits = opts->tile_bits;
         req.grid_blocks = opts->grid_blocks;
+        req.load_mode = opts->load_mode;
         p->mode = opts->mode;
     }
     bmmc_status s = plan_pass(n, p->rows, p->inv, c, (int)elem, req, &p->main);

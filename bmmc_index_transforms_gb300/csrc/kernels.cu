@@ -53,6 +53,19 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                  : "memory");
 }
 
+// Asynchronous 16-byte copy global -> shared (LDGSTS): the data never
+// passes through registers; completion is awaited with cp.async.wait_group
+// (a hardware wait, no spin loop).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint64_t warp_xor64(uint64_t v) {
     const uint32_t lo = __reduce_xor_sync(0xffffffffu, (uint32_t)v);
     const uint32_t hi = __reduce_xor_sync(0xffffffffu, (uint32_t)(v >> 32));
@@ -205,6 +218,129 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
     }
 }
 
+// Blocks per SM for the asynchronous-load kernel: no payload is held in
+// registers, so the shared memory (STAGES x 32 KiB for the default tiles)
+// sets the residency.
+template <int QPT, int STAGES>
+struct AsyncMinBlocks {
+    static constexpr int value = QPT >= 16 ? 3 : QPT == 8 ? (STAGES == 1 ? 7 : 3) : 8;
+};
+
+// Variant of bmmc_tiled_kernel for plans whose layout keeps input vectors
+// whole: the tile's input vectors are copied straight into their shared
+// slots with cp.async.  STAGES = 2 double-buffers blocks that walk more than
+// one tile (the next tile's copies are issued before the current tile is
+// gathered); STAGES = 1 serves grids of one tile per block.
+template <int ELEM, int NT, int QPT, typename OFF, int STAGES>
+__global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
+    bmmc_tiled_async_kernel(const __grid_constant__ TiledParams p, const uint4* __restrict__ in,
+                            uint4* __restrict__ out) {
+    using T = typename ElemType<ELEM>::T;
+    constexpr int VEC = 16 / ELEM;
+    constexpr int EB = ELEM == 4 ? 2 : ELEM == 8 ? 3 : 4;
+    extern __shared__ uint4 smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(smem_raw);
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
+    unsigned char* dst = reinterpret_cast<unsigned char*>(out);
+    const uint32_t tile_bytes = p.chunks * 16u;
+
+    const uint32_t tid = threadIdx.x;
+    const uint32_t lane = tid & 31u;
+    OFF in_t = 0, out_t = 0;
+    uint32_t ph_t = 0, ga_t = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxThreadBits; ++k) {
+        if ((1 << k) < NT && ((tid >> k) & 1u)) {
+            in_t ^= (OFF)p.tid_in[k];
+            out_t ^= (OFF)p.tid_out[k];
+            ph_t ^= p.tid_phi[k];
+            ga_t ^= p.tid_gam[k];
+        }
+    }
+    OFF my_cin = 0;
+    uint64_t my_cout = 0;
+    if ((int)lane < p.n_block_bits) {
+        my_cin = (OFF)(p.col_in[lane] << EB);
+        my_cout = p.col_out[lane];
+    }
+    uint32_t my_gl = 0;
+    if ((int)lane < p.t_out) my_gl = p.gam[lane] << EB;
+    const uint64_t lowm = (1ull << p.t_out) - 1ull;
+    bool act[QPT];
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) act[i] = tid + (uint32_t)i * NT < p.chunks;
+
+    auto tile_bases = [&](uint64_t b, OFF& ib, OFF& ob, uint32_t& g) {
+        const bool bit = (b >> lane) & 1ull;
+        ib = warp_xor<OFF>(bit ? my_cin : (OFF)0);
+        const uint64_t raw = warp_xor64(bit ? my_cout : 0ull) ^ p.c;
+        ob = (OFF)((raw & ~lowm) << EB);
+        const uint32_t delta = (uint32_t)(raw & lowm);
+        g = __reduce_xor_sync(0xffffffffu, ((delta >> lane) & 1u) ? my_gl : 0u);
+    };
+    // Issue the copies of tile b into stage buffer `stage`.
+    auto issue = [&](uint64_t b, int stage, OFF& ob, uint32_t& g) {
+        OFF ib;
+        tile_bases(b, ib, ob, g);
+        OFF it = in_t ^ ib;
+        opaque(it);
+        unsigned char* base = smem + (uint32_t)stage * tile_bytes;
+#pragma unroll
+        for (int i = 0; i < QPT; ++i)
+            if (act[i]) cp_async16(base + (ph_t ^ p.st_slot[i * VEC]), src + (it ^ (OFF)p.it_in[i]));
+        cp_async_commit();
+    };
+    auto gather_store = [&](int stage, OFF ob, uint32_t g) {
+        const unsigned char* base = smem + (uint32_t)stage * tile_bytes;
+        const uint32_t ga = ga_t ^ g;
+        OFF ot = out_t ^ ob;
+        opaque(ot);
+#pragma unroll
+        for (int i = 0; i < QPT; ++i) {
+            if (!act[i]) continue;
+            T e[VEC];
+            uint32_t gi = ga;
+            opaque(gi);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) e[j] = *reinterpret_cast<const T*>(base + (gi ^ p.ld_slot[i * VEC + j]));
+            uint4 v;
+            memcpy(&v, e, 16);
+            st_stream(reinterpret_cast<uint4*>(dst + (ot ^ (OFF)p.it_out[i])), v);
+        }
+    };
+
+    const uint64_t nt = p.n_tiles;
+    if (STAGES == 1) {
+        for (uint64_t b = blockIdx.x; b < nt; b += gridDim.x) {
+            OFF ob;
+            uint32_t g;
+            issue(b, 0, ob, g);
+            cp_async_wait<0>();
+            __syncthreads();
+            gather_store(0, ob, g);
+            __syncthreads();
+        }
+    } else {
+        OFF ob[2] = {0, 0};
+        uint32_t g[2] = {0, 0};
+        uint64_t b = blockIdx.x;
+        if (b < nt) issue(b, 0, ob[0], g[0]);
+        for (int k = 0; b < nt; b += gridDim.x, ++k) {
+            const int s = k & 1;
+            const uint64_t nb = b + gridDim.x;
+            if (nb < nt) {
+                issue(nb, s ^ 1, ob[s ^ 1], g[s ^ 1]);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+            gather_store(s, ob[s], g[s]);
+            __syncthreads();
+        }
+    }
+}
+
 // Per-element kernel for arrays too small for one 16-byte vector per run.
 template <int ELEM>
 __global__ void __launch_bounds__(32)
@@ -326,26 +462,66 @@ static cudaError_t blocks_per_sm(int dev, const void* fn, int threads, int smem,
     return cudaSuccess;
 }
 
+using AsyncFn = void (*)(const TiledParams, const uint4*, uint4*);
+
+template <int ELEM, typename OFF, int STAGES>
+static AsyncFn pick_async(int nt, int qpt) {
+    if (nt != 256) return nullptr;
+    switch (qpt) {
+        case 4: return bmmc_tiled_async_kernel<ELEM, 256, 4, OFF, STAGES>;
+        case 8: return bmmc_tiled_async_kernel<ELEM, 256, 8, OFF, STAGES>;
+        case 16: return bmmc_tiled_async_kernel<ELEM, 256, 16, OFF, STAGES>;
+    }
+    return nullptr;
+}
+
+template <int ELEM>
+static AsyncFn async_fn_elem(int nt, int qpt, bool wide, int stages) {
+    if (stages == 1)
+        return wide ? pick_async<ELEM, uint64_t, 1>(nt, qpt) : pick_async<ELEM, uint32_t, 1>(nt, qpt);
+    return wide ? pick_async<ELEM, uint64_t, 2>(nt, qpt) : pick_async<ELEM, uint32_t, 2>(nt, qpt);
+}
+
+static AsyncFn async_fn(int elem, int nt, int qpt, bool wide, int stages) {
+    switch (elem) {
+        case 4: return async_fn_elem<4>(nt, qpt, wide, stages);
+        case 8: return async_fn_elem<8>(nt, qpt, wide, stages);
+        case 16: return async_fn_elem<16>(nt, qpt, wide, stages);
+    }
+    return nullptr;
+}
+
 cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStream_t stream,
                          int grid_override) {
     const bool wide = ((uint64_t)P.elem << P.n) > 0xFFFFFFFFull;
-    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide, P.vector_scatter);
-    if (!fn) return cudaErrorInvalidConfiguration;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     int sms = 0, per = 0;
     if ((e = sm_count(dev, &sms)) != cudaSuccess) return e;
-    if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
     // Default grid: one block per tile for tiles of 8 chunks per thread or
     // more, else 64 blocks per SM, each block walking tiles blockIdx.x,
     // blockIdx.x + grid, ...; on GB300 these flat, oversubscribed grids
     // measured faster than one resident wave of persistent blocks.
-    (void)per;
     uint64_t grid = P.qpt >= 8 ? P.tiles : (uint64_t)sms * 64u;
-    if (grid > 0x7FFFFFFFull) grid = 0x7FFFFFFFull;
     if (grid_override > 0) grid = (uint64_t)grid_override;
     if (grid > P.tiles) grid = P.tiles;
+    if (grid > 0x7FFFFFFFull) grid = 0x7FFFFFFFull;
+    const bool use_async = P.vector_scatter && P.load_mode != 2 && (P.load_mode == 1 || P.async_default) &&
+                           P.threads == 256 && (P.qpt == 4 || P.qpt == 8 || P.qpt == 16);
+    if (use_async) {
+        const int stages = grid < P.tiles ? 2 : 1;
+        AsyncFn fn = async_fn(P.elem, P.threads, P.qpt, wide, stages);
+        if (!fn) return cudaErrorInvalidConfiguration;
+        const int smem = stages * P.smem_bytes;
+        if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, smem, &per)) != cudaSuccess) return e;
+        fn<<<(unsigned)grid, P.threads, smem, stream>>>(P.tp, static_cast<const uint4*>(in),
+                                                         static_cast<uint4*>(out));
+        return cudaGetLastError();
+    }
+    TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide, P.vector_scatter);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
     fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(P.tp, static_cast<const uint4*>(in),
                                                              static_cast<uint4*>(out));
     return cudaGetLastError();

@@ -452,6 +452,8 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
 
     P.kernel = KERNEL_TILED;
     P.grid_blocks = req.grid_blocks;
+    P.load_mode = req.load_mode;
+    P.async_default = false;
     P.threads = NT;
     P.qpt = qpt;
     P.vector_scatter = best.vector_scatter;

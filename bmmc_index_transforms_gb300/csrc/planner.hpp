@@ -22,6 +22,8 @@ struct PassPlan {
     int threads = 256;
     int qpt = 1;             // 16-byte chunks per thread per tile
     bool vector_scatter = false;  // input vectors stored whole (one 16-byte store each)
+    int load_mode = 0;            // 0 default, 1 asynchronous copies, 2 loads through registers
+    bool async_default = false;   // the default for this plan uses asynchronous copies
     int grid_blocks = 0;     // requested grid (0 = default)
     int smem_bytes = 0;
     int t_in = 0, t_out = 0, tile_bits = 0, n_over = 0;
@@ -36,6 +38,7 @@ struct PassPlan {
 struct PlanRequest {
     int t_in = 0, t_out = 0, tile_bits = 0;  // 0 = default
     int grid_blocks = 0;                     // 0 = default
+    int load_mode = 0;                       // 0 default, 1 async copies, 2 through registers
 };
 
 // Build one pass for (rows, c).  inv must be rows' inverse.

@@ -90,6 +90,10 @@ typedef struct {
     int grid_blocks;     /* blocks launched by the tiled kernel; each walks tiles
                             blockIdx.x, blockIdx.x + grid, ...; 0 = default, capped at
                             the number of tiles */
+    int load_mode;       /* tiled kernel input path: 0 = default, 1 = asynchronous
+                            copies straight into shared memory (layouts that keep input
+                            vectors whole, 4-16 chunks per thread), 2 = loads through
+                            registers */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;

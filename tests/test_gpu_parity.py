@@ -342,3 +342,23 @@ def test_device_pointer_errors(bm):
     assert e.value.status == 8
     h.close()
     h2.close()
+
+
+@pytest.mark.parametrize("load_mode", [1, 2])
+@pytest.mark.parametrize("elem", [4, 8, 16])
+def test_load_paths_and_grids(bm, load_mode, elem):
+    """Both input paths of the tiled kernel (asynchronous copies into shared
+    memory, loads through registers), with one block per tile and with
+    blocks that walk several tiles (double-buffered), give the oracle's
+    bytes."""
+    for n, seed, D, grid in [(20, 1, 0, 0), (20, 2, 0, 7), (21, 3, 0, 152), (19, 4, 0, 1),
+                             ({4: 18, 8: 17, 16: 16}[elem], 5, {4: 12, 8: 11, 16: 10}[elem], 13),
+                             ({4: 18, 8: 17, 16: 16}[elem], 6, {4: 14, 8: 13, 16: 12}[elem], 3)]:
+        rows, c = _random(seed * 31 + elem, n)
+        arr = synth.fill_int(n, elem)
+        got, info = _run(bm, rows, c, arr, tile_bits=D, grid_blocks=grid, load_mode=load_mode)
+        assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), (n, D, grid, info)
+    for rows in (ref.bitrev_rows(18), ref.rotate_rows(18, 9)):
+        arr = synth.fill_int(18, elem)
+        got, _ = _run(bm, rows, 0x155, arr, load_mode=load_mode, grid_blocks=29)
+        assert got.tobytes() == oracle.scatter(18, rows, 0x155, arr).tobytes()
