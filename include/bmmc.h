@@ -18,10 +18,14 @@
  *   - A_rows[i] holds row i of A: bit j of A_rows[i] is A[i][j], so output
  *     bit i is parity(A_rows[i] & x) XOR bit i of c.  Bits at or above n in
  *     A_rows[i] or in c are rejected (BMMC_ERR_INVALID_ARG).
- *   - Device pointers are caller-owned device (or managed) memory of exactly
- *     2^n * elem_size bytes, 16-byte aligned (BMMC_ERR_MISALIGNED otherwise).
- *     The library never allocates on a permute call, except as stated for the
- *     two-factor mode below.
+ *   - Array pointers are caller-owned memory of exactly 2^n * elem_size
+ *     bytes, 16-byte aligned (BMMC_ERR_MISALIGNED otherwise), that the GPU can
+ *     reach: device or managed memory, pinned host memory, or any host memory
+ *     on a device with pageable-memory access (otherwise BMMC_ERR_INVALID_ARG).
+ *     With host memory the kernels read and write it directly (on GB300 over
+ *     NVLink-C2C), which is the fastest end-to-end path for host-resident
+ *     arrays.  The library never allocates on a permute call, except as
+ *     stated for the two-factor mode below.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls enqueue work and return without synchronising; launch
  *     failures are reported as BMMC_ERR_CUDA.  A failed call enqueues nothing

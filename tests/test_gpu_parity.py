@@ -300,10 +300,21 @@ def test_end_to_end_host_buffers(bm):
     h_out = torch.zeros_like(h_in).pin_memory()
     d_in = torch.empty(arr.nbytes, dtype=torch.uint8, device="cuda")
     d_out = torch.empty_like(d_in)
+    want = oracle.scatter(n, rows, c, arr).tobytes()
     with bm.Plan(rows, c, elem) as p:
         p.permute_host(h_in, h_out, d_in, d_out)
         torch.cuda.current_stream().synchronize()
-    assert h_out.numpy().view(np.uint32).tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
+        assert h_out.numpy().view(np.uint32).tobytes() == want
+        # the kernel reading and writing the pinned host buffers directly
+        h_out.zero_()
+        p.permute(h_in, h_out)
+        torch.cuda.current_stream().synchronize()
+        assert h_out.numpy().view(np.uint32).tobytes() == want
+        # mixed: host input, device output
+        d_out.zero_()
+        p.permute(h_in, d_out)
+        torch.cuda.synchronize()
+        assert d_out.cpu().numpy().view(np.uint32).tobytes() == want
 
 
 def test_streams_and_repeat_calls(bm):
@@ -362,3 +373,39 @@ def test_load_paths_and_grids(bm, load_mode, elem):
         arr = synth.fill_int(18, elem)
         got, _ = _run(bm, rows, 0x155, arr, load_mode=load_mode, grid_blocks=29)
         assert got.tobytes() == oracle.scatter(18, rows, 0x155, arr).tobytes()
+
+
+@pytest.mark.parametrize("n,elem,kind", [(31, 4, "random"), (30, 8, "bitrev")])
+def test_arrays_over_4_gib(bm, n, elem, kind):
+    """8 GiB arrays take the 64-bit-offset kernels: exact oracle check of the
+    first and last 2^22 outputs (the last ones sit beyond the 4 GiB mark),
+    4096 sampled outputs one by one, and every input index placed exactly
+    once (a bitmap over the whole output)."""
+    N = 1 << n
+    rows, c = (_random(3, n) if kind == "random" else (ref.bitrev_rows(n), 0))
+    if elem == 4:
+        d_in = torch.arange(N, dtype=torch.int32, device="cuda")
+    else:
+        d_in = torch.arange(N, dtype=torch.int64, device="cuda")
+    d_out = torch.empty_like(d_in)
+    with bm.Plan(rows, c, elem) as p:
+        p.permute(d_in, d_out)
+    torch.cuda.synchronize()
+    del d_in
+    xs = synth.sample_indices(n + elem, n, 4096)
+    ys = np.array([oracle.index(n, rows, c, int(x)) for x in xs], dtype=np.int64)
+    got = d_out[torch.from_numpy(ys).cuda()].cpu().numpy().astype(np.int64)
+    assert np.array_equal(got, xs.astype(np.int64))
+    seen = torch.zeros(N, dtype=torch.bool, device="cuda")
+    step = 1 << 26
+    for k in range(0, N, step):
+        seen[d_out[k:k + step].long()] = True
+    assert bool(seen.all())
+    del seen
+    host = d_out.cpu().numpy()
+    inv = ref.f2_inverse(n, rows)
+    for lo, hi in [(0, 1 << 22), (N - (1 << 22), N)]:
+        bad, first = oracle.check_index_fill(n, inv, c, host, elem, threads=HOST_THREADS, y_range=(lo, hi))
+        assert bad == 0, first
+    del d_out
+    torch.cuda.empty_cache()
