@@ -24,7 +24,8 @@ __all__ = [
     "BmmcError", "Plan", "bmmc_plan", "bmmc_plan_ex", "bmmc_plan_destroy", "bmmc_plan_info",
     "bmmc_plan_factor", "bmmc_plan_tile", "bmmc_permute", "bmmc_permute_scratch",
     "bmmc_permute_host", "bmmc_permute_static_scratch", "transpose2d", "bpc_permute", "bmmc_dims_permute",
-    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_status_string", "bmmc_version", "library_path",
+    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "bmmc_parm_rows", "bmmc_inverse_rows",
+    "bmmc_status_string", "bmmc_version", "library_path",
 ]
 
 CLASS_NAMES = {0: "identity", 1: "complement", 2: "bp", 3: "bpc", 4: "bmmc"}
@@ -189,6 +190,43 @@ def bmmc_dims_permute_bits(dims_log2: Sequence[int], axes: Sequence[int]) -> lis
     out = (ctypes.c_int * 64)()
     _check(_capi.lib().bmmc_dims_permute_bits(d, dl, ax, out), "bmmc_dims_permute_bits")
     return [int(out[i]) for i in range(sum(dims_log2))]
+
+
+def _lmad_args(dims_log2, in_offset, in_strides, out_offset, out_strides):
+    d = len(dims_log2)
+    if len(in_strides) != d or len(out_strides) != d:
+        raise ValueError("one stride per dimension on each side")
+    return (d, (ctypes.c_int * d)(*dims_log2), int(in_offset), (ctypes.c_int64 * d)(*in_strides),
+            int(out_offset), (ctypes.c_int64 * d)(*out_strides))
+
+
+def bmmc_lmad_copy(dims_log2: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
+                   out_strides: Sequence[int], elem_size: int, inp, out, stream=None) -> None:
+    args = _lmad_args(dims_log2, in_offset, in_strides, out_offset, out_strides)
+    _check(_capi.lib().bmmc_lmad_copy(*args, elem_size, _ptr(inp), _ptr(out), _stream(stream, inp, out)),
+           "bmmc_lmad_copy")
+
+
+def bmmc_lmad_bpc(dims_log2: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
+                  out_strides: Sequence[int]) -> tuple[list[int], int]:
+    args = _lmad_args(dims_log2, in_offset, in_strides, out_offset, out_strides)
+    perm = (ctypes.c_int * 64)()
+    c = ctypes.c_uint64(0)
+    _check(_capi.lib().bmmc_lmad_bpc(*args, perm, ctypes.byref(c)), "bmmc_lmad_bpc")
+    return [int(perm[i]) for i in range(sum(dims_log2))], int(c.value)
+
+
+def bmmc_inverse_rows(A_rows: Sequence[int]) -> list[int]:
+    n = len(A_rows)
+    out = (ctypes.c_uint64 * 64)()
+    _check(_capi.lib().bmmc_inverse_rows(n, _rows(n, A_rows), out), "bmmc_inverse_rows")
+    return [int(out[i]) for i in range(n)]
+
+
+def bmmc_parm_rows(n: int, mask: int) -> list[int]:
+    rows = (ctypes.c_uint64 * 64)()
+    _check(_capi.lib().bmmc_parm_rows(n, int(mask), rows), "bmmc_parm_rows")
+    return [int(rows[i]) for i in range(n)]
 
 
 def bmmc_copy(inp, out, nbytes: int | None = None, stream=None) -> None:

@@ -18,6 +18,7 @@ _lib = None
 u64 = ctypes.c_uint64
 u64p = ctypes.POINTER(ctypes.c_uint64)
 intp = ctypes.POINTER(ctypes.c_int)
+i64p = ctypes.POINTER(ctypes.c_int64)
 vp = ctypes.c_void_p
 
 # Status codes (bmmc_status)
@@ -72,6 +73,12 @@ SIGNATURES = {
     "bmmc_dims_permute": (ctypes.c_int, [ctypes.c_int, intp, intp, ctypes.c_size_t, vp, vp, vp]),
     "bmmc_dims_permute_bits": (ctypes.c_int, [ctypes.c_int, intp, intp, intp]),
     "bmmc_copy": (ctypes.c_int, [vp, vp, ctypes.c_size_t, vp]),
+    "bmmc_lmad_copy": (ctypes.c_int, [ctypes.c_int, intp, ctypes.c_int64, i64p, ctypes.c_int64, i64p,
+                                      ctypes.c_size_t, vp, vp, vp]),
+    "bmmc_lmad_bpc": (ctypes.c_int, [ctypes.c_int, intp, ctypes.c_int64, i64p, ctypes.c_int64, i64p, intp,
+                                     u64p]),
+    "bmmc_parm_rows": (ctypes.c_int, [ctypes.c_int, u64, u64p]),
+    "bmmc_inverse_rows": (ctypes.c_int, [ctypes.c_int, u64p, u64p]),
     "bmmc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bmmc_version": (ctypes.c_int, []),
 }

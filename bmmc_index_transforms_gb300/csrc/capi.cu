@@ -320,6 +320,90 @@ bmmc_status bmmc_dims_permute(int ndims, const int* dims_log2, const int* axes, 
     return bpc_permute(n, perm, 0, elem_size, in, out, stream);
 }
 
+// One LMAD side: the bit range and direction of every dimension.  Returns
+// false unless the LMAD maps the index space one-to-one onto [0, 2^n).
+static bool lmad_bits(int ndims, const int* dims_log2, int64_t offset, const int64_t* strides, int* pos,
+                      bool* neg) {
+    uint64_t covered = 0;
+    int n = 0;
+    int64_t want_offset = 0;
+    for (int k = 0; k < ndims; ++k) {
+        n += dims_log2[k];
+        pos[k] = 0;
+        neg[k] = false;
+        if (dims_log2[k] == 0) continue;  // a size-1 dimension never moves
+        const int64_t s = strides[k];
+        if (s == 0) return false;
+        const uint64_t mag = s < 0 ? (uint64_t)(-(s + 1)) + 1u : (uint64_t)s;
+        if (mag & (mag - 1)) return false;  // not a power of two
+        const int p = __builtin_ctzll(mag);
+        if (p + dims_log2[k] > kMaxN) return false;
+        const uint64_t bits = ((1ull << dims_log2[k]) - 1) << p;
+        if (covered & bits) return false;
+        covered |= bits;
+        pos[k] = p;
+        neg[k] = s < 0;
+        if (s < 0) want_offset += (int64_t)(((1ull << dims_log2[k]) - 1) << p);
+    }
+    if (n < 1 || n > kMaxN || covered != lowmask(n)) return false;
+    return offset == want_offset;
+}
+
+bmmc_status bmmc_lmad_bpc(int ndims, const int* dims_log2, int64_t in_offset, const int64_t* in_strides,
+                          int64_t out_offset, const int64_t* out_strides, int* perm_out, uint64_t* c_out) {
+    if (!dims_log2 || !in_strides || !out_strides || !perm_out || !c_out || ndims < 1 || ndims > 64)
+        return BMMC_ERR_INVALID_ARG;
+    int n = 0;
+    for (int k = 0; k < ndims; ++k) {
+        if (dims_log2[k] < 0 || dims_log2[k] > kMaxN) return BMMC_ERR_INVALID_ARG;
+        n += dims_log2[k];
+        if (n > kMaxN) return BMMC_ERR_INVALID_ARG;
+    }
+    int pin[64], pout[64];
+    bool nin[64], nout[64];
+    if (!lmad_bits(ndims, dims_log2, in_offset, in_strides, pin, nin) ||
+        !lmad_bits(ndims, dims_log2, out_offset, out_strides, pout, nout))
+        return BMMC_ERR_INVALID_ARG;
+    uint64_t c = 0;
+    for (int k = 0; k < ndims; ++k)
+        for (int j = 0; j < dims_log2[k]; ++j) {
+            perm_out[pout[k] + j] = pin[k] + j;
+            if (nin[k] != nout[k]) c |= 1ull << (pout[k] + j);
+        }
+    *c_out = c;
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_lmad_copy(int ndims, const int* dims_log2, int64_t in_offset, const int64_t* in_strides,
+                           int64_t out_offset, const int64_t* out_strides, size_t elem_size, const void* in,
+                           void* out, void* stream) {
+    int perm[64];
+    uint64_t c = 0;
+    bmmc_status s = bmmc_lmad_bpc(ndims, dims_log2, in_offset, in_strides, out_offset, out_strides, perm, &c);
+    if (s != BMMC_OK) return s;
+    int n = 0;
+    for (int k = 0; k < ndims; ++k) n += dims_log2[k];
+    return bpc_permute(n, perm, c, elem_size, in, out, stream);
+}
+
+bmmc_status bmmc_inverse_rows(int n, const uint64_t* A_rows, uint64_t* inv_rows_out) {
+    if (!inv_rows_out) return BMMC_ERR_INVALID_ARG;
+    bmmc_status s = check_matrix(n, A_rows, 0);
+    if (s != BMMC_OK) return s;
+    uint64_t inv[64];
+    if (!inverse_rows(n, A_rows, inv)) return BMMC_ERR_SINGULAR;
+    for (int i = 0; i < n; ++i) inv_rows_out[i] = inv[i];
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_parm_rows(int n, uint64_t mask, uint64_t* rows_out) {
+    if (!rows_out || n < 1 || n > kMaxN || mask == 0 || (mask & ~lowmask(n))) return BMMC_ERR_INVALID_ARG;
+    const int p = __builtin_ctzll(mask);
+    for (int i = 0; i < n - 1; ++i) rows_out[i] = 1ull << (i < p ? i : i + 1);
+    rows_out[n - 1] = mask;
+    return BMMC_OK;
+}
+
 bmmc_status bmmc_copy(const void* in, void* out, size_t bytes, void* stream) {
     if (bytes == 0) return BMMC_OK;
     bmmc_status s = check_buffers(in, out, bytes);

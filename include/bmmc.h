@@ -233,6 +233,46 @@ bmmc_status bmmc_dims_permute(int ndims, const int *dims_log2, const int *axes,
 bmmc_status bmmc_dims_permute_bits(int ndims, const int *dims_log2, const int *axes,
                                    int *perm_out);
 
+/* Copy between two LMAD views whose sizes are powers of two ("Speeding up
+ * GPU copies by permuting iteration spaces", Futhark blog, "Futhark's array
+ * representation" and "Optimising LMAD copies"): for every index tuple
+ * (i_0, ..., i_{d-1}), 0 <= i_k < 2^dims_log2[k],
+ *     out[out_offset + sum_k i_k * out_strides[k]] =
+ *         in[in_offset + sum_k i_k * in_strides[k]]          (element units)
+ * Supported when every stride of a dimension of size > 1 is +-2^p and each
+ * LMAD maps the index space one-to-one onto [0, 2^n), n = sum of dims_log2:
+ * contiguous arrays with permuted and/or reversed dimensions (a negative
+ * stride with the offset pointing at the reversed dimension's last element).
+ * Such a copy is one BPC: output bit q_k + j is input bit p_k + j,
+ * complemented when exactly one side reverses dimension k.  Other LMADs are
+ * rejected with BMMC_ERR_INVALID_ARG (no fallback). */
+bmmc_status bmmc_lmad_copy(int ndims, const int *dims_log2, int64_t in_offset,
+                           const int64_t *in_strides, int64_t out_offset,
+                           const int64_t *out_strides, size_t elem_size, const void *in,
+                           void *out, void *stream);
+
+/* The BPC bmmc_lmad_copy runs: perm_out[i] (n entries) is the input bit of
+ * output bit i, *c_out the complement.  Host only. */
+bmmc_status bmmc_lmad_bpc(int ndims, const int *dims_log2, int64_t in_offset,
+                          const int64_t *in_strides, int64_t out_offset,
+                          const int64_t *out_strides, int *perm_out, uint64_t *c_out);
+
+/* Inverse of an invertible n x n bit matrix over F2 (rows as in bmmc_plan):
+ * inv_rows_out receives A^-1, so permuting by (A^-1, A^-1.c) undoes (A, c).
+ * Errors: INVALID_ARG, SINGULAR.  Host only. */
+bmmc_status bmmc_inverse_rows(int n, const uint64_t *A_rows, uint64_t *inv_rows_out);
+
+/* The parm combinator of "Efficient GPU Implementation of Affine Index
+ * Permutations on Arrays" (introduction: parm mask f xs splits xs by the F2
+ * dot product i.mask, applies f to both parts and stitches them back) is
+ * lowered as  parm mask f = P_(A^-1) . parm 2^(n-1) f . P_A : rows_out
+ * receives A (n rows), which moves every index with i.mask = b to the half b
+ * (output bit n-1 = parity(i & mask)) and keeps the relative order inside
+ * each half (the other output bits are the index bits except the lowest set
+ * bit of mask, in order).  mask must be non-zero with no bit at or above n.
+ * Host only. */
+bmmc_status bmmc_parm_rows(int n, uint64_t mask, uint64_t *rows_out);
+
 /* Plain copy of `bytes` bytes (16-byte vectors, any tail byte-wise): the
  * practical ceiling a permutation is measured against ("A kernel that is
  * correct", "The ceiling: a copy").  Pointers 16-byte aligned. */

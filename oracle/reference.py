@@ -45,6 +45,8 @@ __all__ = [
     "rotate_rows",
     "axes_permute_bits",
     "r2_tiled",
+    "lmad_copy",
+    "parm",
 ]
 
 
@@ -279,3 +281,46 @@ def r2_tiled(n: int, rows, t: int) -> bool:
             col |= ((inv[i] >> j) & 1) << i
         support |= col >> t << t
     return bin(support).count("1") <= t
+
+
+# ---------------------------------------------------------------------------
+# LMAD copies ("Speeding up GPU copies by permuting iteration spaces",
+# Futhark blog, "Futhark's array representation": an LMAD is a list of
+# (size, stride) pairs plus an offset; a copy is, for every index tuple,
+# out[L_out(i)] = in[L_in(i)])
+# ---------------------------------------------------------------------------
+
+def lmad_copy(dims_log2, in_offset, in_strides, out_offset, out_strides, arr):
+    """The copy loop written out over all index tuples (numpy index arrays).
+    Positions no tuple writes stay zero."""
+    arr = np.asarray(arr)
+    sizes = [1 << int(b) for b in dims_log2]
+    idx = np.indices(sizes).reshape(len(sizes), -1).astype(np.int64)
+    src = np.full(idx.shape[1], int(in_offset), dtype=np.int64)
+    dst = np.full(idx.shape[1], int(out_offset), dtype=np.int64)
+    for k in range(len(sizes)):
+        src += int(in_strides[k]) * idx[k]
+        dst += int(out_strides[k]) * idx[k]
+    out = np.zeros_like(arr)
+    out[dst] = arr[src]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The parm combinator ("Efficient GPU Implementation of Affine Index
+# Permutations on Arrays", introduction): parm mask f xs sends element i to
+# the first or the second part according to the F2 dot product i.mask,
+# applies f to each part and puts the results back where the parts came
+# from.  Reading taken: each part keeps index order.
+# ---------------------------------------------------------------------------
+
+def parm(mask: int, f, xs):
+    N = len(xs)
+    out = [None] * N
+    for b in (0, 1):
+        where = [i for i in range(N) if parity(i & mask) == b]
+        ys = list(f([xs[i] for i in where]))
+        assert len(ys) == len(where)
+        for i, y in zip(where, ys):
+            out[i] = y
+    return out

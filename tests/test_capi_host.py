@@ -293,3 +293,100 @@ def test_dims_permute_bits_against_oracle():
         bm.bmmc_dims_permute_bits((3, 4), (0, 0))
     with pytest.raises(bm.BmmcError):
         bm.bmmc_dims_permute_bits((0, 0), (0, 1))
+
+
+
+def _lmad_case(rng, dims_log2):
+    """A random pair of power-of-two LMADs over the same index space: each
+    side a row-major layout of the dims in a random order, with random
+    dimensions reversed."""
+    d = len(dims_log2)
+
+    def side():
+        order = list(rng.permutation(d))
+        strides = [0] * d
+        acc = 1
+        for k in reversed(order):  # last in order = fastest
+            strides[k] = acc
+            acc <<= dims_log2[k]
+        offset = 0
+        for k in range(d):
+            if dims_log2[k] and rng.random() < 0.5:
+                offset += ((1 << dims_log2[k]) - 1) * strides[k]
+                strides[k] = -strides[k]
+        return offset, strides
+
+    io, ist = side()
+    oo, ost = side()
+    return io, ist, oo, ost
+
+
+def test_lmad_front_end_against_oracle():
+    """The BPC the library derives from two LMADs, applied by the oracle's
+    BPC scatter, equals the oracle's LMAD copy loop."""
+    rng = np.random.default_rng(7)
+    for trial in range(60):
+        d = int(rng.integers(1, 5))
+        dims = [int(v) for v in rng.integers(0, 4, size=d)]
+        if sum(dims) == 0:
+            dims[0] = 1
+        io, ist, oo, ost = _lmad_case(rng, dims)
+        n = sum(dims)
+        arr = np.arange(1 << n, dtype=np.uint32)
+        want = ref.lmad_copy(dims, io, ist, oo, ost, arr)
+        perm, c = bm.bmmc_lmad_bpc(dims, io, ist, oo, ost)
+        assert np.array_equal(ref.bpc_permute(n, perm, c, arr), want), (dims, io, ist, oo, ost)
+
+
+def test_lmad_front_end_rejections():
+    with pytest.raises(bm.BmmcError):   # stride not a power of two
+        bm.bmmc_lmad_bpc((2, 2), 0, (3, 1), 0, (4, 1))
+    with pytest.raises(bm.BmmcError):   # overlapping dimensions
+        bm.bmmc_lmad_bpc((2, 2), 0, (2, 1), 0, (4, 1))
+    with pytest.raises(bm.BmmcError):   # reversed dimension without its offset
+        bm.bmmc_lmad_bpc((2, 2), 0, (4, -1), 0, (4, 1))
+    with pytest.raises(bm.BmmcError):   # gap: not contiguous
+        bm.bmmc_lmad_bpc((2, 2), 0, (8, 1), 0, (4, 1))
+    # Futhark's reversed_rows [8192][8192]: a BPC with c = 2^13 - 1 on the column bits
+    perm, c = bm.bmmc_lmad_bpc((13, 13), 8191, (8192, -1), 0, (8192, 1))
+    assert perm == list(range(26)) and c == 8191
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 16, 28])
+def test_parm_rows_structure(n):
+    """Top output bit is the parity of i & mask, A is invertible (oracle rank),
+    and inside each half the index order is kept (checked on every index for
+    small n)."""
+    rng = np.random.default_rng(n)
+    for _ in range(5):
+        mask = int(rng.integers(1, 1 << n)) if n < 63 else 1
+        A = bm.bmmc_parm_rows(n, mask)
+        assert A[n - 1] == mask
+        assert ref.f2_rank(n, A) == n
+        if n <= 8:
+            ys = [ref.bmmc_index(n, A, 0, x) for x in range(1 << n)]
+            for b in (0, 1):
+                part = [x for x in range(1 << n) if ref.parity(x & mask) == b]
+                pos = [ys[x] for x in part]
+                assert pos == list(range(b << (n - 1), (b + 1) << (n - 1)))
+    with pytest.raises(bm.BmmcError):
+        bm.bmmc_parm_rows(n, 0)
+    with pytest.raises(bm.BmmcError):
+        bm.bmmc_parm_rows(n, 1 << n)
+
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_inverse_rows_brute_force(n):
+    """bmmc_inverse_rows undoes A's index map on every index, for every
+    invertible A (every 5th matrix at n = 4); singular A are rejected."""
+    for code in range(0, 1 << (n * n), 5 if n == 4 else 1):
+        A = [(code >> (n * i)) & ((1 << n) - 1) for i in range(n)]
+        if ref.f2_rank(n, A) < n:
+            with pytest.raises(bm.BmmcError) as e:
+                bm.bmmc_inverse_rows(A)
+            assert e.value.status == _capi.ERR_SINGULAR
+            continue
+        inv = bm.bmmc_inverse_rows(A)
+        for x in range(1 << n):
+            assert ref.bmmc_index(n, inv, 0, ref.bmmc_index(n, A, 0, x)) == x

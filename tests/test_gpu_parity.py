@@ -409,3 +409,58 @@ def test_arrays_over_4_gib(bm, n, elem, kind):
         assert bad == 0, first
     del d_out
     torch.cuda.empty_cache()
+
+
+
+def test_lmad_copy_on_gpu(bm):
+    """Power-of-two LMAD copies (permuted and reversed dimensions, both sides)
+    against the oracle's LMAD copy loop, including Futhark's reversed_rows at
+    [8192][8192] int32."""
+    from test_capi_host import _lmad_case
+
+    rng = np.random.default_rng(11)
+    for trial in range(12):
+        d = int(rng.integers(2, 6))
+        dims = [int(v) for v in rng.integers(1, 6, size=d)]
+        io, ist, oo, ost = _lmad_case(rng, dims)
+        n = sum(dims)
+        for elem in (4, 16):
+            arr = synth.fill_int(n, elem)
+            d_in, d_out = _dev(arr), torch.zeros(arr.nbytes, dtype=torch.uint8, device="cuda")
+            bm.bmmc_lmad_copy(dims, io, ist, oo, ost, elem, d_in, d_out)
+            torch.cuda.synchronize()
+            assert _host(d_out, arr).tobytes() == ref.lmad_copy(dims, io, ist, oo, ost, arr).tobytes()
+    a = torch.arange(1 << 26, dtype=torch.int32, device="cuda")
+    b = torch.empty_like(a)
+    bm.bmmc_lmad_copy((13, 13), 8191, (8192, -1), 0, (8192, 1), 4, a, b)
+    torch.cuda.synchronize()
+    assert torch.equal(b.view(8192, 8192), torch.flip(a.view(8192, 8192), dims=[1]))
+
+
+@pytest.mark.parametrize("n,mask", [(10, 0b1011001110), (16, 1), (16, 0x8000), (20, 0xF0F0F)])
+def test_parm_lowering_on_gpu(bm, n, mask):
+    """parm mask f = P_(A^-1) . (f on each half) . P_A with the library's
+    permutes, against the oracle's parm definition; f reverses a part and
+    adds its position."""
+    import torch as t
+
+    A = bm.bmmc_parm_rows(n, mask)
+    inv = bm.bmmc_inverse_rows(A)
+    xs = np.arange(1 << n, dtype=np.int64) * 3 + 1
+
+    def f_list(v):
+        return [int(x) + 1000 * i for i, x in enumerate(reversed(v))]
+
+    want = np.array(ref.parm(mask, f_list, xs.tolist()), dtype=np.int64)
+    d = t.from_numpy(xs).cuda()
+    mid = t.empty_like(d)
+    with bm.Plan(A, 0, 8) as p:
+        p.permute(d, mid)
+    half = 1 << (n - 1)
+    pos = t.arange(half, device="cuda", dtype=t.int64) * 1000
+    mid2 = t.cat([t.flip(mid[:half], dims=[0]) + pos, t.flip(mid[half:], dims=[0]) + pos])
+    out = t.empty_like(d)
+    with bm.Plan(inv, 0, 8) as p:
+        p.permute(mid2, out)
+    t.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), want)

@@ -256,3 +256,37 @@ def test_generator_is_splitmix64_and_deterministic():
     rows, c, tries = synth.draw_bmmc(3, 28, lambda r: ref.f2_rank(28, r) == 28, low_to_high=10)
     for i in range(10):
         assert rows[i] & 0x3FF == 0
+
+
+def test_lmad_copy_special_cases():
+    """Futhark's reversed_rows (copy (map reverse xss)) is flip on the last
+    axis; a transposed LMAD is numpy's transpose; permuted dims with one
+    reversed dim are numpy transpose then flip."""
+    R, C = 3, 4  # log2 sizes: 8 x 16
+    a = np.arange(1 << (R + C), dtype=np.uint32)
+    m = a.reshape(1 << R, 1 << C)
+    # source view map reverse xss: stride -1 on the column, offset at its end
+    got = ref.lmad_copy((R, C), (1 << C) - 1, (1 << C, -1), 0, (1 << C, 1), a)
+    assert np.array_equal(got, np.flip(m, axis=1).ravel())
+    # destination column-major: the transpose
+    got = ref.lmad_copy((R, C), 0, (1 << C, 1), 0, (1, 1 << R), a)
+    assert np.array_equal(got, m.T.copy().ravel())
+    shape = (1, 2, 3)
+    b = np.arange(1 << 6, dtype=np.uint32)
+    t = b.reshape(2, 4, 8)
+    want = np.flip(t.transpose(2, 0, 1), axis=1).copy().ravel()  # out[k][i][j] = in[i][3-j'][...]
+    # index tuple (i, j, k) over in-shape (2,4,8); out shape (8,2,4) reversed on its axis 1 (size 2)
+    out_strides = (4 * -1, 1, 8)  # dim i -> out axis 1 (stride 4) reversed, j -> axis 2 (1), k -> axis 0 (8)
+    got = ref.lmad_copy(shape, 0, (32, 8, 1), 4, out_strides, b)
+    assert np.array_equal(got, want)
+
+
+def test_parm_pins():
+    """parm with mask 2^(n-1) applies f to the first and second halves (stated
+    on the page); a hand-worked mask 0b11 example; mask 1 splits even/odd."""
+    rev = lambda v: list(reversed(v))  # noqa: E731
+    xs = list("abcdefgh")
+    assert ref.parm(4, rev, xs) == list("dcbahgfe")
+    assert ref.parm(0b11, rev, list("abcd")) == list("dcba")  # parts {0,3}, {1,2}
+    even_odd = ref.parm(1, rev, xs)
+    assert even_odd[0::2] == list("geca") and even_odd[1::2] == list("hfdb")
