@@ -257,19 +257,44 @@ def job_throughput_gbs(world: int, launches_per_rank: int, bytes_per_launch: flo
 
 
 def time_launches(torch, fn, reps: int, warm: int = 2):
-    """Median / min / mean milliseconds of fn() with CUDA events on the
-    current stream."""
+    """Mean milliseconds per call of fn() over `reps` back-to-back calls
+    between two CUDA events on the current stream (the queue stays full, so
+    no host launch latency is counted).  For arrays larger than the L2 this
+    is the cold-cache time of one launch.  Returns (mean, mean, mean) for the
+    (median, min, mean) interface."""
     for _ in range(warm):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    return ms, ms, ms
+
+
+def time_small(torch, fn, flush_buf, reps: int = 30):
+    """Two figures for arrays that fit in the L2: `flushed` - before each
+    timed launch a write of a buffer larger than the L2 both evicts the
+    array and keeps the GPU busy, so the event pair brackets only the
+    kernel; `warm` - the median of back-to-back launches with the array
+    resident in the L2."""
+    for _ in range(3):
         fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     torch.cuda.synchronize()
     for a, b in ev:
+        flush_buf.zero_()
         a.record()
         fn()
         b.record()
     torch.cuda.synchronize()
-    ms = [a.elapsed_time(b) for a, b in ev]
-    return median(ms), min(ms), sum(ms) / len(ms)
+    flushed = median([a.elapsed_time(b) for a, b in ev])
+    warm, _, _ = time_launches(torch, fn, reps, warm=1)
+    return flushed, warm
 
 
 def run_ours(args):
@@ -431,16 +456,23 @@ def run_ours(args):
 
 
 def other_configs(torch, bm, synth, dev, stream):
-    """Effective GB/s of the other benchmark configurations (median of 30)."""
+    """Effective GB/s of the other benchmark configurations.  Arrays larger
+    than the L2: mean of 30 back-to-back launches.  Arrays that fit in it:
+    L2-flushed median and warm back-to-back mean."""
     from bmmc_index_transforms_gb300.maps import axes_rows, bitrev_rows, rotate_rows
 
     out = {}
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
-    def gbs(n, elem, fn):
-        med, mn, mean = time_launches(torch, fn, 30)
+    def big(n, elem, fn):
+        ms, _, _ = time_launches(torch, fn, 30)
+        return {"gbs": round(2.0 * (1 << n) * elem / (ms / 1e3) / 1e9, 1), "ms": round(ms, 4)}
+
+    def small(n, elem, fn):
+        fl, warm = time_small(torch, fn, flush_buf)
         b = 2.0 * (1 << n) * elem
-        return {"median_gbs": round(b / (med / 1e3) / 1e9, 1), "min_ms": round(mn, 4),
-                "median_ms": round(med, 4)}
+        return {"gbs_l2_flushed": round(b / (fl / 1e3) / 1e9, 1), "ms_l2_flushed": round(fl, 4),
+                "gbs_warm": round(b / (warm / 1e3) / 1e9, 1), "ms_warm": round(warm, 4)}
 
     def accept(n):
         def f(rows):
@@ -451,38 +483,40 @@ def other_configs(torch, bm, synth, dev, stream):
                 return False
         return f
 
-    # C1: n=16 random int32, seed 0 (launch-bound)
+    # C1: n=16 random int32, seed 0 (512 KiB moved: launch latency and L2)
     rows, c, _ = synth.draw_bmmc(0, 16, accept(16))
     a = torch.arange(1 << 16, dtype=torch.int32, device=dev)
     b = torch.empty_like(a)
     with bm.Plan(rows, c, 4) as p:
-        out["n16_random_int32"] = gbs(16, 4, lambda: p.permute(a, b, stream))
-    # C2: 4096^2 fp32 transpose (n=24, 128 MiB: near L2 size, no flush)
+        out["n16_random_int32"] = small(16, 4, lambda: p.permute(a, b, stream))
+    out["n16_copy"] = small(16, 4, lambda: bm.bmmc_copy(a, b, 1 << 18, stream))
+    # C2: 4096^2 fp32 transpose (n=24, 128 MiB moved: the L2's size)
     a = torch.arange(1 << 24, dtype=torch.float32, device=dev)
     b = torch.empty_like(a)
     with bm.Plan(rotate_rows(24, 12), 0, 4) as p:
-        out["transpose_4096_fp32"] = gbs(24, 4, lambda: p.permute(a, b, stream))
+        out["transpose_4096_fp32"] = small(24, 4, lambda: p.permute(a, b, stream))
+    out["transpose_4096_copy"] = small(24, 4, lambda: bm.bmmc_copy(a, b, 1 << 26, stream))
     del a, b
     # C3: bit reversal n=28 int32 / int64
     a = torch.arange(1 << 28, dtype=torch.int64, device=dev)
     b = torch.empty_like(a)
     with bm.Plan(bitrev_rows(28), 0, 8) as p:
-        out["bitrev_n28_int64"] = gbs(28, 8, lambda: p.permute(a, b, stream))
+        out["bitrev_n28_int64"] = big(28, 8, lambda: p.permute(a, b, stream))
     a32 = a[: 1 << 27].view(torch.int32)
     b32 = b[: 1 << 27].view(torch.int32)
     with bm.Plan(bitrev_rows(28), 0, 4) as p:
-        out["bitrev_n28_int32"] = gbs(28, 4, lambda: p.permute(a32, b32, stream))
+        out["bitrev_n28_int32"] = big(28, 4, lambda: p.permute(a32, b32, stream))
     # C5: 5-D [32,64,64,64,32] fp32 perm (4,2,0,3,1), and the float4 view
     with bm.Plan(axes_rows((5, 6, 6, 6, 5), synth.FIVE_D_AXES), 0, 4) as p:
-        out["dims5_fp32"] = gbs(28, 4, lambda: p.permute(a32, b32, stream))
+        out["dims5_fp32"] = big(28, 4, lambda: p.permute(a32, b32, stream))
     with bm.Plan(axes_rows((5, 6, 6, 6, 3), synth.FIVE_D_AXES), 0, 16) as p:
-        out["dims5_float4"] = gbs(26, 16, lambda: p.permute(a32, b32, stream))
-    # two-factor mode on seed 0 (the paper's two-kernel scheme), same bytes
+        out["dims5_float4"] = big(26, 16, lambda: p.permute(a32, b32, stream))
+    # two-factor mode on seed 0 (the paper's two-kernel scheme), same algorithmic bytes
     rows, c, _ = synth.draw_bmmc(0, 28, accept(28))
     scratch = torch.empty(1 << 28, dtype=torch.int32, device=dev)
     with bm.Plan(rows, c, 4, mode=1) as p:
-        out["random_n28_int32_two_factor"] = gbs(28, 4, lambda: p.permute_scratch(a32, b32, scratch, stream))
-    del a, b, scratch
+        out["random_n28_int32_two_factor"] = big(28, 4, lambda: p.permute_scratch(a32, b32, scratch, stream))
+    del a, b, scratch, flush_buf
     torch.cuda.empty_cache()
     return out
 
