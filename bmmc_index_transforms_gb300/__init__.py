@@ -93,10 +93,12 @@ def library_path() -> str:
 
 def bmmc_plan_ex(n: int, A_rows: Sequence[int], c: int, elem_size: int, mode: int = 0,
                  t_in: int = 0, t_out: int = 0, tile_bits: int = 0,
-                 alloc_scratch: bool = False, grid_blocks: int = 0, load_mode: int = 0) -> int:
+                 alloc_scratch: bool = False, grid_blocks: int = 0, load_mode: int = 0,
+                 block_order: int = 0, layout: int = 0) -> int:
     """Returns an opaque plan handle (int); free it with bmmc_plan_destroy."""
     h = ctypes.c_void_p()
-    opts = PlanOpts(mode, t_in, t_out, tile_bits, int(bool(alloc_scratch)), grid_blocks, load_mode)
+    opts = PlanOpts(mode, t_in, t_out, tile_bits, int(bool(alloc_scratch)), grid_blocks, load_mode,
+                    block_order, layout)
     _check(_capi.lib().bmmc_plan_ex(ctypes.byref(h), n, _rows(n, A_rows), int(c), elem_size,
                                     ctypes.byref(opts)), "bmmc_plan_ex")
     return int(h.value)
@@ -129,12 +131,13 @@ def bmmc_plan_factor(plan: int, which: int) -> list[int]:
 
 
 def bmmc_plan_tile(plan: int) -> tuple[list[int], list[int]]:
+    """(tile basis, block basis) of a single-pass plan, as F2^n vectors."""
     info = bmmc_plan_info(plan)
     basis = (ctypes.c_uint64 * 64)()
-    bits = (ctypes.c_int * 64)()
-    _check(_capi.lib().bmmc_plan_tile(plan, basis, bits), "bmmc_plan_tile")
+    blocks = (ctypes.c_uint64 * 64)()
+    _check(_capi.lib().bmmc_plan_tile(plan, basis, blocks), "bmmc_plan_tile")
     D = info["tile_bits"]
-    return [int(basis[i]) for i in range(D)], [int(bits[i]) for i in range(info["n"] - D)]
+    return [int(basis[i]) for i in range(D)], [int(blocks[i]) for i in range(info["n"] - D)]
 
 
 # --------------------------------------------------------------------------
@@ -240,10 +243,10 @@ class Plan:
 
     def __init__(self, A_rows: Sequence[int], c: int = 0, elem_size: int = 4, *, mode: int = 0,
                  t_in: int = 0, t_out: int = 0, tile_bits: int = 0, alloc_scratch: bool = False,
-                 grid_blocks: int = 0, load_mode: int = 0):
+                 grid_blocks: int = 0, load_mode: int = 0, block_order: int = 0, layout: int = 0):
         self.n = len(A_rows)
         self.handle = bmmc_plan_ex(self.n, A_rows, c, elem_size, mode, t_in, t_out, tile_bits,
-                                   alloc_scratch, grid_blocks, load_mode)
+                                   alloc_scratch, grid_blocks, load_mode, block_order, layout)
         self.elem_size = elem_size
 
     @property

@@ -42,7 +42,8 @@ MODE_TWO_FACTOR = 1
 class PlanOpts(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("t_in", ctypes.c_int), ("t_out", ctypes.c_int),
                 ("tile_bits", ctypes.c_int), ("alloc_scratch", ctypes.c_int),
-                ("grid_blocks", ctypes.c_int), ("load_mode", ctypes.c_int)]
+                ("grid_blocks", ctypes.c_int), ("load_mode", ctypes.c_int),
+                ("block_order", ctypes.c_int), ("layout", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -63,7 +64,7 @@ SIGNATURES = {
     "bmmc_plan_destroy": (ctypes.c_int, [vp]),
     "bmmc_plan_info": (ctypes.c_int, [vp, ctypes.POINTER(PlanInfo)]),
     "bmmc_plan_factor": (ctypes.c_int, [vp, ctypes.c_int, u64p]),
-    "bmmc_plan_tile": (ctypes.c_int, [vp, u64p, intp]),
+    "bmmc_plan_tile": (ctypes.c_int, [vp, u64p, u64p]),
     "bmmc_permute": (ctypes.c_int, [vp, vp, vp, vp]),
     "bmmc_permute_scratch": (ctypes.c_int, [vp, vp, vp, vp, vp]),
     "bmmc_permute_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),

@@ -81,7 +81,8 @@ bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows, uint64_t c, 
     if (opts) {
         if (opts->t_in < 0 || opts->t_in > 16 || opts->t_out < 0 || opts->t_out > 16 ||
             opts->tile_bits < 0 || opts->tile_bits > kMaxTileBits || opts->grid_blocks < 0 ||
-            opts->load_mode < 0 || opts->load_mode > 2)
+            opts->load_mode < 0 || opts->load_mode > 2 || opts->block_order < 0 || opts->block_order > 2 ||
+            opts->layout < 0 || opts->layout > 1)
             return BMMC_ERR_INVALID_ARG;
         if (opts->mode != BMMC_MODE_SINGLE_PASS && opts->mode != BMMC_MODE_TWO_FACTOR)
             return BMMC_ERR_INVALID_ARG;
@@ -90,6 +91,8 @@ bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows, uint64_t c, 
         req.tile_bits = opts->tile_bits;
         req.grid_blocks = opts->grid_blocks;
         req.load_mode = opts->load_mode;
+        req.block_order = opts->block_order;
+        req.layout = opts->layout;
         p->mode = opts->mode;
     }
     bmmc_status s = plan_pass(n, p->rows, p->inv, c, (int)elem, req, &p->main);
@@ -223,14 +226,14 @@ bmmc_status bmmc_plan_factor(bmmc_plan_t plan, int which, uint64_t* rows_out) {
     return BMMC_OK;
 }
 
-bmmc_status bmmc_plan_tile(bmmc_plan_t plan, uint64_t* tile_basis, int* block_bits) {
+bmmc_status bmmc_plan_tile(bmmc_plan_t plan, uint64_t* tile_basis, uint64_t* block_basis) {
     if (!plan) return BMMC_ERR_INVALID_ARG;
     const PassPlan& m = plan->main;
     if (m.kernel != KERNEL_TILED) return BMMC_ERR_INVALID_ARG;
     if (tile_basis)
         for (size_t i = 0; i < m.tile_basis.size(); ++i) tile_basis[i] = m.tile_basis[i];
-    if (block_bits)
-        for (size_t i = 0; i < m.block_bits.size(); ++i) block_bits[i] = m.block_bits[i];
+    if (block_basis)
+        for (size_t i = 0; i < m.block_basis.size(); ++i) block_basis[i] = m.block_basis[i];
     return BMMC_OK;
 }
 

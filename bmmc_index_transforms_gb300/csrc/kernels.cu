@@ -36,19 +36,28 @@ template <> struct ElemType<4> { using T = uint32_t; };
 template <> struct ElemType<8> { using T = uint2; };
 template <> struct ElemType<16> { using T = uint4; };
 
-// Streaming 16-byte load: read-only path, no L1 allocation (each byte is
-// read once).
+// Cache hints of the streaming loads and stores (compile-time; each byte
+// of the input is read once and each byte of the output written once).
+#ifndef BMMC_LD_QUALIFIERS
+#define BMMC_LD_QUALIFIERS ".nc.L1::no_allocate"
+#endif
+#ifndef BMMC_ST_QUALIFIERS
+#define BMMC_ST_QUALIFIERS ".cs"
+#endif
+
+// Streaming 16-byte load: read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global" BMMC_LD_QUALIFIERS ".v4.u32 {%0,%1,%2,%3}, [%4];"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
 }
 
-// Streaming 16-byte store (evict-first: nothing rereads the output).
+// Streaming 16-byte store (evict-first by default: nothing rereads the
+// output).
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+    asm volatile("st.global" BMMC_ST_QUALIFIERS ".v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
 }

@@ -251,6 +251,70 @@ static int simulate(int elem, int vb, int NT, int qpt, uint32_t chunks, const st
     return extra;
 }
 
+// Basis of the intersection of two subspaces of F2^n (n <= 40), by
+// Zassenhaus: reduce the rows (u | u), u in U, and (w | 0), w in W; the rows
+// whose left half vanishes carry a basis of U n W in their right half.
+static std::vector<uint64_t> intersect(int n, const std::vector<uint64_t>& U, const std::vector<uint64_t>& W) {
+    using u128 = unsigned __int128;
+    std::vector<u128> rows;
+    for (uint64_t u : U) rows.push_back(((u128)u << n) | u);
+    for (uint64_t w : W) rows.push_back((u128)w << n);
+    auto hb = [](u128 v) {
+        const uint64_t hi = (uint64_t)(v >> 64);
+        return hi ? 64 + highbit(hi) : highbit((uint64_t)v);
+    };
+    std::vector<u128> basis;
+    for (u128 r : rows) {
+        for (u128 b : basis)
+            if ((r >> hb(b)) & 1) r ^= b;
+        if (!r) continue;
+        const int p = hb(r);
+        for (u128& b : basis)
+            if ((b >> p) & 1) b ^= r;
+        basis.push_back(r);
+    }
+    std::vector<uint64_t> out;
+    const u128 right = ((u128)1 << n) - 1;
+    for (u128 b : basis)
+        if ((b >> n) == 0) out.push_back((uint64_t)(b & right));
+    return out;
+}
+
+// Block basis with locality on both sides.  Blocks with neighbouring indices
+// run at the same time, so the low block bits should move the input origin
+// and the output origin as little as possible: for growing windows X_m (the
+// low m index bits), the vectors of (X_m + T) n (A^-1 X_m + T) that are new
+// modulo T and the vectors already taken come next (input and output both
+// inside a 2^m-element window modulo the tile).  Representatives are reduced
+// against T, so they have no low input bits.
+static std::vector<uint64_t> local_block_basis(int n, const uint64_t* inv, const std::vector<uint64_t>& tb) {
+    Echelon TC;
+    for (uint64_t x : tb) TC.insert(x);
+    const int want = n - (int)tb.size();
+    std::vector<uint64_t> chosen;
+    for (int m = 1; m <= n && (int)chosen.size() < want; ++m) {
+        std::vector<uint64_t> U1(tb), U2(tb);
+        for (int j = 0; j < m; ++j) {
+            U1.push_back(1ull << j);
+            U2.push_back(column(n, inv, j));
+        }
+        Echelon fresh;
+        for (uint64_t v : intersect(n, U1, U2)) {
+            const uint64_t r = TC.reduce(v);
+            if (r) fresh.insert(r);
+        }
+        std::vector<uint64_t> add = fresh.vec;
+        std::sort(add.begin(), add.end(), [](uint64_t a, uint64_t b) { return highbit(a) < highbit(b); });
+        for (uint64_t v : add) {
+            const uint64_t r = TC.reduce(v);
+            if (!r) continue;
+            TC.insert(r);
+            chosen.push_back(r);
+        }
+    }
+    return chosen;
+}
+
 bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t c, int elem,
                       const PlanRequest& req, PassPlan* out) {
     PassPlan P;
@@ -300,10 +364,32 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     std::vector<uint64_t> tb;
     for (int i = 0; i < t_in; ++i) tb.push_back(1ull << i);
     for (uint64_t v : Vs) tb.push_back(v);
-    // Block bits: neither low nor a row pivot.
-    std::vector<int> C;
-    for (int p = t_in; p < n; ++p)
-        if (!((V.pivots >> p) & 1ull)) C.push_back(p);
+    // Block basis: n - D vectors completing T to F2^n; block b's input origin
+    // is the XOR of the vectors selected by the bits of b.
+    std::vector<uint64_t> C;
+    if (req.block_order == 1) {
+        C = local_block_basis(n, inv, tb);
+    } else if (req.block_order == 2) {
+        // output coordinate bits that are neither low output bits nor output
+        // row pivots, ascending, pulled back through A^-1 and reduced modulo
+        // the tile: blocks that run together write neighbouring output runs
+        Echelon Wp;
+        for (uint64_t x : tb) Wp.insert(matvec_rows(n, rows, x) & ~lowmask(t_out));
+        Echelon TC;
+        for (uint64_t x : tb) TC.insert(x);
+        for (int q = t_out; q < n; ++q) {
+            if ((Wp.pivots >> q) & 1ull) continue;
+            const uint64_t r = TC.reduce(column(n, inv, q));
+            if (!r) return BMMC_ERR_INTERNAL;
+            TC.insert(r);
+            C.push_back(r);
+        }
+    } else {
+        // coordinate bits that are neither low bits nor row pivots, ascending:
+        // blocks that run together read neighbouring input runs
+        for (int p = t_in; p < n; ++p)
+            if (!((V.pivots >> p) & 1ull)) C.push_back(1ull << p);
+    }
     if ((int)C.size() != n - D || (int)C.size() > kMaxBlockBits) return BMMC_ERR_INTERNAL;
 
     // Output rows: A T reduced modulo L_out.
@@ -334,10 +420,10 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     const int eb = ilog2(elem);       // byte shift of one element
 
     LayoutChoice best;
-    // Vector layout: each input vector stays whole in shared memory (one
+    // Vector layout (unless the per-element layout is requested): each input vector stays whole in shared memory (one
     // 16-byte store); the gather lanes are chosen among the output bits so
     // that their sources cover every bank.
-    if (elem < 16 && cb >= bw) {
+    if (elem < 16 && cb >= bw && req.layout != 1) {
         const int extra = bw - 3;  // gather lane bits beyond the three that keep 128-byte store segments
         std::vector<int> cand;
         for (int w = vb + 3; w < D; ++w) cand.push_back(w);
@@ -421,8 +507,8 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     tp.n_tiles = 1ull << (n - D);
     tp.chunks = chunks;
     for (size_t i = 0; i < C.size(); ++i) {
-        tp.col_in[i] = 1ull << C[i];
-        tp.col_out[i] = matvec_rows(n, rows, 1ull << C[i]);
+        tp.col_in[i] = C[i];
+        tp.col_out[i] = matvec_rows(n, rows, C[i]);
     }
     for (int j = 0; j < D; ++j) tp.gam[j] = (uint32_t)gamu[j];
     for (int k = 0; k < tbits && k < cb; ++k) {
@@ -465,7 +551,7 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     P.bank_conflicts = best.conflicts;
     P.tiles = tp.n_tiles;
     P.tile_basis = tb;
-    P.block_bits = C;
+    P.block_basis = C;
     *out = P;
     return BMMC_OK;
 }

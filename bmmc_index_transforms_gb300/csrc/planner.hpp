@@ -32,13 +32,15 @@ struct PassPlan {
     TiledParams tp{};
     NaiveParams np{};
     std::vector<uint64_t> tile_basis;  // tile_bits vectors of F2^n
-    std::vector<int> block_bits;       // n - tile_bits input bit positions
+    std::vector<uint64_t> block_basis; // n - tile_bits input-origin vectors of the block bits
 };
 
 struct PlanRequest {
     int t_in = 0, t_out = 0, tile_bits = 0;  // 0 = default
     int grid_blocks = 0;                     // 0 = default
     int load_mode = 0;                       // 0 default, 1 async copies, 2 through registers
+    int block_order = 0;                     // 0 input coordinate bits ascending, 1 local on both sides
+    int layout = 0;                          // 0 automatic, 1 per-element stores
 };
 
 // Build one pass for (rows, c).  inv must be rows' inverse.

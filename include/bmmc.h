@@ -98,6 +98,14 @@ typedef struct {
                             copies straight into shared memory (layouts that keep input
                             vectors whole, 4-16 chunks per thread), 2 = loads through
                             registers */
+    int block_order;     /* which tiles neighbouring blocks take: 0 = default (input
+                            coordinate bits ascending: blocks that run together read
+                            neighbouring input runs), 1 = blocks that run together stay
+                            in small windows of both the input and the output, 2 = output
+                            coordinate bits ascending (neighbouring output runs) */
+    int layout;          /* shared-memory layout: 0 = automatic (input vectors stored
+                            whole when a conflict-free gather exists), 1 = per-element
+                            stores */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;
@@ -152,9 +160,10 @@ bmmc_status bmmc_plan_factor(bmmc_plan_t plan, int which, uint64_t *rows_out);
 
 /* Input tile of the single-pass plan, for inspection: tile_basis receives
  * tile_bits vectors in F2^n (the low t_in unit vectors first, then the
- * extra row vectors), block_bits receives the n - tile_bits input bit
- * positions that select the tile.  Either pointer may be NULL. */
-bmmc_status bmmc_plan_tile(bmmc_plan_t plan, uint64_t *tile_basis, int *block_bits);
+ * extra row vectors), block_basis receives n - tile_bits vectors: block b
+ * reads the tile whose input origin is the XOR of block_basis[i] over the
+ * set bits i of b.  Either pointer may be NULL. */
+bmmc_status bmmc_plan_tile(bmmc_plan_t plan, uint64_t *tile_basis, uint64_t *block_basis);
 
 /* Permute: out[A.x XOR c] = in[x].  in, out: device pointers of
  * 2^n * elem_size bytes each, 16-byte aligned, not overlapping.

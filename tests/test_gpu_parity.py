@@ -464,3 +464,52 @@ def test_parm_lowering_on_gpu(bm, n, mask):
         p.permute(mid2, out)
     t.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), want)
+
+
+def test_fuzz_plan_options(bm):
+    """Seeded random combinations of size, element size, run lengths, tile
+    size, grid and input path, against the oracle."""
+    rng = np.random.default_rng(2024)
+    done = 0
+    for trial in range(150):
+        elem = int(rng.choice([4, 8, 16]))
+        vb = {4: 2, 8: 1, 16: 0}[elem]
+        n = int(rng.integers(max(1, vb), 17))
+        t_in = int(rng.integers(vb, 9))
+        t_out = int(rng.integers(vb, 9))
+        D = int(rng.choice([0, 0, int(rng.integers(1, 15))]))
+        grid = int(rng.choice([0, 0, 1, 3, 17]))
+        load_mode = int(rng.choice([0, 1, 2]))
+        kind = rng.random()
+        if kind < 0.6:
+            rows, c = _random(int(rng.integers(0, 1 << 30)), n)
+        elif kind < 0.8:
+            perm = [int(v) for v in rng.permutation(n)]
+            rows, c = [1 << p for p in perm], int(rng.integers(0, 1 << n))
+        else:
+            rows, c = ref.identity_rows(n), int(rng.integers(0, 1 << n))
+        arr = synth.fill_int(n, elem)
+        try:
+            got, info = _run(bm, rows, c, arr, t_in=t_in, t_out=t_out, tile_bits=D, grid_blocks=grid,
+                             load_mode=load_mode)
+        except bm.BmmcError as e:
+            assert e.status == 1, (n, elem, t_in, t_out, D)  # only oversized tiles may be refused
+            continue
+        assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), (n, elem, t_in, t_out, D, grid,
+                                                                              load_mode, info)
+        done += 1
+    assert done >= 100
+
+
+@pytest.mark.parametrize("block_order", [1, 2])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_block_orders_and_layouts(bm, block_order, layout):
+    """The non-default block orders and the forced per-element layout give the
+    oracle's bytes (random, bit-reversal and complement maps)."""
+    for n, elem in [(20, 4), (19, 8), (18, 16)]:
+        arr = synth.fill_int(n, elem)
+        for rows, c in [_random(n * 5 + block_order, n), (ref.bitrev_rows(n), 3), (ref.identity_rows(n), 0x5555)]:
+            got, info = _run(bm, rows, c, arr, block_order=block_order, layout=layout)
+            assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), (n, elem, info)
+            if layout == 1 and elem < 16:
+                assert info["vector_stores"] == 0
