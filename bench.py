@@ -175,7 +175,7 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # CPU oracle (the baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_gbs(sample_log2: int, seed: int, threads: int, x_offset: int = 0):
+def oracle_sample_gbs(sample_log2: int, seed: int, threads: int, x_offset: int = 0, n_bits: int = N_BITS):
     """Time the CPU oracle (as it stands) scattering a contiguous sample of
     2^sample_log2 source indices of the n = 28 workload for one seed."""
     import numpy as np
@@ -184,18 +184,20 @@ def oracle_sample_gbs(sample_log2: int, seed: int, threads: int, x_offset: int =
     from oracle import reference as ref
     from bmmc_index_transforms_gb300 import synth
 
-    rows, c, _ = synth.draw_bmmc(seed, N_BITS, lambda r: ref.f2_rank(N_BITS, r) == N_BITS)
+    rows, c, _ = synth.draw_bmmc(seed, n_bits, lambda r: ref.f2_rank(n_bits, r) == n_bits)
     global _ORACLE_BUFS
     try:
         inp, out = _ORACLE_BUFS
+        assert inp.shape[0] == 1 << n_bits
     except NameError:
-        inp = np.arange(1 << N_BITS, dtype=np.uint32)
+        inp = np.arange(1 << n_bits, dtype=np.uint32)
         out = np.empty_like(inp)
+        out.fill(0)  # touch every page now, so the timed scatter takes no first-touch faults
         _ORACLE_BUFS = (inp, out)
-    lo = x_offset % (1 << N_BITS)
-    hi = min(1 << N_BITS, lo + (1 << sample_log2))
+    lo = x_offset % (1 << n_bits)
+    hi = min(1 << n_bits, lo + (1 << sample_log2))
     t0 = time.perf_counter()
-    oracle.scatter(N_BITS, rows, c, inp, out, threads=threads, x_range=(lo, hi))
+    oracle.scatter(n_bits, rows, c, inp, out, threads=threads, x_range=(lo, hi))
     dt = time.perf_counter() - t0
     return 2.0 * (hi - lo) * ELEM / dt / 1e9, dt, hi - lo
 
@@ -208,17 +210,18 @@ def run_reference(args):
 
     threads = oracle.host_threads()
     total = args.warmup + args.steps
-    sample_log2 = 23 if total <= 60 else 22 if total <= 200 else 20
+    sample_log2 = args.ref_sample_log2 or (23 if total <= 60 else 22 if total <= 200 else 20)
     vals = []
     t_all = 0.0
     for s in range(total):
-        gbs, dt, cnt = oracle_sample_gbs(sample_log2, s % SEEDS, threads, x_offset=s << sample_log2)
+        gbs, dt, cnt = oracle_sample_gbs(sample_log2, s % SEEDS, threads, x_offset=s << sample_log2,
+                                         n_bits=args.ref_n)
         if s >= args.warmup:
             vals.append((cnt, dt))
             t_all += dt
     moved = sum(2.0 * cnt * ELEM for cnt, _ in vals)
     value = moved / t_all / 1e9
-    sample = (f"per step 2^{sample_log2} consecutive source indices of one seed's n=28 int32 "
+    sample = (f"per step 2^{sample_log2} consecutive source indices of one seed's n={args.ref_n} int32 "
               f"permutation (seed = step mod 32), plain C oracle loop split over {threads} host threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
@@ -575,6 +578,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the other configurations")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--ref-n", type=int, default=N_BITS,
+                    help="reference arm: n of the workload (default the benchmark's 28; smaller only for smoke tests)")
+    ap.add_argument("--ref-sample-log2", type=int, default=0,
+                    help="reference arm: log2 source indices per step (0 = sized to the step count)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -52,7 +52,7 @@ def test_replicas_take_max_time_and_sum_bytes():
 def test_reference_arm_line():
     env = dict(os.environ, PYTHONPATH=ROOT)
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                          "--warmup", "3"], capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+                          "--warmup", "3", "--ref-sample-log2", "16", "--ref-n", "20"], capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference"
