@@ -24,7 +24,7 @@ __all__ = [
     "BmmcError", "Plan", "bmmc_plan", "bmmc_plan_ex", "bmmc_plan_destroy", "bmmc_plan_info",
     "bmmc_plan_factor", "bmmc_plan_tile", "bmmc_permute", "bmmc_permute_scratch",
     "bmmc_permute_host", "bmmc_permute_static_scratch", "transpose2d", "bpc_permute", "bmmc_dims_permute",
-    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "bmmc_parm_rows", "bmmc_inverse_rows",
+    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "bmmc_parm_rows", "bmmc_inverse_rows", "bmmc_compose",
     "bmmc_status_string", "bmmc_version", "library_path",
 ]
 
@@ -94,11 +94,11 @@ def library_path() -> str:
 def bmmc_plan_ex(n: int, A_rows: Sequence[int], c: int, elem_size: int, mode: int = 0,
                  t_in: int = 0, t_out: int = 0, tile_bits: int = 0,
                  alloc_scratch: bool = False, grid_blocks: int = 0, load_mode: int = 0,
-                 block_order: int = 0, layout: int = 0) -> int:
+                 block_order: int = 0, layout: int = 0, gather: bool = False, batch_log2: int = 0) -> int:
     """Returns an opaque plan handle (int); free it with bmmc_plan_destroy."""
     h = ctypes.c_void_p()
     opts = PlanOpts(mode, t_in, t_out, tile_bits, int(bool(alloc_scratch)), grid_blocks, load_mode,
-                    block_order, layout)
+                    block_order, layout, int(bool(gather)), batch_log2)
     _check(_capi.lib().bmmc_plan_ex(ctypes.byref(h), n, _rows(n, A_rows), int(c), elem_size,
                                     ctypes.byref(opts)), "bmmc_plan_ex")
     return int(h.value)
@@ -226,6 +226,17 @@ def bmmc_inverse_rows(A_rows: Sequence[int]) -> list[int]:
     return [int(out[i]) for i in range(n)]
 
 
+def bmmc_compose(second: tuple, first: tuple) -> tuple[list[int], int]:
+    """(A2, c2) after (A1, c1) as one permutation: (A2.A1, A2.c1 ^ c2)."""
+    (A2, c2), (A1, c1) = second, first
+    n = len(A1)
+    out = (ctypes.c_uint64 * 64)()
+    oc = ctypes.c_uint64(0)
+    _check(_capi.lib().bmmc_compose(n, _rows(n, A2), int(c2), _rows(n, A1), int(c1), out, ctypes.byref(oc)),
+           "bmmc_compose")
+    return [int(out[i]) for i in range(n)], int(oc.value)
+
+
 def bmmc_parm_rows(n: int, mask: int) -> list[int]:
     rows = (ctypes.c_uint64 * 64)()
     _check(_capi.lib().bmmc_parm_rows(n, int(mask), rows), "bmmc_parm_rows")
@@ -243,10 +254,12 @@ class Plan:
 
     def __init__(self, A_rows: Sequence[int], c: int = 0, elem_size: int = 4, *, mode: int = 0,
                  t_in: int = 0, t_out: int = 0, tile_bits: int = 0, alloc_scratch: bool = False,
-                 grid_blocks: int = 0, load_mode: int = 0, block_order: int = 0, layout: int = 0):
+                 grid_blocks: int = 0, load_mode: int = 0, block_order: int = 0, layout: int = 0,
+                 gather: bool = False, batch_log2: int = 0):
         self.n = len(A_rows)
         self.handle = bmmc_plan_ex(self.n, A_rows, c, elem_size, mode, t_in, t_out, tile_bits,
-                                   alloc_scratch, grid_blocks, load_mode, block_order, layout)
+                                   alloc_scratch, grid_blocks, load_mode, block_order, layout, gather,
+                                   batch_log2)
         self.elem_size = elem_size
 
     @property

@@ -43,7 +43,8 @@ class PlanOpts(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("t_in", ctypes.c_int), ("t_out", ctypes.c_int),
                 ("tile_bits", ctypes.c_int), ("alloc_scratch", ctypes.c_int),
                 ("grid_blocks", ctypes.c_int), ("load_mode", ctypes.c_int),
-                ("block_order", ctypes.c_int), ("layout", ctypes.c_int)]
+                ("block_order", ctypes.c_int), ("layout", ctypes.c_int), ("gather", ctypes.c_int),
+                ("batch_log2", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -80,6 +81,7 @@ SIGNATURES = {
                                      u64p]),
     "bmmc_parm_rows": (ctypes.c_int, [ctypes.c_int, u64, u64p]),
     "bmmc_inverse_rows": (ctypes.c_int, [ctypes.c_int, u64p, u64p]),
+    "bmmc_compose": (ctypes.c_int, [ctypes.c_int, u64p, u64, u64p, u64, u64p, u64p]),
     "bmmc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bmmc_version": (ctypes.c_int, []),
 }

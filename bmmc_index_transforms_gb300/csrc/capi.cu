@@ -69,8 +69,27 @@ bmmc_status check_buffers(const void* in, const void* out, size_t bytes) {
 
 bmmc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BMMC_OK : BMMC_ERR_CUDA; }
 
-bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows, uint64_t c, size_t elem,
+bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows_in, uint64_t c, size_t elem,
                        const bmmc_plan_opts* opts) {
+    uint64_t rows[64];
+    for (int i = 0; i < n; ++i) rows[i] = rows_in[i];
+    if (opts && (opts->gather < 0 || opts->gather > 1 || opts->batch_log2 < 0 || opts->batch_log2 > kMaxN))
+        return BMMC_ERR_INVALID_ARG;
+    if (opts && opts->gather) {
+        // out[y] = in[A y + c]  <=>  out[A^-1 (x + c)] = in[x]: scatter by (A^-1, A^-1 c)
+        uint64_t inv[64];
+        if (!inverse_rows(n, rows, inv)) return BMMC_ERR_SINGULAR;
+        c = matvec_rows(n, inv, c);
+        for (int i = 0; i < n; ++i) rows[i] = inv[i];
+    }
+    if (opts && opts->batch_log2) {
+        // 2^b arrays one after another: the batch index is the high b bits,
+        // left unchanged
+        const int b = opts->batch_log2;
+        if (n + b > kMaxN) return BMMC_ERR_INVALID_ARG;
+        for (int i = n; i < n + b; ++i) rows[i] = 1ull << i;
+        n += b;
+    }
     p->n = n;
     p->elem = (int)elem;
     p->c = c;
@@ -387,6 +406,19 @@ bmmc_status bmmc_lmad_copy(int ndims, const int* dims_log2, int64_t in_offset, c
     int n = 0;
     for (int k = 0; k < ndims; ++k) n += dims_log2[k];
     return bpc_permute(n, perm, c, elem_size, in, out, stream);
+}
+
+bmmc_status bmmc_compose(int n, const uint64_t* A2_rows, uint64_t c2, const uint64_t* A1_rows, uint64_t c1,
+                         uint64_t* out_rows, uint64_t* out_c) {
+    if (!out_rows || !out_c) return BMMC_ERR_INVALID_ARG;
+    bmmc_status s = check_matrix(n, A2_rows, c2);
+    if (s == BMMC_OK) s = check_matrix(n, A1_rows, c1);
+    if (s != BMMC_OK) return s;
+    uint64_t prod[64];
+    matmul_rows(n, A2_rows, A1_rows, prod);
+    *out_c = matvec_rows(n, A2_rows, c1) ^ c2;
+    for (int i = 0; i < n; ++i) out_rows[i] = prod[i];
+    return BMMC_OK;
 }
 
 bmmc_status bmmc_inverse_rows(int n, const uint64_t* A_rows, uint64_t* inv_rows_out) {

@@ -106,6 +106,14 @@ typedef struct {
     int layout;          /* shared-memory layout: 0 = automatic (input vectors stored
                             whole when a conflict-free gather exists), 1 = per-element
                             stores */
+    int gather;          /* 0 = scatter, out[A.x XOR c] = in[x] (default); 1 = gather,
+                            out[y] = in[A.y XOR c] (the convention of the introduction's
+                            bit-reverse example), run as the scatter by
+                            (A^-1, A^-1.c) */
+    int batch_log2;      /* 0 = one array; b > 0 = 2^b independent arrays of 2^n elements
+                            stored one after another, each permuted by (A, c) in one
+                            launch (the map on n + b bits is A on the low n bits and the
+                            identity on the b high bits); n + b <= 40 */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;
@@ -270,6 +278,12 @@ bmmc_status bmmc_lmad_bpc(int ndims, const int *dims_log2, int64_t in_offset,
  * inv_rows_out receives A^-1, so permuting by (A^-1, A^-1.c) undoes (A, c).
  * Errors: INVALID_ARG, SINGULAR.  Host only. */
 bmmc_status bmmc_inverse_rows(int n, const uint64_t *A_rows, uint64_t *inv_rows_out);
+
+/* Composition: permuting by (A1, c1) and then by (A2, c2) is the single
+ * permutation (A2.A1, A2.c1 XOR c2), so two passes fuse into one.
+ * out_rows may alias neither input.  Errors: INVALID_ARG.  Host only. */
+bmmc_status bmmc_compose(int n, const uint64_t *A2_rows, uint64_t c2, const uint64_t *A1_rows,
+                         uint64_t c1, uint64_t *out_rows, uint64_t *out_c);
 
 /* The parm combinator of "Efficient GPU Implementation of Affine Index
  * Permutations on Arrays" (introduction: parm mask f xs splits xs by the F2

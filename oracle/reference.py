@@ -45,6 +45,7 @@ __all__ = [
     "rotate_rows",
     "axes_permute_bits",
     "r2_tiled",
+    "bmmc_gather",
     "lmad_copy",
     "parm",
 ]
@@ -104,6 +105,15 @@ def bmmc_permute(n: int, rows, c: int, arr: np.ndarray) -> np.ndarray:
     out = np.empty_like(arr)
     out[ys.astype(np.int64)] = arr
     return out
+
+
+def bmmc_gather(n: int, rows, c: int, arr: np.ndarray) -> np.ndarray:
+    """Gather convention: out[y] = in[A.y (+) c] for every y (the
+    introduction's motivating kernel reads input[bit-rev(i)])."""
+    N = 1 << n
+    arr = np.asarray(arr)
+    src = bmmc_index_array(n, rows, c, np.arange(N, dtype=np.uint64))
+    return arr[src.astype(np.int64)]
 
 
 # ---------------------------------------------------------------------------

@@ -392,3 +392,25 @@ def test_inverse_rows_brute_force(n):
         inv = bm.bmmc_inverse_rows(A)
         for x in range(1 << n):
             assert ref.bmmc_index(n, inv, 0, ref.bmmc_index(n, A, 0, x)) == x
+
+
+
+def test_compose_matches_oracle():
+    for seed in range(6):
+        n = 6 + seed * 5
+        A1, c1 = _random(seed, n)
+        A2, c2 = _random(seed + 50, n)
+        assert bm.bmmc_compose((A2, c2), (A1, c1)) == tuple(ref.compose(n, (A2, c2), (A1, c1)))
+    with pytest.raises(bm.BmmcError):
+        bm.bmmc_compose(([1, 2, 4 | 8], 0), ([1, 2, 4], 0))
+
+
+def test_batched_and_gather_plans():
+    n = 12
+    A, c = _random(4, n)
+    with bm.Plan(A, c, 4, batch_log2=5) as p:
+        assert p.info["n"] == n + 5
+    with bm.Plan(A, c, 4, gather=True) as p:
+        assert p.info["c"] == ref.bmmc_index(n, ref.f2_inverse(n, A), 0, c)
+    with pytest.raises(bm.BmmcError):
+        bm.Plan(A, c, 4, batch_log2=40 - n + 1)

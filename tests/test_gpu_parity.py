@@ -513,3 +513,31 @@ def test_block_orders_and_layouts(bm, block_order, layout):
             assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), (n, elem, info)
             if layout == 1 and elem < 16:
                 assert info["vector_stores"] == 0
+
+
+
+@pytest.mark.parametrize("elem", [4, 8, 16])
+def test_gather_and_batched_plans(bm, elem):
+    """gather=True gives out[y] = in[A.y ^ c]; batch_log2 = b permutes 2^b
+    arrays stored one after another, each by (A, c); composition fuses two
+    permutations into one pass."""
+    n = 14
+    A, c = _random(21 + elem, n)
+    arr = synth.fill_int(n, elem)
+    got, _ = _run(bm, A, c, arr, gather=True)
+    assert got.tobytes() == ref.bmmc_gather(n, A, c, arr).tobytes()
+    b = 4
+    big = synth.fill_int(n + b, elem)
+    d_in = _dev(big)
+    d_out = torch.zeros_like(d_in)
+    with bm.Plan(A, c, elem, batch_log2=b) as p:
+        p.permute(d_in, d_out)
+    torch.cuda.synchronize()
+    got = _host(d_out, big)
+    per = big.reshape((1 << b, 1 << n) + big.shape[1:])
+    want = np.concatenate([oracle.scatter(n, A, c, np.ascontiguousarray(per[k])) for k in range(1 << b)])
+    assert got.tobytes() == want.tobytes()
+    A2, c2 = _random(77 + elem, n)
+    Af, cf = bm.bmmc_compose((A2, c2), (A, c))
+    got, _ = _run(bm, Af, cf, arr)
+    assert got.tobytes() == ref.bmmc_permute(n, A2, c2, ref.bmmc_permute(n, A, c, arr)).tobytes()

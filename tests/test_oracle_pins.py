@@ -290,3 +290,20 @@ def test_parm_pins():
     assert ref.parm(0b11, rev, list("abcd")) == list("dcba")  # parts {0,3}, {1,2}
     even_odd = ref.parm(1, rev, xs)
     assert even_odd[0::2] == list("geca") and even_odd[1::2] == list("hfdb")
+
+
+def test_gather_convention_pins():
+    """The introduction's kernel reads input[bit-rev(n, i)] into output[i]:
+    with bit-rev(4,7) = 14, output[7] is input[14]; gather by A equals
+    scatter by A^-1 (argsort of the forward map)."""
+    n = 4
+    arr = np.arange(16) * 10
+    out = ref.bmmc_gather(n, ref.bitrev_rows(n), 0, arr)
+    assert out[7] == arr[14] and out[14] == arr[7]
+    A, c = _random_invertible(9, 10)
+    arr = np.arange(1 << 10, dtype=np.uint32)
+    fwd = ref.bmmc_index_array(10, A, c, np.arange(1 << 10, dtype=np.uint64)).astype(np.int64)
+    assert np.array_equal(ref.bmmc_gather(10, A, c, arr), arr[fwd])
+    inv_perm = np.argsort(fwd)
+    scat = ref.bmmc_permute(10, A, c, arr)
+    assert np.array_equal(scat, arr[inv_perm])
