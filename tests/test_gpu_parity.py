@@ -541,3 +541,71 @@ def test_gather_and_batched_plans(bm, elem):
     Af, cf = bm.bmmc_compose((A2, c2), (A, c))
     got, _ = _run(bm, Af, cf, arr)
     assert got.tobytes() == ref.bmmc_permute(n, A2, c2, ref.bmmc_permute(n, A, c, arr)).tobytes()
+
+
+def test_cuda_graph_capture_and_replay(bm):
+    """Permutes enqueue only kernel launches (no allocation, no host
+    synchronisation), so a sequence of them can be captured in a CUDA graph
+    and replayed; every replay gives the oracle's bytes."""
+    n, elem = 18, 4
+    arr = synth.fill_int(n, elem)
+    d_in = _dev(arr)
+    mids = [torch.zeros_like(d_in) for _ in range(3)]
+    plans = [bm.Plan(*_random(300 + k, n), elem) for k in range(3)]
+    for p, m in zip(plans, mids):  # first calls outside capture: per-device set-up
+        p.permute(d_in, m)
+    torch.cuda.synchronize()
+    for m in mids:
+        m.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plans[0].permute(d_in, mids[0])
+        plans[1].permute(mids[0], mids[1])
+        plans[2].permute(mids[1], mids[2])
+    for _ in range(2):
+        for m in mids:
+            m.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        want = arr
+        for k in range(3):
+            rows, c = _random(300 + k, n)
+            want = oracle.scatter(n, rows, c, want)
+            assert _host(mids[k], arr).tobytes() == want.tobytes()
+    for p in plans:
+        p.close()
+
+
+def test_pageable_host_memory_when_the_device_can_reach_it(bm):
+    """On a device with pageable-memory access (GB300 with Grace: the GPU
+    reaches ordinary host memory), the kernel permutes plain numpy arrays in
+    place of device buffers; elsewhere such pointers are rejected before any
+    launch."""
+    from bmmc_index_transforms_gb300 import _capi
+
+    dev = torch.cuda.current_device()
+    pageable = torch.cuda.get_device_properties(dev)  # noqa: F841 (device is initialised)
+    import ctypes
+
+    cudart = None
+    for name in ("libcudart.so", "libcudart.so.13", "libcudart.so.12"):
+        try:
+            cudart = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    n, elem = 16, 4
+    A, c = _random(5, n)
+    arr = synth.fill_int(n, elem)
+    out = np.zeros_like(arr)
+    attr = ctypes.c_int(0)
+    if cudart is not None:
+        cudart.cudaDeviceGetAttribute(ctypes.byref(attr), 88, dev)  # cudaDevAttrPageableMemoryAccess
+    with bm.Plan(A, c, elem) as p:
+        st = _capi.lib().bmmc_permute(p.handle, arr.ctypes.data, out.ctypes.data, None)
+        if attr.value:
+            assert st == 0
+            torch.cuda.synchronize()
+            assert out.tobytes() == oracle.scatter(n, A, c, arr).tobytes()
+        else:
+            assert st == _capi.ERR_INVALID_ARG
