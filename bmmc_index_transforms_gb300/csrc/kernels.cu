@@ -98,6 +98,54 @@ __device__ __forceinline__ uint64_t warp_xor<uint64_t>(uint64_t v) {
 __device__ __forceinline__ void opaque(uint32_t& v) { asm volatile("" : "+r"(v)); }
 __device__ __forceinline__ void opaque(uint64_t& v) { asm volatile("" : "+l"(v)); }
 
+// Per-thread state shared by the tiled kernels: the byte offsets owned by
+// this thread (the bits of its chunk index that come from threadIdx.x; the
+// iteration and element bits come from the uniform tables), and the lane's
+// column of the tile-index -> origin map.
+template <int ELEM, int NT, typename OFF>
+struct TileThread {
+    static constexpr int EB = ELEM == 4 ? 2 : ELEM == 8 ? 3 : 4;
+    OFF in_t = 0, out_t = 0;   // input / output byte offset of the thread's chunk
+    uint32_t ph_t = 0, ga_t = 0;  // shared-memory byte offset it stores to / gathers from
+    OFF my_cin = 0;            // input origin (bytes) of block bit `lane`
+    uint64_t my_cout = 0;      // raw output origin (elements) of block bit `lane`
+    uint32_t my_gl = 0;        // shared-memory realignment (bytes) of output-run bit `lane`
+    uint64_t lowm = 0;         // mask of the output-run bits
+    uint32_t lane = 0;
+
+    __device__ __forceinline__ TileThread(const TiledParams& p, uint32_t tid) {
+        lane = tid & 31u;
+#pragma unroll
+        for (int k = 0; k < kMaxThreadBits; ++k) {
+            if ((1 << k) < NT && ((tid >> k) & 1u)) {
+                in_t ^= (OFF)p.tid_in[k];
+                out_t ^= (OFF)p.tid_out[k];
+                ph_t ^= p.tid_phi[k];
+                ga_t ^= p.tid_gam[k];
+            }
+        }
+        if ((int)lane < p.n_block_bits) {
+            my_cin = (OFF)(p.col_in[lane] << EB);
+            my_cout = p.col_out[lane];
+        }
+        if ((int)lane < p.t_out) my_gl = p.gam[lane] << EB;
+        lowm = (1ull << p.t_out) - 1ull;
+    }
+
+    // Byte origins of tile b: input origin ib, output run origin ob, and the
+    // shared-memory offset g that realigns output run positions with the
+    // tile.  Evaluated by warp XOR reductions (all 32 lanes must take part).
+    __device__ __forceinline__ void tile_bases(const TiledParams& p, uint64_t b, OFF& ib, OFF& ob,
+                                               uint32_t& g) const {
+        const bool bit = (b >> lane) & 1ull;
+        ib = warp_xor<OFF>(bit ? my_cin : (OFF)0);
+        const uint64_t raw = warp_xor64(bit ? my_cout : 0ull) ^ p.c;
+        ob = (OFF)((raw & ~lowm) << EB);
+        const uint32_t delta = (uint32_t)(raw & lowm);
+        g = __reduce_xor_sync(0xffffffffu, ((delta >> lane) & 1u) ? my_gl : 0u);
+    }
+};
+
 // Blocks per SM the register budget is sized for: enough 16-byte loads in
 // flight per SM to cover HBM latency, without spilling.
 template <int NT, int QPT, bool WIDE>
@@ -117,58 +165,22 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
                       uint4* __restrict__ out) {
     using T = typename ElemType<ELEM>::T;
     constexpr int VEC = 16 / ELEM;
-    constexpr int EB = ELEM == 4 ? 2 : ELEM == 8 ? 3 : 4;
     extern __shared__ uint4 smem_raw[];
     unsigned char* tile = reinterpret_cast<unsigned char*>(smem_raw);
     const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
     unsigned char* dst = reinterpret_cast<unsigned char*>(out);
 
     const uint32_t tid = threadIdx.x;
-    const uint32_t lane = tid & 31u;
-
-    // Offsets owned by this thread (the bits of its chunk index that come
-    // from threadIdx.x), all in bytes; the iteration and element bits come
-    // from the uniform tables.
-    OFF in_t = 0, out_t = 0;
-    uint32_t ph_t = 0, ga_t = 0;
-#pragma unroll
-    for (int k = 0; k < kMaxThreadBits; ++k) {
-        if ((1 << k) < NT && ((tid >> k) & 1u)) {
-            in_t ^= (OFF)p.tid_in[k];
-            out_t ^= (OFF)p.tid_out[k];
-            ph_t ^= p.tid_phi[k];
-            ga_t ^= p.tid_gam[k];
-        }
-    }
-    OFF my_cin = 0;
-    uint64_t my_cout = 0;
-    if ((int)lane < p.n_block_bits) {
-        my_cin = (OFF)(p.col_in[lane] << EB);
-        my_cout = p.col_out[lane];
-    }
-    uint32_t my_gl = 0;
-    if ((int)lane < p.t_out) my_gl = p.gam[lane] << EB;
-    const uint64_t lowm = (1ull << p.t_out) - 1ull;
-
+    const TileThread<ELEM, NT, OFF> th(p, tid);
     bool act[QPT];
 #pragma unroll
     for (int i = 0; i < QPT; ++i) act[i] = tid + (uint32_t)i * NT < p.chunks;
-
-    // Byte origins of tile b: input origin ib, output run origin ob, and the
-    // shared-memory offset g that realigns output run positions with the tile.
-    auto tile_bases = [&](uint64_t b, OFF& ib, OFF& ob, uint32_t& g) {
-        const bool bit = (b >> lane) & 1ull;
-        ib = warp_xor<OFF>(bit ? my_cin : (OFF)0);
-        const uint64_t raw = warp_xor64(bit ? my_cout : 0ull) ^ p.c;
-        ob = (OFF)((raw & ~lowm) << EB);
-        const uint32_t delta = (uint32_t)(raw & lowm);
-        g = __reduce_xor_sync(0xffffffffu, ((delta >> lane) & 1u) ? my_gl : 0u);
-    };
+    auto tile_bases = [&](uint64_t b, OFF& ib, OFF& ob, uint32_t& g) { th.tile_bases(p, b, ib, ob, g); };
     // The thread's own offsets are passed through an empty asm each tile so
     // the compiler recomputes the per-chunk addresses (one XOR each) instead of
     // holding dozens of loop-invariant addresses in registers.
     auto load_tile = [&](OFF ib, uint4 (&r)[QPT]) {
-        OFF it = in_t ^ ib;
+        OFF it = th.in_t ^ ib;
         opaque(it);
 #pragma unroll
         for (int i = 0; i < QPT; ++i)
@@ -185,7 +197,7 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
         load_tile(ib, r);
     }
     for (; b < nt; b += gridDim.x) {
-        uint32_t ph = ph_t;
+        uint32_t ph = th.ph_t;
         asm volatile("" : "+r"(ph));
 #pragma unroll
         for (int i = 0; i < QPT; ++i) {
@@ -203,13 +215,13 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
         }
         __syncthreads();
         const OFF cur_ob = ob;
-        const uint32_t ga = ga_t ^ g;
+        const uint32_t ga = th.ga_t ^ g;
         const uint64_t nb = b + gridDim.x;
         if (nb < nt) {
             tile_bases(nb, ib, ob, g);
             load_tile(ib, r);
         }
-        OFF ot = out_t ^ cur_ob;
+        OFF ot = th.out_t ^ cur_ob;
         opaque(ot);
 #pragma unroll
         for (int i = 0; i < QPT; ++i) {
@@ -246,7 +258,6 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
                             uint4* __restrict__ out) {
     using T = typename ElemType<ELEM>::T;
     constexpr int VEC = 16 / ELEM;
-    constexpr int EB = ELEM == 4 ? 2 : ELEM == 8 ? 3 : 4;
     extern __shared__ uint4 smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(smem_raw);
     const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
@@ -254,55 +265,27 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
     const uint32_t tile_bytes = p.chunks * 16u;
 
     const uint32_t tid = threadIdx.x;
-    const uint32_t lane = tid & 31u;
-    OFF in_t = 0, out_t = 0;
-    uint32_t ph_t = 0, ga_t = 0;
-#pragma unroll
-    for (int k = 0; k < kMaxThreadBits; ++k) {
-        if ((1 << k) < NT && ((tid >> k) & 1u)) {
-            in_t ^= (OFF)p.tid_in[k];
-            out_t ^= (OFF)p.tid_out[k];
-            ph_t ^= p.tid_phi[k];
-            ga_t ^= p.tid_gam[k];
-        }
-    }
-    OFF my_cin = 0;
-    uint64_t my_cout = 0;
-    if ((int)lane < p.n_block_bits) {
-        my_cin = (OFF)(p.col_in[lane] << EB);
-        my_cout = p.col_out[lane];
-    }
-    uint32_t my_gl = 0;
-    if ((int)lane < p.t_out) my_gl = p.gam[lane] << EB;
-    const uint64_t lowm = (1ull << p.t_out) - 1ull;
+    const TileThread<ELEM, NT, OFF> th(p, tid);
     bool act[QPT];
 #pragma unroll
     for (int i = 0; i < QPT; ++i) act[i] = tid + (uint32_t)i * NT < p.chunks;
-
-    auto tile_bases = [&](uint64_t b, OFF& ib, OFF& ob, uint32_t& g) {
-        const bool bit = (b >> lane) & 1ull;
-        ib = warp_xor<OFF>(bit ? my_cin : (OFF)0);
-        const uint64_t raw = warp_xor64(bit ? my_cout : 0ull) ^ p.c;
-        ob = (OFF)((raw & ~lowm) << EB);
-        const uint32_t delta = (uint32_t)(raw & lowm);
-        g = __reduce_xor_sync(0xffffffffu, ((delta >> lane) & 1u) ? my_gl : 0u);
-    };
+    auto tile_bases = [&](uint64_t b, OFF& ib, OFF& ob, uint32_t& g) { th.tile_bases(p, b, ib, ob, g); };
     // Issue the copies of tile b into stage buffer `stage`.
     auto issue = [&](uint64_t b, int stage, OFF& ob, uint32_t& g) {
         OFF ib;
         tile_bases(b, ib, ob, g);
-        OFF it = in_t ^ ib;
+        OFF it = th.in_t ^ ib;
         opaque(it);
         unsigned char* base = smem + (uint32_t)stage * tile_bytes;
 #pragma unroll
         for (int i = 0; i < QPT; ++i)
-            if (act[i]) cp_async16(base + (ph_t ^ p.st_slot[i * VEC]), src + (it ^ (OFF)p.it_in[i]));
+            if (act[i]) cp_async16(base + (th.ph_t ^ p.st_slot[i * VEC]), src + (it ^ (OFF)p.it_in[i]));
         cp_async_commit();
     };
     auto gather_store = [&](int stage, OFF ob, uint32_t g) {
         const unsigned char* base = smem + (uint32_t)stage * tile_bytes;
-        const uint32_t ga = ga_t ^ g;
-        OFF ot = out_t ^ ob;
+        const uint32_t ga = th.ga_t ^ g;
+        OFF ot = th.out_t ^ ob;
         opaque(ot);
 #pragma unroll
         for (int i = 0; i < QPT; ++i) {
