@@ -527,6 +527,23 @@ def other_configs(torch, bm, synth, dev, stream):
     scratch = torch.empty(1 << 28, dtype=torch.int32, device=dev)
     with bm.Plan(rows, c, 4, mode=1) as p:
         out["random_n28_int32_two_factor"] = big(28, 4, lambda: p.permute_scratch(a32, b32, scratch, stream))
+    # LMAD front end: Futhark's reversed_rows (copy (map reverse xss)) on
+    # [8192][8192] i32 and [2^24][4] i32, each one BPC
+    out["lmad_reversed_rows_8192x8192_int32"] = big(
+        26, 4, lambda: bm.bmmc_lmad_copy((13, 13), 8191, (8192, -1), 0, (8192, 1), 4, a32, b32, stream))
+    out["lmad_reversed_rows_2p24x4_int32"] = big(
+        26, 4, lambda: bm.bmmc_lmad_copy((24, 2), 3, (4, -1), 0, (4, 1), 4, a32, b32, stream))
+    # parm lowering at n=28 int32: P_A, f (here the identity), P_(A^-1): two passes,
+    # algorithmic bytes of one permutation each
+    mask = 0x9ABCDEF & ((1 << 28) - 1)
+    A = bm.bmmc_parm_rows(28, mask)
+    with bm.Plan(A, 0, 4) as pa, bm.Plan(bm.bmmc_inverse_rows(A), 0, 4) as pb:
+        def parm_pass():
+            pa.permute(a32, b32, stream)
+            pb.permute(b32, a32, stream)
+        r = big(28, 4, parm_pass)
+        out["parm_lowering_n28_int32_two_permutes"] = {"gbs_per_permute": round(2 * r["gbs"], 1),
+                                                        "ms_both": r["ms"]}
     del a, b, scratch, flush_buf
     torch.cuda.empty_cache()
     return out
