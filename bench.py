@@ -533,6 +533,10 @@ def other_configs(torch, bm, synth, dev, stream):
         26, 4, lambda: bm.bmmc_lmad_copy((13, 13), 8191, (8192, -1), 0, (8192, 1), 4, a32, b32, stream))
     out["lmad_reversed_rows_2p24x4_int32"] = big(
         26, 4, lambda: bm.bmmc_lmad_copy((24, 2), 3, (4, -1), 0, (4, 1), 4, a32, b32, stream))
+    # the n=16 random map on 4096 arrays at once (batch_log2 = 12: 1 GiB in one launch)
+    rows16, c16, _ = synth.draw_bmmc(0, 16, accept(16))
+    with bm.Plan(rows16, c16, 4, batch_log2=12) as p:
+        out["n16_random_int32_batch4096"] = big(28, 4, lambda: p.permute(a32, b32, stream))
     # parm lowering at n=28 int32: P_A, f (here the identity), P_(A^-1): two passes,
     # algorithmic bytes of one permutation each
     mask = 0x9ABCDEF & ((1 << 28) - 1)

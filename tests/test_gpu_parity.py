@@ -609,3 +609,24 @@ def test_pageable_host_memory_when_the_device_can_reach_it(bm):
             assert out.tobytes() == oracle.scatter(n, A, c, arr).tobytes()
         else:
             assert st == _capi.ERR_INVALID_ARG
+
+
+def test_fuzz_larger_sizes(bm):
+    """Seeded random sizes 17..24 with random options, against the C oracle
+    on all host threads."""
+    rng = np.random.default_rng(77)
+    for trial in range(24):
+        elem = int(rng.choice([4, 8, 16]))
+        n = int(rng.integers(17, 25 if elem == 4 else 23))
+        kind = rng.random()
+        if kind < 0.7:
+            rows, c = _random(int(rng.integers(0, 1 << 30)), n)
+        else:
+            perm = [int(v) for v in rng.permutation(n)]
+            rows, c = [1 << p for p in perm], int(rng.integers(0, 1 << n))
+        opts = dict(grid_blocks=int(rng.choice([0, 0, 152, 1000])), load_mode=int(rng.choice([0, 1, 2])),
+                    block_order=int(rng.choice([0, 1, 2])), layout=int(rng.choice([0, 0, 1])))
+        arr = synth.fill_int(n, elem)
+        got, info = _run(bm, rows, c, arr, **opts)
+        want = oracle.scatter(n, rows, c, arr, threads=HOST_THREADS)
+        assert got.tobytes() == want.tobytes(), (n, elem, opts, info)
