@@ -3,6 +3,7 @@
     python -m bmmc_index_transforms_gb300.profile_case --kind random --n 26 --reps 3
 
 Kinds: random (seed), worst (seed, low 10 bits mapped to high bits), bitrev,
+complement (A = I, c on the high bits: contiguous tiles on both sides),
 transpose (square, n even), dims5 (the 5-D (4,2,0,3,1) permutation of a
 [32,64,64,64,32]-shaped array scaled to n bits), copy (the copy kernel on the
 same bytes), two_factor (seed, two passes through caller scratch).
@@ -35,7 +36,8 @@ def _accept(n, elem):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--kind", default="random",
-                    choices=["random", "worst", "bitrev", "transpose", "dims5", "copy", "two_factor"])
+                    choices=["random", "worst", "bitrev", "transpose", "dims5", "copy", "two_factor",
+                             "complement"])
     ap.add_argument("--n", type=int, default=26)
     ap.add_argument("--elem", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
@@ -53,6 +55,9 @@ def main(argv=None):
         rows, c, _ = synth.draw_bmmc(a.seed, n, _accept(n, elem))
     elif a.kind == "worst":
         rows, c, _ = synth.draw_bmmc(a.seed, n, _accept(n, elem), low_to_high=min(10, n // 2))
+    elif a.kind == "complement":
+        # A = I, c on the bits above the tile: every tile is contiguous on both sides
+        rows, c = maps.identity_rows(n), ((1 << n) - 1) & ~((1 << 16) - 1)
     elif a.kind == "bitrev":
         rows, c = maps.bitrev_rows(n), 0
     elif a.kind == "transpose":
