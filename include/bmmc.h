@@ -109,11 +109,14 @@ typedef struct {
     int gather;          /* 0 = scatter, out[A.x XOR c] = in[x] (default); 1 = gather,
                             out[y] = in[A.y XOR c] (the convention of the introduction's
                             bit-reverse example), run as the scatter by
-                            (A^-1, A^-1.c) */
+                            (A^-1, A^-1.c); bmmc_plan_info, bmmc_plan_factor and
+                            bmmc_plan_tile then describe that scatter */
     int batch_log2;      /* 0 = one array; b > 0 = 2^b independent arrays of 2^n elements
                             stored one after another, each permuted by (A, c) in one
                             launch (the map on n + b bits is A on the low n bits and the
-                            identity on the b high bits); n + b <= 40 */
+                            identity on the b high bits); n + b <= 40.  The plan then
+                            covers 2^(n+b) elements: bmmc_plan_info reports n + b and
+                            the permute calls take buffers of 2^(n+b) * elem_size bytes */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;
@@ -158,7 +161,8 @@ bmmc_status bmmc_plan_ex(bmmc_plan_t *plan, int n, const uint64_t *A_rows, uint6
  * using its scratch buffer is still running on a stream. */
 bmmc_status bmmc_plan_destroy(bmmc_plan_t plan);
 
-/* Describe a plan.  Errors: INVALID_ARG for NULL arguments. */
+/* Describe a plan (the single-pass shape also in TWO_FACTOR mode, whose two
+ * passes are planned the same way).  Errors: INVALID_ARG for NULL arguments. */
 bmmc_status bmmc_plan_info(bmmc_plan_t plan, bmmc_plan_info_t *info);
 
 /* The paper's §5 contract: A = T1.T2 with both factors tiled in the narrow
