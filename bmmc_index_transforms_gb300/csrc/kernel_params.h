@@ -43,6 +43,9 @@ struct TiledParams {
     int32_t tile_bits;                // D: log2 elements per tile
     int32_t n_block_bits;             // n - D
     int32_t t_out;
+    // Tile walk of a block: 0 = tiles blockIdx.x, blockIdx.x + gridDim.x, ...;
+    // otherwise tiles [blockIdx.x * span, (blockIdx.x + 1) * span) in order.
+    uint32_t span;
 };
 
 // Per-element fallback kernel (arrays smaller than one 16-byte vector per

@@ -187,8 +187,10 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
             if (act[i]) r[i] = ld_stream(reinterpret_cast<const uint4*>(src + (it ^ (OFF)p.it_in[i])));
     };
 
-    const uint64_t nt = p.n_tiles;
-    uint64_t b = blockIdx.x;
+    // Tile walk: a grid stride, or a contiguous range of `span` tiles.
+    const uint64_t step = p.span ? 1u : gridDim.x;
+    uint64_t b = p.span ? (uint64_t)blockIdx.x * p.span : blockIdx.x;
+    const uint64_t nt = p.span ? (b + p.span < p.n_tiles ? b + p.span : p.n_tiles) : p.n_tiles;
     uint4 r[QPT];
     OFF ib = 0, ob = 0;
     uint32_t g = 0;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
         tile_bases(b, ib, ob, g);
         load_tile(ib, r);
     }
-    for (; b < nt; b += gridDim.x) {
+    for (; b < nt; b += step) {
         uint32_t ph = th.ph_t;
         asm volatile("" : "+r"(ph));
 #pragma unroll
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
         __syncthreads();
         const OFF cur_ob = ob;
         const uint32_t ga = th.ga_t ^ g;
-        const uint64_t nb = b + gridDim.x;
+        const uint64_t nb = b + step;
         if (nb < nt) {
             tile_bases(nb, ib, ob, g);
             load_tile(ib, r);
@@ -301,9 +303,11 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
         }
     };
 
-    const uint64_t nt = p.n_tiles;
+    const uint64_t step = p.span ? 1u : gridDim.x;
+    const uint64_t b0 = p.span ? (uint64_t)blockIdx.x * p.span : blockIdx.x;
+    const uint64_t nt = p.span ? (b0 + p.span < p.n_tiles ? b0 + p.span : p.n_tiles) : p.n_tiles;
     if (STAGES == 1) {
-        for (uint64_t b = blockIdx.x; b < nt; b += gridDim.x) {
+        for (uint64_t b = b0; b < nt; b += step) {
             OFF ob;
             uint32_t g;
             issue(b, 0, ob, g);
@@ -315,11 +319,11 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
     } else {
         OFF ob[2] = {0, 0};
         uint32_t g[2] = {0, 0};
-        uint64_t b = blockIdx.x;
+        uint64_t b = b0;
         if (b < nt) issue(b, 0, ob[0], g[0]);
-        for (int k = 0; b < nt; b += gridDim.x, ++k) {
+        for (int k = 0; b < nt; b += step, ++k) {
             const int s = k & 1;
-            const uint64_t nb = b + gridDim.x;
+            const uint64_t nb = b + step;
             if (nb < nt) {
                 issue(nb, s ^ 1, ob[s ^ 1], g[s ^ 1]);
                 cp_async_wait<1>();
@@ -499,6 +503,14 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
     if (grid_override > 0) grid = (uint64_t)grid_override;
     if (grid > P.tiles) grid = P.tiles;
     if (grid > 0x7FFFFFFFull) grid = 0x7FFFFFFFull;
+    TiledParams tp = P.tp;
+    tp.span = 0;
+    if (P.tile_walk == 1 && grid < P.tiles) {
+        const uint64_t span = (P.tiles + grid - 1) / grid;
+        if (span > 0xFFFFFFFFull) return cudaErrorInvalidConfiguration;
+        tp.span = (uint32_t)span;
+        grid = (P.tiles + span - 1) / span;
+    }
     const bool use_async = P.vector_scatter && P.load_mode != 2 && (P.load_mode == 1 || P.async_default) &&
                            P.threads == 256 && (P.qpt == 4 || P.qpt == 8 || P.qpt == 16);
     if (use_async) {
@@ -507,14 +519,14 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
         if (!fn) return cudaErrorInvalidConfiguration;
         const int smem = stages * P.smem_bytes;
         if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, smem, &per)) != cudaSuccess) return e;
-        fn<<<(unsigned)grid, P.threads, smem, stream>>>(P.tp, static_cast<const uint4*>(in),
+        fn<<<(unsigned)grid, P.threads, smem, stream>>>(tp, static_cast<const uint4*>(in),
                                                          static_cast<uint4*>(out));
         return cudaGetLastError();
     }
     TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide, P.vector_scatter);
     if (!fn) return cudaErrorInvalidConfiguration;
     if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
-    fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(P.tp, static_cast<const uint4*>(in),
+    fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(tp, static_cast<const uint4*>(in),
                                                              static_cast<uint4*>(out));
     return cudaGetLastError();
 }

@@ -539,6 +539,7 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     P.kernel = KERNEL_TILED;
     P.grid_blocks = req.grid_blocks;
     P.load_mode = req.load_mode;
+    P.tile_walk = req.tile_walk;
     P.async_default = false;
     P.threads = NT;
     P.qpt = qpt;

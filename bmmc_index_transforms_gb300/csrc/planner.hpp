@@ -23,6 +23,7 @@ struct PassPlan {
     int qpt = 1;             // 16-byte chunks per thread per tile
     bool vector_scatter = false;  // input vectors stored whole (one 16-byte store each)
     int load_mode = 0;            // 0 default, 1 asynchronous copies, 2 loads through registers
+    int tile_walk = 0;            // 0 grid stride, 1 contiguous range of tiles per block
     bool async_default = false;   // the default for this plan uses asynchronous copies
     int grid_blocks = 0;     // requested grid (0 = default)
     int smem_bytes = 0;
@@ -41,6 +42,7 @@ struct PlanRequest {
     int load_mode = 0;                       // 0 default, 1 async copies, 2 through registers
     int block_order = 0;                     // 0 input coordinate bits ascending, 1 local on both sides
     int layout = 0;                          // 0 automatic, 1 per-element stores
+    int tile_walk = 0;                       // 0 grid stride, 1 contiguous ranges
 };
 
 // Build one pass for (rows, c).  inv must be rows' inverse.

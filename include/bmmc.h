@@ -117,6 +117,9 @@ typedef struct {
                             identity on the b high bits); n + b <= 40.  The plan then
                             covers 2^(n+b) elements: bmmc_plan_info reports n + b and
                             the permute calls take buffers of 2^(n+b) * elem_size bytes */
+    int tile_walk;       /* with grid_blocks below the number of tiles: 0 = block k takes
+                            tiles k, k + grid, ... (default); 1 = block k takes a
+                            contiguous range of tiles */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;

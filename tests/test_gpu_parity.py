@@ -630,3 +630,16 @@ def test_fuzz_larger_sizes(bm):
         got, info = _run(bm, rows, c, arr, **opts)
         want = oracle.scatter(n, rows, c, arr, threads=HOST_THREADS)
         assert got.tobytes() == want.tobytes(), (n, elem, opts, info)
+
+
+@pytest.mark.parametrize("load_mode", [0, 1])
+def test_contiguous_tile_walk(bm, load_mode):
+    """tile_walk = 1 (each block a contiguous range of tiles, ranges of
+    uneven length at the end) gives the oracle's bytes."""
+    for n, elem, grid in [(20, 4, 7), (21, 8, 152), (19, 16, 5), (22, 4, 1000), (18, 4, 3)]:
+        rows, c = _random(n * 3 + grid, n)
+        arr = synth.fill_int(n, elem)
+        for order in (0, 1):
+            got, info = _run(bm, rows, c, arr, grid_blocks=grid, tile_walk=1, load_mode=load_mode,
+                             block_order=order)
+            assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), (n, elem, grid, info)
