@@ -61,3 +61,12 @@ def test_reference_arm_line():
     assert line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["warmup"] >= 3
+
+
+def test_effective_bandwidth_bytes_match_the_page(golden):
+    """The bench's algorithmic bytes per permutation, 2 * 2^n * elem, equal the
+    byte count the transpose tutorial prints for 4096 x 4096 floats."""
+    for n, elem, want in golden("effective_bandwidth.txt"):
+        n, elem, want = int(n), int(elem), int(want)
+        assert 2.0 * (1 << n) * elem == want
+        assert bench.job_throughput_gbs(1, 1, 2.0 * (1 << n) * elem, 1.0) == want / 1e-3 / 1e9
