@@ -123,3 +123,120 @@ def candidates(seed: int, n: int, low_to_high: int = 0) -> Iterator[list[int]]:
     rng = SplitMix64(seed)
     while True:
         yield candidate_rows(rng, n, low_to_high)
+
+
+# --------------------------------------------------------------------------
+# LMAD copy workloads ("Speeding up GPU copies by permuting iteration
+# spaces", Futhark blog).  An LMAD here is (sizes, offset, strides) in
+# element units; these helpers describe inputs (views of row-major arrays)
+# and perform no copy.
+# --------------------------------------------------------------------------
+
+# The "Impact" section's benchmark functions on i32 arrays: copy xss[:, 1:],
+# copy xsss[:, :, 1:] and copy (map reverse xss), at the shapes it lists.
+LMAD_PAGE_WORKLOADS = (
+    ("slice_2d", (8192, 8193)),
+    ("slice_2d", (65536, 1025)),
+    ("slice_2d", (1048576, 65)),
+    ("slice_2d", (16777216, 5)),
+    ("slice_3d", (256, 256, 1025)),
+    ("slice_3d", (65536, 32, 33)),
+    ("reversed_rows", (8192, 8192)),
+    ("reversed_rows", (16777216, 4)),
+)
+
+
+def row_major_strides(shape) -> list[int]:
+    strides, acc = [], 1
+    for n in reversed(shape):
+        strides.append(acc)
+        acc *= int(n)
+    return strides[::-1]
+
+
+def page_lmad_workload(kind: str, shape) -> dict:
+    """Source view and destination of one "Impact" workload: the source is a
+    view of a row-major array of ``shape`` (its last axis sliced from 1, or
+    reversed), the destination the row-major array of the view's shape.
+    Returns sizes, offsets, strides and the element counts of both arrays."""
+    shape = [int(v) for v in shape]
+    src_strides = row_major_strides(shape)
+    total = 1
+    for v in shape:
+        total *= v
+    if kind in ("slice_2d", "slice_3d"):
+        sizes = shape[:-1] + [shape[-1] - 1]
+        in_offset, in_strides = 1, src_strides
+    elif kind == "reversed_rows":
+        sizes = list(shape)
+        in_offset = shape[-1] - 1
+        in_strides = src_strides[:-1] + [-1]
+    else:
+        raise ValueError(kind)
+    out_elems = 1
+    for v in sizes:
+        out_elems *= v
+    return dict(sizes=sizes, in_offset=in_offset, in_strides=in_strides, in_elems=total,
+                out_offset=0, out_strides=row_major_strides(sizes), out_elems=out_elems)
+
+
+def draw_lmad_view(seed: int, max_dims: int = 4, max_elems: int = 1 << 14) -> dict:
+    """A random copy between two array views, for fuzzing.
+
+    Source: a row-major base array of random shape, viewed through a random
+    slice of every axis (start, stop, step in {+-1, +-2, +-3}) and a random
+    order of the axes.  Destination: a row-major array of a random shape
+    padded around the view's shape in a random axis order, written through
+    the view's index space (so both LMADs are injective and in bounds).
+    Returns sizes, offsets, strides and element counts of both arrays."""
+    rng = SplitMix64(seed * 0x9E3779B1 + 17)
+    d = 1 + rng.next() % max_dims
+    shape = []
+    budget = max_elems
+    for k in range(d):
+        cap = max(1, int(round(budget ** (1.0 / (d - k)))) * 2)
+        v = 1 + rng.next() % cap
+        v = min(v, max(1, budget))
+        shape.append(v)
+        budget = max(1, budget // v)
+    base_strides = row_major_strides(shape)
+    base_elems = 1
+    for v in shape:
+        base_elems *= v
+    sizes, in_strides, in_offset = [], [], 0
+    for n, s in zip(shape, base_strides):
+        step = 1 + rng.next() % 3 if rng.next() % 4 == 0 else 1
+        count = 1 + rng.next() % max(1, (n + step - 1) // step)
+        first = rng.next() % (n - (count - 1) * step)
+        if rng.next() % 3 == 0:  # walk the axis backwards
+            first += (count - 1) * step
+            step = -step
+        sizes.append(count)
+        in_strides.append(s * step)
+        in_offset += first * s
+    order = list(range(d))
+    for i in range(d - 1, 0, -1):
+        j = rng.next() % (i + 1)
+        order[i], order[j] = order[j], order[i]
+    sizes = [sizes[k] for k in order]
+    in_strides = [in_strides[k] for k in order]
+    # destination: padded row-major array in another axis order
+    dorder = list(range(d))
+    for i in range(d - 1, 0, -1):
+        j = rng.next() % (i + 1)
+        dorder[i], dorder[j] = dorder[j], dorder[i]
+    pad = [sizes[k] + (rng.next() % 3 if rng.next() % 3 == 0 else 0) for k in dorder]
+    pstrides = row_major_strides(pad)
+    out_strides = [0] * d
+    out_offset = 0
+    for pos, k in enumerate(dorder):
+        out_strides[k] = pstrides[pos]
+        out_offset += (pad[pos] - sizes[k]) // 2 * pstrides[pos] if pad[pos] > sizes[k] else 0
+        if rng.next() % 4 == 0 and sizes[k] > 1:  # destination walks the axis backwards
+            out_offset += (sizes[k] - 1) * pstrides[pos]
+            out_strides[k] = -pstrides[pos]
+    out_elems = 1
+    for v in pad:
+        out_elems *= v
+    return dict(sizes=sizes, in_offset=in_offset, in_strides=in_strides, in_elems=base_elems,
+                out_offset=out_offset, out_strides=out_strides, out_elems=out_elems)

@@ -47,6 +47,8 @@ __all__ = [
     "r2_tiled",
     "bmmc_gather",
     "lmad_copy",
+    "lmad_copy_general",
+    "lmad_normalize",
     "parm",
 ]
 
@@ -314,6 +316,77 @@ def lmad_copy(dims_log2, in_offset, in_strides, out_offset, out_strides, arr):
     out = np.zeros_like(arr)
     out[dst] = arr[src]
     return out
+
+
+def _lmad_offsets(sizes, offset, strides) -> np.ndarray:
+    """offset + sum_k i_k * strides[k] for every index tuple, the tuples in
+    one fixed order (the same order for any strides of the same sizes)."""
+    off = np.array([int(offset)], dtype=np.int64)
+    for n, s in zip(sizes, strides):
+        off = np.add.outer(off, np.arange(int(n), dtype=np.int64) * int(s)).ravel()
+    return off
+
+
+def lmad_copy_general(sizes, in_offset, in_strides, out_offset, out_strides, src, dst):
+    """The copy loop of "Optimising LMAD copies" for sizes of any value (not
+    only powers of two): for every index tuple i, 0 <= i_k < sizes[k],
+        dst[out_offset + sum_k i_k * out_strides[k]] = src[in_offset + sum_k i_k * in_strides[k]]
+    in element units, an element being one entry along the first axis of src
+    and dst.  Returns a copy of dst with those positions overwritten; every
+    other position keeps its value.  An empty index space (a size 0) copies
+    nothing; no dimensions at all is one tuple (one element)."""
+    src = np.asarray(src)
+    out = np.array(dst, copy=True)
+    if any(int(n) == 0 for n in sizes):
+        return out
+    s_off = _lmad_offsets(sizes, in_offset, in_strides)
+    d_off = _lmad_offsets(sizes, out_offset, out_strides)
+    out[d_off] = src[s_off]
+    return out
+
+
+def lmad_normalize(sizes, in_offset, in_strides, out_offset, out_strides):
+    """The run-time analysis of "Optimising LMAD copies" and of the
+    coalescing section that follows it, on a pair of LMADs copied one to the
+    other (the same index tuples on both sides):
+
+    1. A dimension whose source stride is negative is walked backwards: both
+       offsets move to its last index and both strides change sign, so the
+       copied pairs are unchanged (reading taken: the page only shows
+       positive strides).
+    2. Singleton dimensions are ignored.
+    3. Selection sort by increasing source stride, ties by the magnitude of
+       the destination stride.
+    4. Neighbouring dimensions collapse, inner (n_1, s_1, t_1) and next
+       (n_2, s_2, t_2), into (n_1 n_2, s_1, t_1) when s_2 = s_1 n_1 and
+       t_2 = t_1 n_1 (the page's collapse rule, written inner dimension first
+       and required on both sides).
+
+    Returns (dims, in_offset, out_offset), dims a list of [size, in_stride,
+    out_stride], fastest (smallest source stride) first."""
+    dims = []
+    for n, s, t in zip(sizes, in_strides, out_strides):
+        n, s, t = int(n), int(s), int(t)
+        if n == 1:
+            continue
+        if s < 0:
+            in_offset += (n - 1) * s
+            out_offset += (n - 1) * t
+            s, t = -s, -t
+        dims.append([n, s, t])
+    for i in range(len(dims)):
+        best = i
+        for k in range(i + 1, len(dims)):
+            if (dims[k][1], abs(dims[k][2])) < (dims[best][1], abs(dims[best][2])):
+                best = k
+        dims[i], dims[best] = dims[best], dims[i]
+    merged = []
+    for n, s, t in dims:
+        if merged and s == merged[-1][1] * merged[-1][0] and t == merged[-1][2] * merged[-1][0]:
+            merged[-1][0] *= n
+        else:
+            merged.append([n, s, t])
+    return merged, int(in_offset), int(out_offset)
 
 
 # ---------------------------------------------------------------------------

@@ -4,8 +4,10 @@ CPU, makes at least one pin of tests/test_oracle_pins.py fail.
 Mistakes planted (one at a time, restored after each case): a transposed
 operand (columns of A used as rows), the complement dropped, a bit index
 shifted by one, the gather written for the scatter, the inverse returned
-transposed, the product taken in the wrong order, and, in the C loop, the
-output bit index shifted.  A mutation that every pin tolerated would mean
+transposed, the product taken in the wrong order, in the C loop the output
+bit index shifted, and, in the LMAD copy, the two strides swapped, the last
+index of a dimension left out, the stride sort reversed and the offsets of a
+walked-back dimension not moved.  A mutation that every pin tolerated would mean
 the oracle was not pinned at that point.
 """
 
@@ -22,7 +24,7 @@ from conftest import read_golden
 from oracle import reference as ref
 
 ORIG = {name: getattr(ref, name) for name in ("bmmc_index", "bmmc_index_array", "bmmc_permute", "f2_inverse",
-                                              "f2_matmul")}
+                                              "f2_matmul", "lmad_copy_general", "lmad_normalize")}
 
 
 def _transposed(rows, n):
@@ -85,8 +87,40 @@ def mut_product_order(monkeypatch):
     monkeypatch.setattr(ref, "f2_matmul", lambda n, a, b: ORIG["f2_matmul"](n, b, a))
 
 
+def mut_lmad_strides_swapped(monkeypatch):
+    def copy(sizes, io, ins, oo, outs, src, dst):
+        return ORIG["lmad_copy_general"](sizes, io, outs, oo, ins, src, dst)
+
+    monkeypatch.setattr(ref, "lmad_copy_general", copy)
+
+
+def mut_lmad_last_index_dropped(monkeypatch):
+    def copy(sizes, io, ins, oo, outs, src, dst):
+        return ORIG["lmad_copy_general"]([max(0, int(v) - 1) if k == 0 else v for k, v in enumerate(sizes)],
+                                         io, ins, oo, outs, src, dst)
+
+    monkeypatch.setattr(ref, "lmad_copy_general", copy)
+
+
+def mut_lmad_sort_descending(monkeypatch):
+    def norm(sizes, io, ins, oo, outs):
+        dims, a, b = ORIG["lmad_normalize"](sizes, io, ins, oo, outs)
+        return dims[::-1], a, b
+
+    monkeypatch.setattr(ref, "lmad_normalize", norm)
+
+
+def mut_lmad_flip_offset_forgotten(monkeypatch):
+    def norm(sizes, io, ins, oo, outs):
+        dims, a, b = ORIG["lmad_normalize"](sizes, io, ins, oo, outs)
+        return dims, io, oo
+
+    monkeypatch.setattr(ref, "lmad_normalize", norm)
+
+
 def _all_pins():
-    """Run every pin; return the names of those that failed."""
+    """Run every pin; return the names of those that failed (an assertion
+    or any other exception, such as an index out of range)."""
     failed = []
     cases = [
         ("worked", lambda: pins.test_worked_examples_python_and_c(read_golden)),
@@ -100,11 +134,16 @@ def _all_pins():
         ("inverse_undo", lambda: pins.test_inverse_undoes_and_scatter_is_gather_by_inverse(0)),
         ("c_vs_py", lambda: pins.test_c_oracle_equals_python_oracle(5, 4)),
         ("gather", pins.test_gather_convention_pins),
+        ("lmad_layouts", pins.test_lmad_general_page_layouts),
+        ("lmad_sorted", lambda: pins.test_lmad_slice_sorted_order_from_the_page(3, 7)),
+        ("lmad_slices", lambda: pins.test_lmad_page_workloads_are_numpy_slices("slice_3d", (5, 6, 7))),
+        ("lmad_reversed", lambda: pins.test_lmad_page_workloads_are_numpy_slices("reversed_rows", (8, 6))),
+        ("lmad_views", lambda: [pins.test_lmad_general_matches_numpy_strided_views(s) for s in range(8)]),
     ]
     for name, fn in cases:
         try:
             fn()
-        except AssertionError:
+        except Exception:
             failed.append(name)
     return failed
 
@@ -114,7 +153,9 @@ def test_pins_pass_on_the_unmutated_oracle():
 
 
 @pytest.mark.parametrize("mutation", [mut_transposed_operand, mut_drop_complement, mut_bit_index_off_by_one,
-                                      mut_gather_for_scatter, mut_inverse_transposed, mut_product_order])
+                                      mut_gather_for_scatter, mut_inverse_transposed, mut_product_order,
+                                      mut_lmad_strides_swapped, mut_lmad_last_index_dropped,
+                                      mut_lmad_sort_descending, mut_lmad_flip_offset_forgotten])
 def test_each_planted_mistake_fails_a_pin(monkeypatch, mutation):
     mutation(monkeypatch)
     assert _all_pins(), f"no pin caught {mutation.__name__}"

@@ -307,3 +307,100 @@ def test_gather_convention_pins():
     inv_perm = np.argsort(fwd)
     scat = ref.bmmc_permute(10, A, c, arr)
     assert np.array_equal(scat, arr[inv_perm])
+
+
+# ---------------------------------------------------------------------------
+# General LMAD copies ("Speeding up GPU copies by permuting iteration spaces")
+# ---------------------------------------------------------------------------
+
+def test_lmad_general_page_layouts():
+    """The page's [4][5] array: row-major LMAD [(4,5),(5,1)], column-major
+    [(4,1),(5,4)].  Copying row-major to column-major is numpy's transpose;
+    row-major to row-major collapses, by the page's rule, to one dimension
+    (20, 1), the memcpy case."""
+    a = np.arange(20, dtype=np.int32) * 7 + 3
+    got = ref.lmad_copy_general((4, 5), 0, (5, 1), 0, (1, 4), a, np.zeros(20, np.int32))
+    assert np.array_equal(got, a.reshape(4, 5).T.ravel())
+    dims, io, oo = ref.lmad_normalize((4, 5), 0, (5, 1), 0, (5, 1))
+    assert dims == [[20, 1, 1]] and io == 0 and oo == 0
+    dims, _, _ = ref.lmad_normalize((4, 5), 0, (5, 1), 0, (1, 4))
+    assert dims == [[5, 1, 4], [4, 5, 1]]
+
+
+@pytest.mark.parametrize("n,m", [(2, 2), (3, 7), (8193, 5), (5, 8193)])
+def test_lmad_slice_sorted_order_from_the_page(n, m):
+    """The coalescing section's worked example: the slice xss[:, 1:] of a
+    row-major [n][m] array has LMAD [(n,m),(m-1,1)] (offset 1) and is copied
+    to [(n,m-1),(m-1,1)]; sorted by stride they become [(m-1,1),(n,m)] and
+    [(m-1,1),(n,m-1)] (n > 1, m > 1 as the page assumes)."""
+    dims, io, oo = ref.lmad_normalize((n, m - 1), 1, (m, 1), 0, (m - 1, 1))
+    if m - 1 == 1:  # a singleton dimension is dropped
+        assert dims == [[n, m, m - 1]]
+    else:
+        assert dims == [[m - 1, 1, 1], [n, m, m - 1]]
+    assert (io, oo) == (1, 0)
+
+
+@pytest.mark.parametrize("kind,shape", [("slice_2d", (9, 10)), ("slice_2d", (64, 5)), ("slice_2d", (3, 65)),
+                                        ("slice_3d", (5, 6, 7)), ("slice_3d", (64, 32, 33)),
+                                        ("reversed_rows", (8, 6)), ("reversed_rows", (33, 4))])
+def test_lmad_page_workloads_are_numpy_slices(kind, shape):
+    """slice_2d = copy xss[:, 1:], slice_3d = copy xsss[:, :, 1:],
+    reversed_rows = copy (map reverse xss): numpy slicing computes each."""
+    w = synth.page_lmad_workload(kind, shape)
+    base = np.arange(w["in_elems"], dtype=np.int32) * 3 + 1
+    got = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
+                                base, np.zeros(w["out_elems"], np.int32))
+    x = base.reshape(shape)
+    want = {"slice_2d": lambda: x[:, 1:], "slice_3d": lambda: x[:, :, 1:],
+            "reversed_rows": lambda: x[:, ::-1]}[kind]()
+    assert np.array_equal(got, np.ascontiguousarray(want).ravel())
+
+
+def _as_strided_copy(w, src, dst):
+    """The same copy done by numpy: an as_strided view of each buffer (byte
+    strides from the element strides) and one slice assignment."""
+    from numpy.lib.stride_tricks import as_strided
+
+    e = src.itemsize
+    sv = as_strided(src[w["in_offset"]:], shape=w["sizes"], strides=[s * e for s in w["in_strides"]])
+    out = dst.copy()
+    dv = as_strided(out[w["out_offset"]:], shape=w["sizes"], strides=[s * e for s in w["out_strides"]],
+                    writeable=True)
+    dv[...] = sv
+    return out
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_lmad_general_matches_numpy_strided_views(seed):
+    """Random views (sliced with steps, reversed, axes permuted, padded
+    destinations): the oracle's loop equals numpy's strided-view assignment,
+    positions outside the destination view keep their sentinel, and the
+    normalised LMAD (flip, drop singletons, sort, collapse) copies the same
+    pairs."""
+    w = synth.draw_lmad_view(seed)
+    src = np.arange(w["in_elems"], dtype=np.int64) * 5 + 2
+    dst = np.full(w["out_elems"], -1, dtype=np.int64)
+    got = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
+                                src, dst)
+    assert np.array_equal(got, _as_strided_copy(w, src, dst))
+    dims, io, oo = ref.lmad_normalize(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],
+                                      w["out_strides"])
+    assert all(d[1] >= 0 and d[0] > 1 for d in dims)
+    assert [d[1] for d in dims] == sorted(d[1] for d in dims)
+    again = ref.lmad_copy_general([d[0] for d in dims], io, [d[1] for d in dims], oo, [d[2] for d in dims],
+                                  src, dst)
+    assert np.array_equal(again, got)
+
+
+def test_lmad_general_degenerate_cases():
+    """A size-0 dimension copies nothing; no dimensions is one element;
+    16-byte elements move whole rows."""
+    src = np.arange(10, dtype=np.int32)
+    dst = np.full(10, -1, dtype=np.int32)
+    assert np.array_equal(ref.lmad_copy_general((0, 4), 0, (4, 1), 0, (4, 1), src, dst), dst)
+    one = ref.lmad_copy_general((), 7, (), 2, (), src, dst)
+    assert one[2] == 7 and (np.delete(one, 2) == -1).all()
+    wide = np.arange(12 * 4, dtype=np.uint32).reshape(12, 4)
+    got = ref.lmad_copy_general((3, 4), 0, (4, 1), 0, (1, 3), wide, np.zeros_like(wide))
+    assert np.array_equal(got, wide.reshape(3, 4, 4).transpose(1, 0, 2).reshape(12, 4))
