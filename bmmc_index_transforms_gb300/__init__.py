@@ -24,12 +24,13 @@ __all__ = [
     "BmmcError", "Plan", "bmmc_plan", "bmmc_plan_ex", "bmmc_plan_destroy", "bmmc_plan_info",
     "bmmc_plan_factor", "bmmc_plan_tile", "bmmc_permute", "bmmc_permute_scratch",
     "bmmc_permute_host", "bmmc_permute_static_scratch", "transpose2d", "bpc_permute", "bmmc_dims_permute",
-    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "bmmc_parm_rows", "bmmc_inverse_rows", "bmmc_compose",
+    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "lmad_copy", "lmad_copy_query", "bmmc_parm_rows", "bmmc_inverse_rows", "bmmc_compose",
     "bmmc_status_string", "bmmc_version", "library_path",
 ]
 
 CLASS_NAMES = {0: "identity", 1: "complement", 2: "bp", 3: "bpc", 4: "bmmc"}
 KERNEL_NAMES = {0: "tiled", 1: "copy", 2: "per-element"}
+LMAD_KIND_NAMES = {0: "empty", 1: "memcpy", 2: "bpc", 3: "transpose", 4: "strided"}
 
 
 class BmmcError(RuntimeError):
@@ -218,6 +219,56 @@ def bmmc_lmad_bpc(dims_log2: Sequence[int], in_offset: int, in_strides: Sequence
     c = ctypes.c_uint64(0)
     _check(_capi.lib().bmmc_lmad_bpc(*args, perm, ctypes.byref(c)), "bmmc_lmad_bpc")
     return [int(perm[i]) for i in range(sum(dims_log2))], int(c.value)
+
+
+def _elems(x, elem_size: int, given) -> int:
+    """Elements of elem_size bytes in buffer x (a tensor or numpy array), or
+    the count given explicitly (needed for raw addresses)."""
+    if given is not None:
+        return int(given)
+    if x is None:
+        raise ValueError("element count needed for a raw address")
+    if hasattr(x, "element_size"):
+        return x.numel() * x.element_size() // elem_size
+    if hasattr(x, "nbytes"):
+        return int(x.nbytes) // elem_size
+    raise ValueError("element count needed for a raw address")
+
+
+def _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides):
+    d = len(sizes)
+    if len(in_strides) != d or len(out_strides) != d:
+        raise ValueError("one stride per dimension on each side")
+    return (d, (ctypes.c_int64 * max(d, 1))(*sizes), int(in_offset), (ctypes.c_int64 * max(d, 1))(*in_strides),
+            int(out_offset), (ctypes.c_int64 * max(d, 1))(*out_strides))
+
+
+def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
+                    out_strides: Sequence[int], elem_size: int, inp=None, out=None, *, in_elems=None,
+                    out_elems=None) -> dict:
+    """What lmad_copy would run (host only; inp / out used for alignment and
+    overlap, may be None with explicit element counts)."""
+    d, sz, io, si, oo, so = _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides)
+    info = _capi.LmadCopyInfo()
+    _check(_capi.lib().lmad_copy_query(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
+                                       _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
+                                       ctypes.byref(info)), "lmad_copy_query")
+    k = info.ndims
+    return {"kind": LMAD_KIND_NAMES.get(info.kind, str(info.kind)), "ndims": k,
+            "dims": [[int(info.sizes[i]), int(info.in_strides[i]), int(info.out_strides[i])] for i in range(k)],
+            "in_offset": int(info.in_offset), "out_offset": int(info.out_offset), "vec": int(info.vec),
+            "transpose_out_dim": int(info.transpose_out_dim), "elements": int(info.elements)}
+
+
+def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
+              out_strides: Sequence[int], elem_size: int, inp, out, stream=None, *, in_elems=None,
+              out_elems=None) -> None:
+    """out[out_offset + sum i_k out_strides[k]] = inp[in_offset + sum i_k in_strides[k]] for every index
+    tuple (element units, any sizes); enqueued on the stream."""
+    d, sz, io, si, oo, so = _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides)
+    _check(_capi.lib().lmad_copy(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
+                                 _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
+                                 _stream(stream, inp, out)), "lmad_copy")
 
 
 def bmmc_inverse_rows(A_rows: Sequence[int]) -> list[int]:

@@ -21,7 +21,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libbmmc_gb300.so")
 HEADER = os.path.join(ROOT, "include", "bmmc.h")
 
-SOURCES = ["kernels.cu", "capi.cu", "planner.cpp", "static_scratch.cu"]
+SOURCES = ["kernels.cu", "capi.cu", "planner.cpp", "static_scratch.cu", "lmad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

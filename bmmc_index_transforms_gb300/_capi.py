@@ -57,6 +57,18 @@ class PlanInfo(ctypes.Structure):
                 ("c", ctypes.c_uint64), ("vector_stores", ctypes.c_int)]
 
 
+LMAD_MAX_DIMS = 16
+LMAD_COPY_EMPTY, LMAD_COPY_MEMCPY, LMAD_COPY_BPC, LMAD_COPY_TRANSPOSE, LMAD_COPY_STRIDED = range(5)
+
+
+class LmadCopyInfo(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("ndims", ctypes.c_int),
+                ("sizes", ctypes.c_int64 * LMAD_MAX_DIMS), ("in_strides", ctypes.c_int64 * LMAD_MAX_DIMS),
+                ("out_strides", ctypes.c_int64 * LMAD_MAX_DIMS), ("in_offset", ctypes.c_int64),
+                ("out_offset", ctypes.c_int64), ("vec", ctypes.c_int), ("transpose_out_dim", ctypes.c_int),
+                ("elements", ctypes.c_uint64)]
+
+
 # name -> (restype, argtypes); every function declared in include/bmmc.h
 SIGNATURES = {
     "bmmc_plan": (ctypes.c_int, [ctypes.POINTER(vp), ctypes.c_int, u64p, u64, ctypes.c_size_t]),
@@ -79,6 +91,11 @@ SIGNATURES = {
                                       ctypes.c_size_t, vp, vp, vp]),
     "bmmc_lmad_bpc": (ctypes.c_int, [ctypes.c_int, intp, ctypes.c_int64, i64p, ctypes.c_int64, i64p, intp,
                                      u64p]),
+    "lmad_copy_query": (ctypes.c_int, [ctypes.c_int, i64p, ctypes.c_int64, i64p, ctypes.c_size_t, ctypes.c_int64,
+                                       i64p, ctypes.c_size_t, ctypes.c_size_t, vp, vp,
+                                       ctypes.POINTER(LmadCopyInfo)]),
+    "lmad_copy": (ctypes.c_int, [ctypes.c_int, i64p, ctypes.c_int64, i64p, ctypes.c_size_t, ctypes.c_int64, i64p,
+                                 ctypes.c_size_t, ctypes.c_size_t, vp, vp, vp]),
     "bmmc_parm_rows": (ctypes.c_int, [ctypes.c_int, u64, u64p]),
     "bmmc_inverse_rows": (ctypes.c_int, [ctypes.c_int, u64p, u64p]),
     "bmmc_compose": (ctypes.c_int, [ctypes.c_int, u64p, u64, u64p, u64, u64p, u64p]),

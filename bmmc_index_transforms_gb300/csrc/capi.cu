@@ -175,6 +175,10 @@ bmmc_status permute_once(int n, const uint64_t* rows, uint64_t c, size_t elem, c
 
 }  // namespace
 
+namespace bmmc {
+bmmc_status pointer_reachable(const void* p) { return check_reachable(p); }
+}  // namespace bmmc
+
 extern "C" {
 
 bmmc_status bmmc_plan_ex(bmmc_plan_t* plan, int n, const uint64_t* A_rows, uint64_t c,

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 
+#include "../../include/bmmc.h"
 #include "planner.hpp"
 
 namespace bmmc {
@@ -18,5 +19,9 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
 
 // Plain copy of `bytes` bytes.
 cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t stream);
+
+// OK when the GPU can read and write through p (device, managed or pinned
+// memory, or pageable host memory on a device with pageable access).
+bmmc_status pointer_reachable(const void* p);
 
 }  // namespace bmmc

@@ -281,6 +281,93 @@ bmmc_status bmmc_lmad_bpc(int ndims, const int *dims_log2, int64_t in_offset,
                           const int64_t *in_strides, int64_t out_offset,
                           const int64_t *out_strides, int *perm_out, uint64_t *c_out);
 
+/* ---- General LMAD copies ---------------------------------------------------
+ * "Speeding up GPU copies by permuting iteration spaces" (Futhark blog).
+ * An LMAD ("Futhark's array representation") is an offset plus one
+ * (size, stride) pair per dimension, in element units.  A copy between two
+ * LMADs of the same sizes is, for every index tuple (i_0, ..., i_{d-1}) with
+ * 0 <= i_k < sizes[k],
+ *     out[out_offset + sum_k i_k * out_strides[k]] =
+ *         in[in_offset + sum_k i_k * in_strides[k]]
+ * and every other element of `out` is left as it was.  Unlike bmmc_lmad_copy
+ * the sizes are arbitrary (slices, odd shapes), strides any non-zero value on
+ * the destination and any value (0 = broadcast) on the source.
+ *
+ * The copy is analysed on the host before launch ("Optimising LMAD copies"
+ * and the coalescing section after "The new case"):
+ *   1. a dimension whose source stride is negative is walked backwards (both
+ *      offsets move to its last index, both strides change sign), singleton
+ *      dimensions are dropped;
+ *   2. the dimensions are sorted by increasing source stride, ties by the
+ *      magnitude of the destination stride (the page's selection sort);
+ *   3. a dimension collapses into the next faster one, (n_1, s_1, t_1) and
+ *      (n_2, s_2, t_2) into (n_1 n_2, s_1, t_1), when s_2 = s_1 n_1 and
+ *      t_2 = t_1 n_1 (the page's rule, on both sides at once);
+ * and the result runs as one of the kinds below. */
+#define LMAD_MAX_DIMS 16  /* dimensions left after step 3; more is INVALID_ARG */
+
+typedef enum {
+    LMAD_COPY_EMPTY = 0,     /* a size is 0: nothing to copy, nothing launched */
+    LMAD_COPY_MEMCPY = 1,    /* one dimension, stride 1 on both sides: the page's
+                                memcpy case, run by the copy kernel (16-byte
+                                vectors) or, when the two ends are not
+                                16-byte aligned, by the strided kernel */
+    LMAD_COPY_BPC = 2,       /* power-of-two sizes and each side a permuted and/or
+                                reversed block of 2^n elements: one BPC through the
+                                tiled BMMC kernel (as bmmc_lmad_copy) */
+    LMAD_COPY_TRANSPOSE = 3, /* the unit-stride source dimension is not the unit-
+                                stride destination dimension: a batched tiled
+                                transpose through shared memory over those two
+                                dimensions, the others as the batch (the page's
+                                transpose and "map transpose" cases, any sizes) */
+    LMAD_COPY_STRIDED = 4    /* anything else: the page's stride-sorted copy, one
+                                thread per index tuple, adjacent threads adjacent
+                                along the smallest source stride */
+} lmad_copy_kind;
+
+typedef struct {
+    int kind;                          /* lmad_copy_kind */
+    int ndims;                         /* dimensions after steps 1-3 */
+    int64_t sizes[LMAD_MAX_DIMS];      /* ... fastest (smallest source stride) first */
+    int64_t in_strides[LMAD_MAX_DIMS];
+    int64_t out_strides[LMAD_MAX_DIMS];
+    int64_t in_offset, out_offset;     /* offsets of index tuple 0 after step 1 */
+    int vec;                           /* STRIDED / MEMCPY fallback: elements moved as one
+                                          word of vec * elem_size bytes (1 when not widened) */
+    int transpose_out_dim;             /* TRANSPOSE: the dimension (index into sizes) with
+                                          destination stride +-1; the source one is 0.  -1
+                                          for other kinds */
+    uint64_t elements;                 /* index tuples copied (product of the sizes) */
+} lmad_copy_info_t;
+
+/* Analyse the copy lmad_copy would run with the same arguments, without
+ * touching memory or the device.  in / out are used for their alignment and
+ * overlap only and may be NULL (taken as aligned, not overlapping).  Errors:
+ *   INVALID_ARG       ndims < 0 or > 64, a size < 0, a null sizes / strides
+ *                     array with ndims > 0, an offset outside [0, in_elems) /
+ *                     [0, out_elems) for some index tuple, a destination LMAD
+ *                     that is not provably one-to-one (sorted by |stride|,
+ *                     each |out_stride| must exceed the span of the faster
+ *                     dimensions: every array layout made of permuted, sliced
+ *                     and reversed dimensions passes), more than 2^40 tuples,
+ *                     or more than LMAD_MAX_DIMS dimensions after step 3;
+ *   UNSUPPORTED_ELEM  elem_size not in {1, 2, 4, 8, 16};
+ *   MISALIGNED        in or out not aligned to elem_size;
+ *   ALIAS             the element ranges the two LMADs touch overlap. */
+bmmc_status lmad_copy_query(int ndims, const int64_t *sizes, int64_t in_offset,
+                            const int64_t *in_strides, size_t in_elems, int64_t out_offset,
+                            const int64_t *out_strides, size_t out_elems, size_t elem_size,
+                            const void *in, const void *out, lmad_copy_info_t *info);
+
+/* Run the copy (arguments as lmad_copy_query; in holds in_elems and out
+ * out_elems elements of elem_size bytes, caller-owned, reachable by the GPU
+ * as for bmmc_permute).  Enqueued on `stream`, no allocation, no CPU
+ * fallback.  Errors as lmad_copy_query, plus CUDA. */
+bmmc_status lmad_copy(int ndims, const int64_t *sizes, int64_t in_offset,
+                      const int64_t *in_strides, size_t in_elems, int64_t out_offset,
+                      const int64_t *out_strides, size_t out_elems, size_t elem_size,
+                      const void *in, void *out, void *stream);
+
 /* Inverse of an invertible n x n bit matrix over F2 (rows as in bmmc_plan):
  * inv_rows_out receives A^-1, so permuting by (A^-1, A^-1.c) undoes (A, c).
  * Errors: INVALID_ARG, SINGULAR.  Host only. */

@@ -1,0 +1,210 @@
+"""General LMAD copies on the GPU against the oracle's copy loop, byte for
+byte ("Speeding up GPU copies by permuting iteration spaces", Futhark blog).
+
+Every case fills the destination with a sentinel first, so positions the
+copy must leave alone are checked too.  Kinds covered: memcpy (aligned and
+not), BPC, batched transpose (ragged tiles, negative strides, batch
+dimensions), stride-sorted copies with 1 to 6 dimensions, broadcasts, all
+five element sizes, 32- and 64-bit index paths, and the page's eight
+workloads at full size."""
+
+import numpy as np
+import pytest
+
+import bmmc_index_transforms_gb300 as bm
+from bmmc_index_transforms_gb300 import synth
+from oracle import reference as ref
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _fill(n_elems, elem, seed):
+    """n_elems elements of elem bytes, rows of a uint8 array, distinct bytes
+    patterns (a multiplicative hash of the byte index and the seed)."""
+    i = np.arange(n_elems * elem, dtype=np.uint64)
+    salt = np.uint64((seed * 0x632BE59BD9B4E019 + 1) & ((1 << 64) - 1))
+    with np.errstate(over="ignore"):
+        b = (i * np.uint64(0x9E3779B97F4A7C15) + salt) >> np.uint64(56)
+    return b.astype(np.uint8).reshape(n_elems, elem)
+
+
+def _run(w, elem, seed=0):
+    src = _fill(w["in_elems"], elem, seed)
+    dst = np.full((w["out_elems"], elem), 0xA5, dtype=np.uint8)
+    d_src = torch.from_numpy(src.reshape(-1)).cuda()
+    d_dst = torch.from_numpy(dst.reshape(-1)).cuda()
+    bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem, d_src, d_dst)
+    torch.cuda.synchronize()
+    got = d_dst.cpu().numpy().reshape(w["out_elems"], elem)
+    want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
+                                 src, dst)
+    return got, want
+
+
+def _check(w, elem, seed=0):
+    got, want = _run(w, elem, seed)
+    bad = np.nonzero((got != want).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} elements differ, first at {bad[:5]}; {w}"
+
+
+@pytest.mark.parametrize("seed", range(150))
+def test_random_views(seed):
+    w = synth.draw_lmad_view(seed)
+    _check(w, (1, 2, 4, 8, 16)[seed % 5], seed)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_views_larger(seed):
+    """Views of up to 2^20 elements: several blocks of every kernel."""
+    w = synth.draw_lmad_view(1000 + seed, max_dims=5, max_elems=1 << 20)
+    _check(w, (4, 8, 16, 1, 2)[seed % 5], seed)
+
+
+@pytest.mark.parametrize("kind,shape", [("slice_2d", (97, 130)), ("slice_2d", (1031, 5)), ("slice_2d", (3, 4099)),
+                                        ("slice_3d", (7, 33, 65)), ("slice_3d", (640, 32, 33)),
+                                        ("reversed_rows", (64, 128)), ("reversed_rows", (100, 37)),
+                                        ("reversed_rows", (1 << 12, 4))])
+@pytest.mark.parametrize("elem", [4, 8])
+def test_page_workloads_reduced(kind, shape, elem):
+    _check(synth.page_lmad_workload(kind, shape), elem)
+
+
+@pytest.mark.parametrize("kind,shape", synth.LMAD_PAGE_WORKLOADS)
+def test_page_workloads_full_size(kind, shape):
+    """The "Impact" section's shapes, int32, the whole output compared."""
+    w = synth.page_lmad_workload(kind, shape)
+    src = np.arange(w["in_elems"], dtype=np.int32)
+    d_src = torch.from_numpy(src).cuda()
+    d_dst = torch.full((w["out_elems"],), -7, dtype=torch.int32, device="cuda")
+    bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4, d_src, d_dst)
+    torch.cuda.synchronize()
+    want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
+                                 src, np.full(w["out_elems"], -7, dtype=np.int32))
+    assert np.array_equal(d_dst.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("shape,perm", [((33, 65), (1, 0)), ((5, 31, 97), (0, 2, 1)), ((31, 5, 97), (2, 1, 0)),
+                                        ((3, 40, 7, 70), (1, 3, 0, 2)), ((2, 3, 4, 5, 6, 7), (5, 3, 1, 0, 2, 4)),
+                                        ((1000, 3), (1, 0)), ((3, 1000), (1, 0)), ((1, 64, 1, 96), (3, 1, 2, 0))])
+@pytest.mark.parametrize("elem", [1, 2, 4, 8, 16])
+def test_axis_permutations_any_sizes(shape, perm, elem):
+    """x.permute(perm) made contiguous for odd shapes: the destination's
+    strides are the row-major strides of the permuted shape (transposes with
+    batch dimensions, ragged tiles)."""
+    src_strides = synth.row_major_strides(shape)
+    out_shape = [shape[p] for p in perm]
+    out_rm = synth.row_major_strides(out_shape)
+    out_strides = [0] * len(shape)
+    for pos, p in enumerate(perm):
+        out_strides[p] = out_rm[pos]
+    total = int(np.prod(shape))
+    w = dict(sizes=list(shape), in_offset=0, in_strides=src_strides, in_elems=total, out_offset=0,
+             out_strides=out_strides, out_elems=total)
+    got, want = _run(w, elem)
+    assert np.array_equal(got, want)
+    if elem == 4:  # and it is numpy's transpose
+        src = _fill(total, 4, 0).view(np.uint32).reshape(shape)
+        assert np.array_equal(got.view(np.uint32).reshape(out_shape), np.transpose(src, perm))
+
+
+def test_reversed_destination_transpose_and_broadcast():
+    # transpose into a destination walked backwards on both axes
+    R, C = 45, 77
+    w = dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C,
+             out_offset=R * C - 1, out_strides=[-1, -R], out_elems=R * C)
+    assert bm.lmad_copy_query(w["sizes"], 0, w["in_strides"], w["out_offset"], w["out_strides"], 4,
+                              in_elems=R * C, out_elems=R * C)["kind"] == "transpose"
+    _check(w, 4)
+    # broadcast a row to every row of a matrix (source stride 0)
+    w = dict(sizes=[300, 70], in_offset=3, in_strides=[0, 1], in_elems=80, out_offset=0, out_strides=[70, 1],
+             out_elems=21000)
+    _check(w, 8)
+    # a column broadcast: source stride 0 on the fast destination dimension
+    w = dict(sizes=[300, 70], in_offset=0, in_strides=[1, 0], in_elems=300, out_offset=0, out_strides=[70, 1],
+             out_elems=21000)
+    _check(w, 4)
+
+
+@pytest.mark.parametrize("offset_elems", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("elem", [1, 2, 4, 8, 16])
+def test_memcpy_aligned_and_not(offset_elems, elem):
+    """One contiguous run: the copy kernel when both ends are 16-byte
+    aligned, the strided kernel (widened where it can) when not."""
+    n = 100003
+    w = dict(sizes=[n], in_offset=offset_elems, in_strides=[1], in_elems=n + 8, out_offset=(3 * offset_elems) % 7,
+             out_strides=[1], out_elems=n + 8)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "memcpy"
+    _check(w, elem)
+
+
+def test_bpc_route_matches_oracle():
+    """Power-of-two sizes that permute and reverse a block go through one BPC."""
+    shape, perm = (8, 16, 32), (2, 0, 1)
+    src_strides = synth.row_major_strides(shape)
+    out_rm = synth.row_major_strides([shape[p] for p in perm])
+    out_strides = [0, 0, 0]
+    for pos, p in enumerate(perm):
+        out_strides[p] = out_rm[pos]
+    total = 8 * 16 * 32
+    # reverse axis 1 on the source, and place the whole block at an offset of 64 elements
+    w = dict(sizes=list(shape), in_offset=15 * 32, in_strides=[512, -32, 1], in_elems=total,
+             out_offset=64, out_strides=out_strides, out_elems=total + 128)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "bpc"
+    _check(w, 4)
+    _check(w, 16)
+
+
+def test_64bit_index_paths():
+    """Spans beyond 2^31 elements take the 64-bit kernels: a 1-byte view
+    whose rows lie 2^31 + 5 bytes apart (a 4 GiB source)."""
+    if torch.cuda.get_device_properties(0).total_memory < (24 << 30):
+        pytest.skip("needs a large device")
+    gap = (1 << 31) + 5
+    in_elems = 2 * gap + 64
+    d_src = torch.empty(in_elems, dtype=torch.uint8, device="cuda")
+    rows = [0, gap, 2 * gap]
+    for r, off in enumerate(rows):
+        d_src[off: off + 64] = torch.arange(64, dtype=torch.uint8, device="cuda") + 64 * r
+    # strided: 3 rows of 60 bytes from offset 3 of each, into a dense 3 x 60
+    d_dst = torch.full((180,), 0xA5, dtype=torch.uint8, device="cuda")
+    q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [60, 1], 1, in_elems=in_elems, out_elems=180)
+    assert q["kind"] == "strided"
+    bm.lmad_copy([3, 60], 3, [gap, 1], 0, [60, 1], 1, d_src, d_dst)
+    want = np.concatenate([np.arange(3, 63) + 64 * r for r in range(3)]).astype(np.uint8)
+    assert np.array_equal(d_dst.cpu().numpy(), want)
+    # transpose: the same rows written as columns of a 60 x 3
+    d_dst2 = torch.full((180,), 0xA5, dtype=torch.uint8, device="cuda")
+    q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [1, 3], 1, in_elems=in_elems, out_elems=180)
+    assert q["kind"] == "transpose"
+    bm.lmad_copy([3, 60], 3, [gap, 1], 0, [1, 3], 1, d_src, d_dst2)
+    assert np.array_equal(d_dst2.cpu().numpy(), want.reshape(3, 60).T.ravel())
+    del d_src
+    torch.cuda.empty_cache()
+
+
+def test_empty_and_single_element():
+    d_src = torch.arange(10, dtype=torch.int32, device="cuda")
+    d_dst = torch.full((10,), -1, dtype=torch.int32, device="cuda")
+    bm.lmad_copy([4, 0], 0, [1, 1], 0, [1, 1], 4, d_src, d_dst)
+    bm.lmad_copy([], 7, [], 2, [], 4, d_src, d_dst)
+    torch.cuda.synchronize()
+    want = np.full(10, -1, np.int32)
+    want[2] = 7
+    assert np.array_equal(d_dst.cpu().numpy(), want)
+
+
+def test_errors_enqueue_nothing():
+    d_src = torch.arange(20, dtype=torch.int32, device="cuda")
+    d_dst = torch.full((20,), -1, dtype=torch.int32, device="cuda")
+    with pytest.raises(bm.BmmcError):
+        bm.lmad_copy([4, 5], 1, [5, 1], 0, [5, 1], 4, d_src, d_dst)  # source past its end
+    with pytest.raises(bm.BmmcError):
+        bm.lmad_copy([4, 5], 0, [5, 1], 0, [5, 1], 4, d_src, d_src)  # in place
+    torch.cuda.synchronize()
+    assert (d_dst.cpu().numpy() == -1).all()

@@ -1,0 +1,149 @@
+"""Host side of the general LMAD copy, through the C ABI (no GPU needed):
+the library's analysis against the oracle's restatement of the page's
+(flip, drop singletons, sort, collapse), the kind each of the page's cases
+gets, and every rejection."""
+
+import pytest
+
+import bmmc_index_transforms_gb300 as bm
+from bmmc_index_transforms_gb300 import _capi, synth
+from oracle import reference as ref
+
+
+def _query(w, elem=4, inp=None, out=None):
+    return bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                              inp, out, in_elems=w["in_elems"], out_elems=w["out_elems"])
+
+
+def _expect_normalised(w, q):
+    dims, io, oo = ref.lmad_normalize(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],
+                                      w["out_strides"])
+    if not dims:  # a single element is reported as one dimension of size 1
+        dims = [[1, 1, 1]]
+    assert q["dims"] == dims
+    assert (q["in_offset"], q["out_offset"]) == (io, oo)
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_analysis_matches_the_oracle_on_random_views(seed):
+    w = synth.draw_lmad_view(seed)
+    q = _query(w)
+    _expect_normalised(w, q)
+    n = 1
+    for v in w["sizes"]:
+        n *= v
+    assert q["elements"] == n
+
+
+@pytest.mark.parametrize("kind,shape", synth.LMAD_PAGE_WORKLOADS)
+def test_page_workloads(kind, shape):
+    """slice_2d / slice_3d keep the page's sorted order and run as the
+    stride-sorted copy (unit stride on both sides along the sliced axis);
+    reversed_rows of power-of-two rows is one BPC."""
+    w = synth.page_lmad_workload(kind, shape)
+    q = _query(w)
+    _expect_normalised(w, q)
+    if kind == "reversed_rows":
+        assert q["kind"] == "bpc"
+    else:
+        assert q["kind"] == "strided"
+        assert q["dims"][0][1:] == [1, 1]
+
+
+def test_page_layout_examples():
+    row, col = (5, 1), (1, 4)  # [4][5] row-major and column-major
+    q = bm.lmad_copy_query((4, 5), 0, row, 0, col, 4, in_elems=20, out_elems=20)
+    assert q["kind"] == "transpose" and q["dims"] == [[5, 1, 4], [4, 5, 1]] and q["transpose_out_dim"] == 1
+    q = bm.lmad_copy_query((4, 5), 0, row, 0, row, 4, in_elems=20, out_elems=20)
+    assert q["kind"] == "memcpy" and q["dims"] == [[20, 1, 1]]
+    # the same with odd sizes: still one transpose, batch dimension kept apart
+    q = bm.lmad_copy_query((3, 7, 9), 0, (63, 9, 1), 0, (63, 1, 7), 4, in_elems=189, out_elems=189)
+    assert q["kind"] == "transpose" and q["dims"] == [[9, 1, 7], [7, 9, 1], [3, 63, 63]]
+
+
+def test_kinds_and_widening():
+    # reversed rows with a non-power-of-two row: stride-sorted, coalesced on both sides
+    q = bm.lmad_copy_query((8, 6), 5, (6, -1), 0, (6, 1), 4, in_elems=48, out_elems=48)
+    assert q["kind"] == "strided" and q["dims"] == [[6, 1, -1], [8, 6, 6]]
+    # 16-byte words: rows of 8 int32 sliced out of rows of 12, aligned
+    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, in_elems=60, out_elems=40)
+    assert q["kind"] == "strided" and q["vec"] == 4
+    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, 16, 1 << 20, in_elems=60, out_elems=40)
+    assert q["vec"] == 4
+    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, 4, 1 << 20, in_elems=60, out_elems=40)
+    assert q["vec"] == 1  # source tuple 0 at byte 20 of a 4-aligned buffer
+    q = bm.lmad_copy_query((5, 8), 1, (12, 1), 0, (8, 1), 4, in_elems=60, out_elems=40)
+    assert q["vec"] == 1
+    # broadcast source (stride 0) is allowed
+    q = bm.lmad_copy_query((4, 6), 0, (0, 1), 0, (6, 1), 8, in_elems=6, out_elems=24)
+    assert q["kind"] == "strided"
+    # empty
+    q = bm.lmad_copy_query((4, 0, 3), 0, (1, 1, 1), 0, (1, 1, 1), 4, in_elems=0, out_elems=0)
+    assert q["kind"] == "empty" and q["ndims"] == 0
+    # one element, no dimensions
+    q = bm.lmad_copy_query((), 3, (), 5, (), 2, in_elems=4, out_elems=6)
+    assert q["kind"] == "memcpy" and q["dims"] == [[1, 1, 1]] and q["in_offset"] == 3
+
+
+def _status(fn):
+    try:
+        fn()
+    except bm.BmmcError as e:
+        return e.status
+    return _capi.OK
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(sizes=(4, 5), io=1, si=(5, 1), oo=0, so=(5, 1), ie=20, oe=20), _capi.ERR_INVALID_ARG),   # source past end
+    (dict(sizes=(4, 5), io=0, si=(5, 1), oo=0, so=(5, 1), ie=20, oe=19), _capi.ERR_INVALID_ARG),   # dest past end
+    (dict(sizes=(4, 5), io=4, si=(5, -1), oo=0, so=(5, 1), ie=19, oe=20), _capi.ERR_INVALID_ARG),  # walks past end
+    (dict(sizes=(4, 5), io=0, si=(5, 1), oo=0, so=(0, 1), ie=20, oe=20), _capi.ERR_INVALID_ARG),   # dest stride 0
+    (dict(sizes=(4, 5), io=0, si=(5, 1), oo=0, so=(4, 1), ie=20, oe=20), _capi.ERR_INVALID_ARG),   # dest overlaps
+    (dict(sizes=(3, 2), io=0, si=(2, 1), oo=0, so=(2, 3), ie=6, oe=10), _capi.ERR_INVALID_ARG),    # not provable
+    (dict(sizes=(4, -1), io=0, si=(5, 1), oo=0, so=(5, 1), ie=20, oe=20), _capi.ERR_INVALID_ARG),  # negative size
+    (dict(sizes=(4, 5), io=-1, si=(5, 1), oo=0, so=(5, 1), ie=20, oe=20), _capi.ERR_INVALID_ARG),  # before start
+])
+def test_rejections(case, status):
+    c = case
+    assert _status(lambda: bm.lmad_copy_query(c["sizes"], c["io"], c["si"], c["oo"], c["so"], 4,
+                                              in_elems=c["ie"], out_elems=c["oe"])) == status
+
+
+def test_rejections_elem_alias_alignment_and_limits():
+    q = lambda e=4, a=None, b=None, **kw: bm.lmad_copy_query(  # noqa: E731
+        kw.get("sizes", (4, 5)), 0, kw.get("si", (5, 1)), 0, kw.get("so", (1, 4)), e, a, b,
+        in_elems=kw.get("ie", 20), out_elems=kw.get("oe", 20))
+    assert _status(lambda: q(3)) == _capi.ERR_UNSUPPORTED_ELEM
+    assert _status(lambda: q(32)) == _capi.ERR_UNSUPPORTED_ELEM
+    for e in (1, 2, 4, 8, 16):
+        assert _status(lambda: q(e)) == _capi.OK
+    assert _status(lambda: q(4, 0x1002, 0x8000)) == _capi.ERR_MISALIGNED
+    assert _status(lambda: q(4, 0x1000, 0x1000 + 76)) == _capi.ERR_ALIAS       # last source element
+    assert _status(lambda: q(4, 0x1000, 0x1000 + 80)) == _capi.OK
+    assert _status(lambda: q(4, 0x1000 + 80, 0x1000)) == _capi.OK
+    # 17 dimensions that do not collapse (destination strides 3^k)
+    d = 17
+    sizes, si, so = [2] * d, [1 << k for k in range(d)], [3 ** k for k in range(d)]
+    assert _status(lambda: bm.lmad_copy_query(sizes, 0, si, 0, so, 1, in_elems=1 << d,
+                                              out_elems=3 ** d)) == _capi.ERR_INVALID_ARG
+    assert _status(lambda: bm.lmad_copy_query(sizes[:16], 0, si[:16], 0, so[:16], 1, in_elems=1 << 16,
+                                              out_elems=3 ** 16)) == _capi.OK
+    # more than 2^40 index tuples
+    big = (1 << 20, 1 << 21)
+    assert _status(lambda: bm.lmad_copy_query(big, 0, (0, 0), 0, (1 << 21, 1), 1, in_elems=1,
+                                              out_elems=1 << 41)) == _capi.ERR_INVALID_ARG
+    assert _status(lambda: bm.lmad_copy_query([1] * 65, 0, [1] * 65, 0, [1] * 65, 4, in_elems=1,
+                                              out_elems=1)) == _capi.ERR_INVALID_ARG
+
+
+def test_copy_without_device_fails_loudly():
+    """No CPU fallback: without a reachable device the copy call errors."""
+    import numpy as np
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    a = np.arange(20, dtype=np.int32)
+    b = np.zeros(20, dtype=np.int32)
+    assert _status(lambda: bm.lmad_copy((4, 5), 0, (5, 1), 0, (1, 4), 4, a, b)) == _capi.ERR_CUDA
+    assert (b == 0).all()
