@@ -257,7 +257,10 @@ def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[i
     return {"kind": LMAD_KIND_NAMES.get(info.kind, str(info.kind)), "ndims": k,
             "dims": [[int(info.sizes[i]), int(info.in_strides[i]), int(info.out_strides[i])] for i in range(k)],
             "in_offset": int(info.in_offset), "out_offset": int(info.out_offset), "vec": int(info.vec),
-            "transpose_out_dim": int(info.transpose_out_dim), "elements": int(info.elements)}
+            "transpose_out_dim": int(info.transpose_out_dim),
+            "group_a": [i for i in range(k) if (info.group_a >> i) & 1],
+            "group_b": [i for i in range(k) if (info.group_b >> i) & 1],
+            "tile": (int(info.tile_a), int(info.tile_b)), "elements": int(info.elements)}
 
 
 def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,

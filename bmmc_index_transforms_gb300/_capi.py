@@ -66,7 +66,8 @@ class LmadCopyInfo(ctypes.Structure):
                 ("sizes", ctypes.c_int64 * LMAD_MAX_DIMS), ("in_strides", ctypes.c_int64 * LMAD_MAX_DIMS),
                 ("out_strides", ctypes.c_int64 * LMAD_MAX_DIMS), ("in_offset", ctypes.c_int64),
                 ("out_offset", ctypes.c_int64), ("vec", ctypes.c_int), ("transpose_out_dim", ctypes.c_int),
-                ("elements", ctypes.c_uint64)]
+                ("group_a", ctypes.c_uint32), ("group_b", ctypes.c_uint32), ("tile_a", ctypes.c_int),
+                ("tile_b", ctypes.c_int), ("elements", ctypes.c_uint64)]
 
 
 # name -> (restype, argtypes); every function declared in include/bmmc.h

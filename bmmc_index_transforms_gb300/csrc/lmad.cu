@@ -64,14 +64,16 @@ struct LmadStridedParams {
     int64_t sin[kLmadMaxDims], sout[kLmadMaxDims];
 };
 
-struct LmadTransposeParams {
-    uint64_t tiles;          // tiles_a * tiles_b * batch
-    LmadDiv div_a, div_b;    // tiles along a, tiles along b
-    int64_t n_a, n_b;        // sizes of the source (a) and destination (b) unit-stride dims
-    int64_t s_b, t_a, t_b;   // source stride of b; destination strides of a and b
-    int nb;                  // batch dimensions
-    LmadDiv div[kLmadMaxDims];
-    int64_t sin[kLmadMaxDims], sout[kLmadMaxDims];
+struct LmadTileParams {
+    uint64_t tiles;            // tiles_a * tiles_b * batch
+    uint64_t n_a, n_b;         // flat sizes of groups A and B
+    int la, lb;                // log2 of the tile sides TA, TB
+    LmadDiv div_ta, div_tb;    // tiles along A, tiles along B
+    int na, nb, nc;            // dimensions in A, in B, in the batch (fastest first)
+    LmadDiv adiv[kLmadMaxDims], bdiv[kLmadMaxDims], cdiv[kLmadMaxDims];
+    int64_t as[kLmadMaxDims], at[kLmadMaxDims];   // source / destination strides of A
+    int64_t bs[kLmadMaxDims], bt[kLmadMaxDims];
+    int64_t cs[kLmadMaxDims], ct[kLmadMaxDims];
 };
 
 // ---------------------------------------------------------------------------
@@ -136,54 +138,225 @@ __global__ void __launch_bounds__(256)
         if (base + (uint64_t)j * 256u < p.total) __stcs(out + dst[j], v[j]);
 }
 
-// Batched transpose of 32 x 32 tiles.  Dimension a has source stride 1 and
-// dimension b destination stride +-1; a block loads a tile with warps along
-// a (coalesced reads), and stores it with warps along b (coalesced writes),
-// through a padded shared tile (column reads hit 32 distinct banks).  Tile
-// index = ta + tiles_a * (tb + tiles_b * batch); the batch index unpacks over
-// the remaining dimensions.  Ragged edges are masked.
-template <typename W, bool WIDE>
-__global__ void __launch_bounds__(256)
-    lmad_transpose_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTransposeParams p) {
+// Tile shapes of the transpose kernel per word size: T elements per tile,
+// shared-memory row padding and the elements per thread staged in registers
+// at a time.  The default A x B shape (64 x 64, or 32 x 32 for 8- and
+// 16-byte words) is chosen on the host (tile_shape_log2).  Either side shrinks to the size of a short group
+// (not below 16) and the other grows, keeping TA * TB = T, so both sides
+// stay within [16, T / 16].
+template <int BYTES> struct TileShape;
+template <> struct TileShape<1> { static constexpr int T = 4096, PAD = 4, CH = 8; };
+template <> struct TileShape<2> { static constexpr int T = 4096, PAD = 2, CH = 8; };
+template <> struct TileShape<4> { static constexpr int T = 4096, PAD = 1, CH = 8; };
+template <> struct TileShape<8> { static constexpr int T = 1024, PAD = 1, CH = 4; };
+template <> struct TileShape<16> { static constexpr int T = 1024, PAD = 1, CH = 4; };
+constexpr int kMinTileSide = 16;
+// Word sizes (a mask of 4, 8, 16) whose load phase uses cp.async; the others
+// stage through registers.
+#ifndef LMAD_TILE_ASYNC_WORDS
+#define LMAD_TILE_ASYNC_WORDS (4 | 8 | 16)
+#endif
+
+
+// One asynchronous global -> shared copy of a 4-, 8- or 16-byte word
+// (cp.async; 16-byte words bypass L1).  Both addresses are aligned to the
+// word: the tile is an array of words and the arrays are word-aligned.
+template <typename W>
+__device__ __forceinline__ void cp_async_word(W* smem, const W* gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    if constexpr (sizeof(W) == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(gmem), "n"((int)sizeof(W))
+                     : "memory");
+}
+
+// Offsets of a tile element (ia, ib) relative to the tile's origin, as an
+// A part plus a B part on each side.  TabAddr reads them from the tables a
+// block builds for multi-dimension groups; LinAddr computes them when each
+// group is one dimension (A has source stride 1).
+template <typename O>
+struct TabAddr {
+    const O *ts, *td;
+    int TA;
+    __device__ __forceinline__ O src_a(int ia) const { return ts[ia]; }
+    __device__ __forceinline__ O src_b(int ib) const { return ts[TA + ib]; }
+    __device__ __forceinline__ O dst_a(int ia) const { return td[ia]; }
+    __device__ __forceinline__ O dst_b(int ib) const { return td[TA + ib]; }
+};
+template <typename O>
+struct LinAddr {
+    O sb, ta, tb;  // source stride of B; destination strides of A and B
+    __device__ __forceinline__ O src_a(int ia) const { return (O)ia; }
+    __device__ __forceinline__ O src_b(int ib) const { return (O)ib * sb; }
+    __device__ __forceinline__ O dst_a(int ia) const { return (O)ia * ta; }
+    __device__ __forceinline__ O dst_b(int ib) const { return (O)ib * tb; }
+};
+
+// The two phases of one tile.  Both tile sides are at most 256 (T / 16), so
+// in the load phase a thread keeps one A-index (lanes along A) and steps
+// through B-indices, and in the store phase keeps one B-index and steps
+// through A-indices.  The load phase of 4- to 16-byte words issues every
+// element as an asynchronous copy into shared memory and waits once; 1- and
+// 2-byte words (which cp.async cannot copy) and the store phase run in
+// chunks of CH elements per thread staged in registers.  FULL: the tile has no
+// ragged edge, so no element needs a bounds test.
+template <typename W, bool FULL, typename Addr>
+__device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __restrict__ dst, W* tile, const Addr& ad,
+                                            int TA, int TB, int la, int lb, int ra, int rb) {
+    using S = TileShape<sizeof(W)>;
+    constexpr int E = S::T / 256, CH = S::CH;
+    static_assert(E % CH == 0, "chunks must tile a phase");
+    const int t = threadIdx.x, pitch = TA + S::PAD;
+    {
+        const int ia = t & (TA - 1), ib0 = t >> la, step = 256 >> la;
+        const W* s = src + ad.src_a(ia);
+        const bool ok = FULL || ia < ra;
+        if constexpr ((LMAD_TILE_ASYNC_WORDS & sizeof(W)) != 0) {
+            // asynchronous copies straight into shared memory: every load of
+            // the phase in flight at once, no registers held (partly
+            // unrolled so that addresses are not all computed up front)
+#pragma unroll 4
+            for (int r = 0; r < E; ++r) {
+                const int ib = ib0 + r * step;
+                if (FULL || (ok && ib < rb)) cp_async_word(&tile[ib * pitch + ia], s + ad.src_b(ib));
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        } else {
+#pragma unroll 1
+            for (int c = 0; c < E; c += CH) {
+                W v[CH];
+#pragma unroll
+                for (int r = 0; r < CH; ++r) {
+                    const int ib = ib0 + (c + r) * step;
+                    if (FULL || (ok && ib < rb)) v[r] = __ldg(s + ad.src_b(ib));
+                }
+#pragma unroll
+                for (int r = 0; r < CH; ++r) {
+                    const int ib = ib0 + (c + r) * step;
+                    if (FULL || (ok && ib < rb)) tile[ib * pitch + ia] = v[r];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    {
+        const int ib = t & (TB - 1), ia0 = t >> lb, step = 256 >> lb;
+        W* o = dst + ad.dst_b(ib);
+        const bool ok = FULL || ib < rb;
+#pragma unroll 1
+        for (int c = 0; c < E; c += CH) {
+            W v[CH];
+#pragma unroll
+            for (int r = 0; r < CH; ++r) {
+                const int ia = ia0 + (c + r) * step;
+                if (FULL || (ok && ia < ra)) v[r] = tile[ib * pitch + ia];
+            }
+#pragma unroll
+            for (int r = 0; r < CH; ++r) {
+                const int ia = ia0 + (c + r) * step;
+                if (FULL || (ok && ia < ra)) __stcs(o + ad.dst_a(ia), v[r]);
+            }
+        }
+    }
+}
+
+// Batched tiled transpose between two groups of dimensions.  Group A holds
+// the source's unit-stride dimension and the dimensions that continue it
+// contiguously in the source; group B the destination's unit-stride
+// dimension and those continuing it in the destination; the rest is the
+// batch.  A tile is TA consecutive A-indices x TB consecutive B-indices of
+// one batch index.  The block first tabulates, in shared memory, the source
+// and destination offsets of its TA A-indices and TB B-indices (an element's
+// offset is the A part plus the B part), then loads the tile with lanes
+// along A (consecutive source addresses), stores it into a padded shared
+// tile, and writes it out with lanes along B (consecutive destination
+// addresses).  Row pitch TA + PAD makes the column reads conflict-free.
+// Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
+// masked.
+template <typename W, bool WIDE, bool GENERAL>
+__global__ void __launch_bounds__(256, sizeof(W) >= 8 ? 6 : 1)
+    lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
-    __shared__ W tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    using S = TileShape<sizeof(W)>;
+    constexpr int kTab = S::T / kMinTileSide + kMinTileSide;  // >= TA + TB
+    __shared__ W tile[S::T + (S::T / kMinTileSide) * S::PAD];
+    __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
+    const int TA = 1 << p.la, TB = 1 << p.lb;
+    const int t = threadIdx.x;
     for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
         I x = (I)blk;
-        I q = div_q(x, p.div_a);
-        const O ta = (O)(x - q * (I)p.div_a.d);
+        I q = div_q(x, p.div_ta);
+        const I ta = x - q * (I)p.div_ta.d;
         x = q;
-        q = div_q(x, p.div_b);
-        const O tb = (O)(x - q * (I)p.div_b.d);
+        q = div_q(x, p.div_tb);
+        const I tb = x - q * (I)p.div_tb.d;
         x = q;
         O so = 0, d = 0;
-        for (int k = 0; k < p.nb; ++k) {
-            O r;
-            if (k + 1 < p.nb) {
-                q = div_q(x, p.div[k]);
-                r = (O)(x - q * (I)p.div[k].d);
+        for (int k = 0; k < p.nc; ++k) {
+            I r = x;
+            if (k + 1 < p.nc) {
+                q = div_q(x, p.cdiv[k]);
+                r = x - q * (I)p.cdiv[k].d;
                 x = q;
-            } else {
-                r = (O)x;
             }
-            so += r * (O)p.sin[k];
-            d += r * (O)p.sout[k];
+            so += (O)r * (O)p.cs[k];
+            d += (O)r * (O)p.ct[k];
         }
-        const O a0 = ta * 32, b0 = tb * 32;
-        const O ra = (O)p.n_a - a0, rb = (O)p.n_b - b0;  // valid extent of this tile
-        const W* src = in + so + a0 + b0 * (O)p.s_b;
-        W* dstp = out + d + a0 * (O)p.t_a + b0 * (O)p.t_b;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int ib = ty + 8 * r;
-            if (tx < ra && ib < rb) tile[ib][tx] = __ldg(src + tx + (O)ib * (O)p.s_b);
+        const I a0 = ta << p.la, b0 = tb << p.lb;
+        const int ra = (int)min((uint64_t)TA, p.n_a - (uint64_t)a0);
+        const int rb = (int)min((uint64_t)TB, p.n_b - (uint64_t)b0);
+        if constexpr (GENERAL) {
+            // offset tables of this tile's A- and B-indices
+            for (int i = t; i < TA + TB; i += 256) {
+                O ts = 0, td = 0;
+                if (i < TA) {
+                    if (i < ra) {
+                        I y = a0 + (I)i;
+                        for (int k = 0; k < p.na; ++k) {
+                            I r = y;
+                            if (k + 1 < p.na) {
+                                const I qq = div_q(y, p.adiv[k]);
+                                r = y - qq * (I)p.adiv[k].d;
+                                y = qq;
+                            }
+                            ts += (O)r * (O)p.as[k];
+                            td += (O)r * (O)p.at[k];
+                        }
+                    }
+                } else if (i - TA < rb) {
+                    I y = b0 + (I)(i - TA);
+                    for (int k = 0; k < p.nb; ++k) {
+                        I r = y;
+                        if (k + 1 < p.nb) {
+                            const I qq = div_q(y, p.bdiv[k]);
+                            r = y - qq * (I)p.bdiv[k].d;
+                            y = qq;
+                        }
+                        ts += (O)r * (O)p.bs[k];
+                        td += (O)r * (O)p.bt[k];
+                    }
+                }
+                tab_src[i] = ts;
+                tab_dst[i] = td;
+            }
+            __syncthreads();
         }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int ia = ty + 8 * r;
-            if (ia < ra && tx < rb) __stcs(dstp + (O)ia * (O)p.t_a + (O)tx * (O)p.t_b, tile[tx][ia]);
+        if constexpr (GENERAL) {
+            const TabAddr<O> ad{tab_src, tab_dst, TA};
+            if (ra == TA && rb == TB)
+                tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+            else
+                tile_phases<W, false>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+        } else {
+            const LinAddr<O> ad{(O)p.bs[0], (O)p.at[0], (O)p.bt[0]};
+            const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
+            W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
+            if (ra == TA && rb == TB)
+                tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+            else
+                tile_phases<W, false>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
         }
         __syncthreads();
     }
@@ -204,6 +377,10 @@ struct LmadCopy {
     int64_t in_off = 0, out_off = 0;
     uint64_t elements = 0;
     int tdim = -1;
+    // TRANSPOSE: the groups (indices into d, fastest first) and tile sides
+    int ga[kLmadMaxDims], gb[kLmadMaxDims], gc[kLmadMaxDims];
+    int na = 0, nb = 0, nc = 0;
+    int la = 0, lb = 0;
     // STRIDED / unaligned MEMCPY: the widened copy
     int vec = 1;
     // BPC
@@ -282,6 +459,75 @@ int widen_factor(const LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t ou
         if (ok) return v;
     }
     return 1;
+}
+
+int ceil_log2(uint64_t v) {
+    int l = 0;
+    while (l < 63 && (1ull << l) < v) ++l;
+    return l;
+}
+
+// Host copy of the tile shapes the transpose kernel is compiled with
+// (TileShape<BYTES>): log2 of T, TA and TB.
+void tile_shape_log2(size_t word, int* lt, int* la, int* lb) {
+    switch (word) {
+        case 1: *lt = 12, *la = 6, *lb = 6; return;
+        case 2: *lt = 12, *la = 6, *lb = 6; return;
+        case 4: *lt = 12, *la = 6, *lb = 6; return;
+        case 8: *lt = 10, *la = 5, *lb = 5; return;
+        default: *lt = 10, *la = 5, *lb = 5; return;
+    }
+}
+
+// Groups of the transpose: A = d[0] (source stride 1) and the dimensions
+// continuing it contiguously in the source, stopping at the destination's
+// unit-stride dimension tdim; B = tdim and the dimensions continuing it
+// contiguously in the destination; C = the rest.  Tile sides: the default
+// shape, or a side shrunk to a short group (not below 16) and the other
+// grown so that the tile still holds T elements.
+void choose_groups(LmadCopy& C, size_t word) {
+    bool used[64] = {};
+    C.na = C.nb = C.nc = 0;
+    C.ga[C.na++] = 0;
+    used[0] = true;
+    for (int k = 1; k < C.nd && k != C.tdim; ++k) {
+        const Dim& l = C.d[C.ga[C.na - 1]];
+        if (C.d[k].s != l.s * l.n) break;
+        C.ga[C.na++] = k;
+        used[k] = true;
+    }
+    C.gb[C.nb++] = C.tdim;
+    used[C.tdim] = true;
+    for (;;) {
+        const Dim& l = C.d[C.gb[C.nb - 1]];
+        int next = -1;
+        for (int k = 0; k < C.nd && next < 0; ++k)
+            if (!used[k] && iabs(C.d[k].t) == iabs(l.t) * (uint64_t)l.n) next = k;
+        if (next < 0) break;
+        C.gb[C.nb++] = next;
+        used[next] = true;
+    }
+    for (int k = 0; k < C.nd; ++k)
+        if (!used[k]) C.gc[C.nc++] = k;
+    uint64_t n_a = 1, n_b = 1;
+    for (int k = 0; k < C.na; ++k) n_a *= (uint64_t)C.d[C.ga[k]].n;
+    for (int k = 0; k < C.nb; ++k) n_b *= (uint64_t)C.d[C.gb[k]].n;
+    int lt, la, lb;
+    tile_shape_log2(word, &lt, &la, &lb);
+    const int lmin = 4, lmax = lt - 4;  // sides within [16, T / 16]
+    const int pa = std::min(std::max(ceil_log2(n_a), lmin), lmax);
+    const int pb = std::min(std::max(ceil_log2(n_b), lmin), lmax);
+    // TA * TB = T always: the kernel's loops cover exactly T elements, and a
+    // group shorter than its side leaves a ragged (masked) tile
+    if (pa < la) {
+        la = pa;
+        lb = lt - la;
+    } else if (pb < lb) {
+        lb = pb;
+        la = lt - lb;
+    }
+    C.la = la;
+    C.lb = lb;
 }
 
 bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
@@ -385,6 +631,7 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
                 if (iabs(C.d[b].t) == 1) {
                     C.kind = LMAD_COPY_TRANSPOSE;
                     C.tdim = b;
+                    choose_groups(C, elem);
                     break;
                 }
     }
@@ -438,41 +685,63 @@ cudaError_t launch_strided_w(const W* in, W* out, const Dim* d, int nd, uint64_t
 
 template <typename W>
 cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStream_t stream) {
-    const Dim& a = C.d[0];
-    const Dim& b = C.d[C.tdim];
-    const uint64_t tiles_a = ((uint64_t)a.n + 31) / 32, tiles_b = ((uint64_t)b.n + 31) / 32;
-    uint64_t batch = 1;
-    for (int k = 1; k < C.nd; ++k)
-        if (k != C.tdim) batch *= (uint64_t)C.d[k].n;
+    uint64_t n_a = 1, n_b = 1, batch = 1;
+    for (int k = 0; k < C.na; ++k) n_a *= (uint64_t)C.d[C.ga[k]].n;
+    for (int k = 0; k < C.nb; ++k) n_b *= (uint64_t)C.d[C.gb[k]].n;
+    for (int k = 0; k < C.nc; ++k) batch *= (uint64_t)C.d[C.gc[k]].n;
+    const uint64_t tiles_a = (n_a + (1ull << C.la) - 1) >> C.la, tiles_b = (n_b + (1ull << C.lb) - 1) >> C.lb;
     const uint64_t tiles = tiles_a * tiles_b * batch;
-    // masked lanes of a ragged tile form addresses up to 32 rows / columns
-    // past the array's span; 32-bit offsets must hold those too
-    const uint64_t slack = 32 * (iabs(b.s) + iabs(a.t) + iabs(b.t) + 1);
-    const bool wide = tiles > 0xFFFFFFFFull || span_of(C.d, C.nd, false) + slack > 0x7FFFFFFFull ||
-                      span_of(C.d, C.nd, true) + slack > 0x7FFFFFFFull;
+    // masked lanes of a ragged tile form (unused) offsets up to one tile side
+    // past the span; 32-bit offsets must hold those too
+    uint64_t slack_in = 1ull << C.la, slack_out = 0;
+    for (int k = 0; k < C.na; ++k) slack_out += (1ull << C.la) * iabs(C.d[C.ga[k]].t);
+    for (int k = 0; k < C.nb; ++k) {
+        slack_in += (1ull << C.lb) * iabs(C.d[C.gb[k]].s);
+        slack_out += (1ull << C.lb) * iabs(C.d[C.gb[k]].t);
+    }
+    const bool wide = tiles > 0xFFFFFFFFull || n_a > 0xFFFFFFFFull || n_b > 0xFFFFFFFFull ||
+                      span_of(C.d, C.nd, false) + slack_in > 0x7FFFFFFFull ||
+                      span_of(C.d, C.nd, true) + slack_out > 0x7FFFFFFFull;
     const int bits = wide ? 64 : 32;
-    LmadTransposeParams p{};
+    LmadTileParams p{};
     p.tiles = tiles;
-    p.div_a = make_div(tiles_a, bits);
-    p.div_b = make_div(tiles_b, bits);
-    p.n_a = a.n;
-    p.n_b = b.n;
-    p.s_b = b.s;
-    p.t_a = a.t;
-    p.t_b = b.t;
-    p.nb = 0;
-    for (int k = 1; k < C.nd; ++k) {
-        if (k == C.tdim) continue;
-        p.div[p.nb] = make_div((uint64_t)C.d[k].n, bits);
-        p.sin[p.nb] = C.d[k].s;
-        p.sout[p.nb] = C.d[k].t;
-        ++p.nb;
+    p.n_a = n_a;
+    p.n_b = n_b;
+    p.la = C.la;
+    p.lb = C.lb;
+    p.div_ta = make_div(tiles_a, bits);
+    p.div_tb = make_div(tiles_b, bits);
+    p.na = C.na;
+    p.nb = C.nb;
+    p.nc = C.nc;
+    for (int k = 0; k < C.na; ++k) {
+        const Dim& x = C.d[C.ga[k]];
+        p.adiv[k] = make_div((uint64_t)x.n, bits);
+        p.as[k] = x.s;
+        p.at[k] = x.t;
+    }
+    for (int k = 0; k < C.nb; ++k) {
+        const Dim& x = C.d[C.gb[k]];
+        p.bdiv[k] = make_div((uint64_t)x.n, bits);
+        p.bs[k] = x.s;
+        p.bt[k] = x.t;
+    }
+    for (int k = 0; k < C.nc; ++k) {
+        const Dim& x = C.d[C.gc[k]];
+        p.cdiv[k] = make_div((uint64_t)x.n, bits);
+        p.cs[k] = x.s;
+        p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
-    if (wide)
-        lmad_transpose_kernel<W, true><<<grid, 256, 0, stream>>>(in, out, p);
+    const bool general = C.na > 1 || C.nb > 1;
+    if (wide && general)
+        lmad_tile_kernel<W, true, true><<<grid, 256, 0, stream>>>(in, out, p);
+    else if (wide)
+        lmad_tile_kernel<W, true, false><<<grid, 256, 0, stream>>>(in, out, p);
+    else if (general)
+        lmad_tile_kernel<W, false, true><<<grid, 256, 0, stream>>>(in, out, p);
     else
-        lmad_transpose_kernel<W, false><<<grid, 256, 0, stream>>>(in, out, p);
+        lmad_tile_kernel<W, false, false><<<grid, 256, 0, stream>>>(in, out, p);
     return cudaGetLastError();
 }
 
@@ -542,6 +811,12 @@ extern "C" bmmc_status lmad_copy_query(int ndims, const int64_t* sizes, int64_t 
     r.out_offset = C.out_off;
     r.vec = C.vec;
     r.transpose_out_dim = C.kind == LMAD_COPY_TRANSPOSE ? C.tdim : -1;
+    if (C.kind == LMAD_COPY_TRANSPOSE) {
+        for (int k = 0; k < C.na; ++k) r.group_a |= 1u << C.ga[k];
+        for (int k = 0; k < C.nb; ++k) r.group_b |= 1u << C.gb[k];
+        r.tile_a = 1 << C.la;
+        r.tile_b = 1 << C.lb;
+    }
     r.elements = C.elements;
     *info = r;
     return BMMC_OK;

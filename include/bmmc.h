@@ -317,9 +317,13 @@ typedef enum {
                                 tiled BMMC kernel (as bmmc_lmad_copy) */
     LMAD_COPY_TRANSPOSE = 3, /* the unit-stride source dimension is not the unit-
                                 stride destination dimension: a batched tiled
-                                transpose through shared memory over those two
-                                dimensions, the others as the batch (the page's
-                                transpose and "map transpose" cases, any sizes) */
+                                transpose through shared memory between group A
+                                (that source dimension and the dimensions continuing
+                                it contiguously in the source) and group B (the
+                                destination's unit-stride dimension and those
+                                continuing it in the destination), the other
+                                dimensions as the batch (the page's transpose and
+                                "map transpose" cases, any sizes) */
     LMAD_COPY_STRIDED = 4    /* anything else: the page's stride-sorted copy, one
                                 thread per index tuple, adjacent threads adjacent
                                 along the smallest source stride */
@@ -337,6 +341,14 @@ typedef struct {
     int transpose_out_dim;             /* TRANSPOSE: the dimension (index into sizes) with
                                           destination stride +-1; the source one is 0.  -1
                                           for other kinds */
+    uint32_t group_a, group_b;         /* TRANSPOSE: bit k set when dimension k is in group A
+                                          (dimension 0 and those continuing it contiguously
+                                          in the source) / group B (transpose_out_dim and
+                                          those continuing it contiguously in the
+                                          destination); the others are the batch.  0 for
+                                          other kinds */
+    int tile_a, tile_b;                /* TRANSPOSE: tile sides (A-indices x B-indices of one
+                                          batch index), powers of two; 0 for other kinds */
     uint64_t elements;                 /* index tuples copied (product of the sizes) */
 } lmad_copy_info_t;
 

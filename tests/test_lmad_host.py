@@ -147,3 +147,26 @@ def test_copy_without_device_fails_loudly():
     b = np.zeros(20, dtype=np.int32)
     assert _status(lambda: bm.lmad_copy((4, 5), 0, (5, 1), 0, (1, 4), 4, a, b)) == _capi.ERR_CUDA
     assert (b == 0).all()
+
+
+TILE_ELEMS = {1: 4096, 2: 4096, 4: 4096, 8: 1024, 16: 1024}
+
+
+@pytest.mark.parametrize("seed", range(300))
+def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
+    """The tile kernel's loops cover TA * TB = T elements per tile with both
+    sides in [16, T / 16]; the groups partition the dimensions, group A
+    starts at the unit source stride and group B at the unit destination
+    stride."""
+    w = synth.draw_lmad_view(5000 + seed, max_dims=5, max_elems=1 << 16)
+    elem = (1, 2, 4, 8, 16)[seed % 5]
+    q = _query(w, elem)
+    if q["kind"] != "transpose":
+        return
+    ta, tb = q["tile"]
+    T = TILE_ELEMS[elem]
+    assert ta * tb == T and 16 <= ta <= T // 16 and 16 <= tb <= T // 16
+    a, b = q["group_a"], q["group_b"]
+    assert a[0] == 0 and q["dims"][0][1] == 1
+    assert q["transpose_out_dim"] in b and abs(q["dims"][q["transpose_out_dim"]][2]) == 1
+    assert not set(a) & set(b)
