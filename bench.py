@@ -466,6 +466,42 @@ def run_ours(args):
     return 0
 
 
+# Times per copy the Futhark copy post prints ("Impact", with the stride
+# sorting) on an AMD RX 7900 XT, in microseconds: context, not a target.
+PAGE_US_RX7900XT = {
+    ("slice_2d", (8192, 8193)): 971, ("slice_2d", (65536, 1025)): 992,
+    ("slice_2d", (1048576, 65)): 990, ("slice_2d", (16777216, 5)): 1010,
+    ("slice_3d", (256, 256, 1025)): 1366, ("slice_3d", (65536, 32, 33)): 1364,
+    ("reversed_rows", (8192, 8192)): 996, ("reversed_rows", (16777216, 4)): 999,
+}
+
+
+def axes_lmad(synth, shape, perm):
+    """x.permute(perm) made contiguous, as a copy between two LMADs."""
+    out_rm = synth.row_major_strides([shape[p] for p in perm])
+    out_strides = [0] * len(shape)
+    for pos, p in enumerate(perm):
+        out_strides[p] = out_rm[pos]
+    total = 1
+    for v in shape:
+        total *= v
+    return dict(sizes=list(shape), in_offset=0, in_strides=synth.row_major_strides(shape), in_elems=total,
+                out_offset=0, out_strides=out_strides, out_elems=total)
+
+
+def lmad_case(torch, bm, w, a32, b32, stream, page_us=None):
+    """One general LMAD copy of int32 elements: mean of 30 back-to-back
+    launches; effective bytes = one read and one write of the destination."""
+    src, dst = a32[: w["in_elems"]], b32[: w["out_elems"]]
+    args = (w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4)
+    kind = bm.lmad_copy_query(*args, src, dst)["kind"]
+    ms, _, _ = time_launches(torch, lambda: bm.lmad_copy(*args, src, dst, stream), 30)
+    r = {"kind": kind, "us": round(ms * 1e3, 1), "gbs": round(2.0 * w["out_elems"] * 4 / (ms / 1e3) / 1e9, 1)}
+    if page_us:
+        r["page_us_rx7900xt"] = page_us
+    return r
+
+
 def other_configs(torch, bm, synth, dev, stream):
     """Effective GB/s of the other benchmark configurations.  Arrays larger
     than the L2: mean of 30 back-to-back launches.  Arrays that fit in it:
@@ -527,12 +563,6 @@ def other_configs(torch, bm, synth, dev, stream):
     scratch = torch.empty(1 << 28, dtype=torch.int32, device=dev)
     with bm.Plan(rows, c, 4, mode=1) as p:
         out["random_n28_int32_two_factor"] = big(28, 4, lambda: p.permute_scratch(a32, b32, scratch, stream))
-    # LMAD front end: Futhark's reversed_rows (copy (map reverse xss)) on
-    # [8192][8192] i32 and [2^24][4] i32, each one BPC
-    out["lmad_reversed_rows_8192x8192_int32"] = big(
-        26, 4, lambda: bm.bmmc_lmad_copy((13, 13), 8191, (8192, -1), 0, (8192, 1), 4, a32, b32, stream))
-    out["lmad_reversed_rows_2p24x4_int32"] = big(
-        26, 4, lambda: bm.bmmc_lmad_copy((24, 2), 3, (4, -1), 0, (4, 1), 4, a32, b32, stream))
     # the n=16 random map on 4096 arrays at once (batch_log2 = 12: 1 GiB in one launch)
     rows16, c16, _ = synth.draw_bmmc(0, 16, accept(16))
     with bm.Plan(rows16, c16, 4, batch_log2=12) as p:
@@ -548,6 +578,17 @@ def other_configs(torch, bm, synth, dev, stream):
         r = big(28, 4, parm_pass)
         out["parm_lowering_n28_int32_two_permutes"] = {"gbs_per_permute": round(2 * r["gbs"], 1),
                                                         "ms_both": r["ms"]}
+    # general LMAD copies: the "Impact" workloads of the Futhark copy post
+    # (copy xss[:, 1:], copy xsss[:, :, 1:], copy (map reverse xss) on i32),
+    # beside the page's own times with stride sorting on an AMD RX 7900 XT
+    # (context, another machine), and two transposes of odd sizes
+    for kind, shape in synth.LMAD_PAGE_WORKLOADS:
+        w = synth.page_lmad_workload(kind, shape)
+        out["lmad_" + kind + "_" + "x".join(map(str, shape)) + "_int32"] = lmad_case(
+            torch, bm, w, a32, b32, stream, PAGE_US_RX7900XT[(kind, tuple(shape))])
+    for name, shape, perm in (("t2d_8191x8193", (8191, 8193), (1, 0)),
+                              ("batched_64x1000x1000", (64, 1000, 1000), (0, 2, 1))):
+        out["lmad_" + name + "_int32"] = lmad_case(torch, bm, axes_lmad(synth, shape, perm), a32, b32, stream)
     del a, b, scratch, flush_buf
     torch.cuda.empty_cache()
     return out

@@ -456,7 +456,7 @@ const char* bmmc_status_string(bmmc_status status) {
         case BMMC_OK: return "ok";
         case BMMC_ERR_INVALID_ARG: return "invalid argument";
         case BMMC_ERR_SINGULAR: return "matrix is singular over F2 (not a permutation)";
-        case BMMC_ERR_UNSUPPORTED_ELEM: return "element size must be 4, 8 or 16 bytes";
+        case BMMC_ERR_UNSUPPORTED_ELEM: return "unsupported element size (4, 8 or 16 bytes; LMAD copies also 1 or 2)";
         case BMMC_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case BMMC_ERR_ALIAS: return "buffers overlap";
         case BMMC_ERR_CUDA: return "CUDA error";

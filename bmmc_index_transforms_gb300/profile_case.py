@@ -1,12 +1,17 @@
 """Run one permutation configuration a few times, for profilers.
 
     python -m bmmc_index_transforms_gb300.profile_case --kind random --n 26 --reps 3
+    python -m bmmc_index_transforms_gb300.profile_case --kind lmad_slice_2d --shape 8192,8193 --reps 2
 
 Kinds: random (seed), worst (seed, low 10 bits mapped to high bits), bitrev,
 complement (A = I, c on the high bits: contiguous tiles on both sides),
 transpose (square, n even), dims5 (the 5-D (4,2,0,3,1) permutation of a
 [32,64,64,64,32]-shaped array scaled to n bits), copy (the copy kernel on the
 same bytes), two_factor (seed, two passes through caller scratch).
+General LMAD copies (--shape, --elem): lmad_slice_2d, lmad_slice_3d,
+lmad_reversed_rows (the Futhark copy post's "Impact" functions on a
+row-major array of that shape) and lmad_transpose (the shape's axes
+reversed, made contiguous).
 Prints the plan and the CUDA-event time of each repetition.
 """
 
@@ -37,7 +42,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--kind", default="random",
                     choices=["random", "worst", "bitrev", "transpose", "dims5", "copy", "two_factor",
-                             "complement"])
+                             "complement", "lmad_slice_2d", "lmad_slice_3d", "lmad_reversed_rows",
+                             "lmad_transpose"])
     ap.add_argument("--n", type=int, default=26)
     ap.add_argument("--elem", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
@@ -45,7 +51,10 @@ def main(argv=None):
     ap.add_argument("--t-in", type=int, default=0)
     ap.add_argument("--t-out", type=int, default=0)
     ap.add_argument("--tile-bits", type=int, default=0)
+    ap.add_argument("--shape", default="8192,8193")
     a = ap.parse_args(argv)
+    if a.kind.startswith("lmad_"):
+        return lmad_case(a)
     n, elem = a.n, a.elem
     nbytes = (1 << n) * elem
     d_in = torch.arange(nbytes // 4, dtype=torch.int32, device="cuda")
@@ -95,6 +104,38 @@ def main(argv=None):
         print(f"rep {r}: {ms:.4f} ms, {2 * nbytes / ms / 1e6:.1f} GB/s effective")
     if plan:
         plan.close()
+    return 0
+
+
+def lmad_case(a):
+    shape = [int(v) for v in a.shape.split(",")]
+    e = a.elem
+    if a.kind == "lmad_transpose":
+        perm = list(range(len(shape)))[::-1]
+        out_rm = synth.row_major_strides([shape[p] for p in perm])
+        out_strides = [0] * len(shape)
+        for pos, p in enumerate(perm):
+            out_strides[p] = out_rm[pos]
+        total = 1
+        for v in shape:
+            total *= v
+        w = dict(sizes=shape, in_offset=0, in_strides=synth.row_major_strides(shape), in_elems=total,
+                 out_offset=0, out_strides=out_strides, out_elems=total)
+    else:
+        w = synth.page_lmad_workload(a.kind[len("lmad_"):], shape)
+    src = torch.empty(w["in_elems"] * e, dtype=torch.uint8, device="cuda")
+    dst = torch.empty(w["out_elems"] * e, dtype=torch.uint8, device="cuda")
+    args = (w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e)
+    print("analysis:", bm.lmad_copy_query(*args, src, dst))
+    stream = torch.cuda.current_stream()
+    for r in range(a.reps):
+        s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        bm.lmad_copy(*args, src, dst, stream)
+        t.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(t)
+        print(f"rep {r}: {ms:.4f} ms, {2 * w['out_elems'] * e / ms / 1e6:.1f} GB/s effective")
     return 0
 
 

@@ -49,7 +49,8 @@ typedef enum {
     BMMC_OK = 0,
     BMMC_ERR_INVALID_ARG = 1,     /* n out of range, stray bits, null pointer, bad option */
     BMMC_ERR_SINGULAR = 2,        /* A is not invertible over F2: the map is no permutation */
-    BMMC_ERR_UNSUPPORTED_ELEM = 3,/* elem_size not in {4, 8, 16} */
+    BMMC_ERR_UNSUPPORTED_ELEM = 3,/* elem_size not in {4, 8, 16} ({1, 2, 4, 8, 16} for
+                                     the LMAD copies) */
     BMMC_ERR_MISALIGNED = 4,      /* a device pointer is not 16-byte aligned */
     BMMC_ERR_ALIAS = 5,           /* in and out (or scratch) overlap */
     BMMC_ERR_CUDA = 6,            /* a CUDA runtime call or a launch failed */
