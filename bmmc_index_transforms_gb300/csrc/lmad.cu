@@ -275,7 +275,7 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 // Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
 // masked.
 template <typename W, bool WIDE, bool GENERAL>
-__global__ void __launch_bounds__(256, sizeof(W) >= 8 ? 6 : 1)
+__global__ void __launch_bounds__(256, sizeof(W) == 4 ? 8 : 6)
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
