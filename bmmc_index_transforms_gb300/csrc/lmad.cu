@@ -151,6 +151,11 @@ template <> struct TileShape<4> { static constexpr int T = 4096, PAD = 1, CH = 8
 template <> struct TileShape<8> { static constexpr int T = 1024, PAD = 1, CH = 4; };
 template <> struct TileShape<16> { static constexpr int T = 1024, PAD = 1, CH = 4; };
 constexpr int kMinTileSide = 16;
+// 4-byte words, single-dimension groups, 64 x 64 tiles: fetch rows as
+// 16-byte chunks (tile_phases_vec4).
+#ifndef LMAD_TILE_VEC4
+#define LMAD_TILE_VEC4 1
+#endif
 // Word sizes (a mask of 4, 8, 16) whose load phase uses cp.async; the others
 // stage through registers.
 #ifndef LMAD_TILE_ASYNC_WORDS
@@ -261,6 +266,70 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
     }
 }
 
+// The two phases of a whole 64 x 64 tile of 4-byte words with
+// single-dimension groups.  Each source row segment (64 elements) is fetched
+// as 16-byte aligned chunks with cp.async, 16 lanes per row; a row that does
+// not start on a 16-byte boundary (misalignment m = its first element's
+// offset from one, 1..3) leaves 4 elements in the partial chunks at its two
+// ends (4 - m at the head, m at the tail), which a second pass copies one
+// element per thread (64 rows x 4 = 256).  Row ib is kept in shared memory
+// shifted by its misalignment, in 17 chunk slots, chunk k at slot
+// (k + ib / 8) mod 17 (the rotation spreads the store phase's column reads,
+// 32 consecutive rows per warp, over the banks).  Row pitch 68 words.
+template <typename O>
+__device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ src, unsigned* __restrict__ dst,
+                                                 unsigned* tile, const LinAddr<O>& ad) {
+    constexpr int kPitch = 68, kSlots = 17;
+    const int t = threadIdx.x;
+    const unsigned base_mis = (unsigned)(((uintptr_t)src >> 2) & 3u);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int idx = t + 256 * r;
+        const int row = idx >> 4, kk = idx & 15;
+        const O s0 = ad.src_b(row);
+        const int m = (int)((base_mis + (unsigned)s0) & 3u);
+        if (m == 0 || kk < 15) {
+            const int k = kk + (m != 0);
+            int slot = k + (row >> 3);
+            slot -= slot >= kSlots ? kSlots : 0;
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + 4 * slot),
+                          reinterpret_cast<const uint4*>(src + s0 + (4 * k - m)));
+        }
+    }
+    {
+        const int row = t >> 2, j = t & 3;
+        const O s0 = ad.src_b(row);
+        const int m = (int)((base_mis + (unsigned)s0) & 3u);
+        if (m != 0) {
+            const int e = j < 4 - m ? j : 60 + j;  // head elements 0..3-m, tail 64-m..63
+            const int c = e + m;
+            int slot = (c >> 2) + (row >> 3);
+            slot -= slot >= kSlots ? kSlots : 0;
+            cp_async_word(tile + row * kPitch + 4 * slot + (c & 3), src + s0 + e);
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    const int ib = t & 63, ia0 = t >> 6;
+    const int m = (int)((base_mis + (unsigned)ad.src_b(ib)) & 3u);
+    const int rot = ib >> 3;
+    const unsigned* row = tile + ib * kPitch;
+    unsigned* o = dst + ad.dst_b(ib);
+#pragma unroll 1
+    for (int c0 = 0; c0 < 16; c0 += 8) {
+        unsigned v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int c = ia0 + 4 * (c0 + r) + m;
+            int slot = (c >> 2) + rot;
+            slot -= slot >= kSlots ? kSlots : 0;
+            v[r] = row[4 * slot + (c & 3)];
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) __stcs(o + ad.dst_a(ia0 + 4 * (c0 + r)), v[r]);
+    }
+}
+
 // Batched tiled transpose between two groups of dimensions.  Group A holds
 // the source's unit-stride dimension and the dimensions that continue it
 // contiguously in the source; group B the destination's unit-stride
@@ -274,14 +343,19 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 // addresses).  Row pitch TA + PAD makes the column reads conflict-free.
 // Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
 // masked.
-template <typename W, bool WIDE, bool GENERAL>
-__global__ void __launch_bounds__(256, sizeof(W) == 4 ? 8 : 6)
+// MODE: kTileTables (multi-dimension groups), kTileLinear (one dimension
+// each), kTileVec4 (one dimension each, 4-byte words, 64 x 64 tiles).
+enum { kTileLinear = 0, kTileTables = 1, kTileVec4 = 2 };
+
+template <typename W, bool WIDE, int MODE>
+__global__ void __launch_bounds__(256, MODE == kTileVec4 ? 6 : (sizeof(W) == 4 ? 8 : 6))
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     using S = TileShape<sizeof(W)>;
     constexpr int kTab = S::T / kMinTileSide + kMinTileSide;  // >= TA + TB
-    __shared__ W tile[S::T + (S::T / kMinTileSide) * S::PAD];
+    __shared__ __align__(16) W tile[S::T + (S::T / kMinTileSide) * S::PAD];  // 16-byte cp.async targets
+    constexpr bool GENERAL = MODE == kTileTables;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
@@ -353,10 +427,15 @@ __global__ void __launch_bounds__(256, sizeof(W) == 4 ? 8 : 6)
             const LinAddr<O> ad{(O)p.bs[0], (O)p.at[0], (O)p.bt[0]};
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
-            if (ra == TA && rb == TB)
-                tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
-            else
+            if (ra == TA && rb == TB) {
+                if constexpr (MODE == kTileVec4 && sizeof(W) == 4)
+                    tile_phases_vec4<O>(reinterpret_cast<const unsigned*>(src), reinterpret_cast<unsigned*>(dst),
+                                        reinterpret_cast<unsigned*>(tile), ad);
+                else
+                    tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+            } else {
                 tile_phases<W, false>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+            }
         }
         __syncthreads();
     }
@@ -733,15 +812,27 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
-    const bool general = C.na > 1 || C.nb > 1;
-    if (wide && general)
-        lmad_tile_kernel<W, true, true><<<grid, 256, 0, stream>>>(in, out, p);
-    else if (wide)
-        lmad_tile_kernel<W, true, false><<<grid, 256, 0, stream>>>(in, out, p);
-    else if (general)
-        lmad_tile_kernel<W, false, true><<<grid, 256, 0, stream>>>(in, out, p);
-    else
-        lmad_tile_kernel<W, false, false><<<grid, 256, 0, stream>>>(in, out, p);
+    const int mode = (C.na > 1 || C.nb > 1) ? kTileTables
+                     : (sizeof(W) == 4 && LMAD_TILE_VEC4 && C.la == 6 && C.lb == 6) ? kTileVec4
+                                                                                     : kTileLinear;
+#define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
+    if constexpr (sizeof(W) == 4) {
+        if (mode == kTileVec4) {
+            if (wide)
+                LMAD_TILE(true, kTileVec4);
+            else
+                LMAD_TILE(false, kTileVec4);
+            return cudaGetLastError();
+        }
+    }
+    if (wide) {
+        if (mode == kTileTables) LMAD_TILE(true, kTileTables);
+        else LMAD_TILE(true, kTileLinear);
+    } else {
+        if (mode == kTileTables) LMAD_TILE(false, kTileTables);
+        else LMAD_TILE(false, kTileLinear);
+    }
+#undef LMAD_TILE
     return cudaGetLastError();
 }
 

@@ -170,3 +170,49 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert a[0] == 0 and q["dims"][0][1] == 1
     assert q["transpose_out_dim"] in b and abs(q["dims"][q["transpose_out_dim"]][2]) == 1
     assert not set(a) & set(b)
+
+
+def _vec4_tile_emulation(base_mis, sb):
+    """The 4-byte whole-tile path of the tile kernel, replayed on the host: rows
+    of 64 elements fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
+    misaligned rows), the 4 leftover elements of a misaligned row one per
+    thread, rows kept shifted by their misalignment in 17 rotated chunk slots
+    of a 68-word pitch, then read back column-wise.  Every element is placed
+    exactly once, every 16-byte fetch is aligned, and every read returns the
+    element the transpose needs."""
+    pitch, slots = 68, 17
+    tile = {}
+    for t in range(256):
+        for r in range(4):
+            idx = t + 256 * r
+            row, kk = idx >> 4, idx & 15
+            m = (base_mis + row * sb) & 3
+            if m == 0 or kk < 15:
+                k = kk + (1 if m else 0)
+                assert (base_mis + row * sb + 4 * k - m) % 4 == 0
+                slot = (k + (row >> 3)) % slots
+                for j in range(4):
+                    a = row * pitch + 4 * slot + j
+                    assert a not in tile and 0 <= 4 * k - m + j < 64
+                    tile[a] = (row, 4 * k - m + j)
+        row, j = t >> 2, t & 3
+        m = (base_mis + row * sb) & 3
+        if m:
+            e = j if j < 4 - m else 60 + j
+            c = e + m
+            a = row * pitch + 4 * (((c >> 2) + (row >> 3)) % slots) + (c & 3)
+            assert a not in tile
+            tile[a] = (row, e)
+    assert len(tile) == 64 * 64
+    for t in range(256):
+        ib, ia0 = t & 63, t >> 6
+        m = (base_mis + ib * sb) & 3
+        for r in range(16):
+            c = ia0 + 4 * r + m
+            assert tile[ib * pitch + 4 * (((c >> 2) + (ib >> 3)) % slots) + (c & 3)] == (ib, ia0 + 4 * r)
+
+
+@pytest.mark.parametrize("sb", [1, 2, 3, 4, 5, 64, 65, 66, 67, 1000, 1001, 8191, 8192, 8193, 8194])
+def test_vec4_tile_chunk_mapping(sb):
+    for base_mis in range(4):
+        _vec4_tile_emulation(base_mis, sb)
