@@ -266,8 +266,8 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
     }
 }
 
-// The two phases of a whole 64 x 64 tile of 4-byte words with
-// single-dimension groups.  Each source row segment (64 elements) is fetched
+// The two phases of a 64 x 64 tile of 4-byte words whose A side is whole
+// (its B side may be short: rows rb..63 are skipped).  Each source row segment (64 elements) is fetched
 // as 16-byte aligned chunks with cp.async, 16 lanes per row; a row that does
 // not start on a 16-byte boundary (misalignment m = its first element's
 // offset from one, 1..3) leaves 4 elements in the partial chunks at its two
@@ -276,9 +276,11 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 // shifted by its misalignment, in 17 chunk slots, chunk k at slot
 // (k + ib / 8) mod 17 (the rotation spreads the store phase's column reads,
 // 32 consecutive rows per warp, over the banks).  Row pitch 68 words.
-template <typename O>
+// Group A is contiguous in the source (its offset is the A-index itself),
+// so src points at the tile's A-origin and only B parts come from `ad`.
+template <typename O, typename Addr>
 __device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ src, unsigned* __restrict__ dst,
-                                                 unsigned* tile, const LinAddr<O>& ad) {
+                                                 unsigned* tile, const Addr& ad, int rb) {
     constexpr int kPitch = 68, kSlots = 17;
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src >> 2) & 3u);
@@ -286,6 +288,7 @@ __device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ sr
     for (int r = 0; r < 4; ++r) {
         const int idx = t + 256 * r;
         const int row = idx >> 4, kk = idx & 15;
+        if (row >= rb) break;  // rows grow with r
         const O s0 = ad.src_b(row);
         const int m = (int)((base_mis + (unsigned)s0) & 3u);
         if (m == 0 || kk < 15) {
@@ -296,7 +299,7 @@ __device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ sr
                           reinterpret_cast<const uint4*>(src + s0 + (4 * k - m)));
         }
     }
-    {
+    if ((t >> 2) < rb) {
         const int row = t >> 2, j = t & 3;
         const O s0 = ad.src_b(row);
         const int m = (int)((base_mis + (unsigned)s0) & 3u);
@@ -311,6 +314,7 @@ __device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ sr
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     const int ib = t & 63, ia0 = t >> 6;
+    if (ib >= rb) return;  // no barrier follows inside this function
     const int m = (int)((base_mis + (unsigned)ad.src_b(ib)) & 3u);
     const int rot = ib >> 3;
     const unsigned* row = tile + ib * kPitch;
@@ -343,19 +347,21 @@ __device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ sr
 // addresses).  Row pitch TA + PAD makes the column reads conflict-free.
 // Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
 // masked.
-// MODE: kTileTables (multi-dimension groups), kTileLinear (one dimension
-// each), kTileVec4 (one dimension each, 4-byte words, 64 x 64 tiles).
-enum { kTileLinear = 0, kTileTables = 1, kTileVec4 = 2 };
+// MODE: bit 0 = multi-dimension groups (offset tables, else linear
+// offsets), bit 1 = whole 64 x 64 tiles of 4-byte words take the 16-byte
+// chunk path.
+enum { kTileLinear = 0, kTileTables = 1, kTileVec4 = 2, kTileTablesVec4 = 3 };
 
 template <typename W, bool WIDE, int MODE>
-__global__ void __launch_bounds__(256, MODE == kTileVec4 ? 6 : (sizeof(W) == 4 ? 8 : 6))
+__global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 ? 8 : 6))
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     using S = TileShape<sizeof(W)>;
     constexpr int kTab = S::T / kMinTileSide + kMinTileSide;  // >= TA + TB
     __shared__ __align__(16) W tile[S::T + (S::T / kMinTileSide) * S::PAD];  // 16-byte cp.async targets
-    constexpr bool GENERAL = MODE == kTileTables;
+    constexpr bool GENERAL = (MODE & kTileTables) != 0;
+    constexpr bool VEC4 = (MODE & kTileVec4) != 0 && sizeof(W) == 4;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
@@ -419,20 +425,26 @@ __global__ void __launch_bounds__(256, MODE == kTileVec4 ? 6 : (sizeof(W) == 4 ?
         }
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA};
-            if (ra == TA && rb == TB)
+            if (VEC4 && ra == TA) {
+                if constexpr (VEC4)
+                    tile_phases_vec4<O>(reinterpret_cast<const unsigned*>(in + so + tab_src[0]),
+                                        reinterpret_cast<unsigned*>(out + d), reinterpret_cast<unsigned*>(tile), ad,
+                                        rb);
+            } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
-            else
+            } else {
                 tile_phases<W, false>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+            }
         } else {
             const LinAddr<O> ad{(O)p.bs[0], (O)p.at[0], (O)p.bt[0]};
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
-            if (ra == TA && rb == TB) {
-                if constexpr (MODE == kTileVec4 && sizeof(W) == 4)
+            if (VEC4 && ra == TA) {
+                if constexpr (VEC4)
                     tile_phases_vec4<O>(reinterpret_cast<const unsigned*>(src), reinterpret_cast<unsigned*>(dst),
-                                        reinterpret_cast<unsigned*>(tile), ad);
-                else
-                    tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
+                                        reinterpret_cast<unsigned*>(tile), ad, rb);
+            } else if (ra == TA && rb == TB) {
+                tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
                 tile_phases<W, false>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             }
@@ -812,16 +824,15 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
-    const int mode = (C.na > 1 || C.nb > 1) ? kTileTables
-                     : (sizeof(W) == 4 && LMAD_TILE_VEC4 && C.la == 6 && C.lb == 6) ? kTileVec4
-                                                                                     : kTileLinear;
+    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) |
+                     ((sizeof(W) == 4 && LMAD_TILE_VEC4 && C.la == 6 && C.lb == 6) ? kTileVec4 : 0);
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
     if constexpr (sizeof(W) == 4) {
-        if (mode == kTileVec4) {
-            if (wide)
-                LMAD_TILE(true, kTileVec4);
-            else
-                LMAD_TILE(false, kTileVec4);
+        if (mode & kTileVec4) {
+            if (wide && mode == kTileTablesVec4) LMAD_TILE(true, kTileTablesVec4);
+            else if (wide) LMAD_TILE(true, kTileVec4);
+            else if (mode == kTileTablesVec4) LMAD_TILE(false, kTileTablesVec4);
+            else LMAD_TILE(false, kTileVec4);
             return cudaGetLastError();
         }
     }

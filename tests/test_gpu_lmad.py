@@ -208,3 +208,23 @@ def test_errors_enqueue_nothing():
         bm.lmad_copy([4, 5], 0, [5, 1], 0, [5, 1], 4, d_src, d_src)  # in place
     torch.cuda.synchronize()
     assert (d_dst.cpu().numpy() == -1).all()
+
+
+@pytest.mark.parametrize("in_offset", [0, 1, 3])
+def test_multidim_groups_on_whole_chunked_tiles(in_offset):
+    """A 5-D odd shape whose source-contiguous group A spans two dimensions
+    with 64 x 64 tiles: whole tiles take the 16-byte chunk path with offset
+    tables (source offset moved by 0, 1 and 3 elements)."""
+    shape, perm = (6, 70, 12, 14, 34), (4, 2, 0, 3, 1)
+    src_strides = synth.row_major_strides(shape)
+    out_rm = synth.row_major_strides([shape[p] for p in perm])
+    out_strides = [0] * 5
+    for pos, p in enumerate(perm):
+        out_strides[p] = out_rm[pos]
+    total = int(np.prod(shape))
+    w = dict(sizes=list(shape), in_offset=in_offset, in_strides=src_strides, in_elems=total + 4, out_offset=0,
+             out_strides=out_strides, out_elems=total)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and len(q["group_a"]) >= 2 and q["tile"] == (64, 64)
+    _check(w, 4)

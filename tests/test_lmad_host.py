@@ -172,12 +172,13 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert not set(a) & set(b)
 
 
-def _vec4_tile_emulation(base_mis, sb):
+def _vec4_tile_emulation(base_mis, sb, rb=64):
     """The 4-byte whole-tile path of the tile kernel, replayed on the host: rows
     of 64 elements fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
     misaligned rows), the 4 leftover elements of a misaligned row one per
     thread, rows kept shifted by their misalignment in 17 rotated chunk slots
-    of a 68-word pitch, then read back column-wise.  Every element is placed
+    of a 68-word pitch, then read back column-wise; rows rb.. of a tile short
+    along B are skipped.  Every element is placed
     exactly once, every 16-byte fetch is aligned, and every read returns the
     element the transpose needs."""
     pitch, slots = 68, 17
@@ -186,6 +187,8 @@ def _vec4_tile_emulation(base_mis, sb):
         for r in range(4):
             idx = t + 256 * r
             row, kk = idx >> 4, idx & 15
+            if row >= rb:
+                break
             m = (base_mis + row * sb) & 3
             if m == 0 or kk < 15:
                 k = kk + (1 if m else 0)
@@ -197,15 +200,17 @@ def _vec4_tile_emulation(base_mis, sb):
                     tile[a] = (row, 4 * k - m + j)
         row, j = t >> 2, t & 3
         m = (base_mis + row * sb) & 3
-        if m:
+        if m and row < rb:
             e = j if j < 4 - m else 60 + j
             c = e + m
             a = row * pitch + 4 * (((c >> 2) + (row >> 3)) % slots) + (c & 3)
             assert a not in tile
             tile[a] = (row, e)
-    assert len(tile) == 64 * 64
+    assert len(tile) == 64 * rb
     for t in range(256):
         ib, ia0 = t & 63, t >> 6
+        if ib >= rb:
+            continue
         m = (base_mis + ib * sb) & 3
         for r in range(16):
             c = ia0 + 4 * r + m
@@ -215,4 +220,5 @@ def _vec4_tile_emulation(base_mis, sb):
 @pytest.mark.parametrize("sb", [1, 2, 3, 4, 5, 64, 65, 66, 67, 1000, 1001, 8191, 8192, 8193, 8194])
 def test_vec4_tile_chunk_mapping(sb):
     for base_mis in range(4):
-        _vec4_tile_emulation(base_mis, sb)
+        for rb in (64, 62, 17, 1):
+            _vec4_tile_emulation(base_mis, sb, rb)
