@@ -151,8 +151,8 @@ template <> struct TileShape<4> { static constexpr int T = 4096, PAD = 1, CH = 8
 template <> struct TileShape<8> { static constexpr int T = 1024, PAD = 1, CH = 4; };
 template <> struct TileShape<16> { static constexpr int T = 1024, PAD = 1, CH = 4; };
 constexpr int kMinTileSide = 16;
-// 4-byte words, single-dimension groups, 64 x 64 tiles: fetch rows as
-// 16-byte chunks (tile_phases_vec4).
+// Tiles of 4-byte words with the default shape fetch rows as 16-byte chunks
+// (tile_phases_chunked); 2 = also 8-byte words.
 #ifndef LMAD_TILE_VEC4
 #define LMAD_TILE_VEC4 1
 #endif
@@ -266,71 +266,80 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
     }
 }
 
-// The two phases of a 64 x 64 tile of 4-byte words whose A side is whole
-// (its B side may be short: rows rb..63 are skipped).  Each source row segment (64 elements) is fetched
-// as 16-byte aligned chunks with cp.async, 16 lanes per row; a row that does
-// not start on a 16-byte boundary (misalignment m = its first element's
-// offset from one, 1..3) leaves 4 elements in the partial chunks at its two
-// ends (4 - m at the head, m at the tail), which a second pass copies one
-// element per thread (64 rows x 4 = 256).  Row ib is kept in shared memory
-// shifted by its misalignment, in 17 chunk slots, chunk k at slot
-// (k + ib / 8) mod 17 (the rotation spreads the store phase's column reads,
-// 32 consecutive rows per warp, over the banks).  Row pitch 68 words.
-// Group A is contiguous in the source (its offset is the A-index itself),
-// so src points at the tile's A-origin and only B parts come from `ad`.
-template <typename O, typename Addr>
-__device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ src, unsigned* __restrict__ dst,
-                                                 unsigned* tile, const Addr& ad, int rb) {
-    constexpr int kPitch = 68, kSlots = 17;
+// The two phases of a tile of 4- or 8-byte words whose A side is whole (its
+// B side may be short: rows rb.. are skipped), with the default shape: 64 x
+// 64 for 4-byte words, 32 x 32 for 8-byte words, so each source row segment
+// is 256 bytes, 16 chunks of 16 bytes (V = 16 / word elements each).  The
+// segment is fetched as 16-byte aligned chunks with cp.async, 16 lanes per
+// row; a row that does not start on a 16-byte boundary (misalignment m =
+// its first element's offset from one, 1..V-1) leaves V elements in the
+// partial chunks at its two ends (V - m at the head, m at the tail), which a
+// second pass copies one element per thread.  Row ib is kept in shared
+// memory shifted by its misalignment, in 17 chunk slots, chunk k at slot
+// (k + ib / 8) mod 17 (the rotation spreads the store phase's column reads
+// over the banks).  Group A is contiguous in the source (its offset is the
+// A-index itself), so src points at the tile's A-origin and only B parts
+// come from `ad`.
+template <typename W, typename O, typename Addr>
+__device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
+                                                    const Addr& ad, int rb) {
+    constexpr int V = 16 / (int)sizeof(W), LV = V == 4 ? 2 : 1;
+    constexpr int TA = 16 * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = TB == 64 ? 6 : 5;
+    constexpr int kSlots = 17, kPitch = kSlots * V;
+    static_assert(TB * kPitch <= TileShape<sizeof(W)>::T + TileShape<sizeof(W)>::T / kMinTileSide *
+                                                               TileShape<sizeof(W)>::PAD,
+                  "shifted rows fit the shared tile");
     const int t = threadIdx.x;
-    const unsigned base_mis = (unsigned)(((uintptr_t)src >> 2) & 3u);
+    const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < TB * 16 / 256; ++r) {
         const int idx = t + 256 * r;
         const int row = idx >> 4, kk = idx & 15;
         if (row >= rb) break;  // rows grow with r
         const O s0 = ad.src_b(row);
-        const int m = (int)((base_mis + (unsigned)s0) & 3u);
+        const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m == 0 || kk < 15) {
             const int k = kk + (m != 0);
             int slot = k + (row >> 3);
             slot -= slot >= kSlots ? kSlots : 0;
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + 4 * slot),
-                          reinterpret_cast<const uint4*>(src + s0 + (4 * k - m)));
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * slot),
+                          reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
         }
     }
-    if ((t >> 2) < rb) {
-        const int row = t >> 2, j = t & 3;
+    if (t < TB * V && (t >> LV) < rb) {
+        const int row = t >> LV, j = t & (V - 1);
         const O s0 = ad.src_b(row);
-        const int m = (int)((base_mis + (unsigned)s0) & 3u);
+        const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m != 0) {
-            const int e = j < 4 - m ? j : 60 + j;  // head elements 0..3-m, tail 64-m..63
+            const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
             const int c = e + m;
-            int slot = (c >> 2) + (row >> 3);
+            int slot = (c >> LV) + (row >> 3);
             slot -= slot >= kSlots ? kSlots : 0;
-            cp_async_word(tile + row * kPitch + 4 * slot + (c & 3), src + s0 + e);
+            cp_async_word(tile + row * kPitch + V * slot + (c & (V - 1)), src + s0 + e);
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    const int ib = t & 63, ia0 = t >> 6;
+    const int ib = t & (TB - 1), ia0 = t >> LTB;
+    constexpr int kStep = 256 / TB, kPer = TA / kStep;
     if (ib >= rb) return;  // no barrier follows inside this function
-    const int m = (int)((base_mis + (unsigned)ad.src_b(ib)) & 3u);
+    const int m = (int)((base_mis + (unsigned)ad.src_b(ib)) & (V - 1));
     const int rot = ib >> 3;
-    const unsigned* row = tile + ib * kPitch;
-    unsigned* o = dst + ad.dst_b(ib);
+    const W* row = tile + ib * kPitch;
+    W* o = dst + ad.dst_b(ib);
+    constexpr int CH = kPer < 8 ? kPer : 8;
 #pragma unroll 1
-    for (int c0 = 0; c0 < 16; c0 += 8) {
-        unsigned v[8];
+    for (int c0 = 0; c0 < kPer; c0 += CH) {
+        W v[CH];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int c = ia0 + 4 * (c0 + r) + m;
-            int slot = (c >> 2) + rot;
+        for (int r = 0; r < CH; ++r) {
+            const int c = ia0 + kStep * (c0 + r) + m;
+            int slot = (c >> LV) + rot;
             slot -= slot >= kSlots ? kSlots : 0;
-            v[r] = row[4 * slot + (c & 3)];
+            v[r] = row[V * slot + (c & (V - 1))];
         }
 #pragma unroll
-        for (int r = 0; r < 8; ++r) __stcs(o + ad.dst_a(ia0 + 4 * (c0 + r)), v[r]);
+        for (int r = 0; r < CH; ++r) __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
     }
 }
 
@@ -348,8 +357,8 @@ __device__ __forceinline__ void tile_phases_vec4(const unsigned* __restrict__ sr
 // Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
 // masked.
 // MODE: bit 0 = multi-dimension groups (offset tables, else linear
-// offsets), bit 1 = whole 64 x 64 tiles of 4-byte words take the 16-byte
-// chunk path.
+// offsets), bit 1 = tiles of 4- or 8-byte words with the default shape
+// whose A side is whole take the 16-byte chunk path.
 enum { kTileLinear = 0, kTileTables = 1, kTileVec4 = 2, kTileTablesVec4 = 3 };
 
 template <typename W, bool WIDE, int MODE>
@@ -361,7 +370,7 @@ __global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 
     constexpr int kTab = S::T / kMinTileSide + kMinTileSide;  // >= TA + TB
     __shared__ __align__(16) W tile[S::T + (S::T / kMinTileSide) * S::PAD];  // 16-byte cp.async targets
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
-    constexpr bool VEC4 = (MODE & kTileVec4) != 0 && sizeof(W) == 4;
+    constexpr bool VEC4 = (MODE & kTileVec4) != 0 && (sizeof(W) == 4 || sizeof(W) == 8);
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
@@ -426,10 +435,7 @@ __global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA};
             if (VEC4 && ra == TA) {
-                if constexpr (VEC4)
-                    tile_phases_vec4<O>(reinterpret_cast<const unsigned*>(in + so + tab_src[0]),
-                                        reinterpret_cast<unsigned*>(out + d), reinterpret_cast<unsigned*>(tile), ad,
-                                        rb);
+                if constexpr (VEC4) tile_phases_chunked<W, O>(in + so + tab_src[0], out + d, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -440,9 +446,7 @@ __global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (VEC4 && ra == TA) {
-                if constexpr (VEC4)
-                    tile_phases_vec4<O>(reinterpret_cast<const unsigned*>(src), reinterpret_cast<unsigned*>(dst),
-                                        reinterpret_cast<unsigned*>(tile), ad, rb);
+                if constexpr (VEC4) tile_phases_chunked<W, O>(src, dst, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -824,10 +828,14 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
-    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) |
-                     ((sizeof(W) == 4 && LMAD_TILE_VEC4 && C.la == 6 && C.lb == 6) ? kTileVec4 : 0);
+    // 8-byte words measured slower on the chunk path (32 x 32 tiles: 83-85%
+    // of a copy against 85-90% element-wise), so it is taken for 4-byte
+    // words only; LMAD_TILE_VEC4=2 enables it for 8-byte words too
+    const bool chunked = (LMAD_TILE_VEC4 && sizeof(W) == 4 && C.la == 6 && C.lb == 6) ||
+                         (LMAD_TILE_VEC4 == 2 && sizeof(W) == 8 && C.la == 5 && C.lb == 5);
+    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileVec4 : 0);
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
-    if constexpr (sizeof(W) == 4) {
+    if constexpr (sizeof(W) == 4 || sizeof(W) == 8) {
         if (mode & kTileVec4) {
             if (wide && mode == kTileTablesVec4) LMAD_TILE(true, kTileTablesVec4);
             else if (wide) LMAD_TILE(true, kTileVec4);

@@ -172,53 +172,58 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert not set(a) & set(b)
 
 
-def _vec4_tile_emulation(base_mis, sb, rb=64):
-    """The 4-byte whole-tile path of the tile kernel, replayed on the host: rows
-    of 64 elements fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
-    misaligned rows), the 4 leftover elements of a misaligned row one per
-    thread, rows kept shifted by their misalignment in 17 rotated chunk slots
-    of a 68-word pitch, then read back column-wise; rows rb.. of a tile short
-    along B are skipped.  Every element is placed
-    exactly once, every 16-byte fetch is aligned, and every read returns the
-    element the transpose needs."""
-    pitch, slots = 68, 17
+def _chunk_tile_emulation(word, base_mis, sb, rb):
+    """The chunk path of the tile kernel, replayed on the host for 4- and
+    8-byte words: rows of 256 bytes (64 or 32 elements, V = 16 / word per
+    chunk) fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
+    misaligned rows), the V leftover elements of a misaligned row one per
+    thread, rows kept shifted by their misalignment in 17 rotated chunk slots,
+    then read back column-wise; rows rb.. of a tile short along B are
+    skipped.  Every element is placed exactly once, every 16-byte fetch is
+    aligned, and every read returns the element the transpose needs."""
+    V = 16 // word
+    TA, TB, slots = 16 * V, 4096 // (16 * V) if word == 4 else 1024 // (16 * V), 17
+    pitch = slots * V
     tile = {}
     for t in range(256):
-        for r in range(4):
+        for r in range(TB * 16 // 256):
             idx = t + 256 * r
             row, kk = idx >> 4, idx & 15
             if row >= rb:
                 break
-            m = (base_mis + row * sb) & 3
+            m = (base_mis + row * sb) % V
             if m == 0 or kk < 15:
                 k = kk + (1 if m else 0)
-                assert (base_mis + row * sb + 4 * k - m) % 4 == 0
+                assert (base_mis + row * sb + V * k - m) % V == 0
                 slot = (k + (row >> 3)) % slots
-                for j in range(4):
-                    a = row * pitch + 4 * slot + j
-                    assert a not in tile and 0 <= 4 * k - m + j < 64
-                    tile[a] = (row, 4 * k - m + j)
-        row, j = t >> 2, t & 3
-        m = (base_mis + row * sb) & 3
-        if m and row < rb:
-            e = j if j < 4 - m else 60 + j
-            c = e + m
-            a = row * pitch + 4 * (((c >> 2) + (row >> 3)) % slots) + (c & 3)
-            assert a not in tile
-            tile[a] = (row, e)
-    assert len(tile) == 64 * rb
+                for j in range(V):
+                    a = row * pitch + V * slot + j
+                    assert a not in tile and 0 <= V * k - m + j < TA
+                    tile[a] = (row, V * k - m + j)
+        if t < TB * V:
+            row, j = t // V, t % V
+            m = (base_mis + row * sb) % V
+            if m and row < rb:
+                e = j if j < V - m else TA - V + j
+                c = e + m
+                a = row * pitch + V * (((c // V) + (row >> 3)) % slots) + c % V
+                assert a not in tile
+                tile[a] = (row, e)
+    assert len(tile) == TA * min(rb, TB) and max(tile) < TB * pitch
+    step = 256 // TB
     for t in range(256):
-        ib, ia0 = t & 63, t >> 6
+        ib, ia0 = t % TB, t // TB
         if ib >= rb:
             continue
-        m = (base_mis + ib * sb) & 3
-        for r in range(16):
-            c = ia0 + 4 * r + m
-            assert tile[ib * pitch + 4 * (((c >> 2) + (ib >> 3)) % slots) + (c & 3)] == (ib, ia0 + 4 * r)
+        m = (base_mis + ib * sb) % V
+        for r in range(TA // step):
+            c = ia0 + step * r + m
+            assert tile[ib * pitch + V * (((c // V) + (ib >> 3)) % slots) + c % V] == (ib, ia0 + step * r)
 
 
 @pytest.mark.parametrize("sb", [1, 2, 3, 4, 5, 64, 65, 66, 67, 1000, 1001, 8191, 8192, 8193, 8194])
-def test_vec4_tile_chunk_mapping(sb):
-    for base_mis in range(4):
-        for rb in (64, 62, 17, 1):
-            _vec4_tile_emulation(base_mis, sb, rb)
+@pytest.mark.parametrize("word", [4, 8])
+def test_chunked_tile_mapping(word, sb):
+    for base_mis in range(16 // word):
+        for rb in (64, 62, 32, 31, 17, 1):
+            _chunk_tile_emulation(word, base_mis, sb, rb)
