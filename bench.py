@@ -430,6 +430,10 @@ def run_ours(args):
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"2^{log2} consecutive source indices of the seed-0 n=28 int32 permutation "
                          f"({dt:.2f} s wall on {threads} host threads; plain C oracle loop)"}
+        # the same loop on one host thread (a 2^22-index sample, about a second)
+        g1, dt1, _ = oracle_sample_gbs(22, 0, 1, x_offset=1 << 26)
+        cpu["single_thread"] = {"value": round(g1, 4), "unit": UNIT, "cores": 1,
+                                "sample": f"2^22 source indices of the same permutation ({dt1:.2f} s)"}
 
     if rank == 0:
         line = {
