@@ -228,3 +228,53 @@ def test_multidim_groups_on_whole_chunked_tiles(in_offset):
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and len(q["group_a"]) >= 2 and q["tile"] == (64, 64)
     _check(w, 4)
+
+
+def test_pinned_host_buffers():
+    """Source and destination in pinned host memory: the kernels read and
+    write host memory directly (the slice case and a transpose)."""
+    for kind, shape in (("slice_2d", (300, 77)), ("reversed_rows", (64, 50))):
+        w = synth.page_lmad_workload(kind, shape)
+        src = torch.from_numpy(_fill(w["in_elems"], 4, 5).reshape(-1)).pin_memory()
+        dst = torch.full((w["out_elems"] * 4,), 0xA5, dtype=torch.uint8).pin_memory()
+        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4, src, dst,
+                     torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],
+                                     w["out_strides"], src.numpy().reshape(-1, 4),
+                                     np.full((w["out_elems"], 4), 0xA5, np.uint8))
+        assert np.array_equal(dst.numpy().reshape(-1, 4), want)
+
+
+def test_cuda_graph_capture_and_replay():
+    """lmad_copy allocates nothing and never synchronises, so copies of every
+    kind can be captured in a CUDA graph and replayed."""
+    shape = (33, 70, 65)
+    w_t = dict(sizes=list(shape), in_offset=0, in_strides=synth.row_major_strides(shape), in_elems=33 * 70 * 65,
+               out_offset=0, out_strides=[1, 33 * 65, 33], out_elems=33 * 70 * 65)   # transpose kind
+    w_s = synth.page_lmad_workload("slice_3d", (9, 40, 33))                             # strided kind
+    cases = [(w_t, 4), (w_s, 8)]
+    bufs = []
+    for w, e in cases:
+        src = torch.from_numpy(_fill(w["in_elems"], e, 9).reshape(-1)).cuda()
+        dst = torch.zeros(w["out_elems"] * e, dtype=torch.uint8, device="cuda")
+        bufs.append((src, dst))
+    for (w, e), (src, dst) in zip(cases, bufs):  # first calls outside capture: per-device set-up
+        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e, src, dst)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for (w, e), (src, dst) in zip(cases, bufs):
+                bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e,
+                             src, dst, torch.cuda.current_stream())
+    for _, dst in bufs:
+        dst.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for (w, e), (src, dst) in zip(cases, bufs):
+        want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],
+                                     w["out_strides"], src.cpu().numpy().reshape(-1, e),
+                                     np.zeros((w["out_elems"], e), np.uint8))
+        assert np.array_equal(dst.cpu().numpy().reshape(-1, e), want)
