@@ -48,6 +48,7 @@ __all__ = [
     "bmmc_gather",
     "lmad_copy",
     "lmad_copy_general",
+    "lmad_offset",
     "lmad_normalize",
     "parm",
 ]
@@ -324,6 +325,16 @@ def _lmad_offsets(sizes, offset, strides) -> np.ndarray:
     off = np.array([int(offset)], dtype=np.int64)
     for n, s in zip(sizes, strides):
         off = np.add.outer(off, np.arange(int(n), dtype=np.int64) * int(s)).ravel()
+    return off
+
+
+def lmad_offset(index_arrays, offset, strides) -> np.ndarray:
+    """L(i) = offset + sum_k i_k * strides[k] for given index tuples (one
+    array per dimension): the LMAD applied to sampled tuples, for checks of
+    copies too large to run the whole loop."""
+    off = np.full(np.asarray(index_arrays[0]).shape, int(offset), dtype=np.int64)
+    for ik, s in zip(index_arrays, strides):
+        off += np.asarray(ik, dtype=np.int64) * int(s)
     return off
 
 

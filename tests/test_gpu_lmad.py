@@ -278,3 +278,53 @@ def test_cuda_graph_capture_and_replay():
                                      w["out_strides"], src.cpu().numpy().reshape(-1, e),
                                      np.zeros((w["out_elems"], e), np.uint8))
         assert np.array_equal(dst.cpu().numpy().reshape(-1, e), want)
+
+
+def _byte_fill_device(n_bytes, salt):
+    """A byte pattern of n_bytes on the device (a multiplicative hash of the
+    byte index), written in 256 MiB pieces."""
+    out = torch.empty(n_bytes, dtype=torch.uint8, device="cuda")
+    step = 1 << 28
+    for lo in range(0, n_bytes, step):
+        i = torch.arange(lo, min(n_bytes, lo + step), dtype=torch.int64, device="cuda")
+        out[lo: lo + i.numel()] = (((i * 2654435761 + salt) >> 13) & 255).to(torch.uint8)
+    return out
+
+
+def _byte_pattern(idx, salt):
+    return (((idx.astype(np.int64) * 2654435761 + salt) >> 13) & 255).astype(np.uint8)
+
+
+@pytest.mark.parametrize("kind", ["slice", "transpose"])
+def test_more_than_2p32_tuples(kind):
+    """Copies of more than 2^32 one-byte elements (64-bit flat indices and
+    offsets): the slice xss[:, 1:] of a [65536][65538] byte array (strided
+    kernel) and the transpose of a [65536][65537] byte array (tile kernel),
+    checked on 200000 sampled tuples and on a sentinel left outside the
+    destination view."""
+    if torch.cuda.get_device_properties(0).total_memory < (40 << 30):
+        pytest.skip("needs a large device")
+    if kind == "slice":
+        R, C = 65536, 65538
+        sizes, in_off, in_st, out_st = [R, C - 1], 1, [C, 1], [C - 1, 1]
+        in_elems, out_elems = R * C, R * (C - 1)
+    else:
+        R, C = 65536, 65537
+        sizes, in_off, in_st, out_st = [R, C], 0, [C, 1], [1, R]
+        in_elems, out_elems = R * C, R * C
+    assert int(np.prod(sizes)) > (1 << 32)
+    q = bm.lmad_copy_query(sizes, in_off, in_st, 0, out_st, 1, in_elems=in_elems, out_elems=out_elems + 1)
+    assert q["kind"] == ("strided" if kind == "slice" else "transpose")
+    src = _byte_fill_device(in_elems, 11)
+    dst = torch.full((out_elems + 1,), 0x5A, dtype=torch.uint8, device="cuda")
+    bm.lmad_copy(sizes, in_off, in_st, 0, out_st, 1, src, dst)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2)
+    idx = [rng.integers(0, n, 200000) for n in sizes]
+    s_off = ref.lmad_offset(idx, in_off, in_st)
+    d_off = ref.lmad_offset(idx, 0, out_st)
+    got = dst[torch.from_numpy(d_off).cuda()].cpu().numpy()
+    assert np.array_equal(got, _byte_pattern(s_off, 11))
+    assert int(dst[out_elems].item()) == 0x5A
+    del src, dst
+    torch.cuda.empty_cache()

@@ -404,3 +404,17 @@ def test_lmad_general_degenerate_cases():
     wide = np.arange(12 * 4, dtype=np.uint32).reshape(12, 4)
     got = ref.lmad_copy_general((3, 4), 0, (4, 1), 0, (1, 3), wide, np.zeros_like(wide))
     assert np.array_equal(got, wide.reshape(3, 4, 4).transpose(1, 0, 2).reshape(12, 4))
+
+
+def test_lmad_offset_on_sampled_tuples_matches_the_whole_loop():
+    """The per-tuple LMAD used by large sampled checks agrees with numpy's
+    strided view at the same tuples."""
+    from numpy.lib.stride_tricks import as_strided
+
+    w = synth.draw_lmad_view(77, max_dims=4, max_elems=1 << 12)
+    src = np.arange(w["in_elems"], dtype=np.int64)
+    view = as_strided(src[w["in_offset"]:], shape=w["sizes"], strides=[s * 8 for s in w["in_strides"]])
+    rng = np.random.default_rng(5)
+    idx = [rng.integers(0, n, 200) for n in w["sizes"]]
+    got = ref.lmad_offset(idx, w["in_offset"], w["in_strides"])
+    assert np.array_equal(src[got], view[tuple(idx)])
