@@ -13,9 +13,11 @@
 //   - power-of-two sizes that permute or reverse a 2^n block on both sides:
 //     one BPC through the tiled BMMC kernel;
 //   - a source unit-stride dimension that differs from the destination's:
-//     a batched transpose of 32 x 32 tiles through shared memory (the page's
-//     transpose and "map transpose" cases, for any sizes and any number of
-//     batch dimensions);
+//     a batched tiled transpose through shared memory between two groups of
+//     dimensions (the page's transpose and "map transpose" cases, for any
+//     sizes and any number of batch dimensions), 64 x 64 tiles for 1- to
+//     4-byte words and 32 x 32 for 8 and 16, rows of 4-byte words fetched as
+//     16-byte chunks;
 //   - otherwise the page's stride-sorted copy, one element per index tuple,
 //     eight tuples per thread with all loads issued before the stores.
 // Index tuples are unpacked from the flat index with division by invariant
@@ -141,9 +143,9 @@ __global__ void __launch_bounds__(256)
 // Tile shapes of the transpose kernel per word size: T elements per tile,
 // shared-memory row padding and the elements per thread staged in registers
 // at a time.  The default A x B shape (64 x 64, or 32 x 32 for 8- and
-// 16-byte words) is chosen on the host (tile_shape_log2).  Either side shrinks to the size of a short group
-// (not below 16) and the other grows, keeping TA * TB = T, so both sides
-// stay within [16, T / 16].
+// 16-byte words) is chosen on the host (tile_shape_log2): either side
+// shrinks to the size of a short group (not below 16) and the other grows,
+// keeping TA * TB = T, so both sides stay within [16, T / 16].
 template <int BYTES> struct TileShape;
 template <> struct TileShape<1> { static constexpr int T = 4096, PAD = 4, CH = 8; };
 template <> struct TileShape<2> { static constexpr int T = 4096, PAD = 2, CH = 8; };
@@ -153,8 +155,8 @@ template <> struct TileShape<16> { static constexpr int T = 1024, PAD = 1, CH = 
 constexpr int kMinTileSide = 16;
 // Tiles of 4-byte words with the default shape fetch rows as 16-byte chunks
 // (tile_phases_chunked); 2 = also 8-byte words.
-#ifndef LMAD_TILE_VEC4
-#define LMAD_TILE_VEC4 1
+#ifndef LMAD_TILE_CHUNKS
+#define LMAD_TILE_CHUNKS 1
 #endif
 // Word sizes (a mask of 4, 8, 16) whose load phase uses cp.async; the others
 // stage through registers.
@@ -359,10 +361,10 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
 // MODE: bit 0 = multi-dimension groups (offset tables, else linear
 // offsets), bit 1 = tiles of 4- or 8-byte words with the default shape
 // whose A side is whole take the 16-byte chunk path.
-enum { kTileLinear = 0, kTileTables = 1, kTileVec4 = 2, kTileTablesVec4 = 3 };
+enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3 };
 
 template <typename W, bool WIDE, int MODE>
-__global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 ? 8 : 6))
+__global__ void __launch_bounds__(256, (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 
     constexpr int kTab = S::T / kMinTileSide + kMinTileSide;  // >= TA + TB
     __shared__ __align__(16) W tile[S::T + (S::T / kMinTileSide) * S::PAD];  // 16-byte cp.async targets
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
-    constexpr bool VEC4 = (MODE & kTileVec4) != 0 && (sizeof(W) == 4 || sizeof(W) == 8);
+    constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && (sizeof(W) == 4 || sizeof(W) == 8);
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
@@ -434,8 +436,8 @@ __global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 
         }
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA};
-            if (VEC4 && ra == TA) {
-                if constexpr (VEC4) tile_phases_chunked<W, O>(in + so + tab_src[0], out + d, tile, ad, rb);
+            if (CHUNKED && ra == TA) {
+                if constexpr (CHUNKED) tile_phases_chunked<W, O>(in + so + tab_src[0], out + d, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -445,8 +447,8 @@ __global__ void __launch_bounds__(256, (MODE & kTileVec4) ? 6 : (sizeof(W) == 4 
             const LinAddr<O> ad{(O)p.bs[0], (O)p.at[0], (O)p.bt[0]};
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
-            if (VEC4 && ra == TA) {
-                if constexpr (VEC4) tile_phases_chunked<W, O>(src, dst, tile, ad, rb);
+            if (CHUNKED && ra == TA) {
+                if constexpr (CHUNKED) tile_phases_chunked<W, O>(src, dst, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -830,17 +832,17 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
     // 8-byte words measured slower on the chunk path (32 x 32 tiles: 83-85%
     // of a copy against 85-90% element-wise), so it is taken for 4-byte
-    // words only; LMAD_TILE_VEC4=2 enables it for 8-byte words too
-    const bool chunked = (LMAD_TILE_VEC4 && sizeof(W) == 4 && C.la == 6 && C.lb == 6) ||
-                         (LMAD_TILE_VEC4 == 2 && sizeof(W) == 8 && C.la == 5 && C.lb == 5);
-    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileVec4 : 0);
+    // words only; LMAD_TILE_CHUNKS=2 enables it for 8-byte words too
+    const bool chunked = (LMAD_TILE_CHUNKS && sizeof(W) == 4 && C.la == 6 && C.lb == 6) ||
+                         (LMAD_TILE_CHUNKS == 2 && sizeof(W) == 8 && C.la == 5 && C.lb == 5);
+    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0);
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
     if constexpr (sizeof(W) == 4 || sizeof(W) == 8) {
-        if (mode & kTileVec4) {
-            if (wide && mode == kTileTablesVec4) LMAD_TILE(true, kTileTablesVec4);
-            else if (wide) LMAD_TILE(true, kTileVec4);
-            else if (mode == kTileTablesVec4) LMAD_TILE(false, kTileTablesVec4);
-            else LMAD_TILE(false, kTileVec4);
+        if (mode & kTileChunked) {
+            if (wide && mode == kTileTablesChunked) LMAD_TILE(true, kTileTablesChunked);
+            else if (wide) LMAD_TILE(true, kTileChunked);
+            else if (mode == kTileTablesChunked) LMAD_TILE(false, kTileTablesChunked);
+            else LMAD_TILE(false, kTileChunked);
             return cudaGetLastError();
         }
     }
