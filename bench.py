@@ -567,6 +567,12 @@ def other_configs(torch, bm, synth, dev, stream):
     scratch = torch.empty(1 << 28, dtype=torch.int32, device=dev)
     with bm.Plan(rows, c, 4, mode=1) as p:
         out["random_n28_int32_two_factor"] = big(28, 4, lambda: p.permute_scratch(a32, b32, scratch, stream))
+    # the per-element (naive) kernel of the paper's comparison: reads
+    # coalesced, every write scattered (seed 0 and bit reversal)
+    with bm.Plan(rows, c, 4, naive=True) as p:
+        out["random_n28_int32_naive"] = big(28, 4, lambda: p.permute(a32, b32, stream))
+    with bm.Plan(bitrev_rows(28), 0, 4, naive=True) as p:
+        out["bitrev_n28_int32_naive"] = big(28, 4, lambda: p.permute(a32, b32, stream))
     # the n=16 random map on 4096 arrays at once (batch_log2 = 12: 1 GiB in one launch)
     rows16, c16, _ = synth.draw_bmmc(0, 16, accept(16))
     with bm.Plan(rows16, c16, 4, batch_log2=12) as p:

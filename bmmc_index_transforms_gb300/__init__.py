@@ -96,11 +96,11 @@ def bmmc_plan_ex(n: int, A_rows: Sequence[int], c: int, elem_size: int, mode: in
                  t_in: int = 0, t_out: int = 0, tile_bits: int = 0,
                  alloc_scratch: bool = False, grid_blocks: int = 0, load_mode: int = 0,
                  block_order: int = 0, layout: int = 0, gather: bool = False, batch_log2: int = 0,
-                 tile_walk: int = 0) -> int:
+                 tile_walk: int = 0, naive: bool = False) -> int:
     """Returns an opaque plan handle (int); free it with bmmc_plan_destroy."""
     h = ctypes.c_void_p()
     opts = PlanOpts(mode, t_in, t_out, tile_bits, int(bool(alloc_scratch)), grid_blocks, load_mode,
-                    block_order, layout, int(bool(gather)), batch_log2, tile_walk)
+                    block_order, layout, int(bool(gather)), batch_log2, tile_walk, int(bool(naive)))
     _check(_capi.lib().bmmc_plan_ex(ctypes.byref(h), n, _rows(n, A_rows), int(c), elem_size,
                                     ctypes.byref(opts)), "bmmc_plan_ex")
     return int(h.value)
@@ -310,11 +310,11 @@ class Plan:
     def __init__(self, A_rows: Sequence[int], c: int = 0, elem_size: int = 4, *, mode: int = 0,
                  t_in: int = 0, t_out: int = 0, tile_bits: int = 0, alloc_scratch: bool = False,
                  grid_blocks: int = 0, load_mode: int = 0, block_order: int = 0, layout: int = 0,
-                 gather: bool = False, batch_log2: int = 0, tile_walk: int = 0):
+                 gather: bool = False, batch_log2: int = 0, tile_walk: int = 0, naive: bool = False):
         self.n = len(A_rows)
         self.handle = bmmc_plan_ex(self.n, A_rows, c, elem_size, mode, t_in, t_out, tile_bits,
                                    alloc_scratch, grid_blocks, load_mode, block_order, layout, gather,
-                                   batch_log2, tile_walk)
+                                   batch_log2, tile_walk, naive)
         self.elem_size = elem_size
 
     @property

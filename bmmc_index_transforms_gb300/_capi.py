@@ -44,7 +44,8 @@ class PlanOpts(ctypes.Structure):
                 ("tile_bits", ctypes.c_int), ("alloc_scratch", ctypes.c_int),
                 ("grid_blocks", ctypes.c_int), ("load_mode", ctypes.c_int),
                 ("block_order", ctypes.c_int), ("layout", ctypes.c_int), ("gather", ctypes.c_int),
-                ("batch_log2", ctypes.c_int), ("tile_walk", ctypes.c_int)]
+                ("batch_log2", ctypes.c_int), ("tile_walk", ctypes.c_int),
+                ("naive", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

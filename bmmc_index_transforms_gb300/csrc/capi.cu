@@ -101,7 +101,8 @@ bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows_in, uint64_t 
         if (opts->t_in < 0 || opts->t_in > 16 || opts->t_out < 0 || opts->t_out > 16 ||
             opts->tile_bits < 0 || opts->tile_bits > kMaxTileBits || opts->grid_blocks < 0 ||
             opts->load_mode < 0 || opts->load_mode > 2 || opts->block_order < 0 || opts->block_order > 2 ||
-            opts->layout < 0 || opts->layout > 1 || opts->tile_walk < 0 || opts->tile_walk > 1)
+            opts->layout < 0 || opts->layout > 1 || opts->tile_walk < 0 || opts->tile_walk > 1 ||
+            opts->naive < 0 || opts->naive > 1 || (opts->naive && opts->mode == BMMC_MODE_TWO_FACTOR))
             return BMMC_ERR_INVALID_ARG;
         if (opts->mode != BMMC_MODE_SINGLE_PASS && opts->mode != BMMC_MODE_TWO_FACTOR)
             return BMMC_ERR_INVALID_ARG;
@@ -113,6 +114,7 @@ bmmc_status build_plan(bmmc_plan_s* p, int n, const uint64_t* rows_in, uint64_t 
         req.block_order = opts->block_order;
         req.layout = opts->layout;
         req.tile_walk = opts->tile_walk;
+        req.naive = opts->naive;
         p->mode = opts->mode;
     }
     bmmc_status s = plan_pass(n, p->rows, p->inv, c, (int)elem, req, &p->main);

@@ -337,9 +337,10 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
     }
 }
 
-// Per-element kernel for arrays too small for one 16-byte vector per run.
+// Per-element kernel: arrays too small for one 16-byte vector per run, or
+// any size on request (the naive kernel, for comparison).
 template <int ELEM>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(256)
     bmmc_naive_kernel(const __grid_constant__ NaiveParams p, const void* __restrict__ in_,
                       void* __restrict__ out_) {
     using T = typename ElemType<ELEM>::T;
@@ -532,11 +533,13 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
 }
 
 cudaError_t launch_naive(const PassPlan& P, const void* in, void* out, cudaStream_t stream) {
-    const unsigned blocks = (unsigned)((P.np.count + 31) / 32);
+    const unsigned threads = (unsigned)P.threads;
+    const uint64_t b = (P.np.count + threads - 1) / threads;
+    const unsigned blocks = (unsigned)(b < 0x7FFFFFFFull ? b : 0x7FFFFFFFull);
     switch (P.elem) {
-        case 4: bmmc_naive_kernel<4><<<blocks, 32, 0, stream>>>(P.np, in, out); break;
-        case 8: bmmc_naive_kernel<8><<<blocks, 32, 0, stream>>>(P.np, in, out); break;
-        case 16: bmmc_naive_kernel<16><<<blocks, 32, 0, stream>>>(P.np, in, out); break;
+        case 4: bmmc_naive_kernel<4><<<blocks, threads, 0, stream>>>(P.np, in, out); break;
+        case 8: bmmc_naive_kernel<8><<<blocks, threads, 0, stream>>>(P.np, in, out); break;
+        case 16: bmmc_naive_kernel<16><<<blocks, threads, 0, stream>>>(P.np, in, out); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -324,6 +324,17 @@ bmmc_status plan_pass(int n, const uint64_t* rows, const uint64_t* inv, uint64_t
     const int vb = ilog2(vec);          // element bits inside a 16-byte vector
     const int bw = 7 - ilog2(elem);     // lane bits of one shared-memory wavefront
 
+    if (req.naive) {
+        // The per-element kernel on request, for comparison (any size).
+        P.kernel = KERNEL_NAIVE;
+        P.threads = n >= 8 ? 256 : 32;
+        for (int i = 0; i < n; ++i) P.np.rows[i] = rows[i];
+        P.np.c = c;
+        P.np.n = n;
+        P.np.count = 1ull << n;
+        *out = P;
+        return BMMC_OK;
+    }
     if (classify(n, rows, c) == BMMC_CLASS_IDENTITY) {
         P.kernel = KERNEL_COPY;
         *out = P;

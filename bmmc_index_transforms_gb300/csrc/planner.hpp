@@ -43,6 +43,7 @@ struct PlanRequest {
     int block_order = 0;                     // 0 input coordinate bits ascending, 1 local on both sides
     int layout = 0;                          // 0 automatic, 1 per-element stores
     int tile_walk = 0;                       // 0 grid stride, 1 contiguous ranges
+    int naive = 0;                           // 1 per-element kernel whatever the size
 };
 
 // Build one pass for (rows, c).  inv must be rows' inverse.

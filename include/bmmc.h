@@ -121,6 +121,12 @@ typedef struct {
     int tile_walk;       /* with grid_blocks below the number of tiles: 0 = block k takes
                             tiles k, k + grid, ... (default); 1 = block k takes a
                             contiguous range of tiles */
+    int naive;           /* 1 = the per-element kernel for any size: each thread
+                            evaluates y = A.x XOR c bit by bit, reads in[x] and writes
+                            out[y] (the naive kernel the paper's evaluation compares
+                            against: coalesced reads, scattered writes); for
+                            comparison only.  Single pass only (INVALID_ARG with
+                            TWO_FACTOR) */
 } bmmc_plan_opts;
 
 typedef struct bmmc_plan_s *bmmc_plan_t;

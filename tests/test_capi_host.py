@@ -414,3 +414,16 @@ def test_batched_and_gather_plans():
         assert p.info["c"] == ref.bmmc_index(n, ref.f2_inverse(n, A), 0, c)
     with pytest.raises(bm.BmmcError):
         bm.Plan(A, c, 4, batch_log2=40 - n + 1)
+
+
+def test_naive_option_plans_the_per_element_kernel():
+    """naive = 1 plans the per-element kernel at any size (256-thread
+    blocks), and is refused together with the two-factor mode."""
+    rows, c, _ = synth.draw_bmmc(0, 24, lambda r: ref.f2_rank(24, r) == 24)
+    with bm.Plan(rows, c, 8, naive=True) as p:
+        assert p.info["kernel_name"] == "per-element" and p.info["threads"] == 256
+    with bm.Plan(rows, c, 8) as p:
+        assert p.info["kernel_name"] == "tiled"
+    with pytest.raises(bm.BmmcError) as e:
+        bm.Plan(rows, c, 8, naive=True, mode=1)
+    assert e.value.status == _capi.ERR_INVALID_ARG

@@ -643,3 +643,19 @@ def test_contiguous_tile_walk(bm, load_mode):
             got, info = _run(bm, rows, c, arr, grid_blocks=grid, tile_walk=1, load_mode=load_mode,
                              block_order=order)
             assert got.tobytes() == oracle.scatter(n, rows, c, arr).tobytes(), (n, elem, grid, info)
+
+
+@pytest.mark.parametrize("elem", [4, 8, 16])
+@pytest.mark.parametrize("n", [3, 12, 20])
+def test_naive_kernel_option(bm, n, elem):
+    """The per-element (naive) kernel requested at any size gives the oracle's
+    bytes (random map, and bit reversal)."""
+    arr = synth.fill_int(n, elem)
+    for rows, c in (_random(40 + n, n), (ref.bitrev_rows(n), 0)):
+        with bm.Plan(rows, c, elem, naive=True) as p:
+            assert p.info["kernel_name"] == "per-element"
+            d_in = _dev(arr)
+            d_out = torch.zeros_like(d_in)
+            p.permute(d_in, d_out)
+            torch.cuda.synchronize()
+            assert _host(d_out, arr).tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
