@@ -30,7 +30,7 @@ __all__ = [
 
 CLASS_NAMES = {0: "identity", 1: "complement", 2: "bp", 3: "bpc", 4: "bmmc"}
 KERNEL_NAMES = {0: "tiled", 1: "copy", 2: "per-element"}
-LMAD_KIND_NAMES = {0: "empty", 1: "memcpy", 2: "bpc", 3: "transpose", 4: "strided"}
+LMAD_KIND_NAMES = {0: "empty", 1: "memcpy", 2: "bpc", 3: "transpose", 4: "strided", 5: "rows"}
 
 
 class BmmcError(RuntimeError):

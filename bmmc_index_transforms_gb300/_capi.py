@@ -59,7 +59,7 @@ class PlanInfo(ctypes.Structure):
 
 
 LMAD_MAX_DIMS = 16
-LMAD_COPY_EMPTY, LMAD_COPY_MEMCPY, LMAD_COPY_BPC, LMAD_COPY_TRANSPOSE, LMAD_COPY_STRIDED = range(5)
+LMAD_COPY_EMPTY, LMAD_COPY_MEMCPY, LMAD_COPY_BPC, LMAD_COPY_TRANSPOSE, LMAD_COPY_STRIDED, LMAD_COPY_ROWS = range(6)
 
 
 class LmadCopyInfo(ctypes.Structure):

@@ -38,6 +38,10 @@ namespace bmmc {
 namespace {
 
 constexpr int kLmadMaxDims = LMAD_MAX_DIMS;
+// Largest element size the rows kernel takes (LMAD_COPY_ROWS).
+#ifndef LMAD_ROWS_MAX_ELEM
+#define LMAD_ROWS_MAX_ELEM 2
+#endif
 constexpr uint64_t kLmadMaxTuples = 1ull << 40;
 
 // q = floor(x / d) = (t + ((x - t) >> s1)) >> s2 with t = mulhi(m, x), for
@@ -64,6 +68,17 @@ struct LmadStridedParams {
     int nd;
     LmadDiv div[kLmadMaxDims];  // div[k].d = size of dimension k
     int64_t sin[kLmadMaxDims], sout[kLmadMaxDims];
+};
+
+struct LmadRowsParams {
+    uint64_t bytes;            // destination bytes (one contiguous run)
+    uint64_t head;             // bytes before the first 16-byte aligned destination address
+    uint64_t chunks;           // whole 16-byte chunks after the head
+    uint64_t row;              // bytes per source row (contiguous in the source)
+    LmadDiv div_row;           // division by the row length
+    int nd;                    // dimensions above the row, fastest first
+    LmadDiv div[kLmadMaxDims];
+    int64_t sb[kLmadMaxDims];  // their source strides in bytes
 };
 
 struct LmadTileParams {
@@ -138,6 +153,85 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < K; ++j)
         if (base + (uint64_t)j * 256u < p.total) __stcs(out + dst[j], v[j]);
+}
+
+// Copies whose destination is one contiguous run and whose source is rows
+// of `row` contiguous bytes (slices and crops of 1- and 2-byte elements, and
+// of wider ones whose rows are not 16-byte aligned).  Thread t of block k
+// writes the aligned 16-byte destination chunks k*256*K + j*256 + t, j < K.
+// A chunk inside one row is assembled from the aligned 4-byte source words
+// that cover its 16 bytes (5 of them when the bytes are not 4-byte aligned,
+// else 4, so every word loaded holds at least one byte of the row) with byte
+// permutes; a chunk that crosses a row boundary, and the unaligned head and
+// tail of the destination, are copied byte by byte.  (Two aligned 16-byte
+// loads per chunk measured no faster.)
+template <bool WIDE>
+__device__ __forceinline__ uint64_t rows_src_byte(const LmadRowsParams& p, uint64_t b, uint64_t* col = nullptr) {
+    using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
+    const I r0 = div_q((I)b, p.div_row);
+    uint64_t off = b - (uint64_t)r0 * p.row;  // column byte
+    if (col) *col = off;
+    I x = r0;
+    for (int k = 0; k < p.nd; ++k) {
+        I r = x;
+        if (k + 1 < p.nd) {
+            const I q = div_q(x, p.div[k]);
+            r = x - q * (I)p.div[k].d;
+            x = q;
+        }
+        off += (uint64_t)((int64_t)r * p.sb[k]);
+    }
+    return off;
+}
+
+template <bool WIDE>
+__global__ void __launch_bounds__(256)
+    lmad_rows_kernel(const unsigned char* __restrict__ in, unsigned char* __restrict__ out, const LmadRowsParams p) {
+    constexpr int K = 4;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (uint64_t b = 0; b < p.head; ++b) out[b] = in[rows_src_byte<WIDE>(p, b)];
+        for (uint64_t b = p.head + 16 * p.chunks; b < p.bytes; ++b) out[b] = in[rows_src_byte<WIDE>(p, b)];
+    }
+    const uint64_t q0 = (uint64_t)blockIdx.x * (256u * K) + threadIdx.x;
+    // all loads of the K chunks first (no branch between them), then the
+    // byte permutes and stores; chunks that cross a row boundary last
+    unsigned x[K][5], sel[K];
+    bool fast[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const uint64_t q = q0 + (uint64_t)j * 256u;
+        uint64_t col = 0, a = 0;
+        if (q < p.chunks) a = rows_src_byte<WIDE>(p, p.head + 16 * q, &col);
+        fast[j] = q < p.chunks && col + 16 <= p.row;
+        const uintptr_t ad = (uintptr_t)(in + a);
+        const unsigned* base = reinterpret_cast<const unsigned*>(ad & ~(uintptr_t)3);
+        const unsigned sh = (unsigned)(ad & 3);
+        sel[j] = 0x3210u + 0x1111u * sh;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[j][i] = fast[j] ? __ldg(base + i) : 0u;
+        x[j][4] = fast[j] && sh ? __ldg(base + 4) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        if (!fast[j]) continue;
+        const uint64_t q = q0 + (uint64_t)j * 256u;
+        __stcs(reinterpret_cast<uint4*>(out + p.head + 16 * q),
+               make_uint4(__byte_perm(x[j][0], x[j][1], sel[j]), __byte_perm(x[j][1], x[j][2], sel[j]),
+                          __byte_perm(x[j][2], x[j][3], sel[j]), __byte_perm(x[j][3], x[j][4], sel[j])));
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const uint64_t q = q0 + (uint64_t)j * 256u;
+        if (fast[j] || q >= p.chunks) continue;
+        const uint64_t o = p.head + 16 * q;
+        unsigned w[4];
+        for (int i = 0; i < 4; ++i) {
+            unsigned word = 0;
+            for (int k = 0; k < 4; ++k) word |= (unsigned)in[rows_src_byte<WIDE>(p, o + 4 * i + k)] << (8 * k);
+            w[i] = word;
+        }
+        __stcs(reinterpret_cast<uint4*>(out + o), make_uint4(w[0], w[1], w[2], w[3]));
+    }
 }
 
 // Tile shapes of the transpose kernel per word size: T elements per tile,
@@ -733,6 +827,15 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
                 }
     }
     if (C.kind == LMAD_COPY_STRIDED || C.kind == LMAD_COPY_MEMCPY) C.vec = widen_factor(C, elem, in_addr, out_addr);
+    // a contiguous destination filled from contiguous source rows of at
+    // least 16 bytes whose widened words are still under 16 bytes: the rows
+    // kernel writes whole 16-byte destination chunks instead
+    if (C.kind == LMAD_COPY_STRIDED && C.nd >= 2 && C.d[0].s == 1 && C.d[0].t == 1 && C.vec * elem < 16 &&
+        elem <= LMAD_ROWS_MAX_ELEM && (uint64_t)C.d[0].n * elem >= 16) {
+        bool contiguous_out = true;
+        for (int k = 1; k < C.nd; ++k) contiguous_out = contiguous_out && C.d[k].t == C.d[k - 1].t * C.d[k - 1].n;
+        if (contiguous_out) C.kind = LMAD_COPY_ROWS;
+    }
     return BMMC_OK;
 }
 
@@ -777,6 +880,33 @@ cudaError_t launch_strided_w(const W* in, W* out, const Dim* d, int nd, uint64_t
         }
     }
 #undef LMAD_STRIDED
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rows(const unsigned char* in, unsigned char* out, const LmadCopy& C, size_t elem,
+                        cudaStream_t stream) {
+    LmadRowsParams p{};
+    p.bytes = C.elements * elem;
+    p.row = (uint64_t)C.d[0].n * elem;
+    p.head = std::min<uint64_t>(p.bytes, (16 - ((uintptr_t)out & 15)) & 15);
+    p.chunks = (p.bytes - p.head) / 16;
+    uint64_t span = p.row;
+    for (int k = 1; k < C.nd; ++k) span += (uint64_t)(C.d[k].n - 1) * iabs(C.d[k].s) * elem;
+    const bool wide = p.bytes > 0x7FFFFFFFull || span > 0x7FFFFFFFull;
+    const int bits = wide ? 64 : 32;
+    p.div_row = make_div(p.row, bits);
+    p.nd = C.nd - 1;
+    for (int k = 1; k < C.nd; ++k) {
+        p.div[k - 1] = make_div((uint64_t)C.d[k].n, bits);
+        p.sb[k - 1] = C.d[k].s * (int64_t)elem;
+    }
+    const uint64_t g = (p.chunks + 1023) / 1024;
+    const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(g, 0x7FFFFFFFull));
+    if (g > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+    if (wide)
+        lmad_rows_kernel<true><<<grid, 256, 0, stream>>>(in, out, p);
+    else
+        lmad_rows_kernel<false><<<grid, 256, 0, stream>>>(in, out, p);
     return cudaGetLastError();
 }
 
@@ -958,6 +1088,7 @@ extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_off
     }
     const unsigned char* a = ib + C.in_off * (int64_t)elem_size;
     unsigned char* o = ob + C.out_off * (int64_t)elem_size;
+    if (C.kind == LMAD_COPY_ROWS) return launch_rows(a, o, C, elem_size, st) == cudaSuccess ? BMMC_OK : BMMC_ERR_CUDA;
     if (C.kind == LMAD_COPY_MEMCPY && (((uintptr_t)a | (uintptr_t)o) & 15u) == 0) {
         e = launch_copy(a, o, (size_t)C.d[0].n * elem_size, st);
     } else {

@@ -331,9 +331,15 @@ typedef enum {
                                 continuing it in the destination), the other
                                 dimensions as the batch (the page's transpose and
                                 "map transpose" cases, any sizes) */
-    LMAD_COPY_STRIDED = 4    /* anything else: the page's stride-sorted copy, one
+    LMAD_COPY_STRIDED = 4,   /* anything else: the page's stride-sorted copy, one
                                 thread per index tuple, adjacent threads adjacent
                                 along the smallest source stride */
+    LMAD_COPY_ROWS = 5       /* 1- and 2-byte elements whose destination is one
+                                contiguous run and whose source is rows of at least 16
+                                bytes, each contiguous (a slice or crop) but not
+                                16-byte aligned: the destination is written in aligned
+                                16-byte chunks, each assembled from the aligned 4-byte
+                                source words covering it */
 } lmad_copy_kind;
 
 typedef struct {

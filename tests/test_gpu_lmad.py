@@ -171,13 +171,20 @@ def test_64bit_index_paths():
     rows = [0, gap, 2 * gap]
     for r, off in enumerate(rows):
         d_src[off: off + 64] = torch.arange(64, dtype=torch.uint8, device="cuda") + 64 * r
-    # strided: 3 rows of 60 bytes from offset 3 of each, into a dense 3 x 60
+    # rows: 3 rows of 60 bytes from offset 3 of each, into a dense 3 x 60
     d_dst = torch.full((180,), 0xA5, dtype=torch.uint8, device="cuda")
     q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [60, 1], 1, in_elems=in_elems, out_elems=180)
-    assert q["kind"] == "strided"
+    assert q["kind"] == "rows"
     bm.lmad_copy([3, 60], 3, [gap, 1], 0, [60, 1], 1, d_src, d_dst)
     want = np.concatenate([np.arange(3, 63) + 64 * r for r in range(3)]).astype(np.uint8)
     assert np.array_equal(d_dst.cpu().numpy(), want)
+    # strided: the same rows into a 3 x 64 destination (rows padded: not one run)
+    d_dst3 = torch.full((192,), 0xA5, dtype=torch.uint8, device="cuda")
+    q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [64, 1], 1, in_elems=in_elems, out_elems=192)
+    assert q["kind"] == "strided"
+    bm.lmad_copy([3, 60], 3, [gap, 1], 0, [64, 1], 1, d_src, d_dst3)
+    got3 = d_dst3.cpu().numpy().reshape(3, 64)
+    assert np.array_equal(got3[:, :60].ravel(), want) and (got3[:, 60:] == 0xA5).all()
     # transpose: the same rows written as columns of a 60 x 3
     d_dst2 = torch.full((180,), 0xA5, dtype=torch.uint8, device="cuda")
     q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [1, 3], 1, in_elems=in_elems, out_elems=180)
@@ -295,26 +302,31 @@ def _byte_pattern(idx, salt):
     return (((idx.astype(np.int64) * 2654435761 + salt) >> 13) & 255).astype(np.uint8)
 
 
-@pytest.mark.parametrize("kind", ["slice", "transpose"])
+@pytest.mark.parametrize("kind", ["slice", "slice_padded", "transpose"])
 def test_more_than_2p32_tuples(kind):
     """Copies of more than 2^32 one-byte elements (64-bit flat indices and
-    offsets): the slice xss[:, 1:] of a [65536][65538] byte array (strided
-    kernel) and the transpose of a [65536][65537] byte array (tile kernel),
-    checked on 200000 sampled tuples and on a sentinel left outside the
-    destination view."""
+    offsets): the slice xss[:, 1:] of a [65536][65538] byte array into a
+    dense array (rows kernel) and into a row-padded one (strided kernel), and
+    the transpose of a [65536][65537] byte array (tile kernel), checked on
+    200000 sampled tuples and on a sentinel left outside the destination
+    view."""
     if torch.cuda.get_device_properties(0).total_memory < (40 << 30):
         pytest.skip("needs a large device")
     if kind == "slice":
         R, C = 65536, 65538
         sizes, in_off, in_st, out_st = [R, C - 1], 1, [C, 1], [C - 1, 1]
         in_elems, out_elems = R * C, R * (C - 1)
+    elif kind == "slice_padded":
+        R, C = 65536, 65538
+        sizes, in_off, in_st, out_st = [R, C - 1], 1, [C, 1], [C, 1]
+        in_elems, out_elems = R * C, R * C
     else:
         R, C = 65536, 65537
         sizes, in_off, in_st, out_st = [R, C], 0, [C, 1], [1, R]
         in_elems, out_elems = R * C, R * C
     assert int(np.prod(sizes)) > (1 << 32)
     q = bm.lmad_copy_query(sizes, in_off, in_st, 0, out_st, 1, in_elems=in_elems, out_elems=out_elems + 1)
-    assert q["kind"] == ("strided" if kind == "slice" else "transpose")
+    assert q["kind"] == {"slice": "rows", "slice_padded": "strided", "transpose": "transpose"}[kind]
     src = _byte_fill_device(in_elems, 11)
     dst = torch.full((out_elems + 1,), 0x5A, dtype=torch.uint8, device="cuda")
     bm.lmad_copy(sizes, in_off, in_st, 0, out_st, 1, src, dst)
@@ -328,3 +340,23 @@ def test_more_than_2p32_tuples(kind):
     assert int(dst[out_elems].item()) == 0x5A
     del src, dst
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("elem", [1, 2])
+@pytest.mark.parametrize("shape,lo,hi,out_off", [((64, 40), 1, 40, 0), ((64, 40), 3, 37, 5), ((1000, 17), 1, 17, 0),
+                                                  ((333, 100), 7, 93, 3), ((5, 4097), 1, 4097, 1),
+                                                  ((2, 33), 0, 32, 0), ((40, 9, 70), 2, 60, 7)])
+def test_rows_kernel_slices(elem, shape, lo, hi, out_off):
+    """Crops of 1- and 2-byte arrays into a contiguous destination (the rows
+    kernel): rows of 16 to 8192 bytes, chunks crossing row boundaries,
+    misaligned starts on both sides (head and tail bytes), 2-D and 3-D."""
+    sizes = list(shape[:-1]) + [hi - lo]
+    in_st = synth.row_major_strides(shape)
+    out_st = synth.row_major_strides(sizes)
+    n_out = int(np.prod(sizes))
+    w = dict(sizes=sizes, in_offset=lo, in_strides=in_st, in_elems=int(np.prod(shape)), out_offset=out_off,
+             out_strides=out_st, out_elems=n_out + out_off + 3)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == ("rows" if (hi - lo) * elem >= 16 else "strided")
+    _check(w, elem, seed=lo + hi)

@@ -227,3 +227,20 @@ def test_chunked_tile_mapping(word, sb):
     for base_mis in range(16 // word):
         for rb in (64, 62, 32, 31, 17, 1):
             _chunk_tile_emulation(word, base_mis, sb, rb)
+
+
+def test_rows_kind_for_small_elements():
+    """Slices of 1- and 2-byte elements into a contiguous destination, rows of
+    at least 16 bytes, run as the rows kernel; 4-byte elements, rows under 16
+    bytes and padded destinations stay on the strided kernel."""
+    def kind(elem, shape, out_pad=0):
+        w = synth.page_lmad_workload("slice_2d", shape)
+        m = shape[1] - 1
+        out_st = [m + out_pad, 1]
+        return bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], 0, out_st, elem,
+                                  in_elems=w["in_elems"], out_elems=shape[0] * (m + out_pad))["kind"]
+    assert kind(1, (100, 17)) == "rows"        # 16-byte rows
+    assert kind(2, (100, 9)) == "rows"
+    assert kind(1, (100, 16)) == "strided"     # 15-byte rows
+    assert kind(4, (100, 9)) == "strided"
+    assert kind(1, (100, 33), out_pad=1) == "strided"
