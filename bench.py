@@ -493,14 +493,16 @@ def axes_lmad(synth, shape, perm):
                 out_offset=0, out_strides=out_strides, out_elems=total)
 
 
-def lmad_case(torch, bm, w, a32, b32, stream, page_us=None):
-    """One general LMAD copy of int32 elements: mean of 30 back-to-back
-    launches; effective bytes = one read and one write of the destination."""
-    src, dst = a32[: w["in_elems"]], b32[: w["out_elems"]]
-    args = (w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4)
+def lmad_case(torch, bm, w, a32, b32, stream, page_us=None, elem=4):
+    """One general LMAD copy (elements of `elem` bytes, buffers viewed as
+    bytes): mean of 30 back-to-back launches; effective bytes = one read and
+    one write of the destination."""
+    src = a32.view(torch.uint8)[: w["in_elems"] * elem]
+    dst = b32.view(torch.uint8)[: w["out_elems"] * elem]
+    args = (w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem)
     kind = bm.lmad_copy_query(*args, src, dst)["kind"]
     ms, _, _ = time_launches(torch, lambda: bm.lmad_copy(*args, src, dst, stream), 30)
-    r = {"kind": kind, "us": round(ms * 1e3, 1), "gbs": round(2.0 * w["out_elems"] * 4 / (ms / 1e3) / 1e9, 1)}
+    r = {"kind": kind, "us": round(ms * 1e3, 1), "gbs": round(2.0 * w["out_elems"] * elem / (ms / 1e3) / 1e9, 1)}
     if page_us:
         r["page_us_rx7900xt"] = page_us
     return r
@@ -599,6 +601,11 @@ def other_configs(torch, bm, synth, dev, stream):
     for name, shape, perm in (("t2d_8191x8193", (8191, 8193), (1, 0)),
                               ("batched_64x1000x1000", (64, 1000, 1000), (0, 2, 1))):
         out["lmad_" + name + "_int32"] = lmad_case(torch, bm, axes_lmad(synth, shape, perm), a32, b32, stream)
+    # the same slice on 1- and 2-byte elements (uint8 crop, fp16 slice: the rows kernel)
+    out["lmad_slice_2d_16384x16385_uint8"] = lmad_case(
+        torch, bm, synth.page_lmad_workload("slice_2d", (16384, 16385)), a32, b32, stream, elem=1)
+    out["lmad_slice_2d_16384x8193_fp16"] = lmad_case(
+        torch, bm, synth.page_lmad_workload("slice_2d", (16384, 8193)), a32, b32, stream, elem=2)
     del a, b, scratch, flush_buf
     torch.cuda.empty_cache()
     return out
