@@ -260,7 +260,8 @@ def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[i
             "transpose_out_dim": int(info.transpose_out_dim),
             "group_a": [i for i in range(k) if (info.group_a >> i) & 1],
             "group_b": [i for i in range(k) if (info.group_b >> i) & 1],
-            "tile": (int(info.tile_a), int(info.tile_b)), "elements": int(info.elements)}
+            "tile": (int(info.tile_a), int(info.tile_b)), "narrow": int(info.narrow),
+            "elements": int(info.elements)}
 
 
 def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,

@@ -68,7 +68,7 @@ class LmadCopyInfo(ctypes.Structure):
                 ("out_strides", ctypes.c_int64 * LMAD_MAX_DIMS), ("in_offset", ctypes.c_int64),
                 ("out_offset", ctypes.c_int64), ("vec", ctypes.c_int), ("transpose_out_dim", ctypes.c_int),
                 ("group_a", ctypes.c_uint32), ("group_b", ctypes.c_uint32), ("tile_a", ctypes.c_int),
-                ("tile_b", ctypes.c_int), ("elements", ctypes.c_uint64)]
+                ("tile_b", ctypes.c_int), ("narrow", ctypes.c_int), ("elements", ctypes.c_uint64)]
 
 
 # name -> (restype, argtypes); every function declared in include/bmmc.h

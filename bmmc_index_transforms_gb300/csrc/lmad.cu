@@ -38,6 +38,11 @@ namespace bmmc {
 namespace {
 
 constexpr int kLmadMaxDims = LMAD_MAX_DIMS;
+// Narrow transposes with 2 to 4 narrow indices and 16-byte alignment take
+// the register-regrouping kernel (lmad_aos_kernel).
+#ifndef LMAD_AOS
+#define LMAD_AOS 1
+#endif
 // Largest element size the rows kernel takes (LMAD_COPY_ROWS).
 #ifndef LMAD_ROWS_MAX_ELEM
 #define LMAD_ROWS_MAX_ELEM 2
@@ -79,6 +84,19 @@ struct LmadRowsParams {
     int nd;                    // dimensions above the row, fastest first
     LmadDiv div[kLmadMaxDims];
     int64_t sb[kLmadMaxDims];  // their source strides in bytes
+};
+
+struct LmadNarrowParams {
+    uint64_t tiles;            // tiles along the wide dimension x batch
+    LmadDiv div_tw;            // tiles along the wide dimension
+    uint64_t n_wide;           // size of the wide dimension
+    int n;                     // size of the narrow dimension (<= 16)
+    int lt;                    // log2 of the tile length along the wide dimension
+    int64_t stride;            // narrow A: destination stride of A; narrow B: source stride of B
+    int vec_load, vec_store;   // 16-byte paths allowed (host-checked alignment)
+    int nc;                    // batch dimensions
+    LmadDiv cdiv[kLmadMaxDims];
+    int64_t cs[kLmadMaxDims], ct[kLmadMaxDims];
 };
 
 struct LmadTileParams {
@@ -236,21 +254,35 @@ __global__ void __launch_bounds__(256)
 
 // Tile shapes of the transpose kernel per word size: T elements per tile,
 // shared-memory row padding and the elements per thread staged in registers
-// at a time.  The default A x B shape (64 x 64, or 32 x 32 for 8- and
-// 16-byte words) is chosen on the host (tile_shape_log2): either side
+// at a time.  The default A x B shape (256 x 32 for 1-byte words, 128 x 64
+// for 2, 64 x 64 for 4, 32 x 32 for 8 and 16: source rows of 256 bytes for 1
+// to 8) is chosen on the host (tile_shape_log2): either side
 // shrinks to the size of a short group (not below 16) and the other grows,
-// keeping TA * TB = T, so both sides stay within [16, T / 16].
+// keeping TA * TB = T, so both sides stay within [T / 256, 256] and at
+// least 16 (TileSides).
 template <int BYTES> struct TileShape;
-template <> struct TileShape<1> { static constexpr int T = 4096, PAD = 4, CH = 8; };
-template <> struct TileShape<2> { static constexpr int T = 4096, PAD = 2, CH = 8; };
+template <> struct TileShape<1> { static constexpr int T = 8192, PAD = 4, CH = 8; };
+template <> struct TileShape<2> { static constexpr int T = 8192, PAD = 2, CH = 8; };
 template <> struct TileShape<4> { static constexpr int T = 4096, PAD = 1, CH = 8; };
 template <> struct TileShape<8> { static constexpr int T = 1024, PAD = 1, CH = 4; };
 template <> struct TileShape<16> { static constexpr int T = 1024, PAD = 1, CH = 4; };
-constexpr int kMinTileSide = 16;
+// Tile sides stay within [T / 256, 256] (and at least 16): the element
+// path keeps one A-index per thread while loading and one B-index while
+// storing, which needs both sides <= 256 (the 256 threads of a block).
+template <int T>
+struct TileSides {
+    static constexpr int kMax = T / 16 < 256 ? T / 16 : 256;
+    static constexpr int kMin = T / kMax;
+};
 // Tiles of 4-byte words with the default shape fetch rows as 16-byte chunks
 // (tile_phases_chunked); 2 = also 8-byte words.
 #ifndef LMAD_TILE_CHUNKS
 #define LMAD_TILE_CHUNKS 1
+#endif
+// Word sizes (a mask of 1, 2, 4, 8) whose chunk path writes 16-byte packs
+// along B when the destination allows it.
+#ifndef LMAD_TILE_PACK_WORDS
+#define LMAD_TILE_PACK_WORDS (1 | 2)
 #endif
 // Word sizes (a mask of 4, 8, 16) whose load phase uses cp.async; the others
 // stage through registers.
@@ -294,7 +326,7 @@ struct LinAddr {
     __device__ __forceinline__ O dst_b(int ib) const { return (O)ib * tb; }
 };
 
-// The two phases of one tile.  Both tile sides are at most 256 (T / 16), so
+// The two phases of one tile.  Both tile sides are at most 256, so
 // in the load phase a thread keeps one A-index (lanes along A) and steps
 // through B-indices, and in the store phase keeps one B-index and steps
 // through A-indices.  The load phase of 4- to 16-byte words issues every
@@ -371,22 +403,30 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 // its first element's offset from one, 1..V-1) leaves V elements in the
 // partial chunks at its two ends (V - m at the head, m at the tail), which a
 // second pass copies one element per thread.  Row ib is kept in shared
-// memory shifted by its misalignment, in 17 chunk slots, chunk k at slot
-// (k + ib / 8) mod 17 (the rotation spreads the store phase's column reads
-// over the banks).  Group A is contiguous in the source (its offset is the
+// memory shifted by its misalignment and rotated by ib / 8 chunks inside a
+// 25-chunk pitch (the rotation spreads the store phase's column reads over
+// the banks; with no wrap-around an element's address is a per-row offset
+// plus its column).  Group A is contiguous in the source (its offset is the
 // A-index itself), so src points at the tile's A-origin and only B parts
 // come from `ad`.
-template <typename W, typename O, typename Addr>
+constexpr int clog2(int v) { return v <= 1 ? 0 : 1 + clog2(v / 2); }
+// Row pitch of the chunk path in 16-byte chunks: 17 for a shifted 256-byte
+// segment plus up to 7 of rotation; 25 * 4 = 100 words keeps neighbouring
+// rows 4 banks apart.
+constexpr int kChunkPitch = 25;
+
+template <typename W, typename O, bool PACK, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
                                                     const Addr& ad, int rb) {
-    constexpr int V = 16 / (int)sizeof(W), LV = V == 4 ? 2 : 1;
-    constexpr int TA = 16 * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = TB == 64 ? 6 : 5;
-    constexpr int kSlots = 17, kPitch = kSlots * V;
-    static_assert(TB * kPitch <= TileShape<sizeof(W)>::T + TileShape<sizeof(W)>::T / kMinTileSide *
-                                                               TileShape<sizeof(W)>::PAD,
-                  "shifted rows fit the shared tile");
+    constexpr int V = 16 / (int)sizeof(W), LV = clog2(V);
+    constexpr int TA = 16 * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
+    constexpr int kPitch = kChunkPitch * V;
+    static_assert(TB / 8 <= kChunkPitch - 17, "rotation fits the pitch");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
+    // row r holds its segment shifted by its misalignment m, starting at
+    // chunk r / 8 of its pitch: element (r, c = column + m) at
+    // r * kPitch + (r / 8) * V + c, whole chunks at 16-byte boundaries
 #pragma unroll
     for (int r = 0; r < TB * 16 / 256; ++r) {
         const int idx = t + 256 * r;
@@ -396,46 +436,302 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m == 0 || kk < 15) {
             const int k = kk + (m != 0);
-            int slot = k + (row >> 3);
-            slot -= slot >= kSlots ? kSlots : 0;
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * slot),
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + (row >> 3))),
                           reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
         }
     }
-    if (t < TB * V && (t >> LV) < rb) {
-        const int row = t >> LV, j = t & (V - 1);
+#pragma unroll
+    for (int u = t; u < TB * V; u += 256) {
+        const int row = u >> LV, j = u & (V - 1);
+        if (row >= rb) break;  // rows grow with u
         const O s0 = ad.src_b(row);
         const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m != 0) {
             const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
-            const int c = e + m;
-            int slot = (c >> LV) + (row >> 3);
-            slot -= slot >= kSlots ? kSlots : 0;
-            cp_async_word(tile + row * kPitch + V * slot + (c & (V - 1)), src + s0 + e);
+            W* slot = tile + row * kPitch + V * (row >> 3) + e + m;
+            if constexpr (sizeof(W) >= 4)
+                cp_async_word(slot, src + s0 + e);
+            else
+                *slot = __ldg(src + s0 + e);
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
+    if constexpr (PACK) {
+        // each item: one column ia and V consecutive B rows, gathered from
+        // shared memory and written as one 16-byte store (B has destination
+        // stride +1 and the host checked the 16-byte alignment); a thread's
+        // rows are the same for all its items, so their offsets are computed
+        // once
+        constexpr int G = TB / V, LG = clog2(G), ITEMS = TA * G;
+        const int g = t & (G - 1), ib0 = g * V;
+        if (ib0 >= rb) return;  // no barrier follows inside this function
+        int off[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int rr = ib0 + k < rb ? ib0 + k : ib0;
+            off[k] = rr * kPitch + V * (rr >> 3) + (int)((base_mis + (unsigned)ad.src_b(rr)) & (V - 1));
+        }
+        W* o = dst + ad.dst_b(ib0);
+        const bool whole = ib0 + V <= rb;
+#pragma unroll 1
+        for (int ia = t >> LG; ia < TA; ia += 256 >> LG) {
+            W v[V];
+#pragma unroll
+            for (int k = 0; k < V; ++k) v[k] = tile[off[k] + ia];
+            W* oa = o + ad.dst_a(ia);
+            if (whole) {
+                __stcs(reinterpret_cast<uint4*>(oa), *reinterpret_cast<const uint4*>(v));
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; ++k)
+                    if (ib0 + k < rb) __stcs(oa + k, v[k]);
+            }
+        }
+        (void)ITEMS;
+        return;
+    }
     const int ib = t & (TB - 1), ia0 = t >> LTB;
     constexpr int kStep = 256 / TB, kPer = TA / kStep;
     if (ib >= rb) return;  // no barrier follows inside this function
-    const int m = (int)((base_mis + (unsigned)ad.src_b(ib)) & (V - 1));
-    const int rot = ib >> 3;
-    const W* row = tile + ib * kPitch;
+    const W* row = tile + ib * kPitch + V * (ib >> 3) + (int)((base_mis + (unsigned)ad.src_b(ib)) & (V - 1));
     W* o = dst + ad.dst_b(ib);
     constexpr int CH = kPer < 8 ? kPer : 8;
 #pragma unroll 1
     for (int c0 = 0; c0 < kPer; c0 += CH) {
         W v[CH];
 #pragma unroll
-        for (int r = 0; r < CH; ++r) {
-            const int c = ia0 + kStep * (c0 + r) + m;
-            int slot = (c >> LV) + rot;
-            slot -= slot >= kSlots ? kSlots : 0;
-            v[r] = row[V * slot + (c & (V - 1))];
-        }
+        for (int r = 0; r < CH; ++r) v[r] = row[ia0 + kStep * (c0 + r)];
 #pragma unroll
         for (int r = 0; r < CH; ++r) __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
+    }
+}
+
+// Transposes with a narrow side: one group is a single dimension of n <= 16
+// elements that continues the other, wide, dimension contiguously on one
+// side (NHWC <-> NCHW with few channels).  A tile is 2^lt wide indices, so
+// on that side it is one contiguous block of n * 2^lt elements (<= 16 KiB).
+// NARROW_A (the narrow group has source stride 1, the wide one source
+// stride n, destination stride +1): the source block is copied into shared
+// memory with 16-byte cp.async chunks, and each of the n destination rows is
+// written with lanes packing 16 / word consecutive wide indices into one
+// 16-byte store.  NARROW_B (the narrow group has destination stride +1, the
+// wide one destination stride n and source stride 1): each of the n source
+// rows is read with 16-byte loads whose elements are scattered into shared
+// memory in destination order, and the destination block is written with
+// 16-byte stores.  Unaligned cases move element by element.  32-bit offsets.
+template <typename W, bool NARROW_A>
+__global__ void __launch_bounds__(256)
+    lmad_narrow_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadNarrowParams p) {
+    constexpr int P = 16 / (int)sizeof(W);  // elements per 16-byte word
+    __shared__ __align__(16) unsigned char smem_bytes[16384];
+    W* smem = reinterpret_cast<W*>(smem_bytes);
+    const int t = threadIdx.x;
+    const int n = p.n;
+    for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
+        uint32_t x = (uint32_t)blk;
+        uint32_t q = div_q(x, p.div_tw);
+        const uint32_t tw = x - q * (uint32_t)p.div_tw.d;
+        x = q;
+        int32_t so = 0, d = 0;
+        for (int k = 0; k < p.nc; ++k) {
+            uint32_t r = x;
+            if (k + 1 < p.nc) {
+                q = div_q(x, p.cdiv[k]);
+                r = x - q * (uint32_t)p.cdiv[k].d;
+                x = q;
+            }
+            so += (int32_t)r * (int32_t)p.cs[k];
+            d += (int32_t)r * (int32_t)p.ct[k];
+        }
+        const int32_t w0 = (int32_t)(tw << p.lt);
+        const int rw = (int)min((uint64_t)1 << p.lt, p.n_wide - (uint64_t)w0);  // wide indices in this tile
+        const int nb = n * rw;                                                  // elements in the block
+        if constexpr (NARROW_A) {
+            const W* blkp = in + so + w0 * n;  // contiguous source block, element (ia, iw) at iw * n + ia
+            int done = 0;
+            if (p.vec_load) {
+                const int chunks = nb / P;
+                for (int c = t; c < chunks; c += 256)
+                    cp_async_word(reinterpret_cast<uint4*>(smem) + c, reinterpret_cast<const uint4*>(blkp) + c);
+                done = chunks * P;
+                asm volatile("cp.async.wait_all;" ::: "memory");
+            }
+            for (int e = done + t; e < nb; e += 256) smem[e] = blkp[e];
+            __syncthreads();
+            W* dbase = out + d + w0;
+            const int groups = p.vec_store ? rw / P : 0;
+            for (int ia = 0; ia < n; ++ia) {
+                W* drow = dbase + ia * (int32_t)p.stride;
+                for (int g = t; g < groups; g += 256) {
+                    if constexpr (P == 1) {
+                        __stcs(drow + g, smem[g * n + ia]);
+                    } else {
+                        W v[P];
+#pragma unroll
+                        for (int k = 0; k < P; ++k) v[k] = smem[(g * P + k) * n + ia];
+                        __stcs(reinterpret_cast<uint4*>(drow) + g, *reinterpret_cast<const uint4*>(v));
+                    }
+                }
+                for (int iw = groups * P + t; iw < rw; iw += 256) __stcs(drow + iw, smem[iw * n + ia]);
+            }
+        } else {
+            const W* sbase = in + so + w0;  // source row ib at sbase + ib * stride, contiguous along the wide index
+            const int groups = p.vec_load ? rw / P : 0;
+            for (int ib = 0; ib < n; ++ib) {
+                const W* srow = sbase + ib * (int32_t)p.stride;
+                for (int g = t; g < groups; g += 256) {
+                    if constexpr (P == 1) {
+                        smem[g * n + ib] = __ldg(srow + g);
+                    } else {
+                        W v[P];
+                        *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(srow) + g);
+#pragma unroll
+                        for (int k = 0; k < P; ++k) smem[(g * P + k) * n + ib] = v[k];
+                    }
+                }
+                for (int iw = groups * P + t; iw < rw; iw += 256) smem[iw * n + ib] = __ldg(srow + iw);
+            }
+            __syncthreads();
+            W* blkp = out + d + w0 * n;  // contiguous destination block
+            int done = 0;
+            if (p.vec_store) {
+                const int chunks = nb / P;
+                for (int c = t; c < chunks; c += 256)
+                    __stcs(reinterpret_cast<uint4*>(blkp) + c, reinterpret_cast<const uint4*>(smem)[c]);
+                done = chunks * P;
+            }
+            for (int e = done + t; e < nb; e += 256) __stcs(blkp + e, smem[e]);
+        }
+        __syncthreads();
+    }
+}
+
+// Element e of a group of 16-byte words held as 32-bit registers, for
+// element sizes 1, 2, 4 and 8 bytes (all indices compile-time constants
+// after unrolling, so the registers stay registers).
+template <int W>
+struct Lanes;
+template <>
+struct Lanes<4> {
+    template <int NW>
+    __device__ __forceinline__ static void move(const unsigned (&in)[NW], int src, unsigned (&out)[NW], int dst) {
+        out[dst] = in[src];
+    }
+};
+template <>
+struct Lanes<8> {
+    template <int NW>
+    __device__ __forceinline__ static void move(const unsigned (&in)[NW], int src, unsigned (&out)[NW], int dst) {
+        out[2 * dst] = in[2 * src];
+        out[2 * dst + 1] = in[2 * src + 1];
+    }
+};
+
+// Output word `o` of a regrouping of 1- or 2-byte elements: element
+// sources given per output element (idx[k] = input element index).
+template <int W, int NW>
+__device__ __forceinline__ unsigned gather_word(const unsigned (&in)[NW], const int (&idx)[4 / W]) {
+    if constexpr (W == 2) {
+        // two halves: bytes 2h, 2h+1 of their words
+        const unsigned a = in[idx[0] >> 1], b = in[idx[1] >> 1];
+        const unsigned sa = (idx[0] & 1) ? 0x32u : 0x10u, sb = (idx[1] & 1) ? 0x76u : 0x54u;
+        return __byte_perm(a, b, sa | (sb << 8));
+    } else {
+        const unsigned lo = __byte_perm(in[idx[0] >> 2], in[idx[1] >> 2], (idx[0] & 3) | ((4 + (idx[1] & 3)) << 4));
+        const unsigned hi = __byte_perm(in[idx[2] >> 2], in[idx[3] >> 2], (idx[2] & 3) | ((4 + (idx[3] & 3)) << 4));
+        return __byte_perm(lo, hi, 0x5410u);
+    }
+}
+
+// out element (c * P + k) <- in element (k * N + c) (deinterleave) or the
+// inverse (interleave), for N groups of P = 16 / W elements.
+template <int W, int N, bool DEINT>
+__device__ __forceinline__ void regroup(const unsigned (&in)[4 * N], unsigned (&out)[4 * N]) {
+    constexpr int P = 16 / W;
+    if constexpr (W >= 4) {
+#pragma unroll
+        for (int c = 0; c < N; ++c)
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                if constexpr (DEINT)
+                    Lanes<W>::move(in, k * N + c, out, c * P + k);
+                else
+                    Lanes<W>::move(in, c * P + k, out, k * N + c);
+            }
+    } else {
+        constexpr int E = 4 / W;  // elements per output word
+#pragma unroll
+        for (int o = 0; o < 4 * N; ++o) {
+            int idx[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                const int e = o * E + i;  // output element
+                const int c = e / (DEINT ? P : N), k = e % (DEINT ? P : N);
+                idx[i] = DEINT ? k * N + c : k * P + c;
+            }
+            out[o] = gather_word<W>(in, idx);
+        }
+    }
+}
+
+// Narrow transposes with N in {2, 3, 4}, everything 16-byte aligned: each
+// thread moves P = 16 / W wide indices of all N narrow indices, with no
+// shared memory.  DEINT (narrow A, source interleaved): N consecutive
+// 16-byte loads hold P groups of N elements; they are regrouped in
+// registers into N words of P elements, one per destination row (plane).
+// Interleave (narrow B): one 16-byte load from each of the N source rows,
+// regrouped into N consecutive 16-byte words of the destination.  The last
+// group of a row may be partial: that thread moves it element by element.
+template <typename W, int N, bool DEINT>
+__global__ void __launch_bounds__(256)
+    lmad_aos_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadNarrowParams p) {
+    constexpr int P = 16 / (int)sizeof(W);
+    const uint64_t item = (uint64_t)blockIdx.x * 256u + threadIdx.x;
+    if (item >= p.tiles) return;  // tiles = groups per row x batch
+    uint32_t x = (uint32_t)item;
+    uint32_t q = div_q(x, p.div_tw);
+    const uint32_t g = x - q * (uint32_t)p.div_tw.d;
+    x = q;
+    int32_t so = 0, d = 0;
+    for (int k = 0; k < p.nc; ++k) {
+        uint32_t r = x;
+        if (k + 1 < p.nc) {
+            q = div_q(x, p.cdiv[k]);
+            r = x - q * (uint32_t)p.cdiv[k].d;
+            x = q;
+        }
+        so += (int32_t)r * (int32_t)p.cs[k];
+        d += (int32_t)r * (int32_t)p.ct[k];
+    }
+    const int32_t w0 = (int32_t)g * P;
+    const int rw = (int)min((uint64_t)P, p.n_wide - (uint64_t)w0);
+    const int32_t st = (int32_t)p.stride;
+    if (rw == P) {
+        unsigned a[4 * N], b[4 * N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            const uint4 v = DEINT ? __ldg(reinterpret_cast<const uint4*>(in + so + w0 * N) + j)
+                                  : __ldg(reinterpret_cast<const uint4*>(in + so + j * st + w0));
+            a[4 * j] = v.x, a[4 * j + 1] = v.y, a[4 * j + 2] = v.z, a[4 * j + 3] = v.w;
+        }
+        regroup<(int)sizeof(W), N, DEINT>(a, b);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            const uint4 v = make_uint4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+            if (DEINT)
+                __stcs(reinterpret_cast<uint4*>(out + d + j * st + w0), v);
+            else
+                __stcs(reinterpret_cast<uint4*>(out + d + w0 * N) + j, v);
+        }
+    } else {
+        for (int iw = 0; iw < rw; ++iw)
+            for (int c = 0; c < N; ++c) {
+                if (DEINT)
+                    out[d + c * st + w0 + iw] = in[so + (w0 + iw) * N + c];
+                else
+                    out[d + (w0 + iw) * N + c] = in[so + c * st + w0 + iw];
+            }
     }
 }
 
@@ -453,20 +749,24 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
 // Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
 // masked.
 // MODE: bit 0 = multi-dimension groups (offset tables, else linear
-// offsets), bit 1 = tiles of 4- or 8-byte words with the default shape
-// whose A side is whole take the 16-byte chunk path.
-enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3 };
+// offsets), bit 1 = tiles with the default shape whose A side is whole take
+// the 16-byte chunk path, bit 2 = that path writes 16-byte packs along B.
+enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3, kTilePack = 4 };
 
 template <typename W, bool WIDE, int MODE>
-__global__ void __launch_bounds__(256, (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
+__global__ void __launch_bounds__(256, (MODE & kTilePack) ? 4 : (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     using S = TileShape<sizeof(W)>;
-    constexpr int kTab = S::T / kMinTileSide + kMinTileSide;  // >= TA + TB
-    __shared__ __align__(16) W tile[S::T + (S::T / kMinTileSide) * S::PAD];  // 16-byte cp.async targets
+    using Sides = TileSides<S::T>;
+    constexpr int kTab = Sides::kMax + Sides::kMin;  // >= TA + TB
+    constexpr int kElemTile = S::T + Sides::kMax * S::PAD;
+    constexpr int kChunkTile = (sizeof(W) <= 8 ? S::T / (256 / (int)sizeof(W)) : 0) * kChunkPitch * (16 / (int)sizeof(W));
+    __shared__ __align__(16) W tile[kElemTile > kChunkTile ? kElemTile : kChunkTile];  // 16-byte cp.async targets
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
-    constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && (sizeof(W) == 4 || sizeof(W) == 8);
+    constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
+    constexpr bool PACK = (MODE & kTilePack) != 0;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
@@ -531,7 +831,7 @@ __global__ void __launch_bounds__(256, (MODE & kTileChunked) ? 6 : (sizeof(W) ==
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA};
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O>(in + so + tab_src[0], out + d, tile, ad, rb);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK>(in + so + tab_src[0], out + d, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -542,7 +842,7 @@ __global__ void __launch_bounds__(256, (MODE & kTileChunked) ? 6 : (sizeof(W) ==
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O>(src, dst, tile, ad, rb);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK>(src, dst, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -572,6 +872,8 @@ struct LmadCopy {
     int ga[kLmadMaxDims], gb[kLmadMaxDims], gc[kLmadMaxDims];
     int na = 0, nb = 0, nc = 0;
     int la = 0, lb = 0;
+    int narrow = 0;  // 1: group A narrow (lmad_narrow_kernel<.., true>), 2: group B narrow
+    int lt = 0;      // narrow kernel: log2 of the tile length along the wide dimension
     // STRIDED / unaligned MEMCPY: the widened copy
     int vec = 1;
     // BPC
@@ -662,8 +964,8 @@ int ceil_log2(uint64_t v) {
 // (TileShape<BYTES>): log2 of T, TA and TB.
 void tile_shape_log2(size_t word, int* lt, int* la, int* lb) {
     switch (word) {
-        case 1: *lt = 12, *la = 6, *lb = 6; return;
-        case 2: *lt = 12, *la = 6, *lb = 6; return;
+        case 1: *lt = 13, *la = 8, *lb = 5; return;
+        case 2: *lt = 13, *la = 7, *lb = 6; return;
         case 4: *lt = 12, *la = 6, *lb = 6; return;
         case 8: *lt = 10, *la = 5, *lb = 5; return;
         default: *lt = 10, *la = 5, *lb = 5; return;
@@ -705,7 +1007,7 @@ void choose_groups(LmadCopy& C, size_t word) {
     for (int k = 0; k < C.nb; ++k) n_b *= (uint64_t)C.d[C.gb[k]].n;
     int lt, la, lb;
     tile_shape_log2(word, &lt, &la, &lb);
-    const int lmin = 4, lmax = lt - 4;  // sides within [16, T / 16]
+    const int lmax = std::min(lt - 4, 8), lmin = lt - lmax;  // sides within [T / 256, 256], at least 16
     const int pa = std::min(std::max(ceil_log2(n_a), lmin), lmax);
     const int pb = std::min(std::max(ceil_log2(n_b), lmin), lmax);
     // TA * TB = T always: the kernel's loops cover exactly T elements, and a
@@ -719,6 +1021,36 @@ void choose_groups(LmadCopy& C, size_t word) {
     }
     C.la = la;
     C.lb = lb;
+}
+
+// The narrow-transpose kernel applies when both groups are one dimension,
+// one of them of at most 16 elements continues the other contiguously on
+// its unit-stride side (A: the wide dimension's source stride is n; B: the
+// wide dimension's destination stride is n), the destination stride along
+// the wide (A narrow) or narrow (B narrow) dimension is +1, and 32-bit
+// offsets hold every span.  Tile length: the largest power of two with
+// n * 2^lt elements in 16 KiB.
+uint64_t span_of(const Dim* d, int nd, bool dest);
+
+void choose_narrow(LmadCopy& C, size_t elem) {
+    C.narrow = 0;
+    if (C.na != 1 || C.nb != 1) return;
+    const Dim& a = C.d[C.ga[0]];
+    const Dim& b = C.d[C.gb[0]];
+    if (span_of(C.d, C.nd, false) > 0x3FFFFFFFull || span_of(C.d, C.nd, true) > 0x3FFFFFFFull) return;
+    int n = 0;
+    if (a.n <= 16 && b.s == a.n && b.t == 1) {
+        C.narrow = 1;
+        n = (int)a.n;
+    } else if (b.n <= 16 && a.t == b.n && b.t == 1) {
+        C.narrow = 2;
+        n = (int)b.n;
+    } else {
+        return;
+    }
+    int lt = 4;
+    while (lt < 20 && (uint64_t)n * (2ull << lt) * elem <= 16384) ++lt;
+    C.lt = lt;
 }
 
 bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
@@ -823,6 +1155,7 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
                     C.kind = LMAD_COPY_TRANSPOSE;
                     C.tdim = b;
                     choose_groups(C, elem);
+                    choose_narrow(C, elem);
                     break;
                 }
     }
@@ -911,7 +1244,72 @@ cudaError_t launch_rows(const unsigned char* in, unsigned char* out, const LmadC
 }
 
 template <typename W>
+cudaError_t launch_narrow_w(const W* in, W* out, const LmadCopy& C, cudaStream_t stream) {
+    const bool narrow_a = C.narrow == 1;
+    const Dim& a = C.d[C.ga[0]];
+    const Dim& b = C.d[C.gb[0]];
+    const Dim& wide = narrow_a ? b : a;
+    const int n = (int)(narrow_a ? a.n : b.n);
+    LmadNarrowParams p{};
+    p.n = n;
+    p.lt = C.lt;
+    p.n_wide = (uint64_t)wide.n;
+    p.stride = narrow_a ? a.t : b.s;
+    const uint64_t tile_len = 1ull << C.lt, tiles_w = (p.n_wide + tile_len - 1) / tile_len;
+    uint64_t batch = 1;
+    bool src16 = ((uintptr_t)in & 15) == 0, dst16 = ((uintptr_t)out & 15) == 0;
+    p.nc = C.nc;
+    for (int k = 0; k < C.nc; ++k) {
+        const Dim& x = C.d[C.gc[k]];
+        p.cdiv[k] = make_div((uint64_t)x.n, 32);
+        p.cs[k] = x.s;
+        p.ct[k] = x.t;
+        batch *= (uint64_t)x.n;
+        src16 = src16 && (iabs(x.s) * sizeof(W)) % 16 == 0;
+        dst16 = dst16 && (iabs(x.t) * sizeof(W)) % 16 == 0;
+    }
+    const bool block16 = ((uint64_t)n * tile_len * sizeof(W)) % 16 == 0;
+    const bool row16 = (tile_len * sizeof(W)) % 16 == 0;
+    if (narrow_a) {
+        p.vec_load = src16 && block16;
+        p.vec_store = dst16 && row16 && (iabs(a.t) * sizeof(W)) % 16 == 0;
+    } else {
+        p.vec_load = src16 && row16 && (iabs(b.s) * sizeof(W)) % 16 == 0;
+        p.vec_store = dst16 && block16;
+    }
+    if constexpr (sizeof(W) <= 8) {
+        if (p.vec_load && p.vec_store && n >= 2 && n <= 4 && LMAD_AOS) {
+            // register regrouping, one thread per group of 16 / W wide indices
+            const uint64_t groups = (p.n_wide + 16 / sizeof(W) - 1) / (16 / sizeof(W));
+            p.tiles = groups * batch;
+            if (p.tiles > 0xFFFFFFFFull) return cudaErrorInvalidValue;
+            p.div_tw = make_div(groups, 32);
+            const uint64_t blocks = (p.tiles + 255) / 256;
+            if (blocks > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+#define LMAD_AOS_LAUNCH(NV)                                                                                     \
+    (narrow_a ? lmad_aos_kernel<W, NV, true><<<(unsigned)blocks, 256, 0, stream>>>(in, out, p)                 \
+              : lmad_aos_kernel<W, NV, false><<<(unsigned)blocks, 256, 0, stream>>>(in, out, p))
+            if (n == 2) LMAD_AOS_LAUNCH(2);
+            else if (n == 3) LMAD_AOS_LAUNCH(3);
+            else LMAD_AOS_LAUNCH(4);
+#undef LMAD_AOS_LAUNCH
+            return cudaGetLastError();
+        }
+    }
+    p.tiles = tiles_w * batch;
+    if (p.tiles > 0xFFFFFFFFull) return cudaErrorInvalidValue;
+    p.div_tw = make_div(tiles_w, 32);
+    const unsigned grid = (unsigned)std::min<uint64_t>(p.tiles, 0x7FFFFFFFull);
+    if (narrow_a)
+        lmad_narrow_kernel<W, true><<<grid, 256, 0, stream>>>(in, out, p);
+    else
+        lmad_narrow_kernel<W, false><<<grid, 256, 0, stream>>>(in, out, p);
+    return cudaGetLastError();
+}
+
+template <typename W>
 cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStream_t stream) {
+    if (C.narrow) return launch_narrow_w(in, out, C, stream);
     uint64_t n_a = 1, n_b = 1, batch = 1;
     for (int k = 0; k < C.na; ++k) n_a *= (uint64_t)C.d[C.ga[k]].n;
     for (int k = 0; k < C.nb; ++k) n_b *= (uint64_t)C.d[C.gb[k]].n;
@@ -963,16 +1361,32 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     // 8-byte words measured slower on the chunk path (32 x 32 tiles: 83-85%
     // of a copy against 85-90% element-wise), so it is taken for 4-byte
     // words only; LMAD_TILE_CHUNKS=2 enables it for 8-byte words too
-    const bool chunked = (LMAD_TILE_CHUNKS && sizeof(W) == 4 && C.la == 6 && C.lb == 6) ||
+    const bool chunked = (LMAD_TILE_CHUNKS && sizeof(W) == 1 && C.la == 8 && C.lb == 5) ||
+                         (LMAD_TILE_CHUNKS && sizeof(W) == 2 && C.la == 7 && C.lb == 6) ||
+                         (LMAD_TILE_CHUNKS && sizeof(W) == 4 && C.la == 6 && C.lb == 6) ||
                          (LMAD_TILE_CHUNKS == 2 && sizeof(W) == 8 && C.la == 5 && C.lb == 5);
-    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0);
+    // 16-byte packs along B: B walks the destination forwards from stride
+    // +1, and every A and batch destination stride and the origin are
+    // 16-byte aligned
+    bool pack = chunked && (LMAD_TILE_PACK_WORDS & sizeof(W)) != 0 && ((uintptr_t)out & 15) == 0;
+    for (int k = 0; pack && k < C.nb; ++k) pack = C.d[C.gb[k]].t > 0;
+    for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * sizeof(W)) % 16 == 0;
+    for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
+    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
+                     (pack ? kTilePack : 0);
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
-    if constexpr (sizeof(W) == 4 || sizeof(W) == 8) {
+    if constexpr (sizeof(W) <= 8) {
         if (mode & kTileChunked) {
-            if (wide && mode == kTileTablesChunked) LMAD_TILE(true, kTileTablesChunked);
-            else if (wide) LMAD_TILE(true, kTileChunked);
-            else if (mode == kTileTablesChunked) LMAD_TILE(false, kTileTablesChunked);
-            else LMAD_TILE(false, kTileChunked);
+            switch (mode | (wide ? 8 : 0)) {
+                case kTileChunked: LMAD_TILE(false, kTileChunked); break;
+                case kTileTablesChunked: LMAD_TILE(false, kTileTablesChunked); break;
+                case kTileChunked | kTilePack: LMAD_TILE(false, kTileChunked | kTilePack); break;
+                case kTileTablesChunked | kTilePack: LMAD_TILE(false, kTileTablesChunked | kTilePack); break;
+                case 8 | kTileChunked: LMAD_TILE(true, kTileChunked); break;
+                case 8 | kTileTablesChunked: LMAD_TILE(true, kTileTablesChunked); break;
+                case 8 | kTileChunked | kTilePack: LMAD_TILE(true, kTileChunked | kTilePack); break;
+                default: LMAD_TILE(true, kTileTablesChunked | kTilePack); break;
+            }
             return cudaGetLastError();
         }
     }
@@ -1058,6 +1472,9 @@ extern "C" bmmc_status lmad_copy_query(int ndims, const int64_t* sizes, int64_t 
         for (int k = 0; k < C.nb; ++k) r.group_b |= 1u << C.gb[k];
         r.tile_a = 1 << C.la;
         r.tile_b = 1 << C.lb;
+        r.narrow = C.narrow;
+        if (C.narrow == 1) r.tile_a = (int)C.d[C.ga[0]].n, r.tile_b = 1 << C.lt;
+        if (C.narrow == 2) r.tile_a = 1 << C.lt, r.tile_b = (int)C.d[C.gb[0]].n;
     }
     r.elements = C.elements;
     *info = r;

@@ -361,7 +361,15 @@ typedef struct {
                                           destination); the others are the batch.  0 for
                                           other kinds */
     int tile_a, tile_b;                /* TRANSPOSE: tile sides (A-indices x B-indices of one
-                                          batch index), powers of two; 0 for other kinds */
+                                          batch index), powers of two except the narrow side
+                                          of a narrow transpose; 0 for other kinds */
+    int narrow;                        /* TRANSPOSE: 1 = group A is one dimension of at most 16
+                                          elements that continues group B contiguously in the
+                                          source, 2 = group B is such a dimension continuing A
+                                          in the destination (e.g. NHWC <-> NCHW with few
+                                          channels): each tile is one contiguous block on that
+                                          side, moved with 16-byte accesses; 0 = the general
+                                          tile kernel */
     uint64_t elements;                 /* index tuples copied (product of the sizes) */
 } lmad_copy_info_t;
 

@@ -360,3 +360,31 @@ def test_rows_kernel_slices(elem, shape, lo, hi, out_off):
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == ("rows" if (hi - lo) * elem >= 16 else "strided")
     _check(w, elem, seed=lo + hi)
+
+
+def _layout_case(shape, perm, in_offset=0, out_offset=0):
+    src_strides = synth.row_major_strides(shape)
+    out_rm = synth.row_major_strides([shape[p] for p in perm])
+    out_strides = [0] * len(shape)
+    for pos, p in enumerate(perm):
+        out_strides[p] = out_rm[pos]
+    total = int(np.prod(shape))
+    return dict(sizes=list(shape), in_offset=in_offset, in_strides=src_strides, in_elems=total + in_offset + 5,
+                out_offset=out_offset, out_strides=out_strides, out_elems=total + out_offset + 5)
+
+
+@pytest.mark.parametrize("elem", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("c", [2, 3, 4, 16])
+@pytest.mark.parametrize("hw,offsets", [((37, 53), (0, 0)), ((64, 64), (0, 0)), ((64, 64), (1, 3)),
+                                        ((300, 41), (2, 0))])
+def test_image_layout_conversions(elem, c, hw, offsets):
+    """NHWC -> NCHW and NCHW -> NHWC with few channels: the narrow
+    transpose (16-byte paths when aligned, element paths when not, ragged
+    last tiles), against the oracle."""
+    h, w = hw
+    for shape, perm, narrow in (((3, h, w, c), (0, 3, 1, 2), 1), ((3, c, h, w), (0, 2, 3, 1), 2)):
+        case = _layout_case(shape, perm, *offsets)
+        q = bm.lmad_copy_query(case["sizes"], case["in_offset"], case["in_strides"], case["out_offset"],
+                               case["out_strides"], elem, in_elems=case["in_elems"], out_elems=case["out_elems"])
+        assert q["kind"] == "transpose" and q["narrow"] == narrow, q
+        _check(case, elem, seed=c * 7 + elem)

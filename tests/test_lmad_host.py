@@ -149,23 +149,24 @@ def test_copy_without_device_fails_loudly():
     assert (b == 0).all()
 
 
-TILE_ELEMS = {1: 4096, 2: 4096, 4: 4096, 8: 1024, 16: 1024}
+TILE_ELEMS = {1: 8192, 2: 8192, 4: 4096, 8: 1024, 16: 1024}
 
 
 @pytest.mark.parametrize("seed", range(300))
 def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     """The tile kernel's loops cover TA * TB = T elements per tile with both
-    sides in [16, T / 16]; the groups partition the dimensions, group A
+    sides in [T / 256, 256] (at least 16); the groups partition the dimensions, group A
     starts at the unit source stride and group B at the unit destination
     stride."""
     w = synth.draw_lmad_view(5000 + seed, max_dims=5, max_elems=1 << 16)
     elem = (1, 2, 4, 8, 16)[seed % 5]
     q = _query(w, elem)
-    if q["kind"] != "transpose":
+    if q["kind"] != "transpose" or q["narrow"]:
         return
     ta, tb = q["tile"]
     T = TILE_ELEMS[elem]
-    assert ta * tb == T and 16 <= ta <= T // 16 and 16 <= tb <= T // 16
+    side_max = min(256, T // 16)
+    assert ta * tb == T and T // side_max <= ta <= side_max and T // side_max <= tb <= side_max
     a, b = q["group_a"], q["group_b"]
     assert a[0] == 0 and q["dims"][0][1] == 1
     assert q["transpose_out_dim"] in b and abs(q["dims"][q["transpose_out_dim"]][2]) == 1
@@ -173,18 +174,25 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
 
 
 def _chunk_tile_emulation(word, base_mis, sb, rb):
-    """The chunk path of the tile kernel, replayed on the host for 4- and
-    8-byte words: rows of 256 bytes (64 or 32 elements, V = 16 / word per
+    """The chunk path of the tile kernel, replayed on the host for 1- to
+    8-byte words: rows of 256 bytes (TA = 16 * V elements, V = 16 / word per
     chunk) fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
     misaligned rows), the V leftover elements of a misaligned row one per
-    thread, rows kept shifted by their misalignment in 17 rotated chunk slots,
-    then read back column-wise; rows rb.. of a tile short along B are
-    skipped.  Every element is placed exactly once, every 16-byte fetch is
-    aligned, and every read returns the element the transpose needs."""
+    thread, rows kept in shared memory shifted by their misalignment and
+    rotated by (row / 8) chunks inside a 25-chunk pitch, then read back
+    column-wise at row offset + column; rows rb.. of a tile short along B are
+    skipped.  Every element is placed exactly once, every 16-byte fetch and
+    every 16-byte shared store is aligned, and every read returns the element
+    the transpose needs."""
     V = 16 // word
-    TA, TB, slots = 16 * V, 4096 // (16 * V) if word == 4 else 1024 // (16 * V), 17
-    pitch = slots * V
+    TA = 16 * V
+    TB = {1: 8192, 2: 8192, 4: 4096, 8: 1024}[word] // TA
+    pitch = 25 * V
     tile = {}
+
+    def base_of(row):
+        return row * pitch + (row >> 3) * V
+
     for t in range(256):
         for r in range(TB * 16 // 256):
             idx = t + 256 * r
@@ -195,18 +203,18 @@ def _chunk_tile_emulation(word, base_mis, sb, rb):
             if m == 0 or kk < 15:
                 k = kk + (1 if m else 0)
                 assert (base_mis + row * sb + V * k - m) % V == 0
-                slot = (k + (row >> 3)) % slots
+                a0 = base_of(row) + V * k
+                assert a0 % V == 0
                 for j in range(V):
-                    a = row * pitch + V * slot + j
-                    assert a not in tile and 0 <= V * k - m + j < TA
+                    a = a0 + j
+                    assert a not in tile and 0 <= V * k - m + j < TA and a < base_of(row) - (row >> 3) * V + pitch
                     tile[a] = (row, V * k - m + j)
-        if t < TB * V:
-            row, j = t // V, t % V
+        for u in range(t, TB * V, 256):
+            row, j = u // V, u % V
             m = (base_mis + row * sb) % V
             if m and row < rb:
                 e = j if j < V - m else TA - V + j
-                c = e + m
-                a = row * pitch + V * (((c // V) + (row >> 3)) % slots) + c % V
+                a = base_of(row) + e + m
                 assert a not in tile
                 tile[a] = (row, e)
     assert len(tile) == TA * min(rb, TB) and max(tile) < TB * pitch
@@ -215,14 +223,13 @@ def _chunk_tile_emulation(word, base_mis, sb, rb):
         ib, ia0 = t % TB, t // TB
         if ib >= rb:
             continue
-        m = (base_mis + ib * sb) % V
+        off = base_of(ib) + (base_mis + ib * sb) % V
         for r in range(TA // step):
-            c = ia0 + step * r + m
-            assert tile[ib * pitch + V * (((c // V) + (ib >> 3)) % slots) + c % V] == (ib, ia0 + step * r)
+            assert tile[off + ia0 + step * r] == (ib, ia0 + step * r)
 
 
 @pytest.mark.parametrize("sb", [1, 2, 3, 4, 5, 64, 65, 66, 67, 1000, 1001, 8191, 8192, 8193, 8194])
-@pytest.mark.parametrize("word", [4, 8])
+@pytest.mark.parametrize("word", [1, 2, 4, 8])
 def test_chunked_tile_mapping(word, sb):
     for base_mis in range(16 // word):
         for rb in (64, 62, 32, 31, 17, 1):
