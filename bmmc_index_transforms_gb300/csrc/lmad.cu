@@ -403,40 +403,41 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 // its first element's offset from one, 1..V-1) leaves V elements in the
 // partial chunks at its two ends (V - m at the head, m at the tail), which a
 // second pass copies one element per thread.  Row ib is kept in shared
-// memory shifted by its misalignment and rotated by ib / 8 chunks inside a
-// 25-chunk pitch (the rotation spreads the store phase's column reads over
-// the banks; with no wrap-around an element's address is a per-row offset
-// plus its column).  Group A is contiguous in the source (its offset is the
+// memory shifted by its misalignment and rotated by (ib / 8) mod 4 chunks
+// inside a pitch of chunk_pitch(NCH) chunks (the rotation spreads the store
+// phase's column reads, 32 consecutive rows per warp, over the banks; with
+// no wrap-around an element's address is a per-row offset plus its column).
+// NCH = 16 or 8 chunks per source row (256- or 128-byte rows).  Group A is contiguous in the source (its offset is the
 // A-index itself), so src points at the tile's A-origin and only B parts
 // come from `ad`.
 constexpr int clog2(int v) { return v <= 1 ? 0 : 1 + clog2(v / 2); }
-// Row pitch of the chunk path in 16-byte chunks: 17 for a shifted 256-byte
-// segment plus up to 7 of rotation; 25 * 4 = 100 words keeps neighbouring
-// rows 4 banks apart.
-constexpr int kChunkPitch = 25;
+// Pitch in chunks for NCH chunks per source row: room for NCH + 1 chunks
+// (a misaligned row) rotated by up to 3, and 1 mod 8 so that neighbouring
+// rows start 4 banks apart.
+constexpr int chunk_pitch(int nch) { return ((nch + 4 + 6) / 8) * 8 + 1; }
 
-template <typename W, typename O, bool PACK, typename Addr>
+template <typename W, typename O, bool PACK, int NCH, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
                                                     const Addr& ad, int rb) {
-    constexpr int V = 16 / (int)sizeof(W), LV = clog2(V);
-    constexpr int TA = 16 * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
-    constexpr int kPitch = kChunkPitch * V;
-    static_assert(TB / 8 <= kChunkPitch - 17, "rotation fits the pitch");
+    constexpr int V = 16 / (int)sizeof(W), LV = clog2(V), LNCH = clog2(NCH);
+    constexpr int TA = NCH * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
+    constexpr int kPitch = chunk_pitch(NCH) * V;
+    static_assert(NCH + 1 + 3 <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
     // row r holds its segment shifted by its misalignment m, starting at
     // chunk r / 8 of its pitch: element (r, c = column + m) at
     // r * kPitch + (r / 8) * V + c, whole chunks at 16-byte boundaries
 #pragma unroll
-    for (int r = 0; r < TB * 16 / 256; ++r) {
+    for (int r = 0; r < TB * NCH / 256; ++r) {
         const int idx = t + 256 * r;
-        const int row = idx >> 4, kk = idx & 15;
+        const int row = idx >> LNCH, kk = idx & (NCH - 1);
         if (row >= rb) break;  // rows grow with r
         const O s0 = ad.src_b(row);
         const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
-        if (m == 0 || kk < 15) {
+        if (m == 0 || kk < NCH - 1) {
             const int k = kk + (m != 0);
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + (row >> 3))),
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ((row >> 3) & 3))),
                           reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
         }
     }
@@ -448,7 +449,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m != 0) {
             const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
-            W* slot = tile + row * kPitch + V * (row >> 3) + e + m;
+            W* slot = tile + row * kPitch + V * ((row >> 3) & 3) + e + m;
             if constexpr (sizeof(W) >= 4)
                 cp_async_word(slot, src + s0 + e);
             else
@@ -470,7 +471,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int rr = ib0 + k < rb ? ib0 + k : ib0;
-            off[k] = rr * kPitch + V * (rr >> 3) + (int)((base_mis + (unsigned)ad.src_b(rr)) & (V - 1));
+            off[k] = rr * kPitch + V * ((rr >> 3) & 3) + (int)((base_mis + (unsigned)ad.src_b(rr)) & (V - 1));
         }
         W* o = dst + ad.dst_b(ib0);
         const bool whole = ib0 + V <= rb;
@@ -494,7 +495,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     const int ib = t & (TB - 1), ia0 = t >> LTB;
     constexpr int kStep = 256 / TB, kPer = TA / kStep;
     if (ib >= rb) return;  // no barrier follows inside this function
-    const W* row = tile + ib * kPitch + V * (ib >> 3) + (int)((base_mis + (unsigned)ad.src_b(ib)) & (V - 1));
+    const W* row = tile + ib * kPitch + V * ((ib >> 3) & 3) + (int)((base_mis + (unsigned)ad.src_b(ib)) & (V - 1));
     W* o = dst + ad.dst_b(ib);
     constexpr int CH = kPer < 8 ? kPer : 8;
 #pragma unroll 1
@@ -750,8 +751,9 @@ __global__ void __launch_bounds__(256)
 // masked.
 // MODE: bit 0 = multi-dimension groups (offset tables, else linear
 // offsets), bit 1 = tiles with the default shape whose A side is whole take
-// the 16-byte chunk path, bit 2 = that path writes 16-byte packs along B.
-enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3, kTilePack = 4 };
+// the 16-byte chunk path, bit 2 = that path writes 16-byte packs along B,
+// bit 3 = the chunk path with 128-byte source rows (8 chunks) instead of 256.
+enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3, kTilePack = 4, kTileHalfRows = 8 };
 
 template <typename W, bool WIDE, int MODE>
 __global__ void __launch_bounds__(256, (MODE & kTilePack) ? 4 : (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
@@ -762,7 +764,11 @@ __global__ void __launch_bounds__(256, (MODE & kTilePack) ? 4 : (MODE & kTileChu
     using Sides = TileSides<S::T>;
     constexpr int kTab = Sides::kMax + Sides::kMin;  // >= TA + TB
     constexpr int kElemTile = S::T + Sides::kMax * S::PAD;
-    constexpr int kChunkTile = (sizeof(W) <= 8 ? S::T / (256 / (int)sizeof(W)) : 0) * kChunkPitch * (16 / (int)sizeof(W));
+    constexpr int NCH = (MODE & kTileHalfRows) ? 8 : 16;  // chunk path: chunks per source row
+    // chunk path: T / TA rows of chunk_pitch(NCH) chunks of 16 / W elements
+    constexpr int kChunkTile = sizeof(W) <= 8 ? (S::T / (NCH * (16 / (int)sizeof(W)))) * chunk_pitch(NCH) *
+                                                    (16 / (int)sizeof(W))
+                                              : 0;
     __shared__ __align__(16) W tile[kElemTile > kChunkTile ? kElemTile : kChunkTile];  // 16-byte cp.async targets
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
@@ -831,7 +837,7 @@ __global__ void __launch_bounds__(256, (MODE & kTilePack) ? 4 : (MODE & kTileChu
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA};
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK>(in + so + tab_src[0], out + d, tile, ad, rb);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH>(in + so + tab_src[0], out + d, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -842,7 +848,7 @@ __global__ void __launch_bounds__(256, (MODE & kTilePack) ? 4 : (MODE & kTileChu
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK>(src, dst, tile, ad, rb);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH>(src, dst, tile, ad, rb);
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -1361,10 +1367,12 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     // 8-byte words measured slower on the chunk path (32 x 32 tiles: 83-85%
     // of a copy against 85-90% element-wise), so it is taken for 4-byte
     // words only; LMAD_TILE_CHUNKS=2 enables it for 8-byte words too
-    const bool chunked = (LMAD_TILE_CHUNKS && sizeof(W) == 1 && C.la == 8 && C.lb == 5) ||
-                         (LMAD_TILE_CHUNKS && sizeof(W) == 2 && C.la == 7 && C.lb == 6) ||
-                         (LMAD_TILE_CHUNKS && sizeof(W) == 4 && C.la == 6 && C.lb == 6) ||
-                         (LMAD_TILE_CHUNKS == 2 && sizeof(W) == 8 && C.la == 5 && C.lb == 5);
+    // the chunk path: source rows of 256 bytes (the default shapes) or 128
+    // bytes (a group A of up to half that), 1- to 4-byte words (8-byte words
+    // measured slower on it; LMAD_TILE_CHUNKS=2 enables them)
+    const uint64_t row_bytes = (1ull << C.la) * sizeof(W);
+    const bool chunked = (LMAD_TILE_CHUNKS && (sizeof(W) <= 4 || LMAD_TILE_CHUNKS == 2) && sizeof(W) <= 8 &&
+                          (row_bytes == 256 || row_bytes == 128) && (1ull << C.lb) <= 256);
     // 16-byte packs along B: B walks the destination forwards from stride
     // +1, and every A and batch destination stride and the origin are
     // 16-byte aligned
@@ -1373,19 +1381,28 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * sizeof(W)) % 16 == 0;
     for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
     const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
-                     (pack ? kTilePack : 0);
+                     (pack ? kTilePack : 0) | (chunked && row_bytes == 128 ? kTileHalfRows : 0);
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
     if constexpr (sizeof(W) <= 8) {
         if (mode & kTileChunked) {
-            switch (mode | (wide ? 8 : 0)) {
-                case kTileChunked: LMAD_TILE(false, kTileChunked); break;
-                case kTileTablesChunked: LMAD_TILE(false, kTileTablesChunked); break;
-                case kTileChunked | kTilePack: LMAD_TILE(false, kTileChunked | kTilePack); break;
-                case kTileTablesChunked | kTilePack: LMAD_TILE(false, kTileTablesChunked | kTilePack); break;
-                case 8 | kTileChunked: LMAD_TILE(true, kTileChunked); break;
-                case 8 | kTileTablesChunked: LMAD_TILE(true, kTileTablesChunked); break;
-                case 8 | kTileChunked | kTilePack: LMAD_TILE(true, kTileChunked | kTilePack); break;
-                default: LMAD_TILE(true, kTileTablesChunked | kTilePack); break;
+            switch (mode | (wide ? 16 : 0)) {
+                case 2: LMAD_TILE(false, 2); break;
+                case 6: LMAD_TILE(false, 6); break;
+                case 3: LMAD_TILE(false, 3); break;
+                case 7: LMAD_TILE(false, 7); break;
+                case 10: LMAD_TILE(false, 10); break;
+                case 14: LMAD_TILE(false, 14); break;
+                case 11: LMAD_TILE(false, 11); break;
+                case 15: LMAD_TILE(false, 15); break;
+                case 18: LMAD_TILE(true, 2); break;
+                case 22: LMAD_TILE(true, 6); break;
+                case 19: LMAD_TILE(true, 3); break;
+                case 23: LMAD_TILE(true, 7); break;
+                case 26: LMAD_TILE(true, 10); break;
+                case 30: LMAD_TILE(true, 14); break;
+                case 27: LMAD_TILE(true, 11); break;
+                case 31: LMAD_TILE(true, 15); break;
+                default: return cudaErrorInvalidValue;
             }
             return cudaGetLastError();
         }

@@ -173,41 +173,42 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert not set(a) & set(b)
 
 
-def _chunk_tile_emulation(word, base_mis, sb, rb):
+def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16):
     """The chunk path of the tile kernel, replayed on the host for 1- to
     8-byte words: rows of 256 bytes (TA = 16 * V elements, V = 16 / word per
     chunk) fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
     misaligned rows), the V leftover elements of a misaligned row one per
     thread, rows kept in shared memory shifted by their misalignment and
-    rotated by (row / 8) chunks inside a 25-chunk pitch, then read back
+    rotated by (row / 8) mod 4 chunks inside a pitch of 25 (16 chunks per
+    row) or 17 (8 chunks per row, 128-byte rows) chunks, then read back
     column-wise at row offset + column; rows rb.. of a tile short along B are
     skipped.  Every element is placed exactly once, every 16-byte fetch and
     every 16-byte shared store is aligned, and every read returns the element
     the transpose needs."""
     V = 16 // word
-    TA = 16 * V
+    TA = nch * V
     TB = {1: 8192, 2: 8192, 4: 4096, 8: 1024}[word] // TA
-    pitch = 25 * V
+    pitch = {16: 25, 8: 17}[nch] * V
     tile = {}
 
     def base_of(row):
-        return row * pitch + (row >> 3) * V
+        return row * pitch + ((row >> 3) & 3) * V
 
     for t in range(256):
-        for r in range(TB * 16 // 256):
+        for r in range(TB * nch // 256):
             idx = t + 256 * r
-            row, kk = idx >> 4, idx & 15
+            row, kk = idx // nch, idx % nch
             if row >= rb:
                 break
             m = (base_mis + row * sb) % V
-            if m == 0 or kk < 15:
+            if m == 0 or kk < nch - 1:
                 k = kk + (1 if m else 0)
                 assert (base_mis + row * sb + V * k - m) % V == 0
                 a0 = base_of(row) + V * k
                 assert a0 % V == 0
                 for j in range(V):
                     a = a0 + j
-                    assert a not in tile and 0 <= V * k - m + j < TA and a < base_of(row) - (row >> 3) * V + pitch
+                    assert a not in tile and 0 <= V * k - m + j < TA and a < row * pitch + pitch
                     tile[a] = (row, V * k - m + j)
         for u in range(t, TB * V, 256):
             row, j = u // V, u % V
@@ -231,9 +232,10 @@ def _chunk_tile_emulation(word, base_mis, sb, rb):
 @pytest.mark.parametrize("sb", [1, 2, 3, 4, 5, 64, 65, 66, 67, 1000, 1001, 8191, 8192, 8193, 8194])
 @pytest.mark.parametrize("word", [1, 2, 4, 8])
 def test_chunked_tile_mapping(word, sb):
-    for base_mis in range(16 // word):
-        for rb in (64, 62, 32, 31, 17, 1):
-            _chunk_tile_emulation(word, base_mis, sb, rb)
+    for nch in (16, 8):
+        for base_mis in range(16 // word):
+            for rb in (128, 100, 64, 62, 32, 31, 17, 1):
+                _chunk_tile_emulation(word, base_mis, sb, rb, nch)
 
 
 def test_rows_kind_for_small_elements():
