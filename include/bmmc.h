@@ -330,7 +330,10 @@ typedef enum {
                                 destination's unit-stride dimension and those
                                 continuing it in the destination), the other
                                 dimensions as the batch (the page's transpose and
-                                "map transpose" cases, any sizes) */
+                                "map transpose" cases, any sizes); when one group is
+                                a single dimension of at most 16 elements continuing
+                                the other (few channels), a narrow-side kernel (see
+                                lmad_copy_info_t.narrow) */
     LMAD_COPY_STRIDED = 4,   /* anything else: the page's stride-sorted copy, one
                                 thread per index tuple, adjacent threads adjacent
                                 along the smallest source stride */
