@@ -451,6 +451,7 @@ def run_ours(args):
             "copy_kernel_gbs": round(copy_gbs, 1),
             "torch_copy_gbs": round(torch_copy_gbs, 1),
             "per_seed_median_gbs": {"mean": round(sum(per_seed_gbs) / len(per_seed_gbs), 1),
+                                    "median": round(median(per_seed_gbs), 1),
                                     "min": round(min(per_seed_gbs), 1),
                                     "max": round(max(per_seed_gbs), 1)},
             "worst_case_gbs": round(worst_gbs, 1),
