@@ -427,3 +427,25 @@ def test_naive_option_plans_the_per_element_kernel():
     with pytest.raises(bm.BmmcError) as e:
         bm.Plan(rows, c, 8, naive=True, mode=1)
     assert e.value.status == _capi.ERR_INVALID_ARG
+
+
+def test_concurrent_planning_from_threads():
+    """Planning is host-only and thread-safe: eight threads planning the same
+    matrices get the same plan descriptions and tile bases as one thread
+    (ctypes releases the GIL, so the calls overlap inside the library)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    mats = [synth.draw_bmmc(s, 24, lambda r: ref.f2_rank(24, r) == 24)[:2] for s in range(40)]
+
+    def plan_all(_):
+        out = []
+        for rows, c in mats:
+            with bm.Plan(rows, c, 4) as p:
+                out.append((p.info, p.tile()))
+        return out
+
+    want = plan_all(None)
+    with ThreadPoolExecutor(8) as ex:
+        results = list(ex.map(plan_all, range(8)))
+    for r in results:
+        assert r == want

@@ -659,3 +659,28 @@ def test_naive_kernel_option(bm, n, elem):
             p.permute(d_in, d_out)
             torch.cuda.synchronize()
             assert _host(d_out, arr).tobytes() == oracle.scatter(n, rows, c, arr).tobytes()
+
+
+def test_one_plan_from_several_threads_and_streams(bm):
+    """A plan is immutable: four host threads permute with the same plan, each
+    on its own stream and buffers, concurrently; every result is the
+    oracle's."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    n, elem = 22, 4
+    rows, c = _random(77, n)
+    arr = synth.fill_int(n, elem)
+    want = oracle.scatter(n, rows, c, arr).tobytes()
+    with bm.Plan(rows, c, elem) as p:
+        def work(k):
+            s = torch.cuda.Stream()
+            d_in = _dev(arr)
+            outs = [torch.zeros_like(d_in) for _ in range(3)]
+            with torch.cuda.stream(s):
+                for o in outs:
+                    p.permute(d_in, o, s)
+            s.synchronize()
+            return [_host(o, arr).tobytes() == want for o in outs]
+        with ThreadPoolExecutor(4) as ex:
+            results = list(ex.map(work, range(4)))
+    assert all(all(r) for r in results)
