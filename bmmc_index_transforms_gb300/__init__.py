@@ -24,7 +24,7 @@ __all__ = [
     "BmmcError", "Plan", "bmmc_plan", "bmmc_plan_ex", "bmmc_plan_destroy", "bmmc_plan_info",
     "bmmc_plan_factor", "bmmc_plan_tile", "bmmc_permute", "bmmc_permute_scratch",
     "bmmc_permute_host", "bmmc_permute_static_scratch", "transpose2d", "bpc_permute", "bmmc_dims_permute",
-    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "lmad_copy", "lmad_copy_query", "bmmc_parm_rows", "bmmc_inverse_rows", "bmmc_compose",
+    "bmmc_dims_permute_bits", "bmmc_copy", "bmmc_lmad_copy", "bmmc_lmad_bpc", "lmad_copy", "lmad_copy_query", "lmad_copy_tensor", "contiguous", "bmmc_parm_rows", "bmmc_inverse_rows", "bmmc_compose",
     "bmmc_status_string", "bmmc_version", "library_path",
 ]
 
@@ -273,6 +273,38 @@ def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], o
     _check(_capi.lib().lmad_copy(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
                                  _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
                                  _stream(stream, inp, out)), "lmad_copy")
+
+
+def _tensor_lmad(x):
+    """A tensor view as an LMAD on its storage: (base address, offset,
+    strides, element count of the storage), all in elements."""
+    es = x.element_size()
+    storage = x.untyped_storage()
+    return int(storage.data_ptr()), int(x.storage_offset()), [int(v) for v in x.stride()], storage.nbytes() // es
+
+
+def lmad_copy_tensor(src, dst, stream=None) -> None:
+    """dst[i] = src[i] for every index of two tensor views of the same shape
+    and element size, whatever their strides and storage offsets: the views
+    are passed to lmad_copy as LMADs on their storages (a tensor view is
+    exactly an offset plus one stride per dimension)."""
+    if tuple(src.shape) != tuple(dst.shape) or src.element_size() != dst.element_size():
+        raise ValueError("lmad_copy_tensor: the views need the same shape and element size")
+    sb, so, ss, se = _tensor_lmad(src)
+    db, do, ds, de = _tensor_lmad(dst)
+    lmad_copy(list(src.shape), so, ss, do, ds, src.element_size(), sb, db, _stream(stream, src, dst),
+              in_elems=se, out_elems=de)
+
+
+def contiguous(x, stream=None):
+    """A new row-major tensor with the contents of the view x (the copy
+    torch's .contiguous() makes), moved by lmad_copy."""
+    import torch
+
+    out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    if out.numel():
+        lmad_copy_tensor(x, out, stream)
+    return out
 
 
 def bmmc_inverse_rows(A_rows: Sequence[int]) -> list[int]:

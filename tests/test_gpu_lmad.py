@@ -426,3 +426,33 @@ def test_concurrent_lmad_copies_from_threads():
 
     with ThreadPoolExecutor(4) as ex:
         assert all(ex.map(work, range(16)))
+
+
+@pytest.mark.parametrize("dtype", ["uint8", "float16", "bfloat16", "float32", "float64", "complex64", "complex128"])
+def test_contiguous_of_tensor_views(dtype):
+    """bm.contiguous(view) equals torch's .contiguous() for transposed,
+    permuted, sliced (with steps), diagonal and expanded views (a view is an
+    offset plus strides on its storage: one LMAD)."""
+    dt = getattr(torch, dtype)
+    g = torch.Generator(device="cpu").manual_seed(3)
+    base = (torch.randn(6, 40, 33, 17, generator=g) * 100)
+    if dtype.startswith("complex"):
+        base = torch.complex(base, base * 0.5)
+    x = base.to(dt).cuda()
+    views = [x.transpose(1, 3), x.permute(3, 1, 0, 2), x[:, 5:37:3, ::2, 1:], x[2, :, 7], x.narrow(2, 4, 20),
+             x[:, :17, :17, 0].diagonal(dim1=1, dim2=2), x[0, 0, 0].expand(9, 17), x[1:4, 3].unsqueeze(1).expand(3, 5, 33, 17)]
+    for v in views:
+        got = bm.contiguous(v)
+        assert got.is_contiguous() and got.shape == v.shape
+        assert torch.equal(got.view(torch.uint8) if dtype != "uint8" else got,
+                           v.contiguous().view(torch.uint8) if dtype != "uint8" else v.contiguous())
+
+
+def test_lmad_copy_tensor_into_a_strided_destination():
+    """Copy a transposed view into every other column of a wider tensor; the
+    columns in between keep their values."""
+    x = torch.arange(50 * 30, dtype=torch.float32, device="cuda").view(50, 30)
+    big = torch.full((30, 100), -1.0, device="cuda")
+    bm.lmad_copy_tensor(x.t(), big[:, ::2])
+    torch.cuda.synchronize()
+    assert torch.equal(big[:, ::2], x.t()) and (big[:, 1::2] == -1).all()

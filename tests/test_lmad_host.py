@@ -253,3 +253,14 @@ def test_rows_kind_for_small_elements():
     assert kind(1, (100, 16)) == "strided"     # 15-byte rows
     assert kind(4, (100, 9)) == "strided"
     assert kind(1, (100, 33), out_pad=1) == "strided"
+
+
+def test_lmad_copy_tensor_argument_checks():
+    """Views of different shapes or element sizes are refused before anything
+    reaches the library."""
+    import torch
+
+    with pytest.raises(ValueError):
+        bm.lmad_copy_tensor(torch.zeros(3, 4), torch.zeros(4, 3))
+    with pytest.raises(ValueError):
+        bm.lmad_copy_tensor(torch.zeros(3, 4), torch.zeros(3, 4, dtype=torch.float64))
