@@ -48,6 +48,10 @@ constexpr int kLmadMaxDims = LMAD_MAX_DIMS;
 #define LMAD_ROWS_MAX_ELEM 2
 #endif
 constexpr uint64_t kLmadMaxTuples = 1ull << 40;
+// Element counts above this are taken as this: no array that large fits an
+// address space, and with every offset below 2^62 the stride products of the
+// analysis (s * n of a dimension that spans less than 2^62) stay inside int64.
+constexpr uint64_t kLmadMaxElems = 1ull << 62;
 
 // q = floor(x / d) = (t + ((x - t) >> s1)) >> s2 with t = mulhi(m, x), for
 // every x of the word size the magic m was made for (32 or 64 bits).
@@ -1073,6 +1077,8 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
     }
     C = LmadCopy();
     if (empty) return BMMC_OK;  // nothing is read or written
+    in_elems = std::min<uint64_t>(in_elems, kLmadMaxElems);
+    out_elems = std::min<uint64_t>(out_elems, kLmadMaxElems);
     unsigned __int128 total = 1;
     for (int k = 0; k < ndims; ++k) {
         total *= (unsigned __int128)sizes[k];

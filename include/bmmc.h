@@ -381,7 +381,8 @@ typedef struct {
  * overlap only and may be NULL (taken as aligned, not overlapping).  Errors:
  *   INVALID_ARG       ndims < 0 or > 64, a size < 0, a null sizes / strides
  *                     array with ndims > 0, an offset outside [0, in_elems) /
- *                     [0, out_elems) for some index tuple, a destination LMAD
+ *                     [0, out_elems) for some index tuple (counts above 2^62
+ *                     are taken as 2^62), a destination LMAD
  *                     that is not provably one-to-one (sorted by |stride|,
  *                     each |out_stride| must exceed the span of the faster
  *                     dimensions: every array layout made of permuted, sliced

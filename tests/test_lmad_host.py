@@ -134,6 +134,15 @@ def test_rejections_elem_alias_alignment_and_limits():
                                               out_elems=1 << 41)) == _capi.ERR_INVALID_ARG
     assert _status(lambda: bm.lmad_copy_query([1] * 65, 0, [1] * 65, 0, [1] * 65, 4, in_elems=1,
                                               out_elems=1)) == _capi.ERR_INVALID_ARG
+    # element counts are capped at 2^62: strides whose spans would overflow
+    # int64 in the analysis are rejected whatever count the caller claims
+    huge = (1 << 64) - 1
+    assert _status(lambda: bm.lmad_copy_query((2, 2), 0, (1 << 61, (1 << 61) + 1), 0, (1, 2), 1,
+                                              in_elems=huge, out_elems=4)) == _capi.ERR_INVALID_ARG
+    assert _status(lambda: bm.lmad_copy_query((2, 2), 0, (1 << 60, (1 << 60) + 1), 0, (1, 2), 1,
+                                              in_elems=huge, out_elems=4)) == _capi.OK
+    assert _status(lambda: bm.lmad_copy_query((2, 2), 0, (1, 2), 0, (1 << 61, (1 << 61) + 1), 1,
+                                              in_elems=4, out_elems=huge)) == _capi.ERR_INVALID_ARG
 
 
 def test_copy_without_device_fails_loudly():
