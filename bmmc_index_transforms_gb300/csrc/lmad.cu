@@ -12,12 +12,14 @@
 //   - one contiguous run on both sides: the copy kernel (the page's memcpy);
 //   - power-of-two sizes that permute or reverse a 2^n block on both sides:
 //     one BPC through the tiled BMMC kernel;
-//   - a source unit-stride dimension that differs from the destination's:
-//     a batched tiled transpose through shared memory between two groups of
-//     dimensions (the page's transpose and "map transpose" cases, for any
-//     sizes and any number of batch dimensions), 64 x 64 tiles for 1- to
-//     4-byte words and 32 x 32 for 8 and 16, rows of 4-byte words fetched as
-//     16-byte chunks;
+//   - a source unit-stride dimension that differs from the destination's
+//     (a dimension 0 that is one aligned word of 2 to 16 bytes on both
+//     sides, such as a pixel, taken as the element first): a batched tiled
+//     transpose through shared memory between two groups of dimensions (the
+//     page's transpose and "map transpose" cases, for any sizes and any
+//     number of batch dimensions), tiles of 256 x 32 1-byte words, 128 x 64
+//     2-byte, 64 x 64 4-byte and 32 x 32 8- and 16-byte words, source rows
+//     of 1- to 4-byte words fetched as 16-byte chunks;
 //   - otherwise the page's stride-sorted copy, one element per index tuple,
 //     eight tuples per thread with all loads issued before the stores.
 // Index tuples are unpacked from the flat index with division by invariant
@@ -283,10 +285,15 @@ struct TileSides {
 #ifndef LMAD_TILE_CHUNKS
 #define LMAD_TILE_CHUNKS 1
 #endif
-// Word sizes (a mask of 1, 2, 4, 8) whose chunk path writes 16-byte packs
-// along B when the destination allows it.
+// Word sizes (a mask of 1, 2, 4, 8) whose chunk path writes packs along B
+// when the destination allows it: 16-byte stores of consecutive B rows, or
+// for 1-byte words 8-byte stores of 8 x 4 blocks transposed in registers.
 #ifndef LMAD_TILE_PACK_WORDS
 #define LMAD_TILE_PACK_WORDS (1 | 2)
+#endif
+// Resident blocks per SM asked of the compiler for the 1-byte pack path.
+#ifndef LMAD_BYTE_BLOCKS
+#define LMAD_BYTE_BLOCKS 6
 #endif
 // Word sizes (a mask of 4, 8, 16) whose load phase uses cp.async; the others
 // stage through registers.
@@ -426,7 +433,11 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     constexpr int V = 16 / (int)sizeof(W), LV = clog2(V), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
-    static_assert(NCH + 1 + 3 <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
+    // 1-byte words with packs move 8 x 4 blocks through registers (below)
+    // and rotate rows by two chunks per 8 rows, the others by one
+    constexpr bool BYTES = PACK && sizeof(W) == 1;
+    constexpr int ROT = BYTES ? 2 : 1;
+    static_assert(NCH + 1 + 3 * ROT <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
     // row r holds its segment shifted by its misalignment m, starting at
@@ -441,7 +452,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m == 0 || kk < NCH - 1) {
             const int k = kk + (m != 0);
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ((row >> 3) & 3))),
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & 3))),
                           reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
         }
     }
@@ -453,7 +464,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m != 0) {
             const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
-            W* slot = tile + row * kPitch + V * ((row >> 3) & 3) + e + m;
+            W* slot = tile + row * kPitch + V * ROT * ((row >> 3) & 3) + e + m;
             if constexpr (sizeof(W) >= 4)
                 cp_async_word(slot, src + s0 + e);
             else
@@ -462,7 +473,69 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if constexpr (PACK) {
+    if constexpr (BYTES) {
+        // each thread: B rows ib0..ib0+7 x columns ia0..ia0+3.  Eight 4-byte
+        // shared loads (two and a funnel shift for a row whose bytes are not
+        // 4-byte aligned there), two 4 x 4 byte transposes by byte permutes,
+        // and one 8-byte store per column.  Lanes l & 3 take four
+        // neighbouring 8-row groups (a whole 32-byte destination sector per
+        // column) and l >> 2 eight neighbouring column words, so with the
+        // two-chunk rotation per 8 rows a warp's loads hit 32 distinct
+        // banks; warps take the 32-byte column stripes, then the row groups.
+        constexpr int STRIPES = TA / 32;
+        static_assert(TA % 32 == 0 && (TA / 4) * (TB / 8) == 256, "one 8 x 4 block per thread");
+        const int w = t >> 5, l = t & 31;
+        const int g = (w / STRIPES) * 4 + (l & 3);
+        const int ia0 = (w % STRIPES) * 32 + 4 * (l >> 2), ib0 = 8 * g;
+        if (ib0 >= rb) return;  // no barrier follows inside this function
+        const unsigned char* tb = reinterpret_cast<const unsigned char*>(tile);
+        const int base = ib0 * kPitch + V * ROT * (g & 3) + ia0;
+        int a[8];
+        unsigned low = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            a[k] = base + k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1));
+            low |= (unsigned)a[k];
+        }
+        uint32_t v[8];
+        if ((low & 3) == 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint32_t*>(tb + a[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (a[k] & ~3));
+                v[k] = __funnelshift_r(p[0], p[1], 8 * (a[k] & 3));
+            }
+        }
+        // byte j of v[k] is element (ib0 + k, ia0 + j); col[j][h] gathers
+        // byte j of v[4h..4h+3]
+        uint32_t col[4][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], 0x5140);
+            const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], 0x7362);
+            const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x5140);
+            const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x7362);
+            col[0][h] = __byte_perm(t0, t2, 0x5410);
+            col[1][h] = __byte_perm(t0, t2, 0x7632);
+            col[2][h] = __byte_perm(t1, t3, 0x5410);
+            col[3][h] = __byte_perm(t1, t3, 0x7632);
+        }
+        W* o = dst + ad.dst_b(ib0);
+        if (ib0 + 8 <= rb) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                __stcs(reinterpret_cast<uint2*>(o + ad.dst_a(ia0 + j)), make_uint2(col[j][0], col[j][1]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (ib0 + k < rb) o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k >> 2] >> (8 * (k & 3)));
+        }
+        return;
+    } else if constexpr (PACK) {
         // each item: one column ia and V consecutive B rows, gathered from
         // shared memory and written as one 16-byte store (B has destination
         // stride +1 and the host checked the 16-byte alignment); a thread's
@@ -760,7 +833,7 @@ __global__ void __launch_bounds__(256)
 enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3, kTilePack = 4, kTileHalfRows = 8 };
 
 template <typename W, bool WIDE, int MODE>
-__global__ void __launch_bounds__(256, (MODE & kTilePack) ? 4 : (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
+__global__ void __launch_bounds__(256, (MODE & kTilePack) ? (sizeof(W) == 1 ? LMAD_BYTE_BLOCKS : 4) : (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
@@ -884,13 +957,15 @@ struct LmadCopy {
     int la = 0, lb = 0;
     int narrow = 0;  // 1: group A narrow (lmad_narrow_kernel<.., true>), 2: group B narrow
     int lt = 0;      // narrow kernel: log2 of the tile length along the wide dimension
-    // STRIDED / unaligned MEMCPY: the widened copy
+    // STRIDED / unaligned MEMCPY: the widened copy; TRANSPOSE: dimension 0
+    // (contiguous on both sides) moved as one word of vec elements
     int vec = 1;
     // BPC
     int bpc_n = 0;
     int perm[64];
     uint64_t bpc_c = 0;
-    int64_t bpc_in_block = 0, bpc_out_block = 0;
+    int64_t bpc_in_block = 0, bpc_out_block = 0;  // in elements
+    size_t bpc_word = 0;                          // bytes per BPC element (elem * vec)
 };
 
 bool valid_lmad_elem(size_t e) { return e == 1 || e == 2 || e == 4 || e == 8 || e == 16; }
@@ -947,6 +1022,7 @@ bool try_bpc(LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t out_addr) {
     C.bpc_c = c;
     C.bpc_in_block = C.in_off;
     C.bpc_out_block = out_block;
+    C.bpc_word = elem;
     return true;
 }
 
@@ -962,6 +1038,37 @@ int widen_factor(const LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t ou
         if (ok) return v;
     }
     return 1;
+}
+
+// A BPC of 1- or 2-byte elements moved in words of vec elements: dimension
+// 0 contiguous on both sides widens into words of 4 to 16 bytes (both
+// offsets multiples of vec), and the copy of those words is a BPC.
+bool try_bpc_words(LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t out_addr) {
+    const int v = widen_factor(C, elem, in_addr, out_addr);
+    if ((size_t)v * elem < 4 || C.in_off % v || C.out_off % v) return false;
+    LmadCopy W;
+    W.nd = 0;
+    for (int k = 0; k < C.nd; ++k) {
+        Dim x = C.d[k];
+        if (k == 0) {
+            x.n /= v;
+        } else {
+            x.s /= v;
+            x.t /= v;
+        }
+        if (x.n > 1) W.d[W.nd++] = x;
+    }
+    W.in_off = C.in_off / v;
+    W.out_off = C.out_off / v;
+    if (W.nd == 0 || !try_bpc(W, elem * v, in_addr, out_addr)) return false;
+    C.bpc_n = W.bpc_n;
+    std::copy(W.perm, W.perm + W.bpc_n, C.perm);
+    C.bpc_c = W.bpc_c;
+    C.bpc_in_block = W.bpc_in_block * v;
+    C.bpc_out_block = W.bpc_out_block * v;
+    C.bpc_word = W.bpc_word;
+    C.vec = v;
+    return true;
 }
 
 int ceil_log2(uint64_t v) {
@@ -1063,6 +1170,24 @@ void choose_narrow(LmadCopy& C, size_t elem) {
     C.lt = lt;
 }
 
+// A transpose whose dimension 0 is one word contiguous on both sides
+// (C.vec elements) seen in those words: dimensions 1.. with strides divided
+// by vec, group and tdim indices moved down by one.
+LmadCopy word_view(const LmadCopy& C) {
+    LmadCopy W = C;
+    const int64_t v = C.vec;
+    W.nd = C.nd - 1;
+    for (int k = 0; k < W.nd; ++k) W.d[k] = Dim{C.d[k + 1].n, C.d[k + 1].s / v, C.d[k + 1].t / v};
+    W.in_off = C.in_off / v;
+    W.out_off = C.out_off / v;
+    W.tdim = C.tdim - 1;
+    for (int k = 0; k < C.na; ++k) W.ga[k] = C.ga[k] - 1;
+    for (int k = 0; k < C.nb; ++k) W.gb[k] = C.gb[k] - 1;
+    for (int k = 0; k < C.nc; ++k) W.gc[k] = C.gc[k] - 1;
+    W.vec = 1;
+    return W;
+}
+
 bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
                     size_t in_elems, int64_t out_offset, const int64_t* out_strides, size_t out_elems,
                     size_t elem, uintptr_t in_addr, uintptr_t out_addr, LmadCopy& C) {
@@ -1157,11 +1282,11 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
     C.elements = (uint64_t)total;
     if (nd == 1 && C.d[0].s == 1 && C.d[0].t == 1) {
         C.kind = LMAD_COPY_MEMCPY;
-    } else if (try_bpc(C, elem, in_addr, out_addr)) {
+    } else if (try_bpc(C, elem, in_addr, out_addr) || (elem < 4 && try_bpc_words(C, elem, in_addr, out_addr))) {
         C.kind = LMAD_COPY_BPC;
     } else {
         C.kind = LMAD_COPY_STRIDED;
-        if (C.d[0].s == 1 && iabs(C.d[0].t) != 1)
+        if (C.d[0].s == 1 && iabs(C.d[0].t) != 1) {
             for (int b = 1; b < nd; ++b)
                 if (iabs(C.d[b].t) == 1) {
                     C.kind = LMAD_COPY_TRANSPOSE;
@@ -1170,6 +1295,28 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
                     choose_narrow(C, elem);
                     break;
                 }
+        } else if (C.d[0].s == 1 && C.d[0].t == 1 && nd >= 3) {
+            // dimension 0 contiguous on both sides and one aligned word of 2
+            // to 16 bytes (a pixel, a small vector): a transpose of those
+            // words when they are one in the source and not in the destination
+            const int v = widen_factor(C, elem, in_addr, out_addr);
+            if (v > 1 && v == C.d[0].n && C.d[1].s == v && iabs(C.d[1].t) != v)
+                for (int b = 2; b < nd; ++b)
+                    if (iabs(C.d[b].t) == v) {
+                        C.kind = LMAD_COPY_TRANSPOSE;
+                        C.vec = v;
+                        C.tdim = b;
+                        LmadCopy W = word_view(C);
+                        choose_groups(W, elem * v);
+                        choose_narrow(W, elem * v);
+                        C.na = W.na, C.nb = W.nb, C.nc = W.nc;
+                        for (int k = 0; k < W.na; ++k) C.ga[k] = W.ga[k] + 1;
+                        for (int k = 0; k < W.nb; ++k) C.gb[k] = W.gb[k] + 1;
+                        for (int k = 0; k < W.nc; ++k) C.gc[k] = W.gc[k] + 1;
+                        C.la = W.la, C.lb = W.lb, C.narrow = W.narrow, C.lt = W.lt;
+                        break;
+                    }
+        }
     }
     if (C.kind == LMAD_COPY_STRIDED || C.kind == LMAD_COPY_MEMCPY) C.vec = widen_factor(C, elem, in_addr, out_addr);
     // a contiguous destination filled from contiguous source rows of at
@@ -1519,11 +1666,13 @@ extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_off
     unsigned char* ob = static_cast<unsigned char*>(out);
     cudaError_t e = cudaSuccess;
     if (C.kind == LMAD_COPY_BPC)
-        return bpc_permute(C.bpc_n, C.perm, C.bpc_c, elem_size, ib + C.bpc_in_block * (int64_t)elem_size,
+        return bpc_permute(C.bpc_n, C.perm, C.bpc_c, C.bpc_word, ib + C.bpc_in_block * (int64_t)elem_size,
                            ob + C.bpc_out_block * (int64_t)elem_size, stream);
     if (C.kind == LMAD_COPY_TRANSPOSE) {
-        e = launch_transpose(ib + C.in_off * (int64_t)elem_size, ob + C.out_off * (int64_t)elem_size, elem_size, C,
-                             st);
+        const unsigned char* a = ib + C.in_off * (int64_t)elem_size;
+        unsigned char* o = ob + C.out_off * (int64_t)elem_size;
+        e = C.vec > 1 ? launch_transpose(a, o, elem_size * (size_t)C.vec, word_view(C), st)
+                      : launch_transpose(a, o, elem_size, C, st);
         return e == cudaSuccess ? BMMC_OK : BMMC_ERR_CUDA;
     }
     const unsigned char* a = ib + C.in_off * (int64_t)elem_size;

@@ -321,7 +321,9 @@ typedef enum {
                                 16-byte aligned, by the strided kernel */
     LMAD_COPY_BPC = 2,       /* power-of-two sizes and each side a permuted and/or
                                 reversed block of 2^n elements: one BPC through the
-                                tiled BMMC kernel (as bmmc_lmad_copy) */
+                                tiled BMMC kernel (as bmmc_lmad_copy); 1- and 2-byte
+                                elements when dimension 0 widens into words of 4 to
+                                16 bytes (vec elements), the BPC of those words */
     LMAD_COPY_TRANSPOSE = 3, /* the unit-stride source dimension is not the unit-
                                 stride destination dimension: a batched tiled
                                 transpose through shared memory between group A
@@ -352,13 +354,20 @@ typedef struct {
     int64_t in_strides[LMAD_MAX_DIMS];
     int64_t out_strides[LMAD_MAX_DIMS];
     int64_t in_offset, out_offset;     /* offsets of index tuple 0 after step 1 */
-    int vec;                           /* STRIDED / MEMCPY fallback: elements moved as one
-                                          word of vec * elem_size bytes (1 when not widened) */
+    int vec;                           /* STRIDED / MEMCPY fallback and BPC: elements moved
+                                          as one word of vec * elem_size bytes (1 when not
+                                          widened).
+                                          TRANSPOSE: > 1 when dimension 0 is vec elements
+                                          contiguous on both sides (a pixel, a small vector)
+                                          moved as one word of vec * elem_size bytes; the
+                                          transpose is then between dimensions 1.. in those
+                                          words */
     int transpose_out_dim;             /* TRANSPOSE: the dimension (index into sizes) with
-                                          destination stride +-1; the source one is 0.  -1
-                                          for other kinds */
+                                          destination stride +-1 (+-vec); the source one is 0
+                                          (1 when vec > 1).  -1 for other kinds */
     uint32_t group_a, group_b;         /* TRANSPOSE: bit k set when dimension k is in group A
-                                          (dimension 0 and those continuing it contiguously
+                                          (dimension 0, or 1 when vec > 1, and those
+                                          continuing it contiguously
                                           in the source) / group B (transpose_out_dim and
                                           those continuing it contiguously in the
                                           destination); the others are the batch.  0 for

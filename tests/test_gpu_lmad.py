@@ -237,6 +237,83 @@ def test_multidim_groups_on_whole_chunked_tiles(in_offset):
     _check(w, 4)
 
 
+def _byte_transpose_view(R, C, in_off=0, in_pitch=None, out_off=0, out_pitch=None):
+    """[R][C] bytes (row pitch in_pitch) written transposed, column c at
+    out_off + c * out_pitch."""
+    in_pitch, out_pitch = in_pitch or C, out_pitch or R
+    return dict(sizes=[R, C], in_offset=in_off, in_strides=[in_pitch, 1], in_elems=in_off + (R - 1) * in_pitch + C,
+                out_offset=out_off, out_strides=[1, out_pitch], out_elems=out_off + (C - 1) * out_pitch + R)
+
+
+@pytest.mark.parametrize("case", [
+    dict(R=256, C=512),                                   # whole tiles, aligned rows
+    dict(R=48, C=1000),                                   # short last B tile, ragged A
+    dict(R=64, C=1000, in_off=3),                         # per-row misalignment (pitch = 8 mod 16)
+    dict(R=64, C=1024, in_off=4),                         # one misalignment, 4-byte aligned words
+    dict(R=64, C=1024, in_off=5),                         # one misalignment, funnel shifts
+    dict(R=37, C=600, out_pitch=64),                      # partial 8-row groups
+    dict(R=100, C=777, in_off=1, in_pitch=779, out_pitch=112),
+    dict(R=512, C=128),                                   # 128-byte source rows
+    dict(R=512, C=128, in_off=7),
+    dict(R=300, C=128, in_pitch=131, out_pitch=304),
+    dict(R=64, C=512, out_off=16),
+    dict(R=64, C=512, out_off=8),                         # destination not 16-byte aligned
+])
+def test_byte_transposes_through_registers(case):
+    """1-byte transposes whose destination takes packs (16-byte aligned A
+    strides, B forwards): the tile kernel moves 8 x 4 blocks through
+    registers with byte permutes, with aligned, uniformly and per-row
+    misaligned source rows, 256- and 128-byte rows and partial row groups."""
+    w = _byte_transpose_view(**case)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and not q["narrow"]
+    _check(w, 1)
+    _check(w, 1, seed=5)
+
+
+def test_byte_transposes_through_registers_with_tables():
+    """The same path with offset tables: group A spans two dimensions that
+    do not collapse (a padded destination), and a batch dimension."""
+    w = dict(sizes=[32, 4, 64], in_offset=0, in_strides=[256, 64, 1], in_elems=32 * 256, out_offset=0,
+             out_strides=[1, 2064, 32], out_elems=3 * 2064 + 63 * 32 + 32)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and len(q["group_a"]) == 2 and q["tile"] == (256, 32)
+    _check(w, 1)
+    w = dict(sizes=[3, 64, 272], in_offset=2, in_strides=[64 * 272, 272, 1], in_elems=2 + 3 * 64 * 272, out_offset=0,
+             out_strides=[272 * 64, 1, 64], out_elems=3 * 272 * 64)
+    _check(w, 1)
+
+
+@pytest.mark.parametrize("shape,perm,elem", [
+    ((64, 48, 4), (1, 0, 2), 1), ((37, 53, 4), (1, 0, 2), 1), ((33, 65, 2), (1, 0, 2), 1),
+    ((300, 129, 16), (1, 0, 2), 1), ((100, 30, 8), (1, 0, 2), 2), ((7, 33, 65, 2), (0, 2, 1, 3), 4),
+    ((50, 60, 2), (1, 0, 2), 8), ((2, 100, 3, 4), (0, 2, 1, 3), 1), ((3, 70, 130, 4), (2, 0, 1, 3), 2),
+    ((64, 64, 4), (1, 0, 2), 1), ((256, 256, 2), (1, 0, 2), 2), ((8, 16, 32, 8), (2, 0, 1, 3), 2),
+    ((16, 32, 16), (1, 0, 2), 1), ((4, 8, 2, 4), (1, 0, 2, 3), 1),
+])
+@pytest.mark.parametrize("in_offset", [0, 1, 16])
+def test_permutations_of_small_inner_words(shape, perm, elem, in_offset):
+    """x.permute(perm) with the last (contiguous) dimension kept: the copy
+    of 2- to 16-byte words (a word transpose, or the BPC of the words for
+    power-of-two sizes), and the element-wise kinds when the view starts
+    inside a word."""
+    src_strides = synth.row_major_strides(shape)
+    out_rm = synth.row_major_strides([shape[p] for p in perm])
+    out_strides = [0] * len(shape)
+    for pos, p in enumerate(perm):
+        out_strides[p] = out_rm[pos]
+    total = int(np.prod(shape))
+    w = dict(sizes=list(shape), in_offset=in_offset, in_strides=src_strides, in_elems=total + in_offset,
+             out_offset=0, out_strides=out_strides, out_elems=total)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    if in_offset % shape[-1] == 0:  # (words may span more than the last dimension)
+        assert q["vec"] % shape[-1] == 0 and q["kind"] in ("transpose", "bpc")
+    _check(w, elem)
+
+
 def test_pinned_host_buffers():
     """Source and destination in pinned host memory: the kernels read and
     write host memory directly (the slice case and a transpose)."""

@@ -85,6 +85,74 @@ def test_kinds_and_widening():
     assert q["kind"] == "memcpy" and q["dims"] == [[1, 1, 1]] and q["in_offset"] == 3
 
 
+def _perm_view(shape, perm, in_offset=0):
+    """x.permute(perm) made contiguous, x row-major."""
+    src = synth.row_major_strides(shape)
+    out_rm = synth.row_major_strides([shape[p] for p in perm])
+    out = [0] * len(shape)
+    for pos, p in enumerate(perm):
+        out[p] = out_rm[pos]
+    total = 1
+    for v in shape:
+        total *= v
+    return dict(sizes=list(shape), in_offset=in_offset, in_strides=src, in_elems=total + in_offset, out_offset=0,
+                out_strides=out, out_elems=total)
+
+
+@pytest.mark.parametrize("shape,perm,elem", [
+    ((64, 48, 4), (1, 0, 2), 1),            # RGBA image transpose: 4-byte pixels
+    ((4000, 4096, 16), (1, 0, 2), 1),       # 16-byte vectors
+    ((256, 256, 2), (1, 0, 2), 1),          # 2-byte words: no BPC below 4 bytes
+    ((100, 30, 8), (1, 0, 2), 2),
+    ((7, 33, 65, 2), (0, 2, 1, 3), 4),      # batched, 8-byte pairs
+    ((50, 60, 2), (1, 0, 2), 8),
+    ((2, 100, 3, 4), (0, 2, 1, 3), 1),      # NHWC -> NCHW of 4-byte words, 3 channels
+])
+def test_small_inner_words_make_transposes(shape, perm, elem):
+    """A dimension 0 that is one aligned word of 2 to 16 bytes on both sides
+    is moved as that word, and the copy is a transpose between the other
+    dimensions in words: the same groups (one dimension up), tile and narrow
+    choice as the copy of those words as elements."""
+    vec = shape[-1]
+    q = _query(_perm_view(shape, perm), elem)
+    assert q["kind"] == "transpose" and q["vec"] == vec and q["dims"][0] == [vec, 1, 1]
+    assert q["group_a"][0] == 1 and q["dims"][1][1] == vec
+    assert abs(q["dims"][q["transpose_out_dim"]][2]) == vec
+    words = _query(_perm_view(shape[:-1], perm[:-1]), elem * vec)
+    assert words["kind"] == "transpose" and words["vec"] == 1
+    assert [[n, s * vec, t * vec] for n, s, t in words["dims"]] == q["dims"][1:]
+    assert [k + 1 for k in words["group_a"]] == q["group_a"] and [k + 1 for k in words["group_b"]] == q["group_b"]
+    assert words["transpose_out_dim"] + 1 == q["transpose_out_dim"]
+    assert words["tile"] == q["tile"] and words["narrow"] == q["narrow"]
+
+
+@pytest.mark.parametrize("shape,perm,elem,vec", [
+    ((4096, 4096, 16), (1, 0, 2), 1, 16),
+    ((64, 64, 4), (1, 0, 2), 1, 4),
+    ((256, 256, 2), (1, 0, 2), 2, 2),
+    ((8, 16, 32, 8), (2, 0, 1, 3), 2, 8),
+])
+def test_small_elements_take_the_bpc_route_in_words(shape, perm, elem, vec):
+    """Power-of-two permutations of 1- and 2-byte elements whose dimension 0
+    widens into words of 4 to 16 bytes run as the BPC of those words, which
+    is itself a BPC as elements."""
+    q = _query(_perm_view(shape, perm), elem)
+    assert q["kind"] == "bpc" and q["vec"] == vec
+    words = _query(_perm_view(shape[:-1], perm[:-1]), elem * vec)
+    assert words["kind"] == "bpc" and words["vec"] == 1
+    # not when the words are under 4 bytes or the view starts inside a word
+    assert _query(_perm_view(shape[:-1] + (2,), perm), 1)["kind"] != "bpc"
+    assert _query(_perm_view(shape, perm, in_offset=1), elem)["kind"] != "bpc"
+
+
+def test_inner_words_that_do_not_widen_stay_strided():
+    # 3-byte pixels, a misaligned source, and a 32-byte inner block (two words)
+    assert _query(_perm_view((64, 48, 3), (1, 0, 2)), 1)["kind"] == "strided"
+    assert _query(_perm_view((64, 48, 4), (1, 0, 2), in_offset=1), 1)["kind"] == "strided"
+    q = _query(_perm_view((64, 48, 32), (1, 0, 2)), 1)
+    assert q["kind"] == "strided" and q["vec"] == 16
+
+
 def _status(fn):
     try:
         fn()
@@ -182,7 +250,7 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert not set(a) & set(b)
 
 
-def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16):
+def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False):
     """The chunk path of the tile kernel, replayed on the host for 1- to
     8-byte words: rows of 256 bytes (TA = 16 * V elements, V = 16 / word per
     chunk) fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
@@ -193,15 +261,21 @@ def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16):
     column-wise at row offset + column; rows rb.. of a tile short along B are
     skipped.  Every element is placed exactly once, every 16-byte fetch and
     every 16-byte shared store is aligned, and every read returns the element
-    the transpose needs."""
+    the transpose needs.  byte_pack: the 1-byte store path instead (rows
+    rotated by two chunks per 8 rows; each thread reads 8 rows x 4 columns
+    as 4-byte words, two and a funnel shift where a row's bytes are not
+    4-byte aligned, and writes one 8-byte store per column); it covers the
+    tile once, stays inside the shared array, and a warp's loads of rows that
+    share one misalignment hit 32 distinct banks."""
     V = 16 // word
     TA = nch * V
     TB = {1: 8192, 2: 8192, 4: 4096, 8: 1024}[word] // TA
     pitch = {16: 25, 8: 17}[nch] * V
+    rot = 2 if byte_pack else 1
     tile = {}
 
     def base_of(row):
-        return row * pitch + ((row >> 3) & 3) * V
+        return row * pitch + ((row >> 3) & 3) * V * rot
 
     for t in range(256):
         for r in range(TB * nch // 256):
@@ -228,6 +302,35 @@ def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16):
                 assert a not in tile
                 tile[a] = (row, e)
     assert len(tile) == TA * min(rb, TB) and max(tile) < TB * pitch
+    if byte_pack:
+        assert word == 1
+        stripes = TA // 32
+        covered = set()
+        words = {}
+        for t in range(256):
+            w, lane = t >> 5, t & 31
+            g = (w // stripes) * 4 + (lane & 3)
+            ia0, ib0 = (w % stripes) * 32 + 4 * (lane >> 2), 8 * g
+            assert 0 <= ia0 < TA and ib0 < TB
+            if ib0 >= rb:
+                continue
+            base = ib0 * pitch + V * rot * (g & 3) + ia0
+            for k in range(8):
+                row = ib0 + k
+                a = base + k * pitch + (base_mis + row * sb) % V
+                assert a == base_of(row) + (base_mis + row * sb) % V + ia0
+                assert (a & ~3) + 8 <= TB * pitch  # the funnel shift's second word
+                words.setdefault((w, k), []).append(a >> 2)
+                if row < rb:
+                    for j in range(4):
+                        assert tile[a + j] == (row, ia0 + j)
+                        assert (ia0 + j, row) not in covered
+                        covered.add((ia0 + j, row))
+        assert len(covered) == TA * min(rb, TB)
+        if sb % V == 0 and base_mis % 4 == 0:
+            for ws in words.values():
+                assert len({x % 32 for x in ws}) == len(set(ws))
+        return
     step = 256 // TB
     for t in range(256):
         ib, ia0 = t % TB, t // TB
@@ -245,6 +348,8 @@ def test_chunked_tile_mapping(word, sb):
         for base_mis in range(16 // word):
             for rb in (128, 100, 64, 62, 32, 31, 17, 1):
                 _chunk_tile_emulation(word, base_mis, sb, rb, nch)
+                if word == 1:
+                    _chunk_tile_emulation(word, base_mis, sb, rb, nch, byte_pack=True)
 
 
 def test_rows_kind_for_small_elements():
