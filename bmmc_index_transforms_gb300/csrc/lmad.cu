@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <type_traits>
@@ -295,6 +296,10 @@ struct TileSides {
 #ifndef LMAD_BYTE_BLOCKS
 #define LMAD_BYTE_BLOCKS 6
 #endif
+// 1-byte pack tiles of 256 x 128 (four times the rows) when B is long.
+#ifndef LMAD_BYTE_TALL
+#define LMAD_BYTE_TALL 1
+#endif
 // Word sizes (a mask of 4, 8, 16) whose load phase uses cp.async; the others
 // stage through registers.
 #ifndef LMAD_TILE_ASYNC_WORDS
@@ -323,10 +328,14 @@ template <typename O>
 struct TabAddr {
     const O *ts, *td;
     int TA;
+    int b0;  // first B entry of the (part of the) tile
     __device__ __forceinline__ O src_a(int ia) const { return ts[ia]; }
-    __device__ __forceinline__ O src_b(int ib) const { return ts[TA + ib]; }
+    __device__ __forceinline__ O src_b(int ib) const { return ts[TA + b0 + ib]; }
     __device__ __forceinline__ O dst_a(int ia) const { return td[ia]; }
-    __device__ __forceinline__ O dst_b(int ib) const { return td[TA + ib]; }
+    __device__ __forceinline__ O dst_b(int ib) const { return td[TA + b0 + ib]; }
+    // every B row starts at the same offset modulo V elements
+    template <int V>
+    __device__ __forceinline__ bool same_mis() const { return false; }
 };
 template <typename O>
 struct LinAddr {
@@ -335,6 +344,8 @@ struct LinAddr {
     __device__ __forceinline__ O src_b(int ib) const { return (O)ib * sb; }
     __device__ __forceinline__ O dst_a(int ia) const { return (O)ia * ta; }
     __device__ __forceinline__ O dst_b(int ib) const { return (O)ib * tb; }
+    template <int V>
+    __device__ __forceinline__ bool same_mis() const { return ((unsigned)sb & (V - 1)) == 0; }
 };
 
 // The two phases of one tile.  Both tile sides are at most 256, so
@@ -426,113 +437,149 @@ constexpr int clog2(int v) { return v <= 1 ? 0 : 1 + clog2(v / 2); }
 // (a misaligned row) rotated by up to 3, and 1 mod 8 so that neighbouring
 // rows start 4 banks apart.
 constexpr int chunk_pitch(int nch) { return ((nch + 4 + 6) / 8) * 8 + 1; }
+// Bytes of dynamic shared memory a tall tile kernel takes: 128 rows of
+// chunk_pitch(16) chunks.
+constexpr int kTallTileBytes = 128 * chunk_pitch(16) * 16;
 
-template <typename W, typename O, bool PACK, int NCH, typename Addr>
+template <typename W, typename O, bool PACK, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
                                                     const Addr& ad, int rb) {
     constexpr int V = 16 / (int)sizeof(W), LV = clog2(V), LNCH = clog2(NCH);
-    constexpr int TA = NCH * V, TB = (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
+    constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
     // 1-byte words with packs move 8 x 4 blocks through registers (below)
     // and rotate rows by two chunks per 8 rows, the others by one
     constexpr bool BYTES = PACK && sizeof(W) == 1;
     constexpr int ROT = BYTES ? 2 : 1;
     static_assert(NCH + 1 + 3 * ROT <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
+    static_assert(TALL == 1 || BYTES, "tall tiles on the 1-byte pack path only");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
+    // every row shares the origin's misalignment (B's source stride a
+    // multiple of V): no per-row arithmetic for it
+    const bool uni = ad.template same_mis<V>();
     // row r holds its segment shifted by its misalignment m, starting at
-    // chunk r / 8 of its pitch: element (r, c = column + m) at
-    // r * kPitch + (r / 8) * V + c, whole chunks at 16-byte boundaries
+    // chunk ROT * ((r / 8) mod 4) of its pitch: element (r, c = column + m)
+    // at r * kPitch + ROT * ((r / 8) mod 4) * V + c, whole chunks at 16-byte
+    // boundaries
 #pragma unroll
     for (int r = 0; r < TB * NCH / 256; ++r) {
         const int idx = t + 256 * r;
         const int row = idx >> LNCH, kk = idx & (NCH - 1);
         if (row >= rb) break;  // rows grow with r
         const O s0 = ad.src_b(row);
-        const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
+        const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m == 0 || kk < NCH - 1) {
             const int k = kk + (m != 0);
             cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & 3))),
                           reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
         }
     }
+    if (!uni || base_mis != 0) {
 #pragma unroll
-    for (int u = t; u < TB * V; u += 256) {
-        const int row = u >> LV, j = u & (V - 1);
-        if (row >= rb) break;  // rows grow with u
-        const O s0 = ad.src_b(row);
-        const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
-        if (m != 0) {
-            const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
-            W* slot = tile + row * kPitch + V * ROT * ((row >> 3) & 3) + e + m;
-            if constexpr (sizeof(W) >= 4)
-                cp_async_word(slot, src + s0 + e);
-            else
-                *slot = __ldg(src + s0 + e);
+        for (int u = t; u < TB * V; u += 256) {
+            const int row = u >> LV, j = u & (V - 1);
+            if (row >= rb) break;  // rows grow with u
+            const O s0 = ad.src_b(row);
+            const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
+            if (m != 0) {
+                const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
+                W* slot = tile + row * kPitch + V * ROT * ((row >> 3) & 3) + e + m;
+                if constexpr (sizeof(W) >= 4)
+                    cp_async_word(slot, src + s0 + e);
+                else
+                    *slot = __ldg(src + s0 + e);
+            }
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if constexpr (BYTES) {
-        // each thread: B rows ib0..ib0+7 x columns ia0..ia0+3.  Eight 4-byte
+        // each item: B rows ib0..ib0+7 x columns ia0..ia0+3.  Eight 4-byte
         // shared loads (two and a funnel shift for a row whose bytes are not
         // 4-byte aligned there), two 4 x 4 byte transposes by byte permutes,
         // and one 8-byte store per column.  Lanes l & 3 take four
         // neighbouring 8-row groups (a whole 32-byte destination sector per
         // column) and l >> 2 eight neighbouring column words, so with the
         // two-chunk rotation per 8 rows a warp's loads hit 32 distinct
-        // banks; warps take the 32-byte column stripes, then the row groups.
-        constexpr int STRIPES = TA / 32;
-        static_assert(TA % 32 == 0 && (TA / 4) * (TB / 8) == 256, "one 8 x 4 block per thread");
+        // banks; warps take the 32-byte column stripes, then the quads of
+        // row groups, and a thread's ITEMS items are QS quads apart (same
+        // columns, so the same destination column offsets).
+        constexpr int STRIPES = TA / 32, QS = 8 / STRIPES, ITEMS = (TA / 4) * (TB / 8) / 256;
+        static_assert(TA % 32 == 0 && ITEMS >= 1 && (TA / 4) * (TB / 8) == 256 * ITEMS, "whole 8 x 4 blocks");
         const int w = t >> 5, l = t & 31;
-        const int g = (w / STRIPES) * 4 + (l & 3);
-        const int ia0 = (w % STRIPES) * 32 + 4 * (l >> 2), ib0 = 8 * g;
-        if (ib0 >= rb) return;  // no barrier follows inside this function
+        const int ia0 = (w % STRIPES) * 32 + 4 * (l >> 2);
         const unsigned char* tb = reinterpret_cast<const unsigned char*>(tile);
-        const int base = ib0 * kPitch + V * ROT * (g & 3) + ia0;
-        int a[8];
-        unsigned low = 0;
+        O da[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            a[k] = base + k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1));
-            low |= (unsigned)a[k];
-        }
-        uint32_t v[8];
-        if ((low & 3) == 0) {
+        for (int j = 0; j < 4; ++j) da[j] = ad.dst_a(ia0 + j);
+        const int lead = V * ROT * (l & 3) + ia0;  // rotation of every item's rows: ((32 q + 8 (l & 3)) / 8) mod 4
+        auto item = [&](const int ib0, auto same) {
+            const int base = ib0 * kPitch + lead;
+            uint32_t v[8];
+            if constexpr (decltype(same)::value) {
+                const int b = base + (int)base_mis;
+                const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (b & ~3));
+                if ((base_mis & 3) == 0) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint32_t*>(tb + a[k]);
-        } else {
+                    for (int k = 0; k < 8; ++k) v[k] = p[k * (kPitch / 4)];
+                } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (a[k] & ~3));
-                v[k] = __funnelshift_r(p[0], p[1], 8 * (a[k] & 3));
+                    for (int k = 0; k < 8; ++k) v[k] = __funnelshift_r(p[k * (kPitch / 4)], p[k * (kPitch / 4) + 1], 8 * (b & 3));
+                }
+            } else {
+                int a[8];
+                unsigned low = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    a[k] = base + k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1));
+                    low |= (unsigned)a[k];
+                }
+                if ((low & 3) == 0) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint32_t*>(tb + a[k]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (a[k] & ~3));
+                        v[k] = __funnelshift_r(p[0], p[1], 8 * (a[k] & 3));
+                    }
+                }
             }
-        }
-        // byte j of v[k] is element (ib0 + k, ia0 + j); col[j][h] gathers
-        // byte j of v[4h..4h+3]
-        uint32_t col[4][2];
+            // byte j of v[k] is element (ib0 + k, ia0 + j); col[j][h] gathers
+            // byte j of v[4h..4h+3]
+            uint32_t col[4][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], 0x5140);
-            const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], 0x7362);
-            const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x5140);
-            const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x7362);
-            col[0][h] = __byte_perm(t0, t2, 0x5410);
-            col[1][h] = __byte_perm(t0, t2, 0x7632);
-            col[2][h] = __byte_perm(t1, t3, 0x5410);
-            col[3][h] = __byte_perm(t1, t3, 0x7632);
-        }
-        W* o = dst + ad.dst_b(ib0);
-        if (ib0 + 8 <= rb) {
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], 0x5140);
+                const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], 0x7362);
+                const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x5140);
+                const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x7362);
+                col[0][h] = __byte_perm(t0, t2, 0x5410);
+                col[1][h] = __byte_perm(t0, t2, 0x7632);
+                col[2][h] = __byte_perm(t1, t3, 0x5410);
+                col[3][h] = __byte_perm(t1, t3, 0x7632);
+            }
+            W* o = dst + ad.dst_b(ib0);
+            if (ib0 + 8 <= rb) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                __stcs(reinterpret_cast<uint2*>(o + ad.dst_a(ia0 + j)), make_uint2(col[j][0], col[j][1]));
-        } else {
+                for (int j = 0; j < 4; ++j) __stcs(reinterpret_cast<uint2*>(o + da[j]), make_uint2(col[j][0], col[j][1]));
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (ib0 + k < rb) o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k >> 2] >> (8 * (k & 3)));
+                    for (int k = 0; k < 8; ++k)
+                        if (ib0 + k < rb) o[da[j] + k] = (W)(col[j][k >> 2] >> (8 * (k & 3)));
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+            const int ib0 = 32 * (w / STRIPES + QS * i) + 8 * (l & 3);
+            if (ib0 >= rb) break;  // rows grow with i; no barrier follows inside this function
+            if (uni)
+                item(ib0, std::true_type{});
+            else
+                item(ib0, std::false_type{});
         }
         return;
     } else if constexpr (PACK) {
@@ -829,24 +876,51 @@ __global__ void __launch_bounds__(256)
 // MODE: bit 0 = multi-dimension groups (offset tables, else linear
 // offsets), bit 1 = tiles with the default shape whose A side is whole take
 // the 16-byte chunk path, bit 2 = that path writes 16-byte packs along B,
-// bit 3 = the chunk path with 128-byte source rows (8 chunks) instead of 256.
-enum { kTileLinear = 0, kTileTables = 1, kTileChunked = 2, kTileTablesChunked = 3, kTilePack = 4, kTileHalfRows = 8 };
+// bit 3 = the chunk path with 128-byte source rows (8 chunks) instead of 256,
+// bit 4 = tall tiles (1-byte pack path, 256-byte rows): four times the rows,
+// 256 x 128, with ragged-A tiles taken by the element path a quarter at a
+// time.
+enum {
+    kTileLinear = 0,
+    kTileTables = 1,
+    kTileChunked = 2,
+    kTileTablesChunked = 3,
+    kTilePack = 4,
+    kTileHalfRows = 8,
+    kTileTall = 16
+};
+
+template <typename W, int MODE>
+constexpr int tile_min_blocks() {
+    return (MODE & kTileTall)   ? 4
+           : (MODE & kTilePack) ? (sizeof(W) == 1 ? LMAD_BYTE_BLOCKS : 4)
+           : (MODE & kTileChunked) ? 6
+                                   : (sizeof(W) == 4 ? 8 : 6);
+}
 
 template <typename W, bool WIDE, int MODE>
-__global__ void __launch_bounds__(256, (MODE & kTilePack) ? (sizeof(W) == 1 ? LMAD_BYTE_BLOCKS : 4) : (MODE & kTileChunked) ? 6 : (sizeof(W) == 4 ? 8 : 6))
+__global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     using S = TileShape<sizeof(W)>;
     using Sides = TileSides<S::T>;
-    constexpr int kTab = Sides::kMax + Sides::kMin;  // >= TA + TB
+    constexpr int TALL = (MODE & kTileTall) ? 4 : 1;
+    constexpr int kTab = Sides::kMax + Sides::kMin * TALL;  // >= TA + TB
     constexpr int kElemTile = S::T + Sides::kMax * S::PAD;
     constexpr int NCH = (MODE & kTileHalfRows) ? 8 : 16;  // chunk path: chunks per source row
-    // chunk path: T / TA rows of chunk_pitch(NCH) chunks of 16 / W elements
-    constexpr int kChunkTile = sizeof(W) <= 8 ? (S::T / (NCH * (16 / (int)sizeof(W)))) * chunk_pitch(NCH) *
+    // chunk path: TALL * T / TA rows of chunk_pitch(NCH) chunks of 16 / W elements
+    constexpr int kChunkTile = sizeof(W) <= 8 ? TALL * (S::T / (NCH * (16 / (int)sizeof(W)))) * chunk_pitch(NCH) *
                                                     (16 / (int)sizeof(W))
                                               : 0;
-    __shared__ __align__(16) W tile[kElemTile > kChunkTile ? kElemTile : kChunkTile];  // 16-byte cp.async targets
+    // 16-byte cp.async targets; tall tiles (over 48 KiB) in dynamic shared
+    // memory, the launcher having raised the kernel's limit
+    constexpr bool DYN = TALL > 1;
+    __shared__ __align__(16) W tile_s[DYN ? 1 : (kElemTile > kChunkTile ? kElemTile : kChunkTile)];
+    extern __shared__ __align__(16) unsigned char lmad_dyn_smem[];
+    W* const tile = DYN ? reinterpret_cast<W*>(lmad_dyn_smem) : tile_s;
+    static_assert(!DYN || (sizeof(W) == 1 && kChunkTile == kTallTileBytes && kElemTile <= kChunkTile),
+                  "the launcher's dynamic shared memory holds the tall tile");
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
     constexpr bool PACK = (MODE & kTilePack) != 0;
@@ -912,9 +986,18 @@ __global__ void __launch_bounds__(256, (MODE & kTilePack) ? (sizeof(W) == 1 ? LM
             __syncthreads();
         }
         if constexpr (GENERAL) {
-            const TabAddr<O> ad{tab_src, tab_dst, TA};
+            const TabAddr<O> ad{tab_src, tab_dst, TA, 0};
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH>(in + so + tab_src[0], out + d, tile, ad, rb);
+                if constexpr (CHUNKED)
+                    tile_phases_chunked<W, O, PACK, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb);
+            } else if constexpr (TALL > 1) {
+                // a ragged-A tall tile: the element path, a quarter of the rows at a time
+                constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
+                for (int j = 0; j * QB < rb; ++j) {
+                    if (j) __syncthreads();
+                    const TabAddr<O> aq{tab_src, tab_dst, TA, j * QB};
+                    tile_phases<W, false>(in + so, out + d, tile, aq, TA, QB, p.la, p.lb - 2, ra, min(QB, rb - j * QB));
+                }
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -925,7 +1008,14 @@ __global__ void __launch_bounds__(256, (MODE & kTilePack) ? (sizeof(W) == 1 ? LM
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH>(src, dst, tile, ad, rb);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH, TALL>(src, dst, tile, ad, rb);
+            } else if constexpr (TALL > 1) {
+                constexpr int QB = S::T >> 8;
+                for (int j = 0; j * QB < rb; ++j) {
+                    if (j) __syncthreads();
+                    tile_phases<W, false>(src + (O)(j * QB) * ad.sb, dst + (O)(j * QB) * ad.tb, tile, ad, TA, QB, p.la,
+                                          p.lb - 2, ra, min(QB, rb - j * QB));
+                }
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
             } else {
@@ -1466,6 +1556,22 @@ cudaError_t launch_narrow_w(const W* in, W* out, const LmadCopy& C, cudaStream_t
     return cudaGetLastError();
 }
 
+// Raise the dynamic shared memory limit of one tall tile kernel, once per
+// device.
+template <typename W, bool WIDE, int MODE>
+cudaError_t allow_tall_tile() {
+    static std::atomic<uint64_t> done{0};  // one bit per device ordinal (mod 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(lmad_tile_kernel<W, WIDE, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTallTileBytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 template <typename W>
 cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStream_t stream) {
     if (C.narrow) return launch_narrow_w(in, out, C, stream);
@@ -1473,15 +1579,32 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     for (int k = 0; k < C.na; ++k) n_a *= (uint64_t)C.d[C.ga[k]].n;
     for (int k = 0; k < C.nb; ++k) n_b *= (uint64_t)C.d[C.gb[k]].n;
     for (int k = 0; k < C.nc; ++k) batch *= (uint64_t)C.d[C.gc[k]].n;
-    const uint64_t tiles_a = (n_a + (1ull << C.la) - 1) >> C.la, tiles_b = (n_b + (1ull << C.lb) - 1) >> C.lb;
+    // the chunk path: source rows of 256 bytes (the default shapes) or 128
+    // bytes (a group A of up to half that), 1- to 4-byte words (8-byte words
+    // measured slower on it: 32 x 32 tiles, 83-85% of a copy against 85-90%
+    // element-wise; LMAD_TILE_CHUNKS=2 enables them)
+    const uint64_t row_bytes = (1ull << C.la) * sizeof(W);
+    const bool chunked = (LMAD_TILE_CHUNKS && (sizeof(W) <= 4 || LMAD_TILE_CHUNKS == 2) && sizeof(W) <= 8 &&
+                          (row_bytes == 256 || row_bytes == 128) && (1ull << C.lb) <= 256);
+    // packs along B: B walks the destination forwards from stride +1, and
+    // every A and batch destination stride and the origin are 16-byte
+    // aligned
+    bool pack = chunked && (LMAD_TILE_PACK_WORDS & sizeof(W)) != 0 && ((uintptr_t)out & 15) == 0;
+    for (int k = 0; pack && k < C.nb; ++k) pack = C.d[C.gb[k]].t > 0;
+    for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * sizeof(W)) % 16 == 0;
+    for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
+    // tall tiles (256 x 128) for 1-byte packs with 256-byte rows and a long B
+    const bool tall = LMAD_BYTE_TALL && sizeof(W) == 1 && pack && row_bytes == 256 && C.lb == 5 && n_b >= 256;
+    const int la = C.la, lb = C.lb + (tall ? 2 : 0);
+    const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + (1ull << lb) - 1) >> lb;
     const uint64_t tiles = tiles_a * tiles_b * batch;
     // masked lanes of a ragged tile form (unused) offsets up to one tile side
     // past the span; 32-bit offsets must hold those too
-    uint64_t slack_in = 1ull << C.la, slack_out = 0;
-    for (int k = 0; k < C.na; ++k) slack_out += (1ull << C.la) * iabs(C.d[C.ga[k]].t);
+    uint64_t slack_in = 1ull << la, slack_out = 0;
+    for (int k = 0; k < C.na; ++k) slack_out += (1ull << la) * iabs(C.d[C.ga[k]].t);
     for (int k = 0; k < C.nb; ++k) {
-        slack_in += (1ull << C.lb) * iabs(C.d[C.gb[k]].s);
-        slack_out += (1ull << C.lb) * iabs(C.d[C.gb[k]].t);
+        slack_in += (1ull << lb) * iabs(C.d[C.gb[k]].s);
+        slack_out += (1ull << lb) * iabs(C.d[C.gb[k]].t);
     }
     const bool wide = tiles > 0xFFFFFFFFull || n_a > 0xFFFFFFFFull || n_b > 0xFFFFFFFFull ||
                       span_of(C.d, C.nd, false) + slack_in > 0x7FFFFFFFull ||
@@ -1491,8 +1614,8 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     p.tiles = tiles;
     p.n_a = n_a;
     p.n_b = n_b;
-    p.la = C.la;
-    p.lb = C.lb;
+    p.la = la;
+    p.lb = lb;
     p.div_ta = make_div(tiles_a, bits);
     p.div_tb = make_div(tiles_b, bits);
     p.na = C.na;
@@ -1517,28 +1640,33 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
-    // 8-byte words measured slower on the chunk path (32 x 32 tiles: 83-85%
-    // of a copy against 85-90% element-wise), so it is taken for 4-byte
-    // words only; LMAD_TILE_CHUNKS=2 enables it for 8-byte words too
-    // the chunk path: source rows of 256 bytes (the default shapes) or 128
-    // bytes (a group A of up to half that), 1- to 4-byte words (8-byte words
-    // measured slower on it; LMAD_TILE_CHUNKS=2 enables them)
-    const uint64_t row_bytes = (1ull << C.la) * sizeof(W);
-    const bool chunked = (LMAD_TILE_CHUNKS && (sizeof(W) <= 4 || LMAD_TILE_CHUNKS == 2) && sizeof(W) <= 8 &&
-                          (row_bytes == 256 || row_bytes == 128) && (1ull << C.lb) <= 256);
-    // 16-byte packs along B: B walks the destination forwards from stride
-    // +1, and every A and batch destination stride and the origin are
-    // 16-byte aligned
-    bool pack = chunked && (LMAD_TILE_PACK_WORDS & sizeof(W)) != 0 && ((uintptr_t)out & 15) == 0;
-    for (int k = 0; pack && k < C.nb; ++k) pack = C.d[C.gb[k]].t > 0;
-    for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * sizeof(W)) % 16 == 0;
-    for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
     const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
-                     (pack ? kTilePack : 0) | (chunked && row_bytes == 128 ? kTileHalfRows : 0);
+                     (pack ? kTilePack : 0) | (chunked && row_bytes == 128 ? kTileHalfRows : 0) |
+                     (tall ? kTileTall : 0);
+    constexpr int kWide = 32;
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
+    if constexpr (sizeof(W) == 1) {
+        if (mode & kTileTall) {
+#define LMAD_TALL(WV, MV)                                                                              \
+    do {                                                                                               \
+        const cudaError_t ea = allow_tall_tile<W, WV, MV>();                                           \
+        if (ea != cudaSuccess) return ea;                                                              \
+        lmad_tile_kernel<W, WV, MV><<<grid, 256, kTallTileBytes, stream>>>(in, out, p);                \
+    } while (0)
+            switch (mode | (wide ? kWide : 0)) {
+                case 22: LMAD_TALL(false, 22); break;
+                case 23: LMAD_TALL(false, 23); break;
+                case 54: LMAD_TALL(true, 22); break;
+                case 55: LMAD_TALL(true, 23); break;
+                default: return cudaErrorInvalidValue;
+            }
+#undef LMAD_TALL
+            return cudaGetLastError();
+        }
+    }
     if constexpr (sizeof(W) <= 8) {
         if (mode & kTileChunked) {
-            switch (mode | (wide ? 16 : 0)) {
+            switch (mode | (wide ? kWide : 0)) {
                 case 2: LMAD_TILE(false, 2); break;
                 case 6: LMAD_TILE(false, 6); break;
                 case 3: LMAD_TILE(false, 3); break;
@@ -1547,14 +1675,14 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                 case 14: LMAD_TILE(false, 14); break;
                 case 11: LMAD_TILE(false, 11); break;
                 case 15: LMAD_TILE(false, 15); break;
-                case 18: LMAD_TILE(true, 2); break;
-                case 22: LMAD_TILE(true, 6); break;
-                case 19: LMAD_TILE(true, 3); break;
-                case 23: LMAD_TILE(true, 7); break;
-                case 26: LMAD_TILE(true, 10); break;
-                case 30: LMAD_TILE(true, 14); break;
-                case 27: LMAD_TILE(true, 11); break;
-                case 31: LMAD_TILE(true, 15); break;
+                case 34: LMAD_TILE(true, 2); break;
+                case 38: LMAD_TILE(true, 6); break;
+                case 35: LMAD_TILE(true, 3); break;
+                case 39: LMAD_TILE(true, 7); break;
+                case 42: LMAD_TILE(true, 10); break;
+                case 46: LMAD_TILE(true, 14); break;
+                case 43: LMAD_TILE(true, 11); break;
+                case 47: LMAD_TILE(true, 15); break;
                 default: return cudaErrorInvalidValue;
             }
             return cudaGetLastError();

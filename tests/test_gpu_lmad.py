@@ -258,6 +258,10 @@ def _byte_transpose_view(R, C, in_off=0, in_pitch=None, out_off=0, out_pitch=Non
     dict(R=300, C=128, in_pitch=131, out_pitch=304),
     dict(R=64, C=512, out_off=16),
     dict(R=64, C=512, out_off=8),                         # destination not 16-byte aligned
+    dict(R=384, C=1000),                                  # 256 x 128 tiles, ragged A by quarters
+    dict(R=400, C=1000, out_pitch=416),                   # a 16-row last tile
+    dict(R=1000, C=777, in_off=1, in_pitch=779, out_pitch=1008),
+    dict(R=520, C=512, in_off=4), dict(R=520, C=512, in_off=5),
 ])
 def test_byte_transposes_through_registers(case):
     """1-byte transposes whose destination takes packs (16-byte aligned A
@@ -284,6 +288,14 @@ def test_byte_transposes_through_registers_with_tables():
     w = dict(sizes=[3, 64, 272], in_offset=2, in_strides=[64 * 272, 272, 1], in_elems=2 + 3 * 64 * 272, out_offset=0,
              out_strides=[272 * 64, 1, 64], out_elems=3 * 272 * 64)
     _check(w, 1)
+    # 300 B rows: 256 x 128 tiles with tables, a short last tile
+    w = dict(sizes=[300, 4, 64], in_offset=0, in_strides=[256, 64, 1], in_elems=300 * 256, out_offset=0,
+             out_strides=[1, 19472, 304], out_elems=3 * 19472 + 63 * 304 + 300)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and len(q["group_a"]) == 2
+    _check(w, 1)
+    _check(dict(w, in_offset=3, in_elems=w["in_elems"] + 3), 1)
 
 
 @pytest.mark.parametrize("shape,perm,elem", [

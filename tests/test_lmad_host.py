@@ -250,7 +250,7 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert not set(a) & set(b)
 
 
-def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False):
+def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False, tall=1):
     """The chunk path of the tile kernel, replayed on the host for 1- to
     8-byte words: rows of 256 bytes (TA = 16 * V elements, V = 16 / word per
     chunk) fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
@@ -266,10 +266,12 @@ def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False):
     as 4-byte words, two and a funnel shift where a row's bytes are not
     4-byte aligned, and writes one 8-byte store per column); it covers the
     tile once, stays inside the shared array, and a warp's loads of rows that
-    share one misalignment hit 32 distinct banks."""
+    share one misalignment hit 32 distinct banks.  tall = 4: the byte path's
+    256 x 128 tiles, four 8 x 4 blocks per thread."""
     V = 16 // word
     TA = nch * V
-    TB = {1: 8192, 2: 8192, 4: 4096, 8: 1024}[word] // TA
+    TB = tall * {1: 8192, 2: 8192, 4: 4096, 8: 1024}[word] // TA
+    assert TB <= 256
     pitch = {16: 25, 8: 17}[nch] * V
     rot = 2 if byte_pack else 1
     tile = {}
@@ -305,27 +307,30 @@ def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False):
     if byte_pack:
         assert word == 1
         stripes = TA // 32
+        qs, items = 8 // stripes, (TA // 4) * (TB // 8) // 256
+        assert (TA // 4) * (TB // 8) == 256 * items
         covered = set()
         words = {}
         for t in range(256):
             w, lane = t >> 5, t & 31
-            g = (w // stripes) * 4 + (lane & 3)
-            ia0, ib0 = (w % stripes) * 32 + 4 * (lane >> 2), 8 * g
-            assert 0 <= ia0 < TA and ib0 < TB
-            if ib0 >= rb:
-                continue
-            base = ib0 * pitch + V * rot * (g & 3) + ia0
-            for k in range(8):
-                row = ib0 + k
-                a = base + k * pitch + (base_mis + row * sb) % V
-                assert a == base_of(row) + (base_mis + row * sb) % V + ia0
-                assert (a & ~3) + 8 <= TB * pitch  # the funnel shift's second word
-                words.setdefault((w, k), []).append(a >> 2)
-                if row < rb:
-                    for j in range(4):
-                        assert tile[a + j] == (row, ia0 + j)
-                        assert (ia0 + j, row) not in covered
-                        covered.add((ia0 + j, row))
+            ia0 = (w % stripes) * 32 + 4 * (lane >> 2)
+            for i in range(items):
+                ib0 = 32 * (w // stripes + qs * i) + 8 * (lane & 3)
+                assert 0 <= ia0 < TA and ib0 < TB
+                if ib0 >= rb:
+                    break
+                base = ib0 * pitch + V * rot * (lane & 3) + ia0
+                for k in range(8):
+                    row = ib0 + k
+                    a = base + k * pitch + (base_mis + row * sb) % V
+                    assert a == base_of(row) + (base_mis + row * sb) % V + ia0
+                    assert (a & ~3) + 8 <= TB * pitch  # the funnel shift's second word
+                    words.setdefault((w, i, k), []).append(a >> 2)
+                    if row < rb:
+                        for j in range(4):
+                            assert tile[a + j] == (row, ia0 + j)
+                            assert (ia0 + j, row) not in covered
+                            covered.add((ia0 + j, row))
         assert len(covered) == TA * min(rb, TB)
         if sb % V == 0 and base_mis % 4 == 0:
             for ws in words.values():
@@ -350,6 +355,8 @@ def test_chunked_tile_mapping(word, sb):
                 _chunk_tile_emulation(word, base_mis, sb, rb, nch)
                 if word == 1:
                     _chunk_tile_emulation(word, base_mis, sb, rb, nch, byte_pack=True)
+                    if nch == 16:
+                        _chunk_tile_emulation(word, base_mis, sb, rb, nch, byte_pack=True, tall=4)
 
 
 def test_rows_kind_for_small_elements():
