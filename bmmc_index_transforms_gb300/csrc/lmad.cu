@@ -447,20 +447,23 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     constexpr int V = 16 / (int)sizeof(W), LV = clog2(V), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
-    // 1-byte words with packs move 8 x 4 blocks through registers (below)
-    // and rotate rows by two chunks per 8 rows, the others by one
-    constexpr bool BYTES = PACK && sizeof(W) == 1;
-    constexpr int ROT = BYTES ? 2 : 1;
-    static_assert(NCH + 1 + 3 * ROT <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
-    static_assert(TALL == 1 || BYTES, "tall tiles on the 1-byte pack path only");
+    // 1- and 2-byte words with packs move 8-row blocks through registers
+    // (below).  Their rows rotate by ROT chunks per 8 rows over PH phases
+    // (1 byte: 2 chunks, 4 phases; 2 bytes: 1 chunk, 8 phases), the others'
+    // by one chunk over 4 phases.
+    constexpr bool REG = PACK && sizeof(W) <= 2;
+    constexpr int ROT = REG && sizeof(W) == 1 ? 2 : 1;
+    constexpr int PH = REG && sizeof(W) == 2 ? 8 : 4;
+    static_assert(NCH + 1 + ROT * (PH - 1) <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
+    static_assert(TALL == 1 || (REG && sizeof(W) == 1), "tall tiles on the 1-byte pack path only");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
     // every row shares the origin's misalignment (B's source stride a
     // multiple of V): no per-row arithmetic for it
     const bool uni = ad.template same_mis<V>();
     // row r holds its segment shifted by its misalignment m, starting at
-    // chunk ROT * ((r / 8) mod 4) of its pitch: element (r, c = column + m)
-    // at r * kPitch + ROT * ((r / 8) mod 4) * V + c, whole chunks at 16-byte
+    // chunk ROT * ((r / 8) mod PH) of its pitch: element (r, c = column + m)
+    // at r * kPitch + ROT * ((r / 8) mod PH) * V + c, whole chunks at 16-byte
     // boundaries
 #pragma unroll
     for (int r = 0; r < TB * NCH / 256; ++r) {
@@ -471,7 +474,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
         if (m == 0 || kk < NCH - 1) {
             const int k = kk + (m != 0);
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & 3))),
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
                           reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
         }
     }
@@ -484,7 +487,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
             if (m != 0) {
                 const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
-                W* slot = tile + row * kPitch + V * ROT * ((row >> 3) & 3) + e + m;
+                W* slot = tile + row * kPitch + V * ROT * ((row >> 3) & (PH - 1)) + e + m;
                 if constexpr (sizeof(W) >= 4)
                     cp_async_word(slot, src + s0 + e);
                 else
@@ -494,45 +497,45 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if constexpr (BYTES) {
-        // each item: B rows ib0..ib0+7 x columns ia0..ia0+3.  Eight 4-byte
-        // shared loads (two and a funnel shift for a row whose bytes are not
-        // 4-byte aligned there), two 4 x 4 byte transposes by byte permutes,
-        // and one 8-byte store per column.  Lanes l & 3 take four
-        // neighbouring 8-row groups (a whole 32-byte destination sector per
-        // column) and l >> 2 eight neighbouring column words, so with the
-        // two-chunk rotation per 8 rows a warp's loads hit 32 distinct
-        // banks; warps take the 32-byte column stripes, then the quads of
-        // row groups, and a thread's ITEMS items are QS quads apart (same
-        // columns, so the same destination column offsets).
-        constexpr int STRIPES = TA / 32, QS = 8 / STRIPES, ITEMS = (TA / 4) * (TB / 8) / 256;
-        static_assert(TA % 32 == 0 && ITEMS >= 1 && (TA / 4) * (TB / 8) == 256 * ITEMS, "whole 8 x 4 blocks");
+    if constexpr (REG) {
+        // each item: B rows ib0..ib0+7 x the EPW columns of one 4-byte word
+        // (ia0..ia0+EPW-1).  Eight 4-byte shared loads (two and a funnel
+        // shift for a row whose elements are not 4-byte aligned there), a
+        // transpose by byte permutes (two 4 x 4 of bytes, or four 2 x 2 of
+        // 2-byte elements), and one 8- or 16-byte store per column.  Lanes
+        // l % RG take RG neighbouring 8-row groups (a whole 32- or 128-byte
+        // destination run per column) and l / RG neighbouring words, so with
+        // the rotation a warp's loads hit 32 distinct banks.  Warp items run
+        // over the stripes of WL words, then over the sets of RG row groups;
+        // a thread's items share their lane's rotation.
+        constexpr int EPW = 4 / (int)sizeof(W), RG = PH, WL = 32 / RG;
+        constexpr int STRIPES = TA / EPW / WL, SETS = TB / (8 * RG), ITEMS = STRIPES * SETS / 8;
+        static_assert(ITEMS >= 1 && STRIPES * SETS == 8 * ITEMS && 16 * ROT == 4 * WL, "whole blocks, distinct banks");
         const int w = t >> 5, l = t & 31;
-        const int ia0 = (w % STRIPES) * 32 + 4 * (l >> 2);
         const unsigned char* tb = reinterpret_cast<const unsigned char*>(tile);
-        O da[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) da[j] = ad.dst_a(ia0 + j);
-        const int lead = V * ROT * (l & 3) + ia0;  // rotation of every item's rows: ((32 q + 8 (l & 3)) / 8) mod 4
-        auto item = [&](const int ib0, auto same) {
-            const int base = ib0 * kPitch + lead;
+        const int lead = V * ROT * (l & (RG - 1));  // ((8 RG set + 8 (l % RG)) / 8) mod PH = l % RG
+        auto item = [&](const int ib0, const int ia0, auto same) {
+            const int base = (ib0 * kPitch + lead + ia0) * (int)sizeof(W);  // bytes
             uint32_t v[8];
             if constexpr (decltype(same)::value) {
-                const int b = base + (int)base_mis;
+                const int b = base + (int)(base_mis * sizeof(W));
                 const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (b & ~3));
-                if ((base_mis & 3) == 0) {
+                if ((b & 3) == 0) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = p[k * (kPitch / 4)];
+                    for (int k = 0; k < 8; ++k) v[k] = p[k * (kPitch * (int)sizeof(W) / 4)];
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = __funnelshift_r(p[k * (kPitch / 4)], p[k * (kPitch / 4) + 1], 8 * (b & 3));
+                    for (int k = 0; k < 8; ++k)
+                        v[k] = __funnelshift_r(p[k * (kPitch * (int)sizeof(W) / 4)],
+                                               p[k * (kPitch * (int)sizeof(W) / 4) + 1], 8 * (b & 3));
                 }
             } else {
                 int a[8];
                 unsigned low = 0;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    a[k] = base + k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1));
+                    a[k] = base + (k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1))) *
+                                      (int)sizeof(W);
                     low |= (unsigned)a[k];
                 }
                 if ((low & 3) == 0) {
@@ -546,40 +549,59 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     }
                 }
             }
-            // byte j of v[k] is element (ib0 + k, ia0 + j); col[j][h] gathers
-            // byte j of v[4h..4h+3]
-            uint32_t col[4][2];
+            // element j of word v[k] is element (ib0 + k, ia0 + j); col[j]
+            // holds rows ib0..ib0+7 of column ia0 + j, two or four rows a word
+            uint32_t col[EPW][8 / EPW];
+            if constexpr (sizeof(W) == 1) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], 0x5140);
-                const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], 0x7362);
-                const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x5140);
-                const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x7362);
-                col[0][h] = __byte_perm(t0, t2, 0x5410);
-                col[1][h] = __byte_perm(t0, t2, 0x7632);
-                col[2][h] = __byte_perm(t1, t3, 0x5410);
-                col[3][h] = __byte_perm(t1, t3, 0x7632);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], 0x5140);
+                    const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], 0x7362);
+                    const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x5140);
+                    const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], 0x7362);
+                    col[0][h] = __byte_perm(t0, t2, 0x5410);
+                    col[1][h] = __byte_perm(t0, t2, 0x7632);
+                    col[2][h] = __byte_perm(t1, t3, 0x5410);
+                    col[3][h] = __byte_perm(t1, t3, 0x7632);
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    col[0][h] = __byte_perm(v[2 * h], v[2 * h + 1], 0x5410);
+                    col[1][h] = __byte_perm(v[2 * h], v[2 * h + 1], 0x7632);
+                }
             }
             W* o = dst + ad.dst_b(ib0);
             if (ib0 + 8 <= rb) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) __stcs(reinterpret_cast<uint2*>(o + da[j]), make_uint2(col[j][0], col[j][1]));
+                for (int j = 0; j < EPW; ++j) {
+                    W* oj = o + ad.dst_a(ia0 + j);
+                    if constexpr (sizeof(W) == 1)
+                        __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
+                    else
+                        __stcs(reinterpret_cast<uint4*>(oj), make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+                }
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < EPW; ++j)
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        if (ib0 + k < rb) o[da[j] + k] = (W)(col[j][k >> 2] >> (8 * (k & 3)));
+                        if (ib0 + k < rb)
+                            o[ad.dst_a(ia0 + j) + k] =
+                                (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
             }
         };
-#pragma unroll
+#pragma unroll 1
         for (int i = 0; i < ITEMS; ++i) {
-            const int ib0 = 32 * (w / STRIPES + QS * i) + 8 * (l & 3);
-            if (ib0 >= rb) break;  // rows grow with i; no barrier follows inside this function
-            if (uni)
-                item(ib0, std::true_type{});
-            else
-                item(ib0, std::false_type{});
+            const int x = w + 8 * i;
+            const int ib0 = 8 * RG * (x / STRIPES) + 8 * (l & (RG - 1));
+            const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
+            if (ib0 < rb) {
+                if (uni)
+                    item(ib0, ia0, std::true_type{});
+                else
+                    item(ib0, ia0, std::false_type{});
+            }
         }
         return;
     } else if constexpr (PACK) {
@@ -893,7 +915,7 @@ enum {
 template <typename W, int MODE>
 constexpr int tile_min_blocks() {
     return (MODE & kTileTall)   ? 4
-           : (MODE & kTilePack) ? (sizeof(W) == 1 ? LMAD_BYTE_BLOCKS : 4)
+           : (MODE & kTilePack) ? (sizeof(W) == 1 ? ((MODE & kTileTables) ? 5 : LMAD_BYTE_BLOCKS) : sizeof(W) == 2 ? 5 : 4)
            : (MODE & kTileChunked) ? 6
                                    : (sizeof(W) == 4 ? 8 : 6);
 }

@@ -276,6 +276,34 @@ def test_byte_transposes_through_registers(case):
     _check(w, 1, seed=5)
 
 
+@pytest.mark.parametrize("case", [
+    dict(R=256, C=512), dict(R=48, C=1000), dict(R=64, C=1000, in_off=3), dict(R=64, C=1024, in_off=2),
+    dict(R=64, C=1024, in_off=1), dict(R=37, C=600, out_pitch=40), dict(R=100, C=777, in_off=1, in_pitch=779, out_pitch=104),
+    dict(R=512, C=64), dict(R=512, C=64, in_off=5), dict(R=300, C=64, in_pitch=67, out_pitch=304),
+    dict(R=64, C=512, out_off=8), dict(R=64, C=512, out_off=4),
+])
+def test_two_byte_transposes_through_registers(case):
+    """The same register path for 2-byte words (bf16 / fp16 transposes):
+    8 x 2 blocks, 2 x 2 transposes of 16-bit halves, 16-byte stores; rows
+    of 256 and 128 bytes, aligned, uniformly and per-row misaligned sources,
+    partial row groups, and a destination that takes no packs."""
+    w = _byte_transpose_view(**case)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 2,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and not q["narrow"]
+    _check(w, 2)
+    _check(w, 2, seed=9)
+
+
+def test_two_byte_transposes_through_registers_with_tables():
+    w = dict(sizes=[64, 4, 32], in_offset=1, in_strides=[128, 32, 1], in_elems=1 + 64 * 128, out_offset=0,
+             out_strides=[1, 2056, 64], out_elems=3 * 2056 + 31 * 64 + 64)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 2,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and len(q["group_a"]) == 2
+    _check(w, 2)
+
+
 def test_byte_transposes_through_registers_with_tables():
     """The same path with offset tables: group A spans two dimensions that
     do not collapse (a padded destination), and a batch dimension."""

@@ -250,7 +250,7 @@ def test_transpose_tiles_hold_exactly_one_tile_of_elements(seed):
     assert not set(a) & set(b)
 
 
-def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False, tall=1):
+def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, reg=False, tall=1):
     """The chunk path of the tile kernel, replayed on the host for 1- to
     8-byte words: rows of 256 bytes (TA = 16 * V elements, V = 16 / word per
     chunk) fetched as 16-byte chunks (16 lanes per row, chunk k + 1 for
@@ -261,23 +261,25 @@ def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False, tall=
     column-wise at row offset + column; rows rb.. of a tile short along B are
     skipped.  Every element is placed exactly once, every 16-byte fetch and
     every 16-byte shared store is aligned, and every read returns the element
-    the transpose needs.  byte_pack: the 1-byte store path instead (rows
-    rotated by two chunks per 8 rows; each thread reads 8 rows x 4 columns
-    as 4-byte words, two and a funnel shift where a row's bytes are not
-    4-byte aligned, and writes one 8-byte store per column); it covers the
-    tile once, stays inside the shared array, and a warp's loads of rows that
-    share one misalignment hit 32 distinct banks.  tall = 4: the byte path's
-    256 x 128 tiles, four 8 x 4 blocks per thread."""
+    the transpose needs.  reg: the register store path of 1- and 2-byte
+    words instead (rows rotated by ROT chunks per 8 rows over PH phases:
+    2 and 4 for bytes, 1 and 8 for 2-byte words; each item is 8 rows x the
+    elements of one 4-byte word, read as 4-byte words, two and a funnel
+    shift where a row's elements are not 4-byte aligned, and written as one
+    store per column); it covers the tile once, stays inside the shared
+    array, and a warp's loads of rows that share one misalignment hit 32
+    distinct banks.  tall = 4: 1-byte tiles of 256 x 128."""
     V = 16 // word
     TA = nch * V
     TB = tall * {1: 8192, 2: 8192, 4: 4096, 8: 1024}[word] // TA
     assert TB <= 256
     pitch = {16: 25, 8: 17}[nch] * V
-    rot = 2 if byte_pack else 1
+    rot, ph = (2, 4) if reg and word == 1 else (1, 8) if reg else (1, 4)
+    assert nch + 1 + rot * (ph - 1) <= pitch // V
     tile = {}
 
     def base_of(row):
-        return row * pitch + ((row >> 3) & 3) * V * rot
+        return row * pitch + ((row >> 3) & (ph - 1)) * V * rot
 
     for t in range(256):
         for r in range(TB * nch // 256):
@@ -304,35 +306,39 @@ def _chunk_tile_emulation(word, base_mis, sb, rb, nch=16, byte_pack=False, tall=
                 assert a not in tile
                 tile[a] = (row, e)
     assert len(tile) == TA * min(rb, TB) and max(tile) < TB * pitch
-    if byte_pack:
-        assert word == 1
-        stripes = TA // 32
-        qs, items = 8 // stripes, (TA // 4) * (TB // 8) // 256
-        assert (TA // 4) * (TB // 8) == 256 * items
+    if reg:
+        assert word in (1, 2)
+        epw, rg = 4 // word, ph
+        wl = 32 // rg
+        stripes, sets = TA // epw // wl, TB // (8 * rg)
+        items = stripes * sets // 8
+        assert items >= 1 and stripes * sets == 8 * items and 16 * rot == 4 * wl
         covered = set()
         words = {}
         for t in range(256):
             w, lane = t >> 5, t & 31
-            ia0 = (w % stripes) * 32 + 4 * (lane >> 2)
             for i in range(items):
-                ib0 = 32 * (w // stripes + qs * i) + 8 * (lane & 3)
+                x = w + 8 * i
+                ib0 = 8 * rg * (x // stripes) + 8 * (lane % rg)
+                ia0 = epw * ((x % stripes) * wl + lane // rg)
                 assert 0 <= ia0 < TA and ib0 < TB
                 if ib0 >= rb:
-                    break
-                base = ib0 * pitch + V * rot * (lane & 3) + ia0
+                    continue
+                base = ib0 * pitch + V * rot * (lane % rg) + ia0
                 for k in range(8):
                     row = ib0 + k
                     a = base + k * pitch + (base_mis + row * sb) % V
                     assert a == base_of(row) + (base_mis + row * sb) % V + ia0
-                    assert (a & ~3) + 8 <= TB * pitch  # the funnel shift's second word
-                    words.setdefault((w, i, k), []).append(a >> 2)
+                    byte = a * word
+                    assert (byte & ~3) + 8 <= TB * pitch * word  # the funnel shift's second word
+                    words.setdefault((w, i, k), []).append(byte >> 2)
                     if row < rb:
-                        for j in range(4):
+                        for j in range(epw):
                             assert tile[a + j] == (row, ia0 + j)
                             assert (ia0 + j, row) not in covered
                             covered.add((ia0 + j, row))
         assert len(covered) == TA * min(rb, TB)
-        if sb % V == 0 and base_mis % 4 == 0:
+        if sb % V == 0 and (base_mis * word) % 4 == 0:
             for ws in words.values():
                 assert len({x % 32 for x in ws}) == len(set(ws))
         return
@@ -353,10 +359,10 @@ def test_chunked_tile_mapping(word, sb):
         for base_mis in range(16 // word):
             for rb in (128, 100, 64, 62, 32, 31, 17, 1):
                 _chunk_tile_emulation(word, base_mis, sb, rb, nch)
-                if word == 1:
-                    _chunk_tile_emulation(word, base_mis, sb, rb, nch, byte_pack=True)
-                    if nch == 16:
-                        _chunk_tile_emulation(word, base_mis, sb, rb, nch, byte_pack=True, tall=4)
+                if word <= 2:
+                    _chunk_tile_emulation(word, base_mis, sb, rb, nch, reg=True)
+                if word == 1 and nch == 16:
+                    _chunk_tile_emulation(word, base_mis, sb, rb, nch, reg=True, tall=4)
 
 
 def test_rows_kind_for_small_elements():
