@@ -443,7 +443,7 @@ constexpr int kTallTileBytes = 128 * chunk_pitch(16) * 16;
 
 template <typename W, typename O, bool PACK, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
-                                                    const Addr& ad, int rb) {
+                                                    const Addr& ad, int rb, int lo) {
     constexpr int V = 16 / (int)sizeof(W), LV = clog2(V), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
@@ -500,7 +500,8 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     if constexpr (REG) {
         // each item: B rows ib0..ib0+7 x the EPW columns of one 4-byte word
         // (ia0..ia0+EPW-1).  Eight 4-byte shared loads (two and a funnel
-        // shift for a row whose elements are not 4-byte aligned there), a
+        // shift for rows whose elements are not 4-byte aligned there, or
+        // whose misalignments differ), a
         // transpose by byte permutes (two 4 x 4 of bytes, or four 2 x 2 of
         // 2-byte elements), and one 8- or 16-byte store per column.  Lanes
         // l % RG take RG neighbouring 8-row groups (a whole 32- or 128-byte
@@ -530,23 +531,14 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                                                p[k * (kPitch * (int)sizeof(W) / 4) + 1], 8 * (b & 3));
                 }
             } else {
-                int a[8];
-                unsigned low = 0;
+                // rows with their own misalignments: two loads and a funnel
+                // shift each
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    a[k] = base + (k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1))) *
-                                      (int)sizeof(W);
-                    low |= (unsigned)a[k];
-                }
-                if ((low & 3) == 0) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint32_t*>(tb + a[k]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (a[k] & ~3));
-                        v[k] = __funnelshift_r(p[0], p[1], 8 * (a[k] & 3));
-                    }
+                    const int a = base + (k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1))) *
+                                             (int)sizeof(W);
+                    const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (a & ~3));
+                    v[k] = __funnelshift_r(p[0], p[1], 8 * (a & 3));
                 }
             }
             // element j of word v[k] is element (ib0 + k, ia0 + j); col[j]
@@ -575,6 +567,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             if (ib0 + 8 <= rb) {
 #pragma unroll
                 for (int j = 0; j < EPW; ++j) {
+                    if (ia0 + j < lo) continue;  // a shifted tile's columns of the previous tile
                     W* oj = o + ad.dst_a(ia0 + j);
                     if constexpr (sizeof(W) == 1)
                         __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
@@ -586,7 +579,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                 for (int j = 0; j < EPW; ++j)
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        if (ib0 + k < rb)
+                        if (ib0 + k < rb && ia0 + j >= lo)
                             o[ad.dst_a(ia0 + j) + k] =
                                 (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
             }
@@ -596,7 +589,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             const int x = w + 8 * i;
             const int ib0 = 8 * RG * (x / STRIPES) + 8 * (l & (RG - 1));
             const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
-            if (ib0 < rb) {
+            if (ib0 < rb && ia0 + EPW > lo) {
                 if (uni)
                     item(ib0, ia0, std::true_type{});
                 else
@@ -623,6 +616,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const bool whole = ib0 + V <= rb;
 #pragma unroll 1
         for (int ia = t >> LG; ia < TA; ia += 256 >> LG) {
+            if (ia < lo) continue;  // a shifted tile's columns of the previous tile
             W v[V];
 #pragma unroll
             for (int k = 0; k < V; ++k) v[k] = tile[off[k] + ia];
@@ -650,7 +644,8 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
 #pragma unroll
         for (int r = 0; r < CH; ++r) v[r] = row[ia0 + kStep * (c0 + r)];
 #pragma unroll
-        for (int r = 0; r < CH; ++r) __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
+        for (int r = 0; r < CH; ++r)
+            if (ia0 + kStep * (c0 + r) >= lo) __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
     }
 }
 
@@ -968,9 +963,18 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             so += (O)r * (O)p.cs[k];
             d += (O)r * (O)p.ct[k];
         }
-        const I a0 = ta << p.la, b0 = tb << p.lb;
-        const int ra = (int)min((uint64_t)TA, p.n_a - (uint64_t)a0);
+        I a0 = ta << p.la;
+        const I b0 = tb << p.lb;
+        int ra = (int)min((uint64_t)TA, p.n_a - (uint64_t)a0);
         const int rb = (int)min((uint64_t)TB, p.n_b - (uint64_t)b0);
+        // the chunk path takes a ragged last A tile shifted back to end at
+        // n_a (whole again), storing only its last ra columns
+        int lo = 0;
+        if (CHUNKED && ra < TA && p.n_a >= (uint64_t)TA) {
+            lo = TA - ra;
+            a0 = (I)(p.n_a - (uint64_t)TA);
+            ra = TA;
+        }
         if constexpr (GENERAL) {
             // offset tables of this tile's A- and B-indices
             for (int i = t; i < TA + TB; i += 256) {
@@ -1011,7 +1015,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const TabAddr<O> ad{tab_src, tab_dst, TA, 0};
             if (CHUNKED && ra == TA) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb);
+                    tile_phases_chunked<W, O, PACK, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb, lo);
             } else if constexpr (TALL > 1) {
                 // a ragged-A tall tile: the element path, a quarter of the rows at a time
                 constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
@@ -1030,7 +1034,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH, TALL>(src, dst, tile, ad, rb);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH, TALL>(src, dst, tile, ad, rb, lo);
             } else if constexpr (TALL > 1) {
                 constexpr int QB = S::T >> 8;
                 for (int j = 0; j * QB < rb; ++j) {
