@@ -602,10 +602,16 @@ def other_configs(torch, bm, synth, dev, stream):
     for name, shape, perm in (("t2d_8191x8193", (8191, 8193), (1, 0)),
                               ("batched_64x1000x1000", (64, 1000, 1000), (0, 2, 1))):
         out["lmad_" + name + "_int32"] = lmad_case(torch, bm, axes_lmad(synth, shape, perm), a32, b32, stream)
-    # image layout conversions and a bf16 transpose (narrow and tile kernels)
+    # image layout conversions, 1- and 2-byte transposes (narrow and tile
+    # kernels, the register path, a ragged last tile) and permutations of
+    # 4-byte pixels and 16-byte vectors (moved as words)
     for name, shape, perm, elem in (("nhwc2nchw_32x1024x1024x3_uint8", (32, 1024, 1024, 3), (0, 3, 1, 2), 1),
                                     ("nhwc2nchw_8x512x512x64_fp16", (8, 512, 512, 64), (0, 3, 1, 2), 2),
-                                    ("t2d_8192x8192_bf16", (8192, 8192), (1, 0), 2)):
+                                    ("t2d_8192x8192_bf16", (8192, 8192), (1, 0), 2),
+                                    ("t2d_16384x16384_uint8", (16384, 16384), (1, 0), 1),
+                                    ("t2d_16384x16400_uint8", (16384, 16400), (1, 0), 1),
+                                    ("swap_hw_8000x6000x4_uint8", (8000, 6000, 4), (1, 0, 2), 1),
+                                    ("swap_4000x4096x16_uint8", (4000, 4096, 16), (1, 0, 2), 1)):
         out["lmad_" + name] = lmad_case(torch, bm, axes_lmad(synth, shape, perm), a32, b32, stream, elem=elem)
     # the same slice on 1- and 2-byte elements (uint8 crop, fp16 slice: the rows kernel)
     out["lmad_slice_2d_16384x16385_uint8"] = lmad_case(
