@@ -610,6 +610,8 @@ def other_configs(torch, bm, synth, dev, stream):
                                     ("t2d_8192x8192_bf16", (8192, 8192), (1, 0), 2),
                                     ("t2d_16384x16384_uint8", (16384, 16384), (1, 0), 1),
                                     ("t2d_16384x16400_uint8", (16384, 16400), (1, 0), 1),
+                                    ("t2d_16383x16385_uint8", (16383, 16385), (1, 0), 1),
+                                    ("t2d_11585x11587_fp16", (11585, 11587), (1, 0), 2),
                                     ("swap_hw_8000x6000x4_uint8", (8000, 6000, 4), (1, 0, 2), 1),
                                     ("swap_4000x4096x16_uint8", (4000, 4096, 16), (1, 0, 2), 1)):
         out["lmad_" + name] = lmad_case(torch, bm, axes_lmad(synth, shape, perm), a32, b32, stream, elem=elem)

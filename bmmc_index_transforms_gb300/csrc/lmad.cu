@@ -292,6 +292,11 @@ struct TileSides {
 #ifndef LMAD_TILE_PACK_WORDS
 #define LMAD_TILE_PACK_WORDS (1 | 2)
 #endif
+// 1- and 2-byte pack path also for destinations that are not 16-byte
+// aligned (each column realigned to 8-byte words by lane shuffles).
+#ifndef LMAD_TILE_SHIFT
+#define LMAD_TILE_SHIFT 1
+#endif
 // Resident blocks per SM asked of the compiler for the 1-byte pack path.
 #ifndef LMAD_BYTE_BLOCKS
 #define LMAD_BYTE_BLOCKS 6
@@ -422,9 +427,9 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 // is 256 bytes, 16 chunks of 16 bytes (V = 16 / word elements each).  The
 // segment is fetched as 16-byte aligned chunks with cp.async, 16 lanes per
 // row; a row that does not start on a 16-byte boundary (misalignment m =
-// its first element's offset from one, 1..V-1) leaves V elements in the
-// partial chunks at its two ends (V - m at the head, m at the tail), which a
-// second pass copies one element per thread.  Row ib is kept in shared
+// its first element's offset from one, 1..V-1) spans 17 aligned chunks, the
+// first holding V - m of its elements and the last m, and a second pass
+// fetches the first chunk of each such row.  Row ib is kept in shared
 // memory shifted by its misalignment and rotated by (ib / 8) mod 4 chunks
 // inside a pitch of chunk_pitch(NCH) chunks (the rotation spreads the store
 // phase's column reads, 32 consecutive rows per warp, over the banks; with
@@ -441,10 +446,45 @@ constexpr int chunk_pitch(int nch) { return ((nch + 4 + 6) / 8) * 8 + 1; }
 // chunk_pitch(16) chunks.
 constexpr int kTallTileBytes = 128 * chunk_pitch(16) * 16;
 
-template <typename W, typename O, bool PACK, int NCH, int TALL, typename Addr>
+// Stores of the low n bytes of v (0 < n < 8) whose last byte ends an
+// aligned 8-byte word (head) or whose first byte starts one (tail), as at
+// most three aligned 1-, 2- and 4-byte stores; a head with n = 8 is one
+// aligned 8-byte store.
+__device__ __forceinline__ void store_head8(unsigned char* p, uint64_t v, int mu) {
+    if (mu == 0) {
+        __stcs(reinterpret_cast<unsigned long long*>(p), (unsigned long long)v);
+        return;
+    }
+    if ((uintptr_t)p & 1u) {
+        __stcs(p, (unsigned char)v);
+        v >>= 8;
+        p += 1;
+    }
+    if ((uintptr_t)p & 2u) {
+        __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)v);
+        v >>= 16;
+        p += 2;
+    }
+    if ((uintptr_t)p & 4u) __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)v);
+}
+__device__ __forceinline__ void store_tail8(unsigned char* p, uint64_t v, int n) {
+    if (n & 4) {
+        __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)v);
+        v >>= 32;
+        p += 4;
+    }
+    if (n & 2) {
+        __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)v);
+        v >>= 16;
+        p += 2;
+    }
+    if (n & 1) __stcs(p, (unsigned char)v);
+}
+
+template <typename W, typename O, bool PACK, bool SHIFT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
                                                     const Addr& ad, int rb, int lo) {
-    constexpr int V = 16 / (int)sizeof(W), LV = clog2(V), LNCH = clog2(NCH);
+    constexpr int V = 16 / (int)sizeof(W), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
     // 1- and 2-byte words with packs move 8-row blocks through registers
@@ -456,6 +496,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     constexpr int PH = REG && sizeof(W) == 2 ? 8 : 4;
     static_assert(NCH + 1 + ROT * (PH - 1) <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
     static_assert(TALL == 1 || (REG && sizeof(W) == 1), "tall tiles on the 1-byte pack path only");
+    static_assert(!SHIFT || REG, "realigned packs on the 1- and 2-byte register path only");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
     // every row shares the origin's misalignment (B's source stride a
@@ -464,7 +505,11 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     // row r holds its segment shifted by its misalignment m, starting at
     // chunk ROT * ((r / 8) mod PH) of its pitch: element (r, c = column + m)
     // at r * kPitch + ROT * ((r / 8) mod PH) * V + c, whole chunks at 16-byte
-    // boundaries
+    // boundaries.  A misaligned row spans NCH + 1 aligned chunks: chunks
+    // 1..NCH here, chunk 0 below.  Its first and last chunks also hold bytes
+    // outside the segment, which are fetched and never used; an aligned
+    // 16-byte chunk that holds a byte of the array lies in the same page as
+    // that byte, so the fetch stays in mapped memory.
 #pragma unroll
     for (int r = 0; r < TB * NCH / 256; ++r) {
         const int idx = t + 256 * r;
@@ -472,27 +517,19 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         if (row >= rb) break;  // rows grow with r
         const O s0 = ad.src_b(row);
         const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
-        if (m == 0 || kk < NCH - 1) {
-            const int k = kk + (m != 0);
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
-                          reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
-        }
+        const int k = kk + (m != 0);
+        cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
+                      reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
     }
     if (!uni || base_mis != 0) {
 #pragma unroll
-        for (int u = t; u < TB * V; u += 256) {
-            const int row = u >> LV, j = u & (V - 1);
-            if (row >= rb) break;  // rows grow with u
+        for (int row = t; row < TB; row += 256) {
+            if (row >= rb) break;  // rows grow
             const O s0 = ad.src_b(row);
             const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
-            if (m != 0) {
-                const int e = j < V - m ? j : TA - V + j;  // head elements 0..V-1-m, tail TA-m..TA-1
-                W* slot = tile + row * kPitch + V * ROT * ((row >> 3) & (PH - 1)) + e + m;
-                if constexpr (sizeof(W) >= 4)
-                    cp_async_word(slot, src + s0 + e);
-                else
-                    *slot = __ldg(src + s0 + e);
-            }
+            if (m != 0)
+                cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * ROT * ((row >> 3) & (PH - 1))),
+                              reinterpret_cast<const uint4*>(src + s0 - m));
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -505,17 +542,24 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         // transpose by byte permutes (two 4 x 4 of bytes, or four 2 x 2 of
         // 2-byte elements), and one 8- or 16-byte store per column.  Lanes
         // l % RG take RG neighbouring 8-row groups (a whole 32- or 128-byte
-        // destination run per column) and l / RG neighbouring words, so with
-        // the rotation a warp's loads hit 32 distinct banks.  Warp items run
-        // over the stripes of WL words, then over the sets of RG row groups;
-        // a thread's items share their lane's rotation.
+        // destination run per column: a "set" of rows) and l / RG
+        // neighbouring words, so with the rotation a warp's loads hit 32
+        // distinct banks.  Warp items run over the stripes of WL words, then
+        // over the sets; a thread's items share their lane's rotation.
         constexpr int EPW = 4 / (int)sizeof(W), RG = PH, WL = 32 / RG;
         constexpr int STRIPES = TA / EPW / WL, SETS = TB / (8 * RG), ITEMS = STRIPES * SETS / 8;
         static_assert(ITEMS >= 1 && STRIPES * SETS == 8 * ITEMS && 16 * ROT == 4 * WL, "whole blocks, distinct banks");
         const int w = t >> 5, l = t & 31;
         const unsigned char* tb = reinterpret_cast<const unsigned char*>(tile);
         const int lead = V * ROT * (l & (RG - 1));  // ((8 RG set + 8 (l % RG)) / 8) mod PH = l % RG
-        auto item = [&](const int ib0, const int ia0, auto same) {
+        // element j of word v[k] is element (ib0 + k, ia0 + j); col[j]
+        // receives rows ib0..ib0+7 of column ia0 + j, two or four rows a word
+        struct Cols {
+            uint32_t c[EPW][8 / EPW];
+        };
+        auto gather = [&](const int ib0, const int ia0, auto same) {
+            Cols out;
+            auto& col = out.c;
             const int base = (ib0 * kPitch + lead + ia0) * (int)sizeof(W);  // bytes
             uint32_t v[8];
             if constexpr (decltype(same)::value) {
@@ -541,9 +585,6 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     v[k] = __funnelshift_r(p[0], p[1], 8 * (a & 3));
                 }
             }
-            // element j of word v[k] is element (ib0 + k, ia0 + j); col[j]
-            // holds rows ib0..ib0+7 of column ia0 + j, two or four rows a word
-            uint32_t col[EPW][8 / EPW];
             if constexpr (sizeof(W) == 1) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -563,37 +604,131 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     col[1][h] = __byte_perm(v[2 * h], v[2 * h + 1], 0x7632);
                 }
             }
+            return out;
+        };
+        auto gather_item = [&](const int ib0, const int ia0) {
+            return uni ? gather(ib0, ia0, std::true_type{}) : gather(ib0, ia0, std::false_type{});
+        };
+        // rows ib0.. of a ragged set (those below rb), element by element
+        auto store_ragged = [&](const int ib0, const int ia0, const Cols& cs) {
+            const auto& col = cs.c;
             W* o = dst + ad.dst_b(ib0);
-            if (ib0 + 8 <= rb) {
+#pragma unroll
+            for (int j = 0; j < EPW; ++j)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (ib0 + k < rb && ia0 + j >= lo)
+                        o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
+        };
+        if constexpr (!SHIFT) {
+#pragma unroll 1
+            for (int i = 0; i < ITEMS; ++i) {
+                const int x = w + 8 * i;
+                const int ib0 = 8 * RG * (x / STRIPES) + 8 * (l & (RG - 1));
+                const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
+                if (ib0 < rb && ia0 + EPW > lo) {
+                    const Cols cs = gather_item(ib0, ia0);
+                    const auto& col = cs.c;
+                    if (ib0 + 8 <= rb) {
+                        W* o = dst + ad.dst_b(ib0);
+#pragma unroll
+                        for (int j = 0; j < EPW; ++j) {
+                            if (ia0 + j < lo) continue;  // a shifted tile's columns of the previous tile
+                            W* oj = o + ad.dst_a(ia0 + j);
+                            if constexpr (sizeof(W) == 1)
+                                __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
+                            else
+                                __stcs(reinterpret_cast<uint4*>(oj),
+                                       make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+                        }
+                    } else {
+                        store_ragged(ib0, ia0, cs);
+                    }
+                }
+            }
+        } else {
+            // Destination columns that do not start on an 8-byte boundary:
+            // column a of a set is 8 RG sizeof(W) consecutive destination
+            // bytes starting mu = (its address mod 8) past an aligned word.
+            // Lane q of the set holds U = sizeof(W) 8-byte units of it (rows
+            // 8q..8q+7); aligned word q U + h is the top mu bytes of the unit
+            // before it and the low 8 - mu bytes of unit h, so each lane gets
+            // its neighbour's last unit by one shuffle and writes whole aligned
+            // 8-byte words (two clamped funnel shifts over a window of three
+            // of the four 32-bit halves).  The first word of a set takes the
+            // top of the previous set's last unit (its carry, kept by lane 0
+            // from the same shuffle one item earlier) when this thread wrote
+            // that set, else its low 8 - mu bytes are written alone; likewise
+            // the last set of a thread writes the mu bytes that spill past its
+            // last word.  Those partial words (at most three aligned 1-, 2-
+            // and 4-byte stores each) meet the neighbouring tile's, which
+            // writes the other bytes.  Sets are warp-uniform, so every lane of
+            // a warp takes part in each shuffle.
+            constexpr int U = (int)sizeof(W);
+            constexpr int SET_ROWS = 8 * RG;
+            // a thread's consecutive items are consecutive sets of one stripe
+            constexpr bool CARRY = STRIPES == 8 && SETS > 1;
+            const int q = l & (RG - 1);
+            const int src_lane = (l & ~(RG - 1)) | ((q - 1) & (RG - 1));
+            uint32_t carry_lo[EPW], carry_hi[EPW];
+#pragma unroll
+            for (int j = 0; j < EPW; ++j) carry_lo[j] = carry_hi[j] = 0;
+#pragma unroll 1
+            for (int i = 0; i < ITEMS; ++i) {
+                const int x = w + 8 * i;
+                const int s0 = SET_ROWS * (x / STRIPES);  // warp-uniform
+                if (s0 >= rb) continue;
+                const int ib0 = s0 + 8 * q;
+                const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
+                const Cols cs = gather_item(ib0, ia0);
+                const auto& col = cs.c;
+                if (s0 + SET_ROWS > rb) {
+                    if (ib0 < rb && ia0 + EPW > lo) store_ragged(ib0, ia0, cs);
+                    continue;
+                }
+                // warp-uniform: this set starts a thread's run of sets (its
+                // first word is partial) / ends one (the bytes past its last
+                // word are written here)
+                const bool first = !(CARRY && i > 0);
+                const bool last = !(CARRY && i + 1 < ITEMS && s0 + 2 * SET_ROWS <= rb);
+                W* o = dst + ad.dst_b(ib0);
 #pragma unroll
                 for (int j = 0; j < EPW; ++j) {
-                    if (ia0 + j < lo) continue;  // a shifted tile's columns of the previous tile
-                    W* oj = o + ad.dst_a(ia0 + j);
-                    if constexpr (sizeof(W) == 1)
-                        __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
-                    else
-                        __stcs(reinterpret_cast<uint4*>(oj), make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+                    // the neighbour's last unit; lane 0 receives lane RG - 1's,
+                    // the carry of the next item
+                    const uint32_t r_lo = __shfl_sync(0xffffffffu, col[j][2 * U - 2], src_lane);
+                    const uint32_t r_hi = __shfl_sync(0xffffffffu, col[j][2 * U - 1], src_lane);
+                    const uint32_t b_lo = q ? r_lo : carry_lo[j], b_hi = q ? r_hi : carry_hi[j];
+                    carry_lo[j] = r_lo;
+                    carry_hi[j] = r_hi;
+                    unsigned char* pb = reinterpret_cast<unsigned char*>(o + ad.dst_a(ia0 + j));
+                    const int mu = (int)((uintptr_t)pb & 7u);
+                    unsigned char* pw = pb - mu;  // aligned word holding the lane's first byte
+                    // word = bytes off..off+7 of (below, unit), off = 8 - mu:
+                    // halves (z0, z1) below, (z2, z3) the unit
+                    const int off = 8 - mu;
+                    const bool up = off >= 4;
+                    const uint32_t sh = 8u * (uint32_t)(up ? off - 4 : off);  // 0..32, clamped
+                    const bool keep = ia0 + j >= lo;  // not a shifted tile's column of the previous tile
+#pragma unroll
+                    for (int h = 0; h < U; ++h) {
+                        const uint32_t z0 = h ? col[j][2 * h - 2] : b_lo, z1 = h ? col[j][2 * h - 1] : b_hi;
+                        const uint32_t z2 = col[j][2 * h], z3 = col[j][2 * h + 1];
+                        const uint32_t a = up ? z1 : z0, b = up ? z2 : z1, c = up ? z3 : z2;
+                        const uint2 word = make_uint2(__funnelshift_rc(a, b, sh), __funnelshift_rc(b, c, sh));
+                        if (keep && (h || q || !first)) __stcs(reinterpret_cast<uint2*>(pw + 8 * h), word);
+                    }
+                    // the partial words (rare: only where a run of sets starts
+                    // or ends), under warp-uniform branches
+                    if (__builtin_expect(first, 0)) {
+                        if (keep && q == 0) store_head8(pb, ((uint64_t)col[j][1] << 32) | col[j][0], mu);
+                    }
+                    if (__builtin_expect(last, 0)) {
+                        if (keep && q == RG - 1 && mu)
+                            store_tail8(pw + 8 * U,
+                                        (((uint64_t)col[j][2 * U - 1] << 32) | col[j][2 * U - 2]) >> (64 - 8 * mu), mu);
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < EPW; ++j)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        if (ib0 + k < rb && ia0 + j >= lo)
-                            o[ad.dst_a(ia0 + j) + k] =
-                                (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
-            }
-        };
-#pragma unroll 1
-        for (int i = 0; i < ITEMS; ++i) {
-            const int x = w + 8 * i;
-            const int ib0 = 8 * RG * (x / STRIPES) + 8 * (l & (RG - 1));
-            const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
-            if (ib0 < rb && ia0 + EPW > lo) {
-                if (uni)
-                    item(ib0, ia0, std::true_type{});
-                else
-                    item(ib0, ia0, std::false_type{});
             }
         }
         return;
@@ -888,15 +1023,17 @@ __global__ void __launch_bounds__(256)
 // along A (consecutive source addresses), stores it into a padded shared
 // tile, and writes it out with lanes along B (consecutive destination
 // addresses).  Row pitch TA + PAD makes the column reads conflict-free.
-// Tile index = ta + tiles_a * (tb + tiles_b * batch).  Ragged edges are
-// masked.
+// Tile index = ta + tiles_a * (tb + tiles_b * batch) (tb + tiles_b * (ta +
+// tiles_a * batch) for realigned packs).  Ragged edges are masked.
 // MODE: bit 0 = multi-dimension groups (offset tables, else linear
 // offsets), bit 1 = tiles with the default shape whose A side is whole take
 // the 16-byte chunk path, bit 2 = that path writes 16-byte packs along B,
 // bit 3 = the chunk path with 128-byte source rows (8 chunks) instead of 256,
 // bit 4 = tall tiles (1-byte pack path, 256-byte rows): four times the rows,
 // 256 x 128, with ragged-A tiles taken by the element path a quarter at a
-// time.
+// time, bit 6 = the 1- and 2-byte pack path for destination columns that
+// are not 16-byte aligned (realigned to 8-byte words by lane shuffles; set
+// with bit 2).  Bit 5 is the launcher's 64-bit offset flag.
 enum {
     kTileLinear = 0,
     kTileTables = 1,
@@ -904,12 +1041,17 @@ enum {
     kTileTablesChunked = 3,
     kTilePack = 4,
     kTileHalfRows = 8,
-    kTileTall = 16
+    kTileTall = 16,
+    kTileShift = 64
 };
 
 template <typename W, int MODE>
 constexpr int tile_min_blocks() {
-    return (MODE & kTileTall)   ? 4
+    // the realigned packs hold more per column (carries, shifts): 76 and 64
+    // registers without spills (the 64-register tall version spilled and ran
+    // 15% slower)
+    return (MODE & kTileTall)    ? ((MODE & kTileShift) ? 3 : 4)
+           : (MODE & kTileShift) ? 4
            : (MODE & kTilePack) ? (sizeof(W) == 1 ? ((MODE & kTileTables) ? 5 : LMAD_BYTE_BLOCKS) : sizeof(W) == 2 ? 5 : 4)
            : (MODE & kTileChunked) ? 6
                                    : (sizeof(W) == 4 ? 8 : 6);
@@ -941,17 +1083,31 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
     constexpr bool PACK = (MODE & kTilePack) != 0;
+    constexpr bool SHIFT = (MODE & kTileShift) != 0;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
     for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
+        // tiles along A fastest; the realigned packs take tiles along B
+        // fastest, so the two tiles that write the halves of a destination
+        // sector at their common B edge run at the same time
         I x = (I)blk;
-        I q = div_q(x, p.div_ta);
-        const I ta = x - q * (I)p.div_ta.d;
-        x = q;
-        q = div_q(x, p.div_tb);
-        const I tb = x - q * (I)p.div_tb.d;
-        x = q;
+        I ta, tb, q;
+        if constexpr (SHIFT) {
+            q = div_q(x, p.div_tb);
+            tb = x - q * (I)p.div_tb.d;
+            x = q;
+            q = div_q(x, p.div_ta);
+            ta = x - q * (I)p.div_ta.d;
+            x = q;
+        } else {
+            q = div_q(x, p.div_ta);
+            ta = x - q * (I)p.div_ta.d;
+            x = q;
+            q = div_q(x, p.div_tb);
+            tb = x - q * (I)p.div_tb.d;
+            x = q;
+        }
         O so = 0, d = 0;
         for (int k = 0; k < p.nc; ++k) {
             I r = x;
@@ -1015,7 +1171,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const TabAddr<O> ad{tab_src, tab_dst, TA, 0};
             if (CHUNKED && ra == TA) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb, lo);
+                    tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb, lo);
             } else if constexpr (TALL > 1) {
                 // a ragged-A tall tile: the element path, a quarter of the rows at a time
                 constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
@@ -1034,7 +1190,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, NCH, TALL>(src, dst, tile, ad, rb, lo);
+                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(src, dst, tile, ad, rb, lo);
             } else if constexpr (TALL > 1) {
                 constexpr int QB = S::T >> 8;
                 for (int j = 0; j * QB < rb; ++j) {
@@ -1615,13 +1771,24 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     // packs along B: B walks the destination forwards from stride +1, and
     // every A and batch destination stride and the origin are 16-byte
     // aligned
-    bool pack = chunked && (LMAD_TILE_PACK_WORDS & sizeof(W)) != 0 && ((uintptr_t)out & 15) == 0;
-    for (int k = 0; pack && k < C.nb; ++k) pack = C.d[C.gb[k]].t > 0;
+    bool forward_b = chunked && (LMAD_TILE_PACK_WORDS & sizeof(W)) != 0;
+    for (int k = 0; forward_b && k < C.nb; ++k) forward_b = C.d[C.gb[k]].t > 0;
+    bool pack = forward_b && ((uintptr_t)out & 15) == 0;
     for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * sizeof(W)) % 16 == 0;
     for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
+    // otherwise 1- and 2-byte words still take the register path, with each
+    // destination column realigned to 8-byte words by lane shuffles
+    // (only when group A fills a tile: shorter groups never reach the chunk
+    // path, and the element path keeps its own occupancy)
+    const bool shift = LMAD_TILE_SHIFT && forward_b && !pack && sizeof(W) <= 2 && n_a >= (1ull << C.la);
     // tall tiles (256 x 128) for 1-byte packs with 256-byte rows and a long B
-    const bool tall = LMAD_BYTE_TALL && sizeof(W) == 1 && pack && row_bytes == 256 && C.lb == 5 && n_b >= 256;
-    const int la = C.la, lb = C.lb + (tall ? 2 : 0);
+    const bool tall =
+        LMAD_BYTE_TALL && sizeof(W) == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 256;
+    // realigned 2-byte packs take 64 x 128 tiles (128-byte source rows), so a
+    // thread's two items are the two row sets of one column stripe and the
+    // carry joins them (partial words once per 128 rows instead of per 64)
+    const bool halve = shift && sizeof(W) == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
+    const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (halve ? 1 : 0);
     const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + (1ull << lb) - 1) >> lb;
     const uint64_t tiles = tiles_a * tiles_b * batch;
     // masked lanes of a ragged tile form (unused) offsets up to one tile side
@@ -1667,8 +1834,8 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
     const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
-                     (pack ? kTilePack : 0) | (chunked && row_bytes == 128 ? kTileHalfRows : 0) |
-                     (tall ? kTileTall : 0);
+                     (pack || shift ? kTilePack : 0) | (shift ? kTileShift : 0) |
+                     (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0);
     constexpr int kWide = 32;
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
     if constexpr (sizeof(W) == 1) {
@@ -1684,6 +1851,10 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                 case 23: LMAD_TALL(false, 23); break;
                 case 54: LMAD_TALL(true, 22); break;
                 case 55: LMAD_TALL(true, 23); break;
+                case 86: LMAD_TALL(false, 86); break;
+                case 87: LMAD_TALL(false, 87); break;
+                case 118: LMAD_TALL(true, 86); break;
+                case 119: LMAD_TALL(true, 87); break;
                 default: return cudaErrorInvalidValue;
             }
 #undef LMAD_TALL
@@ -1709,7 +1880,22 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                 case 46: LMAD_TILE(true, 14); break;
                 case 43: LMAD_TILE(true, 11); break;
                 case 47: LMAD_TILE(true, 15); break;
-                default: return cudaErrorInvalidValue;
+                default:
+                    if constexpr (sizeof(W) <= 2) {
+                        switch (mode | (wide ? kWide : 0)) {
+                            case 70: LMAD_TILE(false, 70); break;
+                            case 71: LMAD_TILE(false, 71); break;
+                            case 78: LMAD_TILE(false, 78); break;
+                            case 79: LMAD_TILE(false, 79); break;
+                            case 102: LMAD_TILE(true, 70); break;
+                            case 103: LMAD_TILE(true, 71); break;
+                            case 110: LMAD_TILE(true, 78); break;
+                            case 111: LMAD_TILE(true, 79); break;
+                            default: return cudaErrorInvalidValue;
+                        }
+                        break;
+                    }
+                    return cudaErrorInvalidValue;
             }
             return cudaGetLastError();
         }

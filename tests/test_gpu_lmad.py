@@ -304,6 +304,48 @@ def test_two_byte_transposes_through_registers_with_tables():
     _check(w, 2)
 
 
+@pytest.mark.parametrize("elem", [1, 2])
+@pytest.mark.parametrize("case", [
+    dict(R=64, C=512, out_pitch=67),                      # every column at its own misalignment
+    dict(R=64, C=512, out_off=1),                         # one misalignment for all columns
+    dict(R=37, C=600, out_pitch=41, out_off=3),           # partial row groups, a ragged set
+    dict(R=130, C=256, out_pitch=133),                    # whole sets, then a ragged one
+    dict(R=300, C=1000, out_pitch=301),                   # tall byte tiles, ragged A and B
+    dict(R=1000, C=777, in_off=1, in_pitch=779, out_pitch=1001, out_off=5),
+    dict(R=512, C=128, out_pitch=515),                    # 128-byte source rows (bytes)
+    dict(R=520, C=512, in_off=5, out_pitch=523, out_off=1),
+    dict(R=1024, C=64, in_off=2, out_pitch=1027),         # 128-byte source rows (2-byte words)
+])
+def test_transposes_into_unaligned_destination_columns(elem, case):
+    """1- and 2-byte transposes whose destination columns do not start on a
+    16-byte boundary: the register path writes each column as aligned 8-byte
+    words, realigned by lane shuffles, with narrow stores only at the edges
+    of a tile's column segment (which meet the neighbouring tile's)."""
+    w = _byte_transpose_view(**case)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and not q["narrow"]
+    _check(w, elem)
+    _check(w, elem, seed=11)
+
+
+@pytest.mark.parametrize("elem", [1, 2])
+def test_unaligned_destination_columns_with_tables(elem):
+    """The realigned register path with offset tables: group A spans two
+    source dimensions whose destination strides (33 and 2113 elements) do
+    not collapse, plus a batch dimension."""
+    w = dict(sizes=[32, 4, 64], in_offset=0, in_strides=[256, 64, 1], in_elems=32 * 256, out_offset=0,
+             out_strides=[1, 2113, 33], out_elems=3 * 2113 + 63 * 33 + 32)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and len(q["group_a"]) == 2
+    _check(w, elem)
+    w = dict(sizes=[3, 300, 4, 64], in_offset=1, in_strides=[300 * 256, 256, 64, 1], in_elems=1 + 3 * 300 * 256,
+             out_offset=7, out_strides=[4 * 64 * 303 + 5, 1, 64 * 303, 303], out_elems=7 + 3 * (4 * 64 * 303 + 5))
+    _check(w, elem)
+    _check(w, elem, seed=3)
+
+
 def test_byte_transposes_through_registers_with_tables():
     """The same path with offset tables: group A spans two dimensions that
     do not collapse (a padded destination), and a batch dimension."""
