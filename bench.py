@@ -607,6 +607,8 @@ def other_configs(torch, bm, synth, dev, stream):
     # 4-byte pixels and 16-byte vectors (moved as words)
     for name, shape, perm, elem in (("nhwc2nchw_32x1024x1024x3_uint8", (32, 1024, 1024, 3), (0, 3, 1, 2), 1),
                                     ("nhwc2nchw_8x512x512x64_fp16", (8, 512, 512, 64), (0, 3, 1, 2), 2),
+                                    ("nhwc2nchw_8x512x512x48_fp16", (8, 512, 512, 48), (0, 3, 1, 2), 2),
+                                    ("nhwc2nchw_4x512x512x100_uint8", (4, 512, 512, 100), (0, 3, 1, 2), 1),
                                     ("t2d_8192x8192_bf16", (8192, 8192), (1, 0), 2),
                                     ("t2d_16384x16384_uint8", (16384, 16384), (1, 0), 1),
                                     ("t2d_16384x16400_uint8", (16384, 16400), (1, 0), 1),

@@ -421,8 +421,10 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
     }
 }
 
-// The two phases of a tile of 4- or 8-byte words whose A side is whole (its
-// B side may be short: rows rb.. are skipped), with the default shape: 64 x
+// The two phases of a tile of 1- to 8-byte words whose A side is whole, or
+// holds all of a group A shorter than the tile (columns hi.. are neither
+// fetched, beyond the chunks holding valid columns, nor stored; its B side
+// may be short: rows rb.. are skipped), with the default shape: 64 x
 // 64 for 4-byte words, 32 x 32 for 8-byte words, so each source row segment
 // is 256 bytes, 16 chunks of 16 bytes (V = 16 / word elements each).  The
 // segment is fetched as 16-byte aligned chunks with cp.async, 16 lanes per
@@ -483,7 +485,7 @@ __device__ __forceinline__ void store_tail8(unsigned char* p, uint64_t v, int n)
 
 template <typename W, typename O, bool PACK, bool SHIFT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
-                                                    const Addr& ad, int rb, int lo) {
+                                                    const Addr& ad, int rb, int lo, int hi) {
     constexpr int V = 16 / (int)sizeof(W), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
@@ -518,8 +520,9 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const O s0 = ad.src_b(row);
         const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
         const int k = kk + (m != 0);
-        cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
-                      reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
+        if (V * k - m < hi)  // (chunks wholly past a short group A are not fetched)
+            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
+                          reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
     }
     if (!uni || base_mis != 0) {
 #pragma unroll
@@ -617,7 +620,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             for (int j = 0; j < EPW; ++j)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    if (ib0 + k < rb && ia0 + j >= lo)
+                    if (ib0 + k < rb && ia0 + j >= lo && ia0 + j < hi)
                         o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
         };
         if constexpr (!SHIFT) {
@@ -626,14 +629,14 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                 const int x = w + 8 * i;
                 const int ib0 = 8 * RG * (x / STRIPES) + 8 * (l & (RG - 1));
                 const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
-                if (ib0 < rb && ia0 + EPW > lo) {
+                if (ib0 < rb && ia0 + EPW > lo && ia0 < hi) {
                     const Cols cs = gather_item(ib0, ia0);
                     const auto& col = cs.c;
                     if (ib0 + 8 <= rb) {
                         W* o = dst + ad.dst_b(ib0);
 #pragma unroll
                         for (int j = 0; j < EPW; ++j) {
-                            if (ia0 + j < lo) continue;  // a shifted tile's columns of the previous tile
+                            if (ia0 + j < lo || ia0 + j >= hi) continue;  // not this tile's column
                             W* oj = o + ad.dst_a(ia0 + j);
                             if constexpr (sizeof(W) == 1)
                                 __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
@@ -683,7 +686,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                 const Cols cs = gather_item(ib0, ia0);
                 const auto& col = cs.c;
                 if (s0 + SET_ROWS > rb) {
-                    if (ib0 < rb && ia0 + EPW > lo) store_ragged(ib0, ia0, cs);
+                    if (ib0 < rb && ia0 + EPW > lo && ia0 < hi) store_ragged(ib0, ia0, cs);
                     continue;
                 }
                 // warp-uniform: this set starts a thread's run of sets (its
@@ -709,7 +712,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     const int off = 8 - mu;
                     const bool up = off >= 4;
                     const uint32_t sh = 8u * (uint32_t)(up ? off - 4 : off);  // 0..32, clamped
-                    const bool keep = ia0 + j >= lo;  // not a shifted tile's column of the previous tile
+                    const bool keep = ia0 + j >= lo && ia0 + j < hi;  // one of this tile's columns
 #pragma unroll
                     for (int h = 0; h < U; ++h) {
                         const uint32_t z0 = h ? col[j][2 * h - 2] : b_lo, z1 = h ? col[j][2 * h - 1] : b_hi;
@@ -751,7 +754,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const bool whole = ib0 + V <= rb;
 #pragma unroll 1
         for (int ia = t >> LG; ia < TA; ia += 256 >> LG) {
-            if (ia < lo) continue;  // a shifted tile's columns of the previous tile
+            if (ia < lo || ia >= hi) continue;  // not this tile's column
             W v[V];
 #pragma unroll
             for (int k = 0; k < V; ++k) v[k] = tile[off[k] + ia];
@@ -780,7 +783,8 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         for (int r = 0; r < CH; ++r) v[r] = row[ia0 + kStep * (c0 + r)];
 #pragma unroll
         for (int r = 0; r < CH; ++r)
-            if (ia0 + kStep * (c0 + r) >= lo) __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
+            if (ia0 + kStep * (c0 + r) >= lo && ia0 + kStep * (c0 + r) < hi)
+                __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
     }
 }
 
@@ -1124,7 +1128,9 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
         int ra = (int)min((uint64_t)TA, p.n_a - (uint64_t)a0);
         const int rb = (int)min((uint64_t)TB, p.n_b - (uint64_t)b0);
         // the chunk path takes a ragged last A tile shifted back to end at
-        // n_a (whole again), storing only its last ra columns
+        // n_a (whole again), storing only its last ra columns; a group A
+        // shorter than one tile takes it too, fetching only the chunks that
+        // hold its ra columns and storing only those
         int lo = 0;
         if (CHUNKED && ra < TA && p.n_a >= (uint64_t)TA) {
             lo = TA - ra;
@@ -1169,9 +1175,10 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
         }
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA, 0};
-            if (CHUNKED && ra == TA) {
+            if (CHUNKED && (ra == TA || p.n_a < (uint64_t)TA)) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb, lo);
+                    tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb, lo,
+                                                                       ra);
             } else if constexpr (TALL > 1) {
                 // a ragged-A tall tile: the element path, a quarter of the rows at a time
                 constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
@@ -1189,8 +1196,9 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const LinAddr<O> ad{(O)p.bs[0], (O)p.at[0], (O)p.bt[0]};
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
-            if (CHUNKED && ra == TA) {
-                if constexpr (CHUNKED) tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(src, dst, tile, ad, rb, lo);
+            if (CHUNKED && (ra == TA || p.n_a < (uint64_t)TA)) {
+                if constexpr (CHUNKED)
+                    tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra);
             } else if constexpr (TALL > 1) {
                 constexpr int QB = S::T >> 8;
                 for (int j = 0; j * QB < rb; ++j) {
@@ -1778,9 +1786,7 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
     // otherwise 1- and 2-byte words still take the register path, with each
     // destination column realigned to 8-byte words by lane shuffles
-    // (only when group A fills a tile: shorter groups never reach the chunk
-    // path, and the element path keeps its own occupancy)
-    const bool shift = LMAD_TILE_SHIFT && forward_b && !pack && sizeof(W) <= 2 && n_a >= (1ull << C.la);
+    const bool shift = LMAD_TILE_SHIFT && forward_b && !pack && sizeof(W) <= 2;
     // tall tiles (256 x 128) for 1-byte packs with 256-byte rows and a long B
     const bool tall =
         LMAD_BYTE_TALL && sizeof(W) == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 256;

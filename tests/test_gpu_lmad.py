@@ -329,6 +329,23 @@ def test_transposes_into_unaligned_destination_columns(elem, case):
     _check(w, elem, seed=11)
 
 
+@pytest.mark.parametrize("elem", [1, 2, 4])
+@pytest.mark.parametrize("C", [17, 33, 48, 63, 100, 127, 200])
+@pytest.mark.parametrize("in_off,out_extra", [(0, 0), (3, 0), (0, 5), (5, 3)])
+def test_short_group_a_on_chunk_path(elem, C, in_off, out_extra):
+    """Transposes whose source rows are shorter than a tile side (NHWC ->
+    NCHW with tens of channels): the chunk path fetches only the aligned
+    chunks that hold a row's C elements and stores only those columns, with
+    aligned and misaligned source rows and destination columns."""
+    R = 300
+    w = _byte_transpose_view(R, C, in_off=in_off, out_pitch=R + out_extra)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose"  # (a group A longer than a tile side: the shifted last tile)
+    _check(w, elem)
+    _check(w, elem, seed=2)
+
+
 @pytest.mark.parametrize("elem", [1, 2])
 def test_unaligned_destination_columns_with_tables(elem):
     """The realigned register path with offset tables: group A spans two
