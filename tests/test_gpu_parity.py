@@ -82,6 +82,32 @@ def test_every_bmmc_of_tiny_size(bm, n, elem):
     assert cases == (1 << n) * {1: 1, 2: 6, 3: 168}[n]
 
 
+@pytest.mark.parametrize("elem", [4, 16])
+def test_every_invertible_matrix_at_n4(bm, elem):
+    """All 20160 invertible 4 x 4 bit matrices on the GPU, c cycling through
+    the 16 complements, plus every complement for every eighth matrix
+    (57,960 maps in all); each output lands in its own slice of one device
+    buffer, checked against the oracle after one synchronisation."""
+    n = 4
+    arr = synth.fill_int(n, elem)
+    mats = [list(A) for A in itertools.product(range(16), repeat=4) if ref.f2_rank(4, list(A)) == 4]
+    assert len(mats) == 20160  # |GL(4, 2)|
+    cases = []
+    for k, A in enumerate(mats):
+        cs = range(16) if k % 8 == 0 else [k % 16]
+        cases.extend((A, c) for c in cs)
+    d_in = _dev(arr)
+    d_out = torch.zeros(len(cases) * arr.nbytes, dtype=torch.uint8, device="cuda")
+    for k, (A, c) in enumerate(cases):
+        with bm.Plan(A, c, elem) as p:
+            p.permute(d_in, d_out[k * arr.nbytes:(k + 1) * arr.nbytes])
+    torch.cuda.synchronize()
+    got = d_out.cpu().numpy().reshape(len(cases), arr.nbytes)
+    for k, (A, c) in enumerate(cases):
+        want = oracle.scatter(n, A, c, arr)
+        assert got[k].tobytes() == want.tobytes(), (A, c)
+
+
 @pytest.mark.parametrize("elem", [4, 8, 16])
 @pytest.mark.parametrize("n", [4, 5, 7, 9, 11, 12, 13, 14, 15, 17, 19, 21])
 def test_random_bmmc_moderate_sizes(bm, n, elem):
