@@ -483,7 +483,7 @@ __device__ __forceinline__ void store_tail8(unsigned char* p, uint64_t v, int n)
     if (n & 1) __stcs(p, (unsigned char)v);
 }
 
-template <typename W, typename O, bool PACK, bool SHIFT, int NCH, int TALL, typename Addr>
+template <typename W, typename O, bool PACK, bool SHIFT, bool SHORT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
                                                     const Addr& ad, int rb, int lo, int hi) {
     constexpr int V = 16 / (int)sizeof(W), LNCH = clog2(NCH);
@@ -520,7 +520,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const O s0 = ad.src_b(row);
         const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
         const int k = kk + (m != 0);
-        if (V * k - m < hi)  // (chunks wholly past a short group A are not fetched)
+        if (!SHORT || V * k - m < hi)  // (chunks wholly past a short group A are not fetched)
             cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
                           reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
     }
@@ -620,7 +620,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             for (int j = 0; j < EPW; ++j)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    if (ib0 + k < rb && ia0 + j >= lo && ia0 + j < hi)
+                    if (ib0 + k < rb && ia0 + j >= lo && (!SHORT || ia0 + j < hi))
                         o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
         };
         if constexpr (!SHIFT) {
@@ -629,14 +629,14 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                 const int x = w + 8 * i;
                 const int ib0 = 8 * RG * (x / STRIPES) + 8 * (l & (RG - 1));
                 const int ia0 = EPW * ((x % STRIPES) * WL + l / RG);
-                if (ib0 < rb && ia0 + EPW > lo && ia0 < hi) {
+                if (ib0 < rb && ia0 + EPW > lo && (!SHORT || ia0 < hi)) {
                     const Cols cs = gather_item(ib0, ia0);
                     const auto& col = cs.c;
                     if (ib0 + 8 <= rb) {
                         W* o = dst + ad.dst_b(ib0);
 #pragma unroll
                         for (int j = 0; j < EPW; ++j) {
-                            if (ia0 + j < lo || ia0 + j >= hi) continue;  // not this tile's column
+                            if (ia0 + j < lo || (SHORT && ia0 + j >= hi)) continue;  // not this tile's column
                             W* oj = o + ad.dst_a(ia0 + j);
                             if constexpr (sizeof(W) == 1)
                                 __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
@@ -686,7 +686,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                 const Cols cs = gather_item(ib0, ia0);
                 const auto& col = cs.c;
                 if (s0 + SET_ROWS > rb) {
-                    if (ib0 < rb && ia0 + EPW > lo && ia0 < hi) store_ragged(ib0, ia0, cs);
+                    if (ib0 < rb && ia0 + EPW > lo && (!SHORT || ia0 < hi)) store_ragged(ib0, ia0, cs);
                     continue;
                 }
                 // warp-uniform: this set starts a thread's run of sets (its
@@ -712,7 +712,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     const int off = 8 - mu;
                     const bool up = off >= 4;
                     const uint32_t sh = 8u * (uint32_t)(up ? off - 4 : off);  // 0..32, clamped
-                    const bool keep = ia0 + j >= lo && ia0 + j < hi;  // one of this tile's columns
+                    const bool keep = ia0 + j >= lo && (!SHORT || ia0 + j < hi);  // one of this tile's columns
 #pragma unroll
                     for (int h = 0; h < U; ++h) {
                         const uint32_t z0 = h ? col[j][2 * h - 2] : b_lo, z1 = h ? col[j][2 * h - 1] : b_hi;
@@ -754,7 +754,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const bool whole = ib0 + V <= rb;
 #pragma unroll 1
         for (int ia = t >> LG; ia < TA; ia += 256 >> LG) {
-            if (ia < lo || ia >= hi) continue;  // not this tile's column
+            if (ia < lo || (SHORT && ia >= hi)) continue;  // not this tile's column
             W v[V];
 #pragma unroll
             for (int k = 0; k < V; ++k) v[k] = tile[off[k] + ia];
@@ -783,7 +783,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         for (int r = 0; r < CH; ++r) v[r] = row[ia0 + kStep * (c0 + r)];
 #pragma unroll
         for (int r = 0; r < CH; ++r)
-            if (ia0 + kStep * (c0 + r) >= lo && ia0 + kStep * (c0 + r) < hi)
+            if (ia0 + kStep * (c0 + r) >= lo && (!SHORT || ia0 + kStep * (c0 + r) < hi))
                 __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
     }
 }
@@ -1037,7 +1037,9 @@ __global__ void __launch_bounds__(256)
 // 256 x 128, with ragged-A tiles taken by the element path a quarter at a
 // time, bit 6 = the 1- and 2-byte pack path for destination columns that
 // are not 16-byte aligned (realigned to 8-byte words by lane shuffles; set
-// with bit 2).  Bit 5 is the launcher's 64-bit offset flag.
+// with bit 2), bit 7 = group A is shorter than one tile (its one tile along A
+// takes the chunk path, fetching and storing only its columns).  Bit 5 is the
+// launcher's 64-bit offset flag.
 enum {
     kTileLinear = 0,
     kTileTables = 1,
@@ -1046,7 +1048,8 @@ enum {
     kTilePack = 4,
     kTileHalfRows = 8,
     kTileTall = 16,
-    kTileShift = 64
+    kTileShift = 64,
+    kTileShort = 128
 };
 
 template <typename W, int MODE>
@@ -1088,6 +1091,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
     constexpr bool PACK = (MODE & kTilePack) != 0;
     constexpr bool SHIFT = (MODE & kTileShift) != 0;
+    constexpr bool SHORT = (MODE & kTileShort) != 0;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
@@ -1175,10 +1179,10 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
         }
         if constexpr (GENERAL) {
             const TabAddr<O> ad{tab_src, tab_dst, TA, 0};
-            if (CHUNKED && (ra == TA || p.n_a < (uint64_t)TA)) {
+            if (CHUNKED && (ra == TA || SHORT)) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad, rb, lo,
-                                                                       ra);
+                    tile_phases_chunked<W, O, PACK, SHIFT, SHORT, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad,
+                                                                              rb, lo, ra);
             } else if constexpr (TALL > 1) {
                 // a ragged-A tall tile: the element path, a quarter of the rows at a time
                 constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
@@ -1196,9 +1200,9 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const LinAddr<O> ad{(O)p.bs[0], (O)p.at[0], (O)p.bt[0]};
             const W* src = in + so + (O)a0 + (O)b0 * ad.sb;
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
-            if (CHUNKED && (ra == TA || p.n_a < (uint64_t)TA)) {
+            if (CHUNKED && (ra == TA || SHORT)) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, SHIFT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra);
+                    tile_phases_chunked<W, O, PACK, SHIFT, SHORT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra);
             } else if constexpr (TALL > 1) {
                 constexpr int QB = S::T >> 8;
                 for (int j = 0; j * QB < rb; ++j) {
@@ -1839,9 +1843,13 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
+    // a group A shorter than one tile takes the chunk path in kernels of its
+    // own (32-bit offsets; with 64-bit ones its tiles take the element path)
+    const bool short_a = chunked && sizeof(W) <= 4 && n_a < (1ull << la) && !wide;
     const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
                      (pack || shift ? kTilePack : 0) | (shift ? kTileShift : 0) |
-                     (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0);
+                     (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0) |
+                     (short_a ? kTileShort : 0);
     constexpr int kWide = 32;
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
     if constexpr (sizeof(W) == 1) {
@@ -1861,9 +1869,40 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                 case 87: LMAD_TALL(false, 87); break;
                 case 118: LMAD_TALL(true, 86); break;
                 case 119: LMAD_TALL(true, 87); break;
+                case 150: LMAD_TALL(false, 150); break;
+                case 151: LMAD_TALL(false, 151); break;
+                case 214: LMAD_TALL(false, 214); break;
+                case 215: LMAD_TALL(false, 215); break;
                 default: return cudaErrorInvalidValue;
             }
 #undef LMAD_TALL
+            return cudaGetLastError();
+        }
+    }
+    if constexpr (sizeof(W) <= 4) {
+        if (mode & kTileShort) {
+            switch (mode) {
+                case 130: LMAD_TILE(false, 130); break;
+                case 131: LMAD_TILE(false, 131); break;
+                case 138: LMAD_TILE(false, 138); break;
+                case 139: LMAD_TILE(false, 139); break;
+                default:
+                    if constexpr (sizeof(W) <= 2) {
+                        switch (mode) {
+                            case 134: LMAD_TILE(false, 134); break;
+                            case 135: LMAD_TILE(false, 135); break;
+                            case 142: LMAD_TILE(false, 142); break;
+                            case 143: LMAD_TILE(false, 143); break;
+                            case 198: LMAD_TILE(false, 198); break;
+                            case 199: LMAD_TILE(false, 199); break;
+                            case 206: LMAD_TILE(false, 206); break;
+                            case 207: LMAD_TILE(false, 207); break;
+                            default: return cudaErrorInvalidValue;
+                        }
+                        break;
+                    }
+                    return cudaErrorInvalidValue;
+            }
             return cudaGetLastError();
         }
     }
