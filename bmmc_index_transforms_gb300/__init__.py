@@ -261,7 +261,9 @@ def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[i
             "group_a": [i for i in range(k) if (info.group_a >> i) & 1],
             "group_b": [i for i in range(k) if (info.group_b >> i) & 1],
             "tile": (int(info.tile_a), int(info.tile_b)), "narrow": int(info.narrow),
-            "elements": int(info.elements)}
+            "elements": int(info.elements),
+            "tile_mode": [name for name, bit in _capi.LMAD_TILE_FLAGS.items() if info.tile_mode & bit],
+            "launch_tile": (int(info.launch_tile_a), int(info.launch_tile_b))}
 
 
 def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,

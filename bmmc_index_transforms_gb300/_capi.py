@@ -68,7 +68,13 @@ class LmadCopyInfo(ctypes.Structure):
                 ("out_strides", ctypes.c_int64 * LMAD_MAX_DIMS), ("in_offset", ctypes.c_int64),
                 ("out_offset", ctypes.c_int64), ("vec", ctypes.c_int), ("transpose_out_dim", ctypes.c_int),
                 ("group_a", ctypes.c_uint32), ("group_b", ctypes.c_uint32), ("tile_a", ctypes.c_int),
-                ("tile_b", ctypes.c_int), ("narrow", ctypes.c_int), ("elements", ctypes.c_uint64)]
+                ("tile_b", ctypes.c_int), ("narrow", ctypes.c_int), ("elements", ctypes.c_uint64),
+                ("tile_mode", ctypes.c_uint32), ("launch_tile_a", ctypes.c_int), ("launch_tile_b", ctypes.c_int)]
+
+
+# lmad_copy_info_t.tile_mode flags
+LMAD_TILE_FLAGS = {"tables": 0x01, "chunked": 0x02, "packs": 0x04, "half_rows": 0x08, "tall": 0x10, "wide": 0x20,
+                   "realigned": 0x40, "short_a": 0x80}
 
 
 # name -> (restype, argtypes); every function declared in include/bmmc.h

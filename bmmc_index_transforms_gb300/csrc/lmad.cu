@@ -1048,9 +1048,15 @@ enum {
     kTilePack = 4,
     kTileHalfRows = 8,
     kTileTall = 16,
+    kTileWide = 32,  // 64-bit offsets: the launcher's key bit, never a kernel MODE bit
     kTileShift = 64,
     kTileShort = 128
 };
+
+static_assert(kTileTables == LMAD_TILE_TABLES && kTileChunked == LMAD_TILE_CHUNKED && kTilePack == LMAD_TILE_PACKS &&
+                  kTileHalfRows == LMAD_TILE_HALF_ROWS && kTileTall == LMAD_TILE_TALL && kTileWide == LMAD_TILE_WIDE &&
+                  kTileShift == LMAD_TILE_REALIGNED && kTileShort == LMAD_TILE_SHORT_A,
+              "the query reports the kernel's mode bits as the header's flags");
 
 template <typename W, int MODE>
 constexpr int tile_min_blocks() {
@@ -1766,9 +1772,17 @@ cudaError_t allow_tall_tile() {
     return e;
 }
 
-template <typename W>
-cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStream_t stream) {
-    if (C.narrow) return launch_narrow_w(in, out, C, stream);
+// How the general tile kernel runs one transpose of words of `word` bytes
+// into the destination origin `out`: its mode bits (kTile* and kWide), the
+// tile sides it launches with and the tile counts.
+struct TileLaunch {
+    int mode;        // kTile* | kWide
+    int la, lb;      // log2 tile sides at launch
+    uint64_t n_a, n_b, batch, tiles_a, tiles_b, tiles;
+};
+
+TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
+    TileLaunch L{};
     uint64_t n_a = 1, n_b = 1, batch = 1;
     for (int k = 0; k < C.na; ++k) n_a *= (uint64_t)C.d[C.ga[k]].n;
     for (int k = 0; k < C.nb; ++k) n_b *= (uint64_t)C.d[C.gb[k]].n;
@@ -1777,27 +1791,26 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     // bytes (a group A of up to half that), 1- to 4-byte words (8-byte words
     // measured slower on it: 32 x 32 tiles, 83-85% of a copy against 85-90%
     // element-wise; LMAD_TILE_CHUNKS=2 enables them)
-    const uint64_t row_bytes = (1ull << C.la) * sizeof(W);
-    const bool chunked = (LMAD_TILE_CHUNKS && (sizeof(W) <= 4 || LMAD_TILE_CHUNKS == 2) && sizeof(W) <= 8 &&
+    const uint64_t row_bytes = (1ull << C.la) * word;
+    const bool chunked = (LMAD_TILE_CHUNKS && (word <= 4 || LMAD_TILE_CHUNKS == 2) && word <= 8 &&
                           (row_bytes == 256 || row_bytes == 128) && (1ull << C.lb) <= 256);
     // packs along B: B walks the destination forwards from stride +1, and
     // every A and batch destination stride and the origin are 16-byte
     // aligned
-    bool forward_b = chunked && (LMAD_TILE_PACK_WORDS & sizeof(W)) != 0;
+    bool forward_b = chunked && (LMAD_TILE_PACK_WORDS & word) != 0;
     for (int k = 0; forward_b && k < C.nb; ++k) forward_b = C.d[C.gb[k]].t > 0;
-    bool pack = forward_b && ((uintptr_t)out & 15) == 0;
-    for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * sizeof(W)) % 16 == 0;
-    for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * sizeof(W)) % 16 == 0;
+    bool pack = forward_b && (out & 15) == 0;
+    for (int k = 0; pack && k < C.na; ++k) pack = (iabs(C.d[C.ga[k]].t) * word) % 16 == 0;
+    for (int k = 0; pack && k < C.nc; ++k) pack = (iabs(C.d[C.gc[k]].t) * word) % 16 == 0;
     // otherwise 1- and 2-byte words still take the register path, with each
     // destination column realigned to 8-byte words by lane shuffles
-    const bool shift = LMAD_TILE_SHIFT && forward_b && !pack && sizeof(W) <= 2;
+    const bool shift = LMAD_TILE_SHIFT && forward_b && !pack && word <= 2;
     // tall tiles (256 x 128) for 1-byte packs with 256-byte rows and a long B
-    const bool tall =
-        LMAD_BYTE_TALL && sizeof(W) == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 256;
+    const bool tall = LMAD_BYTE_TALL && word == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 256;
     // realigned 2-byte packs take 64 x 128 tiles (128-byte source rows), so a
     // thread's two items are the two row sets of one column stripe and the
     // carry joins them (partial words once per 128 rows instead of per 64)
-    const bool halve = shift && sizeof(W) == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
+    const bool halve = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
     const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (halve ? 1 : 0);
     const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + (1ull << lb) - 1) >> lb;
     const uint64_t tiles = tiles_a * tiles_b * batch;
@@ -1812,6 +1825,31 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     const bool wide = tiles > 0xFFFFFFFFull || n_a > 0xFFFFFFFFull || n_b > 0xFFFFFFFFull ||
                       span_of(C.d, C.nd, false) + slack_in > 0x7FFFFFFFull ||
                       span_of(C.d, C.nd, true) + slack_out > 0x7FFFFFFFull;
+    // a group A shorter than one tile takes the chunk path in kernels of its
+    // own (32-bit offsets; with 64-bit ones its tiles take the element path)
+    const bool short_a = chunked && word <= 4 && n_a < (1ull << la) && !wide;
+    L.mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
+             (pack || shift ? kTilePack : 0) | (shift ? kTileShift : 0) |
+             (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0) |
+             (short_a ? kTileShort : 0) | (wide ? kTileWide : 0);
+    L.la = la;
+    L.lb = lb;
+    L.n_a = n_a;
+    L.n_b = n_b;
+    L.batch = batch;
+    L.tiles_a = tiles_a;
+    L.tiles_b = tiles_b;
+    L.tiles = tiles;
+    return L;
+}
+
+template <typename W>
+cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStream_t stream) {
+    if (C.narrow) return launch_narrow_w(in, out, C, stream);
+    const TileLaunch L = tile_launch(C, sizeof(W), (uintptr_t)out);
+    const bool wide = (L.mode & kTileWide) != 0;
+    const int la = L.la, lb = L.lb;
+    const uint64_t n_a = L.n_a, n_b = L.n_b, tiles_a = L.tiles_a, tiles_b = L.tiles_b, tiles = L.tiles;
     const int bits = wide ? 64 : 32;
     LmadTileParams p{};
     p.tiles = tiles;
@@ -1843,14 +1881,8 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         p.ct[k] = x.t;
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
-    // a group A shorter than one tile takes the chunk path in kernels of its
-    // own (32-bit offsets; with 64-bit ones its tiles take the element path)
-    const bool short_a = chunked && sizeof(W) <= 4 && n_a < (1ull << la) && !wide;
-    const int mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
-                     (pack || shift ? kTilePack : 0) | (shift ? kTileShift : 0) |
-                     (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0) |
-                     (short_a ? kTileShort : 0);
-    constexpr int kWide = 32;
+    const int mode = L.mode & ~kTileWide;
+    constexpr int kWide = kTileWide;
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
     if constexpr (sizeof(W) == 1) {
         if (mode & kTileTall) {
@@ -2030,6 +2062,14 @@ extern "C" bmmc_status lmad_copy_query(int ndims, const int64_t* sizes, int64_t 
         r.narrow = C.narrow;
         if (C.narrow == 1) r.tile_a = (int)C.d[C.ga[0]].n, r.tile_b = 1 << C.lt;
         if (C.narrow == 2) r.tile_a = 1 << C.lt, r.tile_b = (int)C.d[C.gb[0]].n;
+        if (!C.narrow) {
+            const size_t word = elem_size * (size_t)C.vec;
+            const LmadCopy& V = C.vec > 1 ? word_view(C) : C;
+            const TileLaunch L = tile_launch(V, word, (uintptr_t)out + (uintptr_t)(C.out_off * (int64_t)elem_size));
+            r.tile_mode = (uint32_t)L.mode;
+            r.launch_tile_a = 1 << L.la;
+            r.launch_tile_b = 1 << L.lb;
+        }
     }
     r.elements = C.elements;
     *info = r;

@@ -383,7 +383,28 @@ typedef struct {
                                           side, moved with 16-byte accesses; 0 = the general
                                           tile kernel */
     uint64_t elements;                 /* index tuples copied (product of the sizes) */
+    uint32_t tile_mode;                /* TRANSPOSE on the general tile kernel (narrow == 0): how
+                                          it runs, a combination of the LMAD_TILE_* flags below
+                                          (decided from the destination's alignment too, so a
+                                          query without the out pointer assumes a 16-byte
+                                          aligned one); 0 for other kinds */
+    int launch_tile_a, launch_tile_b;  /* TRANSPOSE on the general tile kernel: the tile sides
+                                          it launches with (tall byte tiles and realigned 2-byte
+                                          tiles differ from tile_a x tile_b); 0 otherwise */
 } lmad_copy_info_t;
+
+/* lmad_copy_info_t.tile_mode flags (the general tile kernel's variants). */
+#define LMAD_TILE_TABLES    0x01u  /* multi-dimension groups: per-tile offset tables */
+#define LMAD_TILE_CHUNKED   0x02u  /* source rows fetched as aligned 16-byte chunks */
+#define LMAD_TILE_PACKS     0x04u  /* 1- and 2-byte words: register transposes written in packs
+                                      along B */
+#define LMAD_TILE_HALF_ROWS 0x08u  /* 128-byte source rows instead of 256 */
+#define LMAD_TILE_TALL      0x10u  /* 256 x 128 byte tiles */
+#define LMAD_TILE_WIDE      0x20u  /* 64-bit offsets */
+#define LMAD_TILE_REALIGNED 0x40u  /* packs realigned to 8-byte words (destination columns not
+                                      16-byte aligned) */
+#define LMAD_TILE_SHORT_A   0x80u  /* group A shorter than one tile: only its columns fetched
+                                      and stored */
 
 /* Analyse the copy lmad_copy would run with the same arguments, without
  * touching memory or the device.  in / out are used for their alignment and

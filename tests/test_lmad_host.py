@@ -391,3 +391,63 @@ def test_lmad_copy_tensor_argument_checks():
         bm.lmad_copy_tensor(torch.zeros(3, 4), torch.zeros(4, 3))
     with pytest.raises(ValueError):
         bm.lmad_copy_tensor(torch.zeros(3, 4), torch.zeros(3, 4, dtype=torch.float64))
+
+
+def _transpose_2d(R, C, out_off=0, out_pitch=None):
+    out_pitch = out_pitch or R
+    return dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C,
+                out_offset=out_off, out_strides=[1, out_pitch], out_elems=out_off + (C - 1) * out_pitch + R)
+
+
+@pytest.mark.parametrize("R,C,elem,out_off,out_pitch,mode,launch_tile", [
+    # aligned byte transpose with a long B: register packs in 256 x 128 tiles
+    (16384, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
+    # destination columns at odd offsets: the packs are realigned
+    (16385, 16384, 1, 0, None, {"chunked", "packs", "tall", "realigned"}, (256, 128)),
+    (16384, 16384, 1, 3, None, {"chunked", "packs", "tall", "realigned"}, (256, 128)),
+    # a short B keeps 256 x 32 tiles
+    (32, 16384, 1, 0, None, {"chunked", "packs"}, (256, 32)),
+    # 2-byte words: aligned packs in 128 x 64 tiles; realigned ones in 64 x 128
+    (8192, 8192, 2, 0, None, {"chunked", "packs"}, (128, 64)),
+    (11585, 11587, 2, 0, None, {"chunked", "packs", "half_rows", "realigned"}, (64, 128)),
+    # groups A shorter than a tile take the chunk path in their own kernels
+    (300, 48, 2, 0, 304, {"chunked", "packs", "half_rows", "short_a"}, (64, 128)),
+    (300, 48, 2, 0, None, {"chunked", "packs", "half_rows", "realigned", "short_a"}, (64, 128)),
+    (300, 100, 1, 0, 304, {"chunked", "packs", "half_rows", "short_a"}, (128, 64)),
+    (300, 17, 4, 0, None, {"chunked", "half_rows", "short_a"}, (32, 128)),
+    # 4-byte words: chunks, element stores; 8-byte words: the element path
+    (8191, 8193, 4, 0, None, {"chunked"}, (64, 64)),
+    (100, 100, 8, 0, None, set(), (32, 32)),
+])
+def test_tile_kernel_variant_choice(R, C, elem, out_off, out_pitch, mode, launch_tile):
+    """The query reports the tile kernel variant a transpose launches with:
+    register packs when B walks the destination forwards from stride 1 (1- and
+    2-byte words), realigned when a destination column is not 16-byte
+    aligned, tall byte tiles for a long B, 64 x 128 tiles for realigned 2-byte
+    words, separate kernels for a group A shorter than a tile."""
+    w = _transpose_2d(R, C, out_off, out_pitch)
+    q = _query(w, elem)
+    assert q["kind"] == "transpose" and not q["narrow"]
+    assert set(q["tile_mode"]) == mode and q["launch_tile"] == launch_tile
+    ta, tb = q["launch_tile"]
+    assert ta * tb == TILE_ELEMS[elem] * (4 if "tall" in mode else 1)
+
+
+def test_tile_kernel_variant_follows_destination_alignment():
+    """The same copy into a destination whose origin is 16-byte aligned takes
+    aligned packs, into one 8 bytes off it realigned packs (the query reads
+    the alignment from the out address)."""
+    w = _transpose_2d(4096, 4096)
+    assert "realigned" not in _query(w, 1, out=1 << 20)["tile_mode"]
+    assert "realigned" in _query(w, 1, out=(1 << 20) + 8)["tile_mode"]
+
+
+def test_tile_kernel_variant_with_64_bit_offsets():
+    """A span past 2^31 elements takes 64-bit offsets, and a short group A
+    then stays on the element path."""
+    w = dict(sizes=[1 << 26, 48], in_offset=0, in_strides=[48, 1], in_elems=48 << 26,
+             out_offset=0, out_strides=[1, 1 << 26], out_elems=48 << 26)
+    q = _query(w, 2)
+    assert q["kind"] == "transpose" and "wide" in q["tile_mode"] and "short_a" not in q["tile_mode"]
+    q = _query(_transpose_2d(1 << 16, 1 << 16), 1)
+    assert "wide" in q["tile_mode"] and "tall" in q["tile_mode"]
