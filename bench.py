@@ -609,6 +609,7 @@ def other_configs(torch, bm, synth, dev, stream):
                                     ("nhwc2nchw_8x512x512x64_fp16", (8, 512, 512, 64), (0, 3, 1, 2), 2),
                                     ("nhwc2nchw_8x512x512x48_fp16", (8, 512, 512, 48), (0, 3, 1, 2), 2),
                                     ("nhwc2nchw_4x512x512x100_uint8", (4, 512, 512, 100), (0, 3, 1, 2), 1),
+                                    ("reverse_axes_8x512x512x48_fp16", (8, 512, 512, 48), (3, 2, 1, 0), 2),
                                     ("t2d_8192x8192_bf16", (8192, 8192), (1, 0), 2),
                                     ("t2d_16384x16384_uint8", (16384, 16384), (1, 0), 1),
                                     ("t2d_16384x16400_uint8", (16384, 16400), (1, 0), 1),

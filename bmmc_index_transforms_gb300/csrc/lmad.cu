@@ -1398,14 +1398,36 @@ void choose_groups(LmadCopy& C, size_t word) {
     }
     C.gb[C.nb++] = C.tdim;
     used[C.tdim] = true;
-    for (;;) {
-        const Dim& l = C.d[C.gb[C.nb - 1]];
-        int next = -1;
-        for (int k = 0; k < C.nd && next < 0; ++k)
-            if (!used[k] && iabs(C.d[k].t) == iabs(l.t) * (uint64_t)l.n) next = k;
-        if (next < 0) break;
-        C.gb[C.nb++] = next;
-        used[next] = true;
+    auto extend_b = [&]() {
+        for (;;) {
+            const Dim& l = C.d[C.gb[C.nb - 1]];
+            int next = -1;
+            for (int k = 0; k < C.nd && next < 0; ++k)
+                if (!used[k] && iabs(C.d[k].t) == iabs(l.t) * (uint64_t)l.n) next = k;
+            if (next < 0) break;
+            C.gb[C.nb++] = next;
+            used[next] = true;
+        }
+    };
+    extend_b();
+    // A's outermost dimension, when it also continues B in the destination,
+    // goes to B while B is shorter than its tile side (an axis reversal of
+    // [8, 512, 512, 48] would otherwise leave B the 8 outer rows and most of
+    // every tile empty)
+    {
+        int lt0, la0, lb0;
+        tile_shape_log2(word, &lt0, &la0, &lb0);
+        uint64_t nb = 1;
+        for (int k = 0; k < C.nb; ++k) nb *= (uint64_t)C.d[C.gb[k]].n;
+        while (nb < (1ull << lb0) && C.na > 1) {
+            const int cand = C.ga[C.na - 1];
+            const Dim& l = C.d[C.gb[C.nb - 1]];
+            if (iabs(C.d[cand].t) != iabs(l.t) * (uint64_t)l.n) break;
+            --C.na;
+            C.gb[C.nb++] = cand;
+            nb *= (uint64_t)C.d[cand].n;
+            extend_b();
+        }
     }
     for (int k = 0; k < C.nd; ++k)
         if (!used[k]) C.gc[C.nc++] = k;

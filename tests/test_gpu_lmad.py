@@ -87,7 +87,11 @@ def test_page_workloads_full_size(kind, shape):
 
 @pytest.mark.parametrize("shape,perm", [((33, 65), (1, 0)), ((5, 31, 97), (0, 2, 1)), ((31, 5, 97), (2, 1, 0)),
                                         ((3, 40, 7, 70), (1, 3, 0, 2)), ((2, 3, 4, 5, 6, 7), (5, 3, 1, 0, 2, 4)),
-                                        ((1000, 3), (1, 0)), ((3, 1000), (1, 0)), ((1, 64, 1, 96), (3, 1, 2, 0))])
+                                        ((1000, 3), (1, 0)), ((3, 1000), (1, 0)), ((1, 64, 1, 96), (3, 1, 2, 0)),
+                                        # axis reversals (numpy's .T) with short outer dimensions: B takes
+                                        # the dimension it shares with A
+                                        ((8, 60, 70, 48), (3, 2, 1, 0)), ((6, 50, 40, 3), (3, 2, 1, 0)),
+                                        ((4, 33, 65, 17), (3, 2, 1, 0)), ((2, 3, 40, 50, 24), (4, 3, 2, 1, 0))])
 @pytest.mark.parametrize("elem", [1, 2, 4, 8, 16])
 def test_axis_permutations_any_sizes(shape, perm, elem):
     """x.permute(perm) made contiguous for odd shapes: the destination's
