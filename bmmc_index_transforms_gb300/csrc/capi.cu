@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <new>
 
@@ -161,18 +162,59 @@ bmmc_status run_plan(const bmmc_plan_s* p, const void* in, void* out, void* scra
     return from_cuda(launch_pass(p->second_pass, scratch, out, st));
 }
 
-// Plan on the stack, run once (convenience entry points).
+// Default single-pass plans of the convenience entry points (transpose2d,
+// bpc_permute, bmmc_dims_permute and the BPC route of the LMAD copies),
+// kept for reuse: planning takes tens of microseconds of host time, more
+// than the kernel of a small array.  A built plan is immutable and may run
+// on several streams and threads at once; entries are shared, so an entry
+// replaced while another thread runs it lives until that run returns.
+struct CachedPlan {
+    int n = 0;
+    uint64_t c = 0;
+    size_t elem = 0;
+    uint64_t rows[64] = {};
+    std::shared_ptr<bmmc_plan_s> plan;
+};
+constexpr size_t kPlanCacheSize = 32;
+std::mutex g_plan_cache_mu;
+CachedPlan g_plan_cache[kPlanCacheSize];
+size_t g_plan_cache_next = 0;  // replaced round robin
+
+std::shared_ptr<bmmc_plan_s> cached_plan(int n, const uint64_t* rows, uint64_t c, size_t elem, bmmc_status* s) {
+    {
+        std::lock_guard<std::mutex> lk(g_plan_cache_mu);
+        for (const CachedPlan& e : g_plan_cache)
+            if (e.plan && e.n == n && e.c == c && e.elem == elem &&
+                std::memcmp(e.rows, rows, sizeof(uint64_t) * (size_t)n) == 0)
+                return e.plan;
+    }
+    bmmc_plan_s* p = new (std::nothrow) bmmc_plan_s();
+    if (!p) {
+        *s = BMMC_ERR_INTERNAL;
+        return nullptr;
+    }
+    std::shared_ptr<bmmc_plan_s> sp(p, [](bmmc_plan_s* q) { bmmc_plan_destroy(q); });
+    if ((*s = build_plan(p, n, rows, c, elem, nullptr)) != BMMC_OK) return nullptr;
+    std::lock_guard<std::mutex> lk(g_plan_cache_mu);
+    CachedPlan& e = g_plan_cache[g_plan_cache_next];
+    g_plan_cache_next = (g_plan_cache_next + 1) % kPlanCacheSize;
+    e.n = n;
+    e.c = c;
+    e.elem = elem;
+    std::memcpy(e.rows, rows, sizeof(uint64_t) * (size_t)n);
+    e.plan = sp;
+    return sp;
+}
+
+// Plan (or reuse a plan) and run once (convenience entry points).
 bmmc_status permute_once(int n, const uint64_t* rows, uint64_t c, size_t elem, const void* in,
                          void* out, void* stream) {
     if (!valid_elem(elem)) return BMMC_ERR_UNSUPPORTED_ELEM;
     bmmc_status s = check_matrix(n, rows, c);
     if (s != BMMC_OK) return s;
-    bmmc_plan_s* p = new (std::nothrow) bmmc_plan_s();
-    if (!p) return BMMC_ERR_INTERNAL;
-    s = build_plan(p, n, rows, c, elem, nullptr);
-    if (s == BMMC_OK) s = run_plan(p, in, out, nullptr, stream);
-    delete p;
-    return s;
+    const std::shared_ptr<bmmc_plan_s> p = cached_plan(n, rows, c, elem, &s);
+    if (!p) return s;
+    return run_plan(p.get(), in, out, nullptr, stream);
 }
 
 }  // namespace

@@ -1452,6 +1452,16 @@ void choose_groups(LmadCopy& C, size_t word) {
     C.lb = lb;
 }
 
+// Group A shorter than half the tile's smallest side (T / 256 elements).
+bool tiny_group_a(const LmadCopy& C, size_t word) {
+    int lt, la, lb;
+    tile_shape_log2(word, &lt, &la, &lb);
+    const int lmin = lt - std::min(lt - 4, 8);
+    uint64_t n_a = 1;
+    for (int k = 0; k < C.na; ++k) n_a *= (uint64_t)C.d[C.ga[k]].n;
+    return n_a < (1ull << lmin) / 2;
+}
+
 // The narrow-transpose kernel applies when both groups are one dimension,
 // one of them of at most 16 elements continues the other contiguously on
 // its unit-stride side (A: the wide dimension's source stride is n; B: the
@@ -1605,6 +1615,10 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
                     C.tdim = b;
                     choose_groups(C, elem);
                     choose_narrow(C, elem);
+                    // a group A of a few elements would fill a sliver of
+                    // every tile (its side is at least T / 256): the
+                    // stride-sorted copy moves exactly the elements
+                    if (!C.narrow && tiny_group_a(C, elem)) C.kind = LMAD_COPY_STRIDED;
                     break;
                 }
         } else if (C.d[0].s == 1 && C.d[0].t == 1 && nd >= 3) {
