@@ -1841,8 +1841,10 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     // otherwise 1- and 2-byte words still take the register path, with each
     // destination column realigned to 8-byte words by lane shuffles
     const bool shift = LMAD_TILE_SHIFT && forward_b && !pack && word <= 2;
-    // tall tiles (256 x 128) for 1-byte packs with 256-byte rows and a long B
-    const bool tall = LMAD_BYTE_TALL && word == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 256;
+    // tall tiles (256 x 128) for 1-byte packs with 256-byte rows and a B of
+    // at least 64 rows (a ragged last tall tile works only on its rows;
+    // measured no slower than 256 x 32 tiles from 64 rows up)
+    const bool tall = LMAD_BYTE_TALL && word == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 64;
     // realigned 2-byte packs take 64 x 128 tiles (128-byte source rows), so a
     // thread's two items are the two row sets of one column stripe and the
     // carry joins them (partial words once per 128 rows instead of per 64)

@@ -266,6 +266,8 @@ def _byte_transpose_view(R, C, in_off=0, in_pitch=None, out_off=0, out_pitch=Non
     dict(R=400, C=1000, out_pitch=416),                   # a 16-row last tile
     dict(R=1000, C=777, in_off=1, in_pitch=779, out_pitch=1008),
     dict(R=520, C=512, in_off=4), dict(R=520, C=512, in_off=5),
+    dict(R=128, C=1000), dict(R=128, C=512, in_off=3),   # B of exactly one tall tile
+    dict(R=64, C=1000), dict(R=96, C=777, in_off=1, in_pitch=779, out_pitch=112),  # one ragged tall tile
 ])
 def test_byte_transposes_through_registers(case):
     """1-byte transposes whose destination takes packs (16-byte aligned A

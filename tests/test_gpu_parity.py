@@ -710,3 +710,39 @@ def test_one_plan_from_several_threads_and_streams(bm):
         with ThreadPoolExecutor(4) as ex:
             results = list(ex.map(work, range(4)))
     assert all(all(r) for r in results)
+
+
+def test_convenience_calls_share_plans_across_threads(bm):
+    """transpose2d / bpc_permute / bmmc_dims_permute keep their plans in a
+    shared cache of 32: eight threads, each on its own stream, run 48
+    different bit permutations (more than the cache holds, so entries are
+    replaced while other threads run them) three times over; every output is
+    the oracle's."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    n, elem = 14, 4
+    arr = synth.fill_int(n, elem)
+    rng = np.random.default_rng(5)
+    perms = [list(rng.permutation(n)) for _ in range(48)]
+    wants = []
+    for perm in perms:
+        rows = [1 << int(p) for p in perm]
+        wants.append(oracle.scatter(n, rows, 0, arr).tobytes())
+
+    def work(t):
+        s = torch.cuda.Stream()
+        d_in = _dev(arr)
+        ok = []
+        for rep in range(3):
+            for k in range(t, t + len(perms)):
+                perm = perms[k % len(perms)]
+                d_out = torch.zeros_like(d_in)
+                with torch.cuda.stream(s):
+                    bm.bpc_permute(n, [int(p) for p in perm], 0, elem, d_in, d_out, s)
+                s.synchronize()
+                ok.append(_host(d_out, arr).tobytes() == wants[k % len(perms)])
+        return ok
+
+    with ThreadPoolExecutor(8) as ex:
+        results = list(ex.map(work, range(8)))
+    assert all(all(r) for r in results)

@@ -405,8 +405,11 @@ def _transpose_2d(R, C, out_off=0, out_pitch=None):
     # destination columns at odd offsets: the packs are realigned
     (16385, 16384, 1, 0, None, {"chunked", "packs", "tall", "realigned"}, (256, 128)),
     (16384, 16384, 1, 3, None, {"chunked", "packs", "tall", "realigned"}, (256, 128)),
-    # a short B keeps 256 x 32 tiles
+    # a B of under 64 rows keeps 256 x 32 tiles
     (32, 16384, 1, 0, None, {"chunked", "packs"}, (256, 32)),
+    (48, 16384, 1, 0, None, {"chunked", "packs"}, (256, 32)),
+    (64, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
+    (160, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
     # 2-byte words: aligned packs in 128 x 64 tiles; realigned ones in 64 x 128
     (8192, 8192, 2, 0, None, {"chunked", "packs"}, (128, 64)),
     (11585, 11587, 2, 0, None, {"chunked", "packs", "half_rows", "realigned"}, (64, 128)),
