@@ -807,6 +807,14 @@ __global__ void __launch_bounds__(256)
     constexpr int P = 16 / (int)sizeof(W);  // elements per 16-byte word
     __shared__ __align__(16) unsigned char smem_bytes[16384];
     W* smem = reinterpret_cast<W*>(smem_bytes);
+    // The block sits in shared memory as 16-byte chunks placed by an XOR
+    // swizzle, chunk c at c ^ ((c >> 3) & 7): the scatter (narrow B) and the
+    // gather (narrow A) touch one element per 16-byte group of the wide side,
+    // n elements apart, which without it puts a warp's 32 accesses in one bank
+    // for 8-element rows of bytes and the like.  Chunks stay whole, so the
+    // 16-byte phases still move whole chunks.
+    auto swz = [](int c) { return c ^ ((c >> 3) & 7); };
+    auto at = [&](int e) -> W& { return smem[swz(e / P) * P + e % P]; };
     const int t = threadIdx.x;
     const int n = p.n;
     for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
@@ -834,11 +842,11 @@ __global__ void __launch_bounds__(256)
             if (p.vec_load) {
                 const int chunks = nb / P;
                 for (int c = t; c < chunks; c += 256)
-                    cp_async_word(reinterpret_cast<uint4*>(smem) + c, reinterpret_cast<const uint4*>(blkp) + c);
+                    cp_async_word(reinterpret_cast<uint4*>(smem) + swz(c), reinterpret_cast<const uint4*>(blkp) + c);
                 done = chunks * P;
                 asm volatile("cp.async.wait_all;" ::: "memory");
             }
-            for (int e = done + t; e < nb; e += 256) smem[e] = blkp[e];
+            for (int e = done + t; e < nb; e += 256) at(e) = blkp[e];
             __syncthreads();
             W* dbase = out + d + w0;
             const int groups = p.vec_store ? rw / P : 0;
@@ -846,15 +854,15 @@ __global__ void __launch_bounds__(256)
                 W* drow = dbase + ia * (int32_t)p.stride;
                 for (int g = t; g < groups; g += 256) {
                     if constexpr (P == 1) {
-                        __stcs(drow + g, smem[g * n + ia]);
+                        __stcs(drow + g, at(g * n + ia));
                     } else {
                         W v[P];
 #pragma unroll
-                        for (int k = 0; k < P; ++k) v[k] = smem[(g * P + k) * n + ia];
+                        for (int k = 0; k < P; ++k) v[k] = at((g * P + k) * n + ia);
                         __stcs(reinterpret_cast<uint4*>(drow) + g, *reinterpret_cast<const uint4*>(v));
                     }
                 }
-                for (int iw = groups * P + t; iw < rw; iw += 256) __stcs(drow + iw, smem[iw * n + ia]);
+                for (int iw = groups * P + t; iw < rw; iw += 256) __stcs(drow + iw, at(iw * n + ia));
             }
         } else {
             const W* sbase = in + so + w0;  // source row ib at sbase + ib * stride, contiguous along the wide index
@@ -863,15 +871,15 @@ __global__ void __launch_bounds__(256)
                 const W* srow = sbase + ib * (int32_t)p.stride;
                 for (int g = t; g < groups; g += 256) {
                     if constexpr (P == 1) {
-                        smem[g * n + ib] = __ldg(srow + g);
+                        at(g * n + ib) = __ldg(srow + g);
                     } else {
                         W v[P];
                         *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(srow) + g);
 #pragma unroll
-                        for (int k = 0; k < P; ++k) smem[(g * P + k) * n + ib] = v[k];
+                        for (int k = 0; k < P; ++k) at((g * P + k) * n + ib) = v[k];
                     }
                 }
-                for (int iw = groups * P + t; iw < rw; iw += 256) smem[iw * n + ib] = __ldg(srow + iw);
+                for (int iw = groups * P + t; iw < rw; iw += 256) at(iw * n + ib) = __ldg(srow + iw);
             }
             __syncthreads();
             W* blkp = out + d + w0 * n;  // contiguous destination block
@@ -879,10 +887,10 @@ __global__ void __launch_bounds__(256)
             if (p.vec_store) {
                 const int chunks = nb / P;
                 for (int c = t; c < chunks; c += 256)
-                    __stcs(reinterpret_cast<uint4*>(blkp) + c, reinterpret_cast<const uint4*>(smem)[c]);
+                    __stcs(reinterpret_cast<uint4*>(blkp) + c, reinterpret_cast<const uint4*>(smem)[swz(c)]);
                 done = chunks * P;
             }
-            for (int e = done + t; e < nb; e += 256) __stcs(blkp + e, smem[e]);
+            for (int e = done + t; e < nb; e += 256) __stcs(blkp + e, at(e));
         }
         __syncthreads();
     }
@@ -1468,7 +1476,8 @@ bool tiny_group_a(const LmadCopy& C, size_t word) {
 // wide dimension's destination stride is n), the destination stride along
 // the wide (A narrow) or narrow (B narrow) dimension is +1, and 32-bit
 // offsets hold every span.  Tile length: the largest power of two with
-// n * 2^lt elements in 16 KiB.
+// n * 2^lt elements in 16 KiB, and no longer than needed for the wide
+// dimension (at least 16).
 uint64_t span_of(const Dim* d, int nd, bool dest);
 
 void choose_narrow(LmadCopy& C, size_t elem) {
@@ -1487,8 +1496,11 @@ void choose_narrow(LmadCopy& C, size_t elem) {
     } else {
         return;
     }
+    // the longest tile in 16 KiB, but no longer than the wide dimension
+    // (a tile of 2048 wide indices over 100 would be 95 % empty)
+    const Dim& w = C.narrow == 1 ? b : a;
     int lt = 4;
-    while (lt < 20 && (uint64_t)n * (2ull << lt) * elem <= 16384) ++lt;
+    while (lt < 20 && (uint64_t)n * (2ull << lt) * elem <= 16384 && (1ull << lt) < (uint64_t)w.n) ++lt;
     C.lt = lt;
 }
 
