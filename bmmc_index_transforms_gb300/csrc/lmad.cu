@@ -846,7 +846,16 @@ __global__ void __launch_bounds__(256)
                 done = chunks * P;
                 asm volatile("cp.async.wait_all;" ::: "memory");
             }
-            for (int e = done + t; e < nb; e += 256) at(e) = blkp[e];
+            // (four loads in flight before their shared stores)
+            int e = done + t;
+            for (; e + 3 * 256 < nb; e += 4 * 256) {
+                W v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = blkp[e + u * 256];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) at(e + u * 256) = v[u];
+            }
+            for (; e < nb; e += 256) at(e) = blkp[e];
             __syncthreads();
             W* dbase = out + d + w0;
             const int groups = p.vec_store ? rw / P : 0;
@@ -879,7 +888,20 @@ __global__ void __launch_bounds__(256)
                         for (int k = 0; k < P; ++k) at((g * P + k) * n + ib) = v[k];
                     }
                 }
-                for (int iw = groups * P + t; iw < rw; iw += 256) at(iw * n + ib) = __ldg(srow + iw);
+            }
+            // the wide indices past the 16-byte groups (all of them when the
+            // rows are not 16-byte aligned), four rows' loads in flight before
+            // their shared stores
+            for (int iw = groups * P + t; iw < rw; iw += 256) {
+                int ib = 0;
+                for (; ib + 4 <= n; ib += 4) {
+                    W v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[u] = __ldg(sbase + (ib + u) * (int32_t)p.stride + iw);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) at(iw * n + ib + u) = v[u];
+                }
+                for (; ib < n; ++ib) at(iw * n + ib) = __ldg(sbase + ib * (int32_t)p.stride + iw);
             }
             __syncthreads();
             W* blkp = out + d + w0 * n;  // contiguous destination block
