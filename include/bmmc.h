@@ -429,7 +429,12 @@ bmmc_status lmad_copy_query(int ndims, const int64_t *sizes, int64_t in_offset,
 /* Run the copy (arguments as lmad_copy_query; in holds in_elems and out
  * out_elems elements of elem_size bytes, caller-owned, reachable by the GPU
  * as for bmmc_permute).  Enqueued on `stream`, no allocation, no CPU
- * fallback.  Errors as lmad_copy_query, plus CUDA. */
+ * fallback.  Errors as lmad_copy_query, plus CUDA.  Some source reads are
+ * whole aligned 16-byte words that hold at least one element the copy reads:
+ * they may touch up to 15 bytes next to those elements (in the same 16-byte
+ * granule, hence the same page; never written, never used), which a memory
+ * checker tracking allocation sizes to the byte may report at the very ends
+ * of an allocation.  Only destination elements of the LMAD are written. */
 bmmc_status lmad_copy(int ndims, const int64_t *sizes, int64_t in_offset,
                       const int64_t *in_strides, size_t in_elems, int64_t out_offset,
                       const int64_t *out_strides, size_t out_elems, size_t elem_size,
