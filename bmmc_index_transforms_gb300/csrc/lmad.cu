@@ -97,7 +97,7 @@ struct LmadNarrowParams {
     uint64_t tiles;            // tiles along the wide dimension x batch
     LmadDiv div_tw;            // tiles along the wide dimension
     uint64_t n_wide;           // size of the wide dimension
-    int n;                     // size of the narrow dimension (<= 16)
+    int n;                     // size of the narrow dimension (<= 31)
     int lt;                    // log2 of the tile length along the wide dimension
     int64_t stride;            // narrow A: destination stride of A; narrow B: source stride of B
     int vec_load, vec_store;   // 16-byte paths allowed (host-checked alignment)
@@ -1493,7 +1493,8 @@ bool tiny_group_a(const LmadCopy& C, size_t word) {
 }
 
 // The narrow-transpose kernel applies when both groups are one dimension,
-// one of them of at most 16 elements continues the other contiguously on
+// one of them of at most 16 elements (group A of 1- or 2-byte words: 31)
+// continues the other contiguously on
 // its unit-stride side (A: the wide dimension's source stride is n; B: the
 // wide dimension's destination stride is n), the destination stride along
 // the wide (A narrow) or narrow (B narrow) dimension is +1, and 32-bit
@@ -1508,8 +1509,14 @@ void choose_narrow(LmadCopy& C, size_t elem) {
     const Dim& a = C.d[C.ga[0]];
     const Dim& b = C.d[C.gb[0]];
     if (span_of(C.d, C.nd, false) > 0x3FFFFFFFull || span_of(C.d, C.nd, true) > 0x3FFFFFFFull) return;
+    // narrow sides of up to 16 elements; a narrow group A of 1- or 2-byte
+    // words up to 31 elements, whose short rows the tile kernel moves element
+    // by element in a tile 32 wide (17-24 elements: 18-28 % of a copy there,
+    // 46-53 % here; at 32 the tile is full and faster, and so it is for
+    // 8-byte words)
+    const int64_t max_a = elem <= 2 ? 31 : 16;
     int n = 0;
-    if (a.n <= 16 && b.s == a.n && b.t == 1) {
+    if (a.n <= max_a && b.s == a.n && b.t == 1) {
         C.narrow = 1;
         n = (int)a.n;
     } else if (b.n <= 16 && a.t == b.n && b.t == 1) {

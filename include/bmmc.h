@@ -376,8 +376,9 @@ typedef struct {
                                           batch index), powers of two except the narrow side
                                           of a narrow transpose; 0 for other kinds */
     int narrow;                        /* TRANSPOSE: 1 = group A is one dimension of at most 16
-                                          elements that continues group B contiguously in the
-                                          source, 2 = group B is such a dimension continuing A
+                                          elements (31 for elem_size 1 and 2) that
+                                          continues group B contiguously in the
+                                          source, 2 = group B is such a dimension (at most 16) continuing A
                                           in the destination (e.g. NHWC <-> NCHW with few
                                           channels): each tile is one contiguous block on that
                                           side, moved with 16-byte accesses; 0 = the general

@@ -572,16 +572,18 @@ def test_image_layout_conversions(elem, c, hw, offsets):
         _check(case, elem, seed=c * 7 + elem)
 
 
-@pytest.mark.parametrize("elem,c", [(2, 64), (4, 32), (1, 128), (2, 32), (4, 48), (1, 96)])
+@pytest.mark.parametrize("elem,c", [(2, 64), (4, 32), (1, 128), (2, 32), (4, 48), (1, 96), (1, 24), (2, 17), (8, 20),
+                                    (16, 32)])
 @pytest.mark.parametrize("offsets", [(0, 0), (1, 2)])
 def test_mid_channel_layouts(elem, c, offsets):
     """NHWC -> NCHW with 32 to 128 channels (source rows of 64 to 128 bytes:
-    the tile kernel's chunk path with 128-byte rows where it applies),
-    aligned and not, against the oracle."""
+    the tile kernel's chunk path with 128-byte rows where it applies, the
+    narrow kernel for 17 to 31 channels of 1- and 2-byte words, whose short
+    rows the chunk path does not take), aligned and not, against the oracle."""
     case = _layout_case((2, 37, 45, c), (0, 3, 1, 2), *offsets)
     q = bm.lmad_copy_query(case["sizes"], case["in_offset"], case["in_strides"], case["out_offset"],
                            case["out_strides"], elem, in_elems=case["in_elems"], out_elems=case["out_elems"])
-    assert q["kind"] == "transpose" and q["narrow"] == 0
+    assert q["kind"] == "transpose" and q["narrow"] == (1 if c < 32 and elem <= 2 else 0)
     _check(case, elem, seed=c + elem)
 
 
