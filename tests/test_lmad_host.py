@@ -454,3 +454,43 @@ def test_tile_kernel_variant_with_64_bit_offsets():
     assert q["kind"] == "transpose" and "wide" in q["tile_mode"] and "short_a" not in q["tile_mode"]
     q = _query(_transpose_2d(1 << 16, 1 << 16), 1)
     assert "wide" in q["tile_mode"] and "tall" in q["tile_mode"]
+
+
+def test_axis_reversal_gives_b_the_shared_dimension():
+    """Reversing every axis of [8, 512, 512, 48] (numpy's .T): group A would
+    take 48 x 512 x 512 and leave B the 8 outer rows; B takes the dimension
+    that continues it in the destination instead, and the tiles are full."""
+    q = _query(_perm_view((8, 512, 512, 48), (3, 2, 1, 0)), 2)
+    assert q["kind"] == "transpose" and not q["narrow"]
+    sizes = [d[0] for d in q["dims"]]
+    assert [sizes[k] for k in q["group_a"]] == [48, 512]
+    assert sorted(sizes[k] for k in q["group_b"]) == [8, 512]
+    assert q["launch_tile"] == (128, 64) and {"chunked", "packs"} <= set(q["tile_mode"])
+    # a B already as long as its tile side keeps its dimensions
+    q = _query(_perm_view((64, 512, 512, 48), (3, 2, 1, 0)), 2)
+    assert [q["dims"][k][0] for k in q["group_b"]] == [64]
+
+
+def test_tiny_group_a_takes_the_stride_sorted_copy():
+    """A group A of 2 bytes would fill a sliver of every 32-wide tile: the
+    copy runs on the stride-sorted kernel; a group A at the limit (16 of a
+    32-wide tile) stays a transpose."""
+    assert _query(_perm_view((384, 4096, 2, 12, 2), (4, 0, 2, 1, 3)), 1)["kind"] == "strided"
+    q = _query(_perm_view((64, 300, 2, 16), (0, 3, 1, 2)), 1)
+    assert q["kind"] == "transpose"
+
+
+@pytest.mark.parametrize("c,elem,narrow", [
+    (16, 1, 1), (17, 1, 1), (24, 1, 1), (31, 1, 1), (32, 1, 0),   # bytes: narrow A up to 31
+    (17, 2, 1), (31, 2, 1), (32, 2, 0),                           # 2-byte words the same
+    (16, 4, 1), (17, 4, 0), (24, 4, 0),                           # 4-byte rows of 17+ take the chunk path
+    (17, 8, 0), (20, 16, 0),                                      # 8- and 16-byte words stay at 16
+])
+def test_narrow_group_limits(c, elem, narrow):
+    """NHWC -> NCHW with c channels: a narrow group A of 1- or 2-byte words
+    may have up to 31 elements, other words 16; NCHW -> NHWC (a narrow
+    group B) stays at 16."""
+    q = _query(_perm_view((4, 64, 96, c), (0, 3, 1, 2)), elem)
+    assert q["kind"] == "transpose" and q["narrow"] == narrow
+    q = _query(_perm_view((4, c, 64, 96), (0, 2, 3, 1)), elem)
+    assert q["kind"] == "transpose" and q["narrow"] == (2 if c <= 16 else 0)
