@@ -449,3 +449,37 @@ def test_concurrent_planning_from_threads():
         results = list(ex.map(plan_all, range(8)))
     for r in results:
         assert r == want
+
+
+def test_convenience_plan_cache_from_threads():
+    """bpc_permute plans (or reuses a plan from its 32-entry cache) before it
+    looks at the buffers.  Eight threads call it with 48 different bit
+    permutations, so entries are replaced while other threads use them: every
+    call returns the same status as a single call (on a machine without a GPU
+    the host buffers are refused with BMMC_ERR_CUDA after planning; where
+    the GPU can reach them the output is checked), and nothing crashes."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    L = _capi.lib()
+    n = 10
+    rng = np.random.default_rng(3)
+    perms = [[int(p) for p in rng.permutation(n)] for _ in range(48)]
+    src = np.arange(1 << n, dtype=np.uint32)
+
+    def work(t):
+        out = []
+        for k in range(t, t + 3 * len(perms)):
+            perm = perms[k % len(perms)]
+            dst = np.zeros_like(src)
+            pa = (ctypes.c_int * n)(*perm)
+            s = L.bpc_permute(n, pa, 0, 4, src.ctypes.data, dst.ctypes.data, None)
+            if s == _capi.OK:
+                want = ref.bmmc_permute(n, [1 << p for p in perm], 0, src)
+                out.append(dst.tobytes() == want.tobytes())
+            else:
+                out.append(s == _capi.ERR_CUDA)
+        return out
+
+    with ThreadPoolExecutor(8) as ex:
+        results = list(ex.map(work, range(8)))
+    assert all(all(r) for r in results)
