@@ -8,6 +8,7 @@ from the library.
 """
 
 import ctypes
+import itertools
 import math
 import os
 import re
@@ -483,3 +484,30 @@ def test_convenience_plan_cache_from_threads():
     with ThreadPoolExecutor(8) as ex:
         results = list(ex.map(work, range(8)))
     assert all(all(r) for r in results)
+
+
+@pytest.mark.parametrize("t", [1, 2])
+def test_two_factor_contract_for_every_4x4_matrix(t):
+    """The two-factor contract over all 20160 invertible 4 x 4 bit matrices
+    at runs of 2^t elements: A = T1 T2 (oracle product), both factors tiled
+    in the narrow sense (oracle predicate), T2 fixes the low t bits, and one
+    factor exactly when A itself is tiled."""
+    n = 4
+    mats = [list(A) for A in itertools.product(range(16), repeat=n) if ref.f2_rank(n, list(A)) == n]
+    assert len(mats) == 20160
+    ones = copies = 0
+    for A in mats:
+        with bm.Plan(A, 0, 16, t_in=t, t_out=t) as p:
+            if p.info["kernel_name"] == "copy":  # the identity: no tiles, one factor
+                assert A == ref.identity_rows(n) and p.info["r2_factors"] == 1
+                copies += 1
+                continue
+            assert p.info["t_out"] == t
+            T1, T2 = p.factor(1), p.factor(2)
+            assert ref.f2_matmul(n, T1, T2) == A, A
+            assert ref.r2_tiled(n, T1, t) and ref.r2_tiled(n, T2, t), A
+            assert all(ref.bmmc_index(n, T2, 0, 1 << j) == 1 << j for j in range(t)), A
+            tiled = ref.r2_tiled(n, A, t)
+            assert p.info["r2_factors"] == (1 if tiled else 2), A
+            ones += tiled
+    assert copies == 1 and 0 < ones < len(mats)  # both kinds occur
