@@ -163,7 +163,10 @@ bmmc_status bmmc_plan(bmmc_plan_t *plan, int n, const uint64_t *A_rows, uint64_t
 
 /* bmmc_plan with options (opts may be NULL for defaults).  With
  * mode = TWO_FACTOR and alloc_scratch = 1 this call allocates device memory
- * (BMMC_ERR_CUDA when that fails). */
+ * (BMMC_ERR_CUDA when that fails).  Besides bmmc_plan's errors, INVALID_ARG
+ * for an option out of its range and for run lengths or a tile size whose
+ * tile does not fit one block: more than 2^15 elements or 64 KiB (16 chunks
+ * of 16 bytes per thread) - e.g. 8-byte elements with runs of 2^7. */
 bmmc_status bmmc_plan_ex(bmmc_plan_t *plan, int n, const uint64_t *A_rows, uint64_t c,
                          size_t elem_size, const bmmc_plan_opts *opts);
 
