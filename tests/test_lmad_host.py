@@ -3,6 +3,7 @@ the library's analysis against the oracle's restatement of the page's
 (flip, drop singletons, sort, collapse), the kind each of the page's cases
 gets, and every rejection."""
 
+import numpy as np
 import pytest
 
 import bmmc_index_transforms_gb300 as bm
@@ -494,3 +495,119 @@ def test_narrow_group_limits(c, elem, narrow):
     assert q["kind"] == "transpose" and q["narrow"] == narrow
     q = _query(_perm_view((4, c, 64, 96), (0, 2, 3, 1)), elem)
     assert q["kind"] == "transpose" and q["narrow"] == (2 if c <= 16 else 0)
+
+
+def _realigned_store_replay(R, C, elem, out_pitch, out_off, nch, tall):
+    """The realigned-pack store schedule of the tile kernel replayed on the
+    host for the transpose of a row-major [R][C] array of 1- or 2-byte words
+    into columns of pitch out_pitch (B = R rows, destination stride 1; A = C
+    columns): tiles TA = nch * 16 / elem wide and TB = tall * 8192 / TA high,
+    the last A tile shifted back (or, for a group A shorter than a tile, its
+    columns masked), lanes in groups of RG holding 8-row units, every aligned
+    8-byte word formed from a unit and the one below it (the previous lane's,
+    or the carry from the thread's previous row set), partial words where a
+    run of sets starts or ends, element stores for a ragged set.  Returns the
+    byte image written and how often each byte was written."""
+    V, T = 16 // elem, 8192
+    TA = nch * V
+    TB = tall * T // TA
+    RG = 8 if elem == 2 else 4
+    EPW, WL, U = 4 // elem, 32 // RG, elem
+    STRIPES, SETS = TA // EPW // WL, TB // (8 * RG)
+    ITEMS = STRIPES * SETS // 8
+    SET_ROWS, CARRY = 8 * RG, STRIPES == 8 and SETS > 1
+    out_bytes = (out_off + (C - 1) * out_pitch + R) * elem
+    mem = np.full(out_bytes + 64, -1, dtype=np.int64)
+    cnt = np.zeros(out_bytes + 64, dtype=np.int64)
+    M = (1 << 64) - 1
+
+    def val(a, b, k):
+        return ((b * C + a) * elem + k) % 251
+
+    def write(addr, vals):
+        for i, v in enumerate(vals):
+            mem[addr + i] = v
+            cnt[addr + i] += 1
+
+    for ta in range((C + TA - 1) // TA):
+        for tb in range((R + TB - 1) // TB):
+            a0, b0 = ta * TA, tb * TB
+            ra, rb, lo = min(TA, C - a0), min(TB, R - b0), 0
+            hi = ra
+            if ra < TA and C >= TA:
+                lo, a0, ra, hi = TA - ra, C - TA, TA, TA
+
+            def dst(ia, ib):
+                return (out_off + (a0 + ia) * out_pitch + b0 + ib) * elem
+
+            def unit_bytes(ia, ib0):
+                return [val(a0 + ia, b0 + ib0 + r, k) if ib0 + r < rb and ia < C - a0 else 0
+                        for r in range(8) for k in range(elem)]
+
+            for w in range(8):
+                carry = {}
+                for i in range(ITEMS):
+                    x = w + 8 * i
+                    s0 = SET_ROWS * (x // STRIPES)
+                    if s0 >= rb:
+                        continue
+                    lanes = [(l % RG, s0 + 8 * (l % RG), EPW * ((x % STRIPES) * WL + l // RG)) for l in range(32)]
+                    if s0 + SET_ROWS > rb:  # ragged set: element stores
+                        for q, ib0, ia0 in lanes:
+                            for j in range(EPW):
+                                for r in range(8):
+                                    if ib0 + r < rb and lo <= ia0 + j < hi:
+                                        write(dst(ia0 + j, ib0 + r), [val(a0 + ia0 + j, b0 + ib0 + r, k)
+                                                                      for k in range(elem)])
+                        continue
+                    first = not (CARRY and i > 0)
+                    last = not (CARRY and i + 1 < ITEMS and s0 + 2 * SET_ROWS <= rb)
+                    for j in range(EPW):
+                        units = {}
+                        for l, (q, ib0, ia0) in enumerate(lanes):
+                            b = unit_bytes(ia0 + j, ib0)
+                            units[l] = [int.from_bytes(bytes(b[8 * h:8 * h + 8]), "little") for h in range(U)]
+                        for l, (q, ib0, ia0) in enumerate(lanes):
+                            rot = units[(l & ~(RG - 1)) | ((q - 1) & (RG - 1))][U - 1]
+                            below0 = rot if q else carry.get((l, j), 0)
+                            if q == 0:
+                                carry[(l, j)] = rot
+                            if not lo <= ia0 + j < hi:
+                                continue
+                            pb = dst(ia0 + j, ib0)
+                            mu = pb & 7
+                            pw = pb - mu
+                            for h in range(U):
+                                below = units[l][h - 1] if h else below0
+                                if h == 0 and q == 0 and first:
+                                    write(pb, list(units[l][0].to_bytes(8, "little"))[:8 - mu])
+                                else:
+                                    word = ((units[l][h] << (8 * mu)) & M) | ((below >> 1) >> (63 - 8 * mu))
+                                    write(pw + 8 * h, list(word.to_bytes(8, "little")))
+                            if q == RG - 1 and last and mu:
+                                write(pw + 8 * U, list((units[l][U - 1] >> (64 - 8 * mu)).to_bytes(8, "little"))[:mu])
+    want = np.full(out_bytes + 64, -1, dtype=np.int64)
+    for a in range(C):
+        for b in range(R):
+            for k in range(elem):
+                want[(out_off + a * out_pitch + b) * elem + k] = val(a, b, k)
+    return mem, cnt, want
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_realigned_pack_store_schedule_replay(seed):
+    """Every destination byte of a transpose into unaligned columns is
+    written exactly once with its value, and nothing else is written, by the
+    realigned-pack store schedule (host replay; whole, ragged and shifted
+    tiles, short groups A, tall and 128-byte-row tiles, every column phase)."""
+    rng = np.random.default_rng(seed)
+    elem = (1, 2)[seed % 2]
+    nch, tall = [(16, 4), (16, 1), (8, 1)][(seed // 2) % 3] if elem == 1 else [(8, 1), (16, 1)][(seed // 2) % 2]
+    TA = nch * 16 // elem
+    TB = tall * 8192 // TA
+    C = int(rng.choice([TA // 2 + 3, TA - 5, TA + 7, 2 * TA - 1]))
+    R = int(rng.choice([TB // 2 + 5, TB, TB + 40, 2 * TB - 8]))
+    out_pitch = R + int(rng.integers(0, 9))
+    out_off = int(rng.integers(0, 16))
+    mem, cnt, want = _realigned_store_replay(R, C, elem, out_pitch, out_off, nch, tall)
+    assert (cnt <= 1).all() and np.array_equal(mem, want)
