@@ -57,6 +57,42 @@ def _ptr(x) -> int | None:
     raise TypeError(f"cannot take the address of {type(x).__name__}")
 
 
+def _check_buf(x, nbytes: int, where: str, name: str) -> None:
+    """Reject, before the library is called, a tensor or numpy array that
+    cannot hold the nbytes bytes the call reads or writes from its address:
+    a strided view (the kernels address memory as one dense block), one too
+    small, or a CUDA tensor on another device than the current one (the
+    library launches on the current device).  Raw integer addresses are the
+    caller's responsibility and pass unchecked."""
+    if x is None or isinstance(x, int):
+        return
+    if hasattr(x, "data_ptr"):
+        if not x.is_contiguous():
+            raise ValueError(f"{where}: {name} must be a contiguous tensor")
+        have = x.numel() * x.element_size()
+        if getattr(x, "is_cuda", False):
+            import torch
+
+            cur = torch.cuda.current_device()
+            if x.device.index != cur:
+                raise ValueError(f"{where}: {name} is on {x.device}, but the current device is cuda:{cur}")
+    elif hasattr(x, "ctypes"):
+        if not x.flags.c_contiguous:
+            raise ValueError(f"{where}: {name} must be a C-contiguous array")
+        have = int(x.nbytes)
+    else:
+        return
+    if have < nbytes:
+        raise ValueError(f"{where}: {name} holds {have} bytes, the call needs {nbytes}")
+
+
+def _plan_bytes(plan: int) -> tuple[int, int]:
+    """(array bytes, mode) of a plan: 2^n elements of elem_size bytes."""
+    info = PlanInfo()
+    _check(_capi.lib().bmmc_plan_info(plan, ctypes.byref(info)), "bmmc_plan_info")
+    return (1 << info.n) * info.elem_size, info.mode
+
+
 def _stream(stream, *tensors) -> int | None:
     if stream is None:
         for t in tensors:
@@ -146,17 +182,28 @@ def bmmc_plan_tile(plan: int) -> tuple[list[int], list[int]]:
 # Permutes (device pointers; torch tensors accepted)
 # --------------------------------------------------------------------------
 
-def bmmc_permute(plan: int, inp, out, stream=None) -> None:
+def bmmc_permute(plan: int, inp, out, stream=None, *, _nbytes: int | None = None) -> None:
+    nbytes = _nbytes if _nbytes is not None else _plan_bytes(plan)[0]
+    _check_buf(inp, nbytes, "bmmc_permute", "in")
+    _check_buf(out, nbytes, "bmmc_permute", "out")
     _check(_capi.lib().bmmc_permute(plan, _ptr(inp), _ptr(out), _stream(stream, inp, out)),
            "bmmc_permute")
 
 
 def bmmc_permute_scratch(plan: int, inp, out, scratch, stream=None) -> None:
+    nbytes, mode = _plan_bytes(plan)
+    _check_buf(inp, nbytes, "bmmc_permute_scratch", "in")
+    _check_buf(out, nbytes, "bmmc_permute_scratch", "out")
+    if mode == 1:  # single-pass plans ignore the scratch
+        _check_buf(scratch, nbytes, "bmmc_permute_scratch", "scratch")
     _check(_capi.lib().bmmc_permute_scratch(plan, _ptr(inp), _ptr(out), _ptr(scratch),
                                             _stream(stream, inp, out)), "bmmc_permute_scratch")
 
 
 def bmmc_permute_host(plan: int, h_in, h_out, d_in, d_out, stream=None) -> None:
+    nbytes, _ = _plan_bytes(plan)
+    for name, x in (("h_in", h_in), ("h_out", h_out), ("d_in", d_in), ("d_out", d_out)):
+        _check_buf(x, nbytes, "bmmc_permute_host", name)
     _check(_capi.lib().bmmc_permute_host(plan, _ptr(h_in), _ptr(h_out), _ptr(d_in), _ptr(d_out),
                                          _stream(stream, d_in, d_out)), "bmmc_permute_host")
 
@@ -164,16 +211,29 @@ def bmmc_permute_host(plan: int, h_in, h_out, d_in, d_out, stream=None) -> None:
 def bmmc_permute_static_scratch(plan: int, inp, out, stream=None) -> None:
     """Two-factor permute through the library's built-in 16 MiB scratch array,
     for callers that must not allocate device memory (see include/bmmc.h)."""
+    nbytes, _ = _plan_bytes(plan)
+    _check_buf(inp, nbytes, "bmmc_permute_static_scratch", "in")
+    _check_buf(out, nbytes, "bmmc_permute_static_scratch", "out")
     _check(_capi.lib().bmmc_permute_static_scratch(plan, _ptr(inp), _ptr(out), _stream(stream, inp, out)),
            "bmmc_permute_static_scratch")
 
 
+def _bits_bytes(n: int, elem_size: int) -> int:
+    return (1 << n) * elem_size if 0 <= n <= 62 else 0
+
+
 def transpose2d(rows_log2: int, cols_log2: int, elem_size: int, inp, out, stream=None) -> None:
+    nbytes = _bits_bytes(rows_log2 + cols_log2, elem_size)
+    _check_buf(inp, nbytes, "transpose2d", "in")
+    _check_buf(out, nbytes, "transpose2d", "out")
     _check(_capi.lib().transpose2d(rows_log2, cols_log2, elem_size, _ptr(inp), _ptr(out),
                                    _stream(stream, inp, out)), "transpose2d")
 
 
 def bpc_permute(n: int, perm: Sequence[int], c: int, elem_size: int, inp, out, stream=None) -> None:
+    nbytes = _bits_bytes(n, elem_size)
+    _check_buf(inp, nbytes, "bpc_permute", "in")
+    _check_buf(out, nbytes, "bpc_permute", "out")
     p = (ctypes.c_int * max(1, n))(*perm)
     _check(_capi.lib().bpc_permute(n, p, int(c), elem_size, _ptr(inp), _ptr(out),
                                    _stream(stream, inp, out)), "bpc_permute")
@@ -182,6 +242,9 @@ def bpc_permute(n: int, perm: Sequence[int], c: int, elem_size: int, inp, out, s
 def bmmc_dims_permute(dims_log2: Sequence[int], axes: Sequence[int], elem_size: int, inp, out,
                       stream=None) -> None:
     d = len(dims_log2)
+    nbytes = _bits_bytes(sum(dims_log2), elem_size)
+    _check_buf(inp, nbytes, "bmmc_dims_permute", "in")
+    _check_buf(out, nbytes, "bmmc_dims_permute", "out")
     dl = (ctypes.c_int * d)(*dims_log2)
     ax = (ctypes.c_int * d)(*axes)
     _check(_capi.lib().bmmc_dims_permute(d, dl, ax, elem_size, _ptr(inp), _ptr(out),
@@ -208,6 +271,9 @@ def _lmad_args(dims_log2, in_offset, in_strides, out_offset, out_strides):
 def bmmc_lmad_copy(dims_log2: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
                    out_strides: Sequence[int], elem_size: int, inp, out, stream=None) -> None:
     args = _lmad_args(dims_log2, in_offset, in_strides, out_offset, out_strides)
+    nbytes = _bits_bytes(sum(dims_log2), elem_size)
+    _check_buf(inp, nbytes, "bmmc_lmad_copy", "in")
+    _check_buf(out, nbytes, "bmmc_lmad_copy", "out")
     _check(_capi.lib().bmmc_lmad_copy(*args, elem_size, _ptr(inp), _ptr(out), _stream(stream, inp, out)),
            "bmmc_lmad_copy")
 
@@ -272,6 +338,8 @@ def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], o
     """out[out_offset + sum i_k out_strides[k]] = inp[in_offset + sum i_k in_strides[k]] for every index
     tuple (element units, any sizes); enqueued on the stream."""
     d, sz, io, si, oo, so = _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides)
+    _check_buf(inp, 0, "lmad_copy", "in")
+    _check_buf(out, 0, "lmad_copy", "out")
     _check(_capi.lib().lmad_copy(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
                                  _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
                                  _stream(stream, inp, out)), "lmad_copy")
@@ -336,6 +404,8 @@ def bmmc_parm_rows(n: int, mask: int) -> list[int]:
 def bmmc_copy(inp, out, nbytes: int | None = None, stream=None) -> None:
     if nbytes is None:
         nbytes = inp.numel() * inp.element_size()
+    _check_buf(inp, nbytes, "bmmc_copy", "in")
+    _check_buf(out, nbytes, "bmmc_copy", "out")
     _check(_capi.lib().bmmc_copy(_ptr(inp), _ptr(out), nbytes, _stream(stream, inp, out)), "bmmc_copy")
 
 
@@ -351,6 +421,7 @@ class Plan:
                                    alloc_scratch, grid_blocks, load_mode, block_order, layout, gather,
                                    batch_log2, tile_walk, naive)
         self.elem_size = elem_size
+        self.nbytes, self.mode = _plan_bytes(self.handle)
 
     @property
     def info(self) -> dict:
@@ -363,7 +434,7 @@ class Plan:
         return bmmc_plan_tile(self.handle)
 
     def permute(self, inp, out, stream=None) -> None:
-        bmmc_permute(self.handle, inp, out, stream)
+        bmmc_permute(self.handle, inp, out, stream, _nbytes=self.nbytes)
 
     def permute_scratch(self, inp, out, scratch, stream=None) -> None:
         bmmc_permute_scratch(self.handle, inp, out, scratch, stream)

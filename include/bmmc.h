@@ -214,8 +214,9 @@ bmmc_status bmmc_permute_host(bmmc_plan_t plan, const void *h_in, void *h_out, v
 
 /* Capacity of the library's built-in scratch array used by
  * bmmc_permute_static_scratch: 16 MiB, i.e. arrays of at most 2^22 elements
- * of 4 bytes, 2^21 of 8 bytes or 2^20 of 16 bytes.  Every GPU that loads
- * the library holds this much device memory until the process exits. */
+ * of 4 bytes, 2^21 of 8 bytes or 2^20 of 16 bytes.  Every GPU on which the
+ * library's device code is loaded holds this much device memory until the
+ * process exits. */
 #define BMMC_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /* Two-factor permute that allocates no device memory.  This entry point has
@@ -230,8 +231,14 @@ bmmc_status bmmc_permute_host(bmmc_plan_t plan, const void *h_in, void *h_out, v
  *   - Arrays larger than BMMC_STATIC_SCRATCH_BYTES are rejected with
  *     BMMC_ERR_TOO_LARGE before any work is enqueued.
  *   - The first call on a device looks up the array's device address on
- *     that device (the device must be current); make that first call before
- *     any stream capture begins.
+ *     that device (the device must be current) and keeps it for the rest of
+ *     the process; make that first call before any stream capture begins.
+ *     Under lazy module loading that first call is also what loads the
+ *     library's device code on the device, which is when the array's
+ *     device memory is reserved.  The kept address belongs to the device's
+ *     primary context (the one the CUDA runtime uses): it is not valid in
+ *     another context the caller made current through the driver API, nor
+ *     after cudaDeviceReset, so such callers must not use this entry point.
  *   - Every call shares the one array, and it keeps the last call's
  *     contents.  Nothing in it needs to start at zero: the first pass
  *     overwrites every byte the second pass reads.  Calls whose work

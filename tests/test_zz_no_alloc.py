@@ -6,13 +6,15 @@ latency-critical code that cannot afford the device-wide synchronisation an
 allocation may bring.  For them the library keeps one 16 MiB scratch array
 of its own, and this entry point runs the two-factor permutation through it.
 
-The test calls it through the C ABI twice in a row (different matrices and
-element sizes, so the second call starts from the first call's leftover
-scratch contents) and compares each output with the existing two-factor
-entry point, bmmc_permute_scratch, given caller-owned scratch: the outputs
-must be identical byte for byte, the tolerance every permutation test uses.
-It also checks the size limit and the plan-mode check.  The file is named so
-that pytest collects it last.
+The test calls it through the C ABI several times in a row (different
+matrices and element sizes, so each call starts from the previous call's
+leftover scratch contents; one array is smaller than the scratch, so a call
+that used only a stale prefix would show) and compares each output byte for
+byte with the CPU oracle's scatter of the same input, the tolerance every
+permutation test uses, and with the existing two-factor entry point,
+bmmc_permute_scratch, given caller-owned scratch.  It also checks the size
+limit and the plan-mode check.  The file is named so that pytest collects it
+last.
 """
 
 import ctypes
@@ -20,6 +22,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from bmmc_index_transforms_gb300 import synth
 from oracle import reference as ref
 
@@ -35,30 +38,37 @@ def _two_factor_plan(L, capi, n, rows, c, elem):
     return h
 
 
-def test_static_scratch_matches_caller_scratch_two_calls_in_a_row():
+def test_static_scratch_matches_oracle_on_calls_in_a_row():
     from bmmc_index_transforms_gb300 import _build, _capi as capi
 
     _build.build()
     L = capi.lib()
     assert torch.cuda.is_available(), "GPU test needs a CUDA device"
     stream = torch.cuda.current_stream()
-    cases = [(22, 4, 0), (20, 16, 1)]  # 16 MiB and 16 MiB: both at the capacity limit
+    threads = max(1, min(32, oracle.host_threads()))
+    # 16 MiB (the capacity), 2 MiB (below it: the rest of the array holds the
+    # previous call's bytes), 16 MiB again with 16-byte elements
+    cases = [(22, 4, 0), (18, 8, 5), (20, 16, 1)]
     for n, elem, seed in cases:
         rows, c, _ = synth.draw_bmmc(seed, n, lambda r: ref.f2_rank(n, r) == n, low_to_high=10)
         plan = _two_factor_plan(L, capi, n, rows, c, elem)
         nbytes = (1 << n) * elem
-        src = torch.from_numpy(synth.fill_int(n, elem).view(np.uint8).reshape(-1).copy()).cuda()
-        want = torch.zeros_like(src)
+        arr = synth.fill_int(n, elem)
+        src = torch.from_numpy(arr.view(np.uint8).reshape(-1).copy()).cuda()
+        want_lib = torch.zeros_like(src)
         got = torch.full_like(src, 0xEE)
         scratch = torch.empty_like(src)
         try:
-            assert L.bmmc_permute_scratch(plan, src.data_ptr(), want.data_ptr(), scratch.data_ptr(),
-                                          stream.cuda_stream) == capi.OK
             assert L.bmmc_permute_static_scratch(plan, src.data_ptr(), got.data_ptr(),
                                                  stream.cuda_stream) == capi.OK
+            assert L.bmmc_permute_scratch(plan, src.data_ptr(), want_lib.data_ptr(), scratch.data_ptr(),
+                                          stream.cuda_stream) == capi.OK
             torch.cuda.synchronize()
             assert got.numel() == nbytes
-            assert torch.equal(got, want), f"static-scratch output differs (n={n}, elem={elem})"
+            want = oracle.scatter(n, rows, c, arr, threads=threads)
+            assert got.cpu().numpy().tobytes() == want.view(np.uint8).tobytes(), \
+                f"static-scratch output differs from the oracle (n={n}, elem={elem})"
+            assert torch.equal(got, want_lib), f"static-scratch output differs (n={n}, elem={elem})"
         finally:
             L.bmmc_plan_destroy(plan)
 
