@@ -50,7 +50,7 @@ def test_static_scratch_matches_oracle_on_calls_in_a_row():
     # previous call's bytes), 16 MiB again with 16-byte elements
     cases = [(22, 4, 0), (18, 8, 5), (20, 16, 1)]
     for n, elem, seed in cases:
-        rows, c, _ = synth.draw_bmmc(seed, n, lambda r: ref.f2_rank(n, r) == n, low_to_high=10)
+        rows, c, _ = synth.draw_bmmc(seed, n, lambda r: ref.f2_rank(n, r) == n, low_to_high=min(10, n // 2))
         plan = _two_factor_plan(L, capi, n, rows, c, elem)
         nbytes = (1 << n) * elem
         arr = synth.fill_int(n, elem)
