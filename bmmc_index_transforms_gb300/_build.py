@@ -19,6 +19,11 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libbmmc_gb300.so")
+# The bounds-checked debugging build (every kernel access tested against its
+# buffer, failures recorded for bmmc_bounds_report): own objects, own library.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(LIBDIR, "libbmmc_gb300_checked.so")
+CHECK_FLAGS = ["-DBMMC_BOUNDS_CHECK"]
 HEADER = os.path.join(ROOT, "include", "bmmc.h")
 
 SOURCES = ["kernels.cu", "capi.cu", "planner.cpp", "static_scratch.cu", "lmad.cu"]
@@ -38,26 +43,31 @@ def _deps():
     return [f for f in files if os.path.isfile(f)]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def is_stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not is_stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          checked: bool = False) -> str:
+    """Build libbmmc_gb300.so (or, with checked=True, the bounds-checked
+    libbmmc_gb300_checked.so next to it) unless it is up to date."""
+    lib_path, build_dir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if not force and not is_stale(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     cc = nvcc()
-    flags = ARCH + COMMON + list(extra_flags or [])
+    defs = CHECK_FLAGS if checked else []
+    flags = ARCH + COMMON + defs + list(extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         cmd = [cc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cpp"):
-            cmd = [cc, "-x", "c++"] + COMMON + ["-c", os.path.join(CSRC, src), "-o", obj]
+            cmd = [cc, "-x", "c++"] + COMMON + defs + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -69,16 +79,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"linking failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":  # pragma: no cover
     import sys
 
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

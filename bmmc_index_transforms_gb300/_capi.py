@@ -72,6 +72,12 @@ class LmadCopyInfo(ctypes.Structure):
                 ("tile_mode", ctypes.c_uint32), ("launch_tile_a", ctypes.c_int), ("launch_tile_b", ctypes.c_int)]
 
 
+class BoundsReport(ctypes.Structure):
+    _fields_ = [("enabled", ctypes.c_int), ("failures", ctypes.c_uint64), ("site", ctypes.c_int),
+                ("bytes", ctypes.c_int), ("address", ctypes.c_uint64), ("lo", ctypes.c_uint64),
+                ("hi", ctypes.c_uint64)]
+
+
 # lmad_copy_info_t.tile_mode flags
 LMAD_TILE_FLAGS = {"tables": 0x01, "chunked": 0x02, "packs": 0x04, "half_rows": 0x08, "tall": 0x10, "wide": 0x20,
                    "realigned": 0x40, "short_a": 0x80}
@@ -109,11 +115,17 @@ SIGNATURES = {
     "bmmc_compose": (ctypes.c_int, [ctypes.c_int, u64p, u64, u64p, u64, u64p, u64p]),
     "bmmc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bmmc_version": (ctypes.c_int, []),
+    "bmmc_bounds_report": (ctypes.c_int, [ctypes.POINTER(BoundsReport), ctypes.c_int]),
+    "bmmc_bounds_selftest": (ctypes.c_int, [vp, vp]),
 }
+
+# Environment variable naming another build of the library to load instead
+# of the default one (e.g. the bounds-checked build, _build.build(checked=True)).
+LIBRARY_ENV = "BMMC_GB300_LIBRARY"
 
 
 def library_path() -> str:
-    return _build.LIB
+    return os.environ.get(LIBRARY_ENV) or _build.LIB
 
 
 def lib():

@@ -514,4 +514,45 @@ const char* bmmc_status_string(bmmc_status status) {
 
 int bmmc_version(void) { return 100; }
 
+bmmc_status bmmc_bounds_report(bmmc_bounds_report_t* report, int reset) {
+    if (!report) return BMMC_ERR_INVALID_ARG;
+    bmmc_bounds_report_t r{};
+#ifdef BMMC_BOUNDS_CHECK
+    r.enabled = 1;
+#endif
+    unsigned long long a[6] = {}, b[6] = {};
+    if (r.enabled) {
+        if (cudaDeviceSynchronize() != cudaSuccess || bounds_record_kernels(a, reset != 0) != cudaSuccess ||
+            bounds_record_lmad(b, reset != 0) != cudaSuccess) {
+            cudaGetLastError();
+            return BMMC_ERR_CUDA;
+        }
+    }
+    r.failures = a[0] + b[0];
+    const unsigned long long* first = a[0] ? a : b;  // one file's first failure
+    if (r.failures) {
+        r.site = (int)first[1];
+        r.address = first[2];
+        r.lo = first[3];
+        r.hi = first[4];
+        r.bytes = (int)first[5];
+    }
+    *report = r;
+    return BMMC_OK;
+}
+
+bmmc_status bmmc_bounds_selftest(void* buf, void* stream) {
+#ifdef BMMC_BOUNDS_CHECK
+    if (!buf) return BMMC_ERR_INVALID_ARG;
+    if ((uintptr_t)buf & 15u) return BMMC_ERR_MISALIGNED;
+    bmmc_status s = pointer_reachable(buf);
+    if (s != BMMC_OK) return s;
+    return from_cuda(bounds_selftest(buf, static_cast<cudaStream_t>(stream)));
+#else
+    (void)buf;
+    (void)stream;
+    return BMMC_ERR_INVALID_ARG;
+#endif
+}
+
 }  // extern "C"

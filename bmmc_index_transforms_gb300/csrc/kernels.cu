@@ -26,6 +26,8 @@
 #include <mutex>
 #include <tuple>
 
+#define BMMC_CHK_FILE 1  // site tag of this file in bounds-checked builds
+#include "bounds.cuh"
 #include "kernel_params.h"
 #include "launch.hpp"
 
@@ -162,13 +164,14 @@ struct TiledMinBlocks {
 template <int ELEM, int NT, int QPT, typename OFF, bool VS>
 __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)>::value))
     bmmc_tiled_kernel(const __grid_constant__ TiledParams p, const uint4* __restrict__ in,
-                      uint4* __restrict__ out) {
+                      uint4* __restrict__ out BMMC_CHK_PARAM) {
     using T = typename ElemType<ELEM>::T;
     constexpr int VEC = 16 / ELEM;
     extern __shared__ uint4 smem_raw[];
     unsigned char* tile = reinterpret_cast<unsigned char*>(smem_raw);
     const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
     unsigned char* dst = reinterpret_cast<unsigned char*>(out);
+    BMMC_CHK_ENTER(tile, chk::dyn_smem_bytes());
 
     const uint32_t tid = threadIdx.x;
     const TileThread<ELEM, NT, OFF> th(p, tid);
@@ -184,7 +187,8 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
         opaque(it);
 #pragma unroll
         for (int i = 0; i < QPT; ++i)
-            if (act[i]) r[i] = ld_stream(reinterpret_cast<const uint4*>(src + (it ^ (OFF)p.it_in[i])));
+            if (act[i] && BMMC_IN_OK(src + (it ^ (OFF)p.it_in[i]), 16))
+                r[i] = ld_stream(reinterpret_cast<const uint4*>(src + (it ^ (OFF)p.it_in[i])));
     };
 
     // Tile walk: a grid stride, or a contiguous range of `span` tiles.
@@ -207,12 +211,16 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
             uint32_t pi = ph;
             opaque(pi);
             if (VS) {
-                *reinterpret_cast<uint4*>(tile + (pi ^ p.st_slot[i * VEC])) = r[i];
+                unsigned char* q = tile + (pi ^ p.st_slot[i * VEC]);
+                if (BMMC_SH_OK(q, 16)) *reinterpret_cast<uint4*>(q) = r[i];
             } else {
                 T e[VEC];
                 memcpy(e, &r[i], 16);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) *reinterpret_cast<T*>(tile + (pi ^ p.st_slot[i * VEC + j])) = e[j];
+                for (int j = 0; j < VEC; ++j) {
+                    unsigned char* q = tile + (pi ^ p.st_slot[i * VEC + j]);
+                    if (BMMC_SH_OK(q, ELEM)) *reinterpret_cast<T*>(q) = e[j];
+                }
             }
         }
         __syncthreads();
@@ -232,10 +240,14 @@ __global__ void __launch_bounds__(NT, (TiledMinBlocks<NT, QPT, (sizeof(OFF) > 4)
             uint32_t gi = ga;
             opaque(gi);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) e[j] = *reinterpret_cast<const T*>(tile + (gi ^ p.ld_slot[i * VEC + j]));
+            for (int j = 0; j < VEC; ++j) {
+                const unsigned char* q = tile + (gi ^ p.ld_slot[i * VEC + j]);
+                e[j] = BMMC_SH_OK(q, ELEM) ? *reinterpret_cast<const T*>(q) : T{};
+            }
             uint4 v;
             memcpy(&v, e, 16);
-            st_stream(reinterpret_cast<uint4*>(dst + (ot ^ (OFF)p.it_out[i])), v);
+            uint4* o = reinterpret_cast<uint4*>(dst + (ot ^ (OFF)p.it_out[i]));
+            if (BMMC_OUT_OK(o, 16)) st_stream(o, v);
         }
         __syncthreads();
     }
@@ -257,13 +269,14 @@ struct AsyncMinBlocks {
 template <int ELEM, int NT, int QPT, typename OFF, int STAGES>
 __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
     bmmc_tiled_async_kernel(const __grid_constant__ TiledParams p, const uint4* __restrict__ in,
-                            uint4* __restrict__ out) {
+                            uint4* __restrict__ out BMMC_CHK_PARAM) {
     using T = typename ElemType<ELEM>::T;
     constexpr int VEC = 16 / ELEM;
     extern __shared__ uint4 smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(smem_raw);
     const unsigned char* src = reinterpret_cast<const unsigned char*>(in);
     unsigned char* dst = reinterpret_cast<unsigned char*>(out);
+    BMMC_CHK_ENTER(smem, chk::dyn_smem_bytes());
     const uint32_t tile_bytes = p.chunks * 16u;
 
     const uint32_t tid = threadIdx.x;
@@ -281,7 +294,9 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
         unsigned char* base = smem + (uint32_t)stage * tile_bytes;
 #pragma unroll
         for (int i = 0; i < QPT; ++i)
-            if (act[i]) cp_async16(base + (th.ph_t ^ p.st_slot[i * VEC]), src + (it ^ (OFF)p.it_in[i]));
+            if (act[i] && BMMC_SH_OK(base + (th.ph_t ^ p.st_slot[i * VEC]), 16) &&
+                BMMC_IN_OK(src + (it ^ (OFF)p.it_in[i]), 16))
+                cp_async16(base + (th.ph_t ^ p.st_slot[i * VEC]), src + (it ^ (OFF)p.it_in[i]));
         cp_async_commit();
     };
     auto gather_store = [&](int stage, OFF ob, uint32_t g) {
@@ -296,10 +311,14 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
             uint32_t gi = ga;
             opaque(gi);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) e[j] = *reinterpret_cast<const T*>(base + (gi ^ p.ld_slot[i * VEC + j]));
+            for (int j = 0; j < VEC; ++j) {
+                const unsigned char* q = base + (gi ^ p.ld_slot[i * VEC + j]);
+                e[j] = BMMC_SH_OK(q, ELEM) ? *reinterpret_cast<const T*>(q) : T{};
+            }
             uint4 v;
             memcpy(&v, e, 16);
-            st_stream(reinterpret_cast<uint4*>(dst + (ot ^ (OFF)p.it_out[i])), v);
+            uint4* o = reinterpret_cast<uint4*>(dst + (ot ^ (OFF)p.it_out[i]));
+            if (BMMC_OUT_OK(o, 16)) st_stream(o, v);
         }
     };
 
@@ -342,15 +361,16 @@ __global__ void __launch_bounds__(NT, (AsyncMinBlocks<QPT, STAGES>::value))
 template <int ELEM>
 __global__ void __launch_bounds__(256)
     bmmc_naive_kernel(const __grid_constant__ NaiveParams p, const void* __restrict__ in_,
-                      void* __restrict__ out_) {
+                      void* __restrict__ out_ BMMC_CHK_PARAM) {
     using T = typename ElemType<ELEM>::T;
     const T* in = static_cast<const T*>(in_);
     T* out = static_cast<T*>(out_);
+    BMMC_CHK_ENTER_GLOBAL();
     for (uint64_t x = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; x < p.count;
          x += (uint64_t)gridDim.x * blockDim.x) {
         uint64_t y = 0;
         for (int i = 0; i < p.n; ++i) y |= (uint64_t)(__popcll(p.rows[i] & x) & 1) << i;
-        out[y ^ p.c] = in[x];
+        if (BMMC_IN_OK(in + x, sizeof(T)) && BMMC_OUT_OK(out + (y ^ p.c), sizeof(T))) out[y ^ p.c] = in[x];
     }
 }
 
@@ -360,27 +380,69 @@ __global__ void __launch_bounds__(256)
 // pipeline full to the end without synchronised strides.
 template <int U>
 __global__ void __launch_bounds__(256)
-    bmmc_copy_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, uint64_t nvec) {
+    bmmc_copy_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, uint64_t nvec BMMC_CHK_PARAM) {
+    BMMC_CHK_ENTER_GLOBAL();
     const uint64_t base = (uint64_t)blockIdx.x * 256u * U + threadIdx.x;
     uint4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-        if (base + (uint64_t)u * 256u < nvec) v[u] = ld_stream(in + base + (uint64_t)u * 256u);
+        if (base + (uint64_t)u * 256u < nvec && BMMC_IN_OK(in + base + (uint64_t)u * 256u, 16))
+            v[u] = ld_stream(in + base + (uint64_t)u * 256u);
 #pragma unroll
     for (int u = 0; u < U; ++u)
-        if (base + (uint64_t)u * 256u < nvec) st_stream(out + base + (uint64_t)u * 256u, v[u]);
+        if (base + (uint64_t)u * 256u < nvec && BMMC_OUT_OK(out + base + (uint64_t)u * 256u, 16))
+            st_stream(out + base + (uint64_t)u * 256u, v[u]);
 }
 
 __global__ void bmmc_copy_tail_kernel(const unsigned char* __restrict__ in,
-                                      unsigned char* __restrict__ out, uint64_t bytes) {
-    for (uint64_t i = threadIdx.x; i < bytes; i += blockDim.x) out[i] = in[i];
+                                      unsigned char* __restrict__ out, uint64_t bytes BMMC_CHK_PARAM) {
+    BMMC_CHK_ENTER_GLOBAL();
+    for (uint64_t i = threadIdx.x; i < bytes; i += blockDim.x)
+        if (BMMC_IN_OK(in + i, 1) && BMMC_OUT_OK(out + i, 1)) out[i] = in[i];
 }
+
+#ifdef BMMC_BOUNDS_CHECK
+// Self-test of the checks: one warp, a buffer of 32 16-byte words, told that
+// its source is words [0, 16) and its destination words [16, 32), and a
+// shared array of 32 words of which only the first 16 are registered.  Lane
+// t loads word t, stores it to shared word t and writes it back to word t,
+// so 16 loads, 16 shared stores and 16 global stores fail their tests (48
+// records).  Every address lies inside the real buffer and the real shared
+// array, so nothing can fault even if a test were wrong.
+__global__ void bmmc_bounds_selftest_kernel(uint4* buf BMMC_CHK_PARAM) {
+    __shared__ uint4 sh[32];
+    BMMC_CHK_ENTER(sh, (uint32_t)(16 * sizeof(uint4)));
+    const int t = threadIdx.x & 31;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (BMMC_IN_OK(buf + t, 16)) v = buf[t];
+    if (BMMC_SH_OK(sh + t, 16)) sh[t] = v;
+    __syncwarp();
+    if (BMMC_OUT_OK(buf + t, 16)) buf[t] = v;
+}
+
+cudaError_t bounds_selftest(void* buf, cudaStream_t stream) {
+    uint4* b = static_cast<uint4*>(buf);
+    bmmc_bounds_selftest_kernel<<<1, 32, 0, stream>>>(b, chk::bounds(b, 256, b + 16, 256));
+    return cudaGetLastError();
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
 
-using TiledFn = void (*)(const TiledParams, const uint4*, uint4*);
+// The buffers one pass may touch: 2^n elements from each pointer.
+[[maybe_unused]] static chk::Bounds pass_bounds(const PassPlan& P, const void* in, const void* out) {
+    const uint64_t bytes = ((uint64_t)1 << P.n) * (uint64_t)P.elem;
+    return chk::bounds(in, bytes, out, bytes);
+}
+
+// Read (and optionally clear) the bounds record of this file's kernels.
+cudaError_t bounds_record_kernels(unsigned long long out[chk::kRecordWords], bool clear) {
+    return chk::read_record(out, clear);
+}
+
+using TiledFn = void (*)(const TiledParams, const uint4*, uint4* BMMC_CHK_PTYPE);
 
 template <int ELEM, typename OFF, bool VS>
 static TiledFn pick_tiled(int nt, int qpt) {
@@ -459,7 +521,7 @@ static cudaError_t blocks_per_sm(int dev, const void* fn, int threads, int smem,
     return cudaSuccess;
 }
 
-using AsyncFn = void (*)(const TiledParams, const uint4*, uint4*);
+using AsyncFn = void (*)(const TiledParams, const uint4*, uint4* BMMC_CHK_PTYPE);
 
 template <int ELEM, typename OFF, int STAGES>
 static AsyncFn pick_async(int nt, int qpt) {
@@ -521,14 +583,14 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
         const int smem = stages * P.smem_bytes;
         if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, smem, &per)) != cudaSuccess) return e;
         fn<<<(unsigned)grid, P.threads, smem, stream>>>(tp, static_cast<const uint4*>(in),
-                                                         static_cast<uint4*>(out));
+                                                         static_cast<uint4*>(out) BMMC_CHK_ARG(pass_bounds(P, in, out)));
         return cudaGetLastError();
     }
     TiledFn fn = tiled_fn(P.elem, P.threads, P.qpt, wide, P.vector_scatter);
     if (!fn) return cudaErrorInvalidConfiguration;
     if ((e = blocks_per_sm(dev, (const void*)fn, P.threads, P.smem_bytes, &per)) != cudaSuccess) return e;
     fn<<<(unsigned)grid, P.threads, P.smem_bytes, stream>>>(tp, static_cast<const uint4*>(in),
-                                                             static_cast<uint4*>(out));
+                                                             static_cast<uint4*>(out) BMMC_CHK_ARG(pass_bounds(P, in, out)));
     return cudaGetLastError();
 }
 
@@ -537,9 +599,9 @@ cudaError_t launch_naive(const PassPlan& P, const void* in, void* out, cudaStrea
     const uint64_t b = (P.np.count + threads - 1) / threads;
     const unsigned blocks = (unsigned)(b < 0x7FFFFFFFull ? b : 0x7FFFFFFFull);
     switch (P.elem) {
-        case 4: bmmc_naive_kernel<4><<<blocks, threads, 0, stream>>>(P.np, in, out); break;
-        case 8: bmmc_naive_kernel<8><<<blocks, threads, 0, stream>>>(P.np, in, out); break;
-        case 16: bmmc_naive_kernel<16><<<blocks, threads, 0, stream>>>(P.np, in, out); break;
+        case 4: bmmc_naive_kernel<4><<<blocks, threads, 0, stream>>>(P.np, in, out BMMC_CHK_ARG(pass_bounds(P, in, out))); break;
+        case 8: bmmc_naive_kernel<8><<<blocks, threads, 0, stream>>>(P.np, in, out BMMC_CHK_ARG(pass_bounds(P, in, out))); break;
+        case 16: bmmc_naive_kernel<16><<<blocks, threads, 0, stream>>>(P.np, in, out BMMC_CHK_ARG(pass_bounds(P, in, out))); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -552,14 +614,16 @@ cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t st
         const uint64_t grid = (nvec + 256u * U - 1) / (256u * U);
         if (grid > 0x7FFFFFFFull) return cudaErrorInvalidValue;
         bmmc_copy_kernel<U><<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint4*>(in),
-                                                                static_cast<uint4*>(out), nvec);
+                                                                static_cast<uint4*>(out), nvec
+                                                                BMMC_CHK_ARG(chk::bounds(in, bytes, out, bytes)));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     const uint64_t tail = bytes - nvec * 16;
     if (tail) {
         bmmc_copy_tail_kernel<<<1, 32, 0, stream>>>(static_cast<const unsigned char*>(in) + nvec * 16,
-                                                    static_cast<unsigned char*>(out) + nvec * 16, tail);
+                                                    static_cast<unsigned char*>(out) + nvec * 16, tail
+                                                    BMMC_CHK_ARG(chk::bounds(in, bytes, out, bytes)));
         return cudaGetLastError();
     }
     return cudaSuccess;

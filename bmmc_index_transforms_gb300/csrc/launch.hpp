@@ -20,6 +20,16 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
 // Plain copy of `bytes` bytes.
 cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t stream);
 
+// Copy out (and with clear, reset) the bounds record of the kernels of
+// kernels.cu / lmad.cu: kRecordWords values (see bounds.cuh); all zero in
+// builds without BMMC_BOUNDS_CHECK.
+cudaError_t bounds_record_kernels(unsigned long long out[6], bool clear);
+cudaError_t bounds_record_lmad(unsigned long long out[6], bool clear);
+#ifdef BMMC_BOUNDS_CHECK
+// The checks' self-test on a caller's device buffer of 512 bytes.
+cudaError_t bounds_selftest(void* buf, cudaStream_t stream);
+#endif
+
 // OK when the GPU can read and write through p (device, managed or pinned
 // memory, or pageable host memory on a device with pageable access).
 bmmc_status pointer_reachable(const void* p);

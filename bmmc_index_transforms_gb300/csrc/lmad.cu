@@ -35,6 +35,8 @@
 #include <type_traits>
 
 #include "../../include/bmmc.h"
+#define BMMC_CHK_FILE 2  // site tag of this file in bounds-checked builds
+#include "bounds.cuh"
 #include "launch.hpp"
 
 namespace bmmc {
@@ -145,7 +147,8 @@ __device__ __forceinline__ uint64_t div_q(uint64_t x, const LmadDiv& f) {
 // offsets (otherwise the host has checked that 32 bits hold them).
 template <typename W, int ND, bool WIDE>
 __global__ void __launch_bounds__(256)
-    lmad_strided_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadStridedParams p) {
+    lmad_strided_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadStridedParams p BMMC_CHK_PARAM) {
+    BMMC_CHK_ENTER_GLOBAL();
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     constexpr int K = 8;
@@ -171,13 +174,13 @@ __global__ void __launch_bounds__(256)
             }
             so += (O)x * (O)p.sin[nd - 1];
             d += (O)x * (O)p.sout[nd - 1];
-            v[j] = __ldg(in + so);
+            if (BMMC_IN_OK(in + so, sizeof(W))) v[j] = __ldg(in + so);
             dst[j] = d;
         }
     }
 #pragma unroll
     for (int j = 0; j < K; ++j)
-        if (base + (uint64_t)j * 256u < p.total) __stcs(out + dst[j], v[j]);
+        if (base + (uint64_t)j * 256u < p.total && BMMC_OUT_OK(out + dst[j], sizeof(W))) __stcs(out + dst[j], v[j]);
 }
 
 // Copies whose destination is one contiguous run and whose source is rows
@@ -211,11 +214,19 @@ __device__ __forceinline__ uint64_t rows_src_byte(const LmadRowsParams& p, uint6
 
 template <bool WIDE>
 __global__ void __launch_bounds__(256)
-    lmad_rows_kernel(const unsigned char* __restrict__ in, unsigned char* __restrict__ out, const LmadRowsParams p) {
+    lmad_rows_kernel(const unsigned char* __restrict__ in, unsigned char* __restrict__ out,
+                     const LmadRowsParams p BMMC_CHK_PARAM) {
+    BMMC_CHK_ENTER_GLOBAL();
     constexpr int K = 4;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        for (uint64_t b = 0; b < p.head; ++b) out[b] = in[rows_src_byte<WIDE>(p, b)];
-        for (uint64_t b = p.head + 16 * p.chunks; b < p.bytes; ++b) out[b] = in[rows_src_byte<WIDE>(p, b)];
+        for (uint64_t b = 0; b < p.head; ++b) {
+            const unsigned char* a = in + rows_src_byte<WIDE>(p, b);
+            if (BMMC_IN_OK(a, 1) && BMMC_OUT_OK(out + b, 1)) out[b] = *a;
+        }
+        for (uint64_t b = p.head + 16 * p.chunks; b < p.bytes; ++b) {
+            const unsigned char* a = in + rows_src_byte<WIDE>(p, b);
+            if (BMMC_IN_OK(a, 1) && BMMC_OUT_OK(out + b, 1)) out[b] = *a;
+        }
     }
     const uint64_t q0 = (uint64_t)blockIdx.x * (256u * K) + threadIdx.x;
     // all loads of the K chunks first (no branch between them), then the
@@ -233,13 +244,14 @@ __global__ void __launch_bounds__(256)
         const unsigned sh = (unsigned)(ad & 3);
         sel[j] = 0x3210u + 0x1111u * sh;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) x[j][i] = fast[j] ? __ldg(base + i) : 0u;
-        x[j][4] = fast[j] && sh ? __ldg(base + 4) : 0u;
+        for (int i = 0; i < 4; ++i) x[j][i] = fast[j] && BMMC_IN_WORD_OK(base + i, 4) ? __ldg(base + i) : 0u;
+        x[j][4] = fast[j] && sh && BMMC_IN_WORD_OK(base + 4, 4) ? __ldg(base + 4) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         if (!fast[j]) continue;
         const uint64_t q = q0 + (uint64_t)j * 256u;
+        if (!BMMC_OUT_OK(out + p.head + 16 * q, 16)) continue;
         __stcs(reinterpret_cast<uint4*>(out + p.head + 16 * q),
                make_uint4(__byte_perm(x[j][0], x[j][1], sel[j]), __byte_perm(x[j][1], x[j][2], sel[j]),
                           __byte_perm(x[j][2], x[j][3], sel[j]), __byte_perm(x[j][3], x[j][4], sel[j])));
@@ -252,10 +264,13 @@ __global__ void __launch_bounds__(256)
         unsigned w[4];
         for (int i = 0; i < 4; ++i) {
             unsigned word = 0;
-            for (int k = 0; k < 4; ++k) word |= (unsigned)in[rows_src_byte<WIDE>(p, o + 4 * i + k)] << (8 * k);
+            for (int k = 0; k < 4; ++k) {
+                const unsigned char* a = in + rows_src_byte<WIDE>(p, o + 4 * i + k);
+                word |= (BMMC_IN_OK(a, 1) ? (unsigned)*a : 0u) << (8 * k);
+            }
             w[i] = word;
         }
-        __stcs(reinterpret_cast<uint4*>(out + o), make_uint4(w[0], w[1], w[2], w[3]));
+        if (BMMC_OUT_OK(out + o, 16)) __stcs(reinterpret_cast<uint4*>(out + o), make_uint4(w[0], w[1], w[2], w[3]));
     }
 }
 
@@ -334,10 +349,14 @@ struct TabAddr {
     const O *ts, *td;
     int TA;
     int b0;  // first B entry of the (part of the) tile
-    __device__ __forceinline__ O src_a(int ia) const { return ts[ia]; }
-    __device__ __forceinline__ O src_b(int ib) const { return ts[TA + b0 + ib]; }
-    __device__ __forceinline__ O dst_a(int ia) const { return td[ia]; }
-    __device__ __forceinline__ O dst_b(int ib) const { return td[TA + b0 + ib]; }
+    __device__ __forceinline__ O src_a(int ia) const { return BMMC_SH_OK(ts + ia, sizeof(O)) ? ts[ia] : O(0); }
+    __device__ __forceinline__ O src_b(int ib) const {
+        return BMMC_SH_OK(ts + TA + b0 + ib, sizeof(O)) ? ts[TA + b0 + ib] : O(0);
+    }
+    __device__ __forceinline__ O dst_a(int ia) const { return BMMC_SH_OK(td + ia, sizeof(O)) ? td[ia] : O(0); }
+    __device__ __forceinline__ O dst_b(int ib) const {
+        return BMMC_SH_OK(td + TA + b0 + ib, sizeof(O)) ? td[TA + b0 + ib] : O(0);
+    }
     // every B row starts at the same offset modulo V elements
     template <int V>
     __device__ __forceinline__ bool same_mis() const { return false; }
@@ -379,7 +398,11 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 #pragma unroll 4
             for (int r = 0; r < E; ++r) {
                 const int ib = ib0 + r * step;
-                if (FULL || (ok && ib < rb)) cp_async_word(&tile[ib * pitch + ia], s + ad.src_b(ib));
+                if (FULL || (ok && ib < rb)) {
+                    W* q = &tile[ib * pitch + ia];
+                    const W* a = s + ad.src_b(ib);
+                    if (BMMC_SH_OK(q, sizeof(W)) && BMMC_IN_OK(a, sizeof(W))) cp_async_word(q, a);
+                }
             }
             asm volatile("cp.async.wait_all;" ::: "memory");
         } else {
@@ -389,12 +412,16 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 #pragma unroll
                 for (int r = 0; r < CH; ++r) {
                     const int ib = ib0 + (c + r) * step;
-                    if (FULL || (ok && ib < rb)) v[r] = __ldg(s + ad.src_b(ib));
+                    if (FULL || (ok && ib < rb)) {
+                        const W* a = s + ad.src_b(ib);
+                        if (BMMC_IN_OK(a, sizeof(W))) v[r] = __ldg(a);
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < CH; ++r) {
                     const int ib = ib0 + (c + r) * step;
-                    if (FULL || (ok && ib < rb)) tile[ib * pitch + ia] = v[r];
+                    if ((FULL || (ok && ib < rb)) && BMMC_SH_OK(&tile[ib * pitch + ia], sizeof(W)))
+                        tile[ib * pitch + ia] = v[r];
                 }
             }
         }
@@ -410,12 +437,16 @@ __device__ __forceinline__ void tile_phases(const W* __restrict__ src, W* __rest
 #pragma unroll
             for (int r = 0; r < CH; ++r) {
                 const int ia = ia0 + (c + r) * step;
-                if (FULL || (ok && ia < ra)) v[r] = tile[ib * pitch + ia];
+                if ((FULL || (ok && ia < ra)) && BMMC_SH_OK(&tile[ib * pitch + ia], sizeof(W)))
+                    v[r] = tile[ib * pitch + ia];
             }
 #pragma unroll
             for (int r = 0; r < CH; ++r) {
                 const int ia = ia0 + (c + r) * step;
-                if (FULL || (ok && ia < ra)) __stcs(o + ad.dst_a(ia), v[r]);
+                if (FULL || (ok && ia < ra)) {
+                    W* q = o + ad.dst_a(ia);
+                    if (BMMC_OUT_OK(q, sizeof(W))) __stcs(q, v[r]);
+                }
             }
         }
     }
@@ -454,33 +485,33 @@ constexpr int kTallTileBytes = 128 * chunk_pitch(16) * 16;
 // aligned 8-byte store.
 __device__ __forceinline__ void store_head8(unsigned char* p, uint64_t v, int mu) {
     if (mu == 0) {
-        __stcs(reinterpret_cast<unsigned long long*>(p), (unsigned long long)v);
+        if (BMMC_OUT_OK(p, 8)) __stcs(reinterpret_cast<unsigned long long*>(p), (unsigned long long)v);
         return;
     }
     if ((uintptr_t)p & 1u) {
-        __stcs(p, (unsigned char)v);
+        if (BMMC_OUT_OK(p, 1)) __stcs(p, (unsigned char)v);
         v >>= 8;
         p += 1;
     }
     if ((uintptr_t)p & 2u) {
-        __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)v);
+        if (BMMC_OUT_OK(p, 2)) __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)v);
         v >>= 16;
         p += 2;
     }
-    if ((uintptr_t)p & 4u) __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)v);
+    if (((uintptr_t)p & 4u) && BMMC_OUT_OK(p, 4)) __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)v);
 }
 __device__ __forceinline__ void store_tail8(unsigned char* p, uint64_t v, int n) {
     if (n & 4) {
-        __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)v);
+        if (BMMC_OUT_OK(p, 4)) __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)v);
         v >>= 32;
         p += 4;
     }
     if (n & 2) {
-        __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)v);
+        if (BMMC_OUT_OK(p, 2)) __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)v);
         v >>= 16;
         p += 2;
     }
-    if (n & 1) __stcs(p, (unsigned char)v);
+    if ((n & 1) && BMMC_OUT_OK(p, 1)) __stcs(p, (unsigned char)v);
 }
 
 template <typename W, typename O, bool PACK, bool SHIFT, bool SHORT, int NCH, int TALL, typename Addr>
@@ -520,9 +551,11 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         const O s0 = ad.src_b(row);
         const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
         const int k = kk + (m != 0);
-        if (!SHORT || V * k - m < hi)  // (chunks wholly past a short group A are not fetched)
-            cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1)))),
-                          reinterpret_cast<const uint4*>(src + s0 + (V * k - m)));
+        if (!SHORT || V * k - m < hi) {  // (chunks wholly past a short group A are not fetched)
+            uint4* q = reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1))));
+            const uint4* a = reinterpret_cast<const uint4*>(src + s0 + (V * k - m));
+            if (BMMC_SH_OK(q, 16) && BMMC_IN_WORD_OK(a, 16)) cp_async_word(q, a);
+        }
     }
     if (!uni || base_mis != 0) {
 #pragma unroll
@@ -530,9 +563,11 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             if (row >= rb) break;  // rows grow
             const O s0 = ad.src_b(row);
             const int m = (int)((base_mis + (unsigned)s0) & (V - 1));
-            if (m != 0)
-                cp_async_word(reinterpret_cast<uint4*>(tile + row * kPitch + V * ROT * ((row >> 3) & (PH - 1))),
-                              reinterpret_cast<const uint4*>(src + s0 - m));
+            if (m != 0) {
+                uint4* q = reinterpret_cast<uint4*>(tile + row * kPitch + V * ROT * ((row >> 3) & (PH - 1)));
+                const uint4* a = reinterpret_cast<const uint4*>(src + s0 - m);
+                if (BMMC_SH_OK(q, 16) && BMMC_IN_WORD_OK(a, 16)) cp_async_word(q, a);
+            }
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -568,14 +603,15 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             if constexpr (decltype(same)::value) {
                 const int b = base + (int)(base_mis * sizeof(W));
                 const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (b & ~3));
+                auto ld = [&](int i) -> uint32_t { return BMMC_SH_OK(p + i, 4) ? p[i] : 0u; };
                 if ((b & 3) == 0) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = p[k * (kPitch * (int)sizeof(W) / 4)];
+                    for (int k = 0; k < 8; ++k) v[k] = ld(k * (kPitch * (int)sizeof(W) / 4));
                 } else {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        v[k] = __funnelshift_r(p[k * (kPitch * (int)sizeof(W) / 4)],
-                                               p[k * (kPitch * (int)sizeof(W) / 4) + 1], 8 * (b & 3));
+                        v[k] = __funnelshift_r(ld(k * (kPitch * (int)sizeof(W) / 4)),
+                                               ld(k * (kPitch * (int)sizeof(W) / 4) + 1), 8 * (b & 3));
                 }
             } else {
                 // rows with their own misalignments: two loads and a funnel
@@ -585,7 +621,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     const int a = base + (k * kPitch + (int)((base_mis + (unsigned)ad.src_b(ib0 + k)) & (V - 1))) *
                                              (int)sizeof(W);
                     const uint32_t* p = reinterpret_cast<const uint32_t*>(tb + (a & ~3));
-                    v[k] = __funnelshift_r(p[0], p[1], 8 * (a & 3));
+                    v[k] = __funnelshift_r(BMMC_SH_OK(p, 4) ? p[0] : 0u, BMMC_SH_OK(p + 1, 4) ? p[1] : 0u, 8 * (a & 3));
                 }
             }
             if constexpr (sizeof(W) == 1) {
@@ -620,7 +656,8 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             for (int j = 0; j < EPW; ++j)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    if (ib0 + k < rb && ia0 + j >= lo && (!SHORT || ia0 + j < hi))
+                    if (ib0 + k < rb && ia0 + j >= lo && (!SHORT || ia0 + j < hi) &&
+                        BMMC_OUT_OK(o + ad.dst_a(ia0 + j) + k, sizeof(W)))
                         o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
         };
         if constexpr (!SHIFT) {
@@ -638,6 +675,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                         for (int j = 0; j < EPW; ++j) {
                             if (ia0 + j < lo || (SHORT && ia0 + j >= hi)) continue;  // not this tile's column
                             W* oj = o + ad.dst_a(ia0 + j);
+                            if (!BMMC_OUT_OK(oj, 8 * sizeof(W))) continue;
                             if constexpr (sizeof(W) == 1)
                                 __stcs(reinterpret_cast<uint2*>(oj), make_uint2(col[j][0], col[j][1]));
                             else
@@ -719,7 +757,8 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                         const uint32_t z2 = col[j][2 * h], z3 = col[j][2 * h + 1];
                         const uint32_t a = up ? z1 : z0, b = up ? z2 : z1, c = up ? z3 : z2;
                         const uint2 word = make_uint2(__funnelshift_rc(a, b, sh), __funnelshift_rc(b, c, sh));
-                        if (keep && (h || q || !first)) __stcs(reinterpret_cast<uint2*>(pw + 8 * h), word);
+                        if (keep && (h || q || !first) && BMMC_OUT_OK(pw + 8 * h, 8))
+                            __stcs(reinterpret_cast<uint2*>(pw + 8 * h), word);
                     }
                     // the partial words (rare: only where a run of sets starts
                     // or ends), under warp-uniform branches
@@ -757,14 +796,14 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             if (ia < lo || (SHORT && ia >= hi)) continue;  // not this tile's column
             W v[V];
 #pragma unroll
-            for (int k = 0; k < V; ++k) v[k] = tile[off[k] + ia];
+            for (int k = 0; k < V; ++k) v[k] = BMMC_SH_OK(&tile[off[k] + ia], sizeof(W)) ? tile[off[k] + ia] : W{};
             W* oa = o + ad.dst_a(ia);
             if (whole) {
-                __stcs(reinterpret_cast<uint4*>(oa), *reinterpret_cast<const uint4*>(v));
+                if (BMMC_OUT_OK(oa, 16)) __stcs(reinterpret_cast<uint4*>(oa), *reinterpret_cast<const uint4*>(v));
             } else {
 #pragma unroll
                 for (int k = 0; k < V; ++k)
-                    if (ib0 + k < rb) __stcs(oa + k, v[k]);
+                    if (ib0 + k < rb && BMMC_OUT_OK(oa + k, sizeof(W))) __stcs(oa + k, v[k]);
             }
         }
         (void)ITEMS;
@@ -780,10 +819,12 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     for (int c0 = 0; c0 < kPer; c0 += CH) {
         W v[CH];
 #pragma unroll
-        for (int r = 0; r < CH; ++r) v[r] = row[ia0 + kStep * (c0 + r)];
+        for (int r = 0; r < CH; ++r)
+            v[r] = BMMC_SH_OK(&row[ia0 + kStep * (c0 + r)], sizeof(W)) ? row[ia0 + kStep * (c0 + r)] : W{};
 #pragma unroll
         for (int r = 0; r < CH; ++r)
-            if (ia0 + kStep * (c0 + r) >= lo && (!SHORT || ia0 + kStep * (c0 + r) < hi))
+            if (ia0 + kStep * (c0 + r) >= lo && (!SHORT || ia0 + kStep * (c0 + r) < hi) &&
+                BMMC_OUT_OK(o + ad.dst_a(ia0 + kStep * (c0 + r)), sizeof(W)))
                 __stcs(o + ad.dst_a(ia0 + kStep * (c0 + r)), v[r]);
     }
 }
@@ -803,10 +844,11 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
 // 16-byte stores.  Unaligned cases move element by element.  32-bit offsets.
 template <typename W, bool NARROW_A>
 __global__ void __launch_bounds__(256)
-    lmad_narrow_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadNarrowParams p) {
+    lmad_narrow_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadNarrowParams p BMMC_CHK_PARAM) {
     constexpr int P = 16 / (int)sizeof(W);  // elements per 16-byte word
     __shared__ __align__(16) unsigned char smem_bytes[16384];
     W* smem = reinterpret_cast<W*>(smem_bytes);
+    BMMC_CHK_ENTER(smem_bytes, (uint32_t)sizeof(smem_bytes));
     // The block sits in shared memory as 16-byte chunks placed by an XOR
     // swizzle, chunk c at c ^ ((c >> 3) & 7): the scatter (narrow B) and the
     // gather (narrow A) touch one element per 16-byte group of the wide side,
@@ -814,7 +856,15 @@ __global__ void __launch_bounds__(256)
     // for 8-element rows of bytes and the like.  Chunks stay whole, so the
     // 16-byte phases still move whole chunks.
     auto swz = [](int c) { return c ^ ((c >> 3) & 7); };
+#ifdef BMMC_BOUNDS_CHECK
+    W spare{};  // stands in for a slot outside the array (bounds-checked builds)
+    auto at = [&](int e) -> W& {
+        W* q = &smem[swz(e / P) * P + e % P];
+        return BMMC_SH_OK(q, sizeof(W)) ? *q : spare;
+    };
+#else
     auto at = [&](int e) -> W& { return smem[swz(e / P) * P + e % P]; };
+#endif
     const int t = threadIdx.x;
     const int n = p.n;
     for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
@@ -841,8 +891,11 @@ __global__ void __launch_bounds__(256)
             int done = 0;
             if (p.vec_load) {
                 const int chunks = nb / P;
-                for (int c = t; c < chunks; c += 256)
-                    cp_async_word(reinterpret_cast<uint4*>(smem) + swz(c), reinterpret_cast<const uint4*>(blkp) + c);
+                for (int c = t; c < chunks; c += 256) {
+                    uint4* q = reinterpret_cast<uint4*>(smem) + swz(c);
+                    const uint4* a = reinterpret_cast<const uint4*>(blkp) + c;
+                    if (BMMC_SH_OK(q, 16) && BMMC_IN_OK(a, 16)) cp_async_word(q, a);
+                }
                 done = chunks * P;
                 asm volatile("cp.async.wait_all;" ::: "memory");
             }
@@ -851,11 +904,11 @@ __global__ void __launch_bounds__(256)
             for (; e + 3 * 256 < nb; e += 4 * 256) {
                 W v[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = blkp[e + u * 256];
+                for (int u = 0; u < 4; ++u) v[u] = BMMC_IN_OK(blkp + e + u * 256, sizeof(W)) ? blkp[e + u * 256] : W{};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) at(e + u * 256) = v[u];
             }
-            for (; e < nb; e += 256) at(e) = blkp[e];
+            for (; e < nb; e += 256) at(e) = BMMC_IN_OK(blkp + e, sizeof(W)) ? blkp[e] : W{};
             __syncthreads();
             W* dbase = out + d + w0;
             const int groups = p.vec_store ? rw / P : 0;
@@ -863,15 +916,17 @@ __global__ void __launch_bounds__(256)
                 W* drow = dbase + ia * (int32_t)p.stride;
                 for (int g = t; g < groups; g += 256) {
                     if constexpr (P == 1) {
-                        __stcs(drow + g, at(g * n + ia));
+                        if (BMMC_OUT_OK(drow + g, sizeof(W))) __stcs(drow + g, at(g * n + ia));
                     } else {
                         W v[P];
 #pragma unroll
                         for (int k = 0; k < P; ++k) v[k] = at((g * P + k) * n + ia);
-                        __stcs(reinterpret_cast<uint4*>(drow) + g, *reinterpret_cast<const uint4*>(v));
+                        if (BMMC_OUT_OK(reinterpret_cast<uint4*>(drow) + g, 16))
+                            __stcs(reinterpret_cast<uint4*>(drow) + g, *reinterpret_cast<const uint4*>(v));
                     }
                 }
-                for (int iw = groups * P + t; iw < rw; iw += 256) __stcs(drow + iw, at(iw * n + ia));
+                for (int iw = groups * P + t; iw < rw; iw += 256)
+                    if (BMMC_OUT_OK(drow + iw, sizeof(W))) __stcs(drow + iw, at(iw * n + ia));
             }
         } else {
             const W* sbase = in + so + w0;  // source row ib at sbase + ib * stride, contiguous along the wide index
@@ -880,10 +935,12 @@ __global__ void __launch_bounds__(256)
                 const W* srow = sbase + ib * (int32_t)p.stride;
                 for (int g = t; g < groups; g += 256) {
                     if constexpr (P == 1) {
-                        at(g * n + ib) = __ldg(srow + g);
+                        at(g * n + ib) = BMMC_IN_OK(srow + g, sizeof(W)) ? __ldg(srow + g) : W{};
                     } else {
                         W v[P];
-                        *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(srow) + g);
+                        *reinterpret_cast<uint4*>(v) = BMMC_IN_OK(reinterpret_cast<const uint4*>(srow) + g, 16)
+                                                           ? __ldg(reinterpret_cast<const uint4*>(srow) + g)
+                                                           : uint4{};
 #pragma unroll
                         for (int k = 0; k < P; ++k) at((g * P + k) * n + ib) = v[k];
                     }
@@ -897,11 +954,17 @@ __global__ void __launch_bounds__(256)
                 for (; ib + 4 <= n; ib += 4) {
                     W v[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) v[u] = __ldg(sbase + (ib + u) * (int32_t)p.stride + iw);
+                    for (int u = 0; u < 4; ++u) {
+                        const W* a = sbase + (ib + u) * (int32_t)p.stride + iw;
+                        v[u] = BMMC_IN_OK(a, sizeof(W)) ? __ldg(a) : W{};
+                    }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) at(iw * n + ib + u) = v[u];
                 }
-                for (; ib < n; ++ib) at(iw * n + ib) = __ldg(sbase + ib * (int32_t)p.stride + iw);
+                for (; ib < n; ++ib) {
+                    const W* a = sbase + ib * (int32_t)p.stride + iw;
+                    at(iw * n + ib) = BMMC_IN_OK(a, sizeof(W)) ? __ldg(a) : W{};
+                }
             }
             __syncthreads();
             W* blkp = out + d + w0 * n;  // contiguous destination block
@@ -909,10 +972,13 @@ __global__ void __launch_bounds__(256)
             if (p.vec_store) {
                 const int chunks = nb / P;
                 for (int c = t; c < chunks; c += 256)
-                    __stcs(reinterpret_cast<uint4*>(blkp) + c, reinterpret_cast<const uint4*>(smem)[swz(c)]);
+                    if (BMMC_OUT_OK(reinterpret_cast<uint4*>(blkp) + c, 16) &&
+                        BMMC_SH_OK(reinterpret_cast<const uint4*>(smem) + swz(c), 16))
+                        __stcs(reinterpret_cast<uint4*>(blkp) + c, reinterpret_cast<const uint4*>(smem)[swz(c)]);
                 done = chunks * P;
             }
-            for (int e = done + t; e < nb; e += 256) __stcs(blkp + e, at(e));
+            for (int e = done + t; e < nb; e += 256)
+                if (BMMC_OUT_OK(blkp + e, sizeof(W))) __stcs(blkp + e, at(e));
         }
         __syncthreads();
     }
@@ -996,7 +1062,8 @@ __device__ __forceinline__ void regroup(const unsigned (&in)[4 * N], unsigned (&
 // group of a row may be partial: that thread moves it element by element.
 template <typename W, int N, bool DEINT>
 __global__ void __launch_bounds__(256)
-    lmad_aos_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadNarrowParams p) {
+    lmad_aos_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadNarrowParams p BMMC_CHK_PARAM) {
+    BMMC_CHK_ENTER_GLOBAL();
     constexpr int P = 16 / (int)sizeof(W);
     const uint64_t item = (uint64_t)blockIdx.x * 256u + threadIdx.x;
     if (item >= p.tiles) return;  // tiles = groups per row x batch
@@ -1022,26 +1089,38 @@ __global__ void __launch_bounds__(256)
         unsigned a[4 * N], b[4 * N];
 #pragma unroll
         for (int j = 0; j < N; ++j) {
-            const uint4 v = DEINT ? __ldg(reinterpret_cast<const uint4*>(in + so + w0 * N) + j)
-                                  : __ldg(reinterpret_cast<const uint4*>(in + so + j * st + w0));
+            const uint4 v =
+                DEINT ? (BMMC_IN_OK(reinterpret_cast<const uint4*>(in + so + w0 * N) + j, 16)
+                             ? __ldg(reinterpret_cast<const uint4*>(in + so + w0 * N) + j)
+                             : uint4{})
+                      : (BMMC_IN_OK(reinterpret_cast<const uint4*>(in + so + j * st + w0), 16)
+                             ? __ldg(reinterpret_cast<const uint4*>(in + so + j * st + w0))
+                             : uint4{});
             a[4 * j] = v.x, a[4 * j + 1] = v.y, a[4 * j + 2] = v.z, a[4 * j + 3] = v.w;
         }
         regroup<(int)sizeof(W), N, DEINT>(a, b);
 #pragma unroll
         for (int j = 0; j < N; ++j) {
             const uint4 v = make_uint4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
-            if (DEINT)
-                __stcs(reinterpret_cast<uint4*>(out + d + j * st + w0), v);
-            else
-                __stcs(reinterpret_cast<uint4*>(out + d + w0 * N) + j, v);
+            if (DEINT) {
+                if (BMMC_OUT_OK(out + d + j * st + w0, 16)) __stcs(reinterpret_cast<uint4*>(out + d + j * st + w0), v);
+            } else {
+                if (BMMC_OUT_OK(reinterpret_cast<uint4*>(out + d + w0 * N) + j, 16))
+                    __stcs(reinterpret_cast<uint4*>(out + d + w0 * N) + j, v);
+            }
         }
     } else {
         for (int iw = 0; iw < rw; ++iw)
             for (int c = 0; c < N; ++c) {
-                if (DEINT)
-                    out[d + c * st + w0 + iw] = in[so + (w0 + iw) * N + c];
-                else
-                    out[d + (w0 + iw) * N + c] = in[so + c * st + w0 + iw];
+                if (DEINT) {
+                    if (BMMC_IN_OK(in + so + (w0 + iw) * N + c, sizeof(W)) &&
+                        BMMC_OUT_OK(out + d + c * st + w0 + iw, sizeof(W)))
+                        out[d + c * st + w0 + iw] = in[so + (w0 + iw) * N + c];
+                } else {
+                    if (BMMC_IN_OK(in + so + c * st + w0 + iw, sizeof(W)) &&
+                        BMMC_OUT_OK(out + d + (w0 + iw) * N + c, sizeof(W)))
+                        out[d + (w0 + iw) * N + c] = in[so + c * st + w0 + iw];
+                }
             }
     }
 }
@@ -1102,7 +1181,7 @@ constexpr int tile_min_blocks() {
 
 template <typename W, bool WIDE, int MODE>
 __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
-    lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p) {
+    lmad_tile_kernel(const W* __restrict__ in, W* __restrict__ out, const LmadTileParams p BMMC_CHK_PARAM) {
     using I = typename std::conditional<WIDE, uint64_t, uint32_t>::type;
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     using S = TileShape<sizeof(W)>;
@@ -1129,6 +1208,8 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     constexpr bool SHIFT = (MODE & kTileShift) != 0;
     constexpr bool SHORT = (MODE & kTileShort) != 0;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
+    BMMC_CHK_ENTER(tile, DYN ? chk::dyn_smem_bytes() : (uint32_t)sizeof(tile_s), tab_src, (uint32_t)sizeof(tab_src),
+                   tab_dst, (uint32_t)sizeof(tab_dst));
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
     for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
@@ -1208,8 +1289,10 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
                         td += (O)r * (O)p.bt[k];
                     }
                 }
-                tab_src[i] = ts;
-                tab_dst[i] = td;
+                if (BMMC_SH_OK(tab_src + i, sizeof(O)) && BMMC_SH_OK(tab_dst + i, sizeof(O))) {
+                    tab_src[i] = ts;
+                    tab_dst[i] = td;
+                }
             }
             __syncthreads();
         }
@@ -1702,6 +1785,17 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
 // Launchers
 // ---------------------------------------------------------------------------
 
+#ifdef BMMC_BOUNDS_CHECK
+// The caller's two buffers of the lmad_copy call being launched on this host
+// thread (bounds-checked builds): every LMAD kernel is checked against them.
+thread_local chk::Bounds t_lmad_bounds{};
+chk::Bounds lmad_bounds() { return t_lmad_bounds; }
+uintptr_t span_end(const void* p, size_t elems, size_t elem) {
+    const uintptr_t a = (uintptr_t)p, room = UINTPTR_MAX - a;
+    return elems > room / elem ? UINTPTR_MAX : a + elems * elem;
+}
+#endif
+
 uint64_t span_of(const Dim* d, int nd, bool dest) {
     uint64_t s = 0;
     for (int k = 0; k < nd; ++k) s += (uint64_t)(d[k].n - 1) * iabs(dest ? d[k].t : d[k].s);
@@ -1722,7 +1816,8 @@ cudaError_t launch_strided_w(const W* in, W* out, const Dim* d, int nd, uint64_t
     }
     const uint64_t grid = (total + 2047) / 2048;
     if (grid > 0x7FFFFFFFull) return cudaErrorInvalidValue;
-#define LMAD_STRIDED(NDV, WV) lmad_strided_kernel<W, NDV, WV><<<(unsigned)grid, 256, 0, stream>>>(in, out, p)
+#define LMAD_STRIDED(NDV, WV) \
+    lmad_strided_kernel<W, NDV, WV><<<(unsigned)grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()))
     if (wide) {
         switch (nd) {
             case 1: LMAD_STRIDED(1, true); break;
@@ -1763,9 +1858,9 @@ cudaError_t launch_rows(const unsigned char* in, unsigned char* out, const LmadC
     const unsigned grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(g, 0x7FFFFFFFull));
     if (g > 0x7FFFFFFFull) return cudaErrorInvalidValue;
     if (wide)
-        lmad_rows_kernel<true><<<grid, 256, 0, stream>>>(in, out, p);
+        lmad_rows_kernel<true><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()));
     else
-        lmad_rows_kernel<false><<<grid, 256, 0, stream>>>(in, out, p);
+        lmad_rows_kernel<false><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()));
     return cudaGetLastError();
 }
 
@@ -1813,8 +1908,8 @@ cudaError_t launch_narrow_w(const W* in, W* out, const LmadCopy& C, cudaStream_t
             const uint64_t blocks = (p.tiles + 255) / 256;
             if (blocks > 0x7FFFFFFFull) return cudaErrorInvalidValue;
 #define LMAD_AOS_LAUNCH(NV)                                                                                     \
-    (narrow_a ? lmad_aos_kernel<W, NV, true><<<(unsigned)blocks, 256, 0, stream>>>(in, out, p)                 \
-              : lmad_aos_kernel<W, NV, false><<<(unsigned)blocks, 256, 0, stream>>>(in, out, p))
+    (narrow_a ? lmad_aos_kernel<W, NV, true><<<(unsigned)blocks, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds())) \
+              : lmad_aos_kernel<W, NV, false><<<(unsigned)blocks, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds())))
             if (n == 2) LMAD_AOS_LAUNCH(2);
             else if (n == 3) LMAD_AOS_LAUNCH(3);
             else LMAD_AOS_LAUNCH(4);
@@ -1827,9 +1922,9 @@ cudaError_t launch_narrow_w(const W* in, W* out, const LmadCopy& C, cudaStream_t
     p.div_tw = make_div(tiles_w, 32);
     const unsigned grid = (unsigned)std::min<uint64_t>(p.tiles, 0x7FFFFFFFull);
     if (narrow_a)
-        lmad_narrow_kernel<W, true><<<grid, 256, 0, stream>>>(in, out, p);
+        lmad_narrow_kernel<W, true><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()));
     else
-        lmad_narrow_kernel<W, false><<<grid, 256, 0, stream>>>(in, out, p);
+        lmad_narrow_kernel<W, false><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()));
     return cudaGetLastError();
 }
 
@@ -1962,14 +2057,15 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     const unsigned grid = (unsigned)std::min<uint64_t>(tiles, 0x7FFFFFFFull);
     const int mode = L.mode & ~kTileWide;
     constexpr int kWide = kTileWide;
-#define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p)
+#define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()))
     if constexpr (sizeof(W) == 1) {
         if (mode & kTileTall) {
 #define LMAD_TALL(WV, MV)                                                                              \
     do {                                                                                               \
         const cudaError_t ea = allow_tall_tile<W, WV, MV>();                                           \
         if (ea != cudaSuccess) return ea;                                                              \
-        lmad_tile_kernel<W, WV, MV><<<grid, 256, kTallTileBytes, stream>>>(in, out, p);                \
+        lmad_tile_kernel<W, WV, MV><<<grid, 256, kTallTileBytes, stream>>>(in, out,                    \
+                                                                          p BMMC_CHK_ARG(lmad_bounds())); \
     } while (0)
             switch (mode | (wide ? kWide : 0)) {
                 case 22: LMAD_TALL(false, 22); break;
@@ -2108,6 +2204,12 @@ void widened(const LmadCopy& C, Dim* d, uint64_t* total) {
 }
 
 }  // namespace
+
+// Read (and optionally clear) the bounds record of this file's kernels.
+cudaError_t bounds_record_lmad(unsigned long long out[chk::kRecordWords], bool clear) {
+    return chk::read_record(out, clear);
+}
+
 }  // namespace bmmc
 
 using namespace bmmc;
@@ -2165,6 +2267,10 @@ extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_off
     if (s != BMMC_OK) return s;
     if (C.kind == LMAD_COPY_EMPTY) return BMMC_OK;
     if ((s = pointer_reachable(in)) != BMMC_OK || (s = pointer_reachable(out)) != BMMC_OK) return s;
+#ifdef BMMC_BOUNDS_CHECK
+    t_lmad_bounds = chk::Bounds{{(uintptr_t)in, span_end(in, in_elems, elem_size)},
+                                {(uintptr_t)out, span_end(out, out_elems, elem_size)}};
+#endif
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned char* ib = static_cast<const unsigned char*>(in);
     unsigned char* ob = static_cast<unsigned char*>(out);

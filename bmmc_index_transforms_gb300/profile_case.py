@@ -5,6 +5,8 @@
 
 Kinds: random (seed), worst (seed, low 10 bits mapped to high bits), bitrev,
 complement (A = I, c on the high bits: contiguous tiles on both sides),
+window (seed, a random BMMC on the low --window bits and the identity above:
+tiles scattered only inside aligned windows of 2^window elements),
 transpose (square, n even), dims5 (the 5-D (4,2,0,3,1) permutation of a
 [32,64,64,64,32]-shaped array scaled to n bits), copy (the copy kernel on the
 same bytes), two_factor (seed, two passes through caller scratch).
@@ -42,7 +44,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--kind", default="random",
                     choices=["random", "worst", "bitrev", "transpose", "dims5", "copy", "two_factor",
-                             "complement", "lmad_slice_2d", "lmad_slice_3d", "lmad_reversed_rows",
+                             "complement", "window", "lmad_slice_2d", "lmad_slice_3d", "lmad_reversed_rows",
                              "lmad_transpose"])
     ap.add_argument("--n", type=int, default=26)
     ap.add_argument("--elem", type=int, default=4)
@@ -52,6 +54,7 @@ def main(argv=None):
     ap.add_argument("--t-out", type=int, default=0)
     ap.add_argument("--tile-bits", type=int, default=0)
     ap.add_argument("--shape", default="8192,8193")
+    ap.add_argument("--window", type=int, default=22, help="window: log2 elements of a window")
     a = ap.parse_args(argv)
     if a.kind.startswith("lmad_"):
         return lmad_case(a)
@@ -64,6 +67,10 @@ def main(argv=None):
         rows, c, _ = synth.draw_bmmc(a.seed, n, _accept(n, elem))
     elif a.kind == "worst":
         rows, c, _ = synth.draw_bmmc(a.seed, n, _accept(n, elem), low_to_high=min(10, n // 2))
+    elif a.kind == "window":
+        m = min(a.window, n)
+        low, cl, _ = synth.draw_bmmc(a.seed, m, _accept(m, elem))
+        rows, c = list(low) + maps.identity_rows(n)[m:], cl
     elif a.kind == "complement":
         # A = I, c on the bits above the tile: every tile is contiguous on both sides
         rows, c = maps.identity_rows(n), ((1 << n) - 1) & ~((1 << 16) - 1)

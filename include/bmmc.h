@@ -146,8 +146,12 @@ typedef struct {
     int chunks_per_thread;
     uint64_t tiles;      /* number of tiles (units of work) of the tiled kernel */
     int smem_bytes;      /* shared memory per block */
-    int bank_conflicts;  /* extra shared-memory wavefronts per tile found by the planner's
-                            self-check of its layout (0 = conflict-free on both phases) */
+    int bank_conflicts;  /* extra shared-memory wavefronts per tile in the planner's model of
+                            its layout (a simulation of each shared-memory instruction kind;
+                            0 = conflict-free on both phases).  A model figure: with the array
+                            in L2 the hardware counters match it exactly; at DRAM-bound sizes
+                            they also count replays from contention with global traffic in the
+                            shared data banks, which no layout removes */
     uint64_t c;
     int vector_stores;   /* 1 = input vectors are stored whole in shared memory (one
                             16-byte store each), 0 = one store per element */
@@ -477,6 +481,45 @@ bmmc_status bmmc_parm_rows(int n, uint64_t mask, uint64_t *rows_out);
  * practical ceiling a permutation is measured against ("A kernel that is
  * correct", "The ceiling: a copy").  Pointers 16-byte aligned. */
 bmmc_status bmmc_copy(const void *in, void *out, size_t bytes, void *stream);
+
+/* ---- Bounds-checked builds --------------------------------------------------
+ * A debugging build of the library (every source compiled with
+ * -DBMMC_BOUNDS_CHECK) makes each global and shared-memory access of every
+ * kernel test its address first: loads must lie inside the launch's source
+ * buffer (a whole aligned 16- or 4-byte word fetched next to the copied
+ * elements must start on a multiple of its size and overlap that buffer),
+ * stores inside its destination buffer, shared accesses inside the kernel's
+ * shared arrays.  A failing access is skipped, never trapped (a load gives
+ * zero), and counted.  The source and destination buffers are the pass's
+ * 2^n * elem_size bytes for the permutes and the caller's in_elems and
+ * out_elems for lmad_copy.  This stands in for a memory checker; it is
+ * slower and not meant for production. */
+typedef struct {
+    int enabled;        /* 1 in a bounds-checked build, else 0 (and the rest zero) */
+    uint64_t failures;  /* accesses that failed their test since the last reset */
+    int site;           /* first failure: source file tag * 100000 + line
+                           (tag 1: kernels.cu, 2: lmad.cu) */
+    int bytes;          /* its access size */
+    uint64_t address;   /* its address (a shared-memory offset for shared accesses) */
+    uint64_t lo, hi;    /* the range [lo, hi) it was tested against */
+} bmmc_bounds_report_t;
+
+/* Read the failure record of the bounds-checked build (device-wide for the
+ * current device; the call synchronises with the device).  reset != 0 clears
+ * it afterwards.  In an ordinary build *report is all zero and the call does
+ * no device work.  Errors: INVALID_ARG for a NULL report, CUDA. */
+bmmc_status bmmc_bounds_report(bmmc_bounds_report_t* report, int reset);
+
+/* Positive control of the checks (bounds-checked builds only; elsewhere
+ * INVALID_ARG): buf is a caller-owned, 16-byte aligned device buffer of 512
+ * bytes.  One warp loads its 32 16-byte words and writes them back while the
+ * launch's bounds name words 0..15 as the source and 16..31 as the
+ * destination, and only half of a 32-word shared array is registered: 48
+ * accesses fail their tests (16 loads, 16 shared stores, 16 stores) and are
+ * recorded.  Every address touched lies inside buf and the shared array, so
+ * the control cannot fault.  The first 16 words of buf are left as they
+ * were, the last 16 zeroed.  Errors: INVALID_ARG, MISALIGNED, CUDA. */
+bmmc_status bmmc_bounds_selftest(void* buf, void* stream);
 
 /* Static string for a status code (never NULL). */
 const char *bmmc_status_string(bmmc_status status);
