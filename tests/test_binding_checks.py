@@ -12,9 +12,17 @@ import numpy as np
 import pytest
 
 import bmmc_index_transforms_gb300 as bm
+from bmmc_index_transforms_gb300 import _build
 from oracle import reference as ref
 
 torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    """Plans are made by the real library, so it must exist before the
+    first test of this module runs (in a fresh tree nothing has built it)."""
+    _build.build()
 
 
 def _plan(n=12, elem=4, **kw):
