@@ -80,7 +80,7 @@ class BoundsReport(ctypes.Structure):
 
 # lmad_copy_info_t.tile_mode flags
 LMAD_TILE_FLAGS = {"tables": 0x01, "chunked": 0x02, "packs": 0x04, "half_rows": 0x08, "tall": 0x10, "wide": 0x20,
-                   "realigned": 0x40, "short_a": 0x80}
+                   "realigned": 0x40, "short_a": 0x80, "staged": 0x100}
 
 
 # name -> (restype, argtypes); every function declared in include/bmmc.h

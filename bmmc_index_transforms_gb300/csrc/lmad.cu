@@ -312,6 +312,12 @@ struct TileSides {
 #ifndef LMAD_TILE_SHIFT
 #define LMAD_TILE_SHIFT 1
 #endif
+// On 128-row tiles (tall byte tiles, 64 x 128 2-byte tiles) such
+// destinations are restaged destination-major and written as whole aligned
+// 16-byte words instead.
+#ifndef LMAD_TILE_STAGE
+#define LMAD_TILE_STAGE 1
+#endif
 // Resident blocks per SM asked of the compiler for the 1-byte pack path.
 #ifndef LMAD_BYTE_BLOCKS
 #define LMAD_BYTE_BLOCKS 6
@@ -514,9 +520,34 @@ __device__ __forceinline__ void store_tail8(unsigned char* p, uint64_t v, int n)
     if ((n & 1) && BMMC_OUT_OK(p, 1)) __stcs(p, (unsigned char)v);
 }
 
-template <typename W, typename O, bool PACK, bool SHIFT, bool SHORT, int NCH, int TALL, typename Addr>
+// Stores bytes 0..n-1 (0 <= n <= 16) of v at p, in the largest naturally
+// aligned pieces (8, 4, 2 or 1 bytes) that fit: the partial 16-byte words
+// at the ends of a destination column.
+__device__ __forceinline__ void store_bytes16(unsigned char* p, uint4 v, int n) {
+    uint64_t lo = ((uint64_t)v.y << 32) | v.x, hi = ((uint64_t)v.w << 32) | v.z;
+    while (n > 0) {
+        const uintptr_t a = (uintptr_t)p;
+        const int s = (n >= 8 && (a & 7u) == 0) ? 8 : (n >= 4 && (a & 3u) == 0) ? 4 : (n >= 2 && (a & 1u) == 0) ? 2 : 1;
+        if (BMMC_OUT_OK(p, s)) {
+            if (s == 8)
+                __stcs(reinterpret_cast<unsigned long long*>(p), (unsigned long long)lo);
+            else if (s == 4)
+                __stcs(reinterpret_cast<unsigned int*>(p), (unsigned int)lo);
+            else if (s == 2)
+                __stcs(reinterpret_cast<unsigned short*>(p), (unsigned short)lo);
+            else
+                __stcs(p, (unsigned char)lo);
+        }
+        lo = s == 8 ? hi : (lo >> (8 * s)) | (hi << (64 - 8 * s));
+        hi = s == 8 ? 0 : hi >> (8 * s);
+        p += s;
+        n -= s;
+    }
+}
+
+template <typename W, typename O, bool PACK, bool SHIFT, bool STAGE, bool SHORT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
-                                                    const Addr& ad, int rb, int lo, int hi) {
+                                                    const Addr& ad, int rb, int lo, int hi, bool first_b) {
     constexpr int V = 16 / (int)sizeof(W), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
@@ -525,11 +556,13 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     // (1 byte: 2 chunks, 4 phases; 2 bytes: 1 chunk, 8 phases), the others'
     // by one chunk over 4 phases.
     constexpr bool REG = PACK && sizeof(W) <= 2;
-    constexpr int ROT = REG && sizeof(W) == 1 ? 2 : 1;
+    // (staged tiles read one row per shared load, so rows need no rotation)
+    constexpr int ROT = STAGE ? 0 : REG && sizeof(W) == 1 ? 2 : 1;
     constexpr int PH = REG && sizeof(W) == 2 ? 8 : 4;
     static_assert(NCH + 1 + ROT * (PH - 1) <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
     static_assert(TALL == 1 || (REG && sizeof(W) == 1), "tall tiles on the 1-byte pack path only");
     static_assert(!SHIFT || REG, "realigned packs on the 1- and 2-byte register path only");
+    static_assert(!STAGE || (REG && !SHIFT && TB == 128), "staged columns: 1- and 2-byte words, 128-row tiles");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
     // every row shares the origin's misalignment (B's source stride a
@@ -586,7 +619,8 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         // over the sets; a thread's items share their lane's rotation.
         constexpr int EPW = 4 / (int)sizeof(W), RG = PH, WL = 32 / RG;
         constexpr int STRIPES = TA / EPW / WL, SETS = TB / (8 * RG), ITEMS = STRIPES * SETS / 8;
-        static_assert(ITEMS >= 1 && STRIPES * SETS == 8 * ITEMS && 16 * ROT == 4 * WL, "whole blocks, distinct banks");
+        static_assert(ITEMS >= 1 && STRIPES * SETS == 8 * ITEMS && (STAGE || 16 * ROT == 4 * WL),
+                      "whole blocks, distinct banks");
         const int w = t >> 5, l = t & 31;
         const unsigned char* tb = reinterpret_cast<const unsigned char*>(tile);
         const int lead = V * ROT * (l & (RG - 1));  // ((8 RG set + 8 (l % RG)) / 8) mod PH = l % RG
@@ -660,7 +694,170 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                         BMMC_OUT_OK(o + ad.dst_a(ia0 + j) + k, sizeof(W)))
                         o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
         };
-        if constexpr (!SHIFT) {
+        if constexpr (STAGE) {
+            // Destination columns that do not start on a 16-byte boundary,
+            // restaged destination-major.  The launcher steps tiles by
+            // TB - V rows along B, so neighbouring tiles share V rows: each
+            // column of a tile writes the whole aligned 16-byte destination
+            // words that start in its first TB - V rows (they end inside the
+            // TB rows fetched), and the tile holding B index 0 also writes
+            // the partial word before a column's first aligned one; words are
+            // cut at the last fetched row (rb), which ends B.  Every item is
+            // gathered into registers (below), the tile is rewritten with
+            // column ia a contiguous run at ia * DP bytes of the same shared
+            // memory (8- or 16-byte stores at the run's row offset; with the
+            // slot rotation, DP = 136 for bytes and 272 for 2-byte words put
+            // each half (quarter) warp's stores in 32 distinct banks), and
+            // each column run is read back in aligned 16-byte granules,
+            // shifted to the destination's alignment in registers and
+            // written as 16-byte stores (below).
+            constexpr int DP = sizeof(W) == 1 ? TB + 8 : 2 * TB + 16;  // bytes between column runs
+            constexpr int NB = (TB - V) / V;                         // whole words a column owns
+            static_assert(TA * DP <= TALL * (TileShape<sizeof(W)>::T / (NCH * V)) * chunk_pitch(NCH) * 16,
+                          "the destination-major tile fits the shared tile");
+            // Gather: an item is 8 rows x 32 consecutive 4-byte words of one
+            // row segment (lane l takes word l, so each shared load reads
+            // 128 consecutive bytes of one row: no bank conflict whatever
+            // the row's misalignment), transposed by byte permutes into EPW
+            // columns of 8 rows.  Slot j of lane l holds its column
+            // (j + rot) mod EPW, rot = (l / 4) mod EPW, so that the
+            // destination-major stores below fall in distinct banks.
+            constexpr int WPR = TA * (int)sizeof(W) / 4;  // words per row segment
+            constexpr int CB = WPR / 32, SITEMS = (TB / 8) * CB / 8;
+            static_assert(CB * 32 == WPR && SITEMS * 8 == (TB / 8) * CB, "whole items");
+            const int rot = (l >> 2) & (EPW - 1);
+            uint32_t s_lo, s_hi;  // first-stage byte selectors (bytes) / the two halves (2-byte words)
+            if constexpr (sizeof(W) == 1) {
+                const uint32_t c0 = (uint32_t)rot, c1 = (uint32_t)((rot + 1) & 3), c2 = (uint32_t)((rot + 2) & 3),
+                               c3 = (uint32_t)((rot + 3) & 3);
+                s_lo = c0 | (4u + c0) << 4 | c1 << 8 | (4u + c1) << 12;
+                s_hi = c2 | (4u + c2) << 4 | c3 << 8 | (4u + c3) << 12;
+            } else {
+                s_lo = rot ? 0x7632u : 0x5410u;
+                s_hi = rot ? 0x5410u : 0x7632u;
+            }
+            const unsigned char* const sb = reinterpret_cast<const unsigned char*>(tile);
+            const bool fast = uni && ((base_mis * (unsigned)sizeof(W)) & 3u) == 0;
+            Cols held[SITEMS];
+#pragma unroll
+            for (int i = 0; i < SITEMS; ++i) {
+                const int x = w + 8 * i;
+                const int r0 = 8 * (x / CB), wi = 32 * (x % CB) + l;
+                uint32_t v[8];
+                if (fast) {
+                    // every row shares a 4-byte aligned misalignment
+                    const uint32_t* p = reinterpret_cast<const uint32_t*>(
+                        sb + (r0 * kPitch + (int)base_mis) * (int)sizeof(W) + 4 * wi);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        v[k] = BMMC_SH_OK(p + k * (kPitch * (int)sizeof(W) / 4), 4) ? p[k * (kPitch * (int)sizeof(W) / 4)]
+                                                                                    : 0u;
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int mk = (int)((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1));
+                        const int byte = ((r0 + k) * kPitch + mk) * (int)sizeof(W) + 4 * wi;
+                        const uint32_t* p = reinterpret_cast<const uint32_t*>(sb + (byte & ~3));
+                        const uint32_t a = BMMC_SH_OK(p, 4) ? p[0] : 0u;
+                        if ((byte & 3) == 0) {  // warp-uniform: one row per load
+                            v[k] = a;
+                        } else {
+                            const uint32_t b = BMMC_SH_OK(p + 1, 4) ? p[1] : 0u;
+                            v[k] = __funnelshift_r(a, b, 8 * (byte & 3));
+                        }
+                    }
+                }
+                auto& col = held[i].c;
+                if constexpr (sizeof(W) == 1) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], s_lo);
+                        const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], s_hi);
+                        const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], s_lo);
+                        const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], s_hi);
+                        col[0][h] = __byte_perm(t0, t2, 0x5410);
+                        col[1][h] = __byte_perm(t0, t2, 0x7632);
+                        col[2][h] = __byte_perm(t1, t3, 0x5410);
+                        col[3][h] = __byte_perm(t1, t3, 0x7632);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        col[0][h] = __byte_perm(v[2 * h], v[2 * h + 1], s_lo);
+                        col[1][h] = __byte_perm(v[2 * h], v[2 * h + 1], s_hi);
+                    }
+                }
+            }
+            __syncthreads();  // the source-major tile is read
+            unsigned char* const dm = reinterpret_cast<unsigned char*>(tile);
+#pragma unroll
+            for (int i = 0; i < SITEMS; ++i) {
+                const int x = w + 8 * i;
+                const int r0 = 8 * (x / CB), c0 = (32 * (x % CB) + l) * EPW;
+#pragma unroll
+                for (int j = 0; j < EPW; ++j) {
+                    unsigned char* q = dm + (c0 + ((j + rot) & (EPW - 1))) * DP + r0 * (int)sizeof(W);
+                    if constexpr (sizeof(W) == 1) {
+                        if (BMMC_SH_OK(q, 8)) *reinterpret_cast<uint2*>(q) = make_uint2(held[i].c[j][0], held[i].c[j][1]);
+                    } else {
+                        if (BMMC_SH_OK(q, 16))
+                            *reinterpret_cast<uint4*>(q) =
+                                make_uint4(held[i].c[j][0], held[i].c[j][1], held[i].c[j][2], held[i].c[j][3]);
+                    }
+                }
+            }
+            __syncthreads();  // the destination-major tile is written
+            // Each column run is written by LPR lanes (8 for bytes, 16 for
+            // 2-byte words), lane k holding the run's 16-byte granule k (two
+            // 8-byte or one 16-byte shared load; a half or quarter warp reads
+            // whole 128-byte stretches, no bank conflict) and taking
+            // granule k + 1 from its neighbour by shuffles.  Its aligned
+            // destination word k (run bytes fb + 16 k ..) is bytes fb.. of
+            // that pair: the words are picked by two selects on fb / 4 and
+            // joined by funnel shifts on fb mod 4.
+            constexpr int LPR = sizeof(W) == 1 ? 8 : 16;  // lanes per column run (TB * sizeof(W) / 16)
+            constexpr int CPI = 32 / LPR;                 // columns per warp step
+            static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
+            const int k = l & (LPR - 1);
+            const int rbb = rb * (int)sizeof(W);  // fetched bytes of a column
+#pragma unroll 1
+            for (int it = 0; it < TA / (8 * CPI); ++it) {
+                const int ia = (it * 8 + w) * CPI + l / LPR;
+                const bool mine = ia >= lo && (!SHORT || ia < hi);  // one of this tile's columns
+                unsigned char* const pc = reinterpret_cast<unsigned char*>(dst + ad.dst_a(ia) + ad.dst_b(0));
+                const int fb = (int)((16u - (unsigned)((uintptr_t)pc & 15u)) & 15u);  // bytes before its first aligned word
+                const unsigned char* const g = dm + ia * DP + 16 * k;
+                uint32_t w0, w1, w2, w3;
+                if constexpr (sizeof(W) == 1) {
+                    const uint2 a = BMMC_SH_OK(g, 8) ? *reinterpret_cast<const uint2*>(g) : make_uint2(0u, 0u);
+                    const uint2 b = BMMC_SH_OK(g + 8, 8) ? *reinterpret_cast<const uint2*>(g + 8) : make_uint2(0u, 0u);
+                    w0 = a.x, w1 = a.y, w2 = b.x, w3 = b.y;
+                } else {
+                    const uint4 a = BMMC_SH_OK(g, 16) ? *reinterpret_cast<const uint4*>(g) : make_uint4(0u, 0u, 0u, 0u);
+                    w0 = a.x, w1 = a.y, w2 = a.z, w3 = a.w;
+                }
+                const uint32_t n0 = __shfl_down_sync(0xffffffffu, w0, 1, LPR), n1 = __shfl_down_sync(0xffffffffu, w1, 1, LPR),
+                               n2 = __shfl_down_sync(0xffffffffu, w2, 1, LPR), n3 = __shfl_down_sync(0xffffffffu, w3, 1, LPR);
+                const bool q2 = (fb & 8) != 0, q1 = (fb & 4) != 0;
+                const uint32_t y0 = q2 ? w2 : w0, y1 = q2 ? w3 : w1, y2 = q2 ? n0 : w2, y3 = q2 ? n1 : w3,
+                               y4 = q2 ? n2 : n0, y5 = q2 ? n3 : n1;
+                const uint32_t z0 = q1 ? y1 : y0, z1 = q1 ? y2 : y1, z2 = q1 ? y3 : y2, z3 = q1 ? y4 : y3,
+                               z4 = q1 ? y5 : y4;
+                const uint32_t sh = 8u * (uint32_t)(fb & 3);
+                const uint4 word = make_uint4(__funnelshift_r(z0, z1, sh), __funnelshift_r(z1, z2, sh),
+                                              __funnelshift_r(z2, z3, sh), __funnelshift_r(z3, z4, sh));
+                const int b = fb + 16 * k;
+                if (mine && k < NB) {
+                    if (b + 16 <= rbb) {
+                        if (BMMC_OUT_OK(pc + b, 16)) __stcs(reinterpret_cast<uint4*>(pc + b), word);
+                    } else if (b < rbb) {
+                        store_bytes16(pc + b, word, rbb - b);
+                    }
+                }
+                if (mine && first_b && k == 0 && fb > 0) store_bytes16(pc, make_uint4(w0, w1, w2, w3), fb < rbb ? fb : rbb);
+            }
+            return;
+        } else if constexpr (!SHIFT) {
 #pragma unroll 1
             for (int i = 0; i < ITEMS; ++i) {
                 const int x = w + 8 * i;
@@ -1147,8 +1344,11 @@ __global__ void __launch_bounds__(256)
 // time, bit 6 = the 1- and 2-byte pack path for destination columns that
 // are not 16-byte aligned (realigned to 8-byte words by lane shuffles; set
 // with bit 2), bit 7 = group A is shorter than one tile (its one tile along A
-// takes the chunk path, fetching and storing only its columns).  Bit 5 is the
-// launcher's 64-bit offset flag.
+// takes the chunk path, fetching and storing only its columns), bit 8 = the
+// 1- and 2-byte pack path for such destination columns restaged destination-
+// major in shared memory (128-row tiles stepped by 128 - 16 / sizeof(W) rows
+// along B, each column written as whole aligned 16-byte words; set with bit 2
+// instead of bit 6).  Bit 5 is the launcher's 64-bit offset flag.
 enum {
     kTileLinear = 0,
     kTileTables = 1,
@@ -1159,12 +1359,14 @@ enum {
     kTileTall = 16,
     kTileWide = 32,  // 64-bit offsets: the launcher's key bit, never a kernel MODE bit
     kTileShift = 64,
-    kTileShort = 128
+    kTileShort = 128,
+    kTileStaged = 256
 };
 
 static_assert(kTileTables == LMAD_TILE_TABLES && kTileChunked == LMAD_TILE_CHUNKED && kTilePack == LMAD_TILE_PACKS &&
                   kTileHalfRows == LMAD_TILE_HALF_ROWS && kTileTall == LMAD_TILE_TALL && kTileWide == LMAD_TILE_WIDE &&
-                  kTileShift == LMAD_TILE_REALIGNED && kTileShort == LMAD_TILE_SHORT_A,
+                  kTileShift == LMAD_TILE_REALIGNED && kTileShort == LMAD_TILE_SHORT_A &&
+                  kTileStaged == LMAD_TILE_STAGED,
               "the query reports the kernel's mode bits as the header's flags");
 
 template <typename W, int MODE>
@@ -1173,7 +1375,7 @@ constexpr int tile_min_blocks() {
     // registers without spills (the 64-register tall version spilled and ran
     // 15% slower)
     return (MODE & kTileTall)    ? ((MODE & kTileShift) ? 3 : 4)
-           : (MODE & kTileShift) ? 4
+           : (MODE & (kTileShift | kTileStaged)) ? 4
            : (MODE & kTilePack) ? (sizeof(W) == 1 ? ((MODE & kTileTables) ? 5 : LMAD_BYTE_BLOCKS) : sizeof(W) == 2 ? 5 : 4)
            : (MODE & kTileChunked) ? 6
                                    : (sizeof(W) == 4 ? 8 : 6);
@@ -1206,6 +1408,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
     constexpr bool PACK = (MODE & kTilePack) != 0;
     constexpr bool SHIFT = (MODE & kTileShift) != 0;
+    constexpr bool STAGE = (MODE & kTileStaged) != 0;
     constexpr bool SHORT = (MODE & kTileShort) != 0;
     __shared__ O tab_src[GENERAL ? kTab : 1], tab_dst[GENERAL ? kTab : 1];  // A entries at [0, TA), B at [TA, TA + TB)
     BMMC_CHK_ENTER(tile, DYN ? chk::dyn_smem_bytes() : (uint32_t)sizeof(tile_s), tab_src, (uint32_t)sizeof(tab_src),
@@ -1213,12 +1416,13 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     const int TA = 1 << p.la, TB = 1 << p.lb;
     const int t = threadIdx.x;
     for (uint64_t blk = blockIdx.x; blk < p.tiles; blk += gridDim.x) {
-        // tiles along A fastest; the realigned packs take tiles along B
-        // fastest, so the two tiles that write the halves of a destination
-        // sector at their common B edge run at the same time
+        // tiles along A fastest; the realigned and staged packs take tiles
+        // along B fastest, so the two tiles that write the halves of a
+        // destination sector at their common B edge (or that both fetch the
+        // rows they share) run at the same time
         I x = (I)blk;
         I ta, tb, q;
-        if constexpr (SHIFT) {
+        if constexpr (SHIFT || STAGE) {
             q = div_q(x, p.div_tb);
             tb = x - q * (I)p.div_tb.d;
             x = q;
@@ -1245,7 +1449,9 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             d += (O)r * (O)p.ct[k];
         }
         I a0 = ta << p.la;
-        const I b0 = tb << p.lb;
+        // staged tiles step by TB - 16 / sizeof(W) rows along B (neighbours
+        // share a destination word's rows)
+        const I b0 = STAGE ? tb * (I)(TB - 16 / (int)sizeof(W)) : tb << p.lb;
         int ra = (int)min((uint64_t)TA, p.n_a - (uint64_t)a0);
         const int rb = (int)min((uint64_t)TB, p.n_b - (uint64_t)b0);
         // the chunk path takes a ragged last A tile shifted back to end at
@@ -1300,8 +1506,8 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             const TabAddr<O> ad{tab_src, tab_dst, TA, 0};
             if (CHUNKED && (ra == TA || SHORT)) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, SHIFT, SHORT, NCH, TALL>(in + so + tab_src[0], out + d, tile, ad,
-                                                                              rb, lo, ra);
+                    tile_phases_chunked<W, O, PACK, SHIFT, STAGE, SHORT, NCH, TALL>(in + so + tab_src[0], out + d,
+                                                                                     tile, ad, rb, lo, ra, b0 == 0);
             } else if constexpr (TALL > 1) {
                 // a ragged-A tall tile: the element path, a quarter of the rows at a time
                 constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
@@ -1321,7 +1527,8 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             W* dst = out + d + (O)a0 * ad.ta + (O)b0 * ad.tb;
             if (CHUNKED && (ra == TA || SHORT)) {
                 if constexpr (CHUNKED)
-                    tile_phases_chunked<W, O, PACK, SHIFT, SHORT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra);
+                    tile_phases_chunked<W, O, PACK, SHIFT, STAGE, SHORT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra,
+                                                                                     b0 == 0);
             } else if constexpr (TALL > 1) {
                 constexpr int QB = S::T >> 8;
                 for (int j = 0; j * QB < rb; ++j) {
@@ -1986,7 +2193,12 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     // carry joins them (partial words once per 128 rows instead of per 64)
     const bool halve = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
     const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (halve ? 1 : 0);
-    const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + (1ull << lb) - 1) >> lb;
+    // 128-row tiles of these (tall byte tiles, 64 x 128 tiles of 2-byte
+    // words) restage the tile destination-major instead, stepping by
+    // 128 - 16 / word rows along B
+    const bool staged = LMAD_TILE_STAGE && shift && lb == 7 && (tall || (word == 2 && la == 6));
+    const uint64_t step_b = staged ? (1ull << lb) - 16 / word : (1ull << lb);
+    const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + step_b - 1) / step_b;
     const uint64_t tiles = tiles_a * tiles_b * batch;
     // masked lanes of a ragged tile form (unused) offsets up to one tile side
     // past the span; 32-bit offsets must hold those too
@@ -2003,7 +2215,7 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     // own (32-bit offsets; with 64-bit ones its tiles take the element path)
     const bool short_a = chunked && word <= 4 && n_a < (1ull << la) && !wide;
     L.mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
-             (pack || shift ? kTilePack : 0) | (shift ? kTileShift : 0) |
+             (pack || shift ? kTilePack : 0) | (shift && !staged ? kTileShift : 0) | (staged ? kTileStaged : 0) |
              (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0) |
              (short_a ? kTileShort : 0) | (wide ? kTileWide : 0);
     L.la = la;
@@ -2080,6 +2292,12 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                 case 151: LMAD_TALL(false, 151); break;
                 case 214: LMAD_TALL(false, 214); break;
                 case 215: LMAD_TALL(false, 215); break;
+                case 278: LMAD_TALL(false, 278); break;
+                case 279: LMAD_TALL(false, 279); break;
+                case 310: LMAD_TALL(true, 278); break;
+                case 311: LMAD_TALL(true, 279); break;
+                case 406: LMAD_TALL(false, 406); break;
+                case 407: LMAD_TALL(false, 407); break;
                 default: return cudaErrorInvalidValue;
             }
 #undef LMAD_TALL
@@ -2104,7 +2322,16 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                             case 199: LMAD_TILE(false, 199); break;
                             case 206: LMAD_TILE(false, 206); break;
                             case 207: LMAD_TILE(false, 207); break;
-                            default: return cudaErrorInvalidValue;
+                            default:
+                                if constexpr (sizeof(W) == 2) {
+                                    switch (mode) {
+                                        case 398: LMAD_TILE(false, 398); break;
+                                        case 399: LMAD_TILE(false, 399); break;
+                                        default: return cudaErrorInvalidValue;
+                                    }
+                                    break;
+                                }
+                                return cudaErrorInvalidValue;
                         }
                         break;
                     }
@@ -2143,7 +2370,18 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                             case 103: LMAD_TILE(true, 71); break;
                             case 110: LMAD_TILE(true, 78); break;
                             case 111: LMAD_TILE(true, 79); break;
-                            default: return cudaErrorInvalidValue;
+                            default:
+                                if constexpr (sizeof(W) == 2) {
+                                    switch (mode | (wide ? kWide : 0)) {
+                                        case 270: LMAD_TILE(false, 270); break;
+                                        case 271: LMAD_TILE(false, 271); break;
+                                        case 302: LMAD_TILE(true, 270); break;
+                                        case 303: LMAD_TILE(true, 271); break;
+                                        default: return cudaErrorInvalidValue;
+                                    }
+                                    break;
+                                }
+                                return cudaErrorInvalidValue;
                         }
                         break;
                     }

@@ -420,6 +420,12 @@ typedef struct {
                                       16-byte aligned) */
 #define LMAD_TILE_SHORT_A   0x80u  /* group A shorter than one tile: only its columns fetched
                                       and stored */
+#define LMAD_TILE_STAGED    0x100u /* destination columns not 16-byte aligned, 1- and 2-byte
+                                      words on 128-row tiles: the tile is restaged
+                                      destination-major in shared memory and each column
+                                      written as whole aligned 16-byte words; tiles step by
+                                      launch_tile_b - 16 / elem_size B-indices, so neighbours
+                                      share the rows of one destination word */
 
 /* Analyse the copy lmad_copy would run with the same arguments, without
  * touching memory or the device.  in / out are used for their alignment and

@@ -403,20 +403,24 @@ def _transpose_2d(R, C, out_off=0, out_pitch=None):
 @pytest.mark.parametrize("R,C,elem,out_off,out_pitch,mode,launch_tile", [
     # aligned byte transpose with a long B: register packs in 256 x 128 tiles
     (16384, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
-    # destination columns at odd offsets: the packs are realigned
-    (16385, 16384, 1, 0, None, {"chunked", "packs", "tall", "realigned"}, (256, 128)),
-    (16384, 16384, 1, 3, None, {"chunked", "packs", "tall", "realigned"}, (256, 128)),
+    # destination columns at odd offsets: tall tiles restaged destination-major
+    (16385, 16384, 1, 0, None, {"chunked", "packs", "tall", "staged"}, (256, 128)),
+    (16384, 16384, 1, 3, None, {"chunked", "packs", "tall", "staged"}, (256, 128)),
+    # ... but stay realigned in 256 x 32 tiles when B is short
+    (48, 16384, 1, 3, None, {"chunked", "packs", "realigned"}, (256, 32)),
     # a B of under 64 rows keeps 256 x 32 tiles
     (32, 16384, 1, 0, None, {"chunked", "packs"}, (256, 32)),
     (48, 16384, 1, 0, None, {"chunked", "packs"}, (256, 32)),
     (64, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
     (160, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
-    # 2-byte words: aligned packs in 128 x 64 tiles; realigned ones in 64 x 128
+    # 2-byte words: aligned packs in 128 x 64 tiles; unaligned columns staged
+    # in 64 x 128 tiles (realigned in 128 x 64 ones when B is short)
     (8192, 8192, 2, 0, None, {"chunked", "packs"}, (128, 64)),
-    (11585, 11587, 2, 0, None, {"chunked", "packs", "half_rows", "realigned"}, (64, 128)),
+    (11585, 11587, 2, 0, None, {"chunked", "packs", "half_rows", "staged"}, (64, 128)),
+    (100, 8192, 2, 0, 101, {"chunked", "packs", "realigned"}, (128, 64)),
     # groups A shorter than a tile take the chunk path in their own kernels
     (300, 48, 2, 0, 304, {"chunked", "packs", "half_rows", "short_a"}, (64, 128)),
-    (300, 48, 2, 0, None, {"chunked", "packs", "half_rows", "realigned", "short_a"}, (64, 128)),
+    (300, 48, 2, 0, None, {"chunked", "packs", "half_rows", "staged", "short_a"}, (64, 128)),
     (300, 100, 1, 0, 304, {"chunked", "packs", "half_rows", "short_a"}, (128, 64)),
     (300, 17, 4, 0, None, {"chunked", "half_rows", "short_a"}, (32, 128)),
     # 4-byte words: chunks, element stores; 8-byte words: the element path
@@ -426,9 +430,10 @@ def _transpose_2d(R, C, out_off=0, out_pitch=None):
 def test_tile_kernel_variant_choice(R, C, elem, out_off, out_pitch, mode, launch_tile):
     """The query reports the tile kernel variant a transpose launches with:
     register packs when B walks the destination forwards from stride 1 (1- and
-    2-byte words), realigned when a destination column is not 16-byte
-    aligned, tall byte tiles for a long B, 64 x 128 tiles for realigned 2-byte
-    words, separate kernels for a group A shorter than a tile."""
+    2-byte words), tall byte tiles for a long B, and when a destination
+    column is not 16-byte aligned either staged (128-row tiles: tall byte
+    tiles, 64 x 128 tiles of 2-byte words) or realigned (shorter B),
+    separate kernels for a group A shorter than a tile."""
     w = _transpose_2d(R, C, out_off, out_pitch)
     q = _query(w, elem)
     assert q["kind"] == "transpose" and not q["narrow"]
@@ -439,11 +444,14 @@ def test_tile_kernel_variant_choice(R, C, elem, out_off, out_pitch, mode, launch
 
 def test_tile_kernel_variant_follows_destination_alignment():
     """The same copy into a destination whose origin is 16-byte aligned takes
-    aligned packs, into one 8 bytes off it realigned packs (the query reads
-    the alignment from the out address)."""
+    aligned packs, into one 8 bytes off it staged packs, or realigned ones
+    when B is short (the query reads the alignment from the out address)."""
     w = _transpose_2d(4096, 4096)
-    assert "realigned" not in _query(w, 1, out=1 << 20)["tile_mode"]
-    assert "realigned" in _query(w, 1, out=(1 << 20) + 8)["tile_mode"]
+    m = _query(w, 1, out=1 << 20)["tile_mode"]
+    assert "realigned" not in m and "staged" not in m
+    m = _query(w, 1, out=(1 << 20) + 8)["tile_mode"]
+    assert "staged" in m and "realigned" not in m
+    assert "realigned" in _query(_transpose_2d(32, 4096), 1, out=(1 << 20) + 8)["tile_mode"]
 
 
 def test_tile_kernel_variant_with_64_bit_offsets():
@@ -610,4 +618,85 @@ def test_realigned_pack_store_schedule_replay(seed):
     out_pitch = R + int(rng.integers(0, 9))
     out_off = int(rng.integers(0, 16))
     mem, cnt, want = _realigned_store_replay(R, C, elem, out_pitch, out_off, nch, tall)
+    assert (cnt <= 1).all() and np.array_equal(mem, want)
+
+
+def _staged_store_replay(R, C, elem, out_pitch, out_off):
+    """The staged store schedule of the tile kernel replayed on the host for
+    the transpose of a row-major [R][C] array of 1- or 2-byte words into
+    columns of pitch out_pitch (B = R rows, destination stride 1; A = C
+    columns): 128-row tiles (256 x 128 for bytes, 64 x 128 for 2-byte words)
+    stepped by 128 - 16 / elem rows along B, the last A tile shifted back (or,
+    for a group A shorter than a tile, its columns masked); each column of a
+    tile holds its fetched rows as one run, and writes the aligned 16-byte
+    words starting in its first 128 - 16 / elem rows, each formed from the
+    run's aligned 4-byte words by funnel shifts, cut at the last fetched row,
+    plus (B index 0 only) the partial word before the first aligned one.
+    Returns the byte image written and how often each byte was written."""
+    V, TB = 16 // elem, 128
+    TA = 256 if elem == 1 else 64
+    STEP, NB = TB - V, (TB - V) // V
+    out_bytes = (out_off + (C - 1) * out_pitch + R) * elem
+    mem = np.full(out_bytes + 64, -1, dtype=np.int64)
+    cnt = np.zeros(out_bytes + 64, dtype=np.int64)
+
+    def val(a, b, k):
+        return ((b * C + a) * elem + k) % 251
+
+    def write(addr, vals):
+        for i, v in enumerate(vals):
+            mem[addr + i] = v
+            cnt[addr + i] += 1
+
+    def funnel(lo, hi, sh):
+        return ((hi << 32 | lo) >> sh) & 0xFFFFFFFF
+
+    for ta in range((C + TA - 1) // TA):
+        for tb in range((R + STEP - 1) // STEP):
+            a0, b0 = ta * TA, tb * STEP
+            ra, rb, lo = min(TA, C - a0), min(TB, R - b0), 0
+            hi = ra
+            if ra < TA and C >= TA:
+                lo, a0, ra, hi = TA - ra, C - TA, TA, TA
+            for ia in range(lo, hi):
+                # the column's run: fetched rows hold their bytes, the rest is stale
+                run = [val(a0 + ia, b0 + ib, k) if ib < rb else 255 for ib in range(TB) for k in range(elem)]
+                pc = (out_off + (a0 + ia) * out_pitch + b0) * elem
+                fb, rbb = (16 - pc % 16) % 16, rb * elem
+                wp = [int.from_bytes(bytes(run[(fb & ~3) + 4 * i:(fb & ~3) + 4 * i + 4]), "little")
+                      for i in range((TB * elem - (fb & ~3)) // 4)]
+                sh = 8 * (fb & 3)
+                for k in range(NB):
+                    words = [funnel(wp[4 * k + i], wp[4 * k + i + 1], sh) for i in range(4)]
+                    data = list(b"".join(x.to_bytes(4, "little") for x in words))
+                    b = fb + 16 * k
+                    assert (pc + b) % 16 == 0
+                    if b + 16 <= rbb:
+                        write(pc + b, data)
+                    elif b < rbb:
+                        write(pc + b, data[:rbb - b])
+                if b0 == 0 and fb > 0:
+                    write(pc, run[:min(fb, rbb)])
+    want = np.full(out_bytes + 64, -1, dtype=np.int64)
+    for a in range(C):
+        for b in range(R):
+            for k in range(elem):
+                want[(out_off + a * out_pitch + b) * elem + k] = val(a, b, k)
+    return mem, cnt, want
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_staged_store_schedule_replay(seed):
+    """Every destination byte of a transpose into unaligned columns is
+    written exactly once with its value, and nothing else is written, by the
+    staged store schedule (host replay; whole, ragged and shifted tiles,
+    short groups A, B shorter than one step, every column phase)."""
+    rng = np.random.default_rng(1000 + seed)
+    elem = (1, 2)[seed % 2]
+    TA = 256 if elem == 1 else 64
+    C = int(rng.choice([TA // 2 + 3, TA - 5, TA + 7, 2 * TA - 1]))
+    R = int(rng.choice([5, 64 + 3, 128 - 16 // elem, 128, 200, 3 * 128 - 7]))
+    out_pitch = R + int(rng.integers(0, 17))
+    out_off = int(rng.integers(0, 16))
+    mem, cnt, want = _staged_store_replay(R, C, elem, out_pitch, out_off)
     assert (cnt <= 1).all() and np.array_equal(mem, want)
