@@ -560,7 +560,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     constexpr int ROT = STAGE ? 0 : REG && sizeof(W) == 1 ? 2 : 1;
     constexpr int PH = REG && sizeof(W) == 2 ? 8 : 4;
     static_assert(NCH + 1 + ROT * (PH - 1) <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
-    static_assert(TALL == 1 || (REG && sizeof(W) == 1), "tall tiles on the 1-byte pack path only");
+    static_assert(TALL == 1 || (REG && (sizeof(W) == 1 || STAGE)), "tall tiles on the 1-byte or staged pack path only");
     static_assert(!SHIFT || REG, "realigned packs on the 1- and 2-byte register path only");
     static_assert(!STAGE || (REG && !SHIFT && TB == 128), "staged columns: 1- and 2-byte words, 128-row tiles");
     const int t = threadIdx.x;
@@ -753,17 +753,23 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                         v[k] = BMMC_SH_OK(p + k * (kPitch * (int)sizeof(W) / 4), 4) ? p[k * (kPitch * (int)sizeof(W) / 4)]
                                                                                     : 0u;
                 } else {
+                    // rows with their own misalignments (mb bytes): two
+                    // aligned loads and a funnel shift each where mb is not
+                    // a multiple of 4 (three rows in four for bytes, which
+                    // take the two loads unconditionally; one in two for
+                    // 2-byte words, under a warp-uniform branch)
+                    const unsigned char* const rowp = sb + r0 * kPitch * (int)sizeof(W) + 4 * wi;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const int mk = (int)((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1));
-                        const int byte = ((r0 + k) * kPitch + mk) * (int)sizeof(W) + 4 * wi;
-                        const uint32_t* p = reinterpret_cast<const uint32_t*>(sb + (byte & ~3));
+                        const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
+                        const uint32_t* p =
+                            reinterpret_cast<const uint32_t*>(rowp + k * kPitch * (int)sizeof(W) + (mb & ~3));
                         const uint32_t a = BMMC_SH_OK(p, 4) ? p[0] : 0u;
-                        if ((byte & 3) == 0) {  // warp-uniform: one row per load
-                            v[k] = a;
-                        } else {
+                        if (sizeof(W) == 1 || (mb & 3) != 0) {
                             const uint32_t b = BMMC_SH_OK(p + 1, 4) ? p[1] : 0u;
-                            v[k] = __funnelshift_r(a, b, 8 * (byte & 3));
+                            v[k] = __funnelshift_r(a, b, 8 * (mb & 3));
+                        } else {
+                            v[k] = a;
                         }
                     }
                 }
@@ -1339,9 +1345,10 @@ __global__ void __launch_bounds__(256)
 // offsets), bit 1 = tiles with the default shape whose A side is whole take
 // the 16-byte chunk path, bit 2 = that path writes 16-byte packs along B,
 // bit 3 = the chunk path with 128-byte source rows (8 chunks) instead of 256,
-// bit 4 = tall tiles (1-byte pack path, 256-byte rows): four times the rows,
-// 256 x 128, with ragged-A tiles taken by the element path a quarter at a
-// time, bit 6 = the 1- and 2-byte pack path for destination columns that
+// bit 4 = tall tiles (1-byte pack path and 2-byte staged path, 256-byte
+// rows): four times the rows for bytes, 256 x 128, twice for 2-byte words,
+// 128 x 128, with ragged-A tiles taken by the element path a quarter (half)
+// of the rows at a time, bit 6 = the 1- and 2-byte pack path for destination columns that
 // are not 16-byte aligned (realigned to 8-byte words by lane shuffles; set
 // with bit 2), bit 7 = group A is shorter than one tile (its one tile along A
 // takes the chunk path, fetching and storing only its columns), bit 8 = the
@@ -1373,9 +1380,12 @@ template <typename W, int MODE>
 constexpr int tile_min_blocks() {
     // the realigned packs hold more per column (carries, shifts): 76 and 64
     // registers without spills (the 64-register tall version spilled and ran
-    // 15% slower)
-    return (MODE & kTileTall)    ? ((MODE & kTileShift) ? 3 : 4)
-           : (MODE & (kTileShift | kTileStaged)) ? 4
+    // 15% slower); staged tall tiles hold a 32 KiB tile in registers between
+    // the two shared layouts (64 registers, 85 with offset tables), staged
+    // 64 x 128 tiles half that (48)
+    return (MODE & kTileTall) ? (((MODE & kTileShift) || ((MODE & kTileStaged) && (MODE & kTileTables))) ? 3 : 4)
+           : (MODE & kTileStaged) ? 5
+           : (MODE & kTileShift) ? 4
            : (MODE & kTilePack) ? (sizeof(W) == 1 ? ((MODE & kTileTables) ? 5 : LMAD_BYTE_BLOCKS) : sizeof(W) == 2 ? 5 : 4)
            : (MODE & kTileChunked) ? 6
                                    : (sizeof(W) == 4 ? 8 : 6);
@@ -1388,7 +1398,8 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     using O = typename std::conditional<WIDE, int64_t, int32_t>::type;
     using S = TileShape<sizeof(W)>;
     using Sides = TileSides<S::T>;
-    constexpr int TALL = (MODE & kTileTall) ? 4 : 1;
+    // tall tiles: 256 x 128 bytes, 128 x 128 2-byte words
+    constexpr int TALL = (MODE & kTileTall) ? (sizeof(W) == 1 ? 4 : 2) : 1;
     constexpr int kTab = Sides::kMax + Sides::kMin * TALL;  // >= TA + TB
     constexpr int kElemTile = S::T + Sides::kMax * S::PAD;
     constexpr int NCH = (MODE & kTileHalfRows) ? 8 : 16;  // chunk path: chunks per source row
@@ -1402,7 +1413,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     __shared__ __align__(16) W tile_s[DYN ? 1 : (kElemTile > kChunkTile ? kElemTile : kChunkTile)];
     extern __shared__ __align__(16) unsigned char lmad_dyn_smem[];
     W* const tile = DYN ? reinterpret_cast<W*>(lmad_dyn_smem) : tile_s;
-    static_assert(!DYN || (sizeof(W) == 1 && kChunkTile == kTallTileBytes && kElemTile <= kChunkTile),
+    static_assert(!DYN || (sizeof(W) <= 2 && kChunkTile * (int)sizeof(W) == kTallTileBytes && kElemTile <= kChunkTile),
                   "the launcher's dynamic shared memory holds the tall tile");
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
@@ -1509,12 +1520,13 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
                     tile_phases_chunked<W, O, PACK, SHIFT, STAGE, SHORT, NCH, TALL>(in + so + tab_src[0], out + d,
                                                                                      tile, ad, rb, lo, ra, b0 == 0);
             } else if constexpr (TALL > 1) {
-                // a ragged-A tall tile: the element path, a quarter of the rows at a time
-                constexpr int QB = S::T >> 8;  // rows of a quarter (A side 256)
+                // a ragged-A tall tile: the element path, 1 / TALL of the rows at a time
+                constexpr int QB = S::T / (NCH * (16 / (int)sizeof(W)));  // rows of a part (A side of the chunk path)
                 for (int j = 0; j * QB < rb; ++j) {
                     if (j) __syncthreads();
                     const TabAddr<O> aq{tab_src, tab_dst, TA, j * QB};
-                    tile_phases<W, false>(in + so, out + d, tile, aq, TA, QB, p.la, p.lb - 2, ra, min(QB, rb - j * QB));
+                    tile_phases<W, false>(in + so, out + d, tile, aq, TA, QB, p.la, p.lb - clog2(TALL), ra,
+                                          min(QB, rb - j * QB));
                 }
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(in + so, out + d, tile, ad, TA, TB, p.la, p.lb, ra, rb);
@@ -1530,11 +1542,11 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
                     tile_phases_chunked<W, O, PACK, SHIFT, STAGE, SHORT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra,
                                                                                      b0 == 0);
             } else if constexpr (TALL > 1) {
-                constexpr int QB = S::T >> 8;
+                constexpr int QB = S::T / (NCH * (16 / (int)sizeof(W)));
                 for (int j = 0; j * QB < rb; ++j) {
                     if (j) __syncthreads();
                     tile_phases<W, false>(src + (O)(j * QB) * ad.sb, dst + (O)(j * QB) * ad.tb, tile, ad, TA, QB, p.la,
-                                          p.lb - 2, ra, min(QB, rb - j * QB));
+                                          p.lb - clog2(TALL), ra, min(QB, rb - j * QB));
                 }
             } else if (ra == TA && rb == TB) {
                 tile_phases<W, true>(src, dst, tile, ad, TA, TB, p.la, p.lb, ra, rb);
@@ -2188,15 +2200,18 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     // at least 64 rows (a ragged last tall tile works only on its rows;
     // measured no slower than 256 x 32 tiles from 64 rows up)
     const bool tall = LMAD_BYTE_TALL && word == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 64;
-    // realigned 2-byte packs take 64 x 128 tiles (128-byte source rows), so a
-    // thread's two items are the two row sets of one column stripe and the
-    // carry joins them (partial words once per 128 rows instead of per 64)
-    const bool halve = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
-    const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (halve ? 1 : 0);
-    // 128-row tiles of these (tall byte tiles, 64 x 128 tiles of 2-byte
-    // words) restage the tile destination-major instead, stepping by
-    // 128 - 16 / word rows along B
-    const bool staged = LMAD_TILE_STAGE && shift && lb == 7 && (tall || (word == 2 && la == 6));
+    // 2-byte words with a B of at least 128 rows into such destinations take
+    // 128 x 128 tiles restaged destination-major (below), or without that
+    // path 64 x 128 realigned tiles (128-byte source rows, so a thread's two
+    // items are the two row sets of one column stripe and the carry joins
+    // them: partial words once per 128 rows instead of per 64)
+    const bool long2 = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
+    const bool tall2 = LMAD_TILE_STAGE && long2, halve = !LMAD_TILE_STAGE && long2;
+    const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (tall2 || halve ? 1 : 0);
+    // 128-row tiles of these (tall byte tiles, 128 x 128 or, for a group A
+    // shorter than 128, 64 x 128 tiles of 2-byte words) restage the tile
+    // destination-major instead, stepping by 128 - 16 / word rows along B
+    const bool staged = LMAD_TILE_STAGE && shift && lb == 7 && (tall || tall2 || (word == 2 && la == 6));
     const uint64_t step_b = staged ? (1ull << lb) - 16 / word : (1ull << lb);
     const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + step_b - 1) / step_b;
     const uint64_t tiles = tiles_a * tiles_b * batch;
@@ -2216,7 +2231,7 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     const bool short_a = chunked && word <= 4 && n_a < (1ull << la) && !wide;
     L.mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
              (pack || shift ? kTilePack : 0) | (shift && !staged ? kTileShift : 0) | (staged ? kTileStaged : 0) |
-             (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall ? kTileTall : 0) |
+             (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall || tall2 ? kTileTall : 0) |
              (short_a ? kTileShort : 0) | (wide ? kTileWide : 0);
     L.la = la;
     L.lb = lb;
@@ -2270,7 +2285,7 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     const int mode = L.mode & ~kTileWide;
     constexpr int kWide = kTileWide;
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()))
-    if constexpr (sizeof(W) == 1) {
+    if constexpr (sizeof(W) <= 2) {
         if (mode & kTileTall) {
 #define LMAD_TALL(WV, MV)                                                                              \
     do {                                                                                               \
@@ -2279,7 +2294,17 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         lmad_tile_kernel<W, WV, MV><<<grid, 256, kTallTileBytes, stream>>>(in, out,                    \
                                                                           p BMMC_CHK_ARG(lmad_bounds())); \
     } while (0)
-            switch (mode | (wide ? kWide : 0)) {
+            if constexpr (sizeof(W) == 2) {
+                switch (mode | (wide ? kWide : 0)) {
+                    case 278: LMAD_TALL(false, 278); break;
+                    case 279: LMAD_TALL(false, 279); break;
+                    case 310: LMAD_TALL(true, 278); break;
+                    case 311: LMAD_TALL(true, 279); break;
+                    case 406: LMAD_TALL(false, 406); break;
+                    case 407: LMAD_TALL(false, 407); break;
+                    default: return cudaErrorInvalidValue;
+                }
+            } else switch (mode | (wide ? kWide : 0)) {
                 case 22: LMAD_TALL(false, 22); break;
                 case 23: LMAD_TALL(false, 23); break;
                 case 54: LMAD_TALL(true, 22); break;

@@ -414,7 +414,7 @@ typedef struct {
 #define LMAD_TILE_PACKS     0x04u  /* 1- and 2-byte words: register transposes written in packs
                                       along B */
 #define LMAD_TILE_HALF_ROWS 0x08u  /* 128-byte source rows instead of 256 */
-#define LMAD_TILE_TALL      0x10u  /* 256 x 128 byte tiles */
+#define LMAD_TILE_TALL      0x10u  /* 256 x 128 byte tiles, 128 x 128 2-byte tiles (staged) */
 #define LMAD_TILE_WIDE      0x20u  /* 64-bit offsets */
 #define LMAD_TILE_REALIGNED 0x40u  /* packs realigned to 8-byte words (destination columns not
                                       16-byte aligned) */

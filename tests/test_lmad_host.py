@@ -414,9 +414,9 @@ def _transpose_2d(R, C, out_off=0, out_pitch=None):
     (64, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
     (160, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
     # 2-byte words: aligned packs in 128 x 64 tiles; unaligned columns staged
-    # in 64 x 128 tiles (realigned in 128 x 64 ones when B is short)
+    # in 128 x 128 tiles (realigned in 128 x 64 ones when B is short)
     (8192, 8192, 2, 0, None, {"chunked", "packs"}, (128, 64)),
-    (11585, 11587, 2, 0, None, {"chunked", "packs", "half_rows", "staged"}, (64, 128)),
+    (11585, 11587, 2, 0, None, {"chunked", "packs", "tall", "staged"}, (128, 128)),
     (100, 8192, 2, 0, 101, {"chunked", "packs", "realigned"}, (128, 64)),
     # groups A shorter than a tile take the chunk path in their own kernels
     (300, 48, 2, 0, 304, {"chunked", "packs", "half_rows", "short_a"}, (64, 128)),
@@ -432,14 +432,15 @@ def test_tile_kernel_variant_choice(R, C, elem, out_off, out_pitch, mode, launch
     register packs when B walks the destination forwards from stride 1 (1- and
     2-byte words), tall byte tiles for a long B, and when a destination
     column is not 16-byte aligned either staged (128-row tiles: tall byte
-    tiles, 64 x 128 tiles of 2-byte words) or realigned (shorter B),
+    tiles, 128 x 128 (64 x 128 for a short group A) tiles of 2-byte words)
+    or realigned (shorter B),
     separate kernels for a group A shorter than a tile."""
     w = _transpose_2d(R, C, out_off, out_pitch)
     q = _query(w, elem)
     assert q["kind"] == "transpose" and not q["narrow"]
     assert set(q["tile_mode"]) == mode and q["launch_tile"] == launch_tile
     ta, tb = q["launch_tile"]
-    assert ta * tb == TILE_ELEMS[elem] * (4 if "tall" in mode else 1)
+    assert ta * tb == TILE_ELEMS[elem] * ((4 if elem == 1 else 2) if "tall" in mode else 1)
 
 
 def test_tile_kernel_variant_follows_destination_alignment():
@@ -621,12 +622,12 @@ def test_realigned_pack_store_schedule_replay(seed):
     assert (cnt <= 1).all() and np.array_equal(mem, want)
 
 
-def _staged_store_replay(R, C, elem, out_pitch, out_off):
+def _staged_store_replay(R, C, elem, out_pitch, out_off, TA):
     """The staged store schedule of the tile kernel replayed on the host for
     the transpose of a row-major [R][C] array of 1- or 2-byte words into
     columns of pitch out_pitch (B = R rows, destination stride 1; A = C
-    columns): 128-row tiles (256 x 128 for bytes, 64 x 128 for 2-byte words)
-    stepped by 128 - 16 / elem rows along B, the last A tile shifted back (or,
+    columns): TA x 128 tiles (TA = 256 for bytes, 128 or, for a group A
+    shorter than that, 64 for 2-byte words) stepped by 128 - 16 / elem rows along B, the last A tile shifted back (or,
     for a group A shorter than a tile, its columns masked); each column of a
     tile holds its fetched rows as one run, and writes the aligned 16-byte
     words starting in its first 128 - 16 / elem rows, each formed from the
@@ -634,7 +635,6 @@ def _staged_store_replay(R, C, elem, out_pitch, out_off):
     plus (B index 0 only) the partial word before the first aligned one.
     Returns the byte image written and how often each byte was written."""
     V, TB = 16 // elem, 128
-    TA = 256 if elem == 1 else 64
     STEP, NB = TB - V, (TB - V) // V
     out_bytes = (out_off + (C - 1) * out_pitch + R) * elem
     mem = np.full(out_bytes + 64, -1, dtype=np.int64)
@@ -685,18 +685,17 @@ def _staged_store_replay(R, C, elem, out_pitch, out_off):
     return mem, cnt, want
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(18))
 def test_staged_store_schedule_replay(seed):
     """Every destination byte of a transpose into unaligned columns is
     written exactly once with its value, and nothing else is written, by the
     staged store schedule (host replay; whole, ragged and shifted tiles,
     short groups A, B shorter than one step, every column phase)."""
     rng = np.random.default_rng(1000 + seed)
-    elem = (1, 2)[seed % 2]
-    TA = 256 if elem == 1 else 64
+    elem, TA = ((1, 256), (2, 128), (2, 64))[seed % 3]
     C = int(rng.choice([TA // 2 + 3, TA - 5, TA + 7, 2 * TA - 1]))
     R = int(rng.choice([5, 64 + 3, 128 - 16 // elem, 128, 200, 3 * 128 - 7]))
     out_pitch = R + int(rng.integers(0, 17))
     out_off = int(rng.integers(0, 16))
-    mem, cnt, want = _staged_store_replay(R, C, elem, out_pitch, out_off)
+    mem, cnt, want = _staged_store_replay(R, C, elem, out_pitch, out_off, TA)
     assert (cnt <= 1).all() and np.array_equal(mem, want)
