@@ -826,32 +826,42 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
             const int k = l & (LPR - 1);
             const int rbb = rb * (int)sizeof(W);  // fetched bytes of a column
-#pragma unroll 1
-            for (int it = 0; it < TA / (8 * CPI); ++it) {
-                const int ia = (it * 8 + w) * CPI + l / LPR;
+            constexpr int STEPS = TA / (8 * CPI);  // warp steps per tile
+            // One warp step for column ia.  QC: the word offset fb / 4 of
+            // every column of the step when the caller fixed it (0..3), or
+            // -1: each lane picks its words by two selects.
+            auto step = [&](const int ia, auto QC) {
+                constexpr int Q = decltype(QC)::value;
                 const bool mine = ia >= lo && (!SHORT || ia < hi);  // one of this tile's columns
                 unsigned char* const pc = reinterpret_cast<unsigned char*>(dst + ad.dst_a(ia) + ad.dst_b(0));
                 const int fb = (int)((16u - (unsigned)((uintptr_t)pc & 15u)) & 15u);  // bytes before its first aligned word
                 const unsigned char* const g = dm + ia * DP + 16 * k;
-                uint32_t w0, w1, w2, w3;
+                uint32_t wv[8];
                 if constexpr (sizeof(W) == 1) {
                     const uint2 a = BMMC_SH_OK(g, 8) ? *reinterpret_cast<const uint2*>(g) : make_uint2(0u, 0u);
                     const uint2 b = BMMC_SH_OK(g + 8, 8) ? *reinterpret_cast<const uint2*>(g + 8) : make_uint2(0u, 0u);
-                    w0 = a.x, w1 = a.y, w2 = b.x, w3 = b.y;
+                    wv[0] = a.x, wv[1] = a.y, wv[2] = b.x, wv[3] = b.y;
                 } else {
                     const uint4 a = BMMC_SH_OK(g, 16) ? *reinterpret_cast<const uint4*>(g) : make_uint4(0u, 0u, 0u, 0u);
-                    w0 = a.x, w1 = a.y, w2 = a.z, w3 = a.w;
+                    wv[0] = a.x, wv[1] = a.y, wv[2] = a.z, wv[3] = a.w;
                 }
-                const uint32_t n0 = __shfl_down_sync(0xffffffffu, w0, 1, LPR), n1 = __shfl_down_sync(0xffffffffu, w1, 1, LPR),
-                               n2 = __shfl_down_sync(0xffffffffu, w2, 1, LPR), n3 = __shfl_down_sync(0xffffffffu, w3, 1, LPR);
-                const bool q2 = (fb & 8) != 0, q1 = (fb & 4) != 0;
-                const uint32_t y0 = q2 ? w2 : w0, y1 = q2 ? w3 : w1, y2 = q2 ? n0 : w2, y3 = q2 ? n1 : w3,
-                               y4 = q2 ? n2 : n0, y5 = q2 ? n3 : n1;
-                const uint32_t z0 = q1 ? y1 : y0, z1 = q1 ? y2 : y1, z2 = q1 ? y3 : y2, z3 = q1 ? y4 : y3,
-                               z4 = q1 ? y5 : y4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) wv[4 + i] = __shfl_down_sync(0xffffffffu, wv[i], 1, LPR);
+                uint32_t z[5];
+                if constexpr (Q >= 0) {
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) z[i] = Q + i < 8 ? wv[Q + i] : 0u;
+                } else {
+                    const bool q2 = (fb & 8) != 0, q1 = (fb & 4) != 0;
+                    uint32_t y[6];
+#pragma unroll
+                    for (int i = 0; i < 6; ++i) y[i] = q2 ? wv[i + 2] : wv[i];
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) z[i] = q1 ? y[i + 1] : y[i];
+                }
                 const uint32_t sh = 8u * (uint32_t)(fb & 3);
-                const uint4 word = make_uint4(__funnelshift_r(z0, z1, sh), __funnelshift_r(z1, z2, sh),
-                                              __funnelshift_r(z2, z3, sh), __funnelshift_r(z3, z4, sh));
+                const uint4 word = make_uint4(__funnelshift_r(z[0], z[1], sh), __funnelshift_r(z[1], z[2], sh),
+                                              __funnelshift_r(z[2], z[3], sh), __funnelshift_r(z[3], z[4], sh));
                 const int b = fb + 16 * k;
                 if (mine && k < NB) {
                     if (b + 16 <= rbb) {
@@ -860,7 +870,43 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                         store_bytes16(pc + b, word, rbb - b);
                     }
                 }
-                if (mine && first_b && k == 0 && fb > 0) store_bytes16(pc, make_uint4(w0, w1, w2, w3), fb < rbb ? fb : rbb);
+                if (mine && first_b && k == 0 && fb > 0)
+                    store_bytes16(pc, make_uint4(wv[0], wv[1], wv[2], wv[3]), fb < rbb ? fb : rbb);
+            };
+            bool ordered = false;
+            if constexpr (std::is_same<Addr, LinAddr<O>>::value) {
+                ordered = (ad.ta & 1) != 0;
+                if (ordered) {
+                    // A single-dimension group A with an odd destination stride
+                    // ta: column ia starts p0 + ia * ta elements past an aligned
+                    // word (mod V), which runs through every residue as ia runs
+                    // through V consecutive columns.  Step s of the tile takes,
+                    // from columns V * (s / 4) .. + V - 1, the CPI columns whose
+                    // first aligned word is fb = 4 (s mod 4) .. 4 (s mod 4) + 3
+                    // bytes away: ia = V * (s / 4) + (-(fb / e) - p0) / ta mod V.
+                    // A warp's steps then share s mod 4 = w mod 4, so its word
+                    // offset is fixed for the whole tile.
+                    const unsigned p0 = (unsigned)(((uintptr_t)(dst + ad.dst_b(0)) / sizeof(W)) & (V - 1));
+                    const unsigned ta = (unsigned)ad.ta;
+                    unsigned tinv = ta;                        // ta^-1 mod 8 (ta odd) ...
+                    tinv *= 2u - ta * tinv;                    // ... mod 64 (Newton)
+                    const unsigned fbe = (unsigned)(4 * (w & 3) / (int)sizeof(W)) + (unsigned)(l / LPR);  // fb / e
+                    const int rho = (int)(((0u - fbe - p0) * tinv) & (unsigned)(V - 1));
+                    auto run = [&](auto QC) {
+#pragma unroll 1
+                        for (int it = 0; it < STEPS; ++it) step(V * (2 * it + (w >> 2)) + rho, QC);
+                    };
+                    switch (w & 3) {
+                        case 0: run(std::integral_constant<int, 0>{}); break;
+                        case 1: run(std::integral_constant<int, 1>{}); break;
+                        case 2: run(std::integral_constant<int, 2>{}); break;
+                        default: run(std::integral_constant<int, 3>{}); break;
+                    }
+                }
+            }
+            if (!ordered) {
+#pragma unroll 1
+                for (int it = 0; it < STEPS; ++it) step((it * 8 + w) * CPI + l / LPR, std::integral_constant<int, -1>{});
             }
             return;
         } else if constexpr (!SHIFT) {
