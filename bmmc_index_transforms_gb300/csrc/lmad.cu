@@ -576,18 +576,40 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     // outside the segment, which are fetched and never used; an aligned
     // 16-byte chunk that holds a byte of the array lies in the same page as
     // that byte, so the fetch stays in mapped memory.
-#pragma unroll
-    for (int r = 0; r < TB * NCH / 256; ++r) {
-        const int idx = t + 256 * r;
-        const int row = idx >> LNCH, kk = idx & (NCH - 1);
-        if (row >= rb) break;  // rows grow with r
-        const O s0 = ad.src_b(row);
+    if constexpr (STAGE && std::is_same<Addr, LinAddr<O>>::value) {
+        // a thread's rows are 256 / NCH apart, a multiple of V, so they
+        // share one misalignment and its chunk offsets advance by constants
+        constexpr int RS = 256 / NCH;
+        const int row0 = t >> LNCH, kk = t & (NCH - 1);
+        const O s0 = ad.src_b(row0);
         const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
         const int k = kk + (m != 0);
         if (!SHORT || V * k - m < hi) {  // (chunks wholly past a short group A are not fetched)
-            uint4* q = reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1))));
-            const uint4* a = reinterpret_cast<const uint4*>(src + s0 + (V * k - m));
-            if (BMMC_SH_OK(q, 16) && BMMC_IN_WORD_OK(a, 16)) cp_async_word(q, a);
+            const W* a0 = src + s0 + (V * k - m);
+            W* const q0 = tile + row0 * kPitch + V * k;
+            const O astep = (O)RS * ad.sb;
+#pragma unroll
+            for (int r = 0; r < TB * NCH / 256; ++r) {
+                if (row0 + RS * r >= rb) break;  // rows grow with r
+                uint4* q = reinterpret_cast<uint4*>(q0 + RS * r * kPitch);
+                const uint4* a = reinterpret_cast<const uint4*>(a0 + (O)r * astep);
+                if (BMMC_SH_OK(q, 16) && BMMC_IN_WORD_OK(a, 16)) cp_async_word(q, a);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < TB * NCH / 256; ++r) {
+            const int idx = t + 256 * r;
+            const int row = idx >> LNCH, kk = idx & (NCH - 1);
+            if (row >= rb) break;  // rows grow with r
+            const O s0 = ad.src_b(row);
+            const int m = uni ? (int)base_mis : (int)((base_mis + (unsigned)s0) & (V - 1));
+            const int k = kk + (m != 0);
+            if (!SHORT || V * k - m < hi) {  // (chunks wholly past a short group A are not fetched)
+                uint4* q = reinterpret_cast<uint4*>(tile + row * kPitch + V * (k + ROT * ((row >> 3) & (PH - 1))));
+                const uint4* a = reinterpret_cast<const uint4*>(src + s0 + (V * k - m));
+                if (BMMC_SH_OK(q, 16) && BMMC_IN_WORD_OK(a, 16)) cp_async_word(q, a);
+            }
         }
     }
     if (!uni || base_mis != 0) {
@@ -738,6 +760,19 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
             }
             const unsigned char* const sb = reinterpret_cast<const unsigned char*>(tile);
             const bool fast = uni && ((base_mis * (unsigned)sizeof(W)) & 3u) == 0;
+            // a single-dimension B: a lane's items are 8 * 8 / CB rows apart,
+            // a multiple of V, so row r0 + k has the same misalignment in all
+            // of them: its word offset (bits 0-7) and shift (bits 8-15), once
+            constexpr bool LIN = std::is_same<Addr, LinAddr<O>>::value;
+            uint32_t rowmis[LIN ? 8 : 1];
+            if constexpr (LIN) {
+                const int r0 = 8 * (w / CB);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
+                    rowmis[k] = (uint32_t)(mb & ~3) | (uint32_t)(8 * (mb & 3)) << 8;
+                }
+            }
             Cols held[SITEMS];
 #pragma unroll
             for (int i = 0; i < SITEMS; ++i) {
@@ -761,13 +796,21 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                     const unsigned char* const rowp = sb + r0 * kPitch * (int)sizeof(W) + 4 * wi;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
+                        uint32_t off, shk;
+                        if constexpr (LIN) {
+                            off = rowmis[k] & 0xFFu;
+                            shk = rowmis[k] >> 8;
+                        } else {
+                            const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
+                            off = (uint32_t)(mb & ~3);
+                            shk = (uint32_t)(8 * (mb & 3));
+                        }
                         const uint32_t* p =
-                            reinterpret_cast<const uint32_t*>(rowp + k * kPitch * (int)sizeof(W) + (mb & ~3));
+                            reinterpret_cast<const uint32_t*>(rowp + k * kPitch * (int)sizeof(W) + (int)off);
                         const uint32_t a = BMMC_SH_OK(p, 4) ? p[0] : 0u;
-                        if (sizeof(W) == 1 || (mb & 3) != 0) {
+                        if (sizeof(W) == 1 || shk != 0) {
                             const uint32_t b = BMMC_SH_OK(p + 1, 4) ? p[1] : 0u;
-                            v[k] = __funnelshift_r(a, b, 8 * (mb & 3));
+                            v[k] = __funnelshift_r(a, b, shk);
                         } else {
                             v[k] = a;
                         }
