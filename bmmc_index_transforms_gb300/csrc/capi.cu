@@ -520,16 +520,21 @@ bmmc_status bmmc_bounds_report(bmmc_bounds_report_t* report, int reset) {
 #ifdef BMMC_BOUNDS_CHECK
     r.enabled = 1;
 #endif
-    unsigned long long a[6] = {}, b[6] = {};
+    unsigned long long rec[4][6] = {};
     if (r.enabled) {
-        if (cudaDeviceSynchronize() != cudaSuccess || bounds_record_kernels(a, reset != 0) != cudaSuccess ||
-            bounds_record_lmad(b, reset != 0) != cudaSuccess) {
+        if (cudaDeviceSynchronize() != cudaSuccess || bounds_record_kernels(rec[0], reset != 0) != cudaSuccess ||
+            bounds_record_lmad(rec[1], reset != 0) != cudaSuccess ||
+            bounds_record_lmad_transpose_1_2(rec[2], reset != 0) != cudaSuccess ||
+            bounds_record_lmad_transpose_4_8_16(rec[3], reset != 0) != cudaSuccess) {
             cudaGetLastError();
             return BMMC_ERR_CUDA;
         }
     }
-    r.failures = a[0] + b[0];
-    const unsigned long long* first = a[0] ? a : b;  // one file's first failure
+    const unsigned long long* first = nullptr;  // one file's first failure
+    for (auto& f : rec) {
+        r.failures += f[0];
+        if (f[0] && !first) first = f;
+    }
     if (r.failures) {
         r.site = (int)first[1];
         r.address = first[2];

@@ -21,10 +21,13 @@ cudaError_t launch_tiled(const PassPlan& P, const void* in, void* out, cudaStrea
 cudaError_t launch_copy(const void* in, void* out, size_t bytes, cudaStream_t stream);
 
 // Copy out (and with clear, reset) the bounds record of the kernels of
-// kernels.cu / lmad.cu: kRecordWords values (see bounds.cuh); all zero in
+// kernels.cu / lmad.cu / lmad_transpose_1_2.cu / lmad_transpose_4_8_16.cu:
+// kRecordWords values (see bounds.cuh); all zero in
 // builds without BMMC_BOUNDS_CHECK.
 cudaError_t bounds_record_kernels(unsigned long long out[6], bool clear);
 cudaError_t bounds_record_lmad(unsigned long long out[6], bool clear);
+cudaError_t bounds_record_lmad_transpose_1_2(unsigned long long out[6], bool clear);
+cudaError_t bounds_record_lmad_transpose_4_8_16(unsigned long long out[6], bool clear);
 #ifdef BMMC_BOUNDS_CHECK
 // The checks' self-test on a caller's device buffer of 512 bytes.
 cudaError_t bounds_selftest(void* buf, cudaStream_t stream);

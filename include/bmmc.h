@@ -504,7 +504,8 @@ typedef struct {
     int enabled;        /* 1 in a bounds-checked build, else 0 (and the rest zero) */
     uint64_t failures;  /* accesses that failed their test since the last reset */
     int site;           /* first failure: source file tag * 100000 + line
-                           (tag 1: kernels.cu, 2: lmad.cu) */
+                           (tag 1: kernels.cu, 2: lmad.cu, 3: lmad_transpose_1_2.cu,
+                           4: lmad_transpose_4_8_16.cu) */
     int bytes;          /* its access size */
     uint64_t address;   /* its address (a shared-memory offset for shared accesses) */
     uint64_t lo, hi;    /* the range [lo, hi) it was tested against */
