@@ -335,6 +335,81 @@ def test_transposes_into_unaligned_destination_columns(elem, case):
     _check(w, elem, seed=11)
 
 
+def _two_dim_group_a_view(Rb, a1, a0, in_off=0, out_off=0, pad=5, bpad=3):
+    """Group A of two source dimensions (a1 x a0, contiguous in the source)
+    whose destination strides do not collapse, B = Rb rows of destination
+    stride 1 (columns of pitch Rb + bpad, odd): the tile kernel's offset
+    tables."""
+    out_strides = [1, a0 * (Rb + bpad) + pad, Rb + bpad]
+    return dict(sizes=[Rb, a1, a0], in_offset=in_off, in_strides=[a1 * a0, a0, 1], in_elems=in_off + Rb * a1 * a0,
+                out_offset=out_off, out_strides=out_strides,
+                out_elems=out_off + (a1 - 1) * out_strides[1] + (a0 - 1) * out_strides[2] + Rb)
+
+
+@pytest.mark.parametrize("elem,view,flags", [
+    # bytes: 256 x 128 tiles, one source misalignment / one per row, a group A
+    # shorter than a tile, offset tables with and without a short group A
+    (1, dict(R=300, C=1000, out_pitch=301), {"tall"}),
+    (1, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=2, out_pitch=301), {"tall"}),
+    (1, dict(R=129, C=777, in_off=5, in_pitch=781, out_pitch=143), {"tall"}),
+    (1, dict(R=300, C=200, out_pitch=303), {"tall", "short_a"}),
+    (1, ("tables", 300, 4, 64), {"tables", "tall"}),
+    (1, ("tables", 300, 3, 64), {"tables", "tall", "short_a"}),
+    # 2-byte words: 128 x 128 tiles, or 64 x 128 where group A is 64 or shorter
+    (2, dict(R=300, C=1000, out_pitch=301), {"tall"}),
+    (2, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=3, out_pitch=301), {"tall"}),
+    (2, dict(R=128, C=130, out_pitch=135), {"tall"}),
+    (2, dict(R=300, C=100, out_pitch=301), {"tall", "short_a"}),
+    (2, dict(R=300, C=64, out_pitch=301), {"half_rows"}),
+    (2, dict(R=300, C=48, in_off=3, in_pitch=53, out_pitch=301), {"half_rows", "short_a"}),
+    (2, ("tables", 300, 4, 32), {"tables", "tall"}),
+    (2, ("tables", 300, 3, 32), {"tables", "tall", "short_a"}),
+    (2, ("tables", 300, 2, 32), {"tables", "half_rows"}),
+    (2, ("tables", 300, 3, 16), {"tables", "half_rows", "short_a"}),
+])
+def test_staged_variants_match_oracle(elem, view, flags):
+    """Every kernel variant of the destination-major restaging (tiles of 128
+    rows stepped by 128 - 16 / elem, each destination column written as
+    whole aligned 16-byte words): the query names the variant, and the output
+    matches the oracle's copy loop byte for byte, positions outside the copy
+    untouched."""
+    w = _two_dim_group_a_view(*view[1:]) if isinstance(view, tuple) else _byte_transpose_view(**view)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and not q["narrow"]
+    assert set(q["tile_mode"]) == {"chunked", "packs", "staged"} | flags, q["tile_mode"]
+    _check(w, elem)
+    _check(w, elem, seed=5)
+
+
+@pytest.mark.parametrize("elem,R,C,pitch", [(1, 70, 256, (1 << 23) + 5), (2, 130, 128, (1 << 24) + 3),
+                                            (2, 130, 64, (1 << 25) + 1)])
+def test_staged_variants_with_64bit_offsets(elem, R, C, pitch):
+    """The restaged variants with 64-bit offsets: columns of a transpose
+    spread over a destination of more than 2^31 elements (2-4 GiB).  Each
+    column and the 16 elements on either side are read back and compared."""
+    if torch.cuda.get_device_properties(0).total_memory < (24 << 30):
+        pytest.skip("needs a large device")
+    w = dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C, out_offset=0, out_strides=[1, pitch],
+             out_elems=(C - 1) * pitch + R + 16)
+    q = bm.lmad_copy_query(w["sizes"], 0, w["in_strides"], 0, w["out_strides"], elem, in_elems=w["in_elems"],
+                           out_elems=w["out_elems"])
+    assert q["kind"] == "transpose" and {"wide", "staged"} <= set(q["tile_mode"]), q["tile_mode"]
+    src = _fill(w["in_elems"], elem, 9)
+    d_src = torch.from_numpy(src.reshape(-1)).cuda()
+    d_dst = torch.full((w["out_elems"] * elem,), 0xA5, dtype=torch.uint8, device="cuda")
+    bm.lmad_copy(w["sizes"], 0, w["in_strides"], 0, w["out_strides"], elem, d_src, d_dst)
+    torch.cuda.synchronize()
+    for c in range(C):
+        lo = max(0, c * pitch - 16)
+        got = d_dst[lo * elem:(c * pitch + R + 16) * elem].cpu().numpy().reshape(-1, elem)
+        col = got[c * pitch - lo:c * pitch - lo + R]
+        assert np.array_equal(col, src.reshape(R, C, elem)[:, c]), f"column {c}"
+        assert (got[:c * pitch - lo] == 0xA5).all() and (got[c * pitch - lo + R:] == 0xA5).all(), f"around column {c}"
+    del d_dst
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("elem", [1, 2, 4])
 @pytest.mark.parametrize("C", [17, 33, 48, 63, 100, 127, 200])
 @pytest.mark.parametrize("in_off,out_extra", [(0, 0), (3, 0), (0, 5), (5, 3)])
