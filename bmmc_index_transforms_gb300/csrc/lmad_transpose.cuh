@@ -293,6 +293,258 @@ __device__ __forceinline__ void store_bytes16(unsigned char* p, uint4 v, int n) 
     }
 }
 
+// The store phase of a staged tile (the chunk path's fill has put the TB
+// source rows in shared memory, row r shifted by its misalignment: base_mis
+// plus B's source offset of r modulo V, the same for all rows when uni).
+template <typename W, typename O, bool SHORT, int NCH, int TALL, typename Addr>
+__device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, const Addr& ad, int rb, int lo, int hi,
+                                                  bool first_b, unsigned base_mis, bool uni) {
+    constexpr int V = 16 / (int)sizeof(W);
+    constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA;
+    constexpr int kPitch = chunk_pitch(NCH) * V;
+    constexpr int EPW = 4 / (int)sizeof(W);  // elements of a 4-byte word
+    static_assert(sizeof(W) <= 2 && TB == 128, "staged tiles: 1- and 2-byte words, 128 rows");
+    const int t = threadIdx.x, w = t >> 5, l = t & 31;
+    // rows 0..7 of EPW columns, two or four rows a 32-bit word
+    struct Cols {
+        uint32_t c[EPW][8 / EPW];
+    };
+    // Destination columns that do not start on a 16-byte boundary,
+    // restaged destination-major.  The launcher steps tiles by
+    // TB - V rows along B, so neighbouring tiles share V rows: each
+    // column of a tile writes the whole aligned 16-byte destination
+    // words that start in its first TB - V rows (they end inside the
+    // TB rows fetched), and the tile holding B index 0 also writes
+    // the partial word before a column's first aligned one; words are
+    // cut at the last fetched row (rb), which ends B.  Every item is
+    // gathered into registers (below), the tile is rewritten with
+    // column ia a contiguous run at ia * DP bytes of the same shared
+    // memory (8- or 16-byte stores at the run's row offset; with the
+    // slot rotation, DP = 136 for bytes and 272 for 2-byte words put
+    // each half (quarter) warp's stores in 32 distinct banks), and
+    // each column run is read back in aligned 16-byte granules,
+    // shifted to the destination's alignment in registers and
+    // written as 16-byte stores (below).
+    constexpr int DP = sizeof(W) == 1 ? TB + 8 : 2 * TB + 16;  // bytes between column runs
+    constexpr int NB = (TB - V) / V;                         // whole words a column owns
+    static_assert(TA * DP <= TALL * (TileShape<sizeof(W)>::T / (NCH * V)) * chunk_pitch(NCH) * 16,
+                  "the destination-major tile fits the shared tile");
+    // Gather: an item is 8 rows x 32 consecutive 4-byte words of one
+    // row segment (lane l takes word l, so each shared load reads
+    // 128 consecutive bytes of one row: no bank conflict whatever
+    // the row's misalignment), transposed by byte permutes into EPW
+    // columns of 8 rows.  Slot j of lane l holds its column
+    // (j + rot) mod EPW, rot = (l / 4) mod EPW, so that the
+    // destination-major stores below fall in distinct banks.
+    constexpr int WPR = TA * (int)sizeof(W) / 4;  // words per row segment
+    constexpr int CB = WPR / 32, SITEMS = (TB / 8) * CB / 8;
+    static_assert(CB * 32 == WPR && SITEMS * 8 == (TB / 8) * CB, "whole items");
+    const int rot = (l >> 2) & (EPW - 1);
+    uint32_t s_lo, s_hi;  // first-stage byte selectors (bytes) / the two halves (2-byte words)
+    if constexpr (sizeof(W) == 1) {
+        const uint32_t c0 = (uint32_t)rot, c1 = (uint32_t)((rot + 1) & 3), c2 = (uint32_t)((rot + 2) & 3),
+                       c3 = (uint32_t)((rot + 3) & 3);
+        s_lo = c0 | (4u + c0) << 4 | c1 << 8 | (4u + c1) << 12;
+        s_hi = c2 | (4u + c2) << 4 | c3 << 8 | (4u + c3) << 12;
+    } else {
+        s_lo = rot ? 0x7632u : 0x5410u;
+        s_hi = rot ? 0x5410u : 0x7632u;
+    }
+    const unsigned char* const sb = reinterpret_cast<const unsigned char*>(tile);
+    const bool fast = uni && ((base_mis * (unsigned)sizeof(W)) & 3u) == 0;
+    // a single-dimension B: a lane's items are 8 * 8 / CB rows apart,
+    // a multiple of V, so row r0 + k has the same misalignment in all
+    // of them: its word offset (bits 0-7) and shift (bits 8-15), once
+    constexpr bool LIN = std::is_same<Addr, LinAddr<O>>::value;
+    uint32_t rowmis[LIN ? 8 : 1];
+    if constexpr (LIN) {
+        const int r0 = 8 * (w / CB);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
+            rowmis[k] = (uint32_t)(mb & ~3) | (uint32_t)(8 * (mb & 3)) << 8;
+        }
+    }
+    Cols held[SITEMS];
+#pragma unroll
+    for (int i = 0; i < SITEMS; ++i) {
+        const int x = w + 8 * i;
+        const int r0 = 8 * (x / CB), wi = 32 * (x % CB) + l;
+        uint32_t v[8];
+        if (fast) {
+            // every row shares a 4-byte aligned misalignment
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(
+                sb + (r0 * kPitch + (int)base_mis) * (int)sizeof(W) + 4 * wi);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                v[k] = BMMC_SH_OK(p + k * (kPitch * (int)sizeof(W) / 4), 4) ? p[k * (kPitch * (int)sizeof(W) / 4)]
+                                                                            : 0u;
+        } else {
+            // rows with their own misalignments (mb bytes): two
+            // aligned loads and a funnel shift each where mb is not
+            // a multiple of 4 (three rows in four for bytes, which
+            // take the two loads unconditionally; one in two for
+            // 2-byte words, under a warp-uniform branch)
+            const unsigned char* const rowp = sb + r0 * kPitch * (int)sizeof(W) + 4 * wi;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint32_t off, shk;
+                if constexpr (LIN) {
+                    off = rowmis[k] & 0xFFu;
+                    shk = rowmis[k] >> 8;
+                } else {
+                    const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
+                    off = (uint32_t)(mb & ~3);
+                    shk = (uint32_t)(8 * (mb & 3));
+                }
+                const uint32_t* p =
+                    reinterpret_cast<const uint32_t*>(rowp + k * kPitch * (int)sizeof(W) + (int)off);
+                const uint32_t a = BMMC_SH_OK(p, 4) ? p[0] : 0u;
+                if (sizeof(W) == 1 || shk != 0) {
+                    const uint32_t b = BMMC_SH_OK(p + 1, 4) ? p[1] : 0u;
+                    v[k] = __funnelshift_r(a, b, shk);
+                } else {
+                    v[k] = a;
+                }
+            }
+        }
+        auto& col = held[i].c;
+        if constexpr (sizeof(W) == 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], s_lo);
+                const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], s_hi);
+                const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], s_lo);
+                const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], s_hi);
+                col[0][h] = __byte_perm(t0, t2, 0x5410);
+                col[1][h] = __byte_perm(t0, t2, 0x7632);
+                col[2][h] = __byte_perm(t1, t3, 0x5410);
+                col[3][h] = __byte_perm(t1, t3, 0x7632);
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                col[0][h] = __byte_perm(v[2 * h], v[2 * h + 1], s_lo);
+                col[1][h] = __byte_perm(v[2 * h], v[2 * h + 1], s_hi);
+            }
+        }
+    }
+    __syncthreads();  // the source-major tile is read
+    unsigned char* const dm = reinterpret_cast<unsigned char*>(tile);
+#pragma unroll
+    for (int i = 0; i < SITEMS; ++i) {
+        const int x = w + 8 * i;
+        const int r0 = 8 * (x / CB), c0 = (32 * (x % CB) + l) * EPW;
+#pragma unroll
+        for (int j = 0; j < EPW; ++j) {
+            unsigned char* q = dm + (c0 + ((j + rot) & (EPW - 1))) * DP + r0 * (int)sizeof(W);
+            if constexpr (sizeof(W) == 1) {
+                if (BMMC_SH_OK(q, 8)) *reinterpret_cast<uint2*>(q) = make_uint2(held[i].c[j][0], held[i].c[j][1]);
+            } else {
+                if (BMMC_SH_OK(q, 16))
+                    *reinterpret_cast<uint4*>(q) =
+                        make_uint4(held[i].c[j][0], held[i].c[j][1], held[i].c[j][2], held[i].c[j][3]);
+            }
+        }
+    }
+    __syncthreads();  // the destination-major tile is written
+    // Each column run is written by LPR lanes (8 for bytes, 16 for
+    // 2-byte words), lane k holding the run's 16-byte granule k (two
+    // 8-byte or one 16-byte shared load; a half or quarter warp reads
+    // whole 128-byte stretches, no bank conflict) and taking
+    // granule k + 1 from its neighbour by shuffles.  Its aligned
+    // destination word k (run bytes fb + 16 k ..) is bytes fb.. of
+    // that pair: the words are picked by two selects on fb / 4 and
+    // joined by funnel shifts on fb mod 4.
+    constexpr int LPR = sizeof(W) == 1 ? 8 : 16;  // lanes per column run (TB * sizeof(W) / 16)
+    constexpr int CPI = 32 / LPR;                 // columns per warp step
+    static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
+    const int k = l & (LPR - 1);
+    const int rbb = rb * (int)sizeof(W);  // fetched bytes of a column
+    constexpr int STEPS = TA / (8 * CPI);  // warp steps per tile
+    // One warp step for column ia.  QC: the word offset fb / 4 of
+    // every column of the step when the caller fixed it (0..3), or
+    // -1: each lane picks its words by two selects.
+    auto step = [&](const int ia, auto QC) {
+        constexpr int Q = decltype(QC)::value;
+        const bool mine = ia >= lo && (!SHORT || ia < hi);  // one of this tile's columns
+        unsigned char* const pc = reinterpret_cast<unsigned char*>(dst + ad.dst_a(ia) + ad.dst_b(0));
+        const int fb = (int)((16u - (unsigned)((uintptr_t)pc & 15u)) & 15u);  // bytes before its first aligned word
+        const unsigned char* const g = dm + ia * DP + 16 * k;
+        uint32_t wv[8];
+        if constexpr (sizeof(W) == 1) {
+            const uint2 a = BMMC_SH_OK(g, 8) ? *reinterpret_cast<const uint2*>(g) : make_uint2(0u, 0u);
+            const uint2 b = BMMC_SH_OK(g + 8, 8) ? *reinterpret_cast<const uint2*>(g + 8) : make_uint2(0u, 0u);
+            wv[0] = a.x, wv[1] = a.y, wv[2] = b.x, wv[3] = b.y;
+        } else {
+            const uint4 a = BMMC_SH_OK(g, 16) ? *reinterpret_cast<const uint4*>(g) : make_uint4(0u, 0u, 0u, 0u);
+            wv[0] = a.x, wv[1] = a.y, wv[2] = a.z, wv[3] = a.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wv[4 + i] = __shfl_down_sync(0xffffffffu, wv[i], 1, LPR);
+        uint32_t z[5];
+        if constexpr (Q >= 0) {
+#pragma unroll
+            for (int i = 0; i < 5; ++i) z[i] = Q + i < 8 ? wv[Q + i] : 0u;
+        } else {
+            const bool q2 = (fb & 8) != 0, q1 = (fb & 4) != 0;
+            uint32_t y[6];
+#pragma unroll
+            for (int i = 0; i < 6; ++i) y[i] = q2 ? wv[i + 2] : wv[i];
+#pragma unroll
+            for (int i = 0; i < 5; ++i) z[i] = q1 ? y[i + 1] : y[i];
+        }
+        const uint32_t sh = 8u * (uint32_t)(fb & 3);
+        const uint4 word = make_uint4(__funnelshift_r(z[0], z[1], sh), __funnelshift_r(z[1], z[2], sh),
+                                      __funnelshift_r(z[2], z[3], sh), __funnelshift_r(z[3], z[4], sh));
+        const int b = fb + 16 * k;
+        if (mine && k < NB) {
+            if (b + 16 <= rbb) {
+                if (BMMC_OUT_OK(pc + b, 16)) __stcs(reinterpret_cast<uint4*>(pc + b), word);
+            } else if (b < rbb) {
+                store_bytes16(pc + b, word, rbb - b);
+            }
+        }
+        if (mine && first_b && k == 0 && fb > 0)
+            store_bytes16(pc, make_uint4(wv[0], wv[1], wv[2], wv[3]), fb < rbb ? fb : rbb);
+    };
+    bool ordered = false;
+    if constexpr (std::is_same<Addr, LinAddr<O>>::value) {
+        ordered = (ad.ta & 1) != 0;
+        if (ordered) {
+            // A single-dimension group A with an odd destination stride
+            // ta: column ia starts p0 + ia * ta elements past an aligned
+            // word (mod V), which runs through every residue as ia runs
+            // through V consecutive columns.  Step s of the tile takes,
+            // from columns V * (s / 4) .. + V - 1, the CPI columns whose
+            // first aligned word is fb = 4 (s mod 4) .. 4 (s mod 4) + 3
+            // bytes away: ia = V * (s / 4) + (-(fb / e) - p0) / ta mod V.
+            // A warp's steps then share s mod 4 = w mod 4, so its word
+            // offset is fixed for the whole tile.
+            const unsigned p0 = (unsigned)(((uintptr_t)(dst + ad.dst_b(0)) / sizeof(W)) & (V - 1));
+            const unsigned ta = (unsigned)ad.ta;
+            unsigned tinv = ta;                        // ta^-1 mod 8 (ta odd) ...
+            tinv *= 2u - ta * tinv;                    // ... mod 64 (Newton)
+            const unsigned fbe = (unsigned)(4 * (w & 3) / (int)sizeof(W)) + (unsigned)(l / LPR);  // fb / e
+            const int rho = (int)(((0u - fbe - p0) * tinv) & (unsigned)(V - 1));
+            auto run = [&](auto QC) {
+#pragma unroll 1
+                for (int it = 0; it < STEPS; ++it) step(V * (2 * it + (w >> 2)) + rho, QC);
+            };
+            switch (w & 3) {
+                case 0: run(std::integral_constant<int, 0>{}); break;
+                case 1: run(std::integral_constant<int, 1>{}); break;
+                case 2: run(std::integral_constant<int, 2>{}); break;
+                default: run(std::integral_constant<int, 3>{}); break;
+            }
+        }
+    }
+    if (!ordered) {
+#pragma unroll 1
+        for (int it = 0; it < STEPS; ++it) step((it * 8 + w) * CPI + l / LPR, std::integral_constant<int, -1>{});
+    }
+}
+
 template <typename W, typename O, bool PACK, bool SHIFT, bool STAGE, bool SHORT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
                                                     const Addr& ad, int rb, int lo, int hi, bool first_b) {
@@ -375,7 +627,10 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if constexpr (REG) {
+    if constexpr (STAGE) {
+        tile_store_staged<W, O, SHORT, NCH, TALL>(dst, tile, ad, rb, lo, hi, first_b, base_mis, uni);
+        return;
+    } else if constexpr (REG) {
         // each item: B rows ib0..ib0+7 x the EPW columns of one 4-byte word
         // (ia0..ia0+EPW-1).  Eight 4-byte shared loads (two and a funnel
         // shift for rows whose elements are not 4-byte aligned there, or
@@ -389,8 +644,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
         // over the sets; a thread's items share their lane's rotation.
         constexpr int EPW = 4 / (int)sizeof(W), RG = PH, WL = 32 / RG;
         constexpr int STRIPES = TA / EPW / WL, SETS = TB / (8 * RG), ITEMS = STRIPES * SETS / 8;
-        static_assert(ITEMS >= 1 && STRIPES * SETS == 8 * ITEMS && (STAGE || 16 * ROT == 4 * WL),
-                      "whole blocks, distinct banks");
+        static_assert(ITEMS >= 1 && STRIPES * SETS == 8 * ITEMS && 16 * ROT == 4 * WL, "whole blocks, distinct banks");
         const int w = t >> 5, l = t & 31;
         const unsigned char* tb = reinterpret_cast<const unsigned char*>(tile);
         const int lead = V * ROT * (l & (RG - 1));  // ((8 RG set + 8 (l % RG)) / 8) mod PH = l % RG
@@ -464,243 +718,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                         BMMC_OUT_OK(o + ad.dst_a(ia0 + j) + k, sizeof(W)))
                         o[ad.dst_a(ia0 + j) + k] = (W)(col[j][k / EPW] >> (8 * (int)sizeof(W) * (k % EPW)));
         };
-        if constexpr (STAGE) {
-            // Destination columns that do not start on a 16-byte boundary,
-            // restaged destination-major.  The launcher steps tiles by
-            // TB - V rows along B, so neighbouring tiles share V rows: each
-            // column of a tile writes the whole aligned 16-byte destination
-            // words that start in its first TB - V rows (they end inside the
-            // TB rows fetched), and the tile holding B index 0 also writes
-            // the partial word before a column's first aligned one; words are
-            // cut at the last fetched row (rb), which ends B.  Every item is
-            // gathered into registers (below), the tile is rewritten with
-            // column ia a contiguous run at ia * DP bytes of the same shared
-            // memory (8- or 16-byte stores at the run's row offset; with the
-            // slot rotation, DP = 136 for bytes and 272 for 2-byte words put
-            // each half (quarter) warp's stores in 32 distinct banks), and
-            // each column run is read back in aligned 16-byte granules,
-            // shifted to the destination's alignment in registers and
-            // written as 16-byte stores (below).
-            constexpr int DP = sizeof(W) == 1 ? TB + 8 : 2 * TB + 16;  // bytes between column runs
-            constexpr int NB = (TB - V) / V;                         // whole words a column owns
-            static_assert(TA * DP <= TALL * (TileShape<sizeof(W)>::T / (NCH * V)) * chunk_pitch(NCH) * 16,
-                          "the destination-major tile fits the shared tile");
-            // Gather: an item is 8 rows x 32 consecutive 4-byte words of one
-            // row segment (lane l takes word l, so each shared load reads
-            // 128 consecutive bytes of one row: no bank conflict whatever
-            // the row's misalignment), transposed by byte permutes into EPW
-            // columns of 8 rows.  Slot j of lane l holds its column
-            // (j + rot) mod EPW, rot = (l / 4) mod EPW, so that the
-            // destination-major stores below fall in distinct banks.
-            constexpr int WPR = TA * (int)sizeof(W) / 4;  // words per row segment
-            constexpr int CB = WPR / 32, SITEMS = (TB / 8) * CB / 8;
-            static_assert(CB * 32 == WPR && SITEMS * 8 == (TB / 8) * CB, "whole items");
-            const int rot = (l >> 2) & (EPW - 1);
-            uint32_t s_lo, s_hi;  // first-stage byte selectors (bytes) / the two halves (2-byte words)
-            if constexpr (sizeof(W) == 1) {
-                const uint32_t c0 = (uint32_t)rot, c1 = (uint32_t)((rot + 1) & 3), c2 = (uint32_t)((rot + 2) & 3),
-                               c3 = (uint32_t)((rot + 3) & 3);
-                s_lo = c0 | (4u + c0) << 4 | c1 << 8 | (4u + c1) << 12;
-                s_hi = c2 | (4u + c2) << 4 | c3 << 8 | (4u + c3) << 12;
-            } else {
-                s_lo = rot ? 0x7632u : 0x5410u;
-                s_hi = rot ? 0x5410u : 0x7632u;
-            }
-            const unsigned char* const sb = reinterpret_cast<const unsigned char*>(tile);
-            const bool fast = uni && ((base_mis * (unsigned)sizeof(W)) & 3u) == 0;
-            // a single-dimension B: a lane's items are 8 * 8 / CB rows apart,
-            // a multiple of V, so row r0 + k has the same misalignment in all
-            // of them: its word offset (bits 0-7) and shift (bits 8-15), once
-            constexpr bool LIN = std::is_same<Addr, LinAddr<O>>::value;
-            uint32_t rowmis[LIN ? 8 : 1];
-            if constexpr (LIN) {
-                const int r0 = 8 * (w / CB);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
-                    rowmis[k] = (uint32_t)(mb & ~3) | (uint32_t)(8 * (mb & 3)) << 8;
-                }
-            }
-            Cols held[SITEMS];
-#pragma unroll
-            for (int i = 0; i < SITEMS; ++i) {
-                const int x = w + 8 * i;
-                const int r0 = 8 * (x / CB), wi = 32 * (x % CB) + l;
-                uint32_t v[8];
-                if (fast) {
-                    // every row shares a 4-byte aligned misalignment
-                    const uint32_t* p = reinterpret_cast<const uint32_t*>(
-                        sb + (r0 * kPitch + (int)base_mis) * (int)sizeof(W) + 4 * wi);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        v[k] = BMMC_SH_OK(p + k * (kPitch * (int)sizeof(W) / 4), 4) ? p[k * (kPitch * (int)sizeof(W) / 4)]
-                                                                                    : 0u;
-                } else {
-                    // rows with their own misalignments (mb bytes): two
-                    // aligned loads and a funnel shift each where mb is not
-                    // a multiple of 4 (three rows in four for bytes, which
-                    // take the two loads unconditionally; one in two for
-                    // 2-byte words, under a warp-uniform branch)
-                    const unsigned char* const rowp = sb + r0 * kPitch * (int)sizeof(W) + 4 * wi;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        uint32_t off, shk;
-                        if constexpr (LIN) {
-                            off = rowmis[k] & 0xFFu;
-                            shk = rowmis[k] >> 8;
-                        } else {
-                            const int mb = (int)(((base_mis + (unsigned)ad.src_b(r0 + k)) & (V - 1)) * sizeof(W));
-                            off = (uint32_t)(mb & ~3);
-                            shk = (uint32_t)(8 * (mb & 3));
-                        }
-                        const uint32_t* p =
-                            reinterpret_cast<const uint32_t*>(rowp + k * kPitch * (int)sizeof(W) + (int)off);
-                        const uint32_t a = BMMC_SH_OK(p, 4) ? p[0] : 0u;
-                        if (sizeof(W) == 1 || shk != 0) {
-                            const uint32_t b = BMMC_SH_OK(p + 1, 4) ? p[1] : 0u;
-                            v[k] = __funnelshift_r(a, b, shk);
-                        } else {
-                            v[k] = a;
-                        }
-                    }
-                }
-                auto& col = held[i].c;
-                if constexpr (sizeof(W) == 1) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t t0 = __byte_perm(v[4 * h], v[4 * h + 1], s_lo);
-                        const uint32_t t1 = __byte_perm(v[4 * h], v[4 * h + 1], s_hi);
-                        const uint32_t t2 = __byte_perm(v[4 * h + 2], v[4 * h + 3], s_lo);
-                        const uint32_t t3 = __byte_perm(v[4 * h + 2], v[4 * h + 3], s_hi);
-                        col[0][h] = __byte_perm(t0, t2, 0x5410);
-                        col[1][h] = __byte_perm(t0, t2, 0x7632);
-                        col[2][h] = __byte_perm(t1, t3, 0x5410);
-                        col[3][h] = __byte_perm(t1, t3, 0x7632);
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        col[0][h] = __byte_perm(v[2 * h], v[2 * h + 1], s_lo);
-                        col[1][h] = __byte_perm(v[2 * h], v[2 * h + 1], s_hi);
-                    }
-                }
-            }
-            __syncthreads();  // the source-major tile is read
-            unsigned char* const dm = reinterpret_cast<unsigned char*>(tile);
-#pragma unroll
-            for (int i = 0; i < SITEMS; ++i) {
-                const int x = w + 8 * i;
-                const int r0 = 8 * (x / CB), c0 = (32 * (x % CB) + l) * EPW;
-#pragma unroll
-                for (int j = 0; j < EPW; ++j) {
-                    unsigned char* q = dm + (c0 + ((j + rot) & (EPW - 1))) * DP + r0 * (int)sizeof(W);
-                    if constexpr (sizeof(W) == 1) {
-                        if (BMMC_SH_OK(q, 8)) *reinterpret_cast<uint2*>(q) = make_uint2(held[i].c[j][0], held[i].c[j][1]);
-                    } else {
-                        if (BMMC_SH_OK(q, 16))
-                            *reinterpret_cast<uint4*>(q) =
-                                make_uint4(held[i].c[j][0], held[i].c[j][1], held[i].c[j][2], held[i].c[j][3]);
-                    }
-                }
-            }
-            __syncthreads();  // the destination-major tile is written
-            // Each column run is written by LPR lanes (8 for bytes, 16 for
-            // 2-byte words), lane k holding the run's 16-byte granule k (two
-            // 8-byte or one 16-byte shared load; a half or quarter warp reads
-            // whole 128-byte stretches, no bank conflict) and taking
-            // granule k + 1 from its neighbour by shuffles.  Its aligned
-            // destination word k (run bytes fb + 16 k ..) is bytes fb.. of
-            // that pair: the words are picked by two selects on fb / 4 and
-            // joined by funnel shifts on fb mod 4.
-            constexpr int LPR = sizeof(W) == 1 ? 8 : 16;  // lanes per column run (TB * sizeof(W) / 16)
-            constexpr int CPI = 32 / LPR;                 // columns per warp step
-            static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
-            const int k = l & (LPR - 1);
-            const int rbb = rb * (int)sizeof(W);  // fetched bytes of a column
-            constexpr int STEPS = TA / (8 * CPI);  // warp steps per tile
-            // One warp step for column ia.  QC: the word offset fb / 4 of
-            // every column of the step when the caller fixed it (0..3), or
-            // -1: each lane picks its words by two selects.
-            auto step = [&](const int ia, auto QC) {
-                constexpr int Q = decltype(QC)::value;
-                const bool mine = ia >= lo && (!SHORT || ia < hi);  // one of this tile's columns
-                unsigned char* const pc = reinterpret_cast<unsigned char*>(dst + ad.dst_a(ia) + ad.dst_b(0));
-                const int fb = (int)((16u - (unsigned)((uintptr_t)pc & 15u)) & 15u);  // bytes before its first aligned word
-                const unsigned char* const g = dm + ia * DP + 16 * k;
-                uint32_t wv[8];
-                if constexpr (sizeof(W) == 1) {
-                    const uint2 a = BMMC_SH_OK(g, 8) ? *reinterpret_cast<const uint2*>(g) : make_uint2(0u, 0u);
-                    const uint2 b = BMMC_SH_OK(g + 8, 8) ? *reinterpret_cast<const uint2*>(g + 8) : make_uint2(0u, 0u);
-                    wv[0] = a.x, wv[1] = a.y, wv[2] = b.x, wv[3] = b.y;
-                } else {
-                    const uint4 a = BMMC_SH_OK(g, 16) ? *reinterpret_cast<const uint4*>(g) : make_uint4(0u, 0u, 0u, 0u);
-                    wv[0] = a.x, wv[1] = a.y, wv[2] = a.z, wv[3] = a.w;
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) wv[4 + i] = __shfl_down_sync(0xffffffffu, wv[i], 1, LPR);
-                uint32_t z[5];
-                if constexpr (Q >= 0) {
-#pragma unroll
-                    for (int i = 0; i < 5; ++i) z[i] = Q + i < 8 ? wv[Q + i] : 0u;
-                } else {
-                    const bool q2 = (fb & 8) != 0, q1 = (fb & 4) != 0;
-                    uint32_t y[6];
-#pragma unroll
-                    for (int i = 0; i < 6; ++i) y[i] = q2 ? wv[i + 2] : wv[i];
-#pragma unroll
-                    for (int i = 0; i < 5; ++i) z[i] = q1 ? y[i + 1] : y[i];
-                }
-                const uint32_t sh = 8u * (uint32_t)(fb & 3);
-                const uint4 word = make_uint4(__funnelshift_r(z[0], z[1], sh), __funnelshift_r(z[1], z[2], sh),
-                                              __funnelshift_r(z[2], z[3], sh), __funnelshift_r(z[3], z[4], sh));
-                const int b = fb + 16 * k;
-                if (mine && k < NB) {
-                    if (b + 16 <= rbb) {
-                        if (BMMC_OUT_OK(pc + b, 16)) __stcs(reinterpret_cast<uint4*>(pc + b), word);
-                    } else if (b < rbb) {
-                        store_bytes16(pc + b, word, rbb - b);
-                    }
-                }
-                if (mine && first_b && k == 0 && fb > 0)
-                    store_bytes16(pc, make_uint4(wv[0], wv[1], wv[2], wv[3]), fb < rbb ? fb : rbb);
-            };
-            bool ordered = false;
-            if constexpr (std::is_same<Addr, LinAddr<O>>::value) {
-                ordered = (ad.ta & 1) != 0;
-                if (ordered) {
-                    // A single-dimension group A with an odd destination stride
-                    // ta: column ia starts p0 + ia * ta elements past an aligned
-                    // word (mod V), which runs through every residue as ia runs
-                    // through V consecutive columns.  Step s of the tile takes,
-                    // from columns V * (s / 4) .. + V - 1, the CPI columns whose
-                    // first aligned word is fb = 4 (s mod 4) .. 4 (s mod 4) + 3
-                    // bytes away: ia = V * (s / 4) + (-(fb / e) - p0) / ta mod V.
-                    // A warp's steps then share s mod 4 = w mod 4, so its word
-                    // offset is fixed for the whole tile.
-                    const unsigned p0 = (unsigned)(((uintptr_t)(dst + ad.dst_b(0)) / sizeof(W)) & (V - 1));
-                    const unsigned ta = (unsigned)ad.ta;
-                    unsigned tinv = ta;                        // ta^-1 mod 8 (ta odd) ...
-                    tinv *= 2u - ta * tinv;                    // ... mod 64 (Newton)
-                    const unsigned fbe = (unsigned)(4 * (w & 3) / (int)sizeof(W)) + (unsigned)(l / LPR);  // fb / e
-                    const int rho = (int)(((0u - fbe - p0) * tinv) & (unsigned)(V - 1));
-                    auto run = [&](auto QC) {
-#pragma unroll 1
-                        for (int it = 0; it < STEPS; ++it) step(V * (2 * it + (w >> 2)) + rho, QC);
-                    };
-                    switch (w & 3) {
-                        case 0: run(std::integral_constant<int, 0>{}); break;
-                        case 1: run(std::integral_constant<int, 1>{}); break;
-                        case 2: run(std::integral_constant<int, 2>{}); break;
-                        default: run(std::integral_constant<int, 3>{}); break;
-                    }
-                }
-            }
-            if (!ordered) {
-#pragma unroll 1
-                for (int it = 0; it < STEPS; ++it) step((it * 8 + w) * CPI + l / LPR, std::integral_constant<int, -1>{});
-            }
-            return;
-        } else if constexpr (!SHIFT) {
+        if constexpr (!SHIFT) {
 #pragma unroll 1
             for (int i = 0; i < ITEMS; ++i) {
                 const int x = w + 8 * i;
