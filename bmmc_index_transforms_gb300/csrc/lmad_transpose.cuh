@@ -298,7 +298,7 @@ __device__ __forceinline__ void store_bytes16(unsigned char* p, uint4 v, int n) 
 // plus B's source offset of r modulo V, the same for all rows when uni).
 template <typename W, typename O, bool SHORT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, const Addr& ad, int rb, int lo, int hi,
-                                                  bool first_b, unsigned base_mis, bool uni) {
+                                                  bool first_b, bool last_b, unsigned base_mis, bool uni) {
     constexpr int V = 16 / (int)sizeof(W);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA;
     constexpr int kPitch = chunk_pitch(NCH) * V;
@@ -314,9 +314,10 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     // TB - V rows along B, so neighbouring tiles share V rows: each
     // column of a tile writes the whole aligned 16-byte destination
     // words that start in its first TB - V rows (they end inside the
-    // TB rows fetched), and the tile holding B index 0 also writes
-    // the partial word before a column's first aligned one; words are
-    // cut at the last fetched row (rb), which ends B.  Every item is
+    // TB rows fetched); the last tile along B, whose rows reach the end
+    // of B, writes every word that starts in its rows, cut where B ends;
+    // and the tile holding B index 0 also writes the partial word
+    // before a column's first aligned one.  Every item is
     // gathered into registers (below), the tile is rewritten with
     // column ia a contiguous run at ia * DP bytes of the same shared
     // memory (8- or 16-byte stores at the run's row offset; with the
@@ -326,7 +327,6 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     // shifted to the destination's alignment in registers and
     // written as 16-byte stores (below).
     constexpr int DP = sizeof(W) == 1 ? TB + 8 : 2 * TB + 16;  // bytes between column runs
-    constexpr int NB = (TB - V) / V;                         // whole words a column owns
     static_assert(TA * DP <= TALL * (TileShape<sizeof(W)>::T / (NCH * V)) * chunk_pitch(NCH) * 16,
                   "the destination-major tile fits the shared tile");
     // Gather: an item is 8 rows x 32 consecutive 4-byte words of one
@@ -435,6 +435,7 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     for (int i = 0; i < SITEMS; ++i) {
         const int x = w + 8 * i;
         const int r0 = 8 * (x / CB), c0 = (32 * (x % CB) + l) * EPW;
+        if (r0 >= rb) continue;  // rows not fetched
 #pragma unroll
         for (int j = 0; j < EPW; ++j) {
             unsigned char* q = dm + (c0 + ((j + rot) & (EPW - 1))) * DP + r0 * (int)sizeof(W);
@@ -461,6 +462,8 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
     const int k = l & (LPR - 1);
     const int rbb = rb * (int)sizeof(W);  // fetched bytes of a column
+    // the words whose first byte is below `own` are this tile's
+    const int own = last_b ? rbb : (TB - V) * (int)sizeof(W);
     constexpr int STEPS = TA / (8 * CPI);  // warp steps per tile
     // One warp step for column ia.  QC: the word offset fb / 4 of
     // every column of the step when the caller fixed it (0..3), or
@@ -498,7 +501,7 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
         const uint4 word = make_uint4(__funnelshift_r(z[0], z[1], sh), __funnelshift_r(z[1], z[2], sh),
                                       __funnelshift_r(z[2], z[3], sh), __funnelshift_r(z[3], z[4], sh));
         const int b = fb + 16 * k;
-        if (mine && k < NB) {
+        if (mine && b < own) {
             if (b + 16 <= rbb) {
                 if (BMMC_OUT_OK(pc + b, 16)) __stcs(reinterpret_cast<uint4*>(pc + b), word);
             } else if (b < rbb) {
@@ -547,7 +550,8 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
 
 template <typename W, typename O, bool PACK, bool SHIFT, bool STAGE, bool SHORT, int NCH, int TALL, typename Addr>
 __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W* __restrict__ dst, W* tile,
-                                                    const Addr& ad, int rb, int lo, int hi, bool first_b) {
+                                                    const Addr& ad, int rb, int lo, int hi, bool first_b,
+                                                    bool last_b) {
     constexpr int V = 16 / (int)sizeof(W), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
     constexpr int kPitch = chunk_pitch(NCH) * V;
@@ -628,7 +632,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if constexpr (STAGE) {
-        tile_store_staged<W, O, SHORT, NCH, TALL>(dst, tile, ad, rb, lo, hi, first_b, base_mis, uni);
+        tile_store_staged<W, O, SHORT, NCH, TALL>(dst, tile, ad, rb, lo, hi, first_b, last_b, base_mis, uni);
         return;
     } else if constexpr (REG) {
         // each item: B rows ib0..ib0+7 x the EPW columns of one 4-byte word
@@ -1373,7 +1377,8 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             if (CHUNKED && (ra == TA || SHORT)) {
                 if constexpr (CHUNKED)
                     tile_phases_chunked<W, O, PACK, SHIFT, STAGE, SHORT, NCH, TALL>(in + so + tab_src[0], out + d,
-                                                                                     tile, ad, rb, lo, ra, b0 == 0);
+                                                                                     tile, ad, rb, lo, ra, b0 == 0,
+                                                                                     tb + 1 == (I)p.div_tb.d);
             } else if constexpr (TALL > 1) {
                 // a ragged-A tall tile: the element path, 1 / TALL of the rows at a time
                 constexpr int QB = S::T / (NCH * (16 / (int)sizeof(W)));  // rows of a part (A side of the chunk path)
@@ -1395,7 +1400,7 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
             if (CHUNKED && (ra == TA || SHORT)) {
                 if constexpr (CHUNKED)
                     tile_phases_chunked<W, O, PACK, SHIFT, STAGE, SHORT, NCH, TALL>(src, dst, tile, ad, rb, lo, ra,
-                                                                                     b0 == 0);
+                                                                                     b0 == 0, tb + 1 == (I)p.div_tb.d);
             } else if constexpr (TALL > 1) {
                 constexpr int QB = S::T / (NCH * (16 / (int)sizeof(W)));
                 for (int j = 0; j * QB < rb; ++j) {

@@ -43,15 +43,24 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     // path 64 x 128 realigned tiles (128-byte source rows, so a thread's two
     // items are the two row sets of one column stripe and the carry joins
     // them: partial words once per 128 rows instead of per 64)
+    // Measured crossover (GB300): the restaging below wins from 112 rows of
+    // bytes and from 129 rows of 2-byte words; B of one tile or less with
+    // whole 32- or 64-row sets (64 or 128 byte rows, 128 2-byte rows)
+    // stays faster realigned.
+    const bool stage_ok = LMAD_TILE_STAGE && n_b >= (word == 1 ? 112u : 129u);
     const bool long2 = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
-    const bool tall2 = LMAD_TILE_STAGE && long2, halve = !LMAD_TILE_STAGE && long2;
+    const bool tall2 = stage_ok && long2, halve = !stage_ok && long2;
     const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (tall2 || halve ? 1 : 0);
     // 128-row tiles of these (tall byte tiles, 128 x 128 or, for a group A
     // shorter than 128, 64 x 128 tiles of 2-byte words) restage the tile
     // destination-major instead, stepping by 128 - 16 / word rows along B
-    const bool staged = LMAD_TILE_STAGE && shift && lb == 7 && (tall || tall2 || (word == 2 && la == 6));
+    const bool staged = stage_ok && shift && lb == 7 && (tall || tall2 || (word == 2 && la == 6));
+    // (the last tile along B takes every row it reaches: one tile when B
+    // has at most 128 rows)
     const uint64_t step_b = staged ? (1ull << lb) - 16 / word : (1ull << lb);
-    const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la, tiles_b = (n_b + step_b - 1) / step_b;
+    const uint64_t tiles_a = (n_a + (1ull << la) - 1) >> la;
+    const uint64_t tiles_b = !staged ? (n_b + step_b - 1) / step_b
+                             : n_b <= (1ull << lb) ? 1 : 1 + (n_b - (1ull << lb) + step_b - 1) / step_b;
     const uint64_t tiles = tiles_a * tiles_b * batch;
     // masked lanes of a ragged tile form (unused) offsets up to one tile side
     // past the span; 32-bit offsets must hold those too

@@ -425,7 +425,8 @@ typedef struct {
                                       destination-major in shared memory and each column
                                       written as whole aligned 16-byte words; tiles step by
                                       launch_tile_b - 16 / elem_size B-indices, so neighbours
-                                      share the rows of one destination word */
+                                      share the rows of one destination word (the last tile
+                                      takes every B-index it reaches) */
 
 /* Analyse the copy lmad_copy would run with the same arguments, without
  * touching memory or the device.  in / out are used for their alignment and

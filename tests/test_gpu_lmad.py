@@ -358,7 +358,7 @@ def _two_dim_group_a_view(Rb, a1, a0, in_off=0, out_off=0, pad=5, bpad=3):
     # 2-byte words: 128 x 128 tiles, or 64 x 128 where group A is 64 or shorter
     (2, dict(R=300, C=1000, out_pitch=301), {"tall"}),
     (2, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=3, out_pitch=301), {"tall"}),
-    (2, dict(R=128, C=130, out_pitch=135), {"tall"}),
+    (2, dict(R=129, C=130, out_pitch=135), {"tall"}),
     (2, dict(R=300, C=100, out_pitch=301), {"tall", "short_a"}),
     (2, dict(R=300, C=64, out_pitch=301), {"half_rows"}),
     (2, dict(R=300, C=48, in_off=3, in_pitch=53, out_pitch=301), {"half_rows", "short_a"}),
@@ -382,7 +382,7 @@ def test_staged_variants_match_oracle(elem, view, flags):
     _check(w, elem, seed=5)
 
 
-@pytest.mark.parametrize("elem,R,C,pitch", [(1, 70, 256, (1 << 23) + 5), (2, 130, 128, (1 << 24) + 3),
+@pytest.mark.parametrize("elem,R,C,pitch", [(1, 120, 256, (1 << 23) + 5), (2, 130, 128, (1 << 24) + 3),
                                             (2, 130, 64, (1 << 25) + 1)])
 def test_staged_variants_with_64bit_offsets(elem, R, C, pitch):
     """The restaged variants with 64-bit offsets: columns of a transpose
