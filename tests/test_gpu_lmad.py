@@ -353,6 +353,11 @@ def _two_dim_group_a_view(Rb, a1, a0, in_off=0, out_off=0, pad=5, bpad=3):
     (1, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=2, out_pitch=301), {"tall"}),
     (1, dict(R=129, C=777, in_off=5, in_pitch=781, out_pitch=143), {"tall"}),
     (1, dict(R=300, C=200, out_pitch=303), {"tall", "short_a"}),
+    # even destination strides (per-lane word selection) and one
+    # misalignment shared by every column (stride a multiple of 16)
+    (1, dict(R=300, C=1000, out_pitch=302), {"tall"}),
+    (1, dict(R=300, C=1000, in_off=3, out_pitch=306), {"tall"}),
+    (1, dict(R=300, C=1000, out_off=5, out_pitch=304), {"tall"}),
     (1, ("tables", 300, 4, 64), {"tables", "tall"}),
     (1, ("tables", 300, 3, 64), {"tables", "tall", "short_a"}),
     # 2-byte words: 128 x 128 tiles, or 64 x 128 where group A is 64 or shorter
@@ -360,6 +365,8 @@ def _two_dim_group_a_view(Rb, a1, a0, in_off=0, out_off=0, pad=5, bpad=3):
     (2, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=3, out_pitch=301), {"tall"}),
     (2, dict(R=129, C=130, out_pitch=135), {"tall"}),
     (2, dict(R=300, C=100, out_pitch=301), {"tall", "short_a"}),
+    (2, dict(R=300, C=1000, out_pitch=302), {"tall"}),
+    (2, dict(R=300, C=1000, out_off=3, out_pitch=304), {"tall"}),
     (2, dict(R=300, C=64, out_pitch=301), {"half_rows"}),
     (2, dict(R=300, C=48, in_off=3, in_pitch=53, out_pitch=301), {"half_rows", "short_a"}),
     (2, ("tables", 300, 4, 32), {"tables", "tall"}),
