@@ -389,6 +389,29 @@ def test_staged_variants_match_oracle(elem, view, flags):
     _check(w, elem, seed=5)
 
 
+@pytest.mark.parametrize("elem", [1, 2])
+def test_staged_with_reversed_columns_and_batches(elem):
+    """Restaged transposes whose group A walks the destination backwards (the
+    columns of the transpose in reverse order: a negative odd stride, which
+    the per-warp column order handles modulo 16), and a batch of three
+    transposes with padded batch strides."""
+    R, C, pitch = 300, 1000, 301
+    w = dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C, out_offset=(C - 1) * pitch,
+             out_strides=[1, -pitch], out_elems=(C - 1) * pitch + R)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert "staged" in q["tile_mode"]
+    _check(w, elem)
+    nb = 3
+    w = dict(sizes=[nb, R, C], in_offset=0, in_strides=[R * C + 7, C, 1], in_elems=nb * (R * C + 7), out_offset=5,
+             out_strides=[C * pitch + 3, 1, pitch], out_elems=5 + (nb - 1) * (C * pitch + 3) + (C - 1) * pitch + R)
+    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+                           in_elems=w["in_elems"], out_elems=w["out_elems"])
+    assert "staged" in q["tile_mode"]
+    _check(w, elem)
+    _check(w, elem, seed=4)
+
+
 @pytest.mark.parametrize("elem,R,C,pitch", [(1, 120, 256, (1 << 23) + 5), (2, 130, 128, (1 << 24) + 3),
                                             (2, 130, 64, (1 << 25) + 1)])
 def test_staged_variants_with_64bit_offsets(elem, R, C, pitch):
