@@ -60,7 +60,8 @@ struct TileSides {
 #ifndef LMAD_TILE_SHIFT
 #define LMAD_TILE_SHIFT 1
 #endif
-// On 128-row tiles (tall byte tiles, 64 x 128 2-byte tiles) such
+// On 128-row tiles (tall byte tiles, 128 x 128 or 64 x 128 2-byte tiles)
+// with a B of at least 112 (bytes) or 129 (2-byte words) rows, such
 // destinations are restaged destination-major and written as whole aligned
 // 16-byte words instead.
 #ifndef LMAD_TILE_STAGE
@@ -1213,8 +1214,9 @@ __global__ void __launch_bounds__(256)
 // takes the chunk path, fetching and storing only its columns), bit 8 = the
 // 1- and 2-byte pack path for such destination columns restaged destination-
 // major in shared memory (128-row tiles stepped by 128 - 16 / sizeof(W) rows
-// along B, each column written as whole aligned 16-byte words; set with bit 2
-// instead of bit 6).  Bit 5 is the launcher's 64-bit offset flag.
+// along B, the last tile taking every row it reaches, each column written as
+// whole aligned 16-byte words; set with bit 2 instead of bit 6).  Bit 5 is
+// the launcher's 64-bit offset flag.
 enum {
     kTileLinear = 0,
     kTileTables = 1,

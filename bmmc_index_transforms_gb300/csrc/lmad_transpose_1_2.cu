@@ -39,14 +39,14 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     // measured no slower than 256 x 32 tiles from 64 rows up)
     const bool tall = LMAD_BYTE_TALL && word == 1 && (pack || shift) && row_bytes == 256 && C.lb == 5 && n_b >= 64;
     // 2-byte words with a B of at least 128 rows into such destinations take
-    // 128 x 128 tiles restaged destination-major (below), or without that
-    // path 64 x 128 realigned tiles (128-byte source rows, so a thread's two
-    // items are the two row sets of one column stripe and the carry joins
-    // them: partial words once per 128 rows instead of per 64)
-    // Measured crossover (GB300): the restaging below wins from 112 rows of
-    // bytes and from 129 rows of 2-byte words; B of one tile or less with
-    // whole 32- or 64-row sets (64 or 128 byte rows, 128 2-byte rows)
-    // stays faster realigned.
+    // 128 x 128 tiles restaged destination-major (below), or where that path
+    // does not pay 64 x 128 realigned tiles (128-byte source rows, so a
+    // thread's two items are the two row sets of one column stripe and the
+    // carry joins them: partial words once per 128 rows instead of per 64).
+    // Measured crossover (GB300): the restaging wins from 112 rows of bytes
+    // and from 129 rows of 2-byte words; B of one tile or less with whole
+    // 32- or 64-row sets (64 or 128 byte rows, 128 2-byte rows) stays
+    // faster realigned.
     const bool stage_ok = LMAD_TILE_STAGE && n_b >= (word == 1 ? 112u : 129u);
     const bool long2 = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
     const bool tall2 = stage_ok && long2, halve = !stage_ok && long2;
