@@ -62,6 +62,16 @@ def test_random_views_larger(seed):
     _check(w, (4, 8, 16, 1, 2)[seed % 5], seed)
 
 
+def test_many_random_views_of_small_elements():
+    """A thousand more fuzzed views, each copied as 1- and 2-byte elements
+    (the element sizes with the most kernel variants: rows, realigned and
+    restaged transposes), byte for byte against the oracle."""
+    for seed in range(20000, 21000):
+        w = synth.draw_lmad_view(seed, max_dims=5, max_elems=1 << 20)
+        for elem in (1, 2):
+            _check(w, elem, seed)
+
+
 @pytest.mark.parametrize("kind,shape", [("slice_2d", (97, 130)), ("slice_2d", (1031, 5)), ("slice_2d", (3, 4099)),
                                         ("slice_3d", (7, 33, 65)), ("slice_3d", (640, 32, 33)),
                                         ("reversed_rows", (64, 128)), ("reversed_rows", (100, 37)),
