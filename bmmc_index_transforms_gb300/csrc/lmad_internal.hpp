@@ -15,7 +15,6 @@
 namespace bmmc {
 namespace lmad {
 
-
 constexpr int kLmadMaxDims = LMAD_MAX_DIMS;
 constexpr uint64_t kLmadMaxTuples = 1ull << 40;
 // Element counts above this are taken as this: no array that large fits an
@@ -30,6 +29,7 @@ struct LmadDiv {
     uint32_t s1, s2;
 };
 
+// The magic numbers for dividing `bits`-bit words by d (host).
 inline LmadDiv make_div(uint64_t d, int bits) {
     LmadDiv f;
     f.d = d;
