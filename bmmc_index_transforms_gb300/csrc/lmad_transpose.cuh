@@ -67,6 +67,10 @@ struct TileSides {
 #ifndef LMAD_TILE_STAGE
 #define LMAD_TILE_STAGE 1
 #endif
+// Staged byte transposes with a B of at least 256 rows take 128 x 256 tiles.
+#ifndef LMAD_BYTE_DEEP
+#define LMAD_BYTE_DEEP 1
+#endif
 // Resident blocks per SM asked of the compiler for the 1-byte pack path.
 #ifndef LMAD_BYTE_BLOCKS
 #define LMAD_BYTE_BLOCKS 6
@@ -230,6 +234,10 @@ constexpr int clog2(int v) { return v <= 1 ? 0 : 1 + clog2(v / 2); }
 // (a misaligned row) rotated by up to 3, and 1 mod 8 so that neighbouring
 // rows start 4 banks apart.
 constexpr int chunk_pitch(int nch) { return ((nch + 4 + 6) / 8) * 8 + 1; }
+// The pitch the chunk path uses: staged tiles read one whole row per shared
+// load, so their rows need no rotation, only room for a misaligned row's
+// NCH + 1 chunks.
+constexpr int chunk_path_pitch(int nch, bool stage) { return stage ? nch + 1 : chunk_pitch(nch); }
 // Bytes of dynamic shared memory a tall tile kernel takes: 128 rows of
 // chunk_pitch(16) chunks.
 constexpr int kTallTileBytes = 128 * chunk_pitch(16) * 16;
@@ -294,6 +302,17 @@ __device__ __forceinline__ void store_bytes16(unsigned char* p, uint4 v, int n) 
     }
 }
 
+// Bytes of a staged tile's destination-major layout: TA column runs of
+// DP bytes (TB rows plus 8 bytes for 1-byte words, 16 for 2-byte words,
+// which puts a half (quarter) warp's restaging stores in distinct banks).
+template <typename W>
+constexpr int staged_dm_pitch(int tb) { return sizeof(W) == 1 ? tb + 8 : 2 * tb + 16; }
+template <typename W>
+constexpr int staged_dm_bytes(int nch, int tall) {
+    return nch * (16 / (int)sizeof(W)) *
+           staged_dm_pitch<W>(tall * TileShape<sizeof(W)>::T / (nch * (16 / (int)sizeof(W))));
+}
+
 // The store phase of a staged tile (the chunk path's fill has put the TB
 // source rows in shared memory, row r shifted by its misalignment: base_mis
 // plus B's source offset of r modulo V, the same for all rows when uni).
@@ -302,9 +321,10 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
                                                   bool first_b, bool last_b, unsigned base_mis, bool uni) {
     constexpr int V = 16 / (int)sizeof(W);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA;
-    constexpr int kPitch = chunk_pitch(NCH) * V;
+    constexpr int kPitch = chunk_path_pitch(NCH, true) * V;
     constexpr int EPW = 4 / (int)sizeof(W);  // elements of a 4-byte word
-    static_assert(sizeof(W) <= 2 && TB == 128, "staged tiles: 1- and 2-byte words, 128 rows");
+    static_assert(sizeof(W) <= 2 && (TB == 128 || (sizeof(W) == 1 && TB == 256)),
+                  "staged tiles: 1- and 2-byte words, 128 rows (256 for bytes)");
     const int t = threadIdx.x, w = t >> 5, l = t & 31;
     // rows 0..7 of EPW columns, two or four rows a 32-bit word
     struct Cols {
@@ -327,9 +347,8 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     // each column run is read back in aligned 16-byte granules,
     // shifted to the destination's alignment in registers and
     // written as 16-byte stores (below).
-    constexpr int DP = sizeof(W) == 1 ? TB + 8 : 2 * TB + 16;  // bytes between column runs
-    static_assert(TA * DP <= TALL * (TileShape<sizeof(W)>::T / (NCH * V)) * chunk_pitch(NCH) * 16,
-                  "the destination-major tile fits the shared tile");
+    constexpr int DP = staged_dm_pitch<W>(TB);  // bytes between column runs
+    static_assert(TA * DP == staged_dm_bytes<W>(NCH, TALL), "the kernel sizes its tile for the destination-major layout");
     // Gather: an item is 8 rows x 32 consecutive 4-byte words of one
     // row segment (lane l takes word l, so each shared load reads
     // 128 consecutive bytes of one row: no bank conflict whatever
@@ -458,7 +477,7 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     // destination word k (run bytes fb + 16 k ..) is bytes fb.. of
     // that pair: the words are picked by two selects on fb / 4 and
     // joined by funnel shifts on fb mod 4.
-    constexpr int LPR = sizeof(W) == 1 ? 8 : 16;  // lanes per column run (TB * sizeof(W) / 16)
+    constexpr int LPR = TB * (int)sizeof(W) / 16;  // lanes per column run
     constexpr int CPI = 32 / LPR;                 // columns per warp step
     static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
     const int k = l & (LPR - 1);
@@ -522,20 +541,27 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
             // through V consecutive columns.  Step s of the tile takes,
             // from columns V * (s / 4) .. + V - 1, the CPI columns whose
             // first aligned word is fb = 4 (s mod 4) .. 4 (s mod 4) + 3
-            // bytes away: ia = V * (s / 4) + (-(fb / e) - p0) / ta mod V.
-            // A warp's steps then share s mod 4 = w mod 4, so its word
-            // offset is fixed for the whole tile.
+            // bytes away: ia = V * (s / 4) + (-(fb / e) - p0) / ta mod V
+            // (s / (4 HN) and (s / HN) mod 4 when a step has fewer columns
+            // than an offset).  A warp's steps then share one offset, fixed
+            // for the whole tile.
             const unsigned p0 = (unsigned)(((uintptr_t)(dst + ad.dst_b(0)) / sizeof(W)) & (V - 1));
             const unsigned ta = (unsigned)ad.ta;
             unsigned tinv = ta;                        // ta^-1 mod 8 (ta odd) ...
             tinv *= 2u - ta * tinv;                    // ... mod 64 (Newton)
-            const unsigned fbe = (unsigned)(4 * (w & 3) / (int)sizeof(W)) + (unsigned)(l / LPR);  // fb / e
+            // (with CPI columns a step and 4 / e columns of each word offset
+            // in V columns, HN steps take one offset: step s has the offset
+            // (s / HN) mod 4 and its (s mod HN)-th CPI columns)
+            constexpr int HN = 4 / (int)sizeof(W) / CPI;
+            static_assert(HN >= 1 && HN * CPI * (int)sizeof(W) == 4 && 8 % (4 * HN) == 0, "whole offset classes");
+            const int qw = (w / HN) & 3;
+            const unsigned fbe = (unsigned)(4 * qw / (int)sizeof(W) + (w % HN) * CPI + l / LPR);  // fb / e
             const int rho = (int)(((0u - fbe - p0) * tinv) & (unsigned)(V - 1));
             auto run = [&](auto QC) {
 #pragma unroll 1
-                for (int it = 0; it < STEPS; ++it) step(V * (2 * it + (w >> 2)) + rho, QC);
+                for (int it = 0; it < STEPS; ++it) step(V * ((8 * it + w) / (4 * HN)) + rho, QC);
             };
-            switch (w & 3) {
+            switch (qw) {
                 case 0: run(std::integral_constant<int, 0>{}); break;
                 case 1: run(std::integral_constant<int, 1>{}); break;
                 case 2: run(std::integral_constant<int, 2>{}); break;
@@ -555,7 +581,7 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
                                                     bool last_b) {
     constexpr int V = 16 / (int)sizeof(W), LNCH = clog2(NCH);
     constexpr int TA = NCH * V, TB = TALL * (int)TileShape<sizeof(W)>::T / TA, LTB = clog2(TB);
-    constexpr int kPitch = chunk_pitch(NCH) * V;
+    constexpr int kPitch = chunk_path_pitch(NCH, STAGE) * V;
     // 1- and 2-byte words with packs move 8-row blocks through registers
     // (below).  Their rows rotate by ROT chunks per 8 rows over PH phases
     // (1 byte: 2 chunks, 4 phases; 2 bytes: 1 chunk, 8 phases), the others'
@@ -564,10 +590,11 @@ __device__ __forceinline__ void tile_phases_chunked(const W* __restrict__ src, W
     // (staged tiles read one row per shared load, so rows need no rotation)
     constexpr int ROT = STAGE ? 0 : REG && sizeof(W) == 1 ? 2 : 1;
     constexpr int PH = REG && sizeof(W) == 2 ? 8 : 4;
-    static_assert(NCH + 1 + ROT * (PH - 1) <= chunk_pitch(NCH) && TB <= 256, "rotated rows fit the pitch");
+    static_assert(NCH + 1 + ROT * (PH - 1) <= chunk_path_pitch(NCH, STAGE) && TB <= 256, "rotated rows fit the pitch");
     static_assert(TALL == 1 || (REG && (sizeof(W) == 1 || STAGE)), "tall tiles on the 1-byte or staged pack path only");
     static_assert(!SHIFT || REG, "realigned packs on the 1- and 2-byte register path only");
-    static_assert(!STAGE || (REG && !SHIFT && TB == 128), "staged columns: 1- and 2-byte words, 128-row tiles");
+    static_assert(!STAGE || (REG && !SHIFT && (TB == 128 || (sizeof(W) == 1 && TB == 256))),
+                  "staged columns: 1- and 2-byte words, 128-row tiles (256 for bytes)");
     const int t = threadIdx.x;
     const unsigned base_mis = (unsigned)(((uintptr_t)src / sizeof(W)) & (V - 1));
     // every row shares the origin's misalignment (B's source stride a
@@ -1264,17 +1291,22 @@ __global__ void __launch_bounds__(256, tile_min_blocks<W, MODE>())
     constexpr int kTab = Sides::kMax + Sides::kMin * TALL;  // >= TA + TB
     constexpr int kElemTile = S::T + Sides::kMax * S::PAD;
     constexpr int NCH = (MODE & kTileHalfRows) ? 8 : 16;  // chunk path: chunks per source row
-    // chunk path: TALL * T / TA rows of chunk_pitch(NCH) chunks of 16 / W elements
-    constexpr int kChunkTile = sizeof(W) <= 8 ? TALL * (S::T / (NCH * (16 / (int)sizeof(W)))) * chunk_pitch(NCH) *
+    // chunk path: TALL * T / TA rows of chunk_path_pitch chunks of 16 / W
+    // elements (and for staged tiles room for the destination-major layout)
+    constexpr int kChunkTile = sizeof(W) <= 8 ? TALL * (S::T / (NCH * (16 / (int)sizeof(W)))) *
+                                                    chunk_path_pitch(NCH, (MODE & kTileStaged) != 0) *
                                                     (16 / (int)sizeof(W))
                                               : 0;
     // 16-byte cp.async targets; tall tiles (over 48 KiB) in dynamic shared
     // memory, the launcher having raised the kernel's limit
-    constexpr bool DYN = TALL > 1;
-    __shared__ __align__(16) W tile_s[DYN ? 1 : (kElemTile > kChunkTile ? kElemTile : kChunkTile)];
+    constexpr int kStageTile = (MODE & kTileStaged) != 0 ? staged_dm_bytes<W>(NCH, TALL) / (int)sizeof(W) : 0;
+    constexpr int kStatic = std::max(kElemTile, std::max(kChunkTile, kStageTile));
+    // (staged tiles fit in static shared memory)
+    constexpr bool DYN = TALL > 1 && (MODE & kTileStaged) == 0;
+    __shared__ __align__(16) W tile_s[DYN ? 1 : kStatic];
     extern __shared__ __align__(16) unsigned char lmad_dyn_smem[];
     W* const tile = DYN ? reinterpret_cast<W*>(lmad_dyn_smem) : tile_s;
-    static_assert(!DYN || (sizeof(W) <= 2 && kChunkTile * (int)sizeof(W) == kTallTileBytes && kElemTile <= kChunkTile),
+    static_assert(!DYN || (sizeof(W) <= 2 && kStatic * (int)sizeof(W) <= kTallTileBytes),
                   "the launcher's dynamic shared memory holds the tall tile");
     constexpr bool GENERAL = (MODE & kTileTables) != 0;
     constexpr bool CHUNKED = (MODE & kTileChunked) != 0 && sizeof(W) <= 8;
@@ -1545,6 +1577,9 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     const int mode = L.mode & ~kTileWide;
     constexpr int kWide = kTileWide;
 #define LMAD_TILE(WV, MV) lmad_tile_kernel<W, WV, MV><<<grid, 256, 0, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()))
+// staged tiles take static shared memory (measured no slower than the
+// dynamic allocation of the other tall tiles)
+#define LMAD_STAGED(WV, MV) LMAD_TILE(WV, MV)
     if constexpr (sizeof(W) <= 2) {
         if (mode & kTileTall) {
 #define LMAD_TALL(WV, MV)                                                                              \
@@ -1556,12 +1591,12 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
     } while (0)
             if constexpr (sizeof(W) == 2) {
                 switch (mode | (wide ? kWide : 0)) {
-                    case 278: LMAD_TALL(false, 278); break;
-                    case 279: LMAD_TALL(false, 279); break;
-                    case 310: LMAD_TALL(true, 278); break;
-                    case 311: LMAD_TALL(true, 279); break;
-                    case 406: LMAD_TALL(false, 406); break;
-                    case 407: LMAD_TALL(false, 407); break;
+                    case 278: LMAD_STAGED(false, 278); break;
+                    case 279: LMAD_STAGED(false, 279); break;
+                    case 310: LMAD_STAGED(true, 278); break;
+                    case 311: LMAD_STAGED(true, 279); break;
+                    case 406: LMAD_STAGED(false, 406); break;
+                    case 407: LMAD_STAGED(false, 407); break;
                     default: return cudaErrorInvalidValue;
                 }
             } else switch (mode | (wide ? kWide : 0)) {
@@ -1577,12 +1612,20 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
                 case 151: LMAD_TALL(false, 151); break;
                 case 214: LMAD_TALL(false, 214); break;
                 case 215: LMAD_TALL(false, 215); break;
-                case 278: LMAD_TALL(false, 278); break;
-                case 279: LMAD_TALL(false, 279); break;
-                case 310: LMAD_TALL(true, 278); break;
-                case 311: LMAD_TALL(true, 279); break;
-                case 406: LMAD_TALL(false, 406); break;
-                case 407: LMAD_TALL(false, 407); break;
+                case 278: LMAD_STAGED(false, 278); break;
+                case 279: LMAD_STAGED(false, 279); break;
+                case 310: LMAD_STAGED(true, 278); break;
+                case 311: LMAD_STAGED(true, 279); break;
+                case 406: LMAD_STAGED(false, 406); break;
+                case 407: LMAD_STAGED(false, 407); break;
+#if LMAD_BYTE_DEEP
+                case 286: LMAD_STAGED(false, 286); break;  // 128 x 256 staged byte tiles
+                case 287: LMAD_STAGED(false, 287); break;
+                case 318: LMAD_STAGED(true, 286); break;
+                case 319: LMAD_STAGED(true, 287); break;
+                case 414: LMAD_STAGED(false, 414); break;
+                case 415: LMAD_STAGED(false, 415); break;
+#endif
                 default: return cudaErrorInvalidValue;
             }
 #undef LMAD_TALL
@@ -1682,6 +1725,7 @@ cudaError_t launch_transpose_w(const W* in, W* out, const LmadCopy& C, cudaStrea
         if (mode == kTileTables) LMAD_TILE(false, kTileTables);
         else LMAD_TILE(false, kTileLinear);
     }
+#undef LMAD_STAGED
 #undef LMAD_TILE
     return cudaGetLastError();
 }

@@ -50,11 +50,17 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     const bool stage_ok = LMAD_TILE_STAGE && n_b >= (word == 1 ? 112u : 129u);
     const bool long2 = shift && word == 2 && row_bytes == 256 && C.lb == 6 && n_b >= 128;
     const bool tall2 = stage_ok && long2, halve = !stage_ok && long2;
-    const int la = C.la - (halve ? 1 : 0), lb = C.lb + (tall ? 2 : 0) + (tall2 || halve ? 1 : 0);
+    // bytes with a B of at least 256 rows restage 128 x 256 tiles (128-byte
+    // source rows; neighbouring tiles share 16 of 256 rows, not 16 of 128)
+    const bool deep = LMAD_BYTE_DEEP && stage_ok && shift && word == 1 && n_b >= 256 &&
+                      ((row_bytes == 256 && C.lb == 5) || (row_bytes == 128 && C.lb == 6));
+    const int la = deep ? 7 : C.la - (halve ? 1 : 0);
+    const int lb = deep ? 8 : C.lb + (tall ? 2 : 0) + (tall2 || halve ? 1 : 0);
     // 128-row tiles of these (tall byte tiles, 128 x 128 or, for a group A
     // shorter than 128, 64 x 128 tiles of 2-byte words) restage the tile
     // destination-major instead, stepping by 128 - 16 / word rows along B
-    const bool staged = stage_ok && shift && lb == 7 && (tall || tall2 || (word == 2 && la == 6));
+    // (256 - 16 for the deep byte tiles)
+    const bool staged = stage_ok && shift && (deep || (lb == 7 && (tall || tall2 || (word == 2 && la == 6))));
     // (the last tile along B takes every row it reaches: one tile when B
     // has at most 128 rows)
     const uint64_t step_b = staged ? (1ull << lb) - 16 / word : (1ull << lb);
@@ -78,7 +84,8 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out) {
     const bool short_a = chunked && word <= 4 && n_a < (1ull << la) && !wide;
     L.mode = ((C.na > 1 || C.nb > 1) ? kTileTables : kTileLinear) | (chunked ? kTileChunked : 0) |
              (pack || shift ? kTilePack : 0) | (shift && !staged ? kTileShift : 0) | (staged ? kTileStaged : 0) |
-             (chunked && (row_bytes == 128 || halve) ? kTileHalfRows : 0) | (tall || tall2 ? kTileTall : 0) |
+             (chunked && (row_bytes == 128 || halve || deep) ? kTileHalfRows : 0) |
+             (tall || tall2 || deep ? kTileTall : 0) |
              (short_a ? kTileShort : 0) | (wide ? kTileWide : 0);
     L.la = la;
     L.lb = lb;

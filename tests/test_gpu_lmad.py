@@ -357,19 +357,26 @@ def _two_dim_group_a_view(Rb, a1, a0, in_off=0, out_off=0, pad=5, bpad=3):
 
 
 @pytest.mark.parametrize("elem,view,flags", [
-    # bytes: 256 x 128 tiles, one source misalignment / one per row, a group A
-    # shorter than a tile, offset tables with and without a short group A
-    (1, dict(R=300, C=1000, out_pitch=301), {"tall"}),
-    (1, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=2, out_pitch=301), {"tall"}),
+    # bytes, B of 112-255 rows: 256 x 128 tiles, one source misalignment /
+    # one per row, a group A shorter than a tile, offset tables with and
+    # without a short group A
+    (1, dict(R=200, C=1000, out_pitch=201), {"tall"}),
     (1, dict(R=129, C=777, in_off=5, in_pitch=781, out_pitch=143), {"tall"}),
-    (1, dict(R=300, C=200, out_pitch=303), {"tall", "short_a"}),
+    (1, dict(R=200, C=200, out_pitch=203), {"tall", "short_a"}),
+    (1, ("tables", 200, 4, 64), {"tables", "tall"}),
+    (1, ("tables", 200, 3, 64), {"tables", "tall", "short_a"}),
+    # bytes, B of 256 rows or more: 128 x 256 tiles (128-byte source rows)
+    (1, dict(R=300, C=1000, out_pitch=301), {"tall", "half_rows"}),
+    (1, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=2, out_pitch=301), {"tall", "half_rows"}),
+    (1, dict(R=600, C=333, in_off=3, in_pitch=339, out_pitch=611), {"tall", "half_rows"}),
+    (1, dict(R=300, C=100, out_pitch=303), {"tall", "half_rows", "short_a"}),
+    (1, ("tables", 300, 4, 64), {"tables", "tall", "half_rows"}),
+    (1, ("tables", 300, 3, 32), {"tables", "tall", "half_rows", "short_a"}),
     # even destination strides (per-lane word selection) and one
     # misalignment shared by every column (stride a multiple of 16)
-    (1, dict(R=300, C=1000, out_pitch=302), {"tall"}),
-    (1, dict(R=300, C=1000, in_off=3, out_pitch=306), {"tall"}),
-    (1, dict(R=300, C=1000, out_off=5, out_pitch=304), {"tall"}),
-    (1, ("tables", 300, 4, 64), {"tables", "tall"}),
-    (1, ("tables", 300, 3, 64), {"tables", "tall", "short_a"}),
+    (1, dict(R=300, C=1000, out_pitch=302), {"tall", "half_rows"}),
+    (1, dict(R=200, C=1000, in_off=3, out_pitch=206), {"tall"}),
+    (1, dict(R=300, C=1000, out_off=5, out_pitch=304), {"tall", "half_rows"}),
     # 2-byte words: 128 x 128 tiles, or 64 x 128 where group A is 64 or shorter
     (2, dict(R=300, C=1000, out_pitch=301), {"tall"}),
     (2, dict(R=300, C=1000, in_off=1, in_pitch=1003, out_off=3, out_pitch=301), {"tall"}),
@@ -422,8 +429,8 @@ def test_staged_with_reversed_columns_and_batches(elem):
     _check(w, elem, seed=4)
 
 
-@pytest.mark.parametrize("elem,R,C,pitch", [(1, 120, 256, (1 << 23) + 5), (2, 130, 128, (1 << 24) + 3),
-                                            (2, 130, 64, (1 << 25) + 1)])
+@pytest.mark.parametrize("elem,R,C,pitch", [(1, 120, 256, (1 << 23) + 5), (1, 260, 128, (1 << 24) + 7),
+                                            (2, 130, 128, (1 << 24) + 3), (2, 130, 64, (1 << 25) + 1)])
 def test_staged_variants_with_64bit_offsets(elem, R, C, pitch):
     """The restaged variants with 64-bit offsets: columns of a transpose
     spread over a destination of more than 2^31 elements (2-4 GiB).  Each

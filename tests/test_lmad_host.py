@@ -404,8 +404,9 @@ def _transpose_2d(R, C, out_off=0, out_pitch=None):
     # aligned byte transpose with a long B: register packs in 256 x 128 tiles
     (16384, 16384, 1, 0, None, {"chunked", "packs", "tall"}, (256, 128)),
     # destination columns at odd offsets: tall tiles restaged destination-major
-    (16385, 16384, 1, 0, None, {"chunked", "packs", "tall", "staged"}, (256, 128)),
-    (16384, 16384, 1, 3, None, {"chunked", "packs", "tall", "staged"}, (256, 128)),
+    (16385, 16384, 1, 0, None, {"chunked", "packs", "half_rows", "tall", "staged"}, (128, 256)),
+    (16384, 16384, 1, 3, None, {"chunked", "packs", "half_rows", "tall", "staged"}, (128, 256)),
+    (200, 16384, 1, 3, None, {"chunked", "packs", "tall", "staged"}, (256, 128)),
     # ... but stay realigned when B is short: 256 x 32 tiles under 64 rows,
     # tall ones under 112 (where the restaging measured slower)
     (48, 16384, 1, 3, None, {"chunked", "packs", "realigned"}, (256, 32)),
@@ -627,22 +628,23 @@ def test_realigned_pack_store_schedule_replay(seed):
     assert (cnt <= 1).all() and np.array_equal(mem, want)
 
 
-def _staged_store_replay(R, C, elem, out_pitch, out_off, TA):
+def _staged_store_replay(R, C, elem, out_pitch, out_off, TA, TB=128):
     """The staged store schedule of the tile kernel replayed on the host for
     the transpose of a row-major [R][C] array of 1- or 2-byte words into
     columns of pitch out_pitch (B = R rows, destination stride 1; A = C
-    columns): TA x 128 tiles (TA = 256 for bytes, 128 or, for a group A
-    shorter than that, 64 for 2-byte words) stepped by 128 - 16 / elem rows
-    along B (the last tile reaching the end of B, so B of at most 128 rows is
-    one tile), the last A tile shifted back (or, for a group A shorter than a
-    tile, its columns masked); each column of a tile holds its fetched rows
-    as one run, and writes the aligned 16-byte words starting in its first
-    128 - 16 / elem rows (the last tile: in all its rows), each formed from
+    columns): TA x TB tiles (256 x 128 or 128 x 256 for bytes, 128 x 128 or,
+    for a group A shorter than that, 64 x 128 for 2-byte words) stepped by
+    TB - 16 / elem rows along B (the last tile reaching the end of B, so B of
+    at most TB rows is one tile), the last A tile shifted back (or, for a
+    group A shorter than a tile, its columns masked); each column of a tile
+    holds its fetched rows as one run, and writes the aligned 16-byte words
+    starting in its first TB - 16 / elem rows (the last tile: in all its
+    rows), each formed from
     the run's aligned 4-byte words by funnel shifts, cut at the last fetched
     row, plus (B index 0 only) the partial word before the first aligned
     one.  Bytes past the fetched rows hold garbage, which must never land.
     Returns the byte image written and how often each byte was written."""
-    V, TB = 16 // elem, 128
+    V = 16 // elem
     STEP, LPR = TB - V, TB * elem // 16
     tiles_b = 1 if R <= TB else 1 + (R - TB + STEP - 1) // STEP
     out_bytes = (out_off + (C - 1) * out_pitch + R) * elem
@@ -700,17 +702,17 @@ def _staged_store_replay(R, C, elem, out_pitch, out_off, TA):
     return mem, cnt, want
 
 
-@pytest.mark.parametrize("seed", range(27))
+@pytest.mark.parametrize("seed", range(32))
 def test_staged_store_schedule_replay(seed):
     """Every destination byte of a transpose into unaligned columns is
     written exactly once with its value, and nothing else is written, by the
     staged store schedule (host replay; whole, ragged and shifted tiles,
     short groups A, B shorter than one step, every column phase)."""
     rng = np.random.default_rng(1000 + seed)
-    elem, TA = ((1, 256), (2, 128), (2, 64))[seed % 3]
+    elem, TA, TB = ((1, 256, 128), (2, 128, 128), (2, 64, 128), (1, 128, 256))[seed % 4]
     C = int(rng.choice([TA // 2 + 3, TA - 5, TA + 7, 2 * TA - 1]))
-    R = int(rng.choice([5, 64 + 3, 128 - 16 // elem, 128 - 16 // elem + 1, 128, 129, 200, 240, 3 * 128 - 7]))
+    R = int(rng.choice([5, 64 + 3, TB - 16 // elem, TB - 16 // elem + 1, TB, TB + 1, 200, 240, 3 * TB - 7]))
     out_pitch = R + int(rng.integers(0, 17))
     out_off = int(rng.integers(0, 16))
-    mem, cnt, want = _staged_store_replay(R, C, elem, out_pitch, out_off, TA)
+    mem, cnt, want = _staged_store_replay(R, C, elem, out_pitch, out_off, TA, TB)
     assert (cnt <= 1).all() and np.array_equal(mem, want)
