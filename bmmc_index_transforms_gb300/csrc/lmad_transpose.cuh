@@ -469,18 +469,28 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
         }
     }
     __syncthreads();  // the destination-major tile is written
-    // Each column run is written by LPR lanes (8 for bytes, 16 for
-    // 2-byte words), lane k holding the run's 16-byte granule k (two
-    // 8-byte or one 16-byte shared load; a half or quarter warp reads
-    // whole 128-byte stretches, no bank conflict) and taking
-    // granule k + 1 from its neighbour by shuffles.  Its aligned
-    // destination word k (run bytes fb + 16 k ..) is bytes fb.. of
-    // that pair: the words are picked by two selects on fb / 4 and
-    // joined by funnel shifts on fb mod 4.
+    // Each column run is written by LPR lanes (8 for 128-row byte
+    // tiles, 16 for 2-byte words and 256-row byte tiles), the lane of
+    // granule k holding the run's 16-byte granule k (two 8-byte or one
+    // 16-byte shared load) and taking granule k + 1 from its neighbour
+    // by shuffles.  Its aligned destination word k (run bytes
+    // fb + 16 k ..) is bytes fb.. of that pair: the words are picked
+    // by two selects on fb / 4 and joined by funnel shifts on fb mod 4.
+    // A half warp's 8-byte loads (a quarter warp's 16-byte ones) must
+    // cover 128 bytes of distinct banks: 16 lanes along one 256-byte
+    // run would meet every bank twice, so with 16 lanes a byte run the
+    // 8-lane groups alternate between the step's two columns (column
+    // slot c = bit 3 of the lane, granule k = 8 * bit 4 + lane mod 8):
+    // the two columns are an odd number of columns apart and a run is
+    // DP = 264 bytes, 2 banks modulo 4, so their 8-byte words interleave.
     constexpr int LPR = TB * (int)sizeof(W) / 16;  // lanes per column run
     constexpr int CPI = 32 / LPR;                 // columns per warp step
     static_assert(LPR * 16 == TB * (int)sizeof(W) && TA % (8 * CPI) == 0, "one granule a lane, whole steps");
-    const int k = l & (LPR - 1);
+    constexpr bool SPLIT = sizeof(W) == 1 && LPR == 16;
+    const int k = SPLIT ? ((l & 7) | (l >> 4) << 3) : l & (LPR - 1);
+    const int cs = SPLIT ? (l >> 3) & 1 : l / LPR;  // column slot in a step
+    // the lane holding granule k + 1 (the last granule's lane reads its own)
+    const int nl = k == LPR - 1 ? l : SPLIT && (l & 7) == 7 ? l + 9 : l + 1;
     const int rbb = rb * (int)sizeof(W);  // fetched bytes of a column
     // the words whose first byte is below `own` are this tile's
     const int own = last_b ? rbb : (TB - V) * (int)sizeof(W);
@@ -504,7 +514,7 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
             wv[0] = a.x, wv[1] = a.y, wv[2] = a.z, wv[3] = a.w;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) wv[4 + i] = __shfl_down_sync(0xffffffffu, wv[i], 1, LPR);
+        for (int i = 0; i < 4; ++i) wv[4 + i] = __shfl_sync(0xffffffffu, wv[i], nl);
         uint32_t z[5];
         if constexpr (Q >= 0) {
 #pragma unroll
@@ -555,11 +565,11 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
             constexpr int HN = 4 / (int)sizeof(W) / CPI;
             static_assert(HN >= 1 && HN * CPI * (int)sizeof(W) == 4 && 8 % (4 * HN) == 0, "whole offset classes");
             const int qw = (w / HN) & 3;
-            const unsigned fbe = (unsigned)(4 * qw / (int)sizeof(W) + (w % HN) * CPI + l / LPR);  // fb / e
+            const unsigned fbe = (unsigned)(4 * qw / (int)sizeof(W) + (w % HN) * CPI + cs);  // fb / e
             const int rho = (int)(((0u - fbe - p0) * tinv) & (unsigned)(V - 1));
             auto run = [&](auto QC) {
 #pragma unroll 1
-                for (int it = 0; it < STEPS; ++it) step(V * ((8 * it + w) / (4 * HN)) + rho, QC);
+                for (int it = 0; it < STEPS; ++it) step(V * ((8 * it + w) >> clog2(4 * HN)) + rho, QC);
             };
             switch (qw) {
                 case 0: run(std::integral_constant<int, 0>{}); break;
@@ -571,7 +581,7 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
     }
     if (!ordered) {
 #pragma unroll 1
-        for (int it = 0; it < STEPS; ++it) step((it * 8 + w) * CPI + l / LPR, std::integral_constant<int, -1>{});
+        for (int it = 0; it < STEPS; ++it) step((it * 8 + w) * CPI + cs, std::integral_constant<int, -1>{});
     }
 }
 

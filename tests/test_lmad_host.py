@@ -702,6 +702,83 @@ def _staged_store_replay(R, C, elem, out_pitch, out_off, TA, TB=128):
     return mem, cnt, want
 
 
+def _bank_conflicts(accesses, size):
+    """Bank conflicts of one warp instruction under the shared-memory model
+    used throughout: accesses of `size` bytes are served 128 bytes at a
+    time (32 lanes of 4-byte words, half warps of 8-byte words, quarter
+    warps of 16-byte words), and a group conflicts where one of the 32
+    4-byte banks is asked for two different words.  accesses: the lanes'
+    byte addresses in lane order."""
+    per = 128 // size
+    extra = 0
+    for g in range(0, 32, per):
+        banks = {}
+        for a in accesses[g:g + per]:
+            for wd in range(a // 4, (a + size) // 4):
+                banks.setdefault(wd % 32, set()).add(wd)
+        extra += max(len(v) for v in banks.values()) - 1
+    return extra
+
+
+def _staged_shared_conflicts(elem, TA, TB, split=True):
+    """The destination-major phases of a staged tile replayed for bank
+    conflicts: lane l of warp w restages its item's EPW columns of 8 rows
+    (8-byte stores for bytes, 16-byte for 2-byte words) at column * DP +
+    row bytes, column slots rotated by (l / 4) mod EPW; then LPR lanes a
+    column run load its 16-byte granules (two 8-byte loads for bytes, one
+    16-byte load for 2-byte words), CPI columns a warp step.  With 16 lanes
+    a byte run (split), the 8-lane groups alternate between the step's two
+    columns.  Columns of a step are either neighbours or, for the ordered
+    mapping of an odd destination stride ta, V-periodic residues
+    (-(fb / e) - p0) / ta mod V.  Returns the conflicting wavefronts."""
+    V, EPW = 16 // elem, 4 // elem
+    DP = TB + 8 if elem == 1 else 2 * TB + 16
+    WPR = TA * elem // 4
+    CB = WPR // 32
+    SITEMS = (TB // 8) * CB // 8
+    extra = 0
+    for w in range(8):
+        for i in range(SITEMS):
+            x = w + 8 * i
+            r0 = 8 * (x // CB)
+            for j in range(EPW):
+                acc = []
+                for l in range(32):
+                    c0 = (32 * (x % CB) + l) * EPW
+                    rot = (l >> 2) & (EPW - 1)
+                    acc.append((c0 + ((j + rot) & (EPW - 1))) * DP + r0 * elem)
+                extra += _bank_conflicts(acc, 8 if elem == 1 else 16)
+    LPR = TB * elem // 16
+    CPI = 32 // LPR
+    sp = split and elem == 1 and LPR == 16
+    lanes = [((l & 7) | (l >> 4) << 3, (l >> 3) & 1) if sp else (l & (LPR - 1), l // LPR) for l in range(32)]
+    assert sorted(lanes) == sorted({(k, c) for k in range(LPR) for c in range(CPI)})
+    HN = max(1, EPW // CPI)
+    col_sets = [[s * CPI + c for c in range(CPI)] for s in range(4)]
+    for ta in (1, 3, 5, 7, 9, 15):
+        tinv = pow(ta, -1, V)
+        for p0 in range(V):
+            for wq in range(4 * HN):
+                fbe = [4 * ((wq // HN) & 3) // elem + (wq % HN) * CPI + c for c in range(CPI)]
+                col_sets.append([(-(f) - p0) * tinv % V for f in fbe])
+    for cols in col_sets:
+        for half in ((0, 8), (8, 0)) if elem == 1 else ((0, None),):
+            acc = [cols[c] * DP + 16 * k + half[0] for k, c in lanes]
+            extra += _bank_conflicts(acc, 8 if elem == 1 else 16)
+    return extra
+
+
+@pytest.mark.parametrize("elem,TA,TB", [(1, 256, 128), (1, 128, 256), (2, 128, 128), (2, 64, 128)])
+def test_staged_shared_phases_are_conflict_free(elem, TA, TB):
+    """The destination-major restaging stores and the granule loads of the
+    staged tiles meet no bank conflict in the model (every tile shape, both
+    column orders of phase 4); and for 256-row byte tiles, 16 lanes along a
+    single run would."""
+    assert _staged_shared_conflicts(elem, TA, TB) == 0
+    if elem == 1 and TB == 256:
+        assert _staged_shared_conflicts(elem, TA, TB, split=False) > 0
+
+
 @pytest.mark.parametrize("seed", range(32))
 def test_staged_store_schedule_replay(seed):
     """Every destination byte of a transpose into unaligned columns is
