@@ -30,7 +30,9 @@ __all__ = [
 
 CLASS_NAMES = {0: "identity", 1: "complement", 2: "bp", 3: "bpc", 4: "bmmc"}
 KERNEL_NAMES = {0: "tiled", 1: "copy", 2: "per-element"}
-LMAD_KIND_NAMES = {0: "empty", 1: "memcpy", 2: "bpc", 3: "transpose", 4: "strided", 5: "rows"}
+LMAD_KIND_NAMES = {0: "empty", 1: "memcpy", 2: "bpc", 3: "transpose", 4: "strided", 5: "rows", 6: "blocked"}
+# how lmad_copy / lmad_copy_query choose the blocked kernel (flags of lmad_copy_ex)
+LMAD_BLOCKED_FLAGS = {"auto": 0, "force": _capi.LMAD_FORCE_BLOCKED, "never": _capi.LMAD_NO_BLOCKED}
 
 
 class BmmcError(RuntimeError):
@@ -311,14 +313,15 @@ def _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides):
 
 def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
                     out_strides: Sequence[int], elem_size: int, inp=None, out=None, *, in_elems=None,
-                    out_elems=None) -> dict:
+                    out_elems=None, blocked: str = "auto") -> dict:
     """What lmad_copy would run (host only; inp / out used for alignment and
-    overlap, may be None with explicit element counts)."""
+    overlap, may be None with explicit element counts).  blocked: "auto",
+    "force" or "never" (LMAD_FORCE_BLOCKED / LMAD_NO_BLOCKED)."""
     d, sz, io, si, oo, so = _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides)
     info = _capi.LmadCopyInfo()
-    _check(_capi.lib().lmad_copy_query(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
-                                       _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
-                                       ctypes.byref(info)), "lmad_copy_query")
+    _check(_capi.lib().lmad_copy_query_ex(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
+                                          _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
+                                          LMAD_BLOCKED_FLAGS[blocked], ctypes.byref(info)), "lmad_copy_query")
     k = info.ndims
     return {"kind": LMAD_KIND_NAMES.get(info.kind, str(info.kind)), "ndims": k,
             "dims": [[int(info.sizes[i]), int(info.in_strides[i]), int(info.out_strides[i])] for i in range(k)],
@@ -329,20 +332,24 @@ def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[i
             "tile": (int(info.tile_a), int(info.tile_b)), "narrow": int(info.narrow),
             "elements": int(info.elements),
             "tile_mode": [name for name, bit in _capi.LMAD_TILE_FLAGS.items() if info.tile_mode & bit],
-            "launch_tile": (int(info.launch_tile_a), int(info.launch_tile_b))}
+            "launch_tile": (int(info.launch_tile_a), int(info.launch_tile_b)),
+            "block_extent": [int(info.block_extent[i]) for i in range(k)],
+            "block_runs": (int(info.block_run_in), int(info.block_run_out)),
+            "block_tiles": int(info.block_tiles)}
 
 
 def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], out_offset: int,
               out_strides: Sequence[int], elem_size: int, inp, out, stream=None, *, in_elems=None,
-              out_elems=None) -> None:
+              out_elems=None, blocked: str = "auto") -> None:
     """out[out_offset + sum i_k out_strides[k]] = inp[in_offset + sum i_k in_strides[k]] for every index
-    tuple (element units, any sizes); enqueued on the stream."""
+    tuple (element units, any sizes); enqueued on the stream.  blocked: as
+    for lmad_copy_query."""
     d, sz, io, si, oo, so = _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides)
     _check_buf(inp, 0, "lmad_copy", "in")
     _check_buf(out, 0, "lmad_copy", "out")
-    _check(_capi.lib().lmad_copy(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
-                                 _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
-                                 _stream(stream, inp, out)), "lmad_copy")
+    _check(_capi.lib().lmad_copy_ex(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
+                                    _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
+                                    LMAD_BLOCKED_FLAGS[blocked], _stream(stream, inp, out)), "lmad_copy")
 
 
 def _tensor_lmad(x):

@@ -27,7 +27,7 @@ CHECK_FLAGS = ["-DBMMC_BOUNDS_CHECK"]
 HEADER = os.path.join(ROOT, "include", "bmmc.h")
 
 SOURCES = ["kernels.cu", "capi.cu", "planner.cpp", "static_scratch.cu", "lmad.cu", "lmad_transpose_1_2.cu",
-           "lmad_transpose_4_8_16.cu"]
+           "lmad_transpose_4_8_16.cu", "lmad_block.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

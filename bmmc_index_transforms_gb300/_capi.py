@@ -59,7 +59,10 @@ class PlanInfo(ctypes.Structure):
 
 
 LMAD_MAX_DIMS = 16
-LMAD_COPY_EMPTY, LMAD_COPY_MEMCPY, LMAD_COPY_BPC, LMAD_COPY_TRANSPOSE, LMAD_COPY_STRIDED, LMAD_COPY_ROWS = range(6)
+(LMAD_COPY_EMPTY, LMAD_COPY_MEMCPY, LMAD_COPY_BPC, LMAD_COPY_TRANSPOSE, LMAD_COPY_STRIDED, LMAD_COPY_ROWS,
+ LMAD_COPY_BLOCKED) = range(7)
+# lmad_copy_ex / lmad_copy_query_ex flags
+LMAD_FORCE_BLOCKED, LMAD_NO_BLOCKED = 0x1, 0x2
 
 
 class LmadCopyInfo(ctypes.Structure):
@@ -69,7 +72,9 @@ class LmadCopyInfo(ctypes.Structure):
                 ("out_offset", ctypes.c_int64), ("vec", ctypes.c_int), ("transpose_out_dim", ctypes.c_int),
                 ("group_a", ctypes.c_uint32), ("group_b", ctypes.c_uint32), ("tile_a", ctypes.c_int),
                 ("tile_b", ctypes.c_int), ("narrow", ctypes.c_int), ("elements", ctypes.c_uint64),
-                ("tile_mode", ctypes.c_uint32), ("launch_tile_a", ctypes.c_int), ("launch_tile_b", ctypes.c_int)]
+                ("tile_mode", ctypes.c_uint32), ("launch_tile_a", ctypes.c_int), ("launch_tile_b", ctypes.c_int),
+                ("block_extent", ctypes.c_int64 * LMAD_MAX_DIMS), ("block_run_in", ctypes.c_int64),
+                ("block_run_out", ctypes.c_int64), ("block_tiles", ctypes.c_int64)]
 
 
 class BoundsReport(ctypes.Structure):
@@ -110,6 +115,11 @@ SIGNATURES = {
                                        ctypes.POINTER(LmadCopyInfo)]),
     "lmad_copy": (ctypes.c_int, [ctypes.c_int, i64p, ctypes.c_int64, i64p, ctypes.c_size_t, ctypes.c_int64, i64p,
                                  ctypes.c_size_t, ctypes.c_size_t, vp, vp, vp]),
+    "lmad_copy_query_ex": (ctypes.c_int, [ctypes.c_int, i64p, ctypes.c_int64, i64p, ctypes.c_size_t,
+                                          ctypes.c_int64, i64p, ctypes.c_size_t, ctypes.c_size_t, vp, vp,
+                                          ctypes.c_uint, ctypes.POINTER(LmadCopyInfo)]),
+    "lmad_copy_ex": (ctypes.c_int, [ctypes.c_int, i64p, ctypes.c_int64, i64p, ctypes.c_size_t, ctypes.c_int64,
+                                    i64p, ctypes.c_size_t, ctypes.c_size_t, vp, vp, ctypes.c_uint, vp]),
     "bmmc_parm_rows": (ctypes.c_int, [ctypes.c_int, u64, u64p]),
     "bmmc_inverse_rows": (ctypes.c_int, [ctypes.c_int, u64p, u64p]),
     "bmmc_compose": (ctypes.c_int, [ctypes.c_int, u64p, u64, u64p, u64, u64p, u64p]),

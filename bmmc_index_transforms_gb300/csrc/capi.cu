@@ -520,12 +520,13 @@ bmmc_status bmmc_bounds_report(bmmc_bounds_report_t* report, int reset) {
 #ifdef BMMC_BOUNDS_CHECK
     r.enabled = 1;
 #endif
-    unsigned long long rec[4][6] = {};
+    unsigned long long rec[5][6] = {};
     if (r.enabled) {
         if (cudaDeviceSynchronize() != cudaSuccess || bounds_record_kernels(rec[0], reset != 0) != cudaSuccess ||
             bounds_record_lmad(rec[1], reset != 0) != cudaSuccess ||
             bounds_record_lmad_transpose_1_2(rec[2], reset != 0) != cudaSuccess ||
-            bounds_record_lmad_transpose_4_8_16(rec[3], reset != 0) != cudaSuccess) {
+            bounds_record_lmad_transpose_4_8_16(rec[3], reset != 0) != cudaSuccess ||
+            bounds_record_lmad_block(rec[4], reset != 0) != cudaSuccess) {
             cudaGetLastError();
             return BMMC_ERR_CUDA;
         }

@@ -28,6 +28,7 @@ cudaError_t bounds_record_kernels(unsigned long long out[6], bool clear);
 cudaError_t bounds_record_lmad(unsigned long long out[6], bool clear);
 cudaError_t bounds_record_lmad_transpose_1_2(unsigned long long out[6], bool clear);
 cudaError_t bounds_record_lmad_transpose_4_8_16(unsigned long long out[6], bool clear);
+cudaError_t bounds_record_lmad_block(unsigned long long out[6], bool clear);
 #ifdef BMMC_BOUNDS_CHECK
 // The checks' self-test on a caller's device buffer of 512 bytes.
 cudaError_t bounds_selftest(void* buf, cudaStream_t stream);

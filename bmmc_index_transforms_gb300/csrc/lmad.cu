@@ -465,10 +465,94 @@ LmadCopy word_view(const LmadCopy& C) {
     return W;
 }
 
+// Whether the blocked copy should run instead of the kind analysed (the
+// caller's flags aside).  Measured on GB300 over random axis permutations
+// of 3- to 5-D arrays of 16-512 MiB, the blocked kernel beat:
+//   - the stride-sorted copy of a source contiguous along dimension 0 when
+//     the destination is not, or when the destination runs it writes (the
+//     dimensions from 0 that continue one another there) are under 24
+//     bytes of 2-byte or wider elements or under 8 bytes of 1-byte ones (a
+//     warp writes 32 scattered words: 0.10-0.51 against 0.28-0.55 of a
+//     copy; 3-byte pixels 0.11 against 0.17); it lost on longer runs;
+//   - narrow transposes whose tile (narrow side x the wide side's length
+//     in it) is under 4 KiB, batches of tiny transposes (0.02-0.27 against
+//     0.22-0.72);
+//   - the tile kernel's element path when its tiles are less than 60%
+//     full (a B of 2 to 37 indices: 0.07-0.52 against 0.38-0.71; 20
+//     channels of 16 bytes, 62% full, stay: 0.98 against 0.76), and its
+//     per-tile tables for words of up to 4 bytes (0.03-0.50 against
+//     0.22-0.59);
+// it never beat the chunked, packed or restaged tile variants, the copy
+// kernel, the rows kernel or a BPC.
+bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t out_addr) {
+    if (C.kind == LMAD_COPY_STRIDED) {
+        const Dim& d0 = C.d[0];
+        if (d0.s != 1) return false;
+        if (iabs(d0.t) != 1) return true;
+        uint64_t run = (uint64_t)d0.n;
+        for (int k = 1; k < C.nd && C.d[k].t == C.d[k - 1].t * C.d[k - 1].n; ++k) run *= (uint64_t)C.d[k].n;
+        return run * elem < (elem >= 2 ? 24u : 8u);
+    }
+    if (C.kind != LMAD_COPY_TRANSPOSE) return false;
+    const size_t word = elem * (size_t)C.vec;
+    const LmadCopy& V = C.vec > 1 ? word_view(C) : C;
+    uint64_t n_a = 1, n_b = 1;
+    for (int k = 0; k < V.na; ++k) n_a *= (uint64_t)V.d[V.ga[k]].n;
+    for (int k = 0; k < V.nb; ++k) n_b *= (uint64_t)V.d[V.gb[k]].n;
+    if (V.narrow) {
+        const uint64_t narrow = V.narrow == 1 ? n_a : n_b, wide = V.narrow == 1 ? n_b : n_a;
+        return narrow * std::min<uint64_t>(wide, 1ull << V.lt) * word < 4096;
+    }
+    const TileLaunch L = tile_launch(V, word, out_addr + (uintptr_t)(C.out_off * (int64_t)elem));
+    if (L.mode & LMAD_TILE_CHUNKED) return false;
+    if (L.mode & LMAD_TILE_TABLES) return word <= 4;
+    const uint64_t ta = 1ull << V.la, tb = 1ull << V.lb;
+    const double ua = (double)n_a / (double)(((n_a + ta - 1) / ta) * ta);
+    const double ub = (double)n_b / (double)(((n_b + tb - 1) / tb) * tb);
+    return ua * ub < 0.6;
+}
+
+// Takes the blocked copy when the flags or prefer_blocked ask for it: the
+// dimensions in words (dimension 0 widened as for the stride-sorted copy)
+// and the tile plan.
+void choose_blocked(LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t out_addr, unsigned flags) {
+    if (C.kind == LMAD_COPY_EMPTY || (flags & LMAD_NO_BLOCKED)) return;
+    if (!(flags & LMAD_FORCE_BLOCKED) && !prefer_blocked(C, elem, out_addr)) return;
+    const int v = widen_factor(C, elem, in_addr, out_addr);
+    int nd = 0;
+    for (int k = 0; k < C.nd; ++k) {
+        Dim x = C.d[k];
+        if (k == 0) {
+            x.n /= v;
+        } else {
+            x.s /= v;
+            x.t /= v;
+        }
+        if (x.n > 1) {
+            C.bdim[nd] = k;
+            C.bd[nd++] = x;
+        }
+    }
+    if (nd == 0) {
+        C.bdim[0] = 0;
+        C.bd[nd++] = Dim{1, 1, 1};
+    }
+    if (!block_plan(C.bd, nd, elem * (size_t)v, &C.blk)) return;
+    C.bnd = nd;
+    C.kind = LMAD_COPY_BLOCKED;
+    C.vec = v;
+    C.tdim = -1;
+    C.na = C.nb = C.nc = 0;
+    C.narrow = 0;
+}
+
 bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
                     size_t in_elems, int64_t out_offset, const int64_t* out_strides, size_t out_elems,
-                    size_t elem, uintptr_t in_addr, uintptr_t out_addr, LmadCopy& C) {
+                    size_t elem, uintptr_t in_addr, uintptr_t out_addr, LmadCopy& C, unsigned flags = 0) {
     if (ndims < 0 || ndims > 64 || (ndims > 0 && (!sizes || !in_strides || !out_strides)))
+        return BMMC_ERR_INVALID_ARG;
+    if ((flags & ~(LMAD_FORCE_BLOCKED | LMAD_NO_BLOCKED)) ||
+        (flags & (LMAD_FORCE_BLOCKED | LMAD_NO_BLOCKED)) == (LMAD_FORCE_BLOCKED | LMAD_NO_BLOCKED))
         return BMMC_ERR_INVALID_ARG;
     if (!valid_lmad_elem(elem)) return BMMC_ERR_UNSUPPORTED_ELEM;
     if ((in_addr | out_addr) % elem) return BMMC_ERR_MISALIGNED;
@@ -609,6 +693,7 @@ bmmc_status analyse(int ndims, const int64_t* sizes, int64_t in_offset, const in
         for (int k = 1; k < C.nd; ++k) contiguous_out = contiguous_out && C.d[k].t == C.d[k - 1].t * C.d[k - 1].n;
         if (contiguous_out) C.kind = LMAD_COPY_ROWS;
     }
+    choose_blocked(C, elem, in_addr, out_addr, flags);
     return BMMC_OK;
 }
 
@@ -720,14 +805,14 @@ cudaError_t bounds_record_lmad(unsigned long long out[chk::kRecordWords], bool c
 using namespace bmmc;
 using namespace bmmc::lmad;
 
-extern "C" bmmc_status lmad_copy_query(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
-                                       size_t in_elems, int64_t out_offset, const int64_t* out_strides,
-                                       size_t out_elems, size_t elem_size, const void* in, const void* out,
-                                       lmad_copy_info_t* info) {
+extern "C" bmmc_status lmad_copy_query_ex(int ndims, const int64_t* sizes, int64_t in_offset,
+                                          const int64_t* in_strides, size_t in_elems, int64_t out_offset,
+                                          const int64_t* out_strides, size_t out_elems, size_t elem_size,
+                                          const void* in, const void* out, unsigned flags, lmad_copy_info_t* info) {
     if (!info) return BMMC_ERR_INVALID_ARG;
     LmadCopy C;
     bmmc_status s = analyse(ndims, sizes, in_offset, in_strides, in_elems, out_offset, out_strides, out_elems,
-                            elem_size, (uintptr_t)in, (uintptr_t)out, C);
+                            elem_size, (uintptr_t)in, (uintptr_t)out, C, flags);
     if (s != BMMC_OK) return s;
     lmad_copy_info_t r{};
     r.kind = C.kind;
@@ -758,18 +843,34 @@ extern "C" bmmc_status lmad_copy_query(int ndims, const int64_t* sizes, int64_t 
             r.launch_tile_b = 1 << L.lb;
         }
     }
+    if (C.kind == LMAD_COPY_BLOCKED) {
+        for (int k = 0; k < r.ndims; ++k) r.block_extent[k] = 1;
+        for (int k = 0; k < C.bnd; ++k) r.block_extent[C.bdim[k]] = C.blk.m[k];
+        r.block_run_in = C.blk.rs;
+        r.block_run_out = C.blk.rd;
+        r.block_tiles = (int64_t)C.blk.tiles;
+    }
     r.elements = C.elements;
     *info = r;
     return BMMC_OK;
 }
 
-extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
-                                 size_t in_elems, int64_t out_offset, const int64_t* out_strides, size_t out_elems,
-                                 size_t elem_size, const void* in, void* out, void* stream) {
+extern "C" bmmc_status lmad_copy_query(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
+                                       size_t in_elems, int64_t out_offset, const int64_t* out_strides,
+                                       size_t out_elems, size_t elem_size, const void* in, const void* out,
+                                       lmad_copy_info_t* info) {
+    return lmad_copy_query_ex(ndims, sizes, in_offset, in_strides, in_elems, out_offset, out_strides, out_elems,
+                              elem_size, in, out, 0u, info);
+}
+
+extern "C" bmmc_status lmad_copy_ex(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
+                                    size_t in_elems, int64_t out_offset, const int64_t* out_strides,
+                                    size_t out_elems, size_t elem_size, const void* in, void* out, unsigned flags,
+                                    void* stream) {
     if (!in || !out) return BMMC_ERR_INVALID_ARG;
     LmadCopy C;
     bmmc_status s = analyse(ndims, sizes, in_offset, in_strides, in_elems, out_offset, out_strides, out_elems,
-                            elem_size, (uintptr_t)in, (uintptr_t)out, C);
+                            elem_size, (uintptr_t)in, (uintptr_t)out, C, flags);
     if (s != BMMC_OK) return s;
     if (C.kind == LMAD_COPY_EMPTY) return BMMC_OK;
     if ((s = pointer_reachable(in)) != BMMC_OK || (s = pointer_reachable(out)) != BMMC_OK) return s;
@@ -793,6 +894,9 @@ extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_off
     }
     const unsigned char* a = ib + C.in_off * (int64_t)elem_size;
     unsigned char* o = ob + C.out_off * (int64_t)elem_size;
+    if (C.kind == LMAD_COPY_BLOCKED)
+        return launch_block(a, o, elem_size * (size_t)C.vec, C.bd, C.blk, st) == cudaSuccess ? BMMC_OK
+                                                                                          : BMMC_ERR_CUDA;
     if (C.kind == LMAD_COPY_ROWS) return launch_rows(a, o, C, elem_size, st) == cudaSuccess ? BMMC_OK : BMMC_ERR_CUDA;
     if (C.kind == LMAD_COPY_MEMCPY && (((uintptr_t)a | (uintptr_t)o) & 15u) == 0) {
         e = launch_copy(a, o, (size_t)C.d[0].n * elem_size, st);
@@ -803,4 +907,11 @@ extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_off
         e = launch_strided(a, o, elem_size * (size_t)C.vec, d, C.nd, total, st);
     }
     return e == cudaSuccess ? BMMC_OK : BMMC_ERR_CUDA;
+}
+
+extern "C" bmmc_status lmad_copy(int ndims, const int64_t* sizes, int64_t in_offset, const int64_t* in_strides,
+                                 size_t in_elems, int64_t out_offset, const int64_t* out_strides, size_t out_elems,
+                                 size_t elem_size, const void* in, void* out, void* stream) {
+    return lmad_copy_ex(ndims, sizes, in_offset, in_strides, in_elems, out_offset, out_strides, out_elems, elem_size,
+                        in, out, 0u, stream);
 }

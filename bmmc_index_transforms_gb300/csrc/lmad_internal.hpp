@@ -128,6 +128,32 @@ struct Dim {
     int64_t n, s, t;  // size, source stride, destination stride
 };
 
+// How a copy runs as LMAD_COPY_BLOCKED, over dimensions d[0..nd) in words
+// (source strides positive and increasing, as analysed).  The tile has
+// extent m[k] along dimension k.  The source run is dimensions 0..srun-1
+// (each contiguous with the one before in the source, all but the last
+// whole), rs words; phase 1 walks its rows, the other tile dimensions
+// rows1[0..nrows1), fastest first (q1 rows).  The destination run is
+// drun[0..ndrun) with extents dext (each contiguous with the one before in
+// the destination, by increasing |t|, all but the last whole), rd <= 256
+// words; when the last one's tile extent is longer it is split, its first
+// dext words in the run and the rest a row dimension of its own (split,
+// split_lo = dext of it).  Phase 2 walks the rows of the destination run:
+// rows2[0..nrows2) with extents r2ext and coordinate multipliers r2mul
+// (q2 rows).  Shared memory holds the tile source-major: source run r at
+// r * rsp words, rsp >= rs padded so that neighbouring runs start in other
+// banks.
+struct BlockPlan {
+    int nd = 0;
+    int64_t m[kLmadMaxDims] = {};
+    int srun = 0, ndrun = 0, nrows1 = 0, nrows2 = 0, split = -1;
+    int drun[4] = {}, rows1[kLmadMaxDims] = {}, rows2[kLmadMaxDims + 1] = {};
+    int64_t dext[4] = {}, r2ext[kLmadMaxDims + 1] = {}, r2mul[kLmadMaxDims + 1] = {};
+    int64_t rs = 0, rd = 0, rsp = 0, q1 = 0, q2 = 0, elems = 0;
+    uint64_t tiles = 0;
+    size_t smem = 0;  // bytes of dynamic shared memory a block takes
+};
+
 struct LmadCopy {
     int kind = LMAD_COPY_EMPTY;
     int nd = 0;
@@ -150,6 +176,13 @@ struct LmadCopy {
     uint64_t bpc_c = 0;
     int64_t bpc_in_block = 0, bpc_out_block = 0;  // in elements
     size_t bpc_word = 0;                          // bytes per BPC element (elem * vec)
+    // BLOCKED: the dimensions in words of vec elements (dimension 0 of
+    // d divided by vec, dropped when that leaves one word), bdim[k] the
+    // dimension of d that word dimension k is, and the plan
+    int bnd = 0;
+    Dim bd[kLmadMaxDims];
+    int bdim[kLmadMaxDims];
+    BlockPlan blk;
 };
 
 inline uint64_t iabs(int64_t v) { return v < 0 ? (uint64_t)0 - (uint64_t)v : (uint64_t)v; }
@@ -176,6 +209,37 @@ TileLaunch tile_launch(const LmadCopy& C, size_t word, uintptr_t out);
 // its part for 4-, 8- and 16-byte words (lmad_transpose_4_8_16.cu).
 cudaError_t launch_transpose(const void* in, void* out, size_t word, const LmadCopy& C, cudaStream_t s);
 cudaError_t launch_transpose_wide(const void* in, void* out, size_t word, const LmadCopy& C, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Blocked copies (lmad_block.cu)
+// ---------------------------------------------------------------------------
+
+// The parameters of lmad_block_kernel, built from a BlockPlan.
+struct LmadBlockParams {
+    uint64_t tiles;
+    int nd, srun, nrows1, nrows2, split;
+    int32_t rs, rsp, q1, q2, rd;
+    int32_t nseg1;                               // phase-1 segments per row (runs of 32 words or more)
+    int32_t lg1, lg2;                            // log2 of a short run's lanes (runs under 32 words)
+    int32_t u2;                                  // phase-2 positions per lane
+    int64_t s0;                                  // source stride of dimension 0
+    LmadDiv tpre[kLmadMaxDims];                  // tiles of the dimensions faster than each one (64-bit)
+    LmadDiv tdiv[kLmadMaxDims];                  // tiles along each dimension (64-bit)
+    int64_t n[kLmadMaxDims], m[kLmadMaxDims], s[kLmadMaxDims], t[kLmadMaxDims];
+    int32_t sig[kLmadMaxDims];                   // shared-memory stride of each tile dimension
+    int8_t rows1[kLmadMaxDims], rows2[kLmadMaxDims + 1], drun[4];
+    int32_t dext[4];                             // extents of the destination run's dimensions
+    int32_t r2ext[kLmadMaxDims + 1], r2mul[kLmadMaxDims + 1];
+    LmadDiv rdiv1[kLmadMaxDims], rdiv2[kLmadMaxDims + 1], ddiv[4];  // by those extents (32-bit)
+    LmadDiv div_nseg1;                           // a phase-1 item into its row (32-bit)
+};
+
+// Plans the blocked copy of words of `word` bytes; false when no tile fits
+// (never for the dimension counts analyse admits).
+bool block_plan(const Dim* d, int nd, size_t word, BlockPlan* out);
+
+// Launches it (in / out: the words of index tuple 0).
+cudaError_t launch_block(const void* in, void* out, size_t word, const Dim* d, const BlockPlan& B, cudaStream_t s);
 
 #ifdef BMMC_BOUNDS_CHECK
 // The caller's two buffers of the lmad_copy call being launched on this host

@@ -569,7 +569,7 @@ __device__ __forceinline__ void tile_store_staged(W* __restrict__ dst, W* tile, 
             const int rho = (int)(((0u - fbe - p0) * tinv) & (unsigned)(V - 1));
             auto run = [&](auto QC) {
 #pragma unroll 1
-                for (int it = 0; it < STEPS; ++it) step(V * ((8 * it + w) >> clog2(4 * HN)) + rho, QC);
+                for (int it = 0; it < STEPS; ++it) step(V * ((8 / (4 * HN)) * it + (w >> clog2(4 * HN))) + rho, QC);
             };
             switch (qw) {
                 case 0: run(std::integral_constant<int, 0>{}); break;

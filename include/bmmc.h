@@ -353,13 +353,29 @@ typedef enum {
     LMAD_COPY_STRIDED = 4,   /* anything else: the page's stride-sorted copy, one
                                 thread per index tuple, adjacent threads adjacent
                                 along the smallest source stride */
-    LMAD_COPY_ROWS = 5       /* 1- and 2-byte elements whose destination is one
+    LMAD_COPY_ROWS = 5,      /* 1- and 2-byte elements whose destination is one
                                 contiguous run and whose source is rows of at least 16
                                 bytes, each contiguous (a slice or crop) but not
                                 16-byte aligned: the destination is written in aligned
                                 16-byte chunks, each assembled from the aligned 4-byte
                                 source words covering it */
+    LMAD_COPY_BLOCKED = 6    /* any other copy: tiles spanning the source's innermost
+                                contiguous dimensions and the destination's (any
+                                number of dimensions, the outermost of each run cut
+                                to a tile extent), each tile loaded along its source
+                                runs into shared memory and stored along its
+                                destination runs (lmad_copy_info_t.block_*); taken
+                                for transposes and strided copies whose other kernels
+                                would move short runs or mostly empty tiles, or when
+                                LMAD_FORCE_BLOCKED asks for it */
 } lmad_copy_kind;
+
+/* Flags of lmad_copy_ex / lmad_copy_query_ex (lmad_copy and lmad_copy_query
+ * pass 0).  Neither changes the result, only the kernel that computes it. */
+#define LMAD_FORCE_BLOCKED 0x1u  /* run every copy that moves elements (all kinds but
+                                    EMPTY) as LMAD_COPY_BLOCKED */
+#define LMAD_NO_BLOCKED    0x2u  /* never choose LMAD_COPY_BLOCKED (the other kinds
+                                    only); with LMAD_FORCE_BLOCKED: INVALID_ARG */
 
 typedef struct {
     int kind;                          /* lmad_copy_kind */
@@ -406,6 +422,13 @@ typedef struct {
     int launch_tile_a, launch_tile_b;  /* TRANSPOSE on the general tile kernel: the tile sides
                                           it launches with (tall byte tiles and realigned 2-byte
                                           tiles differ from tile_a x tile_b); 0 otherwise */
+    int64_t block_extent[LMAD_MAX_DIMS]; /* BLOCKED: the tile's extent along each dimension of
+                                          sizes (1: the dimension is not in the tile), in words
+                                          of vec elements along dimension 0; 0 for other kinds */
+    int64_t block_run_in, block_run_out; /* BLOCKED: words per source run / destination run of a
+                                          whole tile (runs are contiguous when the strides of
+                                          their fastest dimension are +-1) */
+    int64_t block_tiles;               /* BLOCKED: tiles launched */
 } lmad_copy_info_t;
 
 /* lmad_copy_info_t.tile_mode flags (the general tile kernel's variants). */
@@ -448,6 +471,14 @@ bmmc_status lmad_copy_query(int ndims, const int64_t *sizes, int64_t in_offset,
                             const int64_t *out_strides, size_t out_elems, size_t elem_size,
                             const void *in, const void *out, lmad_copy_info_t *info);
 
+/* lmad_copy_query with flags (LMAD_FORCE_BLOCKED, LMAD_NO_BLOCKED; other
+ * bits: INVALID_ARG). */
+bmmc_status lmad_copy_query_ex(int ndims, const int64_t *sizes, int64_t in_offset,
+                               const int64_t *in_strides, size_t in_elems, int64_t out_offset,
+                               const int64_t *out_strides, size_t out_elems, size_t elem_size,
+                               const void *in, const void *out, unsigned flags,
+                               lmad_copy_info_t *info);
+
 /* Run the copy (arguments as lmad_copy_query; in holds in_elems and out
  * out_elems elements of elem_size bytes, caller-owned, reachable by the GPU
  * as for bmmc_permute).  Enqueued on `stream`, no allocation, no CPU
@@ -461,6 +492,12 @@ bmmc_status lmad_copy(int ndims, const int64_t *sizes, int64_t in_offset,
                       const int64_t *in_strides, size_t in_elems, int64_t out_offset,
                       const int64_t *out_strides, size_t out_elems, size_t elem_size,
                       const void *in, void *out, void *stream);
+
+/* lmad_copy with flags (as lmad_copy_query_ex). */
+bmmc_status lmad_copy_ex(int ndims, const int64_t *sizes, int64_t in_offset,
+                         const int64_t *in_strides, size_t in_elems, int64_t out_offset,
+                         const int64_t *out_strides, size_t out_elems, size_t elem_size,
+                         const void *in, void *out, unsigned flags, void *stream);
 
 /* Inverse of an invertible n x n bit matrix over F2 (rows as in bmmc_plan):
  * inv_rows_out receives A^-1, so permuting by (A^-1, A^-1.c) undoes (A, c).
@@ -506,7 +543,7 @@ typedef struct {
     uint64_t failures;  /* accesses that failed their test since the last reset */
     int site;           /* first failure: source file tag * 100000 + line
                            (tag 1: kernels.cu, 2: lmad.cu, 3: lmad_transpose_1_2.cu,
-                           4: lmad_transpose_4_8_16.cu) */
+                           4: lmad_transpose_4_8_16.cu, 5: lmad_block.cu) */
     int bytes;          /* its access size */
     uint64_t address;   /* its address (a shared-memory offset for shared accesses) */
     uint64_t lo, hi;    /* the range [lo, hi) it was tested against */

@@ -64,7 +64,8 @@ def test_gpu_suites_on_the_bounds_checked_build():
     env = dict(os.environ, BMMC_GB300_LIBRARY=path)
     deselect = ("not n28 and not five_d and not over_4_gib and not more_than_2p32 and not every_seed")
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
-           "tests/test_gpu_lmad.py", "tests/test_gpu_parity.py", "tests/test_zz_no_alloc.py", "-k", deselect]
+           "tests/test_gpu_lmad.py", "tests/test_gpu_lmad_blocked.py", "tests/test_gpu_parity.py",
+           "tests/test_zz_no_alloc.py", "-k", deselect]
     r = subprocess.run(cmd, env=env, cwd=ROOT, capture_output=True, text=True, timeout=2400)
     tail = (r.stdout + r.stderr)[-4000:]
     assert r.returncode == 0, tail

@@ -20,6 +20,19 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
+# These tests pin the page's kinds and the transpose variants, so they run
+# without the blocked kernel (tests/test_gpu_lmad_blocked.py covers it and
+# the analysis' own choice between them).
+def _query(*args, **kw):
+    kw.setdefault("blocked", "never")
+    return bm.lmad_copy_query(*args, **kw)
+
+
+def _copy(*args, **kw):
+    kw.setdefault("blocked", "never")
+    return bm.lmad_copy(*args, **kw)
+
+
 def _fill(n_elems, elem, seed):
     """n_elems elements of elem bytes, rows of a uint8 array, distinct bytes
     patterns (a multiplicative hash of the byte index and the seed)."""
@@ -35,7 +48,7 @@ def _run(w, elem, seed=0):
     dst = np.full((w["out_elems"], elem), 0xA5, dtype=np.uint8)
     d_src = torch.from_numpy(src.reshape(-1)).cuda()
     d_dst = torch.from_numpy(dst.reshape(-1)).cuda()
-    bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem, d_src, d_dst)
+    _copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem, d_src, d_dst)
     torch.cuda.synchronize()
     got = d_dst.cpu().numpy().reshape(w["out_elems"], elem)
     want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
@@ -88,7 +101,7 @@ def test_page_workloads_full_size(kind, shape):
     src = np.arange(w["in_elems"], dtype=np.int32)
     d_src = torch.from_numpy(src).cuda()
     d_dst = torch.full((w["out_elems"],), -7, dtype=torch.int32, device="cuda")
-    bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4, d_src, d_dst)
+    _copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4, d_src, d_dst)
     torch.cuda.synchronize()
     want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
                                  src, np.full(w["out_elems"], -7, dtype=np.int32))
@@ -128,7 +141,7 @@ def test_reversed_destination_transpose_and_broadcast():
     R, C = 45, 77
     w = dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C,
              out_offset=R * C - 1, out_strides=[-1, -R], out_elems=R * C)
-    assert bm.lmad_copy_query(w["sizes"], 0, w["in_strides"], w["out_offset"], w["out_strides"], 4,
+    assert _query(w["sizes"], 0, w["in_strides"], w["out_offset"], w["out_strides"], 4,
                               in_elems=R * C, out_elems=R * C)["kind"] == "transpose"
     _check(w, 4)
     # broadcast a row to every row of a matrix (source stride 0)
@@ -149,7 +162,7 @@ def test_memcpy_aligned_and_not(offset_elems, elem):
     n = 100003
     w = dict(sizes=[n], in_offset=offset_elems, in_strides=[1], in_elems=n + 8, out_offset=(3 * offset_elems) % 7,
              out_strides=[1], out_elems=n + 8)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "memcpy"
     _check(w, elem)
@@ -167,7 +180,7 @@ def test_bpc_route_matches_oracle():
     # reverse axis 1 on the source, and place the whole block at an offset of 64 elements
     w = dict(sizes=list(shape), in_offset=15 * 32, in_strides=[512, -32, 1], in_elems=total,
              out_offset=64, out_strides=out_strides, out_elems=total + 128)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "bpc"
     _check(w, 4)
@@ -187,23 +200,23 @@ def test_64bit_index_paths():
         d_src[off: off + 64] = torch.arange(64, dtype=torch.uint8, device="cuda") + 64 * r
     # rows: 3 rows of 60 bytes from offset 3 of each, into a dense 3 x 60
     d_dst = torch.full((180,), 0xA5, dtype=torch.uint8, device="cuda")
-    q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [60, 1], 1, in_elems=in_elems, out_elems=180)
+    q = _query([3, 60], 3, [gap, 1], 0, [60, 1], 1, in_elems=in_elems, out_elems=180)
     assert q["kind"] == "rows"
-    bm.lmad_copy([3, 60], 3, [gap, 1], 0, [60, 1], 1, d_src, d_dst)
+    _copy([3, 60], 3, [gap, 1], 0, [60, 1], 1, d_src, d_dst)
     want = np.concatenate([np.arange(3, 63) + 64 * r for r in range(3)]).astype(np.uint8)
     assert np.array_equal(d_dst.cpu().numpy(), want)
     # strided: the same rows into a 3 x 64 destination (rows padded: not one run)
     d_dst3 = torch.full((192,), 0xA5, dtype=torch.uint8, device="cuda")
-    q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [64, 1], 1, in_elems=in_elems, out_elems=192)
+    q = _query([3, 60], 3, [gap, 1], 0, [64, 1], 1, in_elems=in_elems, out_elems=192)
     assert q["kind"] == "strided"
-    bm.lmad_copy([3, 60], 3, [gap, 1], 0, [64, 1], 1, d_src, d_dst3)
+    _copy([3, 60], 3, [gap, 1], 0, [64, 1], 1, d_src, d_dst3)
     got3 = d_dst3.cpu().numpy().reshape(3, 64)
     assert np.array_equal(got3[:, :60].ravel(), want) and (got3[:, 60:] == 0xA5).all()
     # transpose: the same rows written as columns of a 60 x 3
     d_dst2 = torch.full((180,), 0xA5, dtype=torch.uint8, device="cuda")
-    q = bm.lmad_copy_query([3, 60], 3, [gap, 1], 0, [1, 3], 1, in_elems=in_elems, out_elems=180)
+    q = _query([3, 60], 3, [gap, 1], 0, [1, 3], 1, in_elems=in_elems, out_elems=180)
     assert q["kind"] == "transpose"
-    bm.lmad_copy([3, 60], 3, [gap, 1], 0, [1, 3], 1, d_src, d_dst2)
+    _copy([3, 60], 3, [gap, 1], 0, [1, 3], 1, d_src, d_dst2)
     assert np.array_equal(d_dst2.cpu().numpy(), want.reshape(3, 60).T.ravel())
     del d_src
     torch.cuda.empty_cache()
@@ -212,8 +225,8 @@ def test_64bit_index_paths():
 def test_empty_and_single_element():
     d_src = torch.arange(10, dtype=torch.int32, device="cuda")
     d_dst = torch.full((10,), -1, dtype=torch.int32, device="cuda")
-    bm.lmad_copy([4, 0], 0, [1, 1], 0, [1, 1], 4, d_src, d_dst)
-    bm.lmad_copy([], 7, [], 2, [], 4, d_src, d_dst)
+    _copy([4, 0], 0, [1, 1], 0, [1, 1], 4, d_src, d_dst)
+    _copy([], 7, [], 2, [], 4, d_src, d_dst)
     torch.cuda.synchronize()
     want = np.full(10, -1, np.int32)
     want[2] = 7
@@ -224,9 +237,9 @@ def test_errors_enqueue_nothing():
     d_src = torch.arange(20, dtype=torch.int32, device="cuda")
     d_dst = torch.full((20,), -1, dtype=torch.int32, device="cuda")
     with pytest.raises(bm.BmmcError):
-        bm.lmad_copy([4, 5], 1, [5, 1], 0, [5, 1], 4, d_src, d_dst)  # source past its end
+        _copy([4, 5], 1, [5, 1], 0, [5, 1], 4, d_src, d_dst)  # source past its end
     with pytest.raises(bm.BmmcError):
-        bm.lmad_copy([4, 5], 0, [5, 1], 0, [5, 1], 4, d_src, d_src)  # in place
+        _copy([4, 5], 0, [5, 1], 0, [5, 1], 4, d_src, d_src)  # in place
     torch.cuda.synchronize()
     assert (d_dst.cpu().numpy() == -1).all()
 
@@ -245,7 +258,7 @@ def test_multidim_groups_on_whole_chunked_tiles(in_offset):
     total = int(np.prod(shape))
     w = dict(sizes=list(shape), in_offset=in_offset, in_strides=src_strides, in_elems=total + 4, out_offset=0,
              out_strides=out_strides, out_elems=total)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and len(q["group_a"]) >= 2 and q["tile"] == (64, 64)
     _check(w, 4)
@@ -285,7 +298,7 @@ def test_byte_transposes_through_registers(case):
     registers with byte permutes, with aligned, uniformly and per-row
     misaligned source rows, 256- and 128-byte rows and partial row groups."""
     w = _byte_transpose_view(**case)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and not q["narrow"]
     _check(w, 1)
@@ -304,7 +317,7 @@ def test_two_byte_transposes_through_registers(case):
     of 256 and 128 bytes, aligned, uniformly and per-row misaligned sources,
     partial row groups, and a destination that takes no packs."""
     w = _byte_transpose_view(**case)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 2,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 2,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and not q["narrow"]
     _check(w, 2)
@@ -314,7 +327,7 @@ def test_two_byte_transposes_through_registers(case):
 def test_two_byte_transposes_through_registers_with_tables():
     w = dict(sizes=[64, 4, 32], in_offset=1, in_strides=[128, 32, 1], in_elems=1 + 64 * 128, out_offset=0,
              out_strides=[1, 2056, 64], out_elems=3 * 2056 + 31 * 64 + 64)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 2,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 2,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and len(q["group_a"]) == 2
     _check(w, 2)
@@ -338,7 +351,7 @@ def test_transposes_into_unaligned_destination_columns(elem, case):
     words, realigned by lane shuffles, with narrow stores only at the edges
     of a tile's column segment (which meet the neighbouring tile's)."""
     w = _byte_transpose_view(**case)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and not q["narrow"]
     _check(w, elem)
@@ -398,7 +411,7 @@ def test_staged_variants_match_oracle(elem, view, flags):
     matches the oracle's copy loop byte for byte, positions outside the copy
     untouched."""
     w = _two_dim_group_a_view(*view[1:]) if isinstance(view, tuple) else _byte_transpose_view(**view)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and not q["narrow"]
     assert set(q["tile_mode"]) == {"chunked", "packs", "staged"} | flags, q["tile_mode"]
@@ -415,14 +428,14 @@ def test_staged_with_reversed_columns_and_batches(elem):
     R, C, pitch = 300, 1000, 301
     w = dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C, out_offset=(C - 1) * pitch,
              out_strides=[1, -pitch], out_elems=(C - 1) * pitch + R)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert "staged" in q["tile_mode"]
     _check(w, elem)
     nb = 3
     w = dict(sizes=[nb, R, C], in_offset=0, in_strides=[R * C + 7, C, 1], in_elems=nb * (R * C + 7), out_offset=5,
              out_strides=[C * pitch + 3, 1, pitch], out_elems=5 + (nb - 1) * (C * pitch + 3) + (C - 1) * pitch + R)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert "staged" in q["tile_mode"]
     _check(w, elem)
@@ -439,13 +452,13 @@ def test_staged_variants_with_64bit_offsets(elem, R, C, pitch):
         pytest.skip("needs a large device")
     w = dict(sizes=[R, C], in_offset=0, in_strides=[C, 1], in_elems=R * C, out_offset=0, out_strides=[1, pitch],
              out_elems=(C - 1) * pitch + R + 16)
-    q = bm.lmad_copy_query(w["sizes"], 0, w["in_strides"], 0, w["out_strides"], elem, in_elems=w["in_elems"],
+    q = _query(w["sizes"], 0, w["in_strides"], 0, w["out_strides"], elem, in_elems=w["in_elems"],
                            out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and {"wide", "staged"} <= set(q["tile_mode"]), q["tile_mode"]
     src = _fill(w["in_elems"], elem, 9)
     d_src = torch.from_numpy(src.reshape(-1)).cuda()
     d_dst = torch.full((w["out_elems"] * elem,), 0xA5, dtype=torch.uint8, device="cuda")
-    bm.lmad_copy(w["sizes"], 0, w["in_strides"], 0, w["out_strides"], elem, d_src, d_dst)
+    _copy(w["sizes"], 0, w["in_strides"], 0, w["out_strides"], elem, d_src, d_dst)
     torch.cuda.synchronize()
     for c in range(C):
         lo = max(0, c * pitch - 16)
@@ -467,7 +480,7 @@ def test_short_group_a_on_chunk_path(elem, C, in_off, out_extra):
     aligned and misaligned source rows and destination columns."""
     R = 300
     w = _byte_transpose_view(R, C, in_off=in_off, out_pitch=R + out_extra)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose"  # (a group A longer than a tile side: the shifted last tile)
     _check(w, elem)
@@ -481,7 +494,7 @@ def test_unaligned_destination_columns_with_tables(elem):
     not collapse, plus a batch dimension."""
     w = dict(sizes=[32, 4, 64], in_offset=0, in_strides=[256, 64, 1], in_elems=32 * 256, out_offset=0,
              out_strides=[1, 2113, 33], out_elems=3 * 2113 + 63 * 33 + 32)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and len(q["group_a"]) == 2
     _check(w, elem)
@@ -496,7 +509,7 @@ def test_byte_transposes_through_registers_with_tables():
     do not collapse (a padded destination), and a batch dimension."""
     w = dict(sizes=[32, 4, 64], in_offset=0, in_strides=[256, 64, 1], in_elems=32 * 256, out_offset=0,
              out_strides=[1, 2064, 32], out_elems=3 * 2064 + 63 * 32 + 32)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and len(q["group_a"]) == 2 and q["tile"] == (256, 32)
     _check(w, 1)
@@ -506,7 +519,7 @@ def test_byte_transposes_through_registers_with_tables():
     # 300 B rows: 256 x 128 tiles with tables, a short last tile
     w = dict(sizes=[300, 4, 64], in_offset=0, in_strides=[256, 64, 1], in_elems=300 * 256, out_offset=0,
              out_strides=[1, 19472, 304], out_elems=3 * 19472 + 63 * 304 + 300)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 1,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == "transpose" and len(q["group_a"]) == 2
     _check(w, 1)
@@ -534,7 +547,7 @@ def test_permutations_of_small_inner_words(shape, perm, elem, in_offset):
     total = int(np.prod(shape))
     w = dict(sizes=list(shape), in_offset=in_offset, in_strides=src_strides, in_elems=total + in_offset,
              out_offset=0, out_strides=out_strides, out_elems=total)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     if in_offset % shape[-1] == 0:  # (words may span more than the last dimension)
         assert q["vec"] % shape[-1] == 0 and q["kind"] in ("transpose", "bpc")
@@ -548,7 +561,7 @@ def test_pinned_host_buffers():
         w = synth.page_lmad_workload(kind, shape)
         src = torch.from_numpy(_fill(w["in_elems"], 4, 5).reshape(-1)).pin_memory()
         dst = torch.full((w["out_elems"] * 4,), 0xA5, dtype=torch.uint8).pin_memory()
-        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4, src, dst,
+        _copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], 4, src, dst,
                      torch.cuda.current_stream())
         torch.cuda.synchronize()
         want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],
@@ -571,14 +584,14 @@ def test_cuda_graph_capture_and_replay():
         dst = torch.zeros(w["out_elems"] * e, dtype=torch.uint8, device="cuda")
         bufs.append((src, dst))
     for (w, e), (src, dst) in zip(cases, bufs):  # first calls outside capture: per-device set-up
-        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e, src, dst)
+        _copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e, src, dst)
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for (w, e), (src, dst) in zip(cases, bufs):
-                bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e,
+                _copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e,
                              src, dst, torch.cuda.current_stream())
     for _, dst in bufs:
         dst.zero_()
@@ -629,11 +642,11 @@ def test_more_than_2p32_tuples(kind):
         sizes, in_off, in_st, out_st = [R, C], 0, [C, 1], [1, R]
         in_elems, out_elems = R * C, R * C
     assert int(np.prod(sizes)) > (1 << 32)
-    q = bm.lmad_copy_query(sizes, in_off, in_st, 0, out_st, 1, in_elems=in_elems, out_elems=out_elems + 1)
+    q = _query(sizes, in_off, in_st, 0, out_st, 1, in_elems=in_elems, out_elems=out_elems + 1)
     assert q["kind"] == {"slice": "rows", "slice_padded": "strided", "transpose": "transpose"}[kind]
     src = _byte_fill_device(in_elems, 11)
     dst = torch.full((out_elems + 1,), 0x5A, dtype=torch.uint8, device="cuda")
-    bm.lmad_copy(sizes, in_off, in_st, 0, out_st, 1, src, dst)
+    _copy(sizes, in_off, in_st, 0, out_st, 1, src, dst)
     torch.cuda.synchronize()
     rng = np.random.default_rng(2)
     idx = [rng.integers(0, n, 200000) for n in sizes]
@@ -660,7 +673,7 @@ def test_rows_kernel_slices(elem, shape, lo, hi, out_off):
     n_out = int(np.prod(sizes))
     w = dict(sizes=sizes, in_offset=lo, in_strides=in_st, in_elems=int(np.prod(shape)), out_offset=out_off,
              out_strides=out_st, out_elems=n_out + out_off + 3)
-    q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
+    q = _query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
                            in_elems=w["in_elems"], out_elems=w["out_elems"])
     assert q["kind"] == ("rows" if (hi - lo) * elem >= 16 else "strided")
     _check(w, elem, seed=lo + hi)
@@ -688,7 +701,7 @@ def test_image_layout_conversions(elem, c, hw, offsets):
     h, w = hw
     for shape, perm, narrow in (((3, h, w, c), (0, 3, 1, 2), 1), ((3, c, h, w), (0, 2, 3, 1), 2)):
         case = _layout_case(shape, perm, *offsets)
-        q = bm.lmad_copy_query(case["sizes"], case["in_offset"], case["in_strides"], case["out_offset"],
+        q = _query(case["sizes"], case["in_offset"], case["in_strides"], case["out_offset"],
                                case["out_strides"], elem, in_elems=case["in_elems"], out_elems=case["out_elems"])
         assert q["kind"] == "transpose" and q["narrow"] == narrow, q
         _check(case, elem, seed=c * 7 + elem)
@@ -703,7 +716,7 @@ def test_mid_channel_layouts(elem, c, offsets):
     narrow kernel for 17 to 31 channels of 1- and 2-byte words, whose short
     rows the chunk path does not take), aligned and not, against the oracle."""
     case = _layout_case((2, 37, 45, c), (0, 3, 1, 2), *offsets)
-    q = bm.lmad_copy_query(case["sizes"], case["in_offset"], case["in_strides"], case["out_offset"],
+    q = _query(case["sizes"], case["in_offset"], case["in_strides"], case["out_offset"],
                            case["out_strides"], elem, in_elems=case["in_elems"], out_elems=case["out_elems"])
     assert q["kind"] == "transpose" and q["narrow"] == (1 if c < 32 and elem <= 2 else 0)
     _check(case, elem, seed=c + elem)
@@ -723,7 +736,7 @@ def test_concurrent_lmad_copies_from_threads():
         d_src = torch.from_numpy(src.reshape(-1)).cuda()
         d_dst = torch.from_numpy(dst.reshape(-1)).cuda()
         torch.cuda.synchronize()
-        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem, d_src,
+        _copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem, d_src,
                      d_dst, s)
         s.synchronize()
         want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],

@@ -11,9 +11,12 @@ from bmmc_index_transforms_gb300 import _capi, synth
 from oracle import reference as ref
 
 
-def _query(w, elem=4, inp=None, out=None):
+def _query(w, elem=4, inp=None, out=None, blocked="never"):
+    """The analysis of a view.  By default without the blocked kernel: the
+    page's kinds and the transpose variants, which decide every copy that
+    the blocked kernel does not take (that choice has tests of its own)."""
     return bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem,
-                              inp, out, in_elems=w["in_elems"], out_elems=w["out_elems"])
+                              inp, out, in_elems=w["in_elems"], out_elems=w["out_elems"], blocked=blocked)
 
 
 def _expect_normalised(w, q):
@@ -53,36 +56,37 @@ def test_page_workloads(kind, shape):
 
 def test_page_layout_examples():
     row, col = (5, 1), (1, 4)  # [4][5] row-major and column-major
-    q = bm.lmad_copy_query((4, 5), 0, row, 0, col, 4, in_elems=20, out_elems=20)
+    q = bm.lmad_copy_query((4, 5), 0, row, 0, col, 4, in_elems=20, out_elems=20, blocked="never")
     assert q["kind"] == "transpose" and q["dims"] == [[5, 1, 4], [4, 5, 1]] and q["transpose_out_dim"] == 1
-    q = bm.lmad_copy_query((4, 5), 0, row, 0, row, 4, in_elems=20, out_elems=20)
+    q = bm.lmad_copy_query((4, 5), 0, row, 0, row, 4, in_elems=20, out_elems=20, blocked="never")
     assert q["kind"] == "memcpy" and q["dims"] == [[20, 1, 1]]
     # the same with odd sizes: still one transpose, batch dimension kept apart
-    q = bm.lmad_copy_query((3, 7, 9), 0, (63, 9, 1), 0, (63, 1, 7), 4, in_elems=189, out_elems=189)
+    q = bm.lmad_copy_query((3, 7, 9), 0, (63, 9, 1), 0, (63, 1, 7), 4, in_elems=189, out_elems=189,
+                           blocked="never")
     assert q["kind"] == "transpose" and q["dims"] == [[9, 1, 7], [7, 9, 1], [3, 63, 63]]
 
 
 def test_kinds_and_widening():
     # reversed rows with a non-power-of-two row: stride-sorted, coalesced on both sides
-    q = bm.lmad_copy_query((8, 6), 5, (6, -1), 0, (6, 1), 4, in_elems=48, out_elems=48)
+    q = bm.lmad_copy_query((8, 6), 5, (6, -1), 0, (6, 1), 4, in_elems=48, out_elems=48, blocked="never")
     assert q["kind"] == "strided" and q["dims"] == [[6, 1, -1], [8, 6, 6]]
     # 16-byte words: rows of 8 int32 sliced out of rows of 12, aligned
-    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, in_elems=60, out_elems=40)
+    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, in_elems=60, out_elems=40, blocked="never")
     assert q["kind"] == "strided" and q["vec"] == 4
-    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, 16, 1 << 20, in_elems=60, out_elems=40)
+    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, 16, 1 << 20, in_elems=60, out_elems=40, blocked="never")
     assert q["vec"] == 4
-    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, 4, 1 << 20, in_elems=60, out_elems=40)
+    q = bm.lmad_copy_query((5, 8), 4, (12, 1), 0, (8, 1), 4, 4, 1 << 20, in_elems=60, out_elems=40, blocked="never")
     assert q["vec"] == 1  # source tuple 0 at byte 20 of a 4-aligned buffer
-    q = bm.lmad_copy_query((5, 8), 1, (12, 1), 0, (8, 1), 4, in_elems=60, out_elems=40)
+    q = bm.lmad_copy_query((5, 8), 1, (12, 1), 0, (8, 1), 4, in_elems=60, out_elems=40, blocked="never")
     assert q["vec"] == 1
     # broadcast source (stride 0) is allowed
-    q = bm.lmad_copy_query((4, 6), 0, (0, 1), 0, (6, 1), 8, in_elems=6, out_elems=24)
+    q = bm.lmad_copy_query((4, 6), 0, (0, 1), 0, (6, 1), 8, in_elems=6, out_elems=24, blocked="never")
     assert q["kind"] == "strided"
     # empty
-    q = bm.lmad_copy_query((4, 0, 3), 0, (1, 1, 1), 0, (1, 1, 1), 4, in_elems=0, out_elems=0)
+    q = bm.lmad_copy_query((4, 0, 3), 0, (1, 1, 1), 0, (1, 1, 1), 4, in_elems=0, out_elems=0, blocked="never")
     assert q["kind"] == "empty" and q["ndims"] == 0
     # one element, no dimensions
-    q = bm.lmad_copy_query((), 3, (), 5, (), 2, in_elems=4, out_elems=6)
+    q = bm.lmad_copy_query((), 3, (), 5, (), 2, in_elems=4, out_elems=6, blocked="never")
     assert q["kind"] == "memcpy" and q["dims"] == [[1, 1, 1]] and q["in_offset"] == 3
 
 
@@ -494,6 +498,51 @@ def test_tiny_group_a_takes_the_stride_sorted_copy():
     assert _query(_perm_view((384, 4096, 2, 12, 2), (4, 0, 2, 1, 3)), 1)["kind"] == "strided"
     q = _query(_perm_view((64, 300, 2, 16), (0, 3, 1, 2)), 1)
     assert q["kind"] == "transpose"
+
+
+@pytest.mark.parametrize("shape,perm,elem,want", [
+    ((300000, 7, 9), (0, 2, 1), 4, "blocked"),          # batched small transposes: narrow tiles under 4 KiB
+    ((1000000, 4, 5), (0, 2, 1), 4, "blocked"),
+    ((100000, 12, 20), (0, 2, 1), 4, "blocked"),
+    ((384, 4096, 2, 12, 2), (4, 0, 2, 1, 3), 1, "blocked"),  # a group A of 2 bytes (was stride-sorted)
+    ((4, 640, 960, 17), (0, 3, 1, 2), 8, "blocked"),    # element tiles 53% full
+    ((8000, 6000, 3), (1, 0, 2), 1, "blocked"),         # 3-byte pixels: 3-byte destination runs
+    ((4, 640, 960, 20), (0, 3, 1, 2), 16, "transpose"),  # 62% full: the element path stays
+    ((32, 3, 1024, 1024), (0, 2, 3, 1), 2, "transpose"),  # a narrow kernel with long tiles
+    ((300, 400, 500), (2, 0, 1), 2, "transpose"),       # chunked tiles
+    ((100, 100, 3000), (1, 0, 2), 8, "strided"),        # rows of 24 KB
+    ((16384, 16385), (1, 0), 1, "transpose"),           # restaged byte tiles
+])
+def test_blocked_kernel_choice(shape, perm, elem, want):
+    """Which copies the analysis hands to the blocked kernel on its own:
+    batched small transposes, nearly empty element tiles, short scattered
+    destination runs; the chunked, packed and restaged tile variants, the
+    narrow kernels with long tiles and long rows keep their kernels."""
+    q = _query(_perm_view(shape, perm), elem, blocked="auto")
+    assert q["kind"] == want, q
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_blocked_plan_covers_the_copy(seed):
+    """A forced blocked plan of a fuzzed view: every tile extent within its
+    dimension, the tiles launched those that cover the index space, the
+    destination run at most 128 words and no run longer than its tile."""
+    w = synth.draw_lmad_view(seed, max_dims=5, max_elems=1 << 22)
+    for elem in (1, 2, 4, 8, 16):
+        q = _query(w, elem, blocked="force")
+        if q["kind"] == "empty":
+            continue
+        assert q["kind"] == "blocked"
+        sizes = [n // q["vec"] if k == 0 else n for k, (n, _, _) in enumerate(q["dims"])]
+        ext = q["block_extent"]
+        tiles = 1
+        for n, m in zip(sizes, ext):
+            assert 1 <= m <= max(n, 1)
+            tiles *= -(-n // m)
+        assert q["block_tiles"] == tiles
+        run_in, run_out = q["block_runs"]
+        tile = int(np.prod(ext))
+        assert 1 <= run_in <= tile and 1 <= run_out <= min(tile, 128)
 
 
 @pytest.mark.parametrize("c,elem,narrow", [
