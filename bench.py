@@ -629,7 +629,13 @@ def other_configs(torch, bm, synth, dev, stream):
                                     ("t2d_16383x16385_uint8", (16383, 16385), (1, 0), 1),
                                     ("t2d_11585x11587_fp16", (11585, 11587), (1, 0), 2),
                                     ("swap_hw_8000x6000x4_uint8", (8000, 6000, 4), (1, 0, 2), 1),
-                                    ("swap_4000x4096x16_uint8", (4000, 4096, 16), (1, 0, 2), 1)):
+                                    ("swap_4000x4096x16_uint8", (4000, 4096, 16), (1, 0, 2), 1),
+                                    # the blocked copy: batches of small transposes, a tiny
+                                    # group A, 3-byte pixels
+                                    ("batched_1000000x4x5_int32", (1000000, 4, 5), (0, 2, 1), 4),
+                                    ("batched_100000x12x20_int32", (100000, 12, 20), (0, 2, 1), 4),
+                                    ("perm_384x4096x2x12x2_uint8", (384, 4096, 2, 12, 2), (4, 0, 2, 1, 3), 1),
+                                    ("swap_hw_8000x6000x3_uint8", (8000, 6000, 3), (1, 0, 2), 1)):
         out["lmad_" + name] = lmad_case(torch, bm, axes_lmad(synth, shape, perm), a32, b32, stream, elem=elem)
     # the same slice on 1- and 2-byte elements (uint8 crop, fp16 slice: the rows kernel)
     out["lmad_slice_2d_16384x16385_uint8"] = lmad_case(

@@ -88,8 +88,9 @@ __host__ __device__ inline BlockLayout block_layout(int64_t q1, int64_t q2, int6
 // run (decomposed once per block over the run's dimensions: destination
 // offset, shared offset, coordinate along the run's last dimension), and a
 // warp writes one row of the run per step (runs under 32 words: several),
-// each word read from its place in the tile.
-template <typename W, int NDR>
+// each word read from its place in the tile.  UNIT: the source run has
+// stride 1.
+template <typename W, int NDR, bool UNIT>
 __global__ void __launch_bounds__(kBlockThreads, 4)
     lmad_block_kernel(const W* __restrict__ in, W* __restrict__ out, const __grid_constant__ LmadBlockParams p
                           BMMC_CHK_PARAM) {
@@ -195,8 +196,7 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         }
         const int64_t bs = hdr[0], bd = hdr[1];
         // the source run's valid length: its dimensions but the last are whole
-        const int32_t last = p.srun - 1;
-        const int32_t len1 = rs / (int32_t)p.m[last] * (int32_t)hdr[2 + last];
+        const int32_t len1 = p.rs_whole * (int32_t)hdr[2 + p.srun - 1];
         __syncthreads();  // the tables are written
         if (p.lg1 >= 5) {
             constexpr int K = kBlockSegWords<W>();
@@ -213,7 +213,8 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
                     const int i = i0 + 32 * k;
-                    if (i < len1) v[k] = BMMC_IN_OK(src + i * s0, sizeof(W)) ? __ldg(src + i * s0) : W{};
+                    const W* a = UNIT ? src + i : src + i * s0;
+                    if (i < len1) v[k] = BMMC_IN_OK(a, sizeof(W)) ? __ldg(a) : W{};
                 }
 #pragma unroll
                 for (int k = 0; k < K; ++k) {
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
                     if (o == kNoRow || i >= len1) {
                         q[k] = -1;
                     } else {
-                        const W* a = in + (bs + o + (int64_t)i * s0);
+                        const W* a = in + (bs + o + (UNIT ? (int64_t)i : (int64_t)i * s0));
                         v[k] = BMMC_IN_OK(a, sizeof(W)) ? __ldg(a) : W{};
                     }
                 }
@@ -451,6 +452,7 @@ cudaError_t launch_block_w(const W* in, W* out, const Dim* d, const BlockPlan& B
     p.nrows2 = B.nrows2;
     p.split = B.split;
     p.rs = (int32_t)B.rs;
+    p.rs_whole = (int32_t)(B.rs / B.m[B.srun - 1]);
     p.rsp = (int32_t)B.rsp;
     p.q1 = (int32_t)B.q1;
     p.q2 = (int32_t)B.q2;
@@ -500,13 +502,19 @@ cudaError_t launch_block_w(const W* in, W* out, const Dim* d, const BlockPlan& B
         p.ddiv[r] = make_div((uint64_t)B.dext[r], 32);
     }
     const unsigned grid = (unsigned)std::min<uint64_t>(B.tiles, 0x7FFFFFFFull);
-#define LMAD_BLOCK(NDR) \
-    lmad_block_kernel<W, NDR><<<grid, kBlockThreads, B.smem, stream>>>(in, out, p BMMC_CHK_ARG(lmad_bounds()))
-    switch (B.ndrun) {
-        case 1: LMAD_BLOCK(1); break;
-        case 2: LMAD_BLOCK(2); break;
-        case 3: LMAD_BLOCK(3); break;
-        default: LMAD_BLOCK(4); break;
+#define LMAD_BLOCK(NDR, UNIT)                                             \
+    lmad_block_kernel<W, NDR, UNIT><<<grid, kBlockThreads, B.smem, stream>>>( \
+        in, out, p BMMC_CHK_ARG(lmad_bounds()))
+    const bool unit = d[0].s == 1;
+    switch (B.ndrun * 2 + (unit ? 1 : 0)) {
+        case 2: LMAD_BLOCK(1, false); break;
+        case 3: LMAD_BLOCK(1, true); break;
+        case 4: LMAD_BLOCK(2, false); break;
+        case 5: LMAD_BLOCK(2, true); break;
+        case 6: LMAD_BLOCK(3, false); break;
+        case 7: LMAD_BLOCK(3, true); break;
+        case 8: LMAD_BLOCK(4, false); break;
+        default: LMAD_BLOCK(4, true); break;
     }
 #undef LMAD_BLOCK
     return cudaGetLastError();

@@ -219,6 +219,7 @@ struct LmadBlockParams {
     uint64_t tiles;
     int nd, srun, nrows1, nrows2, split;
     int32_t rs, rsp, q1, q2, rd;
+    int32_t rs_whole;                            // rs / the last source-run dimension's extent
     int32_t nseg1;                               // phase-1 segments per row (runs of 32 words or more)
     int32_t lg1, lg2;                            // log2 of a short run's lanes (runs under 32 words)
     int32_t u2;                                  // phase-2 positions per lane
