@@ -198,7 +198,43 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         // the source run's valid length: its dimensions but the last are whole
         const int32_t len1 = p.rs_whole * (int32_t)hdr[2 + p.srun - 1];
         __syncthreads();  // the tables are written
-        if (p.lg1 >= 5) {
+        if (UNIT && sizeof(W) <= 2 && p.lg1 >= 5) {
+            // 1- and 2-byte words of contiguous source runs move as aligned
+            // 4-byte words: shared word j of a run holds its bytes 4j..4j+3,
+            // the two aligned source words covering them joined by a funnel
+            // shift (the second loaded only when the run reaches into it;
+            // the bytes past the run's end that the last word carries land
+            // in the row's padding, the pitch being a multiple of 4 bytes)
+            constexpr int KW = kBlockSegWords<W>() * (int)sizeof(W) / 4;
+            const int n_items = p.q1 * p.nseg1, len1b = len1 * (int)sizeof(W);
+#pragma unroll 1
+            for (int it = warp; it < n_items; it += kBlockThreads / 32) {
+                const int q = (int)div_q((uint32_t)it, p.div_nseg1);
+                const int j0 = (it - q * p.nseg1) * (32 * KW) + lane;
+                const int64_t o = row1[q];
+                if (o == kNoRow) continue;
+                const unsigned char* const a = reinterpret_cast<const unsigned char*>(in + (bs + o));
+                const uint32_t mis = (uint32_t)((uintptr_t)a & 3u);
+                const uint32_t* const g = reinterpret_cast<const uint32_t*>(a - mis);
+                uint32_t* const dw = reinterpret_cast<uint32_t*>(tile + q * rsp);
+                uint32_t lo[KW], hi[KW];
+#pragma unroll
+                for (int k = 0; k < KW; ++k) {
+                    const int j = j0 + 32 * k;
+                    lo[k] = hi[k] = 0u;
+                    if (4 * j < len1b) {
+                        if (BMMC_IN_WORD_OK(g + j, 4)) lo[k] = __ldg(g + j);
+                        if (mis != 0u && 4 * j + 4 - (int)mis < len1b && BMMC_IN_WORD_OK(g + j + 1, 4))
+                            hi[k] = __ldg(g + j + 1);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < KW; ++k) {
+                    const int j = j0 + 32 * k;
+                    if (4 * j < len1b && BMMC_SH_OK(dw + j, 4)) dw[j] = __funnelshift_r(lo[k], hi[k], 8u * mis);
+                }
+            }
+        } else if (p.lg1 >= 5) {
             constexpr int K = kBlockSegWords<W>();
             const int n_items = p.q1 * p.nseg1;
 #pragma unroll 1
