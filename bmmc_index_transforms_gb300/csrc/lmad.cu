@@ -473,10 +473,13 @@ LmadCopy word_view(const LmadCopy& C) {
 //     dimensions from 0 that continue one another there) are under 24
 //     bytes of 2-byte or wider elements or under 8 bytes of 1-byte ones (a
 //     warp writes 32 scattered words: 0.10-0.51 against 0.28-0.55 of a
-//     copy; 3-byte pixels 0.11 against 0.17); it lost on longer runs;
+//     copy; 3-byte pixels 0.11 against 0.23); it lost on longer runs and
+//     where dimension 0 widens into words (20-byte runs of 4-byte words:
+//     1.10 against 0.63 of a copy, an array in L2);
 //   - narrow transposes whose tile (narrow side x the wide side's length
 //     in it) is under 4 KiB, batches of tiny transposes (0.02-0.27 against
-//     0.22-0.72);
+//     0.22-0.72), unless the register-regrouping kernel takes them (2 to 4
+//     narrow indices, 16-byte aligned: 0.83 against 0.42 blocked);
 //   - the tile kernel's element path when its tiles are less than 60%
 //     full (a B of 2 to 37 indices: 0.07-0.52 against 0.38-0.71; 20
 //     channels of 16 bytes, 62% full, stay: 0.98 against 0.76), and its
@@ -484,14 +487,14 @@ LmadCopy word_view(const LmadCopy& C) {
 //     0.22-0.59);
 // it never beat the chunked, packed or restaged tile variants, the copy
 // kernel, the rows kernel or a BPC.
-bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t out_addr) {
+bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t out_addr) {
     if (C.kind == LMAD_COPY_STRIDED) {
         const Dim& d0 = C.d[0];
         if (d0.s != 1) return false;
         if (iabs(d0.t) != 1) return true;
         uint64_t run = (uint64_t)d0.n;
         for (int k = 1; k < C.nd && C.d[k].t == C.d[k - 1].t * C.d[k - 1].n; ++k) run *= (uint64_t)C.d[k].n;
-        return run * elem < (elem >= 2 ? 24u : 8u);
+        return C.vec == 1 && run * elem < (elem >= 2 ? 24u : 8u);
     }
     if (C.kind != LMAD_COPY_TRANSPOSE) return false;
     const size_t word = elem * (size_t)C.vec;
@@ -501,6 +504,9 @@ bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t out_addr) {
     for (int k = 0; k < V.nb; ++k) n_b *= (uint64_t)V.d[V.gb[k]].n;
     if (V.narrow) {
         const uint64_t narrow = V.narrow == 1 ? n_a : n_b, wide = V.narrow == 1 ? n_b : n_a;
+        const NarrowVec v = narrow_vec(V, word, in_addr + (uintptr_t)(C.in_off * (int64_t)elem),
+                                       out_addr + (uintptr_t)(C.out_off * (int64_t)elem));
+        if (v.load && v.store && narrow >= 2 && narrow <= 4 && word <= 8) return false;  // register path
         return narrow * std::min<uint64_t>(wide, 1ull << V.lt) * word < 4096;
     }
     const TileLaunch L = tile_launch(V, word, out_addr + (uintptr_t)(C.out_off * (int64_t)elem));
@@ -517,7 +523,7 @@ bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t out_addr) {
 // and the tile plan.
 void choose_blocked(LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t out_addr, unsigned flags) {
     if (C.kind == LMAD_COPY_EMPTY || (flags & LMAD_NO_BLOCKED)) return;
-    if (!(flags & LMAD_FORCE_BLOCKED) && !prefer_blocked(C, elem, out_addr)) return;
+    if (!(flags & LMAD_FORCE_BLOCKED) && !prefer_blocked(C, elem, in_addr, out_addr)) return;
     const int v = widen_factor(C, elem, in_addr, out_addr);
     int nd = 0;
     for (int k = 0; k < C.nd; ++k) {

@@ -195,6 +195,30 @@ inline uint64_t span_of(const Dim* d, int nd, bool dest) {
     return s;
 }
 
+// Whether a narrow transpose (narrow != 0) of words of `word` bytes, tuple 0
+// at in / out, moves its blocks with 16-byte loads / stores: both sides'
+// origins and batch strides 16-byte aligned, and the narrow side's block
+// (loads for a narrow A, stores for a narrow B) or the wide side's rows of
+// one tile a multiple of 16 bytes.  With both and 2 to 4 narrow indices of
+// at most 8 bytes, the register-regrouping kernel runs.
+struct NarrowVec {
+    bool load, store;
+};
+inline NarrowVec narrow_vec(const LmadCopy& C, size_t word, uintptr_t in, uintptr_t out) {
+    const bool narrow_a = C.narrow == 1;
+    const Dim& a = C.d[C.ga[0]];
+    const Dim& b = C.d[C.gb[0]];
+    const uint64_t n = (uint64_t)(narrow_a ? a.n : b.n), tile_len = 1ull << C.lt;
+    bool src16 = (in & 15) == 0, dst16 = (out & 15) == 0;
+    for (int k = 0; k < C.nc; ++k) {
+        src16 = src16 && (iabs(C.d[C.gc[k]].s) * word) % 16 == 0;
+        dst16 = dst16 && (iabs(C.d[C.gc[k]].t) * word) % 16 == 0;
+    }
+    const bool block16 = (n * tile_len * word) % 16 == 0, row16 = (tile_len * word) % 16 == 0;
+    if (narrow_a) return NarrowVec{src16 && block16, dst16 && row16 && (iabs(a.t) * word) % 16 == 0};
+    return NarrowVec{src16 && row16 && (iabs(b.s) * word) % 16 == 0, dst16 && block16};
+}
+
 // How the general tile kernel runs one transpose of words of `word` bytes
 // into the destination origin `out`: its mode bits (the LMAD_TILE_* flags and
 // LMAD_TILE_WIDE), the tile sides it launches with and the tile counts.

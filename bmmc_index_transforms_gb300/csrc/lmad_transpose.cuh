@@ -1480,7 +1480,6 @@ cudaError_t launch_narrow_w(const W* in, W* out, const LmadCopy& C, cudaStream_t
     p.stride = narrow_a ? a.t : b.s;
     const uint64_t tile_len = 1ull << C.lt, tiles_w = (p.n_wide + tile_len - 1) / tile_len;
     uint64_t batch = 1;
-    bool src16 = ((uintptr_t)in & 15) == 0, dst16 = ((uintptr_t)out & 15) == 0;
     p.nc = C.nc;
     for (int k = 0; k < C.nc; ++k) {
         const Dim& x = C.d[C.gc[k]];
@@ -1488,18 +1487,10 @@ cudaError_t launch_narrow_w(const W* in, W* out, const LmadCopy& C, cudaStream_t
         p.cs[k] = x.s;
         p.ct[k] = x.t;
         batch *= (uint64_t)x.n;
-        src16 = src16 && (iabs(x.s) * sizeof(W)) % 16 == 0;
-        dst16 = dst16 && (iabs(x.t) * sizeof(W)) % 16 == 0;
     }
-    const bool block16 = ((uint64_t)n * tile_len * sizeof(W)) % 16 == 0;
-    const bool row16 = (tile_len * sizeof(W)) % 16 == 0;
-    if (narrow_a) {
-        p.vec_load = src16 && block16;
-        p.vec_store = dst16 && row16 && (iabs(a.t) * sizeof(W)) % 16 == 0;
-    } else {
-        p.vec_load = src16 && row16 && (iabs(b.s) * sizeof(W)) % 16 == 0;
-        p.vec_store = dst16 && block16;
-    }
+    const NarrowVec v = narrow_vec(C, sizeof(W), (uintptr_t)in, (uintptr_t)out);
+    p.vec_load = v.load;
+    p.vec_store = v.store;
     if constexpr (sizeof(W) <= 8) {
         if (p.vec_load && p.vec_store && n >= 2 && n <= 4 && LMAD_AOS) {
             // register regrouping, one thread per group of 16 / W wide indices
