@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         dsm[u] = sm;
         dcl[u] = ok ? c : INT32_MAX;  // never below a limit when not a position
     }
-    const int32_t rs = p.rs, rsp = p.rsp;
+    const int32_t rsp = p.rsp;
     const int64_t s0 = p.s0;
     for (uint64_t tix = blockIdx.x; tix < p.tiles; tix += gridDim.x) {
         if (tid < 32) {
@@ -453,12 +453,17 @@ bool block_plan(const Dim* d, int nd, size_t word, BlockPlan* out) {
     dest_order(d, nd, dord);
     const bool src_unit = d[0].s == 1, dst_unit = iabs(d[dord[0]].t) == 1;
     double best = -1.0;
+    // a larger target past the end of a chain gives the same extents as the
+    // last one: those are not scored again
+    int64_t last[kLmadMaxDims] = {};
     for (int ls = 4; ls <= 15; ++ls)
         for (int ld = 4; ld <= 15; ++ld) {
             const int64_t ts = std::max<int64_t>(1, (int64_t)((1 << ls) / word));
             const int64_t td = std::max<int64_t>(1, (int64_t)((1 << ld) / word));
             int64_t m[kLmadMaxDims];
             pick_extents(d, nd, dord, ts, td, m);
+            if (std::equal(m, m + nd, last)) continue;
+            std::copy(m, m + nd, last);
             BlockPlan B;
             if (!derive(d, nd, dord, m, word, B)) continue;
             // runs that are not contiguous (a strided side) move word by word
