@@ -512,6 +512,8 @@ def test_tiny_group_a_takes_the_stride_sorted_copy():
     ((300, 400, 500), (2, 0, 1), 2, "transpose"),       # chunked tiles
     ((100, 100, 3000), (1, 0, 2), 8, "strided"),        # rows of 24 KB
     ((16384, 16385), (1, 0), 1, "transpose"),           # restaged byte tiles
+    ((75798, 2, 16, 3), (1, 0, 3, 2), 2, "transpose"),  # 3 narrow indices: the register-regrouping kernel
+    ((1, 1, 2126, 290, 10), (3, 0, 1, 2, 4), 2, "strided"),  # 20-byte runs moved as 4-byte words
 ])
 def test_blocked_kernel_choice(shape, perm, elem, want):
     """Which copies the analysis hands to the blocked kernel on its own:
