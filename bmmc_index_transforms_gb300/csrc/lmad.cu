@@ -485,8 +485,10 @@ LmadCopy word_view(const LmadCopy& C) {
 //     channels of 16 bytes, 62% full, stay: 0.98 against 0.76), and its
 //     per-tile tables for words of up to 4 bytes (0.03-0.50 against
 //     0.22-0.59);
-// it never beat the chunked, packed or restaged tile variants, the copy
-// kernel, the rows kernel or a BPC.
+//   - the chunked, packed or restaged tile variants only when their tiles
+//     are less than 30% full (a B of 7 bytes in 32-row tiles: 0.04 against
+//     0.28; 40% full and above they won, 0.61-1.08 against 0.21-0.59);
+// it never beat the copy kernel, the rows kernel or a BPC.
 bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t out_addr) {
     if (C.kind == LMAD_COPY_STRIDED) {
         const Dim& d0 = C.d[0];
@@ -510,12 +512,15 @@ bool prefer_blocked(const LmadCopy& C, size_t elem, uintptr_t in_addr, uintptr_t
         return narrow * std::min<uint64_t>(wide, 1ull << V.lt) * word < 4096;
     }
     const TileLaunch L = tile_launch(V, word, out_addr + (uintptr_t)(C.out_off * (int64_t)elem));
-    if (L.mode & LMAD_TILE_CHUNKED) return false;
+    // the share of the launched tiles' places that hold elements
+    auto fill = [&](int la, int lb) {
+        const uint64_t ta = 1ull << la, tb = 1ull << lb;
+        return (double)n_a / (double)(((n_a + ta - 1) / ta) * ta) * (double)n_b /
+               (double)(((n_b + tb - 1) / tb) * tb);
+    };
+    if (L.mode & LMAD_TILE_CHUNKED) return fill(L.la, L.lb) < 0.3;
     if (L.mode & LMAD_TILE_TABLES) return word <= 4;
-    const uint64_t ta = 1ull << V.la, tb = 1ull << V.lb;
-    const double ua = (double)n_a / (double)(((n_a + ta - 1) / ta) * ta);
-    const double ub = (double)n_b / (double)(((n_b + tb - 1) / tb) * tb);
-    return ua * ub < 0.6;
+    return fill(V.la, V.lb) < 0.6;
 }
 
 // Takes the blocked copy when the flags or prefer_blocked ask for it: the

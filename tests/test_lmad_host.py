@@ -514,6 +514,7 @@ def test_tiny_group_a_takes_the_stride_sorted_copy():
     ((16384, 16385), (1, 0), 1, "transpose"),           # restaged byte tiles
     ((75798, 2, 16, 3), (1, 0, 3, 2), 2, "transpose"),  # 3 narrow indices: the register-regrouping kernel
     ((1, 1, 2126, 290, 10), (3, 0, 1, 2, 4), 2, "strided"),  # 20-byte runs moved as 4-byte words
+    ((16, 7, 8, 4006, 59), (0, 2, 4, 3, 1), 1, "blocked"),  # a B of 7 bytes: chunked tiles 22% full
 ])
 def test_blocked_kernel_choice(shape, perm, elem, want):
     """Which copies the analysis hands to the blocked kernel on its own:
