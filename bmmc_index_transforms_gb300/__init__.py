@@ -303,6 +303,12 @@ def _elems(x, elem_size: int, given) -> int:
     raise ValueError("element count needed for a raw address")
 
 
+def _blocked_flags(blocked: str, where: str) -> int:
+    if blocked not in LMAD_BLOCKED_FLAGS:
+        raise ValueError(f"{where}: blocked must be one of {sorted(LMAD_BLOCKED_FLAGS)}, not {blocked!r}")
+    return LMAD_BLOCKED_FLAGS[blocked]
+
+
 def _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides):
     d = len(sizes)
     if len(in_strides) != d or len(out_strides) != d:
@@ -321,7 +327,8 @@ def lmad_copy_query(sizes: Sequence[int], in_offset: int, in_strides: Sequence[i
     info = _capi.LmadCopyInfo()
     _check(_capi.lib().lmad_copy_query_ex(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
                                           _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
-                                          LMAD_BLOCKED_FLAGS[blocked], ctypes.byref(info)), "lmad_copy_query")
+                                          _blocked_flags(blocked, "lmad_copy_query"), ctypes.byref(info)),
+           "lmad_copy_query")
     k = info.ndims
     return {"kind": LMAD_KIND_NAMES.get(info.kind, str(info.kind)), "ndims": k,
             "dims": [[int(info.sizes[i]), int(info.in_strides[i]), int(info.out_strides[i])] for i in range(k)],
@@ -345,11 +352,12 @@ def lmad_copy(sizes: Sequence[int], in_offset: int, in_strides: Sequence[int], o
     tuple (element units, any sizes); enqueued on the stream.  blocked: as
     for lmad_copy_query."""
     d, sz, io, si, oo, so = _general_lmad_args(sizes, in_offset, in_strides, out_offset, out_strides)
+    flags = _blocked_flags(blocked, "lmad_copy")
     _check_buf(inp, 0, "lmad_copy", "in")
     _check_buf(out, 0, "lmad_copy", "out")
     _check(_capi.lib().lmad_copy_ex(d, sz, io, si, _elems(inp, elem_size, in_elems), oo, so,
                                     _elems(out, elem_size, out_elems), elem_size, _ptr(inp), _ptr(out),
-                                    LMAD_BLOCKED_FLAGS[blocked], _stream(stream, inp, out)), "lmad_copy")
+                                    flags, _stream(stream, inp, out)), "lmad_copy")
 
 
 def _tensor_lmad(x):

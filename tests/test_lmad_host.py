@@ -3,6 +3,8 @@ the library's analysis against the oracle's restatement of the page's
 (flip, drop singletons, sort, collapse), the kind each of the page's cases
 gets, and every rejection."""
 
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -523,6 +525,28 @@ def test_blocked_kernel_choice(shape, perm, elem, want):
     narrow kernels with long tiles and long rows keep their kernels."""
     q = _query(_perm_view(shape, perm), elem, blocked="auto")
     assert q["kind"] == want, q
+
+
+def test_blocked_flags():
+    """blocked="force" / "never" reach the library as LMAD_FORCE_BLOCKED /
+    LMAD_NO_BLOCKED; anything else is refused before the call, and both
+    flags at once are INVALID_ARG in the C ABI."""
+    w = _perm_view((1000, 4, 5), (0, 2, 1))
+    assert _query(w, 4, blocked="force")["kind"] == "blocked"
+    assert _query(w, 4, blocked="never")["kind"] == "transpose"
+    with pytest.raises(ValueError):
+        _query(w, 4, blocked="always")
+    info = _capi.LmadCopyInfo()
+    n = len(w["sizes"])
+    arr = lambda v: (ctypes.c_int64 * n)(*v)  # noqa: E731
+    st = _capi.lib().lmad_copy_query_ex(n, arr(w["sizes"]), 0, arr(w["in_strides"]), w["in_elems"], 0,
+                                        arr(w["out_strides"]), w["out_elems"], 4, None, None,
+                                        _capi.LMAD_FORCE_BLOCKED | _capi.LMAD_NO_BLOCKED, ctypes.byref(info))
+    assert st == _capi.ERR_INVALID_ARG
+    st = _capi.lib().lmad_copy_query_ex(n, arr(w["sizes"]), 0, arr(w["in_strides"]), w["in_elems"], 0,
+                                        arr(w["out_strides"]), w["out_elems"], 4, None, None, 0x4,
+                                        ctypes.byref(info))
+    assert st == _capi.ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("seed", range(60))
