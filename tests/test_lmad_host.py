@@ -572,6 +572,158 @@ def test_blocked_plan_covers_the_copy(seed):
         assert 1 <= run_in <= tile and 1 <= run_out <= min(tile, 128)
 
 
+def _blocked_replay(q, word):
+    """The blocked kernel's index arithmetic replayed on the host from the
+    plan the library reports (tile extents, in words of q["vec"] elements):
+    the source run (dimensions 0.. contiguous in the source, all but the last
+    whole), the destination run (by increasing |t|, contiguous, all but the
+    last whole, at most 128 words and 4 dimensions, a longer last one split
+    into its first part and a row dimension), phase 1 copying each row of
+    the source run into a source-major tile (run r at r * rsp), phase 2
+    writing each row of the destination run from it, ragged tiles cut at
+    the array's end.  Returns the run lengths, the tile count and the map
+    destination offset -> source offset (in words) with how often each
+    destination was written."""
+    vec = q["vec"]
+    dims = []
+    for k, (n, si, ti) in enumerate(q["dims"]):
+        if k == 0:
+            n //= vec
+        else:
+            si //= vec
+            ti //= vec
+        if n > 1:
+            dims.append((n, si, ti, q["block_extent"][k]))
+    if not dims:
+        dims = [(1, 1, 1, 1)]
+    nd = len(dims)
+    n = [d[0] for d in dims]
+    s = [d[1] for d in dims]
+    t = [d[2] for d in dims]
+    m = [d[3] for d in dims]
+    srun = 1
+    while srun < nd and m[srun - 1] == n[srun - 1] and m[srun] > 1 and s[srun] == s[srun - 1] * n[srun - 1]:
+        srun += 1
+    rs = int(np.prod(m[:srun]))
+    dord = sorted(range(nd), key=lambda k: abs(t[k]))
+    drun, dext, split, rd = [], [], -1, 1
+    for i, k in enumerate(dord):
+        if len(drun) == 4:
+            break
+        if i > 0:
+            f = dord[i - 1]
+            if m[f] != n[f] or m[k] <= 1 or abs(t[k]) != abs(t[f]) * n[f]:
+                break
+        ext = m[k]
+        if rd * ext > 128:
+            ext = 128 // rd
+            if ext < 2 and drun:
+                break
+            ext = max(ext, 1)
+            split = k
+        drun.append(k)
+        dext.append(ext)
+        rd *= ext
+        if split >= 0 or ext < n[k]:
+            break
+    in_src = set(range(srun))
+    rows1 = [k for k in drun if k not in in_src and m[k] > 1]
+    rows1 += [k for k in range(nd) if k not in in_src and k not in drun and m[k] > 1]
+    rows2 = [(k, m[k], 1) for k in range(nd) if k not in drun and m[k] > 1]
+    if split >= 0:
+        rows2.append((split, -(-m[split] // dext[-1]), dext[-1]))
+    rsp = rs
+    while not ((word >= 4 and rsp % 2 == 1) or (word == 2 and rsp % 4 == 2) or (word == 1 and rsp % 8 == 4)):
+        rsp += 1
+    sig = {}
+    acc = 1
+    for k in range(srun):
+        sig[k] = acc
+        acc *= m[k]
+    acc = rsp
+    for k in rows1:
+        sig[k] = acc
+        acc *= m[k]
+    ntile = [-(-n[k] // m[k]) for k in range(nd)]
+    tiles = int(np.prod(ntile))
+    written = {}
+    for tix in range(tiles):
+        x, c0 = tix, []
+        for k in range(nd):
+            c0.append((x % ntile[k]) * m[k])
+            x //= ntile[k]
+        v = [min(m[k], n[k] - c0[k]) for k in range(nd)]
+        bs = sum(c0[k] * s[k] for k in range(nd))
+        bd = sum(c0[k] * t[k] for k in range(nd))
+        smem = {}
+        len1 = rs // m[srun - 1] * v[srun - 1]
+        for qq in range(int(np.prod([m[k] for k in rows1])) if rows1 else 1):
+            x, o, ok = qq, 0, True
+            for k in rows1:
+                c = x % m[k]
+                x //= m[k]
+                ok = ok and c < v[k]
+                o += c * s[k]
+            if not ok:
+                continue
+            for i in range(len1):
+                assert qq * rsp + i not in smem
+                smem[qq * rsp + i] = bs + o + i * s[0]
+        for qq in range(int(np.prod([e for _, e, _ in rows2])) if rows2 else 1):
+            x, o, sm, ok = qq, 0, 0, True
+            lim = v[drun[-1]]
+            for r, (k, e, mul) in enumerate(rows2):
+                c = (x % e) * mul
+                x //= e
+                if k == split and r + 1 == len(rows2):
+                    lim -= c
+                else:
+                    ok = ok and c < v[k]
+                o += c * t[k]
+                sm += c * sig[k]
+            if not ok or lim <= 0:
+                continue
+            for j in range(rd):
+                x, od, sj, c = j, 0, 0, 0
+                for r, k in enumerate(drun):
+                    c = x % dext[r] if r + 1 < len(drun) else x
+                    x //= dext[r] if r + 1 < len(drun) else 1
+                    od += c * t[k]
+                    sj += c * sig[k]
+                if c >= lim:
+                    continue
+                dst = bd + o + od
+                assert sm + sj in smem, "phase 2 reads a place phase 1 did not fill"
+                src, cnt = written.get(dst, (None, 0))
+                written[dst] = (smem[sm + sj], cnt + 1)
+    return rs, rd, tiles, written
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_blocked_kernel_index_replay(seed):
+    """Replaying the blocked kernel's index arithmetic over every tile of a
+    fuzzed view (all five element sizes) writes every destination tuple
+    exactly once, from its own source tuple, and the library's reported runs
+    and tile count are the replay's."""
+    w = synth.draw_lmad_view(7000 + seed, max_dims=5, max_elems=1 << 11)
+    for elem in (1, 2, 4, 8, 16):
+        q = _query(w, elem, blocked="force")
+        if q["kind"] == "empty":
+            continue
+        word = elem * q["vec"]
+        rs, rd, tiles, written = _blocked_replay(q, word)
+        assert (rs, rd) == q["block_runs"] and tiles == q["block_tiles"]
+        vec = q["vec"]
+        want = {}
+        sizes = [nn // vec if k == 0 else nn for k, (nn, _, _) in enumerate(q["dims"])]
+        for idx in np.ndindex(*sizes):
+            src = sum(i * (si // vec if k else si) for k, (i, (_, si, _)) in enumerate(zip(idx, q["dims"])))
+            dst = sum(i * (ti // vec if k else ti) for k, (i, (_, _, ti)) in enumerate(zip(idx, q["dims"])))
+            want[dst] = src
+        assert {d: v[0] for d, v in written.items()} == want
+        assert all(v[1] == 1 for v in written.values())
+
+
 @pytest.mark.parametrize("c,elem,narrow", [
     (16, 1, 1), (17, 1, 1), (24, 1, 1), (31, 1, 1), (32, 1, 0),   # bytes: narrow A up to 31
     (17, 2, 1), (31, 2, 1), (32, 2, 0),                           # 2-byte words the same
