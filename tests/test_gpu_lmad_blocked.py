@@ -203,3 +203,61 @@ def test_never_blocked_keeps_the_other_kinds():
                            in_elems=w["in_elems"], out_elems=w["out_elems"], blocked="never")
     assert q["kind"] != "blocked"
     _check(w, 4, 3, blocked="never")
+
+
+def test_blocked_copies_in_a_cuda_graph():
+    """The blocked kernel allocates nothing and never synchronises: blocked
+    copies (the analysis' own choice for a batch of small transposes, and a
+    forced one) are captured in a CUDA graph and replayed."""
+    cases = [(_perm_view((20000, 4, 5), (0, 2, 1)), 4, "auto"), (_perm_view((37, 1029), (1, 0)), 2, "force")]
+    bufs = []
+    for w, e, mode in cases:
+        q = bm.lmad_copy_query(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e,
+                               in_elems=w["in_elems"], out_elems=w["out_elems"], blocked=mode)
+        assert q["kind"] == "blocked"
+        src = torch.from_numpy(_fill(w["in_elems"], e, 4).reshape(-1)).cuda()
+        dst = torch.zeros(w["out_elems"] * e, dtype=torch.uint8, device="cuda")
+        bufs.append((src, dst))
+        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e, src, dst,
+                     blocked=mode)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for (w, e, mode), (src, dst) in zip(cases, bufs):
+                bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e, src,
+                             dst, torch.cuda.current_stream(), blocked=mode)
+    for _, dst in bufs:
+        dst.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for (w, e, _), (src, dst) in zip(cases, bufs):
+        want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"],
+                                     src.cpu().numpy().reshape(-1, e), np.zeros((w["out_elems"], e), np.uint8))
+        assert np.array_equal(dst.cpu().numpy().reshape(-1, e), want)
+
+
+def test_concurrent_blocked_copies_from_threads():
+    """Four threads run forced blocked copies of different views at once on
+    their own streams (no state kept between calls)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    def work(seed):
+        w = synth.draw_lmad_view(9000 + seed, max_dims=4, max_elems=1 << 18)
+        elem = (1, 2, 4, 8, 16)[seed % 5]
+        src = _fill(w["in_elems"], elem, seed)
+        dst = np.full((w["out_elems"], elem), 0xA5, dtype=np.uint8)
+        s = torch.cuda.Stream()
+        d_src = torch.from_numpy(src.reshape(-1)).cuda()
+        d_dst = torch.from_numpy(dst.reshape(-1)).cuda()
+        torch.cuda.synchronize()
+        bm.lmad_copy(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], elem, d_src,
+                     d_dst, s, blocked="force")
+        s.synchronize()
+        want = ref.lmad_copy_general(w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"],
+                                     w["out_strides"], src, dst)
+        return np.array_equal(d_dst.cpu().numpy().reshape(-1, elem), want)
+
+    with ThreadPoolExecutor(4) as ex:
+        assert all(ex.map(work, range(20)))
