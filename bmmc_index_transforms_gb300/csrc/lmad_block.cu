@@ -76,6 +76,19 @@ __host__ __device__ inline BlockLayout block_layout(int64_t q1, int64_t q2, int6
 // Device side
 // ---------------------------------------------------------------------------
 
+// One asynchronous global -> shared copy of a 4-, 8- or 16-byte word
+// (cp.async, completion awaited with cp.async.wait_all); both addresses
+// are aligned to the word.
+template <typename W>
+__device__ __forceinline__ void block_cp_async(W* smem, const W* gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    if constexpr (sizeof(W) == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(gmem), "n"((int)sizeof(W))
+                     : "memory");
+}
+
 // One block per tile (a grid-stride loop past 2^31 - 1 tiles).  The lanes
 // of warp 0 decode the tile's origin, one dimension each (its tile index is
 // (tile / tiles of the faster dimensions) mod its tiles), and the extent of
@@ -234,6 +247,28 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
                     if (4 * j < len1b && BMMC_SH_OK(dw + j, 4)) dw[j] = __funnelshift_r(lo[k], hi[k], 8u * mis);
                 }
             }
+        } else if (UNIT && sizeof(W) >= 4 && p.lg1 >= 5) {
+            // 4- to 16-byte words of contiguous source runs: asynchronous
+            // copies straight into the tile, every item's in flight at
+            // once (no registers hold them), awaited before the barrier
+            constexpr int K = kBlockSegWords<W>();
+            const int n_items = p.q1 * p.nseg1;
+#pragma unroll 1
+            for (int it = warp; it < n_items; it += kBlockThreads / 32) {
+                const int q = (int)div_q((uint32_t)it, p.div_nseg1);
+                const int i0 = (it - q * p.nseg1) * (32 * K) + lane;
+                const int64_t o = row1[q];
+                if (o == kNoRow) continue;
+                const W* src = in + (bs + o);
+                W* dst = tile + q * rsp;
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    const int i = i0 + 32 * k;
+                    if (i < len1 && BMMC_SH_OK(dst + i, sizeof(W)) && BMMC_IN_OK(src + i, sizeof(W)))
+                        block_cp_async(dst + i, src + i);
+                }
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
         } else if (p.lg1 >= 5) {
             constexpr int K = kBlockSegWords<W>();
             const int n_items = p.q1 * p.nseg1;
