@@ -12,8 +12,10 @@ transpose (square, n even), dims5 (the 5-D (4,2,0,3,1) permutation of a
 same bytes), two_factor (seed, two passes through caller scratch).
 General LMAD copies (--shape, --elem): lmad_slice_2d, lmad_slice_3d,
 lmad_reversed_rows (the Futhark copy post's "Impact" functions on a
-row-major array of that shape) and lmad_transpose (the shape's axes
-reversed, made contiguous).
+row-major array of that shape), lmad_transpose (the shape's axes
+reversed, made contiguous) and lmad_permute (the shape's axes in the order
+--perm, out dimension k = in dimension perm[k], made contiguous; --blocked
+auto / force / never chooses for the blocked copy).
 Prints the plan and the CUDA-event time of each repetition.
 """
 
@@ -45,7 +47,7 @@ def main(argv=None):
     ap.add_argument("--kind", default="random",
                     choices=["random", "worst", "bitrev", "transpose", "dims5", "copy", "two_factor",
                              "complement", "window", "lmad_slice_2d", "lmad_slice_3d", "lmad_reversed_rows",
-                             "lmad_transpose"])
+                             "lmad_transpose", "lmad_permute"])
     ap.add_argument("--n", type=int, default=26)
     ap.add_argument("--elem", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
@@ -55,6 +57,8 @@ def main(argv=None):
     ap.add_argument("--tile-bits", type=int, default=0)
     ap.add_argument("--shape", default="8192,8193")
     ap.add_argument("--window", type=int, default=22, help="window: log2 elements of a window")
+    ap.add_argument("--perm", default="", help="lmad_permute: axis order of the destination")
+    ap.add_argument("--blocked", default="auto", choices=["auto", "force", "never"])
     a = ap.parse_args(argv)
     if a.kind.startswith("lmad_"):
         return lmad_case(a)
@@ -114,11 +118,15 @@ def main(argv=None):
     return 0
 
 
-def lmad_case(a):
+def lmad_view(a) -> dict:
+    """The LMAD copy of an lmad_* kind: sizes, offsets and strides in
+    elements, as lmad_copy takes them."""
     shape = [int(v) for v in a.shape.split(",")]
-    e = a.elem
-    if a.kind == "lmad_transpose":
-        perm = list(range(len(shape)))[::-1]
+    if a.kind in ("lmad_transpose", "lmad_permute"):
+        perm = ([int(v) for v in a.perm.split(",")] if a.kind == "lmad_permute"
+                else list(range(len(shape)))[::-1])
+        if sorted(perm) != list(range(len(shape))):
+            raise SystemExit("--perm must order the axes of --shape")
         out_rm = synth.row_major_strides([shape[p] for p in perm])
         out_strides = [0] * len(shape)
         for pos, p in enumerate(perm):
@@ -126,19 +134,23 @@ def lmad_case(a):
         total = 1
         for v in shape:
             total *= v
-        w = dict(sizes=shape, in_offset=0, in_strides=synth.row_major_strides(shape), in_elems=total,
-                 out_offset=0, out_strides=out_strides, out_elems=total)
-    else:
-        w = synth.page_lmad_workload(a.kind[len("lmad_"):], shape)
+        return dict(sizes=shape, in_offset=0, in_strides=synth.row_major_strides(shape), in_elems=total,
+                    out_offset=0, out_strides=out_strides, out_elems=total)
+    return synth.page_lmad_workload(a.kind[len("lmad_"):], shape)
+
+
+def lmad_case(a):
+    e = a.elem
+    w = lmad_view(a)
     src = torch.empty(w["in_elems"] * e, dtype=torch.uint8, device="cuda")
     dst = torch.empty(w["out_elems"] * e, dtype=torch.uint8, device="cuda")
     args = (w["sizes"], w["in_offset"], w["in_strides"], w["out_offset"], w["out_strides"], e)
-    print("analysis:", bm.lmad_copy_query(*args, src, dst))
+    print("analysis:", bm.lmad_copy_query(*args, src, dst, blocked=a.blocked))
     stream = torch.cuda.current_stream()
     for r in range(a.reps):
         s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        bm.lmad_copy(*args, src, dst, stream)
+        bm.lmad_copy(*args, src, dst, stream, blocked=a.blocked)
         t.record(stream)
         torch.cuda.synchronize()
         ms = s.elapsed_time(t)

@@ -549,6 +549,27 @@ def test_blocked_flags():
     assert st == _capi.ERR_INVALID_ARG
 
 
+def test_profile_case_permute_views():
+    """profile_case --kind lmad_permute builds the row-major array's axis
+    permutation; the two blocked copies profiled with it get the tiles the
+    profile summary states."""
+    import argparse
+
+    from bmmc_index_transforms_gb300 import profile_case as pc
+
+    for shape, perm, elem, ext, runs, tiles in (("1000000,4,5", "0,2,1", 4, [5, 4, 410], (8200, 120), 2440),
+                                                ("384,4096,2,12,2", "4,0,2,1,3", 1, [2, 12, 2, 683, 1],
+                                                 (32784, 120), 2304)):
+        w = pc.lmad_view(argparse.Namespace(kind="lmad_permute", shape=shape, perm=perm))
+        sizes = [int(v) for v in shape.split(",")]
+        assert w == _perm_view(sizes, [int(v) for v in perm.split(",")])
+        q = _query(w, elem, blocked="auto")
+        assert q["kind"] == "blocked" and q["block_extent"] == ext
+        assert q["block_runs"] == runs and q["block_tiles"] == tiles
+    with pytest.raises(SystemExit):
+        pc.lmad_view(argparse.Namespace(kind="lmad_permute", shape="4,5", perm="0,0"))
+
+
 @pytest.mark.parametrize("seed", range(60))
 def test_blocked_plan_covers_the_copy(seed):
     """A forced blocked plan of a fuzzed view: every tile extent within its
